@@ -1,0 +1,266 @@
+"""CPU oracle for the gradient-compression hot path (test infrastructure).
+
+This package is TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline legs of ``bench.py`` may import it.  The product library
+(``gradient_compression_sgd_gc_gb300``) never imports, links or executes
+anything here, and this package never imports the product.
+
+The arithmetic lives in ``oracle.c`` (plain C, compiled ``-O2
+-ffp-contract=off``); this module only builds it with gcc and marshals numpy
+arrays through ctypes.  Every function cites the page passage it follows in
+``oracle.c``.
+
+Pins: every function here is checked by ``tests/test_oracle_*.py`` against
+values printed on the pages, closed forms, invariants, exact rational
+arithmetic or brute force (none of them re-types the oracle's own formula).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into ``oracle/_build/liboracle.so`` (gcc, this host's arch)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = build()
+        lib = ctypes.CDLL(path)
+        u64, i64, i32, f32, f64, vp = (ctypes.c_uint64, ctypes.c_int64, ctypes.c_int,
+                                       ctypes.c_float, ctypes.c_double, ctypes.c_void_p)
+        sig = {
+            "orc_splitmix64": (u64, [u64]),
+            "orc_uniform": (f64, [u64]),
+            "orc_round_seed": (u64, [u64, u64]),
+            "orc_2bit_quantize": (None, [vp, i32, vp, vp, i64, f32]),
+            "orc_2bit_dequant_sum_update": (None, [vp, i32, i64, f32, i32, f64, f64, vp, vp, vp]),
+            "orc_compensated_sum_update": (None, [vp, i32, vp, i32, i64, f64, vp]),
+            "orc_l2norm_fp32": (f32, [vp, i64]),
+            "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, vp, vp]),
+            "orc_qsgd_dequant_sum": (None, [vp, vp, i32, i64, i64, i32, f64, vp]),
+            "orc_saps_mask_compact": (i64, [i64, f64, u64, vp, i32, vp, vp, i64]),
+            "orc_saps_matching": (i32, [u64, i32, vp]),
+            "orc_saps_peer_average": (None, [vp, vp, vp, i64, vp, i32]),
+            "orc_easgd_step": (None, [vp, i32, i64, f64, f64, vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _check(a: np.ndarray, dtype, name: str, size: int | None = None) -> None:
+    if not isinstance(a, np.ndarray) or a.dtype != np.dtype(dtype):
+        raise TypeError(f"{name}: expected numpy {np.dtype(dtype)}, got {getattr(a, 'dtype', type(a))}")
+    if not a.flags.c_contiguous:
+        raise ValueError(f"{name}: must be C-contiguous")
+    if size is not None and a.size < size:
+        raise ValueError(f"{name}: needs at least {size} elements, has {a.size}")
+
+
+def _ptr_array(arrays):
+    return (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+
+
+# --------------------------------------------------------------------------
+# counter-based random numbers
+# --------------------------------------------------------------------------
+
+def splitmix64(x: int) -> int:
+    return int(_load().orc_splitmix64(x & 0xFFFFFFFFFFFFFFFF))
+
+
+def uniform(key: int) -> float:
+    return float(_load().orc_uniform(key & 0xFFFFFFFFFFFFFFFF))
+
+
+def round_seed(base: int, t: int) -> int:
+    return int(_load().orc_round_seed(base & 0xFFFFFFFFFFFFFFFF, t & 0xFFFFFFFFFFFFFFFF))
+
+
+# --------------------------------------------------------------------------
+# 2-bit threshold quantisation
+# --------------------------------------------------------------------------
+
+def _grad_kind(g: np.ndarray) -> int:
+    """0 for fp32 gradients, 1 for bf16 gradients held as raw uint16 bits."""
+    if g.dtype == np.float32:
+        return 0
+    if g.dtype == np.uint16:
+        return 1
+    raise TypeError("gradient must be float32 or bf16 bits as uint16")
+
+
+def twobit_quantize(grad: np.ndarray, residual: np.ndarray, threshold: float) -> np.ndarray:
+    """Quantise in place: updates ``residual`` (fp32), returns uint32 codes [ceil(n/16)]."""
+    n = grad.size
+    kind = _grad_kind(grad)
+    _check(grad, grad.dtype, "grad")
+    _check(residual, np.float32, "residual", n)
+    codes = np.zeros((n + 15) // 16, dtype=np.uint32)
+    _load().orc_2bit_quantize(_ptr(grad), kind, _ptr(residual), _ptr(codes), n,
+                              ctypes.c_float(np.float32(threshold)))
+    return codes
+
+
+KIND_NONE, KIND_SGD, KIND_EASGD = 0, 1, 2
+
+
+def twobit_dequant_sum_update(codes_list, n: int, threshold: float, kind: int,
+                              lr: float = 0.0, alpha: float = 0.0,
+                              center: np.ndarray | None = None,
+                              weights: np.ndarray | None = None) -> np.ndarray | None:
+    """Dequantise + sum W workers' codes.  kind NONE returns the fp64 average;
+    SGD/EASGD update ``weights`` (fp64) in place and return None."""
+    W = len(codes_list)
+    for c in codes_list:
+        _check(c, np.uint32, "codes", (n + 15) // 16)
+    out = None
+    if kind == KIND_NONE:
+        out = np.zeros(n, dtype=np.float64)
+    else:
+        _check(weights, np.float64, "weights", n)
+    if kind == KIND_EASGD:
+        _check(center, np.float64, "center", n)
+    arr = _ptr_array(codes_list)
+    _load().orc_2bit_dequant_sum_update(
+        arr, W, n, ctypes.c_float(np.float32(threshold)), kind,
+        float(np.float32(lr)), float(np.float32(alpha)),
+        _ptr(center) if center is not None else None,
+        _ptr(weights) if weights is not None else None,
+        _ptr(out) if out is not None else None)
+    return out
+
+
+def compensated_sum_update(grads, residuals, lr: float, weights: np.ndarray) -> None:
+    """CD-SGD correction step: m_w = r_w + g_w (fp32), r_w <- 0, w -= lr * mean_w m_w (fp64)."""
+    W = len(grads)
+    n = grads[0].size
+    kind = _grad_kind(grads[0])
+    for g in grads:
+        _check(g, grads[0].dtype, "grad", n)
+    for r in residuals:
+        _check(r, np.float32, "residual", n)
+    _check(weights, np.float64, "weights", n)
+    _load().orc_compensated_sum_update(_ptr_array(grads), kind, _ptr_array(residuals), W, n,
+                                       float(np.float32(lr)), _ptr(weights))
+
+
+# --------------------------------------------------------------------------
+# QSGD
+# --------------------------------------------------------------------------
+
+def l2norm_fp32(v: np.ndarray) -> np.float32:
+    _check(v, np.float32, "v")
+    return np.float32(_load().orc_l2norm_fp32(_ptr(v), v.size))
+
+
+def qsgd_code_bytes(n: int, s: int) -> int:
+    return (n + 1) // 2 if s <= 7 else n
+
+
+def qsgd_quantize(v: np.ndarray, bucket: int, s: int, seed: int, worker: int):
+    """Returns (norms fp32 [ceil(n/bucket)], codes uint8)."""
+    _check(v, np.float32, "v")
+    n = v.size
+    norms = np.zeros((n + bucket - 1) // bucket, dtype=np.float32)
+    codes = np.zeros(qsgd_code_bytes(n, s), dtype=np.uint8)
+    _load().orc_qsgd_quantize(_ptr(v), n, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker,
+                              _ptr(norms), _ptr(codes))
+    return norms, codes
+
+
+def qsgd_dequant_sum(codes_list, norms_list, n: int, bucket: int, s: int,
+                     scale: float = 1.0) -> np.ndarray:
+    W = len(codes_list)
+    for c in codes_list:
+        _check(c, np.uint8, "codes", qsgd_code_bytes(n, s))
+    for nm in norms_list:
+        _check(nm, np.float32, "norms", (n + bucket - 1) // bucket)
+    out = np.zeros(n, dtype=np.float64)
+    _load().orc_qsgd_dequant_sum(_ptr_array(codes_list), _ptr_array(norms_list), W, n, bucket,
+                                 s, float(np.float32(scale)), _ptr(out))
+    return out
+
+
+# --------------------------------------------------------------------------
+# SAPS + EASGD
+# --------------------------------------------------------------------------
+
+def saps_mask_compact(n: int, p: float, seed_t: int, models, capacity: int | None = None):
+    """Returns (count, idx uint32 [min(count, capacity)], vals list of fp64 arrays)."""
+    W = len(models)
+    for m in models:
+        _check(m, np.float64, "model", n)
+    if capacity is None:
+        capacity = n
+    idx = np.zeros(max(capacity, 1), dtype=np.uint32)
+    vals = [np.zeros(max(capacity, 1), dtype=np.float64) for _ in range(W)]
+    K = int(_load().orc_saps_mask_compact(n, float(p), seed_t & 0xFFFFFFFFFFFFFFFF,
+                                          _ptr_array(models), W, _ptr(idx), _ptr_array(vals),
+                                          capacity))
+    kept = min(K, capacity)
+    return K, idx[:kept].copy(), [v[:kept].copy() for v in vals]
+
+
+def saps_matching(seed_t: int, W: int) -> np.ndarray:
+    pairs = np.zeros(max(W, 1), dtype=np.int32)
+    rc = _load().orc_saps_matching(seed_t & 0xFFFFFFFFFFFFFFFF, W, _ptr(pairs))
+    if rc != 0:
+        raise ValueError("W must be a positive even number")
+    return pairs[:W].copy()
+
+
+def saps_peer_average(models, vals, idx: np.ndarray, pairs: np.ndarray) -> None:
+    W = len(models)
+    K = idx.size
+    for m in models:
+        _check(m, np.float64, "model")
+    vals = [np.ascontiguousarray(v, dtype=np.float64) for v in vals]
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    pairs = np.ascontiguousarray(pairs, dtype=np.int32)
+    _load().orc_saps_peer_average(_ptr_array(models), _ptr_array(vals), _ptr(idx), K,
+                                  _ptr(pairs), W)
+
+
+def easgd_step(models, alpha: float, beta: float, center: np.ndarray) -> None:
+    W = len(models)
+    n = center.size
+    for m in models:
+        _check(m, np.float64, "model", n)
+    _check(center, np.float64, "center", n)
+    _load().orc_easgd_step(_ptr_array(models), W, n, float(np.float32(alpha)),
+                           float(np.float32(beta)), _ptr(center))

@@ -1,0 +1,470 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU reference for the
+ * gradient-compression hot path.
+ *
+ * THIS IS TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load it.  The product library under
+ * gradient_compression_sgd_gc_gb300/ shares no code, header, table or
+ * constant generator with this file, and neither side includes the other.
+ *
+ * Conventions
+ *   - Every loop runs element by element in index order; nothing is blocked,
+ *     fused or reordered beyond what the cited definition says.
+ *   - Where the pages fix fp32 state (the 2-bit residual carried between steps,
+ *     the fp32 messages of the full-precision correction step) the oracle keeps
+ *     that state in fp32 and rounds after every operation exactly as written.
+ *     Where a quantised code is decided by floating point, the decision is made
+ *     in fp32 with the operation order stated beside it.
+ *   - Every other floating-point result (sums, averages, weight updates,
+ *     dequantised values, elastic averaging) is computed in fp64.
+ *   - Build flags: -O2 -ffp-contract=off (no fused multiply-add contraction),
+ *     never -ffast-math.
+ *
+ * Sources (the web pages this method is taken from):
+ *   [MX]   "2bit gradient compression", MXNet pull request #8662, sections
+ *          "Two bit quantization", "Format of compressed gradient",
+ *          "Local kvstore", "Dist kvstore".
+ *   [CD]   "CD-SGD: Distributed Stochastic Gradient Descent with Compression
+ *          and Delay Compensation", eq. 1, eq. 10, Algorithm 1, section 3.1.
+ *   [QS]   "QSGD: Communication-Efficient SGD via Gradient Quantization and
+ *          Encoding" (summary page), Knowl 1 (operator Q_s), Knowl 2 (the
+ *          (norm, sign, level) tuple, norm stored as fp32), Knowl 3
+ *          (synchronous parallel QSGD), Knowl 8 (bucketing).
+ *   [SA]   "Communication-Efficient Decentralized Learning with Sparsification
+ *          and Adaptive Peer Selection", section II (coordinator/worker,
+ *          random mask with a shared seed, single-peer gossip matrix).
+ *   [EA]   IMerge design notes (blog), "Interleaved Communication Scheduling",
+ *          EASGD local and global update equations.
+ *   The counter-based hash (splitmix64 of seed XOR index, top 24 bits scaled
+ *   to [0,1)) is not on the pages; it is the published SplitMix64 finaliser
+ *   (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+ *   OOPSLA 2014).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Counter-based random numbers                                             */
+/* ------------------------------------------------------------------------ */
+
+/* SplitMix64 output function applied to one 64-bit counter value. */
+uint64_t orc_splitmix64(uint64_t x)
+{
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* u(key) = (splitmix64(key) >> 40) / 2^24, a multiple of 2^-24 in [0, 1). */
+double orc_uniform(uint64_t key)
+{
+    return (double)(orc_splitmix64(key) >> 40) / 16777216.0;
+}
+
+/* Round seed for SAPS round t: seed_t = splitmix64(base + t). */
+uint64_t orc_round_seed(uint64_t base, uint64_t t)
+{
+    return orc_splitmix64(base + t);
+}
+
+/* ------------------------------------------------------------------------ */
+/* [MX] 2-bit threshold quantisation with a residual                        */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_bits_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static float grad_at(const void *grad, int is_bf16, int64_t i)
+{
+    if (is_bf16)
+        return bf16_bits_to_float(((const uint16_t *)grad)[i]);
+    return ((const float *)grad)[i];
+}
+
+/*
+ * [MX] "Two bit quantization": the residual accumulates the gradient; a value
+ * greater than or equal to +t becomes code 11 and t is taken off the residual,
+ * a value less than or equal to -t becomes code 10 and t is added back, every
+ * other value becomes 00 and stays in the residual.
+ * [MX] "Format of compressed gradient": one 32-bit word holds 16 codes, the
+ * first element in the two most significant bits; unused tail bits are zero.
+ * The residual is fp32 and updated with one fp32 add per step.
+ */
+void orc_2bit_quantize(const void *grad, int is_bf16, float *residual,
+                       uint32_t *codes, int64_t n, float t)
+{
+    int64_t nwords = (n + 15) / 16;
+    for (int64_t k = 0; k < nwords; ++k)
+        codes[k] = 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        float r = residual[i] + grad_at(grad, is_bf16, i);
+        uint32_t q = 0u;
+        if (r >= t) {
+            q = 3u;
+            r = r - t;
+        } else if (r <= -t) {
+            q = 2u;
+            r = r + t;
+        }
+        residual[i] = r;
+        codes[i / 16] |= q << (30 - 2 * (int)(i % 16));
+    }
+}
+
+/* Decoded value of one 2-bit code: 11 -> +1, 10 -> -1, 00 and 01 -> 0. */
+static int decode_2bit(const uint32_t *codes, int64_t i)
+{
+    uint32_t q = (codes[i / 16] >> (30 - 2 * (int)(i % 16))) & 3u;
+    if (q == 3u)
+        return 1;
+    if (q == 2u)
+        return -1;
+    return 0;
+}
+
+/*
+ * [MX] "Local kvstore" / "Dist kvstore": the receiver dequantises every
+ * worker's codes (11 -> +t, 10 -> -t, 00 -> 0) into arrays of the original
+ * size and sums them.  [CD] eq. 10: W <- W - (eta/N) * sum of the N workers'
+ * compressed gradients.
+ *   kind 0 (none):  out[i] = (sum_w dec_w(i) * t) / W
+ *   kind 1 (SGD):   w[i]  -= lr * avg
+ *   kind 2 (EASGD local step, [EA] with the averaged gradient as g):
+ *                   w[i]  = w[i] - lr * avg - alpha * (w[i] - center[i])
+ * All arithmetic in fp64.
+ */
+void orc_2bit_dequant_sum_update(const uint32_t *const *codes, int W, int64_t n,
+                                 float t, int kind, double lr, double alpha,
+                                 const double *center, double *w, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double sum = 0.0;
+        for (int k = 0; k < W; ++k)
+            sum += (double)decode_2bit(codes[k], i) * (double)t;
+        double avg = sum / (double)W;
+        if (kind == 0) {
+            out[i] = avg;
+        } else if (kind == 1) {
+            w[i] = w[i] - lr * avg;
+        } else {
+            w[i] = w[i] - lr * avg - alpha * (w[i] - center[i]);
+        }
+    }
+}
+
+/*
+ * [CD] Algorithm 1 (formal training, the branch taken when count % k == 0)
+ * and section 3.1: on the correction step no quantisation happens and each
+ * worker pushes a 32-bit gradient.  Reading used here: the pushed message is
+ * the residual-compensated gradient m = r + g in fp32, after which the
+ * residual is empty.  The server applies eq. 1: W <- W - (eta/N) sum_j m_j,
+ * in fp64.
+ */
+void orc_compensated_sum_update(const void *const *grads, int is_bf16,
+                                float *const *residuals, int W, int64_t n,
+                                double lr, double *w)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double sum = 0.0;
+        for (int k = 0; k < W; ++k) {
+            float m = residuals[k][i] + grad_at(grads[k], is_bf16, i);
+            residuals[k][i] = 0.0f;
+            sum += (double)m;
+        }
+        w[i] = w[i] - lr * (sum / (double)W);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* [QS] QSGD stochastic quantisation                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Exact summation of doubles as a non-overlapping expansion (Shewchuk,
+ * "Adaptive Precision Floating-Point Arithmetic and Fast Robust Geometric
+ * Predicates", 1997 -- the partials method behind Python's math.fsum).
+ */
+#define ORC_MAX_PARTIALS 96
+typedef struct {
+    double p[ORC_MAX_PARTIALS];
+    int n;
+} orc_expansion;
+
+static void expansion_add(orc_expansion *e, double x)
+{
+    int j = 0;
+    for (int i = 0; i < e->n; ++i) {
+        double y = e->p[i];
+        if (fabs(x) < fabs(y)) {
+            double tmp = x;
+            x = y;
+            y = tmp;
+        }
+        double hi = x + y;
+        double lo = y - (hi - x);
+        if (lo != 0.0)
+            e->p[j++] = lo;
+        x = hi;
+    }
+    e->p[j++] = x;
+    e->n = j;
+}
+
+/* Sign of (X - m*m); m has at most 25 significant bits so m*m is exact. */
+static int expansion_cmp_square(const orc_expansion *X, double m)
+{
+    orc_expansion e = *X;
+    expansion_add(&e, -(m * m));
+    for (int i = e.n - 1; i >= 0; --i)
+        if (e.p[i] != 0.0)
+            return e.p[i] > 0.0 ? 1 : -1;
+    return 0;
+}
+
+static uint32_t float_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+
+/*
+ * [QS] Knowl 2: the l2 norm of the (bucketed) vector is stored as a single
+ * precision float.  Reading: the stored value is the true l2 norm rounded to
+ * nearest-even fp32.  The sum of squares is formed exactly, then the
+ * candidate is moved until it is the fp32 value nearest to sqrt(sum).
+ */
+float orc_l2norm_fp32(const float *v, int64_t len)
+{
+    orc_expansion X;
+    X.n = 0;
+    for (int64_t i = 0; i < len; ++i) {
+        double d = (double)v[i];
+        expansion_add(&X, d * d); /* fp32 squared is exact in fp64 */
+    }
+    double approx = 0.0;
+    for (int i = 0; i < X.n; ++i)
+        approx += X.p[i];
+    if (approx <= 0.0)
+        return 0.0f;
+    float r = (float)sqrt(approx);
+    for (int guard = 0; guard < 64; ++guard) {
+        float up = nextafterf(r, INFINITY);
+        double mid_hi = ((double)r + (double)up) * 0.5;
+        int c = expansion_cmp_square(&X, mid_hi);
+        if (c > 0 || (c == 0 && (float_bits(r) & 1u))) {
+            r = up;
+            continue;
+        }
+        if (r > 0.0f) {
+            float dn = nextafterf(r, 0.0f);
+            double mid_lo = ((double)r + (double)dn) * 0.5;
+            int c2 = expansion_cmp_square(&X, mid_lo);
+            if (c2 < 0 || (c2 == 0 && (float_bits(r) & 1u))) {
+                r = dn;
+                continue;
+            }
+        }
+        break;
+    }
+    return r;
+}
+
+/*
+ * [QS] Knowl 1 and Knowl 8: per bucket of d coordinates (the last one may be
+ * shorter), Q_s(v_i) = ||v|| * sgn(v_i) * xi_i with xi_i in {l/s, (l+1)/s},
+ * sgn(0) = +1 and Q_s(0) = 0.  The random choice is made as
+ *     level = floor(|v_i| / ||v|| * s + u),   u = uniform(seed_w ^ i)
+ * with the worker folded into the seed as seed_w = seed ^ (worker << 48) and
+ * i the global element index.  fp32 operation order of the decision:
+ *     S = s / norm,  a = |v_i| * S,  x = a + u,  level = min(floor(x), s)
+ * (a NaN x, possible only when s / norm overflows, counts as s).  A bucket
+ * with norm 0 gets level 0 everywhere.
+ * Codes are sign-magnitude: sign bit = (v_i < 0), set above the level bits.
+ *   1 <= s <= 7   : 4-bit codes, two per byte, element 2j in the HIGH nibble
+ *   8 <= s <= 127 : 8-bit codes, one per byte, bit 7 = sign
+ * Outputs: norms[ceil(n/d)] (fp32) and codes (ceil(n/2) or n bytes).
+ */
+void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
+                       uint64_t seed, int worker, float *norms, uint8_t *codes)
+{
+    int four_bit = (s <= 7);
+    int64_t nbuckets = (n + d - 1) / d;
+    uint64_t seed_w = seed ^ ((uint64_t)(uint32_t)worker << 48);
+    if (four_bit)
+        for (int64_t k = 0; k < (n + 1) / 2; ++k)
+            codes[k] = 0;
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        int64_t lo = b * d;
+        int64_t hi = lo + d < n ? lo + d : n;
+        float norm = orc_l2norm_fp32(v + lo, hi - lo);
+        norms[b] = norm;
+        float S = norm > 0.0f ? (float)s / norm : 0.0f;
+        for (int64_t i = lo; i < hi; ++i) {
+            uint32_t level = 0u;
+            if (norm > 0.0f) {
+                float a = fabsf(v[i]) * S;
+                float u = (float)orc_uniform(seed_w ^ (uint64_t)i);
+                float x = a + u;
+                if (x != x || x >= (float)s)
+                    level = (uint32_t)s;
+                else
+                    level = (uint32_t)floorf(x);
+                if (level > (uint32_t)s)
+                    level = (uint32_t)s;
+            }
+            uint32_t sign = v[i] < 0.0f ? 1u : 0u;
+            if (four_bit) {
+                uint32_t code = (sign << 3) | level;
+                if (i % 2 == 0)
+                    codes[i / 2] |= (uint8_t)(code << 4);
+                else
+                    codes[i / 2] |= (uint8_t)code;
+            } else {
+                codes[i] = (uint8_t)((sign << 7) | level);
+            }
+        }
+    }
+}
+
+/* Sign and level of element i from a code buffer written as above. */
+static void qsgd_code_at(const uint8_t *codes, int64_t i, int s, int *sign,
+                         int *level)
+{
+    if (s <= 7) {
+        uint8_t byte = codes[i / 2];
+        uint32_t c = (i % 2 == 0) ? (uint32_t)(byte >> 4) : (uint32_t)(byte & 15u);
+        *sign = (int)(c >> 3);
+        *level = (int)(c & 7u);
+    } else {
+        uint8_t c = codes[i];
+        *sign = (int)(c >> 7);
+        *level = (int)(c & 127u);
+    }
+}
+
+/*
+ * [QS] Knowl 2 (decode the (norm, sign, level) tuple: value = norm * sign *
+ * level / s) and Knowl 3 (sum the K decoded messages; scale = 1/K gives the
+ * average).  out[i] = scale * sum_w sgn * norm_{w,b} * level / s, in fp64.
+ */
+void orc_qsgd_dequant_sum(const uint8_t *const *codes, const float *const *norms,
+                          int W, int64_t n, int64_t d, int s, double scale,
+                          double *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double sum = 0.0;
+        for (int k = 0; k < W; ++k) {
+            int sign, level;
+            qsgd_code_at(codes[k], i, s, &sign, &level);
+            double val = (double)norms[k][i / d] * (double)level / (double)s;
+            sum += sign ? -val : val;
+        }
+        out[i] = scale * sum;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* [SA] SAPS sparsification, matching and peer averaging                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [SA] section II-B: every worker draws the same Bernoulli(p) mask from the
+ * round's shared seed; only masked coordinates are sent, as (index, value)
+ * pairs.  Reading: m_i = [uniform(seed_t ^ i) < p].  Indices come out in
+ * ascending order; every worker's value at each index is gathered.  Returns
+ * the number of masked coordinates; at most `capacity` are written.
+ */
+int64_t orc_saps_mask_compact(int64_t n, double p, uint64_t seed_t,
+                              const double *const *models, int W, uint32_t *idx,
+                              double *const *vals, int64_t capacity)
+{
+    int64_t K = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (orc_uniform(seed_t ^ (uint64_t)i) < p) {
+            if (K < capacity) {
+                idx[K] = (uint32_t)i;
+                for (int k = 0; k < W; ++k)
+                    vals[k][K] = models[k][i];
+            }
+            ++K;
+        }
+    }
+    return K;
+}
+
+/*
+ * [SA] section II-C: single-peer gossip, each worker exchanges with exactly
+ * one peer per round (a perfect matching; the gossip matrix then has two
+ * nonzeros of 1/2 per row and is doubly stochastic).  The pages choose the
+ * matching from measured link bandwidths; with no links here the matching is
+ * a uniformly random one drawn from the round seed: a Fisher-Yates shuffle
+ * with j = splitmix64(splitmix64(seed_t) ^ i) mod (i + 1) for i = W-1 .. 1,
+ * then pairs (perm[0], perm[1]), (perm[2], perm[3]), ...
+ * Returns 0, or -1 when W is not a positive even number.
+ */
+int orc_saps_matching(uint64_t seed_t, int W, int *pairs)
+{
+    if (W <= 0 || W % 2 != 0)
+        return -1;
+    for (int i = 0; i < W; ++i)
+        pairs[i] = i;
+    uint64_t base = orc_splitmix64(seed_t);
+    for (int i = W - 1; i >= 1; --i) {
+        int j = (int)(orc_splitmix64(base ^ (uint64_t)i) % (uint64_t)(i + 1));
+        int tmp = pairs[i];
+        pairs[i] = pairs[j];
+        pairs[j] = tmp;
+    }
+    return 0;
+}
+
+/*
+ * [SA] Algorithm 2 lines 9-10: each worker sends its sparsified model to its
+ * peer and averages what it receives with its own copy.  On masked
+ * coordinates both members of a pair end with (x_a + x_b) / 2; every other
+ * coordinate is unchanged.  fp64.
+ */
+void orc_saps_peer_average(double *const *models, const double *const *vals,
+                           const uint32_t *idx, int64_t K, const int *pairs,
+                           int W)
+{
+    for (int q = 0; q < W / 2; ++q) {
+        int a = pairs[2 * q];
+        int b = pairs[2 * q + 1];
+        for (int64_t k = 0; k < K; ++k) {
+            double m = (vals[a][k] + vals[b][k]) / 2.0;
+            models[a][idx[k]] = m;
+            models[b][idx[k]] = m;
+        }
+    }
+}
+
+/*
+ * [EA] EASGD, with no gradient term:
+ *   w^k_{t+1} = w^k_t - alpha * (w^k_t - c_t)
+ *   c_{t+1}   = (1 - beta) * c_t + beta * (1/K) sum_k w^k_t
+ * Both right-hand sides use the values before the step.  fp64.
+ */
+void orc_easgd_step(double *const *models, int W, int64_t n, double alpha,
+                    double beta, double *center)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double sum = 0.0;
+        for (int k = 0; k < W; ++k)
+            sum += models[k][i];
+        double mean = sum / (double)W;
+        double c = center[i];
+        for (int k = 0; k < W; ++k)
+            models[k][i] = models[k][i] - alpha * (models[k][i] - c);
+        center[i] = (1.0 - beta) * c + beta * mean;
+    }
+}
