@@ -1,0 +1,267 @@
+"""GB300-native gradient compression with error feedback.
+
+Thin Python binding over ``libgc_gb300.so`` (C ABI in ``include/gc_gb300.h``).
+Every function here only checks and marshals arguments -- torch tensors in,
+device pointers and the current CUDA stream out -- and calls the entry point of
+the same name.  All arithmetic runs in the library's sm_103a kernels; there is
+no CPU or PyTorch fallback: if the library cannot be built or loaded, every
+call raises.
+
+Entry points (same names as the C ABI):
+  gc_2bit_quantize, gc_2bit_dequant_sum_update, gc_compensated_sum_update,
+  qsgd_quantize, qsgd_dequant_sum,
+  saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
+  saps_peer_average, easgd_step, gc_status_string, gc_version
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "GcError", "load", "library_path",
+    "GC_OK", "GC_ERR_INVALID", "GC_ERR_ALIGN", "GC_ERR_CUDA", "GC_ERR_CAPACITY", "GC_ERR_TIMEOUT",
+    "GC_UPD_NONE", "GC_UPD_SGD", "GC_UPD_EASGD", "GC_MAX_WORKERS",
+    "gc_status_string", "gc_version", "gc_2bit_quantize", "gc_2bit_dequant_sum_update",
+    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed",
+    "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
+    "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
+]
+
+GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+GC_F32, GC_BF16 = 0, 1
+GC_UPD_NONE, GC_UPD_SGD, GC_UPD_EASGD = 0, 1, 2
+GC_MAX_WORKERS = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {gc_status_string(status)} ({status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libgc_gb300.so, building it with nvcc first if it is missing or
+    stale.  Raises if it cannot be built or loaded."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, u64, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                           ctypes.c_uint64, ctypes.c_float, ctypes.c_double,
+                                           ctypes.c_size_t)
+        sig = {
+            "gc_status_string": (ctypes.c_char_p, [i32]),
+            "gc_version": (i32, []),
+            "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
+            "gc_2bit_dequant_sum_update": (i32, [vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
+            "gc_compensated_sum_update": (i32, [vp, i32, vp, i32, i64, f32, vp, vp]),
+            "qsgd_quantize": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
+            "qsgd_dequant_sum": (i32, [vp, vp, i32, i64, i32, i32, f32, vp, vp]),
+            "saps_round_seed": (u64, [u64, u64]),
+            "saps_matching": (i32, [u64, i32, vp]),
+            "saps_workspace_bytes": (sz, [i64]),
+            "saps_mask_compact": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz, vp, vp]),
+            "saps_peer_average": (i32, [vp, vp, vp, vp, vp, i32, i64, vp]),
+            "easgd_step": (i32, [vp, i32, i64, f32, f32, vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _stream(stream, t: torch.Tensor | None = None):
+    if stream is None:
+        dev = t.device if t is not None else torch.device("cuda", torch.cuda.current_device())
+        return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, numel: int | None = None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: needs at least {numel} elements, has {t.numel()}")
+    return t.data_ptr()
+
+
+def _ptrs(ts, name, dtype=None, numel=None):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]", dtype, numel) for i, t in enumerate(ts)])
+
+
+def _check(status: int, where: str) -> None:
+    if status != GC_OK:
+        raise GcError(status, where)
+
+
+def _gdtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GC_F32
+    if t.dtype == torch.bfloat16:
+        return GC_BF16
+    raise TypeError(f"gradient dtype must be float32 or bfloat16, got {t.dtype}")
+
+
+def code_words(n: int) -> int:
+    """uint32 words of 2-bit codes for n elements."""
+    return (n + 15) // 16
+
+
+def qsgd_code_bytes(n: int, s_levels: int) -> int:
+    return (n + 1) // 2 if s_levels <= 7 else n
+
+
+def qsgd_num_buckets(n: int, bucket: int) -> int:
+    return (n + bucket - 1) // bucket
+
+
+# ---------------------------------------------------------------- entry points
+
+def gc_status_string(status: int) -> str:
+    return load().gc_status_string(int(status)).decode()
+
+
+def gc_version() -> int:
+    return int(load().gc_version())
+
+
+def gc_2bit_quantize(grad: torch.Tensor, residual: torch.Tensor, codes: torch.Tensor,
+                     threshold: float, stream=None) -> None:
+    n = grad.numel()
+    lib = load()
+    st = lib.gc_2bit_quantize(_dev(grad, "grad"), _gdtype(grad), _dev(residual, "residual", torch.float32, n),
+                              _dev(codes, "codes", torch.int32, code_words(n)), n, float(threshold),
+                              _stream(stream, grad))
+    _check(st, "gc_2bit_quantize")
+
+
+def gc_2bit_dequant_sum_update(codes, n: int, threshold: float, kind: int = GC_UPD_NONE,
+                               lr: float = 0.0, alpha: float = 0.0, center=None, weights=None,
+                               out=None, stream=None) -> None:
+    """codes: list of W int32 tensors (the packed uint32 words)."""
+    lib = load()
+    W = len(codes)
+    arr = _ptrs(codes, "codes", torch.int32, code_words(n))
+    st = lib.gc_2bit_dequant_sum_update(
+        arr, W, n, float(threshold), int(kind), float(lr), float(alpha),
+        _dev(center, "center", torch.float32, n) if center is not None else None,
+        _dev(weights, "weights", torch.float32, n) if weights is not None else None,
+        _dev(out, "out", torch.float32, n) if out is not None else None,
+        _stream(stream, codes[0] if W else None))
+    _check(st, "gc_2bit_dequant_sum_update")
+
+
+def gc_compensated_sum_update(grads, residuals, lr: float, weights: torch.Tensor, stream=None) -> None:
+    lib = load()
+    W = len(grads)
+    n = weights.numel()
+    dt = _gdtype(grads[0])
+    st = lib.gc_compensated_sum_update(_ptrs(grads, "grads", grads[0].dtype, n), dt,
+                                       _ptrs(residuals, "residuals", torch.float32, n), W, n,
+                                       float(lr), _dev(weights, "weights", torch.float32, n),
+                                       _stream(stream, weights))
+    _check(st, "gc_compensated_sum_update")
+
+
+def qsgd_quantize(grad: torch.Tensor, bucket: int, s_levels: int, seed: int, worker: int,
+                  norms: torch.Tensor, codes: torch.Tensor, stream=None) -> None:
+    lib = load()
+    n = grad.numel()
+    st = lib.qsgd_quantize(_dev(grad, "grad", torch.float32), n, int(bucket), int(s_levels),
+                           int(seed) & 0xFFFFFFFFFFFFFFFF, int(worker),
+                           _dev(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
+                           _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+                           _stream(stream, grad))
+    _check(st, "qsgd_quantize")
+
+
+def qsgd_dequant_sum(codes, norms, n: int, bucket: int, s_levels: int, scale: float,
+                     out: torch.Tensor, stream=None) -> None:
+    lib = load()
+    W = len(codes)
+    st = lib.qsgd_dequant_sum(_ptrs(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+                              _ptrs(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
+                              W, n, int(bucket), int(s_levels), float(scale),
+                              _dev(out, "out", torch.float32, n), _stream(stream, out))
+    _check(st, "qsgd_dequant_sum")
+
+
+def saps_round_seed(base_seed: int, t: int) -> int:
+    return int(load().saps_round_seed(int(base_seed) & 0xFFFFFFFFFFFFFFFF, int(t) & 0xFFFFFFFFFFFFFFFF))
+
+
+def saps_matching(seed_t: int, W: int) -> list[int]:
+    buf = (ctypes.c_int * max(W, 1))()
+    _check(load().saps_matching(int(seed_t) & 0xFFFFFFFFFFFFFFFF, int(W), buf), "saps_matching")
+    return list(buf)[:W]
+
+
+def saps_workspace_bytes(n: int) -> int:
+    return int(load().saps_workspace_bytes(int(n)))
+
+
+def saps_mask_compact(n: int, p: float, seed_t: int, models, idx: torch.Tensor, vals,
+                      d_count: torch.Tensor, workspace: torch.Tensor, d_status: torch.Tensor,
+                      stream=None) -> None:
+    """models: W fp32 tensors [n]; idx: int32 (uint32 bits) [capacity]; vals: W fp32
+    [capacity]; d_count: int64 [1]; workspace: uint8 [saps_workspace_bytes(n)];
+    d_status: int32 [1] (zeroed by the caller)."""
+    lib = load()
+    W = len(models)
+    capacity = idx.numel()
+    st = lib.saps_mask_compact(int(n), float(p), int(seed_t) & 0xFFFFFFFFFFFFFFFF,
+                               _ptrs(models, "models", torch.float32, n), W,
+                               _dev(idx, "idx", torch.int32), _ptrs(vals, "vals", torch.float32, capacity),
+                               capacity, _dev(d_count, "d_count", torch.int64, 1),
+                               _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+                               _dev(d_status, "d_status", torch.int32, 1), _stream(stream, idx))
+    _check(st, "saps_mask_compact")
+
+
+def saps_peer_average(models, vals, idx: torch.Tensor, d_count: torch.Tensor, pairs,
+                      stream=None) -> None:
+    lib = load()
+    W = len(models)
+    pairs_arr = (ctypes.c_int * W)(*[int(p) for p in pairs])
+    capacity = idx.numel()
+    st = lib.saps_peer_average(_ptrs(models, "models", torch.float32),
+                               _ptrs(vals, "vals", torch.float32, capacity),
+                               _dev(idx, "idx", torch.int32), _dev(d_count, "d_count", torch.int64, 1),
+                               pairs_arr, W, capacity, _stream(stream, idx))
+    _check(st, "saps_peer_average")
+
+
+def easgd_step(models, alpha: float, beta: float, center: torch.Tensor, stream=None) -> None:
+    lib = load()
+    W = len(models)
+    n = center.numel()
+    st = lib.easgd_step(_ptrs(models, "models", torch.float32, n), W, n, float(alpha), float(beta),
+                        _dev(center, "center", torch.float32, n), _stream(stream, center))
+    _check(st, "easgd_step")

@@ -1,0 +1,330 @@
+// qsgd.cu -- QSGD bucketed stochastic quantisation and its dequantise-sum.
+//
+// Source: "QSGD: Communication-Efficient SGD via Gradient Quantization and
+// Encoding" (summary page), Knowl 1 (operator Q_s), Knowl 2 (norm stored as
+// a single-precision float, sign and level per coordinate), Knowl 3 (sum /
+// average of the decoded messages), Knowl 8 (bucketing).
+//
+// One warp owns one bucket of d = 128 * ROUNDS elements; lane l reads the
+// 16-byte vectors at bucket offsets 128j + 4l (j < ROUNDS), so the bucket is
+// read from HBM exactly once and kept in registers between the norm and the
+// quantisation.
+#include "gc_common.cuh"
+
+namespace gc {
+namespace {
+
+// Knuth's TwoSum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// Adds x*x to the double-float accumulator (hi, lo) without losing the
+// rounding error of the square (x*x == p + q exactly).
+__device__ __forceinline__ void acc_square(float x, float& hi, float& lo) {
+    const float p = __fmul_rn(x, x);
+    const float q = __fmaf_rn(x, x, -p);
+    float s, e;
+    two_sum(hi, p, s, e);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(e, q));
+}
+
+// The bucket's l2 norm, rounded to nearest fp32 (equal to the correctly
+// rounded value unless sqrt(sum) lies within about 2^-40 relative of a
+// rounding midpoint).  Every lane returns the same value.
+__device__ __forceinline__ float warp_norm(float hi, float lo) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        float s, e;
+        two_sum(hi, h2, s, e);
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    }
+    const float X = __fadd_rn(hi, lo);
+    const float Xl = __fsub_rn(lo, __fsub_rn(X, hi));
+    if (!(X > 0.0f)) return 0.0f;
+    const float r = __fsqrt_rn(X);
+    const float rem = __fadd_rn(__fmaf_rn(-r, r, X), Xl);     // X + Xl - r^2
+    return __fmaf_rn(rem, __fdiv_rn(0.5f, r), r);             // r + rem / (2r)
+}
+
+struct QArgs {
+    const float* v;
+    int64_t n;
+    int64_t nbuckets;
+    uint64_t seed_w;      // seed ^ (worker << 48)
+    int s;
+    float* norms;
+    uint8_t* codes;
+};
+
+// level = min(floor(|v| * S + u), s) in fp32, u = top24(hash) * 2^-24.
+__device__ __forceinline__ uint32_t qlevel(float x, float S, float s_f, uint32_t s, uint64_t key) {
+    const float u = __fmul_rn(__uint2float_rn(splitmix64_top24(key)), 5.9604644775390625e-8f);
+    const float y = __fadd_rn(__fmul_rn(fabsf(x), S), u);
+    // for 0 <= y < 2^23, rounding y + 2^23 downwards leaves floor(y) in the
+    // mantissa bits
+    const uint32_t fl = __float_as_uint(__fadd_rd(y, 8388608.0f)) & 0x7FFFFFu;
+    return (y < s_f) ? fl : s;
+}
+
+template <int ROUNDS, bool FOUR>
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+k_qsgd_quantize(const QArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    constexpr int D = 128 * ROUNDS;
+    constexpr uint32_t kSignShift = FOUR ? 3 : 7;
+    const float s_f = static_cast<float>(a.s);
+    const uint32_t s_u = static_cast<uint32_t>(a.s);
+
+    for (int64_t b = warp; b < a.nbuckets; b += nwarps) {
+        const int64_t b0 = b * D;
+        const bool full = b0 + D <= a.n;
+        float4 v[ROUNDS];
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < ROUNDS; ++j) v[j] = ld_stream_f4(a.v + b0 + 128 * j + 4 * lane);
+        } else {
+#pragma unroll
+            for (int j = 0; j < ROUNDS; ++j) {
+                const int64_t e = b0 + 128 * j + 4 * lane;
+                v[j].x = e < a.n ? a.v[e] : 0.0f;
+                v[j].y = e + 1 < a.n ? a.v[e + 1] : 0.0f;
+                v[j].z = e + 2 < a.n ? a.v[e + 2] : 0.0f;
+                v[j].w = e + 3 < a.n ? a.v[e + 3] : 0.0f;
+            }
+        }
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j) {
+            acc_square(v[j].x, hi, lo);
+            acc_square(v[j].y, hi, lo);
+            acc_square(v[j].z, hi, lo);
+            acc_square(v[j].w, hi, lo);
+        }
+        const float norm = warp_norm(hi, lo);
+        if (lane == 0) a.norms[b] = norm;
+        const bool zero = !(norm > 0.0f);
+        const float S = zero ? 0.0f : __fdiv_rn(s_f, norm);
+
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j) {
+            const int64_t e = b0 + 128 * j + 4 * lane;
+            const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t c[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t lvl = zero ? 0u : qlevel(xs[k], S, s_f, s_u, a.seed_w ^ static_cast<uint64_t>(e + k));
+                c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
+            }
+            if (FOUR) {
+                const uint32_t lo2 = (c[0] << 4) | c[1];
+                const uint32_t hi2 = (c[2] << 4) | c[3];
+                if (full) {
+                    *reinterpret_cast<uint16_t*>(a.codes + (e >> 1)) = static_cast<uint16_t>(lo2 | (hi2 << 8));
+                } else {
+                    if (e < a.n) a.codes[e >> 1] = static_cast<uint8_t>(e + 1 < a.n ? lo2 : (c[0] << 4));
+                    if (e + 2 < a.n) a.codes[(e >> 1) + 1] = static_cast<uint8_t>(e + 3 < a.n ? hi2 : (c[2] << 4));
+                }
+            } else {
+                if (full) {
+                    *reinterpret_cast<uint32_t*>(a.codes + e) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (e + k < a.n) a.codes[e + k] = static_cast<uint8_t>(c[k]);
+                }
+            }
+        }
+    }
+}
+
+struct DArgs {
+    PtrTable<const uint8_t*> codes;
+    PtrTable<const float*> norms;
+    int W;
+    int64_t n;
+    int64_t nbuckets;
+    int s;
+    float scale;
+    float* out;
+};
+
+template <bool FOUR>
+__device__ __forceinline__ void decode4(const uint8_t* codes, int64_t e, int64_t n, bool full,
+                                        uint32_t (&c)[4]) {
+    if (FOUR) {
+        uint32_t h;
+        if (full) {
+            h = *reinterpret_cast<const uint16_t*>(codes + (e >> 1));
+        } else {
+            h = (e < n ? codes[e >> 1] : 0u) | ((e + 2 < n ? codes[(e >> 1) + 1] : 0u) << 8);
+        }
+        c[0] = (h >> 4) & 15u;
+        c[1] = h & 15u;
+        c[2] = (h >> 12) & 15u;
+        c[3] = (h >> 8) & 15u;
+    } else {
+        uint32_t w;
+        if (full) {
+            w = __ldg(reinterpret_cast<const uint32_t*>(codes + e));
+        } else {
+            w = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (e + k < n) w |= static_cast<uint32_t>(codes[e + k]) << (8 * k);
+        }
+        c[0] = w & 255u;
+        c[1] = (w >> 8) & 255u;
+        c[2] = (w >> 16) & 255u;
+        c[3] = w >> 24;
+    }
+}
+
+template <int ROUNDS, bool FOUR>
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+k_qsgd_dequant_sum(const DArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    constexpr int D = 128 * ROUNDS;
+    constexpr uint32_t kLevelMask = FOUR ? 7u : 127u;
+    constexpr uint32_t kSignBit = FOUR ? 8u : 128u;
+    const float s_f = static_cast<float>(a.s);
+
+    for (int64_t b = warp; b < a.nbuckets; b += nwarps) {
+        const int64_t b0 = b * D;
+        const bool full = b0 + D <= a.n;
+        float sum[ROUNDS][4];
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sum[j][k] = 0.0f;
+        for (int w = 0; w < a.W; ++w) {
+            const uint8_t* cw = a.codes.p[w];
+            const float unit = __fdiv_rn(__ldg(a.norms.p[w] + b), s_f);
+#pragma unroll
+            for (int j = 0; j < ROUNDS; ++j) {
+                const int64_t e = b0 + 128 * j + 4 * lane;
+                uint32_t c[4];
+                decode4<FOUR>(cw, e, a.n, full, c);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float lf = __uint_as_float(0x4B000000u | (c[k] & kLevelMask)) - 8388608.0f;
+                    const float term = __fmul_rn(unit, lf);
+                    sum[j][k] = (c[k] & kSignBit) ? __fsub_rn(sum[j][k], term) : __fadd_rn(sum[j][k], term);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j) {
+            const int64_t e = b0 + 128 * j + 4 * lane;
+            const float4 o = make_float4(__fmul_rn(a.scale, sum[j][0]), __fmul_rn(a.scale, sum[j][1]),
+                                         __fmul_rn(a.scale, sum[j][2]), __fmul_rn(a.scale, sum[j][3]));
+            if (full) {
+                st_stream_f4(a.out + e, o);
+            } else {
+                if (e < a.n) a.out[e] = o.x;
+                if (e + 1 < a.n) a.out[e + 1] = o.y;
+                if (e + 2 < a.n) a.out[e + 2] = o.z;
+                if (e + 3 < a.n) a.out[e + 3] = o.w;
+            }
+        }
+    }
+}
+
+template <bool FOUR>
+int launch_quantize(int rounds, const QArgs& a, int grid, cudaStream_t s) {
+    switch (rounds) {
+        case 1: k_qsgd_quantize<1, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 2: k_qsgd_quantize<2, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 4: k_qsgd_quantize<4, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 8: k_qsgd_quantize<8, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 16: k_qsgd_quantize<16, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        default: return GC_ERR_INVALID;
+    }
+    return launch_status();
+}
+
+template <bool FOUR>
+int launch_dequant(int rounds, const DArgs& a, int grid, cudaStream_t s) {
+    switch (rounds) {
+        case 1: k_qsgd_dequant_sum<1, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 2: k_qsgd_dequant_sum<2, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 4: k_qsgd_dequant_sum<4, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 8: k_qsgd_dequant_sum<8, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 16: k_qsgd_dequant_sum<16, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        default: return GC_ERR_INVALID;
+    }
+    return launch_status();
+}
+
+bool valid_bucket(int bucket) {
+    return bucket == 128 || bucket == 256 || bucket == 512 || bucket == 1024 || bucket == 2048;
+}
+
+}  // namespace
+}  // namespace gc
+
+using namespace gc;
+
+extern "C" {
+
+int qsgd_quantize(const float* grad, int64_t n, int bucket, int s_levels, uint64_t seed, int worker,
+                  float* norms, uint8_t* codes, gc_stream_t stream) {
+    if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127 || worker < 0)
+        return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grad || !norms || !codes) return GC_ERR_INVALID;
+    if (!aligned16(grad) || !aligned16(norms) || !aligned16(codes)) return GC_ERR_ALIGN;
+    QArgs a;
+    a.v = grad;
+    a.n = n;
+    a.nbuckets = (n + bucket - 1) / bucket;
+    a.seed_w = seed ^ (static_cast<uint64_t>(static_cast<uint32_t>(worker)) << 48);
+    a.s = s_levels;
+    a.norms = norms;
+    a.codes = codes;
+    const int grid = grid_for(4);
+    if (grid <= 0) return GC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return s_levels <= 7 ? launch_quantize<true>(bucket / 128, a, grid, s)
+                         : launch_quantize<false>(bucket / 128, a, grid, s);
+}
+
+int qsgd_dequant_sum(const uint8_t* const* codes, const float* const* norms, int W, int64_t n,
+                     int bucket, int s_levels, float scale, float* out, gc_stream_t stream) {
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !valid_bucket(bucket) || s_levels < 1 ||
+        s_levels > 127 || !isfinite(scale))
+        return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!codes || !norms || !out) return GC_ERR_INVALID;
+    DArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!codes[w] || !norms[w]) return GC_ERR_INVALID;
+        if (!aligned16(codes[w]) || !aligned16(norms[w])) return GC_ERR_ALIGN;
+        a.codes.p[w] = codes[w];
+        a.norms.p[w] = norms[w];
+    }
+    if (!aligned16(out)) return GC_ERR_ALIGN;
+    a.W = W;
+    a.n = n;
+    a.nbuckets = (n + bucket - 1) / bucket;
+    a.s = s_levels;
+    a.scale = scale;
+    a.out = out;
+    const int grid = grid_for(4);
+    if (grid <= 0) return GC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return s_levels <= 7 ? launch_dequant<true>(bucket / 128, a, grid, s)
+                         : launch_dequant<false>(bucket / 128, a, grid, s);
+}
+
+}  // extern "C"

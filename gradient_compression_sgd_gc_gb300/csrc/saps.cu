@@ -1,0 +1,439 @@
+// saps.cu -- SAPS seeded random-mask sparsification (stream compaction with a
+// single-pass decoupled look-back scan), peer averaging over a perfect
+// matching, and the EASGD elastic step.
+//
+// Sources: "Communication-Efficient Decentralized Learning with
+// Sparsification and Adaptive Peer Selection", section II (coordinator sends
+// the round seed; all workers draw the same Bernoulli mask; single-peer
+// gossip with a doubly stochastic matrix; Algorithm 2 lines 9-10 average the
+// received sparsified model); EASGD local and global updates from the IMerge
+// design notes.  The look-back scan follows Merrill and Garland,
+// "Single-pass Parallel Prefix Scan with Decoupled Look-back" (NVIDIA
+// technical report NVR-2016-002).
+#include "gc_common.cuh"
+
+namespace gc {
+namespace {
+
+// ------------------------------------------------------------------ K6
+
+constexpr int kItems = 16;                         // rounds of 32 elements per warp
+constexpr int kWarpSpan = 32 * kItems;             // 512 elements per warp
+constexpr int kTileElems = kWarpsPerBlock * kWarpSpan;   // 4096 elements per CTA tile
+constexpr size_t kWsHeader = 64;                   // tile counter + padding
+
+constexpr uint64_t kFlagAgg = 1ull << 62;
+constexpr uint64_t kFlagPrefix = 2ull << 62;
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per look-back wait
+
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+struct MaskArgs {
+    int64_t n;
+    uint64_t seed_t;
+    uint32_t thr;                 // ceil(p * 2^24)
+    int W;
+    PtrTable<const float*> models;
+    PtrTable<float*> vals;
+    uint32_t* idx;
+    int64_t capacity;
+    uint64_t* d_count;
+    unsigned long long* counter; // dynamic tile counter (workspace)
+    uint64_t* state;             // per-tile look-back state (workspace)
+    int64_t ntiles;
+    int* d_status;
+};
+
+// Exclusive prefix of tile `tile` whose own count is `agg`; run by one warp.
+// Publishes (aggregate) first, then walks back 32 predecessors at a time.
+// Every wait is bounded: after kWaitLimitNs the missing predecessors count
+// as zero and GC_ERR_TIMEOUT is recorded.
+__device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
+    if (tile == 0) {
+        if (lane == 0) st_release(a.state, kFlagPrefix | agg);
+        return 0;
+    }
+    if (lane == 0) st_release(a.state + tile, kFlagAgg | agg);
+    uint64_t excl = 0;
+    int64_t end = tile - 1;
+    const uint64_t t0 = global_ns();
+    bool timed_out = false;
+    while (true) {
+        const int64_t j = end - lane;
+        uint64_t st = j >= 0 ? ld_acquire(a.state + j) : kFlagPrefix;
+        unsigned ns = 32;
+        while (true) {
+            const bool pending = (st >> 62) == 0;
+            if (!__any_sync(0xffffffffu, pending)) break;
+            // lane 0's clock decides, so the whole warp leaves together
+            const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs, 0);
+            if (expired) {
+                timed_out = true;
+                if (pending) st = kFlagAgg;   // unknown predecessor counts as 0
+                break;
+            }
+            __nanosleep(ns);
+            if (ns < 1024) ns <<= 1;
+            if (pending) st = ld_acquire(a.state + j);
+        }
+        const unsigned prefix_lanes = __ballot_sync(0xffffffffu, (st >> 62) == 2);
+        const int last = prefix_lanes ? __ffs(prefix_lanes) - 1 : 31;
+        uint64_t v = lane <= last ? (st & kValueMask) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        excl += v;
+        if (prefix_lanes) break;
+        end -= 32;
+    }
+    if (lane == 0) {
+        st_release(a.state + tile, kFlagPrefix | (excl + agg));
+        if (timed_out) atomicExch(a.d_status, GC_ERR_TIMEOUT);
+    }
+    return excl;
+}
+
+// K6: one CTA per 4096-element tile, tiles taken in launch order from a
+// dynamic counter so every predecessor is already running.  Warp w hashes
+// elements tile*4096 + 512w + 32r + lane (r < 16) and keeps the ballot of
+// round r in lane r.  After the scan the CTA lists its masked indices in
+// shared memory and writes idx[] and every worker's vals[] with coalesced
+// stores.
+__global__ void __launch_bounds__(kThreads)
+k_saps_mask_compact(const MaskArgs a) {
+    __shared__ uint32_t s_list[kTileElems];
+    __shared__ uint32_t s_warp_excl[kWarpsPerBlock];
+    __shared__ uint32_t s_warp_tot[kWarpsPerBlock];
+    __shared__ unsigned long long s_tile;
+    __shared__ uint64_t s_excl;
+    __shared__ uint32_t s_agg;
+
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_tile = atomicAdd(a.counter, 1ull);
+    __syncthreads();
+    const int64_t tile = static_cast<int64_t>(s_tile);
+    const int64_t wbase = tile * kTileElems + static_cast<int64_t>(wib) * kWarpSpan;
+
+    uint32_t my_mask = 0;
+#pragma unroll 4
+    for (int r = 0; r < kItems; ++r) {
+        const int64_t e = wbase + 32 * r + lane;
+        const bool hit = e < a.n && splitmix64_top24(a.seed_t ^ static_cast<uint64_t>(e)) < a.thr;
+        const uint32_t m = __ballot_sync(0xffffffffu, hit);
+        if (lane == r) my_mask = m;
+    }
+    const uint32_t cnt = __popc(my_mask);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t round_excl = incl - cnt;
+    if (lane == 31) s_warp_tot[wib] = incl;
+    __syncthreads();
+
+    if (wib == 0) {
+        const uint32_t v = lane < kWarpsPerBlock ? s_warp_tot[lane] : 0u;
+        uint32_t vi = v;
+#pragma unroll
+        for (int o = 1; o < kWarpsPerBlock; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, vi, o);
+            if (lane >= o) vi += t;
+        }
+        if (lane < kWarpsPerBlock) s_warp_excl[lane] = vi - v;
+        const uint32_t agg = __shfl_sync(0xffffffffu, vi, kWarpsPerBlock - 1);
+        const uint64_t excl = lookback(a, tile, agg, lane);
+        if (lane == 0) {
+            s_excl = excl;
+            s_agg = agg;
+        }
+    }
+    __syncthreads();
+
+    const uint32_t wex = s_warp_excl[wib];
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 4
+    for (int r = 0; r < kItems; ++r) {
+        const uint32_t m = __shfl_sync(0xffffffffu, my_mask, r);
+        const uint32_t re = __shfl_sync(0xffffffffu, round_excl, r);
+        if (m & (1u << lane)) s_list[wex + re + __popc(m & lt)] = static_cast<uint32_t>(wbase + 32 * r + lane);
+    }
+    __syncthreads();
+
+    const uint64_t excl = s_excl;
+    const uint32_t agg = s_agg;
+    for (uint32_t k = threadIdx.x; k < agg; k += kThreads) {
+        const uint64_t pos = excl + k;
+        if (pos >= static_cast<uint64_t>(a.capacity)) break;
+        const uint32_t e = s_list[k];
+        a.idx[pos] = e;
+        int w = 0;
+        for (; w + 4 <= a.W; w += 4) {
+            const float v0 = __ldg(a.models.p[w] + e);
+            const float v1 = __ldg(a.models.p[w + 1] + e);
+            const float v2 = __ldg(a.models.p[w + 2] + e);
+            const float v3 = __ldg(a.models.p[w + 3] + e);
+            a.vals.p[w][pos] = v0;
+            a.vals.p[w + 1][pos] = v1;
+            a.vals.p[w + 2][pos] = v2;
+            a.vals.p[w + 3][pos] = v3;
+        }
+        for (; w < a.W; ++w) a.vals.p[w][pos] = __ldg(a.models.p[w] + e);
+    }
+    if (threadIdx.x == 0 && tile == a.ntiles - 1) {
+        const uint64_t total = excl + agg;
+        *a.d_count = total;
+        if (total > static_cast<uint64_t>(a.capacity)) atomicExch(a.d_status, GC_ERR_CAPACITY);
+    }
+}
+
+// ------------------------------------------------------------------ K7
+
+struct AvgArgs {
+    PtrTable<float*> models;
+    PtrTable<const float*> vals;
+    int pairs[GC_MAX_WORKERS];
+    int W;
+    const uint32_t* idx;
+    const uint64_t* d_count;
+    int64_t capacity;
+};
+
+__global__ void __launch_bounds__(kThreads)
+k_saps_peer_average(const AvgArgs a) {
+    const uint64_t cnt = *a.d_count;
+    const int64_t count = cnt < static_cast<uint64_t>(a.capacity) ? static_cast<int64_t>(cnt) : a.capacity;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < count; k += stride) {
+        const uint32_t e = a.idx[k];
+        for (int q = 0; q < a.W / 2; ++q) {
+            const int pa = a.pairs[2 * q], pb = a.pairs[2 * q + 1];
+            const float v = __fmul_rn(__fadd_rn(__ldg(a.vals.p[pa] + k), __ldg(a.vals.p[pb] + k)), 0.5f);
+            a.models.p[pa][e] = v;
+            a.models.p[pb][e] = v;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ K8
+
+struct EasgdArgs {
+    PtrTable<float*> models;
+    int W;
+    int64_t n;
+    float alpha, beta, inv_w;
+    float* center;
+};
+
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+__device__ __forceinline__ float elastic(float w, float c, float alpha) {
+    return fmaf(-alpha, __fsub_rn(w, c), w);
+}
+
+// K8, W <= 16: every worker's float4 at element 4i and the center's are
+// loaded once, the pre-step mean is formed in worker order, and all W + 1
+// vectors are written back.
+template <int MAXW>
+__global__ void __launch_bounds__(kThreads, 2)
+k_easgd(const EasgdArgs a) {
+    const int64_t nv = a.n >> 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i = gtid; i < nv; i += stride) {
+        float4 m[MAXW];
+#pragma unroll
+        for (int k = 0; k < MAXW; ++k)
+            if (k < a.W) m[k] = ld_f4(a.models.p[k] + 4 * i);
+        const float4 c = ld_f4(a.center + 4 * i);
+        float4 sum = m[0];
+#pragma unroll
+        for (int k = 1; k < MAXW; ++k)
+            if (k < a.W) sum = f4_add(sum, m[k]);
+#pragma unroll
+        for (int k = 0; k < MAXW; ++k) {
+            if (k < a.W) {
+                st_stream_f4(a.models.p[k] + 4 * i,
+                             make_float4(elastic(m[k].x, c.x, a.alpha), elastic(m[k].y, c.y, a.alpha),
+                                         elastic(m[k].z, c.z, a.alpha), elastic(m[k].w, c.w, a.alpha)));
+            }
+        }
+        const float4 mean = make_float4(__fmul_rn(sum.x, a.inv_w), __fmul_rn(sum.y, a.inv_w),
+                                        __fmul_rn(sum.z, a.inv_w), __fmul_rn(sum.w, a.inv_w));
+        st_stream_f4(a.center + 4 * i,
+                     make_float4(fmaf(a.beta, __fsub_rn(mean.x, c.x), c.x), fmaf(a.beta, __fsub_rn(mean.y, c.y), c.y),
+                                 fmaf(a.beta, __fsub_rn(mean.z, c.z), c.z), fmaf(a.beta, __fsub_rn(mean.w, c.w), c.w)));
+    }
+    // tail: the last n % 4 elements
+    const int64_t t = (nv << 2) + gtid;
+    if (gtid < (a.n & 3)) {
+        const float c = a.center[t];
+        float sum = 0.0f;
+        for (int k = 0; k < a.W; ++k) sum = __fadd_rn(sum, a.models.p[k][t]);
+        for (int k = 0; k < a.W; ++k) a.models.p[k][t] = elastic(a.models.p[k][t], c, a.alpha);
+        a.center[t] = fmaf(a.beta, __fsub_rn(__fmul_rn(sum, a.inv_w), c), c);
+    }
+}
+
+// K8, any W <= 64: two passes per element (sum, then update), the second
+// re-reading the models.
+__global__ void __launch_bounds__(kThreads)
+k_easgd_wide(const EasgdArgs a) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n; i += stride) {
+        const float c = a.center[i];
+        float sum = 0.0f;
+        for (int k = 0; k < a.W; ++k) sum = __fadd_rn(sum, a.models.p[k][i]);
+        for (int k = 0; k < a.W; ++k) a.models.p[k][i] = elastic(a.models.p[k][i], c, a.alpha);
+        a.center[i] = fmaf(a.beta, __fsub_rn(__fmul_rn(sum, a.inv_w), c), c);
+    }
+}
+
+int64_t mask_tiles(int64_t n) { return (n + kTileElems - 1) / kTileElems; }
+
+}  // namespace
+}  // namespace gc
+
+using namespace gc;
+
+extern "C" {
+
+uint64_t saps_round_seed(uint64_t base_seed, uint64_t t) { return splitmix64(base_seed + t); }
+
+int saps_matching(uint64_t seed_t, int W, int* pairs_out) {
+    if (W < 2 || W > GC_MAX_WORKERS || (W & 1) || !pairs_out) return GC_ERR_INVALID;
+    for (int i = 0; i < W; ++i) pairs_out[i] = i;
+    const uint64_t base = splitmix64(seed_t);
+    for (int i = W - 1; i >= 1; --i) {
+        const int j = static_cast<int>(splitmix64(base ^ static_cast<uint64_t>(i)) % static_cast<uint64_t>(i + 1));
+        const int tmp = pairs_out[i];
+        pairs_out[i] = pairs_out[j];
+        pairs_out[j] = tmp;
+    }
+    return GC_OK;
+}
+
+size_t saps_workspace_bytes(int64_t n) {
+    if (n <= 0) return kWsHeader;
+    return kWsHeader + sizeof(uint64_t) * static_cast<size_t>(mask_tiles(n));
+}
+
+int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* models, int W,
+                      uint32_t* idx, float* const* vals, int64_t capacity, uint64_t* d_count,
+                      void* workspace, size_t workspace_bytes, int* d_status, gc_stream_t stream) {
+    if (n < 0 || n > 0xFFFFFFFFll || W < 1 || W > GC_MAX_WORKERS || capacity < 0) return GC_ERR_INVALID;
+    if (!(p > 0.0 && p <= 1.0)) return GC_ERR_INVALID;
+    if (!d_count || !workspace || !d_status || !models || (capacity > 0 && (!idx || !vals)))
+        return GC_ERR_INVALID;
+    if (workspace_bytes < saps_workspace_bytes(n)) return GC_ERR_INVALID;
+    if (!aligned16(workspace) || !aligned16(d_count)) return GC_ERR_ALIGN;
+    if (capacity > 0 && !aligned16(idx)) return GC_ERR_ALIGN;
+    MaskArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!models[w] || (capacity > 0 && !vals[w])) return GC_ERR_INVALID;
+        if (!aligned16(models[w]) || (capacity > 0 && !aligned16(vals[w]))) return GC_ERR_ALIGN;
+        a.models.p[w] = models[w];
+        a.vals.p[w] = capacity > 0 ? vals[w] : nullptr;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        if (cudaMemsetAsync(d_count, 0, sizeof(uint64_t), s) != cudaSuccess) return GC_ERR_CUDA;
+        return GC_OK;
+    }
+    a.n = n;
+    a.seed_t = seed_t;
+    a.thr = static_cast<uint32_t>(ceil(p * 16777216.0));
+    a.W = W;
+    a.idx = idx;
+    a.capacity = capacity;
+    a.d_count = d_count;
+    a.counter = static_cast<unsigned long long*>(workspace);
+    a.state = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + kWsHeader);
+    a.ntiles = mask_tiles(n);
+    a.d_status = d_status;
+    if (cudaMemsetAsync(workspace, 0, saps_workspace_bytes(n), s) != cudaSuccess) return GC_ERR_CUDA;
+    k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles), kThreads, 0, s>>>(a);
+    return launch_status();
+}
+
+int saps_peer_average(float* const* models, const float* const* vals, const uint32_t* idx,
+                      const uint64_t* d_count, const int* pairs, int W, int64_t capacity,
+                      gc_stream_t stream) {
+    if (W < 2 || W > GC_MAX_WORKERS || (W & 1) || capacity < 0) return GC_ERR_INVALID;
+    if (!models || !pairs || !d_count) return GC_ERR_INVALID;
+    if (capacity == 0) return GC_OK;
+    if (!vals || !idx) return GC_ERR_INVALID;
+    AvgArgs a;
+    bool seen[GC_MAX_WORKERS] = {false};
+    for (int w = 0; w < W; ++w) {
+        const int q = pairs[w];
+        if (q < 0 || q >= W || seen[q]) return GC_ERR_INVALID;
+        seen[q] = true;
+        a.pairs[w] = q;
+        if (!models[w] || !vals[w]) return GC_ERR_INVALID;
+        if (!aligned16(models[w]) || !aligned16(vals[w])) return GC_ERR_ALIGN;
+        a.models.p[w] = models[w];
+        a.vals.p[w] = vals[w];
+    }
+    if (!aligned16(idx)) return GC_ERR_ALIGN;
+    a.W = W;
+    a.idx = idx;
+    a.d_count = d_count;
+    a.capacity = capacity;
+    int grid = grid_for(4);
+    if (grid <= 0) return GC_ERR_CUDA;
+    const int64_t need = (capacity + kThreads - 1) / kThreads;
+    if (need < grid) grid = static_cast<int>(need);
+    k_saps_peer_average<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return launch_status();
+}
+
+int easgd_step(float* const* models, int W, int64_t n, float alpha, float beta, float* center,
+               gc_stream_t stream) {
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !isfinite(alpha) || !isfinite(beta)) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!models || !center) return GC_ERR_INVALID;
+    EasgdArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!models[w]) return GC_ERR_INVALID;
+        if (!aligned16(models[w])) return GC_ERR_ALIGN;
+        a.models.p[w] = models[w];
+    }
+    if (!aligned16(center)) return GC_ERR_ALIGN;
+    a.W = W;
+    a.n = n;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.inv_w = static_cast<float>(1.0 / W);
+    a.center = center;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(W <= 16 ? 2 : 4);
+    if (grid <= 0) return GC_ERR_CUDA;
+    if (W <= 4)
+        k_easgd<4><<<grid, kThreads, 0, s>>>(a);
+    else if (W <= 16)
+        k_easgd<16><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_easgd_wide<<<grid, kThreads, 0, s>>>(a);
+    return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,479 @@
+// twobit.cu -- 2-bit threshold quantisation with error feedback, its fused
+// dequantise-sum + update, and the CD-SGD full-precision correction step.
+//
+// Sources: "2bit gradient compression" (MXNet PR #8662), sections "Two bit
+// quantization", "Format of compressed gradient", "Local kvstore", "Dist
+// kvstore"; "CD-SGD: Distributed Stochastic Gradient Descent with Compression
+// and Delay Compensation", eq. 1, eq. 10, Algorithm 1, section 3.1; EASGD
+// local update from the IMerge design notes.
+//
+// Layout in HBM: every buffer is a flat contiguous array.  A warp owns a
+// "tile" of 512 consecutive elements = 32 packed code words; lane l reads the
+// 16-byte vectors at tile offsets 4l, 128+4l, 256+4l, 384+4l, so every load
+// and store instruction of the warp covers 512 contiguous bytes.
+#include "gc_common.cuh"
+
+namespace gc {
+namespace {
+
+constexpr int kTile = 512;            // elements per warp tile
+constexpr int kWordsPerTile = kTile / 16;
+
+// One element of the threshold rule; returns the 2-bit code and updates r.
+// r + g, r - t and r + t are single fp32 round-to-nearest operations.
+__device__ __forceinline__ uint32_t quantize1(float& r, float g, float t) {
+    const float x = __fadd_rn(r, g);
+    const bool pos = x >= t;
+    const bool neg = x <= -t;
+    r = pos ? __fsub_rn(x, t) : (neg ? __fadd_rn(x, t) : x);
+    return pos ? 3u : (neg ? 2u : 0u);
+}
+
+// 4 consecutive elements -> 8 code bits, first element in the top two bits.
+__device__ __forceinline__ uint32_t quantize4(float4& r, const float4 g, float t) {
+    uint32_t c = quantize1(r.x, g.x, t) << 6;
+    c |= quantize1(r.y, g.y, t) << 4;
+    c |= quantize1(r.z, g.z, t) << 2;
+    c |= quantize1(r.w, g.w, t);
+    return c;
+}
+
+// Byte address (within the code buffer) of the 8 code bits of elements
+// e0..e0+3, e0 a multiple of 4: word e0/16 holds them in byte 3 - (e0/4)%4
+// of its little-endian representation (first element in the MSBs).
+__device__ __forceinline__ int64_t code_byte(int64_t e0) {
+    return 4 * (e0 >> 4) + (3 - ((e0 >> 2) & 3));
+}
+
+// Tail: elements [tile_base, n) of the last, partial tile, one warp.
+template <typename LoadG>
+__device__ void quantize_tail(LoadG loadg, float* __restrict__ r, uint8_t* __restrict__ cb,
+                              int64_t tile_base, int64_t n, float t, int lane) {
+    const int64_t nwords = (n + 15) >> 4;
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+        const int64_t e0 = tile_base + 128 * j + 4 * lane;
+        uint32_t c = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t e = e0 + k;
+            if (e < n) {
+                float rr = r[e];
+                c |= quantize1(rr, loadg(e), t) << (6 - 2 * k);
+                r[e] = rr;
+            }
+        }
+        if ((e0 >> 4) < nwords) cb[code_byte(e0)] = static_cast<uint8_t>(c);
+    }
+}
+
+// K1, fp32 gradients.
+__global__ void __launch_bounds__(kThreads, 4)
+k_2bit_quantize_f32(const float* __restrict__ g, float* __restrict__ r,
+                    uint32_t* __restrict__ codes, int64_t n, float t) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = n / kTile;
+    uint8_t* cb = reinterpret_cast<uint8_t*>(codes);
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const int64_t base = tile * kTile + 4 * lane;
+        float4 gv[4], rv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            gv[j] = ld_stream_f4(g + base + 128 * j);
+            rv[j] = ld_f4(r + base + 128 * j);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t c = quantize4(rv[j], gv[j], t);
+            st_stream_f4(r + base + 128 * j, rv[j]);
+            cb[code_byte(base + 128 * j)] = static_cast<uint8_t>(c);
+        }
+    }
+    if (n % kTile != 0 && warp == ntiles % nwarps)
+        quantize_tail([g](int64_t e) { return g[e]; }, r, cb, ntiles * kTile, n, t, lane);
+}
+
+// K1, bf16 gradients: lane l of round j reads 8 bf16 (16 bytes) at tile
+// offset 256j + 8l, i.e. two code bytes = one 16-bit half of a word.
+__global__ void __launch_bounds__(kThreads, 4)
+k_2bit_quantize_bf16(const uint16_t* __restrict__ g, float* __restrict__ r,
+                     uint32_t* __restrict__ codes, int64_t n, float t) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = n / kTile;
+    uint16_t* ch = reinterpret_cast<uint16_t*>(codes);
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const int64_t base = tile * kTile + 8 * lane;
+        uint4 gv[2];
+        float4 rv[4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            gv[j] = ld_stream_u4(g + base + 256 * j);
+            rv[2 * j] = ld_f4(r + base + 256 * j);
+            rv[2 * j + 1] = ld_f4(r + base + 256 * j + 4);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float4 g0 = make_float4(bf16lo(gv[j].x), bf16hi(gv[j].x),
+                                          bf16lo(gv[j].y), bf16hi(gv[j].y));
+            const float4 g1 = make_float4(bf16lo(gv[j].z), bf16hi(gv[j].z),
+                                          bf16lo(gv[j].w), bf16hi(gv[j].w));
+            const uint32_t c = (quantize4(rv[2 * j], g0, t) << 8) | quantize4(rv[2 * j + 1], g1, t);
+            st_stream_f4(r + base + 256 * j, rv[2 * j]);
+            st_stream_f4(r + base + 256 * j + 4, rv[2 * j + 1]);
+            // elements e..e+7 (e = 8 mod 16 or 0 mod 16) are the high half of
+            // word e/16 when e % 16 == 0, its low half otherwise
+            const int64_t e = base + 256 * j;
+            ch[2 * (e >> 4) + 1 - ((e >> 3) & 1)] = static_cast<uint16_t>(c);
+        }
+    }
+    if (n % kTile != 0 && warp == ntiles % nwarps)
+        quantize_tail([g](int64_t e) { return __uint_as_float(static_cast<uint32_t>(g[e]) << 16); },
+                      r, reinterpret_cast<uint8_t*>(codes), ntiles * kTile, n, t, lane);
+}
+
+// ------------------------------------------------------------------ K2
+
+// Maps a code word to per-field (value + 1): 11 -> 2, 10 -> 0, 00/01 -> 1.
+__device__ __forceinline__ uint32_t plus_one_fields(uint32_t c) {
+    const uint32_t h = c >> 1;
+    const uint32_t two = h & c & 0x55555555u;    // code 11
+    const uint32_t one = ~h & 0x55555555u;       // code 0x
+    return (two << 1) | one;
+}
+
+// Bytes (value+1 sums) for the four elements 4a..4a+3 of a word, from the
+// four byte-lane accumulators (see k_2bit_dqsum).  Byte b of the result is
+// element 4a+b.
+template <int A>
+__device__ __forceinline__ uint32_t pack_quad(uint32_t B0, uint32_t B1, uint32_t B2, uint32_t B3) {
+    constexpr uint32_t sel = (3 - A) | ((7 - A) << 4);
+    const uint32_t t1 = __byte_perm(B3, B1, sel);   // elements 4a, 4a+1
+    const uint32_t t2 = __byte_perm(B2, B0, sel);   // elements 4a+2, 4a+3
+    return __byte_perm(t1, t2, 0x5410);
+}
+
+struct DqArgs {
+    PtrTable<const uint32_t*> codes;
+    int W;
+    int64_t n;
+    float k_out;      // threshold / W                (NONE)
+    float k_lr;       // lr * threshold / W           (SGD, EASGD)
+    float alpha;      // EASGD
+    const float* center;
+    float* weights;
+    float* out;
+};
+
+template <int KIND>
+__device__ __forceinline__ void dq_apply(const DqArgs& a, int64_t e0, uint32_t R, bool full) {
+    const float bias = 8388608.0f + static_cast<float>(a.W);
+    float cnt[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        cnt[b] = __uint_as_float(__byte_perm(R, 0x4B000000u, 0x7540u | b)) - bias;
+    if (full) {
+        if (KIND == GC_UPD_NONE) {
+            st_stream_f4(a.out + e0, make_float4(cnt[0] * a.k_out, cnt[1] * a.k_out,
+                                                 cnt[2] * a.k_out, cnt[3] * a.k_out));
+        } else {
+            float4 w = ld_f4(a.weights + e0);
+            float4 nw;
+            nw.x = fmaf(-cnt[0], a.k_lr, w.x);
+            nw.y = fmaf(-cnt[1], a.k_lr, w.y);
+            nw.z = fmaf(-cnt[2], a.k_lr, w.z);
+            nw.w = fmaf(-cnt[3], a.k_lr, w.w);
+            if (KIND == GC_UPD_EASGD) {
+                const float4 c = ld_stream_f4(a.center + e0);
+                nw.x = fmaf(-a.alpha, w.x - c.x, nw.x);
+                nw.y = fmaf(-a.alpha, w.y - c.y, nw.y);
+                nw.z = fmaf(-a.alpha, w.z - c.z, nw.z);
+                nw.w = fmaf(-a.alpha, w.w - c.w, nw.w);
+            }
+            st_stream_f4(a.weights + e0, nw);
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int64_t e = e0 + b;
+            if (e >= a.n) break;
+            if (KIND == GC_UPD_NONE) {
+                a.out[e] = cnt[b] * a.k_out;
+            } else {
+                const float w = a.weights[e];
+                float nw = fmaf(-cnt[b], a.k_lr, w);
+                if (KIND == GC_UPD_EASGD) nw = fmaf(-a.alpha, w - a.center[e], nw);
+                a.weights[e] = nw;
+            }
+        }
+    }
+}
+
+// K2: one warp per 512-element tile.  Lane m loads word m of the tile from
+// every worker (128 contiguous bytes per worker) and sums, in SWAR form, the
+// per-element (decoded value + 1) over the workers: 4-bit fields for up to 7
+// workers at a time, then 8-bit fields (sums <= 2 * 64 fit a byte).  The
+// per-element sums are regrouped through shared memory so that lane l then
+// owns elements 128j + 4l .. +3 of the tile, matching the coalesced float4
+// layout of the weights.
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 4)
+k_2bit_dqsum(const DqArgs a) {
+    __shared__ uint4 stage[kWarpsPerBlock][32];
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nwords = (a.n + 15) >> 4;
+    const int64_t ntiles = (a.n + kTile - 1) / kTile;
+    const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(&stage[wib][0]);
+
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const int64_t word = tile * kWordsPerTile + lane;
+        const bool have_word = word < nwords;
+        uint32_t B0 = 0, B1 = 0, B2 = 0, B3 = 0;
+        for (int w0 = 0; w0 < a.W; w0 += 7) {
+            uint32_t cw[7];
+#pragma unroll
+            for (int k = 0; k < 7; ++k)
+                cw[k] = (w0 + k < a.W && have_word) ? __ldg(a.codes.p[w0 + k] + word) : 0u;
+            uint32_t A0 = 0, A1 = 0;
+#pragma unroll
+            for (int k = 0; k < 7; ++k) {
+                if (w0 + k < a.W) {
+                    const uint32_t m = plus_one_fields(cw[k]);
+                    A0 += m & 0x33333333u;
+                    A1 += (m >> 2) & 0x33333333u;
+                }
+            }
+            B0 += A0 & 0x0F0F0F0Fu;
+            B1 += (A0 >> 4) & 0x0F0F0F0Fu;
+            B2 += A1 & 0x0F0F0F0Fu;
+            B3 += (A1 >> 4) & 0x0F0F0F0Fu;
+        }
+        stage[wib][lane] = make_uint4(pack_quad<0>(B0, B1, B2, B3), pack_quad<1>(B0, B1, B2, B3),
+                                      pack_quad<2>(B0, B1, B2, B3), pack_quad<3>(B0, B1, B2, B3));
+        __syncwarp();
+        const bool full = (tile + 1) * kTile <= a.n;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t e0 = tile * kTile + 128 * j + 4 * lane;
+            const uint32_t R = stage32[32 * j + lane];
+            if (full || e0 < a.n) dq_apply<KIND>(a, e0, R, full);
+        }
+        __syncwarp();
+    }
+}
+
+// ------------------------------------------------------------------ K3
+
+struct CompArgs {
+    PtrTable<const void*> grads;
+    PtrTable<float*> res;
+    int W;
+    int64_t n;
+    float k_lr;     // lr / W
+    float* weights;
+};
+
+// 8 consecutive gradient values of worker w starting at e (full vectors).
+template <bool BF16>
+__device__ __forceinline__ void load_grad8(const void* g, int64_t e, float (&v)[8]) {
+    if (BF16) {
+        const uint4 u = ld_stream_u4(static_cast<const uint16_t*>(g) + e);
+        v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+        v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+    } else {
+        const float* gf = static_cast<const float*>(g) + e;
+        const float4 a = ld_stream_f4(gf), b = ld_stream_f4(gf + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load_grad1(const void* g, int64_t e) {
+    if (BF16) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(g)[e]) << 16);
+    return static_cast<const float*>(g)[e];
+}
+
+// K3: lane l owns 8 consecutive elements (one 16-byte bf16 vector, or two
+// fp32 vectors) per 256-element warp tile; for every worker it forms
+// m = r + g in fp32, adds it to the running sum in worker order, and writes
+// the residual back as zero.  The weights get w -= (lr/W) * sum.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 2)
+k_compensated(const CompArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t ntiles = a.n / 256;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const int64_t e = tile * 256 + 8 * lane;
+        const float4 w0 = ld_f4(a.weights + e), w1 = ld_f4(a.weights + e + 4);
+        float s[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s[k] = 0.0f;
+        for (int q0 = 0; q0 < a.W; q0 += 4) {
+            float gv[4][8];
+            float4 r0[4], r1[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (q0 + q < a.W) {
+                    load_grad8<BF16>(a.grads.p[q0 + q], e, gv[q]);
+                    r0[q] = ld_f4(a.res.p[q0 + q] + e);
+                    r1[q] = ld_f4(a.res.p[q0 + q] + e + 4);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (q0 + q < a.W) {
+                    s[0] = __fadd_rn(s[0], __fadd_rn(r0[q].x, gv[q][0]));
+                    s[1] = __fadd_rn(s[1], __fadd_rn(r0[q].y, gv[q][1]));
+                    s[2] = __fadd_rn(s[2], __fadd_rn(r0[q].z, gv[q][2]));
+                    s[3] = __fadd_rn(s[3], __fadd_rn(r0[q].w, gv[q][3]));
+                    s[4] = __fadd_rn(s[4], __fadd_rn(r1[q].x, gv[q][4]));
+                    s[5] = __fadd_rn(s[5], __fadd_rn(r1[q].y, gv[q][5]));
+                    s[6] = __fadd_rn(s[6], __fadd_rn(r1[q].z, gv[q][6]));
+                    s[7] = __fadd_rn(s[7], __fadd_rn(r1[q].w, gv[q][7]));
+                    st_stream_f4(a.res.p[q0 + q] + e, zero);
+                    st_stream_f4(a.res.p[q0 + q] + e + 4, zero);
+                }
+            }
+        }
+        st_stream_f4(a.weights + e, make_float4(fmaf(-s[0], a.k_lr, w0.x), fmaf(-s[1], a.k_lr, w0.y),
+                                                fmaf(-s[2], a.k_lr, w0.z), fmaf(-s[3], a.k_lr, w0.w)));
+        st_stream_f4(a.weights + e + 4, make_float4(fmaf(-s[4], a.k_lr, w1.x), fmaf(-s[5], a.k_lr, w1.y),
+                                                    fmaf(-s[6], a.k_lr, w1.z), fmaf(-s[7], a.k_lr, w1.w)));
+    }
+    // tail: elements [ntiles*256, n), spread over the first warps' lanes
+    const int64_t tail0 = ntiles * 256;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (gtid < a.n - tail0) {
+        const int64_t i = tail0 + gtid;
+        float s = 0.0f;
+        for (int q = 0; q < a.W; ++q) {
+            s = __fadd_rn(s, __fadd_rn(a.res.p[q][i], load_grad1<BF16>(a.grads.p[q], i)));
+            a.res.p[q][i] = 0.0f;
+        }
+        a.weights[i] = fmaf(-s, a.k_lr, a.weights[i]);
+    }
+}
+
+}  // namespace
+}  // namespace gc
+
+using namespace gc;
+
+extern "C" {
+
+const char* gc_status_string(int status) {
+    switch (status) {
+        case GC_OK: return "GC_OK";
+        case GC_ERR_INVALID: return "GC_ERR_INVALID: invalid argument";
+        case GC_ERR_ALIGN: return "GC_ERR_ALIGN: data pointer not 16-byte aligned";
+        case GC_ERR_CUDA: return "GC_ERR_CUDA: CUDA launch or runtime error";
+        case GC_ERR_CAPACITY: return "GC_ERR_CAPACITY: more masked entries than capacity";
+        case GC_ERR_TIMEOUT: return "GC_ERR_TIMEOUT: bounded device wait ran out";
+        default: return "unknown status";
+    }
+}
+
+int gc_version(void) { return (1 << 16) | 0; }
+
+int gc_2bit_quantize(const void* grad, gc_dtype dtype, float* residual, uint32_t* codes,
+                     int64_t n, float threshold, gc_stream_t stream) {
+    if (n < 0 || !finite_pos(threshold) || (dtype != GC_F32 && dtype != GC_BF16)) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grad || !residual || !codes) return GC_ERR_INVALID;
+    if (!aligned16(grad) || !aligned16(residual) || !aligned16(codes)) return GC_ERR_ALIGN;
+    const int grid = grid_for(4);
+    if (grid <= 0) return GC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == GC_F32)
+        k_2bit_quantize_f32<<<grid, kThreads, 0, s>>>(static_cast<const float*>(grad), residual,
+                                                      codes, n, threshold);
+    else
+        k_2bit_quantize_bf16<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(grad), residual,
+                                                       codes, n, threshold);
+    return launch_status();
+}
+
+int gc_2bit_dequant_sum_update(const uint32_t* const* codes, int W, int64_t n, float threshold,
+                               gc_update kind, float lr, float alpha, const float* center,
+                               float* weights, float* out, gc_stream_t stream) {
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !finite_pos(threshold)) return GC_ERR_INVALID;
+    if (kind != GC_UPD_NONE && kind != GC_UPD_SGD && kind != GC_UPD_EASGD) return GC_ERR_INVALID;
+    if (!isfinite(lr) || !isfinite(alpha)) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!codes) return GC_ERR_INVALID;
+    DqArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!codes[w]) return GC_ERR_INVALID;
+        if (!aligned16(codes[w])) return GC_ERR_ALIGN;
+        a.codes.p[w] = codes[w];
+    }
+    if (kind == GC_UPD_NONE) {
+        if (!out) return GC_ERR_INVALID;
+        if (!aligned16(out)) return GC_ERR_ALIGN;
+    } else {
+        if (!weights) return GC_ERR_INVALID;
+        if (!aligned16(weights)) return GC_ERR_ALIGN;
+        if (kind == GC_UPD_EASGD) {
+            if (!center) return GC_ERR_INVALID;
+            if (!aligned16(center)) return GC_ERR_ALIGN;
+        }
+    }
+    a.W = W;
+    a.n = n;
+    a.k_out = static_cast<float>(static_cast<double>(threshold) / W);
+    a.k_lr = static_cast<float>(static_cast<double>(lr) * threshold / W);
+    a.alpha = alpha;
+    a.center = center;
+    a.weights = weights;
+    a.out = out;
+    const int grid = grid_for(4);
+    if (grid <= 0) return GC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (kind) {
+        case GC_UPD_NONE: k_2bit_dqsum<GC_UPD_NONE><<<grid, kThreads, 0, s>>>(a); break;
+        case GC_UPD_SGD: k_2bit_dqsum<GC_UPD_SGD><<<grid, kThreads, 0, s>>>(a); break;
+        default: k_2bit_dqsum<GC_UPD_EASGD><<<grid, kThreads, 0, s>>>(a); break;
+    }
+    return launch_status();
+}
+
+int gc_compensated_sum_update(const void* const* grads, gc_dtype dtype, float* const* residuals,
+                              int W, int64_t n, float lr, float* weights, gc_stream_t stream) {
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !isfinite(lr)) return GC_ERR_INVALID;
+    if (dtype != GC_F32 && dtype != GC_BF16) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grads || !residuals || !weights) return GC_ERR_INVALID;
+    CompArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!grads[w] || !residuals[w]) return GC_ERR_INVALID;
+        if (!aligned16(grads[w]) || !aligned16(residuals[w])) return GC_ERR_ALIGN;
+        a.grads.p[w] = grads[w];
+        a.res.p[w] = residuals[w];
+    }
+    if (!aligned16(weights)) return GC_ERR_ALIGN;
+    a.W = W;
+    a.n = n;
+    a.k_lr = static_cast<float>(static_cast<double>(lr) / W);
+    a.weights = weights;
+    // the grid must also cover the < 256 tail elements with one thread each
+    int grid = grid_for(2);
+    if (grid <= 0) return GC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == GC_BF16)
+        k_compensated<true><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_compensated<false><<<grid, kThreads, 0, s>>>(a);
+    return launch_status();
+}
+
+}  // extern "C"

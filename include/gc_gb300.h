@@ -1,0 +1,294 @@
+/*
+ * gc_gb300.h -- C ABI of the GB300 (sm_103a) gradient-compression library
+ * (libgc_gb300.so).
+ *
+ * Gradient compression with error feedback for data-parallel SGD, with the
+ * W data-parallel workers held as separate buffers on one GPU:
+ *   - MXNet-style 2-bit threshold quantisation with a residual, its
+ *     dequantise-sum fused with an SGD or EASGD update, and CD-SGD's periodic
+ *     full-precision correction step;
+ *   - QSGD bucketed stochastic quantisation to 4- or 8-bit sign-magnitude
+ *     codes, and its dequantise-sum;
+ *   - SAPS seeded random-mask sparsification compacted to (index, value)
+ *     pairs, peer averaging over a random perfect matching, and the EASGD
+ *     elastic step.
+ *
+ * Conventions shared by every entry point
+ *   Ownership   The caller allocates and owns every buffer.  The library
+ *               allocates no memory, holds no state between calls and never
+ *               synchronises the device.
+ *   Execution   Each call validates its arguments on the host, enqueues its
+ *               kernels on `stream` (a cudaStream_t; NULL is the legacy
+ *               default stream) and returns.  Results are valid once the
+ *               stream reaches that point.
+ *   Status      The return value is GC_OK or a negative GC_ERR_* code from
+ *               host validation, or GC_ERR_CUDA when a launch failed.  Errors
+ *               found on the device (compaction capacity, look-back timeout)
+ *               are written to the caller's device int `d_status`.
+ *   Pointers    "device" pointers are CUDA device memory of the current
+ *               device; pointer arrays (const float* const* ...) are HOST
+ *               arrays of device pointers, read during the call only.
+ *               Data pointers must be 16-byte aligned (GC_ERR_ALIGN).
+ *   Sizes       n is an element count; n == 0 is a successful no-op, n < 0
+ *               is GC_ERR_INVALID.  Every n up to 2^40 is accepted
+ *               (64-bit indexing).
+ *   Aliasing    Inputs and outputs of one call must not overlap unless the
+ *               argument is documented as in/out.
+ *   Floating    All kernels are IEEE fp32 with round-to-nearest, no
+ *               flush-to-zero and no fast-math.
+ */
+#ifndef GC_GB300_H
+#define GC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GC_API __attribute__((visibility("default")))
+#else
+#define GC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle, ABI-compatible with cudaStream_t. */
+typedef struct CUstream_st *gc_stream_t;
+
+/* Status codes. */
+enum {
+    GC_OK = 0,
+    GC_ERR_INVALID = -1,  /* bad size, count, parameter or NULL pointer      */
+    GC_ERR_ALIGN = -2,    /* a data pointer is not 16-byte aligned           */
+    GC_ERR_CUDA = -3,     /* a CUDA launch or runtime call failed            */
+    GC_ERR_CAPACITY = -4, /* device: more masked entries than the capacity   */
+    GC_ERR_TIMEOUT = -5   /* device: a bounded wait in the compaction ran out */
+};
+
+/* Gradient element type. */
+typedef enum { GC_F32 = 0, GC_BF16 = 1 } gc_dtype;
+
+/* Update applied after the dequantise-sum. */
+typedef enum { GC_UPD_NONE = 0, GC_UPD_SGD = 1, GC_UPD_EASGD = 2 } gc_update;
+
+#define GC_MAX_WORKERS 64
+
+/* Human-readable name of a status code (static string, never NULL). */
+GC_API const char *gc_status_string(int status);
+
+/* Library ABI version, (major << 16) | minor. */
+GC_API int gc_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* 2-bit threshold quantisation with error feedback                       */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * gc_2bit_quantize -- "2bit gradient compression" (MXNet PR #8662),
+ * sections "Two bit quantization" and "Format of compressed gradient".
+ *
+ * For every element i:  r = residual[i] + grad[i]  (one fp32 add);
+ *   r >= +threshold -> code 11, residual[i] = r - threshold
+ *   r <= -threshold -> code 10, residual[i] = r + threshold
+ *   otherwise       -> code 00, residual[i] = r
+ * Codes are packed 16 per uint32 word, element 16k+j in bits (31-2j, 30-2j)
+ * of word k (first element in the most significant bits); the unused bits of
+ * the last word are zero.
+ *
+ *   grad       device, n elements of type `dtype` (fp32 or bf16), read only
+ *   residual   device fp32 [n], in/out (the error-feedback memory)
+ *   codes      device uint32 [ceil(n/16)], written
+ *   threshold  finite, > 0
+ * Errors: GC_ERR_INVALID (n < 0, threshold not finite and positive, bad
+ * dtype, NULL), GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_quantize(const void *grad, gc_dtype dtype, float *residual,
+                     uint32_t *codes, int64_t n, float threshold,
+                     gc_stream_t stream);
+
+/*
+ * gc_2bit_dequant_sum_update -- MXNet PR #8662 "Local kvstore" / "Dist
+ * kvstore" (the receiver dequantises every worker's codes, 11 -> +t,
+ * 10 -> -t, 00 and 01 -> 0, and sums them); CD-SGD eq. 10 (global update
+ * with the averaged compressed gradients); EASGD local update (IMerge design
+ * notes) with the averaged gradient as g.
+ *
+ *   avg_i = (sum_w dec(codes[w], i)) * threshold / W
+ *   GC_UPD_NONE : out[i] = avg_i                       (weights, center unused)
+ *   GC_UPD_SGD  : weights[i] -= lr * avg_i             (out, center unused)
+ *   GC_UPD_EASGD: weights[i] = weights[i] - lr * avg_i
+ *                              - alpha * (weights[i] - center[i])
+ *
+ *   codes      host array of W device pointers, each uint32 [ceil(n/16)]
+ *   W          1 .. GC_MAX_WORKERS
+ *   center     device fp32 [n] (EASGD only, read), else may be NULL
+ *   weights    device fp32 [n] in/out (SGD, EASGD), else may be NULL
+ *   out        device fp32 [n] written (NONE), else may be NULL
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_dequant_sum_update(const uint32_t *const *codes, int W, int64_t n,
+                               float threshold, gc_update kind, float lr,
+                               float alpha, const float *center,
+                               float *weights, float *out, gc_stream_t stream);
+
+/*
+ * gc_compensated_sum_update -- CD-SGD, Algorithm 1 (the branch taken every
+ * k-th step, where the 32-bit gradient is pushed uncompressed) and section
+ * 3.1 (k-step correction).  Reading: the pushed message is the
+ * residual-compensated gradient, after which the residual is empty:
+ *   m_w = residuals[w][i] + grads[w][i]   (fp32);  residuals[w][i] = 0
+ *   weights[i] -= lr * (sum_w m_w) / W    (CD-SGD eq. 1)
+ * No fp32 message is written to memory.
+ *
+ *   grads      host array of W device pointers, n elements of `dtype`
+ *   residuals  host array of W device pointers, fp32 [n], in/out (zeroed)
+ *   weights    device fp32 [n], in/out
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_compensated_sum_update(const void *const *grads, gc_dtype dtype,
+                              float *const *residuals, int W, int64_t n,
+                              float lr, float *weights, gc_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* QSGD                                                                   */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * qsgd_quantize -- "QSGD: Communication-Efficient SGD via Gradient
+ * Quantization and Encoding", Knowl 1 (operator Q_s), Knowl 2 (norm stored
+ * as fp32, sign and level per coordinate), Knowl 8 (bucketing).
+ *
+ * Per bucket b of `bucket` consecutive elements (the last may be shorter):
+ *   norms[b] = the l2 norm of the bucket, rounded to nearest fp32
+ *   S = s_levels / norms[b]                       (fp32 division)
+ *   per element: a = |v| * S, x = a + u, level = min(floor(x), s_levels)
+ *   with u = (splitmix64(seed_w ^ i) >> 40) * 2^-24, seed_w = seed ^
+ *   ((uint64)worker << 48), i the global element index; a bucket whose norm
+ *   is 0 has level 0 everywhere.  Sign bit = (v < 0), so sgn(0) = +1.
+ * Codes are sign-magnitude:
+ *   1 <= s_levels <= 7  : 4-bit codes (sign in bit 3), two per byte, element
+ *                         2j in the HIGH nibble of byte j; codes has
+ *                         ceil(n/2) bytes, the unused low nibble is 0
+ *   8 <= s_levels <= 127: 8-bit codes (sign in bit 7), codes has n bytes
+ *
+ *   grad       device fp32 [n], read only
+ *   bucket     128, 256, 512, 1024 or 2048
+ *   norms      device fp32 [ceil(n/bucket)], written
+ *   codes      device uint8 [ceil(n/2)] or [n], written
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_quantize(const float *grad, int64_t n, int bucket, int s_levels,
+                  uint64_t seed, int worker, float *norms, uint8_t *codes,
+                  gc_stream_t stream);
+
+/*
+ * qsgd_dequant_sum -- QSGD Knowl 2 (decode the tuple: value = norm * sign *
+ * level / s) and Knowl 3 (sum the K decoded messages; scale = 1/K gives
+ * their average).
+ *   out[i] = scale * sum_w sgn_w(i) * (norms[w][b] / s_levels) * level_w(i),
+ *   summed in fp32 in worker order.
+ *
+ *   codes, norms  host arrays of W device pointers laid out as qsgd_quantize
+ *                 writes them
+ *   out           device fp32 [n], written
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_dequant_sum(const uint8_t *const *codes, const float *const *norms,
+                     int W, int64_t n, int bucket, int s_levels, float scale,
+                     float *out, gc_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* SAPS sparsified gossip + EASGD                                         */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * saps_round_seed -- the shared seed of SAPS round t: splitmix64(base + t).
+ * Host only; "Communication-Efficient Decentralized Learning with
+ * Sparsification and Adaptive Peer Selection", section II-A (the
+ * coordinator sends each round's seed to all workers).
+ */
+GC_API uint64_t saps_round_seed(uint64_t base_seed, uint64_t t);
+
+/*
+ * saps_matching -- the round's single-peer gossip partners (SAPS section
+ * II-C: each worker exchanges with exactly one peer; the gossip matrix is
+ * doubly stochastic).  The pages pick the matching from measured link
+ * bandwidths; here it is a uniformly random perfect matching drawn from the
+ * round seed: a Fisher-Yates shuffle with j = splitmix64(splitmix64(seed_t)
+ * ^ i) mod (i + 1) for i = W-1 .. 1.  Host only.
+ *   pairs_out  host int [W]; pairs are (pairs_out[2q], pairs_out[2q+1])
+ * Errors: GC_ERR_INVALID (W not even, W < 2, W > GC_MAX_WORKERS, NULL).
+ */
+GC_API int saps_matching(uint64_t seed_t, int W, int *pairs_out);
+
+/* Bytes of device workspace saps_mask_compact needs for n elements. */
+GC_API size_t saps_workspace_bytes(int64_t n);
+
+/*
+ * saps_mask_compact -- SAPS section II-B: every worker draws the same
+ * Bernoulli(p) mask from the round's shared seed and sends only the masked
+ * coordinates.  m_i = [ (splitmix64(seed_t ^ i) >> 40) < ceil(p * 2^24) ],
+ * i.e. uniform(seed_t ^ i) < p.  A single-pass prefix sum with decoupled
+ * look-back writes the masked indices in ascending order, and in the same
+ * pass gathers every worker's value at those indices.
+ *
+ *   p          in (0, 1]
+ *   models     host array of W device pointers, fp32 [n], read only
+ *   idx        device uint32 [capacity], written (n must be < 2^32)
+ *   vals       host array of W device pointers, fp32 [capacity], written
+ *   capacity   >= 0 entries available in idx and each vals[w]
+ *   d_count    device uint64, written with the number of masked entries
+ *              (also when it exceeds capacity)
+ *   workspace  device, saps_workspace_bytes(n) bytes, 16-byte aligned; the
+ *              call clears it on `stream` before use
+ *   d_status   device int; set to GC_ERR_CAPACITY when the count exceeds
+ *              capacity (only `capacity` entries are written) and to
+ *              GC_ERR_TIMEOUT if a look-back wait ran out (about one
+ *              second; the output is then invalid).  Never cleared by the
+ *              library: zero it before the first call.
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int saps_mask_compact(int64_t n, double p, uint64_t seed_t,
+                      const float *const *models, int W, uint32_t *idx,
+                      float *const *vals, int64_t capacity, uint64_t *d_count,
+                      void *workspace, size_t workspace_bytes, int *d_status,
+                      gc_stream_t stream);
+
+/*
+ * saps_peer_average -- SAPS Algorithm 2, lines 9-10: each worker receives
+ * its peer's sparsified model and averages it with its own.  For every pair
+ * (a, b) and k < min(*d_count, capacity):
+ *   v = (vals[a][k] + vals[b][k]) * 0.5;  models[a][idx[k]] = models[b][idx[k]] = v
+ *
+ *   models     host array of W device pointers, fp32 [n], in/out
+ *   vals, idx  as written by saps_mask_compact
+ *   d_count    device uint64 written by saps_mask_compact
+ *   pairs      host int [W], a perfect matching of 0..W-1 (saps_matching)
+ * Errors: GC_ERR_INVALID (W odd, pairs not a permutation, NULL),
+ * GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int saps_peer_average(float *const *models, const float *const *vals,
+                      const uint32_t *idx, const uint64_t *d_count,
+                      const int *pairs, int W, int64_t capacity,
+                      gc_stream_t stream);
+
+/*
+ * easgd_step -- EASGD local and global updates (IMerge design notes,
+ * "Interleaved Communication Scheduling"), without a gradient term:
+ *   mean_i = (sum_k models[k][i]) / W                (values before the step)
+ *   models[k][i] = models[k][i] - alpha * (models[k][i] - center[i])
+ *   center[i]    = (1 - beta) * center[i] + beta * mean_i
+ *
+ *   models     host array of W device pointers, fp32 [n], in/out
+ *   center     device fp32 [n], in/out
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int easgd_step(float *const *models, int W, int64_t n, float alpha, float beta,
+               float *center, gc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GC_GB300_H */

@@ -63,9 +63,10 @@ def _load():
             "orc_2bit_dequant_sum_update": (None, [vp, i32, i64, f32, i32, f64, f64, vp, vp, vp]),
             "orc_compensated_sum_update": (None, [vp, i32, vp, i32, i64, f64, vp]),
             "orc_l2norm_fp32": (f32, [vp, i64]),
-            "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, vp, vp]),
+            "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
+            "orc_qsgd_scaled_values": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
             "orc_qsgd_dequant_sum": (None, [vp, vp, i32, i64, i64, i32, f64, vp]),
-            "orc_saps_mask_compact": (i64, [i64, f64, u64, vp, i32, vp, vp, i64]),
+            "orc_saps_mask_compact": (i64, [i64, f64, u64, vp, i32, i64, vp, vp, i64]),
             "orc_saps_matching": (i32, [u64, i32, vp]),
             "orc_saps_peer_average": (None, [vp, vp, vp, i64, vp, i32]),
             "orc_easgd_step": (None, [vp, i32, i64, f64, f64, vp]),
@@ -192,15 +193,26 @@ def qsgd_code_bytes(n: int, s: int) -> int:
     return (n + 1) // 2 if s <= 7 else n
 
 
-def qsgd_quantize(v: np.ndarray, bucket: int, s: int, seed: int, worker: int):
-    """Returns (norms fp32 [ceil(n/bucket)], codes uint8)."""
+def qsgd_quantize(v: np.ndarray, bucket: int, s: int, seed: int, worker: int, i0: int = 0):
+    """Returns (norms fp32 [ceil(n/bucket)], codes uint8).  ``v`` may be a
+    bucket-aligned slice starting at global element index ``i0``."""
     _check(v, np.float32, "v")
     n = v.size
     norms = np.zeros((n + bucket - 1) // bucket, dtype=np.float32)
     codes = np.zeros(qsgd_code_bytes(n, s), dtype=np.uint8)
-    _load().orc_qsgd_quantize(_ptr(v), n, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker,
+    _load().orc_qsgd_quantize(_ptr(v), n, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker, i0,
                               _ptr(norms), _ptr(codes))
     return norms, codes
+
+
+def qsgd_scaled_values(v: np.ndarray, bucket: int, s: int, seed: int, worker: int,
+                       i0: int = 0) -> np.ndarray:
+    """fp32 x = |v| * (s / norm) + u whose floor decides each level (0 in zero buckets)."""
+    _check(v, np.float32, "v")
+    x = np.zeros(v.size, dtype=np.float32)
+    _load().orc_qsgd_scaled_values(_ptr(v), v.size, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker,
+                                   i0, _ptr(x))
+    return x
 
 
 def qsgd_dequant_sum(codes_list, norms_list, n: int, bucket: int, s: int,
@@ -220,8 +232,10 @@ def qsgd_dequant_sum(codes_list, norms_list, n: int, bucket: int, s: int,
 # SAPS + EASGD
 # --------------------------------------------------------------------------
 
-def saps_mask_compact(n: int, p: float, seed_t: int, models, capacity: int | None = None):
-    """Returns (count, idx uint32 [min(count, capacity)], vals list of fp64 arrays)."""
+def saps_mask_compact(n: int, p: float, seed_t: int, models, capacity: int | None = None,
+                      i0: int = 0):
+    """Returns (count, idx uint32 [min(count, capacity)], vals list of fp64 arrays).
+    ``models`` may be a slice of n elements starting at global index ``i0``."""
     W = len(models)
     for m in models:
         _check(m, np.float64, "model", n)
@@ -230,7 +244,7 @@ def saps_mask_compact(n: int, p: float, seed_t: int, models, capacity: int | Non
     idx = np.zeros(max(capacity, 1), dtype=np.uint32)
     vals = [np.zeros(max(capacity, 1), dtype=np.float64) for _ in range(W)]
     K = int(_load().orc_saps_mask_compact(n, float(p), seed_t & 0xFFFFFFFFFFFFFFFF,
-                                          _ptr_array(models), W, _ptr(idx), _ptr_array(vals),
+                                          _ptr_array(models), W, i0, _ptr(idx), _ptr_array(vals),
                                           capacity))
     kept = min(K, capacity)
     return K, idx[:kept].copy(), [v[:kept].copy() for v in vals]

@@ -284,7 +284,9 @@ float orc_l2norm_fp32(const float *v, int64_t len)
  * sgn(0) = +1 and Q_s(0) = 0.  The random choice is made as
  *     level = floor(|v_i| / ||v|| * s + u),   u = uniform(seed_w ^ i)
  * with the worker folded into the seed as seed_w = seed ^ (worker << 48) and
- * i the global element index.  fp32 operation order of the decision:
+ * i the global element index (i0 + local index, so that a bucket-aligned
+ * slice of a long vector can be quantised on its own).  fp32 operation order
+ * of the decision:
  *     S = s / norm,  a = |v_i| * S,  x = a + u,  level = min(floor(x), s)
  * (a NaN x, possible only when s / norm overflows, counts as s).  A bucket
  * with norm 0 gets level 0 everywhere.
@@ -294,7 +296,8 @@ float orc_l2norm_fp32(const float *v, int64_t len)
  * Outputs: norms[ceil(n/d)] (fp32) and codes (ceil(n/2) or n bytes).
  */
 void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
-                       uint64_t seed, int worker, float *norms, uint8_t *codes)
+                       uint64_t seed, int worker, int64_t i0, float *norms,
+                       uint8_t *codes)
 {
     int four_bit = (s <= 7);
     int64_t nbuckets = (n + d - 1) / d;
@@ -312,7 +315,7 @@ void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
             uint32_t level = 0u;
             if (norm > 0.0f) {
                 float a = fabsf(v[i]) * S;
-                float u = (float)orc_uniform(seed_w ^ (uint64_t)i);
+                float u = (float)orc_uniform(seed_w ^ (uint64_t)(i0 + i));
                 float x = a + u;
                 if (x != x || x >= (float)s)
                     level = (uint32_t)s;
@@ -330,6 +333,33 @@ void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
                     codes[i / 2] |= (uint8_t)code;
             } else {
                 codes[i] = (uint8_t)((sign << 7) | level);
+            }
+        }
+    }
+}
+
+/*
+ * The fp32 value x = |v_i| * S + u whose floor decides each level above
+ * (0 where the bucket norm is 0).  Used by the tests to tell a level that
+ * sits on a rounding boundary from a wrong one.
+ */
+void orc_qsgd_scaled_values(const float *v, int64_t n, int64_t d, int s,
+                            uint64_t seed, int worker, int64_t i0, float *x_out)
+{
+    int64_t nbuckets = (n + d - 1) / d;
+    uint64_t seed_w = seed ^ ((uint64_t)(uint32_t)worker << 48);
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        int64_t lo = b * d;
+        int64_t hi = lo + d < n ? lo + d : n;
+        float norm = orc_l2norm_fp32(v + lo, hi - lo);
+        float S = norm > 0.0f ? (float)s / norm : 0.0f;
+        for (int64_t i = lo; i < hi; ++i) {
+            if (norm > 0.0f) {
+                float a = fabsf(v[i]) * S;
+                float u = (float)orc_uniform(seed_w ^ (uint64_t)(i0 + i));
+                x_out[i] = a + u;
+            } else {
+                x_out[i] = 0.0f;
             }
         }
     }
@@ -381,17 +411,19 @@ void orc_qsgd_dequant_sum(const uint8_t *const *codes, const float *const *norms
  * round's shared seed; only masked coordinates are sent, as (index, value)
  * pairs.  Reading: m_i = [uniform(seed_t ^ i) < p].  Indices come out in
  * ascending order; every worker's value at each index is gathered.  Returns
- * the number of masked coordinates; at most `capacity` are written.
+ * the number of masked coordinates; at most `capacity` are written.  The
+ * arrays may be a slice starting at global index i0 (indices are global).
  */
 int64_t orc_saps_mask_compact(int64_t n, double p, uint64_t seed_t,
-                              const double *const *models, int W, uint32_t *idx,
-                              double *const *vals, int64_t capacity)
+                              const double *const *models, int W, int64_t i0,
+                              uint32_t *idx, double *const *vals,
+                              int64_t capacity)
 {
     int64_t K = 0;
     for (int64_t i = 0; i < n; ++i) {
-        if (orc_uniform(seed_t ^ (uint64_t)i) < p) {
+        if (orc_uniform(seed_t ^ (uint64_t)(i0 + i)) < p) {
             if (K < capacity) {
-                idx[K] = (uint32_t)i;
+                idx[K] = (uint32_t)(i0 + i);
                 for (int k = 0; k < W; ++k)
                     vals[k][K] = models[k][i];
             }

@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point the header declares, and its host-side logic (argument validation,
+status strings, round seeds, the random perfect matching) behaves as
+documented.  No kernel is launched here: every call below is rejected by host
+validation before any CUDA call, or is host-only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gradient_compression_sgd_gc_gb300 as gc
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gc_gb300.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^GC_API\s+[a-z0-9_ ]+?\**\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("gc_2bit_quantize", "gc_2bit_dequant_sum_update", "qsgd_quantize",
+                     "qsgd_dequant_sum", "saps_mask_compact", "saps_peer_average",
+                     "gc_compensated_sum_update", "easgd_step", "saps_matching",
+                     "saps_round_seed", "saps_workspace_bytes", "gc_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = gc.load()
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert gc.gc_version() >> 16 == 1
+
+
+def test_library_is_the_in_tree_build():
+    assert os.path.realpath(gc.library_path()).startswith(os.path.realpath(ROOT))
+    assert os.path.exists(gc.library_path())
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5):
+        s = gc.gc_status_string(code)
+        assert s and (code != 0 or s == "GC_OK")
+    assert gc.gc_status_string(12345) == "unknown status"
+
+
+FAKE = 0x10000          # an aligned non-null address; never dereferenced below
+MISALIGNED = 0x10004
+
+
+def _call(name, *args):
+    return getattr(gc.load(), name)(*args)
+
+
+def test_quantize_validation():
+    f = "gc_2bit_quantize"
+    assert _call(f, FAKE, 0, FAKE, FAKE, -1, 0.5, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, 0, FAKE, FAKE, 10, 0.0, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, 0, FAKE, FAKE, 10, -1.0, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, 0, FAKE, FAKE, 10, float("inf"), None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, 0, FAKE, FAKE, 10, float("nan"), None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, 7, FAKE, FAKE, 10, 0.5, None) == gc.GC_ERR_INVALID
+    assert _call(f, None, 0, FAKE, FAKE, 10, 0.5, None) == gc.GC_ERR_INVALID
+    assert _call(f, MISALIGNED, 0, FAKE, FAKE, 10, 0.5, None) == gc.GC_ERR_ALIGN
+    assert _call(f, FAKE, 0, MISALIGNED, FAKE, 10, 0.5, None) == gc.GC_ERR_ALIGN
+    assert _call(f, None, 0, None, None, 0, 0.5, None) == gc.GC_OK     # n == 0: no-op
+
+
+def _ptrs(*addrs):
+    return (ctypes.c_void_p * len(addrs))(*addrs)
+
+
+def test_dequant_validation():
+    f = "gc_2bit_dequant_sum_update"
+    codes = _ptrs(FAKE, FAKE)
+    assert _call(f, codes, 0, 10, 0.5, 0, 0.0, 0.0, None, None, FAKE, None) == gc.GC_ERR_INVALID
+    assert _call(f, codes, 65, 10, 0.5, 0, 0.0, 0.0, None, None, FAKE, None) == gc.GC_ERR_INVALID
+    assert _call(f, codes, 2, 10, 0.5, 3, 0.0, 0.0, None, None, FAKE, None) == gc.GC_ERR_INVALID
+    assert _call(f, codes, 2, 10, 0.5, 0, 0.0, 0.0, None, None, None, None) == gc.GC_ERR_INVALID
+    assert _call(f, codes, 2, 10, 0.5, 1, 0.1, 0.0, None, None, None, None) == gc.GC_ERR_INVALID
+    assert _call(f, codes, 2, 10, 0.5, 2, 0.1, 0.9, None, FAKE, None, None) == gc.GC_ERR_INVALID
+    assert _call(f, _ptrs(FAKE, MISALIGNED), 2, 10, 0.5, 0, 0.0, 0.0, None, None, FAKE,
+                 None) == gc.GC_ERR_ALIGN
+    assert _call(f, _ptrs(FAKE, 0), 2, 10, 0.5, 0, 0.0, 0.0, None, None, FAKE,
+                 None) == gc.GC_ERR_INVALID
+
+
+def test_qsgd_validation():
+    f = "qsgd_quantize"
+    assert _call(f, FAKE, 100, 500, 7, 1, 0, FAKE, FAKE, None) == gc.GC_ERR_INVALID   # bucket
+    assert _call(f, FAKE, 100, 512, 0, 1, 0, FAKE, FAKE, None) == gc.GC_ERR_INVALID   # s
+    assert _call(f, FAKE, 100, 512, 128, 1, 0, FAKE, FAKE, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, 100, 512, 7, 1, -1, FAKE, FAKE, None) == gc.GC_ERR_INVALID  # worker
+    assert _call(f, MISALIGNED, 100, 512, 7, 1, 0, FAKE, FAKE, None) == gc.GC_ERR_ALIGN
+    g = "qsgd_dequant_sum"
+    assert _call(g, _ptrs(FAKE), _ptrs(FAKE), 1, 100, 512, 7, float("nan"), FAKE,
+                 None) == gc.GC_ERR_INVALID
+    assert _call(g, _ptrs(FAKE), _ptrs(FAKE), 0, 100, 512, 7, 1.0, FAKE, None) == gc.GC_ERR_INVALID
+
+
+def test_saps_validation():
+    f = "saps_mask_compact"
+    ws = gc.saps_workspace_bytes(1000)
+    models, vals = _ptrs(FAKE), _ptrs(FAKE)
+    ok = (1000, 0.01, 5, models, 1, FAKE, vals, 100, FAKE, FAKE, ws, FAKE, None)
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return _call(f, *a)
+    assert with_(1, 0.0) == gc.GC_ERR_INVALID
+    assert with_(1, 1.5) == gc.GC_ERR_INVALID
+    assert with_(0, 1 << 33) == gc.GC_ERR_INVALID          # indices are uint32
+    assert with_(10, ws - 1) == gc.GC_ERR_INVALID           # workspace too small
+    assert with_(11, None) == gc.GC_ERR_INVALID             # d_status
+    assert with_(9, MISALIGNED) == gc.GC_ERR_ALIGN          # workspace
+    g = "saps_peer_average"
+    pairs = (ctypes.c_int * 4)(0, 1, 2, 2)                  # not a permutation
+    assert _call(g, _ptrs(FAKE, FAKE, FAKE, FAKE), _ptrs(FAKE, FAKE, FAKE, FAKE), FAKE, FAKE,
+                 pairs, 4, 10, None) == gc.GC_ERR_INVALID
+    assert _call(g, _ptrs(FAKE), _ptrs(FAKE), FAKE, FAKE, (ctypes.c_int * 1)(0), 1, 10,
+                 None) == gc.GC_ERR_INVALID
+    h = "easgd_step"
+    assert _call(h, _ptrs(FAKE), 1, 10, float("inf"), 0.9, FAKE, None) == gc.GC_ERR_INVALID
+    assert _call(h, _ptrs(FAKE), 1, 10, 0.9, 0.9, MISALIGNED, None) == gc.GC_ERR_ALIGN
+
+
+def test_workspace_size_grows_with_n():
+    assert gc.saps_workspace_bytes(0) >= 16
+    assert gc.saps_workspace_bytes(25_557_032) > gc.saps_workspace_bytes(1000)
+
+
+@pytest.mark.parametrize("W", [2, 4, 16, 64])
+def test_matching_agrees_with_oracle(W):
+    for t in range(20):
+        seed_t = gc.saps_round_seed(5, t)
+        assert seed_t == oracle.round_seed(5, t)
+        assert gc.saps_matching(seed_t, W) == oracle.saps_matching(seed_t, W).tolist()
+
+
+def test_matching_rejects_bad_w():
+    for W in (0, 1, 3, 66):
+        with pytest.raises(gc.GcError):
+            gc.saps_matching(1, W)

@@ -1,0 +1,156 @@
+"""GPU parity of the SAPS round through the C ABI: seeded mask + decoupled
+look-back compaction (count, indices and gathered values bit-exact), peer
+averaging over the seeded perfect matching, and the EASGD elastic step
+(floats within rel 1e-5 of the fp64 oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_compression_sgd_gc_gb300 as gc
+from gradient_compression_sgd_gc_gb300 import workloads as wl
+import oracle
+from gpu_helpers import assert_close, check_guard, guarded, host_f32, host_u32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class Compactor:
+    """Device buffers for one saps_mask_compact call."""
+
+    def __init__(self, n, W, capacity):
+        self.n, self.W, self.capacity = n, W, capacity
+        self.idx = guarded(capacity, torch.int32)
+        self.vals = [guarded(capacity, torch.float32) for _ in range(W)]
+        self.count = torch.zeros(2, dtype=torch.int64, device=DEV)
+        self.ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+        self.status = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def run(self, p, seed_t, models):
+        gc.saps_mask_compact(self.n, p, seed_t, models, self.idx[:self.capacity],
+                             [v[:self.capacity] for v in self.vals], self.count[:1], self.ws,
+                             self.status)
+
+    def result(self):
+        torch.cuda.synchronize()
+        K = int(self.count[0].item())
+        kept = min(K, self.capacity)
+        return (K, host_u32(self.idx[:kept]), [host_f32(v[:kept]) for v in self.vals],
+                int(self.status.item()))
+
+
+@pytest.mark.parametrize("n", [1, 100, 4095, 4096, 4097, 3 * 4096 + 5, 1_000_003])
+@pytest.mark.parametrize("p", [0.001, 0.01, 0.5, 1.0])
+def test_mask_compact_parity(n, p):
+    W = 3
+    models = [wl.normal(n, 0.05, 4000 + w, device=DEV) for w in range(W)]
+    seed_t = oracle.round_seed(5, n % 7)
+    comp = Compactor(n, W, n)
+    comp.run(p, seed_t, models)
+    K, idx, vals, status = comp.result()
+    rK, ridx, rvals = oracle.saps_mask_compact(n, p, seed_t, [host_f32(m).astype(np.float64)
+                                                              for m in models])
+    assert status == 0
+    assert K == rK
+    np.testing.assert_array_equal(idx, ridx)
+    for w in range(W):
+        np.testing.assert_array_equal(vals[w].astype(np.float64), rvals[w])
+    check_guard(comp.idx, n)
+    for v in comp.vals:
+        check_guard(v, n)
+
+
+def test_mask_compact_sixteen_workers_and_repeat_calls():
+    n, W = 300_007, 16
+    models = [wl.normal(n, 0.05, 4000 + w, device=DEV) for w in range(W)]
+    comp = Compactor(n, W, 6000)
+    hm = [host_f32(m).astype(np.float64) for m in models]
+    for t in range(3):       # the workspace is reused: every call clears it first
+        seed_t = oracle.round_seed(5, t)
+        comp.run(0.01, seed_t, models)
+        K, idx, vals, status = comp.result()
+        rK, ridx, rvals = oracle.saps_mask_compact(n, 0.01, seed_t, hm)
+        assert status == 0 and K == rK
+        np.testing.assert_array_equal(idx, ridx)
+        for w in range(W):
+            np.testing.assert_array_equal(vals[w].astype(np.float64), rvals[w])
+
+
+def test_capacity_overflow_reports_and_truncates():
+    n, W = 50_000, 2
+    models = [wl.normal(n, 1.0, w, device=DEV) for w in range(W)]
+    comp = Compactor(n, W, 100)
+    comp.run(0.1, 99, models)
+    K, idx, vals, status = comp.result()
+    rK, ridx, _ = oracle.saps_mask_compact(n, 0.1, 99, [host_f32(m).astype(np.float64) for m in models])
+    assert K == rK > 100
+    assert status == gc.GC_ERR_CAPACITY
+    np.testing.assert_array_equal(idx, ridx[:100])
+    check_guard(comp.idx, 100)
+
+
+def test_saps_rounds_chain():
+    """Ten full SAPS rounds on 16 workers (mask, compaction, pair average,
+    elastic step) against the oracle's fp64 chain."""
+    n, W, p, alpha, beta = 200_003, 16, 0.01, 0.9, 0.9
+    cfg = wl.scaled(wl.SAPS_P01, n)
+    models = wl.saps_models(cfg, device=DEV)
+    center = wl.saps_initial_center(models)
+    ref = [host_f32(m).astype(np.float64) for m in models]
+    rc = host_f32(center).astype(np.float64)
+    comp = Compactor(n, W, n)
+    for t in range(10):
+        seed_t = gc.saps_round_seed(cfg.base_seed, t)
+        pairs = gc.saps_matching(seed_t, W)
+        comp.run(p, seed_t, models)
+        gc.saps_peer_average(models, [v[:n] for v in comp.vals], comp.idx[:n], comp.count[:1], pairs)
+        gc.easgd_step(models, alpha, beta, center)
+        rK, ridx, rvals = oracle.saps_mask_compact(n, p, seed_t, ref)
+        assert pairs == oracle.saps_matching(seed_t, W).tolist()
+        oracle.saps_peer_average(ref, rvals, ridx, np.array(pairs, np.int32))
+        oracle.easgd_step(ref, alpha, beta, rc)
+        torch.cuda.synchronize()
+        assert int(comp.count[0].item()) == rK
+        scale = np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc)
+        for w in range(W):
+            assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w} round {t}")
+        assert_close(host_f32(center), rc, scale, what=f"center round {t}")
+        assert int(comp.status.item()) == 0
+
+
+def test_peer_average_is_exact_mean_of_pairs():
+    n, W = 40_000, 4
+    models = [wl.normal(n, 1.0, 10 + w, device=DEV) for w in range(W)]
+    before = [host_f32(m) for m in models]
+    comp = Compactor(n, W, n)
+    seed_t = 1234
+    comp.run(0.2, seed_t, models)
+    pairs = gc.saps_matching(seed_t, W)
+    gc.saps_peer_average(models, [v[:n] for v in comp.vals], comp.idx[:n], comp.count[:1], pairs)
+    K, idx, _, _ = comp.result()
+    mask = np.zeros(n, bool)
+    mask[idx] = True
+    after = [host_f32(m) for m in models]
+    for q in range(W // 2):
+        a, b = pairs[2 * q], pairs[2 * q + 1]
+        mean = ((before[a].astype(np.float64) + before[b]) / 2).astype(np.float32)
+        np.testing.assert_array_equal(after[a][mask], mean[mask])
+        np.testing.assert_array_equal(after[b][mask], mean[mask])
+    for w in range(W):
+        np.testing.assert_array_equal(after[w][~mask], before[w][~mask])
+
+
+@pytest.mark.parametrize("W", [1, 2, 4, 5, 16, 17, 64])
+@pytest.mark.parametrize("n", [1, 3, 4, 1001, 65_539])
+def test_easgd_step_parity(W, n):
+    models = [wl.normal(n, 0.05, 50 + w, device=DEV) for w in range(W)]
+    center = wl.normal(n, 0.05, 7, device=DEV)
+    ref = [host_f32(m).astype(np.float64) for m in models]
+    rc = host_f32(center).astype(np.float64)
+    scale = np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc)
+    gc.easgd_step(models, 0.9, 0.5, center)
+    oracle.easgd_step(ref, 0.9, 0.5, rc)
+    torch.cuda.synchronize()
+    for w in range(W):
+        assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w}")
+    assert_close(host_f32(center), rc, scale, what="center")

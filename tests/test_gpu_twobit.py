@@ -1,0 +1,209 @@
+"""GPU parity of the 2-bit path through the C ABI: quantise + residual (fp32
+and bf16 gradients), dequantise-sum + NONE/SGD/EASGD update, and the CD-SGD
+correction step, element by element against the CPU oracle.
+
+Bar: packed codes and residuals bit-exact; float outputs within the relative
+1e-5 of ``gpu_helpers.assert_close``.  Sizes span one to many warp tiles and
+every ragged tail (n mod 16, n mod 512); buffers carry sentinel tails that must
+survive every call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_compression_sgd_gc_gb300 as gc
+from gradient_compression_sgd_gc_gb300 import workloads as wl
+import oracle
+from gpu_helpers import (assert_close, check_guard, guarded, host_bf16_bits, host_f32, host_u32)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+SIZES = [1, 15, 16, 17, 255, 511, 512, 513, 1031, 3 * 512 + 40, 100_008, 262_147]
+
+
+def _grad_host(g: torch.Tensor) -> np.ndarray:
+    return host_bf16_bits(g) if g.dtype == torch.bfloat16 else host_f32(g)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n", SIZES)
+def test_quantize_bit_exact_over_steps(n, dtype):
+    t = 0.5
+    r = guarded(n, torch.float32)
+    r[:n].zero_()
+    codes = guarded(gc.code_words(n), torch.int32)
+    r_ref = np.zeros(n, np.float32)
+    for step in range(4):
+        g = wl.normal(n, 0.7, seed=100 + step, device=DEV, dtype=dtype)
+        gc.gc_2bit_quantize(g, r[:n], codes[:gc.code_words(n)], t)
+        c_ref = oracle.twobit_quantize(_grad_host(g), r_ref, t)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_u32(codes[:gc.code_words(n)]), c_ref)
+        np.testing.assert_array_equal(host_f32(r[:n]).view(np.uint32), r_ref.view(np.uint32))
+    check_guard(r, n)
+    check_guard(codes, gc.code_words(n))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_many_tiles_per_warp(dtype):
+    """Larger than one tile per resident warp, so the grid-stride loop runs
+    several iterations per warp; ragged tail of 23 elements."""
+    n = 5 * 1024 * 1024 + 23
+    t = 1e-3
+    r = torch.zeros(n, dtype=torch.float32, device=DEV)
+    codes = torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV)
+    r_ref = np.zeros(n, np.float32)
+    for step in range(3):
+        g = wl.normal(n, 5e-4, seed=7 + step, device=DEV, dtype=dtype)
+        gc.gc_2bit_quantize(g, r, codes, t)
+        c_ref = oracle.twobit_quantize(_grad_host(g), r_ref, t)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_u32(codes), c_ref)
+        np.testing.assert_array_equal(host_f32(r).view(np.uint32), r_ref.view(np.uint32))
+
+
+def test_quantize_threshold_ties_and_special_values():
+    t = np.float32(0.25)
+    below = np.nextafter(t, np.float32(0))
+    vals = np.array([t, -t, below, -below, 0.0, -0.0, 2 * t, -2 * t, 1e-30, -1e-30,
+                     3.0, -3.0, 0.125, -0.125, t, -t, 7 * t], np.float32)
+    n = vals.size
+    g = torch.from_numpy(vals).to(DEV)
+    r = torch.zeros(n, device=DEV)
+    codes = torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV)
+    r_ref = np.zeros(n, np.float32)
+    for _ in range(3):
+        gc.gc_2bit_quantize(g, r, codes, float(t))
+        c_ref = oracle.twobit_quantize(vals, r_ref, float(t))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_u32(codes), c_ref)
+        np.testing.assert_array_equal(host_f32(r).view(np.uint32), r_ref.view(np.uint32))
+
+
+def test_printed_example_word_on_gpu():
+    grad = torch.tensor([0.5, 2.0, -1.0, -2.5, 3.0, 1.9, -1.9, -2.0], device=DEV)
+    r = torch.zeros(8, device=DEV)
+    codes = torch.empty(1, dtype=torch.int32, device=DEV)
+    gc.gc_2bit_quantize(grad, r, codes, 2.0)
+    torch.cuda.synchronize()
+    assert int(host_u32(codes)[0]) == 0x32C20000
+
+
+def test_config_twobit_w1_ten_steps():
+    """2-bit, one worker, 2^20 elements, t = 0.5, g ~ N(0,1) seeded by step,
+    10 steps with the residual carried; each step dequantised (W = 1)."""
+    cfg = wl.TWOBIT_W1
+    n = cfg.n
+    r = torch.zeros(n, device=DEV)
+    codes = torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV)
+    out = torch.empty(n, device=DEV)
+    r_ref = np.zeros(n, np.float32)
+    for step in range(cfg.steps):
+        g = wl.twobit_grad(cfg, step, 0, device=DEV)
+        gc.gc_2bit_quantize(g, r, codes, cfg.threshold)
+        gc.gc_2bit_dequant_sum_update([codes], n, cfg.threshold, gc.GC_UPD_NONE, out=out)
+        c_ref = oracle.twobit_quantize(host_f32(g), r_ref, cfg.threshold)
+        o_ref = oracle.twobit_dequant_sum_update([c_ref], n, cfg.threshold, oracle.KIND_NONE)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_u32(codes), c_ref)
+        np.testing.assert_array_equal(host_f32(r).view(np.uint32), r_ref.view(np.uint32))
+        np.testing.assert_array_equal(host_f32(out).astype(np.float64), o_ref)
+
+
+def _random_words(nw, rng):
+    return rng.integers(0, 2 ** 32, nw, dtype=np.uint64).astype(np.uint32)
+
+
+@pytest.mark.parametrize("W", [1, 2, 7, 8, 9, 64])
+@pytest.mark.parametrize("n", [1, 100, 513, 70_001])
+def test_dequant_sum_update_all_kinds(W, n):
+    rng = np.random.default_rng(W * 1000 + n)
+    t, lr, alpha = 2e-3, 0.1, 0.9
+    nw = gc.code_words(n)
+    words = [_random_words(nw, rng) for _ in range(W)]
+    # the tail bits beyond n are zero in any code buffer the quantiser writes
+    if n % 16:
+        for w in words:
+            w[-1] &= np.uint32((0xFFFFFFFF << (32 - 2 * (n % 16))) & 0xFFFFFFFF)
+    dcodes = [torch.from_numpy(w.view(np.int32)).to(DEV) for w in words]
+    w0 = rng.uniform(-0.05, 0.05, n).astype(np.float32)
+    c0 = rng.uniform(-0.05, 0.05, n).astype(np.float32)
+    center = torch.from_numpy(c0).to(DEV)
+    # NONE
+    out = guarded(n, torch.float32)
+    gc.gc_2bit_dequant_sum_update(dcodes, n, t, gc.GC_UPD_NONE, out=out[:n])
+    o_ref = oracle.twobit_dequant_sum_update(words, n, t, oracle.KIND_NONE)
+    torch.cuda.synchronize()
+    assert_close(host_f32(out[:n]), o_ref, np.float32(t), what="dequant NONE")
+    check_guard(out, n)
+    # SGD
+    wt = guarded(n, torch.float32)
+    wt[:n].copy_(torch.from_numpy(w0))
+    gc.gc_2bit_dequant_sum_update(dcodes, n, t, gc.GC_UPD_SGD, lr=lr, weights=wt[:n])
+    w_ref = w0.astype(np.float64)
+    oracle.twobit_dequant_sum_update(words, n, t, oracle.KIND_SGD, lr=lr, weights=w_ref)
+    torch.cuda.synchronize()
+    assert_close(host_f32(wt[:n]), w_ref, np.abs(w0) + lr * t, what="dequant SGD")
+    check_guard(wt, n)
+    # EASGD
+    wt = torch.from_numpy(w0.copy()).to(DEV)
+    gc.gc_2bit_dequant_sum_update(dcodes, n, t, gc.GC_UPD_EASGD, lr=lr, alpha=alpha,
+                                  center=center, weights=wt)
+    w_ref = w0.astype(np.float64)
+    oracle.twobit_dequant_sum_update(words, n, t, oracle.KIND_EASGD, lr=lr, alpha=alpha,
+                                     center=c0.astype(np.float64), weights=w_ref)
+    torch.cuda.synchronize()
+    assert_close(host_f32(wt), w_ref, np.abs(w0) + lr * t + alpha * (np.abs(w0) + np.abs(c0)),
+                 what="dequant EASGD")
+
+
+def test_dequant_lr_zero_leaves_weights_bitwise():
+    n = 10_000
+    rng = np.random.default_rng(3)
+    words = [torch.from_numpy(_random_words(gc.code_words(n), rng).view(np.int32)).to(DEV)
+             for _ in range(4)]
+    w0 = torch.randn(n, device=DEV)
+    w = w0.clone()
+    gc.gc_2bit_dequant_sum_update(words, n, 0.5, gc.GC_UPD_SGD, lr=0.0, weights=w)
+    torch.cuda.synchronize()
+    assert torch.equal(w.view(torch.int32), w0.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n", [1, 255, 256, 257, 100_003])
+def test_cdsgd_chain_k4(n, dtype):
+    """Eight CD-SGD steps with k = 4: compressed steps (quantise every worker,
+    dequantise-sum + SGD) and full-precision correction steps 4 and 8."""
+    W, t, lr, k = 4, 1e-3, 0.01, 4
+    res = [torch.zeros(n, device=DEV) for _ in range(W)]
+    codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    w = wl.uniform(n, 0.05, seed=8, device=DEV)
+    res_ref = [np.zeros(n, np.float32) for _ in range(W)]
+    w_ref = host_f32(w).astype(np.float64)
+    scale = np.abs(w_ref).copy()
+    for step in range(1, 9):
+        grads = [wl.normal(n, 5e-4, 3000 + 10 * step + q, device=DEV, dtype=dtype) for q in range(W)]
+        gh = [_grad_host(g) for g in grads]
+        if step % k:
+            for q in range(W):
+                gc.gc_2bit_quantize(grads[q], res[q], codes[q], t)
+            gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=w)
+            c_ref = [oracle.twobit_quantize(gh[q], res_ref[q], t) for q in range(W)]
+            oracle.twobit_dequant_sum_update(c_ref, n, t, oracle.KIND_SGD, lr=lr, weights=w_ref)
+            scale += lr * t
+            torch.cuda.synchronize()
+            for q in range(W):
+                np.testing.assert_array_equal(host_u32(codes[q]), c_ref[q])
+        else:
+            msg = np.sum([np.abs(res_ref[q].astype(np.float64))
+                          + np.abs(gh[q].astype(np.float32) if dtype == torch.float32
+                                   else (gh[q].astype(np.uint32) << 16).view(np.float32))
+                          for q in range(W)], axis=0)
+            gc.gc_compensated_sum_update(grads, res, lr, w)
+            oracle.compensated_sum_update(gh, res_ref, lr, w_ref)
+            scale += lr * msg / W
+            torch.cuda.synchronize()
+        for q in range(W):
+            np.testing.assert_array_equal(host_f32(res[q]).view(np.uint32), res_ref[q].view(np.uint32))
+        assert_close(host_f32(w), w_ref, scale, what=f"weights step {step}")
