@@ -91,7 +91,9 @@ def test_capacity_overflow_reports_and_truncates():
 
 def test_saps_rounds_chain():
     """Ten full SAPS rounds on 16 workers (mask, compaction, pair average,
-    elastic step) against the oracle's fp64 chain."""
+    elastic step) against the oracle's fp64 chain.  The fp32 chain's rounding
+    errors are bounded by ulps of the largest magnitudes an element has taken
+    in any round, so the tolerance scale is that running maximum."""
     n, W, p, alpha, beta = 200_003, 16, 0.01, 0.9, 0.9
     cfg = wl.scaled(wl.SAPS_P01, n)
     models = wl.saps_models(cfg, device=DEV)
@@ -99,6 +101,7 @@ def test_saps_rounds_chain():
     ref = [host_f32(m).astype(np.float64) for m in models]
     rc = host_f32(center).astype(np.float64)
     comp = Compactor(n, W, n)
+    scale = np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc)
     for t in range(10):
         seed_t = gc.saps_round_seed(cfg.base_seed, t)
         pairs = gc.saps_matching(seed_t, W)
@@ -111,7 +114,7 @@ def test_saps_rounds_chain():
         oracle.easgd_step(ref, alpha, beta, rc)
         torch.cuda.synchronize()
         assert int(comp.count[0].item()) == rK
-        scale = np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc)
+        scale = np.maximum(scale, np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc))
         for w in range(W):
             assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w} round {t}")
         assert_close(host_f32(center), rc, scale, what=f"center round {t}")
