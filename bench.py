@@ -48,6 +48,10 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle timings")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--case", default=None,
+                    help="run one kernel on a profiling-sized case three times and exit "
+                         f"({', '.join(CASES)})")
+    ap.add_argument("--case-n", type=int, default=0, help="elements for --case (0 = default)")
     return ap.parse_args()
 
 
@@ -579,10 +583,89 @@ def reference_arm(args, rank, world, pg):
                     "d2h_bytes_per_step": 0}}
 
 
+# ----------------------------------------------------------------------------- profiling cases
+
+CASES = ("quantize_f32", "quantize_bf16", "dqsum_sgd", "qsgd_quantize_s7", "qsgd_quantize_s127",
+         "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated")
+
+
+def run_case(name: str, n: int):
+    """One kernel on inputs larger than L2 but a few GB at most, launched three
+    times; used as the command under ncu."""
+    import torch
+    import gradient_compression_sgd_gc_gb300 as gc
+    from gradient_compression_sgd_gc_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n = n or (1 << 26)
+    if name in ("quantize_f32", "quantize_bf16"):
+        dt = torch.float32 if name == "quantize_f32" else torch.bfloat16
+        g = wl.normal(n, 1e-3, 1, device=dev, dtype=dt)
+        r = torch.zeros(n, device=dev)
+        c = torch.empty(gc.code_words(n), dtype=torch.int32, device=dev)
+        fn = lambda: gc.gc_2bit_quantize(g, r, c, 2e-3)
+    elif name == "dqsum_sgd":
+        W = 8
+        cs = [torch.randint(-2 ** 31, 2 ** 31 - 1, (gc.code_words(n),), dtype=torch.int32, device=dev)
+              for _ in range(W)]
+        w = torch.zeros(n, device=dev)
+        fn = lambda: gc.gc_2bit_dequant_sum_update(cs, n, 2e-3, gc.GC_UPD_SGD, lr=0.1, weights=w)
+    elif name.startswith("qsgd_quantize"):
+        s = 7 if name.endswith("s7") else 127
+        v = wl.qsgd_grad(wl.scaled(wl.QSGD_S7, n), 0, device=dev)
+        nm = torch.empty(gc.qsgd_num_buckets(n, 512), device=dev)
+        c = torch.empty(gc.qsgd_code_bytes(n, s), dtype=torch.uint8, device=dev)
+        fn = lambda: gc.qsgd_quantize(v, 512, s, 42, 0, nm, c)
+    elif name.startswith("qsgd_dequant"):
+        s = 7 if name.endswith("s7") else 127
+        W = 4
+        nb = gc.qsgd_num_buckets(n, 512)
+        cs = [torch.randint(0, 255, (gc.qsgd_code_bytes(n, s),), dtype=torch.uint8, device=dev)
+              for _ in range(W)]
+        nms = [torch.rand(nb, device=dev) for _ in range(W)]
+        out = torch.empty(n, device=dev)
+        fn = lambda: gc.qsgd_dequant_sum(cs, nms, n, 512, s, 0.25, out)
+    elif name in ("saps_mask", "saps_avg", "easgd"):
+        cfg = wl.scaled(wl.SAPS_P01, n if name != "easgd" else n // 4)
+        models = wl.saps_models(cfg, device=dev)
+        cap = int(cfg.n * cfg.p * 1.2 + 10_000)
+        idx = torch.empty(cap, dtype=torch.int32, device=dev)
+        vals = [torch.empty(cap, device=dev) for _ in range(cfg.workers)]
+        cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+        ws = torch.empty(gc.saps_workspace_bytes(cfg.n), dtype=torch.uint8, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        center = wl.saps_initial_center(models)
+        seed_t = gc.saps_round_seed(5, 0)
+        pairs = gc.saps_matching(seed_t, cfg.workers)
+        gc.saps_mask_compact(cfg.n, cfg.p, seed_t, models, idx, vals, cnt, ws, st)
+        if name == "saps_mask":
+            fn = lambda: gc.saps_mask_compact(cfg.n, cfg.p, seed_t, models, idx, vals, cnt, ws, st)
+        elif name == "saps_avg":
+            fn = lambda: gc.saps_peer_average(models, vals, idx, cnt, pairs)
+        else:
+            fn = lambda: gc.easgd_step(models, 0.9, 0.9, center)
+    elif name == "compensated":
+        W = 4
+        gs = [wl.normal(n, 5e-4, w, device=dev, dtype=torch.bfloat16) for w in range(W)]
+        rs = [torch.zeros(n, device=dev) for _ in range(W)]
+        w = torch.zeros(n, device=dev)
+        fn = lambda: gc.gc_compensated_sum_update(gs, rs, 0.01, w)
+    else:
+        raise SystemExit(f"unknown case {name}; one of {CASES}")
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    print(f"case {name} n={n}: 3 launches done")
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
     args = parse_args()
+    if args.case:
+        run_case(args.case, args.case_n)
+        return
     rank, world, local, pg = dist_setup(args)
     if args.impl == "reference":
         line = reference_arm(args, rank, world, pg)
