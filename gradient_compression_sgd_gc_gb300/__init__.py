@@ -31,12 +31,14 @@ __all__ = [
     "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed",
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
+    "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 GC_F32, GC_BF16 = 0, 1
 GC_UPD_NONE, GC_UPD_SGD, GC_UPD_EASGD = 0, 1, 2
 GC_MAX_WORKERS = 64
+GC_NOALLOC_MAX_N = 1 << 26
 
 _lock = threading.Lock()
 _lib = None
@@ -78,6 +80,7 @@ def load():
             "saps_mask_compact": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz, vp, vp]),
             "saps_peer_average": (i32, [vp, vp, vp, vp, vp, i32, i64, vp]),
             "easgd_step": (i32, [vp, i32, i64, f32, f32, vp, vp]),
+            "saps_mask_compact_noalloc": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -265,3 +268,24 @@ def easgd_step(models, alpha: float, beta: float, center: torch.Tensor, stream=N
     st = lib.easgd_step(_ptrs(models, "models", torch.float32, n), W, n, float(alpha), float(beta),
                         _dev(center, "center", torch.float32, n), _stream(stream, center))
     _check(st, "easgd_step")
+
+
+def saps_mask_compact_noalloc(n: int, p: float, seed_t: int, models, idx: torch.Tensor, vals,
+                              d_count: torch.Tensor, d_status: torch.Tensor, stream=None) -> None:
+    """saps_mask_compact without a workspace, for callers that cannot allocate
+    one: the look-back scratch is a fixed array inside the library, so n is
+    limited to GC_NOALLOC_MAX_N elements, and calls that overlap on the GPU
+    race (order them on one stream).  Arguments as saps_mask_compact."""
+    if n > GC_NOALLOC_MAX_N:
+        raise ValueError(f"saps_mask_compact_noalloc: n = {n} exceeds the fixed scratch limit of "
+                         f"{GC_NOALLOC_MAX_N} elements; use saps_mask_compact with a workspace")
+    lib = load()
+    W = len(models)
+    capacity = idx.numel()
+    st = lib.saps_mask_compact_noalloc(int(n), float(p), int(seed_t) & 0xFFFFFFFFFFFFFFFF,
+                                       _ptrs(models, "models", torch.float32, n), W,
+                                       _dev(idx, "idx", torch.int32),
+                                       _ptrs(vals, "vals", torch.float32, capacity), capacity,
+                                       _dev(d_count, "d_count", torch.int64, 1),
+                                       _dev(d_status, "d_status", torch.int32, 1), _stream(stream, idx))
+    _check(st, "saps_mask_compact_noalloc")

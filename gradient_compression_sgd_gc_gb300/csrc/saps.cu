@@ -437,3 +437,107 @@ int easgd_step(float* const* models, int W, int64_t n, float alpha, float beta, 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// saps_mask_compact_noalloc: the same compaction without a caller workspace.
+//
+// Some callers cannot hand this library a workspace: a plug-in running inside
+// a host framework whose device allocator it may not call, a training loop
+// whose device memory is planned once up front and may not grow, or code that
+// must not risk the implicit device-wide synchronisation that cudaMalloc and
+// cudaFree can cause.  For them the look-back scratch (the tile counter and
+// one state word per tile) lives in a fixed array in device memory that every
+// GPU which loads this library holds until the process exits.
+//
+// The array is shared by every call on a device and keeps the last call's
+// contents; each call clears the part it uses on its own stream before the
+// kernel runs.  Two calls whose work overlaps on the GPU (different streams
+// without ordering between them) race on the array and give wrong results:
+// order them on one stream or with events.
+//
+// Host code cannot use the array's name as a device address (on the host it
+// names a host-side stand-in), so the first call on each device looks the
+// address up with cudaGetSymbolAddress, with that device current, and keeps
+// it for later calls.  Make that first call before any stream capture.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+namespace gc {
+namespace {
+
+constexpr int64_t kNoAllocMaxN = int64_t(1) << 26;                  // 67,108,864 elements
+constexpr int64_t kNoAllocMaxTiles = kNoAllocMaxN / kTileElems;    // 16,384 tiles
+constexpr size_t kNoAllocWords = kWsHeader / sizeof(uint64_t) + kNoAllocMaxTiles;
+constexpr int kMaxDevices = 64;
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+}  // namespace
+
+// 16,392 words = 131,136 bytes of device memory per GPU.
+static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocWords];
+
+namespace {
+
+int noalloc_scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return GC_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return GC_OK;
+}
+
+}  // namespace
+}  // namespace gc
+
+extern "C" int saps_mask_compact_noalloc(int64_t n, double p, uint64_t seed_t,
+                                         const float* const* models, int W, uint32_t* idx,
+                                         float* const* vals, int64_t capacity, uint64_t* d_count,
+                                         int* d_status, gc_stream_t stream) {
+    using namespace gc;
+    if (n < 0 || n > kNoAllocMaxN || W < 1 || W > GC_MAX_WORKERS || capacity < 0) return GC_ERR_INVALID;
+    if (!(p > 0.0 && p <= 1.0)) return GC_ERR_INVALID;
+    if (!d_count || !d_status || !models || (capacity > 0 && (!idx || !vals))) return GC_ERR_INVALID;
+    if (!aligned16(d_count)) return GC_ERR_ALIGN;
+    if (capacity > 0 && !aligned16(idx)) return GC_ERR_ALIGN;
+    MaskArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!models[w] || (capacity > 0 && !vals[w])) return GC_ERR_INVALID;
+        if (!aligned16(models[w]) || (capacity > 0 && !aligned16(vals[w]))) return GC_ERR_ALIGN;
+        a.models.p[w] = models[w];
+        a.vals.p[w] = capacity > 0 ? vals[w] : nullptr;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        if (cudaMemsetAsync(d_count, 0, sizeof(uint64_t), s) != cudaSuccess) return GC_ERR_CUDA;
+        return GC_OK;
+    }
+    void* scratch = nullptr;
+    const int st = noalloc_scratch_address(&scratch);
+    if (st != GC_OK) return st;
+    a.n = n;
+    a.seed_t = seed_t;
+    a.thr = static_cast<uint32_t>(ceil(p * 16777216.0));
+    a.W = W;
+    a.idx = idx;
+    a.capacity = capacity;
+    a.d_count = d_count;
+    a.counter = static_cast<unsigned long long*>(scratch);
+    a.state = reinterpret_cast<uint64_t*>(static_cast<char*>(scratch) + kWsHeader);
+    a.ntiles = mask_tiles(n);
+    a.d_status = d_status;
+    const size_t used = kWsHeader + sizeof(uint64_t) * static_cast<size_t>(a.ntiles);
+    if (cudaMemsetAsync(scratch, 0, used, s) != cudaSuccess) return GC_ERR_CUDA;
+    k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles), kThreads, 0, s>>>(a);
+    return launch_status();
+}

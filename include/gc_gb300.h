@@ -287,6 +287,32 @@ GC_API int saps_peer_average(float *const *models, const float *const *vals,
 GC_API int easgd_step(float *const *models, int W, int64_t n, float alpha, float beta,
                float *center, gc_stream_t stream);
 
+/*
+ * saps_mask_compact_noalloc -- no counterpart on the pages: the same
+ * compaction as saps_mask_compact, for callers that cannot provide or
+ * allocate a workspace (a plug-in inside a host framework whose device
+ * allocator it may not call, a loop whose device memory is fixed up front,
+ * code that must avoid the implicit synchronisation of cudaMalloc/cudaFree).
+ * The look-back scratch is a fixed array in device memory inside the library
+ * (131,136 bytes, held by every GPU that loads the library until exit).  The
+ * call allocates nothing.
+ *
+ *   n          0 .. GC_NOALLOC_MAX_N; larger n returns GC_ERR_INVALID
+ *   other arguments as saps_mask_compact
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the array and
+ * clears the part it uses on `stream`; calls that overlap on the GPU race and
+ * must be ordered (one stream, or events).
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+#define GC_NOALLOC_MAX_N (1LL << 26)
+GC_API int saps_mask_compact_noalloc(int64_t n, double p, uint64_t seed_t,
+                                     const float *const *models, int W,
+                                     uint32_t *idx, float *const *vals,
+                                     int64_t capacity, uint64_t *d_count,
+                                     int *d_status, gc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
