@@ -219,28 +219,24 @@ def headline(args, dev, rank, world, pg):
     res = [torch.zeros(n, device=dev) for _ in range(W)]
     codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=dev) for _ in range(W)]
     weights = wl.twobit_weights(cfg, device=dev)
-    gc.load()
-
-    def step(s, timer=None):
-        g = grads[s % pool]
-        for w in range(W):
-            if timer is None:
-                gc.gc_2bit_quantize(g[w], res[w], codes[w], t, stream=stream)
-            else:
-                timer.around("quantize", lambda w=w: gc.gc_2bit_quantize(g[w], res[w], codes[w], t,
-                                                                         stream=stream))
-        if timer is None:
-            gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights, stream=stream)
-        else:
-            timer.around("dqsum", lambda: gc.gc_2bit_dequant_sum_update(
-                codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights, stream=stream))
+    # validated launches with their arguments prepared once (host cost per
+    # launch ~ a ctypes call), so the GPU queue never runs dry
+    quant = [[gc.gc_2bit_quantize(grads[s][w], res[w], codes[w], t, stream=stream, prepare=True)
+              for w in range(W)] for s in range(pool)]
+    dqsum = gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights,
+                                          stream=stream, prepare=True)
 
     for s in range(args.warmup):
-        step(s)
+        for q in quant[s % pool]:
+            q()
+        dqsum()
     torch.cuda.synchronize(dev)
+    evq = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(W)] for _ in range(args.steps)]
+    evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     clocks = ClockSampler(gpu_id_for(dev)) if rank == 0 else None
     time.sleep(0.15)
-    timer = Timer(stream)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(pg, dev)
@@ -248,7 +244,16 @@ def headline(args, dev, rank, world, pg):
     w0 = time.time()
     start.record(stream)
     for s in range(args.steps):
-        step(args.warmup + s, timer)
+        qs = quant[(args.warmup + s) % pool]
+        for w in range(W):
+            a, b = evq[s][w]
+            a.record(stream)
+            qs[w]()
+            b.record(stream)
+        a, b = evd[s]
+        a.record(stream)
+        dqsum()
+        b.record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     w1 = time.time()
@@ -260,9 +265,9 @@ def headline(args, dev, rank, world, pg):
         time.sleep(0.1)
         clocks.stop()
         clk = clocks.summary(w0, w1)
-    q_ms = timer.ms("quantize")
-    d_ms = timer.ms("dqsum")
-    del grads
+    q_ms = [a.elapsed_time(b) for row in evq for (a, b) in row]
+    d_ms = [a.elapsed_time(b) for (a, b) in evd]
+    del grads, quant
     return {"total_ms": total_ms, "quantize_ms": q_ms, "dqsum_ms": d_ms, "clocks": clk,
             "launches": args.steps * (W + 1), "n": n, "W": W}
 
@@ -270,7 +275,9 @@ def headline(args, dev, rank, world, pg):
 def e2e(args, dev):
     """Same metric through the public API with host buffers: every step copies
     the 8 gradients from pinned host memory, runs the path, and reads the 8
-    packed code buffers back."""
+    packed code buffers back.  Copies run on a second stream so that worker
+    w+1's upload overlaps worker w's quantisation; events order each kernel
+    after its own upload."""
     import torch
     import gradient_compression_sgd_gc_gb300 as gc
     from gradient_compression_sgd_gc_gb300 import workloads as wl
@@ -278,27 +285,43 @@ def e2e(args, dev):
     cfg = wl.TWOBIT_DQ_SGD
     n, W, t, lr = cfg.n, cfg.workers, cfg.threshold, cfg.lr
     stream = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
     host_g = [wl.twobit_grad(cfg, 0, w, device="cpu").pin_memory() for w in range(W)]
     host_c = [torch.empty(gc.code_words(n), dtype=torch.int32).pin_memory() for _ in range(W)]
     dev_g = [torch.empty(n, device=dev) for _ in range(W)]
     res = [torch.zeros(n, device=dev) for _ in range(W)]
     codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=dev) for _ in range(W)]
     weights = wl.twobit_weights(cfg, device=dev)
+    quant = [gc.gc_2bit_quantize(dev_g[w], res[w], codes[w], t, stream=stream, prepare=True)
+             for w in range(W)]
+    dqsum = gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights,
+                                          stream=stream, prepare=True)
+    up = [torch.cuda.Event() for _ in range(W)]
+    used = [torch.cuda.Event() for _ in range(W)]
 
     def step():
         for w in range(W):
-            dev_g[w].copy_(host_g[w], non_blocking=True)
-            gc.gc_2bit_quantize(dev_g[w], res[w], codes[w], t, stream=stream)
-        gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights, stream=stream)
+            copy.wait_event(used[w])          # the previous step's kernel has read dev_g[w]
+            with torch.cuda.stream(copy):
+                dev_g[w].copy_(host_g[w], non_blocking=True)
+            up[w].record(copy)
+        for w in range(W):
+            stream.wait_event(up[w])
+            quant[w]()
+            used[w].record(stream)
+        dqsum()
         for w in range(W):
             host_c[w].copy_(codes[w], non_blocking=True)
 
+    for w in range(W):
+        used[w].record(stream)
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    copy.wait_event(a)                        # no upload of the timed steps starts early
     for _ in range(args.e2e_steps):
         step()
     b.record(stream)
@@ -307,7 +330,8 @@ def e2e(args, dev):
     h2d = W * n * 4
     d2h = W * gc.code_words(n) * 4
     return {"value": round(W * n * 4 / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "h2d_GBps": round(h2d / (ms * 1e-3) / 1e9, 1)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -378,15 +402,16 @@ def rows(args, dev, peak):
     c = torch.empty(gc.code_words(n), dtype=torch.int32, device=dev)
     o = torch.empty(n, device=dev)
     tm = Timer(stream)
+    pq = gc.gc_2bit_quantize(g, r, c, cfg.threshold, stream=stream, prepare=True)
+    pd = gc.gc_2bit_dequant_sum_update([c], n, cfg.threshold, gc.GC_UPD_NONE, out=o, stream=stream,
+                                       prepare=True)
     for i in range(reps + 3):
         flush_l2(flush)
-        tm.around("q" if i >= 3 else "w", lambda: gc.gc_2bit_quantize(g, r, c, cfg.threshold, stream=stream))
+        tm.around("q" if i >= 3 else "w", pq)
         flush_l2(flush)
-        tm.around("d" if i >= 3 else "w", lambda: gc.gc_2bit_dequant_sum_update([c], n, cfg.threshold,
-                                                                                 gc.GC_UPD_NONE, out=o,
-                                                                                 stream=stream))
+        tm.around("d" if i >= 3 else "w", pd)
     for i in range(reps + 3):
-        tm.around("qh" if i >= 3 else "w", lambda: gc.gc_2bit_quantize(g, r, c, cfg.threshold, stream=stream))
+        tm.around("qh" if i >= 3 else "w", pq)
     torch.cuda.synchronize(dev)
     out["twobit_w1.quantize"] = _row("twobit_w1", "gc_2bit_quantize f32 (L2 flushed)", 12.25 * n,
                                      tm.ms("q"), peak, n)
@@ -406,12 +431,13 @@ def rows(args, dev, peak):
         codes = [torch.empty(cb, dtype=torch.uint8, device=dev) for _ in range(W)]
         outq = torch.empty(n, device=dev)
         tm = Timer(stream)
+        pq = [gc.qsgd_quantize(vs[w], qcfg.bucket, s, qcfg.seed, w, norms[w], codes[w], stream=stream,
+                               prepare=True) for w in range(W)]
+        pd = gc.qsgd_dequant_sum(codes, norms, n, qcfg.bucket, s, 1.0 / W, outq, stream=stream, prepare=True)
         for i in range(8):
             for w in range(W):
-                tm.around("q" if i >= 2 else "w", lambda w=w: gc.qsgd_quantize(
-                    vs[w], qcfg.bucket, s, qcfg.seed, w, norms[w], codes[w], stream=stream))
-            tm.around("d" if i >= 2 else "w", lambda: gc.qsgd_dequant_sum(
-                codes, norms, n, qcfg.bucket, s, 1.0 / W, outq, stream=stream))
+                tm.around("q" if i >= 2 else "w", pq[w])
+            tm.around("d" if i >= 2 else "w", pd)
         torch.cuda.synchronize(dev)
         out[f"{qcfg.name}.quantize"] = _row(qcfg.name, "qsgd_quantize", n * 4 + cb + 4 * nb, tm.ms("q"),
                                             peak, n)
@@ -436,10 +462,13 @@ def rows(args, dev, peak):
             seed_t = gc.saps_round_seed(scfg.base_seed, rd)
             pairs = gc.saps_matching(seed_t, W)
             k = "" if rd >= 2 else "w"
-            tm.around("m" + k, lambda: gc.saps_mask_compact(n, scfg.p, seed_t, models, idx, vals, cnt, ws, st,
-                                                            stream=stream))
-            tm.around("a" + k, lambda: gc.saps_peer_average(models, vals, idx, cnt, pairs, stream=stream))
-            tm.around("e" + k, lambda: gc.easgd_step(models, scfg.alpha, scfg.beta, center, stream=stream))
+            pm = gc.saps_mask_compact(n, scfg.p, seed_t, models, idx, vals, cnt, ws, st, stream=stream,
+                                      prepare=True)
+            pa = gc.saps_peer_average(models, vals, idx, cnt, pairs, stream=stream, prepare=True)
+            pe = gc.easgd_step(models, scfg.alpha, scfg.beta, center, stream=stream, prepare=True)
+            tm.around("m" + k, pm)
+            tm.around("a" + k, pa)
+            tm.around("e" + k, pe)
         torch.cuda.synchronize(dev)
         K = int(cnt.item())
         assert int(st.item()) == 0
@@ -465,14 +494,17 @@ def rows(args, dev, peak):
         codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=dev) for _ in range(W)]
         wts = wl.twobit_weights(ccfg, device=dev, seed=8)
         tm = Timer(stream)
+        pq = [gc.gc_2bit_quantize(grads[w], res[w], codes[w], ccfg.threshold, stream=stream, prepare=True)
+              for w in range(W)]
+        pd = gc.gc_2bit_dequant_sum_update(codes, n, ccfg.threshold, gc.GC_UPD_SGD, lr=ccfg.lr, weights=wts,
+                                           stream=stream, prepare=True)
+        pc = gc.gc_compensated_sum_update(grads, res, ccfg.lr, wts, stream=stream, prepare=True)
         for i in range(5):
             k = "" if i >= 1 else "w"
             for w in range(W):
-                tm.around("q" + k, lambda w=w: gc.gc_2bit_quantize(grads[w], res[w], codes[w], ccfg.threshold,
-                                                                    stream=stream))
-            tm.around("d" + k, lambda: gc.gc_2bit_dequant_sum_update(codes, n, ccfg.threshold, gc.GC_UPD_SGD,
-                                                                      lr=ccfg.lr, weights=wts, stream=stream))
-            tm.around("c" + k, lambda: gc.gc_compensated_sum_update(grads, res, ccfg.lr, wts, stream=stream))
+                tm.around("q" + k, pq[w])
+            tm.around("d" + k, pd)
+            tm.around("c" + k, pc)
         torch.cuda.synchronize(dev)
         out["cdsgd.quantize_bf16"] = _row("cdsgd", "gc_2bit_quantize bf16", 10.25 * n, tm.ms("q"), peak, n)
         out["cdsgd.dequant_sum_sgd"] = _row("cdsgd", "gc_2bit_dequant_sum_update SGD W=4", (W * 0.25 + 8) * n,

@@ -31,7 +31,7 @@ __all__ = [
     "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed",
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
-    "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N",
+    "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -124,6 +124,30 @@ def _check(status: int, where: str) -> None:
         raise GcError(status, where)
 
 
+class PreparedCall:
+    """One validated entry-point call with its ctypes arguments already built
+    (device pointers, pointer tables, stream).  Calling it launches again on
+    the same buffers and stream; the buffers must stay alive meanwhile.  Used
+    in hot loops, where re-checking the tensors on every launch would cost more
+    host time than the kernel takes."""
+    __slots__ = ("fn", "args", "where", "keep")
+
+    def __init__(self, fn, args, where, keep=()):
+        self.fn, self.args, self.where, self.keep = fn, args, where, keep
+
+    def __call__(self) -> None:
+        st = self.fn(*self.args)
+        if st != GC_OK:
+            raise GcError(st, self.where)
+
+
+def _invoke(fn, args, where: str, prepare: bool, keep=()):
+    if prepare:
+        return PreparedCall(fn, args, where, keep)
+    _check(fn(*args), where)
+    return None
+
+
 def _gdtype(t: torch.Tensor) -> int:
     if t.dtype == torch.float32:
         return GC_F32
@@ -156,64 +180,65 @@ def gc_version() -> int:
 
 
 def gc_2bit_quantize(grad: torch.Tensor, residual: torch.Tensor, codes: torch.Tensor,
-                     threshold: float, stream=None) -> None:
+                     threshold: float, stream=None, prepare: bool = False):
     n = grad.numel()
     lib = load()
-    st = lib.gc_2bit_quantize(_dev(grad, "grad"), _gdtype(grad), _dev(residual, "residual", torch.float32, n),
-                              _dev(codes, "codes", torch.int32, code_words(n)), n, float(threshold),
-                              _stream(stream, grad))
-    _check(st, "gc_2bit_quantize")
+    args = (_dev(grad, "grad"), _gdtype(grad), _dev(residual, "residual", torch.float32, n),
+            _dev(codes, "codes", torch.int32, code_words(n)), n, float(threshold),
+            _stream(stream, grad))
+    return _invoke(lib.gc_2bit_quantize, args, "gc_2bit_quantize", prepare, (grad, residual, codes))
 
 
 def gc_2bit_dequant_sum_update(codes, n: int, threshold: float, kind: int = GC_UPD_NONE,
                                lr: float = 0.0, alpha: float = 0.0, center=None, weights=None,
-                               out=None, stream=None) -> None:
+                               out=None, stream=None, prepare: bool = False):
     """codes: list of W int32 tensors (the packed uint32 words)."""
     lib = load()
     W = len(codes)
     arr = _ptrs(codes, "codes", torch.int32, code_words(n))
-    st = lib.gc_2bit_dequant_sum_update(
-        arr, W, n, float(threshold), int(kind), float(lr), float(alpha),
-        _dev(center, "center", torch.float32, n) if center is not None else None,
-        _dev(weights, "weights", torch.float32, n) if weights is not None else None,
-        _dev(out, "out", torch.float32, n) if out is not None else None,
-        _stream(stream, codes[0] if W else None))
-    _check(st, "gc_2bit_dequant_sum_update")
+    args = (arr, W, n, float(threshold), int(kind), float(lr), float(alpha),
+            _dev(center, "center", torch.float32, n) if center is not None else None,
+            _dev(weights, "weights", torch.float32, n) if weights is not None else None,
+            _dev(out, "out", torch.float32, n) if out is not None else None,
+            _stream(stream, codes[0] if W else None))
+    return _invoke(lib.gc_2bit_dequant_sum_update, args, "gc_2bit_dequant_sum_update", prepare,
+                   (list(codes), center, weights, out))
 
 
-def gc_compensated_sum_update(grads, residuals, lr: float, weights: torch.Tensor, stream=None) -> None:
+def gc_compensated_sum_update(grads, residuals, lr: float, weights: torch.Tensor, stream=None,
+                              prepare: bool = False):
     lib = load()
     W = len(grads)
     n = weights.numel()
     dt = _gdtype(grads[0])
-    st = lib.gc_compensated_sum_update(_ptrs(grads, "grads", grads[0].dtype, n), dt,
-                                       _ptrs(residuals, "residuals", torch.float32, n), W, n,
-                                       float(lr), _dev(weights, "weights", torch.float32, n),
-                                       _stream(stream, weights))
-    _check(st, "gc_compensated_sum_update")
+    args = (_ptrs(grads, "grads", grads[0].dtype, n), dt,
+            _ptrs(residuals, "residuals", torch.float32, n), W, n,
+            float(lr), _dev(weights, "weights", torch.float32, n), _stream(stream, weights))
+    return _invoke(lib.gc_compensated_sum_update, args, "gc_compensated_sum_update", prepare,
+                   (list(grads), list(residuals), weights))
 
 
 def qsgd_quantize(grad: torch.Tensor, bucket: int, s_levels: int, seed: int, worker: int,
-                  norms: torch.Tensor, codes: torch.Tensor, stream=None) -> None:
+                  norms: torch.Tensor, codes: torch.Tensor, stream=None, prepare: bool = False):
     lib = load()
     n = grad.numel()
-    st = lib.qsgd_quantize(_dev(grad, "grad", torch.float32), n, int(bucket), int(s_levels),
-                           int(seed) & 0xFFFFFFFFFFFFFFFF, int(worker),
-                           _dev(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
-                           _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
-                           _stream(stream, grad))
-    _check(st, "qsgd_quantize")
+    args = (_dev(grad, "grad", torch.float32), n, int(bucket), int(s_levels),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, int(worker),
+            _dev(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
+            _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _stream(stream, grad))
+    return _invoke(lib.qsgd_quantize, args, "qsgd_quantize", prepare, (grad, norms, codes))
 
 
 def qsgd_dequant_sum(codes, norms, n: int, bucket: int, s_levels: int, scale: float,
-                     out: torch.Tensor, stream=None) -> None:
+                     out: torch.Tensor, stream=None, prepare: bool = False):
     lib = load()
     W = len(codes)
-    st = lib.qsgd_dequant_sum(_ptrs(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
-                              _ptrs(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
-                              W, n, int(bucket), int(s_levels), float(scale),
-                              _dev(out, "out", torch.float32, n), _stream(stream, out))
-    _check(st, "qsgd_dequant_sum")
+    args = (_ptrs(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _ptrs(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
+            W, n, int(bucket), int(s_levels), float(scale),
+            _dev(out, "out", torch.float32, n), _stream(stream, out))
+    return _invoke(lib.qsgd_dequant_sum, args, "qsgd_dequant_sum", prepare, (list(codes), list(norms), out))
 
 
 def saps_round_seed(base_seed: int, t: int) -> int:
@@ -232,42 +257,44 @@ def saps_workspace_bytes(n: int) -> int:
 
 def saps_mask_compact(n: int, p: float, seed_t: int, models, idx: torch.Tensor, vals,
                       d_count: torch.Tensor, workspace: torch.Tensor, d_status: torch.Tensor,
-                      stream=None) -> None:
+                      stream=None, prepare: bool = False):
     """models: W fp32 tensors [n]; idx: int32 (uint32 bits) [capacity]; vals: W fp32
     [capacity]; d_count: int64 [1]; workspace: uint8 [saps_workspace_bytes(n)];
     d_status: int32 [1] (zeroed by the caller)."""
     lib = load()
     W = len(models)
     capacity = idx.numel()
-    st = lib.saps_mask_compact(int(n), float(p), int(seed_t) & 0xFFFFFFFFFFFFFFFF,
-                               _ptrs(models, "models", torch.float32, n), W,
-                               _dev(idx, "idx", torch.int32), _ptrs(vals, "vals", torch.float32, capacity),
-                               capacity, _dev(d_count, "d_count", torch.int64, 1),
-                               _dev(workspace, "workspace", torch.uint8), workspace.numel(),
-                               _dev(d_status, "d_status", torch.int32, 1), _stream(stream, idx))
-    _check(st, "saps_mask_compact")
+    args = (int(n), float(p), int(seed_t) & 0xFFFFFFFFFFFFFFFF,
+            _ptrs(models, "models", torch.float32, n), W,
+            _dev(idx, "idx", torch.int32), _ptrs(vals, "vals", torch.float32, capacity),
+            capacity, _dev(d_count, "d_count", torch.int64, 1),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+            _dev(d_status, "d_status", torch.int32, 1), _stream(stream, idx))
+    return _invoke(lib.saps_mask_compact, args, "saps_mask_compact", prepare,
+                   (list(models), idx, list(vals), d_count, workspace, d_status))
 
 
 def saps_peer_average(models, vals, idx: torch.Tensor, d_count: torch.Tensor, pairs,
-                      stream=None) -> None:
+                      stream=None, prepare: bool = False):
     lib = load()
     W = len(models)
     pairs_arr = (ctypes.c_int * W)(*[int(p) for p in pairs])
     capacity = idx.numel()
-    st = lib.saps_peer_average(_ptrs(models, "models", torch.float32),
-                               _ptrs(vals, "vals", torch.float32, capacity),
-                               _dev(idx, "idx", torch.int32), _dev(d_count, "d_count", torch.int64, 1),
-                               pairs_arr, W, capacity, _stream(stream, idx))
-    _check(st, "saps_peer_average")
+    args = (_ptrs(models, "models", torch.float32), _ptrs(vals, "vals", torch.float32, capacity),
+            _dev(idx, "idx", torch.int32), _dev(d_count, "d_count", torch.int64, 1),
+            pairs_arr, W, capacity, _stream(stream, idx))
+    return _invoke(lib.saps_peer_average, args, "saps_peer_average", prepare,
+                   (list(models), list(vals), idx, d_count))
 
 
-def easgd_step(models, alpha: float, beta: float, center: torch.Tensor, stream=None) -> None:
+def easgd_step(models, alpha: float, beta: float, center: torch.Tensor, stream=None,
+               prepare: bool = False):
     lib = load()
     W = len(models)
     n = center.numel()
-    st = lib.easgd_step(_ptrs(models, "models", torch.float32, n), W, n, float(alpha), float(beta),
-                        _dev(center, "center", torch.float32, n), _stream(stream, center))
-    _check(st, "easgd_step")
+    args = (_ptrs(models, "models", torch.float32, n), W, n, float(alpha), float(beta),
+            _dev(center, "center", torch.float32, n), _stream(stream, center))
+    return _invoke(lib.easgd_step, args, "easgd_step", prepare, (list(models), center))
 
 
 def saps_mask_compact_noalloc(n: int, p: float, seed_t: int, models, idx: torch.Tensor, vals,

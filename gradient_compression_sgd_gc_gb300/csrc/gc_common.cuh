@@ -40,37 +40,27 @@ struct PtrTable {
 };
 
 // ---------------------------------------------------------------- memory
+// Plain C++ intrinsics (not volatile asm) so that the compiler can hoist
+// independent loads above earlier stores; buffers are __restrict__ where the
+// kernels rely on that.
 
-// Streaming 128-bit read of data used once: not allocated in L1.
+// Streaming 128-bit read of data used once (evict-first, "cache streaming").
 __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
+    return __ldcs(reinterpret_cast<const float4*>(p));
 }
 
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+    return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
-// 128-bit read of data the same kernel later overwrites (no .nc).
+// 128-bit read of data the same thread later overwrites (coherent path).
 __device__ __forceinline__ float4 ld_f4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
+    return __ldcs(reinterpret_cast<const float4*>(p));
 }
 
 // Streaming 128-bit store (evict-first).
 __device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
-    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};"
-                 :: "l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+    __stcs(reinterpret_cast<float4*>(p), v);
 }
 
 // ---------------------------------------------------------------- hash

@@ -168,48 +168,69 @@ struct DqArgs {
     float* out;
 };
 
+// Applies the update to 4 consecutive elements from their per-element
+// (value + 1) sums packed in the bytes of R.  `w`/`c` are the already-loaded
+// weight and center vectors (full tiles).
 template <int KIND>
-__device__ __forceinline__ void dq_apply(const DqArgs& a, int64_t e0, uint32_t R, bool full) {
+__device__ __forceinline__ void dq_apply_full(const DqArgs& a, int64_t e0, uint32_t R, float4 w, float4 c) {
     const float bias = 8388608.0f + static_cast<float>(a.W);
     float cnt[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b)
         cnt[b] = __uint_as_float(__byte_perm(R, 0x4B000000u, 0x7540u | b)) - bias;
-    if (full) {
-        if (KIND == GC_UPD_NONE) {
-            st_stream_f4(a.out + e0, make_float4(cnt[0] * a.k_out, cnt[1] * a.k_out,
-                                                 cnt[2] * a.k_out, cnt[3] * a.k_out));
-        } else {
-            float4 w = ld_f4(a.weights + e0);
-            float4 nw;
-            nw.x = fmaf(-cnt[0], a.k_lr, w.x);
-            nw.y = fmaf(-cnt[1], a.k_lr, w.y);
-            nw.z = fmaf(-cnt[2], a.k_lr, w.z);
-            nw.w = fmaf(-cnt[3], a.k_lr, w.w);
-            if (KIND == GC_UPD_EASGD) {
-                const float4 c = ld_stream_f4(a.center + e0);
-                nw.x = fmaf(-a.alpha, w.x - c.x, nw.x);
-                nw.y = fmaf(-a.alpha, w.y - c.y, nw.y);
-                nw.z = fmaf(-a.alpha, w.z - c.z, nw.z);
-                nw.w = fmaf(-a.alpha, w.w - c.w, nw.w);
-            }
-            st_stream_f4(a.weights + e0, nw);
-        }
+    if (KIND == GC_UPD_NONE) {
+        st_stream_f4(a.out + e0, make_float4(cnt[0] * a.k_out, cnt[1] * a.k_out,
+                                             cnt[2] * a.k_out, cnt[3] * a.k_out));
     } else {
+        float4 nw;
+        nw.x = fmaf(-cnt[0], a.k_lr, w.x);
+        nw.y = fmaf(-cnt[1], a.k_lr, w.y);
+        nw.z = fmaf(-cnt[2], a.k_lr, w.z);
+        nw.w = fmaf(-cnt[3], a.k_lr, w.w);
+        if (KIND == GC_UPD_EASGD) {
+            nw.x = fmaf(-a.alpha, w.x - c.x, nw.x);
+            nw.y = fmaf(-a.alpha, w.y - c.y, nw.y);
+            nw.z = fmaf(-a.alpha, w.z - c.z, nw.z);
+            nw.w = fmaf(-a.alpha, w.w - c.w, nw.w);
+        }
+        st_stream_f4(a.weights + e0, nw);
+    }
+}
+
+// Partial tile: element by element with bounds checks.
+template <int KIND>
+__device__ __forceinline__ void dq_apply_tail(const DqArgs& a, int64_t e0, uint32_t R) {
+    const float bias = 8388608.0f + static_cast<float>(a.W);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int64_t e = e0 + b;
-            if (e >= a.n) break;
-            if (KIND == GC_UPD_NONE) {
-                a.out[e] = cnt[b] * a.k_out;
-            } else {
-                const float w = a.weights[e];
-                float nw = fmaf(-cnt[b], a.k_lr, w);
-                if (KIND == GC_UPD_EASGD) nw = fmaf(-a.alpha, w - a.center[e], nw);
-                a.weights[e] = nw;
-            }
+    for (int b = 0; b < 4; ++b) {
+        const int64_t e = e0 + b;
+        if (e >= a.n) break;
+        const float cnt = __uint_as_float(__byte_perm(R, 0x4B000000u, 0x7540u | b)) - bias;
+        if (KIND == GC_UPD_NONE) {
+            a.out[e] = cnt * a.k_out;
+        } else {
+            const float w = a.weights[e];
+            float nw = fmaf(-cnt, a.k_lr, w);
+            if (KIND == GC_UPD_EASGD) nw = fmaf(-a.alpha, w - a.center[e], nw);
+            a.weights[e] = nw;
         }
     }
+}
+
+// Adds one code word's per-element (value + 1) to the 4-bit accumulators.
+__device__ __forceinline__ void swar_add(uint32_t c, uint32_t& A0, uint32_t& A1) {
+    const uint32_t m = plus_one_fields(c);
+    A0 += m & 0x33333333u;
+    A1 += (m >> 2) & 0x33333333u;
+}
+
+// Moves the 4-bit accumulators (<= 7 workers) into the 8-bit ones.
+__device__ __forceinline__ void swar_spill(uint32_t A0, uint32_t A1, uint32_t& B0, uint32_t& B1,
+                                           uint32_t& B2, uint32_t& B3) {
+    B0 += A0 & 0x0F0F0F0Fu;
+    B1 += (A0 >> 4) & 0x0F0F0F0Fu;
+    B2 += A1 & 0x0F0F0F0Fu;
+    B3 += (A1 >> 4) & 0x0F0F0F0Fu;
 }
 
 // K2: one warp per 512-element tile.  Lane m loads word m of the tile from
@@ -218,9 +239,10 @@ __device__ __forceinline__ void dq_apply(const DqArgs& a, int64_t e0, uint32_t R
 // workers at a time, then 8-bit fields (sums <= 2 * 64 fit a byte).  The
 // per-element sums are regrouped through shared memory so that lane l then
 // owns elements 128j + 4l .. +3 of the tile, matching the coalesced float4
-// layout of the weights.
+// layout of the weights.  Every load of a tile (weights, center, up to 14
+// code words) is issued before any of them is used.
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, KIND == GC_UPD_EASGD ? 3 : 4)
 k_2bit_dqsum(const DqArgs a) {
     __shared__ uint4 stage[kWarpsPerBlock][32];
     const int lane = threadIdx.x & 31;
@@ -232,37 +254,51 @@ k_2bit_dqsum(const DqArgs a) {
     const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(&stage[wib][0]);
 
     for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+        const bool full = (tile + 1) * kTile <= a.n;
+        const int64_t ebase = tile * kTile + 4 * lane;
+        float4 wv[4], cv[4];
+        if (full && KIND != GC_UPD_NONE) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wv[j] = ld_f4(a.weights + ebase + 128 * j);
+            if (KIND == GC_UPD_EASGD) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cv[j] = ld_stream_f4(a.center + ebase + 128 * j);
+            }
+        }
         const int64_t word = tile * kWordsPerTile + lane;
         const bool have_word = word < nwords;
         uint32_t B0 = 0, B1 = 0, B2 = 0, B3 = 0;
-        for (int w0 = 0; w0 < a.W; w0 += 7) {
-            uint32_t cw[7];
+        for (int w0 = 0; w0 < a.W; w0 += 14) {
+            uint32_t cw[14];
 #pragma unroll
-            for (int k = 0; k < 7; ++k)
+            for (int k = 0; k < 14; ++k)
                 cw[k] = (w0 + k < a.W && have_word) ? __ldg(a.codes.p[w0 + k] + word) : 0u;
             uint32_t A0 = 0, A1 = 0;
 #pragma unroll
-            for (int k = 0; k < 7; ++k) {
-                if (w0 + k < a.W) {
-                    const uint32_t m = plus_one_fields(cw[k]);
-                    A0 += m & 0x33333333u;
-                    A1 += (m >> 2) & 0x33333333u;
-                }
+            for (int k = 0; k < 7; ++k)
+                if (w0 + k < a.W) swar_add(cw[k], A0, A1);
+            swar_spill(A0, A1, B0, B1, B2, B3);
+            if (w0 + 7 < a.W) {
+                A0 = A1 = 0;
+#pragma unroll
+                for (int k = 7; k < 14; ++k)
+                    if (w0 + k < a.W) swar_add(cw[k], A0, A1);
+                swar_spill(A0, A1, B0, B1, B2, B3);
             }
-            B0 += A0 & 0x0F0F0F0Fu;
-            B1 += (A0 >> 4) & 0x0F0F0F0Fu;
-            B2 += A1 & 0x0F0F0F0Fu;
-            B3 += (A1 >> 4) & 0x0F0F0F0Fu;
         }
         stage[wib][lane] = make_uint4(pack_quad<0>(B0, B1, B2, B3), pack_quad<1>(B0, B1, B2, B3),
                                       pack_quad<2>(B0, B1, B2, B3), pack_quad<3>(B0, B1, B2, B3));
         __syncwarp();
-        const bool full = (tile + 1) * kTile <= a.n;
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t e0 = tile * kTile + 128 * j + 4 * lane;
-            const uint32_t R = stage32[32 * j + lane];
-            if (full || e0 < a.n) dq_apply<KIND>(a, e0, R, full);
+            for (int j = 0; j < 4; ++j)
+                dq_apply_full<KIND>(a, ebase + 128 * j, stage32[32 * j + lane], wv[j], cv[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t e0 = ebase + 128 * j;
+                if (e0 < a.n) dq_apply_tail<KIND>(a, e0, stage32[32 * j + lane]);
+            }
         }
         __syncwarp();
     }
