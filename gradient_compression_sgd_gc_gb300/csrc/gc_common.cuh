@@ -25,6 +25,11 @@ inline int grid_for(int per_sm) {
     return sms * per_sm;
 }
 
+// Blocks of kThreads threads for one warp per tile.
+inline unsigned blocks_for_tiles(int64_t tiles) {
+    return static_cast<unsigned>((tiles + kWarpsPerBlock - 1) / kWarpsPerBlock);
+}
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

@@ -64,83 +64,86 @@ struct QArgs {
 };
 
 // level = min(floor(|v| * S + u), s) in fp32, u = top24(hash) * 2^-24.
-__device__ __forceinline__ uint32_t qlevel(float x, float S, float s_f, uint32_t s, uint64_t key) {
-    const float u = __fmul_rn(__uint2float_rn(splitmix64_top24(key)), 5.9604644775390625e-8f);
-    const float y = __fadd_rn(__fmul_rn(fabsf(x), S), u);
-    // for 0 <= y < 2^23, rounding y + 2^23 downwards leaves floor(y) in the
-    // mantissa bits
+// u is an exact multiple of 2^-24, so one fma rounds |v|*S + u exactly as the
+// separate add does.  For 0 <= y < 2^23, rounding y + 2^23 downwards leaves
+// floor(y) in the mantissa bits; a NaN y (s / norm overflowed) has all
+// mantissa bits set there, so the min with s maps it to s.
+__device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint64_t key) {
+    const float a = __fmul_rn(fabsf(x), S);
+    const float y = __fmaf_rn(__uint2float_rn(splitmix64_top24(key)), 5.9604644775390625e-8f, a);
     const uint32_t fl = __float_as_uint(__fadd_rd(y, 8388608.0f)) & 0x7FFFFFu;
-    return (y < s_f) ? fl : s;
+    return min(fl, s);
 }
 
+// One warp per bucket; the grid covers every bucket.
 template <int ROUNDS, bool FOUR>
 __global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
 k_qsgd_quantize(const QArgs a) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= a.nbuckets) return;
     constexpr int D = 128 * ROUNDS;
     constexpr uint32_t kSignShift = FOUR ? 3 : 7;
     const float s_f = static_cast<float>(a.s);
     const uint32_t s_u = static_cast<uint32_t>(a.s);
 
-    for (int64_t b = warp; b < a.nbuckets; b += nwarps) {
-        const int64_t b0 = b * D;
-        const bool full = b0 + D <= a.n;
-        float4 v[ROUNDS];
-        if (full) {
+    const int64_t b0 = b * D;
+    const bool full = b0 + D <= a.n;
+    float4 v[ROUNDS];
+    if (full) {
 #pragma unroll
-            for (int j = 0; j < ROUNDS; ++j) v[j] = ld_stream_f4(a.v + b0 + 128 * j + 4 * lane);
-        } else {
-#pragma unroll
-            for (int j = 0; j < ROUNDS; ++j) {
-                const int64_t e = b0 + 128 * j + 4 * lane;
-                v[j].x = e < a.n ? a.v[e] : 0.0f;
-                v[j].y = e + 1 < a.n ? a.v[e + 1] : 0.0f;
-                v[j].z = e + 2 < a.n ? a.v[e + 2] : 0.0f;
-                v[j].w = e + 3 < a.n ? a.v[e + 3] : 0.0f;
-            }
-        }
-        float hi = 0.0f, lo = 0.0f;
-#pragma unroll
-        for (int j = 0; j < ROUNDS; ++j) {
-            acc_square(v[j].x, hi, lo);
-            acc_square(v[j].y, hi, lo);
-            acc_square(v[j].z, hi, lo);
-            acc_square(v[j].w, hi, lo);
-        }
-        const float norm = warp_norm(hi, lo);
-        if (lane == 0) a.norms[b] = norm;
-        const bool zero = !(norm > 0.0f);
-        const float S = zero ? 0.0f : __fdiv_rn(s_f, norm);
-
+        for (int j = 0; j < ROUNDS; ++j) v[j] = ld_stream_f4(a.v + b0 + 128 * j + 4 * lane);
+    } else {
 #pragma unroll
         for (int j = 0; j < ROUNDS; ++j) {
             const int64_t e = b0 + 128 * j + 4 * lane;
-            const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-            uint32_t c[4];
+            v[j].x = e < a.n ? a.v[e] : 0.0f;
+            v[j].y = e + 1 < a.n ? a.v[e + 1] : 0.0f;
+            v[j].z = e + 2 < a.n ? a.v[e + 2] : 0.0f;
+            v[j].w = e + 3 < a.n ? a.v[e + 3] : 0.0f;
+        }
+    }
+    float hi = 0.0f, lo = 0.0f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t lvl = zero ? 0u : qlevel(xs[k], S, s_f, s_u, a.seed_w ^ static_cast<uint64_t>(e + k));
-                c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
-            }
-            if (FOUR) {
-                const uint32_t lo2 = (c[0] << 4) | c[1];
-                const uint32_t hi2 = (c[2] << 4) | c[3];
-                if (full) {
-                    *reinterpret_cast<uint16_t*>(a.codes + (e >> 1)) = static_cast<uint16_t>(lo2 | (hi2 << 8));
-                } else {
-                    if (e < a.n) a.codes[e >> 1] = static_cast<uint8_t>(e + 1 < a.n ? lo2 : (c[0] << 4));
-                    if (e + 2 < a.n) a.codes[(e >> 1) + 1] = static_cast<uint8_t>(e + 3 < a.n ? hi2 : (c[2] << 4));
-                }
+    for (int j = 0; j < ROUNDS; ++j) {
+        acc_square(v[j].x, hi, lo);
+        acc_square(v[j].y, hi, lo);
+        acc_square(v[j].z, hi, lo);
+        acc_square(v[j].w, hi, lo);
+    }
+    const float norm = warp_norm(hi, lo);
+    if (lane == 0) a.norms[b] = norm;
+    const bool zero = !(norm > 0.0f);
+    const float S = zero ? 0.0f : __fdiv_rn(s_f, norm);
+
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+        const int64_t e = b0 + 128 * j + 4 * lane;
+        // e is a multiple of 4, so seed_w ^ (e + k) == (seed_w ^ e) ^ k
+        const uint64_t kbase = a.seed_w ^ static_cast<uint64_t>(e);
+        const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lvl = zero ? 0u : qlevel(xs[k], S, s_u, kbase ^ static_cast<uint64_t>(k));
+            c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
+        }
+        if (FOUR) {
+            const uint32_t lo2 = (c[0] << 4) | c[1];
+            const uint32_t hi2 = (c[2] << 4) | c[3];
+            if (full) {
+                *reinterpret_cast<uint16_t*>(a.codes + (e >> 1)) = static_cast<uint16_t>(lo2 | (hi2 << 8));
             } else {
-                if (full) {
-                    *reinterpret_cast<uint32_t*>(a.codes + e) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-                } else {
+                if (e < a.n) a.codes[e >> 1] = static_cast<uint8_t>(e + 1 < a.n ? lo2 : (c[0] << 4));
+                if (e + 2 < a.n) a.codes[(e >> 1) + 1] = static_cast<uint8_t>(e + 3 < a.n ? hi2 : (c[2] << 4));
+            }
+        } else {
+            if (full) {
+                *reinterpret_cast<uint32_t*>(a.codes + e) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+            } else {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (e + k < a.n) a.codes[e + k] = static_cast<uint8_t>(c[k]);
-                }
+                for (int k = 0; k < 4; ++k)
+                    if (e + k < a.n) a.codes[e + k] = static_cast<uint8_t>(c[k]);
             }
         }
     }
@@ -152,96 +155,103 @@ struct DArgs {
     int W;
     int64_t n;
     int64_t nbuckets;
-    int s;
-    float scale;
+    float unit_scale;     // scale / s, rounded once to fp32
     float* out;
 };
 
+// Raw code bits of elements e..e+3 (e a multiple of 4): 16 bits for 4-bit
+// codes (byte e/2 in bits 0-7, byte e/2+1 in bits 8-15), 32 bits for 8-bit.
 template <bool FOUR>
-__device__ __forceinline__ void decode4(const uint8_t* codes, int64_t e, int64_t n, bool full,
-                                        uint32_t (&c)[4]) {
+__device__ __forceinline__ uint32_t load_raw4(const uint8_t* codes, int64_t e, int64_t n, bool full) {
     if (FOUR) {
-        uint32_t h;
-        if (full) {
-            h = *reinterpret_cast<const uint16_t*>(codes + (e >> 1));
-        } else {
-            h = (e < n ? codes[e >> 1] : 0u) | ((e + 2 < n ? codes[(e >> 1) + 1] : 0u) << 8);
-        }
-        c[0] = (h >> 4) & 15u;
-        c[1] = h & 15u;
-        c[2] = (h >> 12) & 15u;
-        c[3] = (h >> 8) & 15u;
-    } else {
-        uint32_t w;
-        if (full) {
-            w = __ldg(reinterpret_cast<const uint32_t*>(codes + e));
-        } else {
-            w = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (e + k < n) w |= static_cast<uint32_t>(codes[e + k]) << (8 * k);
-        }
-        c[0] = w & 255u;
-        c[1] = (w >> 8) & 255u;
-        c[2] = (w >> 16) & 255u;
-        c[3] = w >> 24;
+        if (full) return __ldg(reinterpret_cast<const uint16_t*>(codes + (e >> 1)));
+        return (e < n ? codes[e >> 1] : 0u) | ((e + 2 < n ? codes[(e >> 1) + 1] : 0u) << 8);
     }
+    if (full) return __ldg(reinterpret_cast<const uint32_t*>(codes + e));
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (e + k < n) w |= static_cast<uint32_t>(codes[e + k]) << (8 * k);
+    return w;
 }
 
+// Code k (0..3) of the raw bits above.
+template <bool FOUR>
+__device__ __forceinline__ uint32_t code_of(uint32_t raw, int k) {
+    if (FOUR) {
+        // byte 0 = (c0 << 4) | c1, byte 1 = (c2 << 4) | c3
+        const int shift = (k == 0) ? 4 : (k == 1) ? 0 : (k == 2) ? 12 : 8;
+        return (raw >> shift) & 15u;
+    }
+    return (raw >> (8 * k)) & 255u;
+}
+
+// One warp per bucket.  Workers are taken WC at a time with every code and
+// norm load of the group issued before any is decoded; each element's sum runs
+// in worker order.  The per-bucket unit is norm * (scale / s).
 template <int ROUNDS, bool FOUR>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 3)
 k_qsgd_dequant_sum(const DArgs a) {
+    constexpr int WC = ROUNDS >= 8 ? 1 : 4;      // workers whose loads are issued together
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= a.nbuckets) return;
     constexpr int D = 128 * ROUNDS;
     constexpr uint32_t kLevelMask = FOUR ? 7u : 127u;
     constexpr uint32_t kSignBit = FOUR ? 8u : 128u;
-    const float s_f = static_cast<float>(a.s);
 
-    for (int64_t b = warp; b < a.nbuckets; b += nwarps) {
-        const int64_t b0 = b * D;
-        const bool full = b0 + D <= a.n;
-        float sum[ROUNDS][4];
+    const int64_t b0 = b * D;
+    const bool full = b0 + D <= a.n;
+    float sum[ROUNDS][4];
 #pragma unroll
-        for (int j = 0; j < ROUNDS; ++j)
+    for (int j = 0; j < ROUNDS; ++j)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) sum[j][k] = 0.0f;
-        for (int w = 0; w < a.W; ++w) {
-            const uint8_t* cw = a.codes.p[w];
-            const float unit = __fdiv_rn(__ldg(a.norms.p[w] + b), s_f);
+        for (int k = 0; k < 4; ++k) sum[j][k] = 0.0f;
+    for (int w0 = 0; w0 < a.W; w0 += WC) {
+        uint32_t raw[WC][ROUNDS];
+        float unit[WC];
 #pragma unroll
-            for (int j = 0; j < ROUNDS; ++j) {
-                const int64_t e = b0 + 128 * j + 4 * lane;
-                uint32_t c[4];
-                decode4<FOUR>(cw, e, a.n, full, c);
+        for (int q = 0; q < WC; ++q) {
+            if (w0 + q < a.W) {
+                unit[q] = __ldg(a.norms.p[w0 + q] + b);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float lf = __uint_as_float(0x4B000000u | (c[k] & kLevelMask)) - 8388608.0f;
-                    const float term = __fmul_rn(unit, lf);
-                    sum[j][k] = (c[k] & kSignBit) ? __fsub_rn(sum[j][k], term) : __fadd_rn(sum[j][k], term);
-                }
+                for (int j = 0; j < ROUNDS; ++j)
+                    raw[q][j] = load_raw4<FOUR>(a.codes.p[w0 + q], b0 + 128 * j + 4 * lane, a.n, full);
             }
         }
 #pragma unroll
-        for (int j = 0; j < ROUNDS; ++j) {
-            const int64_t e = b0 + 128 * j + 4 * lane;
-            const float4 o = make_float4(__fmul_rn(a.scale, sum[j][0]), __fmul_rn(a.scale, sum[j][1]),
-                                         __fmul_rn(a.scale, sum[j][2]), __fmul_rn(a.scale, sum[j][3]));
-            if (full) {
-                st_stream_f4(a.out + e, o);
-            } else {
-                if (e < a.n) a.out[e] = o.x;
-                if (e + 1 < a.n) a.out[e + 1] = o.y;
-                if (e + 2 < a.n) a.out[e + 2] = o.z;
-                if (e + 3 < a.n) a.out[e + 3] = o.w;
+        for (int q = 0; q < WC; ++q) {
+            if (w0 + q < a.W) {
+                const float u = __fmul_rn(unit[q], a.unit_scale);
+#pragma unroll
+                for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t c = code_of<FOUR>(raw[q][j], k);
+                        const float lf = __uint_as_float(0x4B000000u | (c & kLevelMask)) - 8388608.0f;
+                        const float term = __fmul_rn(u, lf);
+                        sum[j][k] = (c & kSignBit) ? __fsub_rn(sum[j][k], term) : __fadd_rn(sum[j][k], term);
+                    }
             }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+        const int64_t e = b0 + 128 * j + 4 * lane;
+        const float4 o = make_float4(sum[j][0], sum[j][1], sum[j][2], sum[j][3]);
+        if (full) {
+            st_stream_f4(a.out + e, o);
+        } else {
+            if (e < a.n) a.out[e] = o.x;
+            if (e + 1 < a.n) a.out[e + 1] = o.y;
+            if (e + 2 < a.n) a.out[e + 2] = o.z;
+            if (e + 3 < a.n) a.out[e + 3] = o.w;
         }
     }
 }
 
 template <bool FOUR>
-int launch_quantize(int rounds, const QArgs& a, int grid, cudaStream_t s) {
+int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
     switch (rounds) {
         case 1: k_qsgd_quantize<1, FOUR><<<grid, kThreads, 0, s>>>(a); break;
         case 2: k_qsgd_quantize<2, FOUR><<<grid, kThreads, 0, s>>>(a); break;
@@ -254,7 +264,7 @@ int launch_quantize(int rounds, const QArgs& a, int grid, cudaStream_t s) {
 }
 
 template <bool FOUR>
-int launch_dequant(int rounds, const DArgs& a, int grid, cudaStream_t s) {
+int launch_dequant(int rounds, const DArgs& a, unsigned grid, cudaStream_t s) {
     switch (rounds) {
         case 1: k_qsgd_dequant_sum<1, FOUR><<<grid, kThreads, 0, s>>>(a); break;
         case 2: k_qsgd_dequant_sum<2, FOUR><<<grid, kThreads, 0, s>>>(a); break;
@@ -292,8 +302,7 @@ int qsgd_quantize(const float* grad, int64_t n, int bucket, int s_levels, uint64
     a.s = s_levels;
     a.norms = norms;
     a.codes = codes;
-    const int grid = grid_for(4);
-    if (grid <= 0) return GC_ERR_CUDA;
+    const unsigned grid = blocks_for_tiles(a.nbuckets);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return s_levels <= 7 ? launch_quantize<true>(bucket / 128, a, grid, s)
                          : launch_quantize<false>(bucket / 128, a, grid, s);
@@ -317,11 +326,9 @@ int qsgd_dequant_sum(const uint8_t* const* codes, const float* const* norms, int
     a.W = W;
     a.n = n;
     a.nbuckets = (n + bucket - 1) / bucket;
-    a.s = s_levels;
-    a.scale = scale;
+    a.unit_scale = static_cast<float>(static_cast<double>(scale) / s_levels);
     a.out = out;
-    const int grid = grid_for(4);
-    if (grid <= 0) return GC_ERR_CUDA;
+    const unsigned grid = blocks_for_tiles(a.nbuckets);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return s_levels <= 7 ? launch_dequant<true>(bucket / 128, a, grid, s)
                          : launch_dequant<false>(bucket / 128, a, grid, s);

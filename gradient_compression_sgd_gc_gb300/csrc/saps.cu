@@ -425,8 +425,9 @@ int easgd_step(float* const* models, int W, int64_t n, float alpha, float beta, 
     a.inv_w = static_cast<float>(1.0 / W);
     a.center = center;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(W <= 16 ? 2 : 4);
-    if (grid <= 0) return GC_ERR_CUDA;
+    // one float4 (one element for the wide kernel) per thread, grid covering n
+    const int64_t items = W <= 16 ? (n >> 2) + 1 : n;
+    const unsigned grid = static_cast<unsigned>((items + kThreads - 1) / kThreads);
     if (W <= 4)
         k_easgd<4><<<grid, kThreads, 0, s>>>(a);
     else if (W <= 16)

@@ -67,16 +67,19 @@ __device__ void quantize_tail(LoadG loadg, float* __restrict__ r, uint8_t* __res
     }
 }
 
-// K1, fp32 gradients.
-__global__ void __launch_bounds__(kThreads, 4)
+// K1, fp32 gradients.  One warp per 512-element tile and a grid that covers
+// every tile: the block scheduler hands out tiles in address order, which
+// keeps the set of tiles in flight a compact window of HBM (measured faster
+// than a persistent grid-stride loop).  The warp whose tile is the partial
+// last one takes the bounds-checked path.
+__global__ void __launch_bounds__(kThreads)
 k_2bit_quantize_f32(const float* __restrict__ g, float* __restrict__ r,
                     uint32_t* __restrict__ codes, int64_t n, float t) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t ntiles = n / kTile;
+    const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nfull = n / kTile;
     uint8_t* cb = reinterpret_cast<uint8_t*>(codes);
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+    if (tile < nfull) {
         const int64_t base = tile * kTile + 4 * lane;
         float4 gv[4], rv[4];
 #pragma unroll
@@ -90,22 +93,22 @@ k_2bit_quantize_f32(const float* __restrict__ g, float* __restrict__ r,
             st_stream_f4(r + base + 128 * j, rv[j]);
             cb[code_byte(base + 128 * j)] = static_cast<uint8_t>(c);
         }
+    } else if (tile == nfull && n % kTile != 0) {
+        quantize_tail([g](int64_t e) { return g[e]; }, r, cb, nfull * kTile, n, t, lane);
     }
-    if (n % kTile != 0 && warp == ntiles % nwarps)
-        quantize_tail([g](int64_t e) { return g[e]; }, r, cb, ntiles * kTile, n, t, lane);
 }
 
 // K1, bf16 gradients: lane l of round j reads 8 bf16 (16 bytes) at tile
-// offset 256j + 8l, i.e. two code bytes = one 16-bit half of a word.
-__global__ void __launch_bounds__(kThreads, 4)
+// offset 256j + 8l, i.e. two code bytes = one 16-bit half of a word.  Same
+// launch shape as the fp32 kernel.
+__global__ void __launch_bounds__(kThreads)
 k_2bit_quantize_bf16(const uint16_t* __restrict__ g, float* __restrict__ r,
                      uint32_t* __restrict__ codes, int64_t n, float t) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t ntiles = n / kTile;
+    const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nfull = n / kTile;
     uint16_t* ch = reinterpret_cast<uint16_t*>(codes);
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+    if (tile < nfull) {
         const int64_t base = tile * kTile + 8 * lane;
         uint4 gv[2];
         float4 rv[4];
@@ -129,10 +132,10 @@ k_2bit_quantize_bf16(const uint16_t* __restrict__ g, float* __restrict__ r,
             const int64_t e = base + 256 * j;
             ch[2 * (e >> 4) + 1 - ((e >> 3) & 1)] = static_cast<uint16_t>(c);
         }
-    }
-    if (n % kTile != 0 && warp == ntiles % nwarps)
+    } else if (tile == nfull && n % kTile != 0) {
         quantize_tail([g](int64_t e) { return __uint_as_float(static_cast<uint32_t>(g[e]) << 16); },
-                      r, reinterpret_cast<uint8_t*>(codes), ntiles * kTile, n, t, lane);
+                      r, reinterpret_cast<uint8_t*>(codes), nfull * kTile, n, t, lane);
+    }
 }
 
 // ------------------------------------------------------------------ K2
@@ -240,20 +243,20 @@ __device__ __forceinline__ void swar_spill(uint32_t A0, uint32_t A1, uint32_t& B
 // per-element sums are regrouped through shared memory so that lane l then
 // owns elements 128j + 4l .. +3 of the tile, matching the coalesced float4
 // layout of the weights.  Every load of a tile (weights, center, up to 14
-// code words) is issued before any of them is used.
+// code words) is issued before any of them is used.  One tile per warp; the
+// grid covers every tile.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, KIND == GC_UPD_EASGD ? 3 : 4)
 k_2bit_dqsum(const DqArgs a) {
     __shared__ uint4 stage[kWarpsPerBlock][32];
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t nwords = (a.n + 15) >> 4;
     const int64_t ntiles = (a.n + kTile - 1) / kTile;
     const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(&stage[wib][0]);
 
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+    const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (tile < ntiles) {
         const bool full = (tile + 1) * kTile <= a.n;
         const int64_t ebase = tile * kTile + 4 * lane;
         float4 wv[4], cv[4];
@@ -300,7 +303,6 @@ k_2bit_dqsum(const DqArgs a) {
                 if (e0 < a.n) dq_apply_tail<KIND>(a, e0, stage32[32 * j + lane]);
             }
         }
-        __syncwarp();
     }
 }
 
@@ -336,19 +338,18 @@ __device__ __forceinline__ float load_grad1(const void* g, int64_t e) {
     return static_cast<const float*>(g)[e];
 }
 
-// K3: lane l owns 8 consecutive elements (one 16-byte bf16 vector, or two
-// fp32 vectors) per 256-element warp tile; for every worker it forms
+// K3: one warp per 256-element tile, lane l owns 8 consecutive elements (one
+// 16-byte bf16 vector, or two fp32 vectors); for every worker it forms
 // m = r + g in fp32, adds it to the running sum in worker order, and writes
 // the residual back as zero.  The weights get w -= (lr/W) * sum.
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 2)
 k_compensated(const CompArgs a) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    const int64_t ntiles = a.n / 256;
+    const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nfull = a.n / 256;
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
+    if (tile < nfull) {
         const int64_t e = tile * 256 + 8 * lane;
         const float4 w0 = ld_f4(a.weights + e), w1 = ld_f4(a.weights + e + 4);
         float s[8];
@@ -385,18 +386,17 @@ k_compensated(const CompArgs a) {
                                                 fmaf(-s[2], a.k_lr, w0.z), fmaf(-s[3], a.k_lr, w0.w)));
         st_stream_f4(a.weights + e + 4, make_float4(fmaf(-s[4], a.k_lr, w1.x), fmaf(-s[5], a.k_lr, w1.y),
                                                     fmaf(-s[6], a.k_lr, w1.z), fmaf(-s[7], a.k_lr, w1.w)));
-    }
-    // tail: elements [ntiles*256, n), spread over the first warps' lanes
-    const int64_t tail0 = ntiles * 256;
-    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (gtid < a.n - tail0) {
-        const int64_t i = tail0 + gtid;
-        float s = 0.0f;
-        for (int q = 0; q < a.W; ++q) {
-            s = __fadd_rn(s, __fadd_rn(a.res.p[q][i], load_grad1<BF16>(a.grads.p[q], i)));
-            a.res.p[q][i] = 0.0f;
+    } else if (tile == nfull) {
+        // tail: elements [nfull*256, n), one per lane, 8 rounds
+        for (int k = lane; nfull * 256 + k < a.n; k += 32) {
+            const int64_t i = nfull * 256 + k;
+            float s = 0.0f;
+            for (int q = 0; q < a.W; ++q) {
+                s = __fadd_rn(s, __fadd_rn(a.res.p[q][i], load_grad1<BF16>(a.grads.p[q], i)));
+                a.res.p[q][i] = 0.0f;
+            }
+            a.weights[i] = fmaf(-s, a.k_lr, a.weights[i]);
         }
-        a.weights[i] = fmaf(-s, a.k_lr, a.weights[i]);
     }
 }
 
@@ -427,8 +427,7 @@ int gc_2bit_quantize(const void* grad, gc_dtype dtype, float* residual, uint32_t
     if (n == 0) return GC_OK;
     if (!grad || !residual || !codes) return GC_ERR_INVALID;
     if (!aligned16(grad) || !aligned16(residual) || !aligned16(codes)) return GC_ERR_ALIGN;
-    const int grid = grid_for(4);
-    if (grid <= 0) return GC_ERR_CUDA;
+    const unsigned grid = blocks_for_tiles((n + 511) / 512);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == GC_F32)
         k_2bit_quantize_f32<<<grid, kThreads, 0, s>>>(static_cast<const float*>(grad), residual,
@@ -472,8 +471,7 @@ int gc_2bit_dequant_sum_update(const uint32_t* const* codes, int W, int64_t n, f
     a.center = center;
     a.weights = weights;
     a.out = out;
-    const int grid = grid_for(4);
-    if (grid <= 0) return GC_ERR_CUDA;
+    const unsigned grid = blocks_for_tiles((n + 511) / 512);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (kind) {
         case GC_UPD_NONE: k_2bit_dqsum<GC_UPD_NONE><<<grid, kThreads, 0, s>>>(a); break;
@@ -501,9 +499,8 @@ int gc_compensated_sum_update(const void* const* grads, gc_dtype dtype, float* c
     a.n = n;
     a.k_lr = static_cast<float>(static_cast<double>(lr) / W);
     a.weights = weights;
-    // the grid must also cover the < 256 tail elements with one thread each
-    int grid = grid_for(2);
-    if (grid <= 0) return GC_ERR_CUDA;
+    // one warp per 256-element tile, plus one for the partial last tile
+    const unsigned grid = blocks_for_tiles(n / 256 + 1);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == GC_BF16)
         k_compensated<true><<<grid, kThreads, 0, s>>>(a);
