@@ -220,19 +220,19 @@ def headline(args, dev, rank, world, pg):
     codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=dev) for _ in range(W)]
     weights = wl.twobit_weights(cfg, device=dev)
     # validated launches with their arguments prepared once (host cost per
-    # launch ~ a ctypes call), so the GPU queue never runs dry
-    quant = [[gc.gc_2bit_quantize(grads[s][w], res[w], codes[w], t, stream=stream, prepare=True)
-              for w in range(W)] for s in range(pool)]
+    # launch ~ a ctypes call), so the GPU queue never runs dry; the 8 workers'
+    # buffers are quantised by one batched launch
+    quant = [gc.gc_2bit_quantize_batched(grads[s], res, codes, t, stream=stream, prepare=True)
+             for s in range(pool)]
     dqsum = gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights,
                                           stream=stream, prepare=True)
 
     for s in range(args.warmup):
-        for q in quant[s % pool]:
-            q()
+        quant[s % pool]()
         dqsum()
     torch.cuda.synchronize(dev)
-    evq = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(W)] for _ in range(args.steps)]
+    evq = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     evd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     clocks = ClockSampler(gpu_id_for(dev)) if rank == 0 else None
@@ -244,12 +244,10 @@ def headline(args, dev, rank, world, pg):
     w0 = time.time()
     start.record(stream)
     for s in range(args.steps):
-        qs = quant[(args.warmup + s) % pool]
-        for w in range(W):
-            a, b = evq[s][w]
-            a.record(stream)
-            qs[w]()
-            b.record(stream)
+        a, b = evq[s]
+        a.record(stream)
+        quant[(args.warmup + s) % pool]()
+        b.record(stream)
         a, b = evd[s]
         a.record(stream)
         dqsum()
@@ -265,17 +263,17 @@ def headline(args, dev, rank, world, pg):
         time.sleep(0.1)
         clocks.stop()
         clk = clocks.summary(w0, w1)
-    q_ms = [a.elapsed_time(b) for row in evq for (a, b) in row]
+    q_ms = [a.elapsed_time(b) for (a, b) in evq]
     d_ms = [a.elapsed_time(b) for (a, b) in evd]
     del grads, quant
     return {"total_ms": total_ms, "quantize_ms": q_ms, "dqsum_ms": d_ms, "clocks": clk,
-            "launches": args.steps * (W + 1), "n": n, "W": W}
+            "launches": args.steps * 2, "n": n, "W": W}
 
 
 def e2e(args, dev):
     """Same metric through the public API with host buffers: every step copies
     the 8 gradients from pinned host memory, runs the path, and reads the 8
-    packed code buffers back.  Copies run on a second stream so that worker
+    packed code buffers back.  Uploads run on two copy streams so that worker
     w+1's upload overlaps worker w's quantisation; events order each kernel
     after its own upload."""
     import torch
@@ -285,7 +283,7 @@ def e2e(args, dev):
     cfg = wl.TWOBIT_DQ_SGD
     n, W, t, lr = cfg.n, cfg.workers, cfg.threshold, cfg.lr
     stream = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
+    copies = [torch.cuda.Stream(dev) for _ in range(2)]
     host_g = [wl.twobit_grad(cfg, 0, w, device="cpu").pin_memory() for w in range(W)]
     host_c = [torch.empty(gc.code_words(n), dtype=torch.int32).pin_memory() for _ in range(W)]
     dev_g = [torch.empty(n, device=dev) for _ in range(W)]
@@ -296,17 +294,22 @@ def e2e(args, dev):
              for w in range(W)]
     dqsum = gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=weights,
                                           stream=stream, prepare=True)
-    up = [torch.cuda.Event() for _ in range(W)]
+    up = [[torch.cuda.Event() for _ in copies] for _ in range(W)]
     used = [torch.cuda.Event() for _ in range(W)]
+    half = n // 2
 
     def step():
+        # each upload is split over two copy streams (two copy engines)
         for w in range(W):
-            copy.wait_event(used[w])          # the previous step's kernel has read dev_g[w]
-            with torch.cuda.stream(copy):
-                dev_g[w].copy_(host_g[w], non_blocking=True)
-            up[w].record(copy)
+            for h, cs in enumerate(copies):
+                cs.wait_event(used[w])        # the previous step's kernel has read dev_g[w]
+                sl = slice(0, half) if h == 0 else slice(half, n)
+                with torch.cuda.stream(cs):
+                    dev_g[w][sl].copy_(host_g[w][sl], non_blocking=True)
+                up[w][h].record(cs)
         for w in range(W):
-            stream.wait_event(up[w])
+            for h in range(len(copies)):
+                stream.wait_event(up[w][h])
             quant[w]()
             used[w].record(stream)
         dqsum()
@@ -321,7 +324,8 @@ def e2e(args, dev):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    copy.wait_event(a)                        # no upload of the timed steps starts early
+    for cs in copies:
+        cs.wait_event(a)                      # no upload of the timed steps starts early
     for _ in range(args.e2e_steps):
         step()
     b.record(stream)
@@ -457,7 +461,7 @@ def rows(args, dev, peak):
         ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         tm = Timer(stream)
-        rounds = 12
+        rounds = 22
         for rd in range(rounds):
             seed_t = gc.saps_round_seed(scfg.base_seed, rd)
             pairs = gc.saps_matching(seed_t, W)
@@ -466,9 +470,14 @@ def rows(args, dev, peak):
                                       prepare=True)
             pa = gc.saps_peer_average(models, vals, idx, cnt, pairs, stream=stream, prepare=True)
             pe = gc.easgd_step(models, scfg.alpha, scfg.beta, center, stream=stream, prepare=True)
+            pf = gc.saps_average_easgd_step(models, vals, cnt, pairs, scfg.alpha, scfg.beta, center, ws,
+                                            stream=stream, prepare=True)
             tm.around("m" + k, pm)
-            tm.around("a" + k, pa)
-            tm.around("e" + k, pe)
+            if rd % 2 == 0:
+                tm.around("a" + k, pa)
+                tm.around("e" + k, pe)
+            else:
+                tm.around("f" + k, pf)
         torch.cuda.synchronize(dev)
         K = int(cnt.item())
         assert int(st.item()) == 0
@@ -478,11 +487,14 @@ def rows(args, dev, peak):
         out[f"{scfg.name}.peer_average"] = _row(scfg.name, "saps_peer_average", (W // 2) * 20 * K,
                                                 tm.ms("a"), peak, None)
         out[f"{scfg.name}.easgd"] = _row(scfg.name, "easgd_step", (2 * W + 2) * 4 * n, tm.ms("e"), peak, W * n)
-        round_ms = [a + b + c for a, b, c in zip(rm, tm.ms("a"), tm.ms("e"))]
-        out[f"{scfg.name}.round"] = {"ms": round(_median(round_ms), 4),
-                                     "bytes": int(4 * K + W * 8 * K + (W // 2) * 20 * K + (2 * W + 2) * 4 * n),
-                                     "frac": round((4 * K + W * 8 * K + (W // 2) * 20 * K + (2 * W + 2) * 4 * n)
-                                                   / (_median(round_ms) * 1e-3) / 1e9 / peak, 3)}
+        out[f"{scfg.name}.average_easgd_fused"] = _row(scfg.name, "saps_average_easgd_step",
+                                                       (2 * W + 2) * 4 * n + W * 4 * K + n // 4,
+                                                       tm.ms("f"), peak, W * n)
+        round_bytes = 4 * K + W * 8 * K + W * 4 * K + (2 * W + 2) * 4 * n + n // 4
+        round_ms = _median(rm) + _median(tm.ms("f"))
+        out[f"{scfg.name}.round"] = {"ms": round(round_ms, 4), "bytes": int(round_bytes),
+                                     "kernels": "saps_mask_compact + saps_average_easgd_step",
+                                     "frac": round(round_bytes / (round_ms * 1e-3) / 1e9 / peak, 3)}
         del models, center, vals, idx
 
     # config 4: CD-SGD, 4 workers x 1.3e9 bf16
@@ -617,7 +629,7 @@ def reference_arm(args, rank, world, pg):
 
 # ----------------------------------------------------------------------------- profiling cases
 
-CASES = ("quantize_f32", "quantize_bf16", "dqsum_sgd", "qsgd_quantize_s7", "qsgd_quantize_s127",
+CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated")
 
 
@@ -637,6 +649,13 @@ def run_case(name: str, n: int):
         r = torch.zeros(n, device=dev)
         c = torch.empty(gc.code_words(n), dtype=torch.int32, device=dev)
         fn = lambda: gc.gc_2bit_quantize(g, r, c, 2e-3)
+    elif name == "quantize_batched":
+        W = 8
+        m = n // W
+        gs = [wl.normal(m, 1e-3, 1 + w, device=dev) for w in range(W)]
+        rs = [torch.zeros(m, device=dev) for _ in range(W)]
+        cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(W)]
+        fn = lambda: gc.gc_2bit_quantize_batched(gs, rs, cs, 2e-3)
     elif name == "dqsum_sgd":
         W = 8
         cs = [torch.randint(-2 ** 31, 2 ** 31 - 1, (gc.code_words(n),), dtype=torch.int32, device=dev)
@@ -658,8 +677,8 @@ def run_case(name: str, n: int):
         nms = [torch.rand(nb, device=dev) for _ in range(W)]
         out = torch.empty(n, device=dev)
         fn = lambda: gc.qsgd_dequant_sum(cs, nms, n, 512, s, 0.25, out)
-    elif name in ("saps_mask", "saps_avg", "easgd"):
-        cfg = wl.scaled(wl.SAPS_P01, n if name != "easgd" else n // 4)
+    elif name in ("saps_mask", "saps_avg", "easgd", "saps_fused"):
+        cfg = wl.scaled(wl.SAPS_P01, n if name not in ("easgd", "saps_fused") else n // 4)
         models = wl.saps_models(cfg, device=dev)
         cap = int(cfg.n * cfg.p * 1.2 + 10_000)
         idx = torch.empty(cap, dtype=torch.int32, device=dev)
@@ -675,6 +694,8 @@ def run_case(name: str, n: int):
             fn = lambda: gc.saps_mask_compact(cfg.n, cfg.p, seed_t, models, idx, vals, cnt, ws, st)
         elif name == "saps_avg":
             fn = lambda: gc.saps_peer_average(models, vals, idx, cnt, pairs)
+        elif name == "saps_fused":
+            fn = lambda: gc.saps_average_easgd_step(models, vals, cnt, pairs, 0.9, 0.9, center, ws)
         else:
             fn = lambda: gc.easgd_step(models, 0.9, 0.9, center)
     elif name == "compensated":
@@ -718,7 +739,7 @@ def main():
     units = W * n * args.steps * world
     value = units * 4 / total_s / 1e9
     q_ms = statistics.mean(h["quantize_ms"])
-    algo_bytes = 12.25 * n
+    algo_bytes = 12.25 * n * W            # one batched launch quantises all W buffers
     achieved = algo_bytes / (q_ms * 1e-3) / 1e9
     line = {
         "metric": HEADLINE_METRIC,
@@ -741,9 +762,9 @@ def main():
         "elements_per_s": round(units / total_s, 1),
         "hbm_frac_step": round((W * 12.25 + (W * 0.25 + 8)) * n / (h["total_ms"] / args.steps * 1e-3) / 1e9
                                / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "gc_2bit_quantize (fp32)",
+        "roofline": {"bound": "hbm", "kernel": "gc_2bit_quantize_batched (fp32, 8 buffers per launch)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic("gc_2bit_quantize_f32"),
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic("gc_2bit_quantize_batched_f32"),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback",
                      "algorithmic_bytes_per_launch": int(algo_bytes),

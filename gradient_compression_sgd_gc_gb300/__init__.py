@@ -8,10 +8,12 @@ no CPU or PyTorch fallback: if the library cannot be built or loaded, every
 call raises.
 
 Entry points (same names as the C ABI):
-  gc_2bit_quantize, gc_2bit_dequant_sum_update, gc_compensated_sum_update,
+  gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update,
+  gc_compensated_sum_update,
   qsgd_quantize, qsgd_dequant_sum,
   saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
-  saps_peer_average, easgd_step, gc_status_string, gc_version
+  saps_peer_average, saps_average_easgd_step, easgd_step, gc_status_string,
+  gc_version
 """
 from __future__ import annotations
 
@@ -27,11 +29,12 @@ __all__ = [
     "GcError", "load", "library_path",
     "GC_OK", "GC_ERR_INVALID", "GC_ERR_ALIGN", "GC_ERR_CUDA", "GC_ERR_CAPACITY", "GC_ERR_TIMEOUT",
     "GC_UPD_NONE", "GC_UPD_SGD", "GC_UPD_EASGD", "GC_MAX_WORKERS",
-    "gc_status_string", "gc_version", "gc_2bit_quantize", "gc_2bit_dequant_sum_update",
+    "gc_status_string", "gc_version", "gc_2bit_quantize", "gc_2bit_quantize_batched",
+    "gc_2bit_dequant_sum_update",
     "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed",
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
-    "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall",
+    "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -70,6 +73,7 @@ def load():
             "gc_status_string": (ctypes.c_char_p, [i32]),
             "gc_version": (i32, []),
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
+            "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
             "gc_2bit_dequant_sum_update": (i32, [vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
             "gc_compensated_sum_update": (i32, [vp, i32, vp, i32, i64, f32, vp, vp]),
             "qsgd_quantize": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
@@ -80,6 +84,7 @@ def load():
             "saps_mask_compact": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz, vp, vp]),
             "saps_peer_average": (i32, [vp, vp, vp, vp, vp, i32, i64, vp]),
             "easgd_step": (i32, [vp, i32, i64, f32, f32, vp, vp]),
+            "saps_average_easgd_step": (i32, [vp, vp, vp, vp, i32, i64, i64, f32, f32, vp, vp, sz, vp]),
             "saps_mask_compact_noalloc": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -189,6 +194,24 @@ def gc_2bit_quantize(grad: torch.Tensor, residual: torch.Tensor, codes: torch.Te
     return _invoke(lib.gc_2bit_quantize, args, "gc_2bit_quantize", prepare, (grad, residual, codes))
 
 
+def gc_2bit_quantize_batched(grads, residuals, codes, threshold: float, stream=None,
+                             prepare: bool = False):
+    """gc_2bit_quantize on B buffers (lists of equal length) in one launch."""
+    lib = load()
+    B = len(grads)
+    if not (len(residuals) == len(codes) == B) or B == 0:
+        raise ValueError("grads, residuals and codes must be non-empty lists of equal length")
+    dt = _gdtype(grads[0])
+    ns = [g.numel() for g in grads]
+    n_arr = (ctypes.c_int64 * B)(*ns)
+    args = (_ptrs(grads, "grads", grads[0].dtype),
+            dt, (ctypes.c_void_p * B)(*[_dev(r, f"residuals[{i}]", torch.float32, ns[i]) for i, r in enumerate(residuals)]),
+            (ctypes.c_void_p * B)(*[_dev(c, f"codes[{i}]", torch.int32, code_words(ns[i])) for i, c in enumerate(codes)]),
+            n_arr, B, float(threshold), _stream(stream, grads[0]))
+    return _invoke(lib.gc_2bit_quantize_batched, args, "gc_2bit_quantize_batched", prepare,
+                   (list(grads), list(residuals), list(codes), n_arr))
+
+
 def gc_2bit_dequant_sum_update(codes, n: int, threshold: float, kind: int = GC_UPD_NONE,
                                lr: float = 0.0, alpha: float = 0.0, center=None, weights=None,
                                out=None, stream=None, prepare: bool = False):
@@ -285,6 +308,24 @@ def saps_peer_average(models, vals, idx: torch.Tensor, d_count: torch.Tensor, pa
             pairs_arr, W, capacity, _stream(stream, idx))
     return _invoke(lib.saps_peer_average, args, "saps_peer_average", prepare,
                    (list(models), list(vals), idx, d_count))
+
+
+def saps_average_easgd_step(models, vals, d_count: torch.Tensor, pairs, alpha: float, beta: float,
+                            center: torch.Tensor, workspace: torch.Tensor, stream=None,
+                            prepare: bool = False):
+    """saps_peer_average + easgd_step in one pass; ``workspace`` must be the one
+    the preceding saps_mask_compact used."""
+    lib = load()
+    W = len(models)
+    n = center.numel()
+    capacity = vals[0].numel() if vals else 0
+    pairs_arr = (ctypes.c_int * W)(*[int(p) for p in pairs])
+    args = (_ptrs(models, "models", torch.float32, n), _ptrs(vals, "vals", torch.float32, capacity),
+            _dev(d_count, "d_count", torch.int64, 1), pairs_arr, W, n, capacity, float(alpha),
+            float(beta), _dev(center, "center", torch.float32, n),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream, center))
+    return _invoke(lib.saps_average_easgd_step, args, "saps_average_easgd_step", prepare,
+                   (list(models), list(vals), d_count, center, workspace, pairs_arr))
 
 
 def easgd_step(models, alpha: float, beta: float, center: torch.Tensor, stream=None,

@@ -57,12 +57,15 @@ struct MaskArgs {
     uint64_t* state;             // per-tile look-back state (workspace)
     int64_t ntiles;
     int* d_status;
+    uint32_t* group_mask = nullptr;  // per 32 elements: the mask bits (workspace), or null
+    uint32_t* group_excl = nullptr;  // per 32 elements: masked entries before them, or null
 };
 
 // Exclusive prefix of tile `tile` whose own count is `agg`; run by one warp.
-// Publishes (aggregate) first, then walks back 32 predecessors at a time.
-// Every wait is bounded: after kWaitLimitNs the missing predecessors count
-// as zero and GC_ERR_TIMEOUT is recorded.
+// Publishes (aggregate) first, then walks back over its predecessors 128 at a
+// time (4 state words per lane) until it meets one that has published its
+// inclusive prefix.  Every wait is bounded: after kWaitLimitNs the missing
+// predecessors count as zero and GC_ERR_TIMEOUT is recorded.
 __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
     if (tile == 0) {
         if (lane == 0) st_release(a.state, kFlagPrefix | agg);
@@ -74,31 +77,52 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
     const uint64_t t0 = global_ns();
     bool timed_out = false;
     while (true) {
-        const int64_t j = end - lane;
-        uint64_t st = j >= 0 ? ld_acquire(a.state + j) : kFlagPrefix;
-        unsigned ns = 32;
+        // state of predecessor end - (4 * lane + q), q = 0..3
+        uint64_t st[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t j = end - (4 * lane + q);
+            st[q] = j >= 0 ? ld_acquire(a.state + j) : kFlagPrefix;
+        }
+        unsigned polls = 0;
         while (true) {
-            const bool pending = (st >> 62) == 0;
+            bool pending = false;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) pending |= (st[q] >> 62) == 0;
             if (!__any_sync(0xffffffffu, pending)) break;
             // lane 0's clock decides, so the whole warp leaves together
             const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs, 0);
             if (expired) {
                 timed_out = true;
-                if (pending) st = kFlagAgg;   // unknown predecessor counts as 0
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if ((st[q] >> 62) == 0) st[q] = kFlagAgg;   // unknown predecessor counts as 0
                 break;
             }
-            __nanosleep(ns);
-            if (ns < 1024) ns <<= 1;
-            if (pending) st = ld_acquire(a.state + j);
+            if (++polls > 8) __nanosleep(polls < 64 ? 64 : 512);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t j = end - (4 * lane + q);
+                if ((st[q] >> 62) == 0) st[q] = ld_acquire(a.state + j);
+            }
         }
-        const unsigned prefix_lanes = __ballot_sync(0xffffffffu, (st >> 62) == 2);
-        const int last = prefix_lanes ? __ffs(prefix_lanes) - 1 : 31;
-        uint64_t v = lane <= last ? (st & kValueMask) : 0;
+        // closest predecessor with a prefix: first lane that has one, then its first q
+        int myq = 4;
+#pragma unroll
+        for (int q = 3; q >= 0; --q)
+            if ((st[q] >> 62) == 2) myq = q;
+        const unsigned lanes = __ballot_sync(0xffffffffu, myq < 4);
+        const int f = lanes ? __ffs(lanes) - 1 : 32;
+        const int fq = lanes ? __shfl_sync(0xffffffffu, myq, f) : 4;
+        uint64_t v = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (lane < f || (lane == f && q <= fq)) v += st[q] & kValueMask;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         excl += v;
-        if (prefix_lanes) break;
-        end -= 32;
+        if (lanes) break;
+        end -= 128;
     }
     if (lane == 0) {
         st_release(a.state + tile, kFlagPrefix | (excl + agg));
@@ -112,7 +136,9 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
 // elements tile*4096 + 512w + 32r + lane (r < 16) and keeps the ballot of
 // round r in lane r.  After the scan the CTA lists its masked indices in
 // shared memory and writes idx[] and every worker's vals[] with coalesced
-// stores.
+// stores.  When the workspace has room it also records, per 32 elements,
+// the mask bits and the number of masked entries before them, which the
+// fused pair-average + elastic step uses to find each entry's rank.
 __global__ void __launch_bounds__(kThreads)
 k_saps_mask_compact(const MaskArgs a) {
     __shared__ uint32_t s_list[kTileElems];
@@ -167,7 +193,17 @@ k_saps_mask_compact(const MaskArgs a) {
     __syncthreads();
 
     const uint32_t wex = s_warp_excl[wib];
+    const uint64_t excl = s_excl;
+    const uint32_t agg = s_agg;
     const uint32_t lt = (1u << lane) - 1u;
+    // per 32-element group: mask bits and the masked count before the group
+    if (a.group_mask != nullptr && lane < kItems) {
+        const int64_t g = (wbase >> 5) + lane;
+        if (g * 32 < a.n) {
+            a.group_mask[g] = my_mask;
+            a.group_excl[g] = static_cast<uint32_t>(excl + wex + round_excl);
+        }
+    }
 #pragma unroll 4
     for (int r = 0; r < kItems; ++r) {
         const uint32_t m = __shfl_sync(0xffffffffu, my_mask, r);
@@ -176,25 +212,16 @@ k_saps_mask_compact(const MaskArgs a) {
     }
     __syncthreads();
 
-    const uint64_t excl = s_excl;
-    const uint32_t agg = s_agg;
-    for (uint32_t k = threadIdx.x; k < agg; k += kThreads) {
-        const uint64_t pos = excl + k;
-        if (pos >= static_cast<uint64_t>(a.capacity)) break;
-        const uint32_t e = s_list[k];
-        a.idx[pos] = e;
-        int w = 0;
-        for (; w + 4 <= a.W; w += 4) {
-            const float v0 = __ldg(a.models.p[w] + e);
-            const float v1 = __ldg(a.models.p[w + 1] + e);
-            const float v2 = __ldg(a.models.p[w + 2] + e);
-            const float v3 = __ldg(a.models.p[w + 3] + e);
-            a.vals.p[w][pos] = v0;
-            a.vals.p[w + 1][pos] = v1;
-            a.vals.p[w + 2][pos] = v2;
-            a.vals.p[w + 3][pos] = v3;
-        }
-        for (; w < a.W; ++w) a.vals.p[w][pos] = __ldg(a.models.p[w] + e);
+    // indices, then one (entry, worker) pair per thread so that every random
+    // read of the gather is in flight at once; stores stay coalesced per worker
+    const uint32_t kept = static_cast<uint64_t>(a.capacity) > excl
+        ? static_cast<uint32_t>(min(static_cast<uint64_t>(agg), static_cast<uint64_t>(a.capacity) - excl)) : 0u;
+    for (uint32_t k = threadIdx.x; k < kept; k += kThreads) a.idx[excl + k] = s_list[k];
+    const uint32_t pairs = kept * static_cast<uint32_t>(a.W);
+    for (uint32_t q = threadIdx.x; q < pairs; q += kThreads) {
+        const uint32_t w = q / kept;
+        const uint32_t k = q - w * kept;
+        a.vals.p[w][excl + k] = __ldg(a.models.p[w] + s_list[k]);
     }
     if (threadIdx.x == 0 && tile == a.ntiles - 1) {
         const uint64_t total = excl + agg;
@@ -309,6 +336,141 @@ k_easgd_wide(const EasgdArgs a) {
 
 int64_t mask_tiles(int64_t n) { return (n + kTileElems - 1) / kTileElems; }
 
+// 32-element groups of n, rounded up to a multiple of 4 (16-byte alignment).
+int64_t ws_groups(int64_t n) { return ((n + 31) / 32 + 3) / 4 * 4; }
+
+uint32_t* ws_group_mask(void* ws, int64_t n) {
+    return reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + kWsHeader + sizeof(uint64_t) * mask_tiles(n));
+}
+
+uint32_t* ws_group_excl(void* ws, int64_t n) { return ws_group_mask(ws, n) + ws_groups(n); }
+
+// ------------------------------------------------------------------ K7 + K8 fused
+
+// SAPS pair averaging applied inside the EASGD pass.  The peers' values come
+// from the compacted payload vals[w][rank]; the rank of a masked element is
+// found from the per-32-element tables saps_mask_compact leaves in the
+// workspace (mask bits + masked entries before the group), so the models are
+// streamed once and never written at scattered addresses.  Worker w's
+// masked coordinate becomes (x_w + received x_partner) * 0.5 -- the same
+// value saps_peer_average writes -- and the elastic step then runs on it.
+struct FusedArgs {
+    PtrTable<float*> models;
+    PtrTable<const float*> vals;
+    int partner[GC_MAX_WORKERS];
+    int W;
+    int64_t n;
+    float alpha, beta, inv_w;
+    float* center;
+    const uint32_t* group_mask;
+    const uint32_t* group_excl;
+    const uint64_t* d_count;
+    int64_t capacity;
+};
+
+template <int MAXW>
+__global__ void __launch_bounds__(kThreads, 2)
+k_saps_average_easgd(const FusedArgs a) {
+    const uint64_t cnt = *a.d_count;
+    const uint64_t usable = cnt < static_cast<uint64_t>(a.capacity) ? cnt : static_cast<uint64_t>(a.capacity);
+    const int64_t nv = a.n >> 2;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < nv) {
+        float4 m[MAXW];
+#pragma unroll
+        for (int k = 0; k < MAXW; ++k)
+            if (k < a.W) m[k] = ld_f4(a.models.p[k] + 4 * i);
+        const float4 c = ld_f4(a.center + 4 * i);
+        const int64_t g = (4 * i) >> 5;
+        const uint32_t sh = static_cast<uint32_t>((4 * i) & 31);
+        const uint32_t gm = __ldg(a.group_mask + g);
+        const uint32_t bits = (gm >> sh) & 15u;
+        if (bits) {
+            const uint32_t base = __ldg(a.group_excl + g) + __popc(gm & ((1u << sh) - 1u));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (!((bits >> e) & 1u)) continue;
+                const uint32_t rank = base + __popc(bits & ((1u << e) - 1u));
+                if (rank >= usable) continue;
+                float recv[MAXW];
+#pragma unroll
+                for (int k = 0; k < MAXW; ++k)
+                    if (k < a.W) recv[k] = __ldg(a.vals.p[a.partner[k]] + rank);
+#pragma unroll
+                for (int k = 0; k < MAXW; ++k) {
+                    if (k < a.W) {
+                        float* x = e == 0 ? &m[k].x : e == 1 ? &m[k].y : e == 2 ? &m[k].z : &m[k].w;
+                        *x = __fmul_rn(__fadd_rn(*x, recv[k]), 0.5f);
+                    }
+                }
+            }
+        }
+        float4 sum = m[0];
+#pragma unroll
+        for (int k = 1; k < MAXW; ++k)
+            if (k < a.W) sum = f4_add(sum, m[k]);
+#pragma unroll
+        for (int k = 0; k < MAXW; ++k) {
+            if (k < a.W) {
+                st_stream_f4(a.models.p[k] + 4 * i,
+                             make_float4(elastic(m[k].x, c.x, a.alpha), elastic(m[k].y, c.y, a.alpha),
+                                         elastic(m[k].z, c.z, a.alpha), elastic(m[k].w, c.w, a.alpha)));
+            }
+        }
+        const float4 mean = make_float4(__fmul_rn(sum.x, a.inv_w), __fmul_rn(sum.y, a.inv_w),
+                                        __fmul_rn(sum.z, a.inv_w), __fmul_rn(sum.w, a.inv_w));
+        st_stream_f4(a.center + 4 * i,
+                     make_float4(fmaf(a.beta, __fsub_rn(mean.x, c.x), c.x), fmaf(a.beta, __fsub_rn(mean.y, c.y), c.y),
+                                 fmaf(a.beta, __fsub_rn(mean.z, c.z), c.z), fmaf(a.beta, __fsub_rn(mean.w, c.w), c.w)));
+    } else if (i == nv && (a.n & 3)) {
+        // the last n % 4 elements, one thread
+        for (int64_t t = nv << 2; t < a.n; ++t) {
+            const uint32_t gm = __ldg(a.group_mask + (t >> 5));
+            const uint32_t sh = static_cast<uint32_t>(t & 31);
+            const bool hit = (gm >> sh) & 1u;
+            const uint32_t rank = __ldg(a.group_excl + (t >> 5)) + __popc(gm & ((1u << sh) - 1u));
+            float v[GC_MAX_WORKERS];
+            for (int k = 0; k < a.W; ++k) v[k] = a.models.p[k][t];
+            if (hit && rank < usable)
+                for (int k = 0; k < a.W; ++k) v[k] = __fmul_rn(__fadd_rn(v[k], a.vals.p[a.partner[k]][rank]), 0.5f);
+            const float c = a.center[t];
+            float sum = 0.0f;
+            for (int k = 0; k < a.W; ++k) sum = __fadd_rn(sum, v[k]);
+            for (int k = 0; k < a.W; ++k) a.models.p[k][t] = elastic(v[k], c, a.alpha);
+            a.center[t] = fmaf(a.beta, __fsub_rn(__fmul_rn(sum, a.inv_w), c), c);
+        }
+    }
+}
+
+// Any W <= 64: one element per thread, models read twice.
+__global__ void __launch_bounds__(kThreads)
+k_saps_average_easgd_wide(const FusedArgs a) {
+    const uint64_t cnt = *a.d_count;
+    const uint64_t usable = cnt < static_cast<uint64_t>(a.capacity) ? cnt : static_cast<uint64_t>(a.capacity);
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= a.n) return;
+    const uint32_t gm = __ldg(a.group_mask + (t >> 5));
+    const uint32_t sh = static_cast<uint32_t>(t & 31);
+    const bool hit = (gm >> sh) & 1u;
+    const uint32_t rank = __ldg(a.group_excl + (t >> 5)) + __popc(gm & ((1u << sh) - 1u));
+    const bool avg = hit && rank < usable;
+    const float c = a.center[t];
+    float sum = 0.0f;
+    for (int k = 0; k < a.W; ++k) {
+        float v = a.models.p[k][t];
+        if (avg) v = __fmul_rn(__fadd_rn(v, a.vals.p[a.partner[k]][rank]), 0.5f);
+        sum = __fadd_rn(sum, v);
+    }
+    for (int k = 0; k < a.W; ++k) {
+        float v = a.models.p[k][t];
+        if (avg) v = __fmul_rn(__fadd_rn(v, a.vals.p[a.partner[k]][rank]), 0.5f);
+        a.models.p[k][t] = elastic(v, c, a.alpha);
+    }
+    a.center[t] = fmaf(a.beta, __fsub_rn(__fmul_rn(sum, a.inv_w), c), c);
+}
+
+
+
 }  // namespace
 }  // namespace gc
 
@@ -333,7 +495,10 @@ int saps_matching(uint64_t seed_t, int W, int* pairs_out) {
 
 size_t saps_workspace_bytes(int64_t n) {
     if (n <= 0) return kWsHeader;
-    return kWsHeader + sizeof(uint64_t) * static_cast<size_t>(mask_tiles(n));
+    // header | tile states (8 B per tile) | group mask (4 B per 32 elements) |
+    // group exclusive counts (4 B per 32 elements), each part 16-byte aligned
+    return kWsHeader + sizeof(uint64_t) * static_cast<size_t>(mask_tiles(n)) +
+           2 * sizeof(uint32_t) * static_cast<size_t>(ws_groups(n));
 }
 
 int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* models, int W,
@@ -369,7 +534,13 @@ int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* 
     a.state = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + kWsHeader);
     a.ntiles = mask_tiles(n);
     a.d_status = d_status;
-    if (cudaMemsetAsync(workspace, 0, saps_workspace_bytes(n), s) != cudaSuccess) return GC_ERR_CUDA;
+    a.group_mask = ws_group_mask(workspace, n);
+    a.group_excl = ws_group_excl(workspace, n);
+    // the counter and look-back states must start at zero; the group tables
+    // are written in full by the kernel
+    if (cudaMemsetAsync(workspace, 0, kWsHeader + sizeof(uint64_t) * static_cast<size_t>(a.ntiles), s) !=
+        cudaSuccess)
+        return GC_ERR_CUDA;
     k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles), kThreads, 0, s>>>(a);
     return launch_status();
 }
@@ -403,6 +574,60 @@ int saps_peer_average(float* const* models, const float* const* vals, const uint
     const int64_t need = (capacity + kThreads - 1) / kThreads;
     if (need < grid) grid = static_cast<int>(need);
     k_saps_peer_average<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return launch_status();
+}
+
+int saps_average_easgd_step(float* const* models, const float* const* vals, const uint64_t* d_count,
+                            const int* pairs, int W, int64_t n, int64_t capacity, float alpha, float beta,
+                            float* center, const void* workspace, size_t workspace_bytes,
+                            gc_stream_t stream) {
+    if (n < 0 || n > 0xFFFFFFFFll || W < 2 || W > GC_MAX_WORKERS || (W & 1) || capacity < 0 ||
+        !isfinite(alpha) || !isfinite(beta))
+        return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!models || !pairs || !d_count || !center || !workspace || (capacity > 0 && !vals))
+        return GC_ERR_INVALID;
+    if (workspace_bytes < saps_workspace_bytes(n)) return GC_ERR_INVALID;
+    if (!aligned16(center) || !aligned16(workspace)) return GC_ERR_ALIGN;
+    FusedArgs a;
+    bool seen[GC_MAX_WORKERS] = {false};
+    for (int w = 0; w < W; ++w) {
+        const int q = pairs[w];
+        if (q < 0 || q >= W || seen[q]) return GC_ERR_INVALID;
+        seen[q] = true;
+    }
+    for (int q = 0; q < W / 2; ++q) {
+        a.partner[pairs[2 * q]] = pairs[2 * q + 1];
+        a.partner[pairs[2 * q + 1]] = pairs[2 * q];
+    }
+    for (int w = 0; w < W; ++w) {
+        if (!models[w] || (capacity > 0 && !vals[w])) return GC_ERR_INVALID;
+        if (!aligned16(models[w]) || (capacity > 0 && !aligned16(vals[w]))) return GC_ERR_ALIGN;
+        a.models.p[w] = models[w];
+        a.vals.p[w] = capacity > 0 ? vals[w] : nullptr;
+    }
+    a.W = W;
+    a.n = n;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.inv_w = static_cast<float>(1.0 / W);
+    a.center = center;
+    void* ws = const_cast<void*>(workspace);
+    a.group_mask = ws_group_mask(ws, n);
+    a.group_excl = ws_group_excl(ws, n);
+    a.d_count = d_count;
+    a.capacity = capacity;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (W <= 16) {
+        const unsigned grid = static_cast<unsigned>(((n >> 2) + 1 + kThreads - 1) / kThreads);
+        if (W <= 4)
+            k_saps_average_easgd<4><<<grid, kThreads, 0, s>>>(a);
+        else
+            k_saps_average_easgd<16><<<grid, kThreads, 0, s>>>(a);
+    } else {
+        const unsigned grid = static_cast<unsigned>((n + kThreads - 1) / kThreads);
+        k_saps_average_easgd_wide<<<grid, kThreads, 0, s>>>(a);
+    }
     return launch_status();
 }
 

@@ -138,6 +138,91 @@ k_2bit_quantize_bf16(const uint16_t* __restrict__ g, float* __restrict__ r,
     }
 }
 
+// ------------------------------------------------------------------ K1, batched
+
+// B gradient buffers (workers, or the gradient tensors of one worker) of
+// possibly different sizes quantised by one launch: the grid covers the
+// concatenation of every buffer's 512-element tiles, and each warp finds its
+// buffer in the tile prefix table.
+struct BatchArgs {
+    PtrTable<const void*> grads;
+    PtrTable<float*> res;
+    PtrTable<uint32_t*> codes;
+    int64_t n[GC_MAX_WORKERS];
+    int64_t tile_start[GC_MAX_WORKERS + 1];
+    int B;
+    float t;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads)
+k_2bit_quantize_batched(const BatchArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t T = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (T >= a.tile_start[a.B]) return;
+    int lo = 0, hi = a.B - 1;           // last b with tile_start[b] <= T
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.tile_start[mid] <= T) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int64_t tile = T - a.tile_start[b];
+    const int64_t n = a.n[b];
+    float* __restrict__ r = a.res.p[b];
+    const float t = a.t;
+    const int64_t nfull = n / kTile;
+    if (!BF16) {
+        const float* __restrict__ g = static_cast<const float*>(a.grads.p[b]);
+        uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[b]);
+        if (tile < nfull) {
+            const int64_t base = tile * kTile + 4 * lane;
+            float4 gv[4], rv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                gv[j] = ld_stream_f4(g + base + 128 * j);
+                rv[j] = ld_f4(r + base + 128 * j);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t c = quantize4(rv[j], gv[j], t);
+                st_stream_f4(r + base + 128 * j, rv[j]);
+                cb[code_byte(base + 128 * j)] = static_cast<uint8_t>(c);
+            }
+        } else {
+            quantize_tail([g](int64_t e) { return g[e]; }, r, cb, nfull * kTile, n, t, lane);
+        }
+    } else {
+        const uint16_t* __restrict__ g = static_cast<const uint16_t*>(a.grads.p[b]);
+        uint16_t* ch = reinterpret_cast<uint16_t*>(a.codes.p[b]);
+        if (tile < nfull) {
+            const int64_t base = tile * kTile + 8 * lane;
+            uint4 gv[2];
+            float4 rv[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                gv[j] = ld_stream_u4(g + base + 256 * j);
+                rv[2 * j] = ld_f4(r + base + 256 * j);
+                rv[2 * j + 1] = ld_f4(r + base + 256 * j + 4);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float4 g0 = make_float4(bf16lo(gv[j].x), bf16hi(gv[j].x),
+                                              bf16lo(gv[j].y), bf16hi(gv[j].y));
+                const float4 g1 = make_float4(bf16lo(gv[j].z), bf16hi(gv[j].z),
+                                              bf16lo(gv[j].w), bf16hi(gv[j].w));
+                const uint32_t c = (quantize4(rv[2 * j], g0, t) << 8) | quantize4(rv[2 * j + 1], g1, t);
+                st_stream_f4(r + base + 256 * j, rv[2 * j]);
+                st_stream_f4(r + base + 256 * j + 4, rv[2 * j + 1]);
+                const int64_t e = base + 256 * j;
+                ch[2 * (e >> 4) + 1 - ((e >> 3) & 1)] = static_cast<uint16_t>(c);
+            }
+        } else {
+            quantize_tail([g](int64_t e) { return __uint_as_float(static_cast<uint32_t>(g[e]) << 16); },
+                          r, reinterpret_cast<uint8_t*>(a.codes.p[b]), nfull * kTile, n, t, lane);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ K2
 
 // Maps a code word to per-field (value + 1): 11 -> 2, 10 -> 0, 00/01 -> 1.
@@ -435,6 +520,38 @@ int gc_2bit_quantize(const void* grad, gc_dtype dtype, float* residual, uint32_t
     else
         k_2bit_quantize_bf16<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(grad), residual,
                                                        codes, n, threshold);
+    return launch_status();
+}
+
+int gc_2bit_quantize_batched(const void* const* grads, gc_dtype dtype, float* const* residuals,
+                             uint32_t* const* codes, const int64_t* n, int B, float threshold,
+                             gc_stream_t stream) {
+    if (B < 1 || B > GC_MAX_WORKERS || !finite_pos(threshold) || (dtype != GC_F32 && dtype != GC_BF16))
+        return GC_ERR_INVALID;
+    if (!grads || !residuals || !codes || !n) return GC_ERR_INVALID;
+    BatchArgs a;
+    a.B = B;
+    a.t = threshold;
+    a.tile_start[0] = 0;
+    for (int b = 0; b < B; ++b) {
+        if (n[b] < 0) return GC_ERR_INVALID;
+        if (n[b] > 0) {
+            if (!grads[b] || !residuals[b] || !codes[b]) return GC_ERR_INVALID;
+            if (!aligned16(grads[b]) || !aligned16(residuals[b]) || !aligned16(codes[b])) return GC_ERR_ALIGN;
+        }
+        a.grads.p[b] = grads[b];
+        a.res.p[b] = residuals[b];
+        a.codes.p[b] = codes[b];
+        a.n[b] = n[b];
+        a.tile_start[b + 1] = a.tile_start[b] + (n[b] + 511) / 512;
+    }
+    if (a.tile_start[B] == 0) return GC_OK;
+    const unsigned grid = blocks_for_tiles(a.tile_start[B]);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == GC_F32)
+        k_2bit_quantize_batched<false><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_2bit_quantize_batched<true><<<grid, kThreads, 0, s>>>(a);
     return launch_status();
 }
 

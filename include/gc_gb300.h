@@ -108,6 +108,23 @@ GC_API int gc_2bit_quantize(const void *grad, gc_dtype dtype, float *residual,
                      gc_stream_t stream);
 
 /*
+ * gc_2bit_quantize_batched -- gc_2bit_quantize on B buffers in one launch
+ * (the W workers held on this GPU, or the many gradient tensors of one
+ * worker); same rule, layout and residual update per buffer.
+ *
+ *   grads      host array of B device pointers, n[b] elements of `dtype`
+ *   residuals  host array of B device pointers, fp32 [n[b]], in/out
+ *   codes      host array of B device pointers, uint32 [ceil(n[b]/16)]
+ *   n          host array of B sizes (0 allowed: that buffer is skipped)
+ *   B          1 .. GC_MAX_WORKERS
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_quantize_batched(const void *const *grads, gc_dtype dtype,
+                                    float *const *residuals, uint32_t *const *codes,
+                                    const int64_t *n, int B, float threshold,
+                                    gc_stream_t stream);
+
+/*
  * gc_2bit_dequant_sum_update -- MXNet PR #8662 "Local kvstore" / "Dist
  * kvstore" (the receiver dequantises every worker's codes, 11 -> +t,
  * 10 -> -t, 00 and 01 -> 0, and sums them); CD-SGD eq. 10 (global update
@@ -241,7 +258,9 @@ GC_API size_t saps_workspace_bytes(int64_t n);
  *   d_count    device uint64, written with the number of masked entries
  *              (also when it exceeds capacity)
  *   workspace  device, saps_workspace_bytes(n) bytes, 16-byte aligned; the
- *              call clears it on `stream` before use
+ *              call clears the part that must start at zero on `stream`,
+ *              and leaves per-32-element mask tables there for
+ *              saps_average_easgd_step
  *   d_status   device int; set to GC_ERR_CAPACITY when the count exceeds
  *              capacity (only `capacity` entries are written) and to
  *              GC_ERR_TIMEOUT if a look-back wait ran out (about one
@@ -272,6 +291,26 @@ GC_API int saps_peer_average(float *const *models, const float *const *vals,
                       const uint32_t *idx, const uint64_t *d_count,
                       const int *pairs, int W, int64_t capacity,
                       gc_stream_t stream);
+
+/*
+ * saps_average_easgd_step -- saps_peer_average followed by easgd_step, in one
+ * pass over the models (SAPS Algorithm 2 lines 9-10, then the EASGD
+ * updates).  The received peer values are read from the compacted payload
+ * vals[w][rank]; the rank of each masked coordinate comes from tables that
+ * saps_mask_compact leaves in `workspace`, so the workspace must be the one
+ * the preceding saps_mask_compact call (same n, same stream order) used.
+ * Results are bit-identical to calling saps_peer_average then easgd_step.
+ *
+ *   models, vals, d_count, pairs, capacity   as saps_peer_average
+ *   n, alpha, beta, center                   as easgd_step
+ *   workspace                                as passed to saps_mask_compact
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int saps_average_easgd_step(float *const *models, const float *const *vals,
+                                   const uint64_t *d_count, const int *pairs, int W,
+                                   int64_t n, int64_t capacity, float alpha,
+                                   float beta, float *center, const void *workspace,
+                                   size_t workspace_bytes, gc_stream_t stream);
 
 /*
  * easgd_step -- EASGD local and global updates (IMerge design notes,

@@ -149,3 +149,37 @@ def test_matching_rejects_bad_w():
     for W in (0, 1, 3, 66):
         with pytest.raises(gc.GcError):
             gc.saps_matching(1, W)
+
+
+def test_batched_quantize_validation():
+    f = "gc_2bit_quantize_batched"
+    two = (ctypes.c_int64 * 2)(10, 20)
+    p2 = _ptrs(FAKE, FAKE)
+    assert _call(f, p2, 0, p2, p2, two, 0, 0.5, None) == gc.GC_ERR_INVALID           # B = 0
+    assert _call(f, p2, 0, p2, p2, two, 65, 0.5, None) == gc.GC_ERR_INVALID          # B > 64
+    assert _call(f, p2, 0, p2, p2, two, 2, 0.0, None) == gc.GC_ERR_INVALID           # threshold
+    assert _call(f, p2, 0, p2, p2, (ctypes.c_int64 * 2)(10, -1), 2, 0.5, None) == gc.GC_ERR_INVALID
+    assert _call(f, _ptrs(FAKE, MISALIGNED), 0, p2, p2, two, 2, 0.5, None) == gc.GC_ERR_ALIGN
+    assert _call(f, _ptrs(FAKE, 0), 0, p2, p2, two, 2, 0.5, None) == gc.GC_ERR_INVALID
+    # every buffer empty: a no-op that never touches the (null) pointers
+    assert _call(f, _ptrs(0, 0), 0, _ptrs(0, 0), _ptrs(0, 0), (ctypes.c_int64 * 2)(0, 0), 2, 0.5,
+                 None) == gc.GC_OK
+
+
+def test_fused_average_easgd_validation():
+    f = "saps_average_easgd_step"
+    ws = gc.saps_workspace_bytes(1000)
+    p4 = _ptrs(FAKE, FAKE, FAKE, FAKE)
+    good = (ctypes.c_int * 4)(2, 0, 3, 1)
+    ok = [p4, p4, FAKE, good, 4, 1000, 100, 0.9, 0.9, FAKE, FAKE, ws, None]
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return _call(f, *a)
+    assert with_(3, (ctypes.c_int * 4)(0, 0, 1, 2)) == gc.GC_ERR_INVALID    # not a permutation
+    assert with_(4, 3) == gc.GC_ERR_INVALID                                 # odd W
+    assert with_(11, ws - 1) == gc.GC_ERR_INVALID                           # workspace too small
+    assert with_(9, MISALIGNED) == gc.GC_ERR_ALIGN                          # center
+    assert with_(7, float("nan")) == gc.GC_ERR_INVALID
+    assert with_(5, 0) == gc.GC_OK                                          # n == 0 no-op

@@ -157,3 +157,56 @@ def test_easgd_step_parity(W, n):
     for w in range(W):
         assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w}")
     assert_close(host_f32(center), rc, scale, what="center")
+
+
+@pytest.mark.parametrize("W", [2, 4, 16, 18])
+@pytest.mark.parametrize("n,p,cap", [(1, 0.5, None), (33, 0.5, None), (4097, 0.01, None),
+                                     (100_003, 0.01, None), (100_003, 0.3, 5000)])
+def test_fused_average_easgd_is_bitwise_the_two_calls(W, n, p, cap):
+    """saps_average_easgd_step == saps_peer_average then easgd_step, bit for
+    bit, including a capacity overflow (entries beyond capacity not averaged)."""
+    capacity = cap or n
+    base = [wl.normal(n, 0.05, 900 + w, device=DEV) for w in range(W)]
+    c0 = wl.saps_initial_center(base)
+    ma = [b.clone() for b in base]
+    mb = [b.clone() for b in base]
+    ca, cb = c0.clone(), c0.clone()
+    seed_t = gc.saps_round_seed(11, n)
+    pairs = gc.saps_matching(seed_t, W)
+    comp = Compactor(n, W, capacity)
+    comp.run(p, seed_t, ma)
+    vals = [v[:capacity] for v in comp.vals]
+    gc.saps_peer_average(ma, vals, comp.idx[:capacity], comp.count[:1], pairs)
+    gc.easgd_step(ma, 0.9, 0.7, ca)
+    gc.saps_average_easgd_step(mb, vals, comp.count[:1], pairs, 0.9, 0.7, cb, comp.ws)
+    torch.cuda.synchronize()
+    for w in range(W):
+        assert torch.equal(ma[w].view(torch.int32), mb[w].view(torch.int32)), f"worker {w}"
+    assert torch.equal(ca.view(torch.int32), cb.view(torch.int32))
+
+
+def test_saps_rounds_chain_fused():
+    """Six SAPS rounds with the fused pair-average + elastic step against the
+    oracle's fp64 chain."""
+    n, W, p, alpha, beta = 150_011, 16, 0.01, 0.9, 0.9
+    cfg = wl.scaled(wl.SAPS_P01, n)
+    models = wl.saps_models(cfg, device=DEV)
+    center = wl.saps_initial_center(models)
+    ref = [host_f32(m).astype(np.float64) for m in models]
+    rc = host_f32(center).astype(np.float64)
+    comp = Compactor(n, W, n)
+    scale = np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc)
+    for t in range(6):
+        seed_t = gc.saps_round_seed(cfg.base_seed, t)
+        pairs = gc.saps_matching(seed_t, W)
+        comp.run(p, seed_t, models)
+        gc.saps_average_easgd_step(models, [v[:n] for v in comp.vals], comp.count[:1], pairs, alpha, beta,
+                                   center, comp.ws)
+        rK, ridx, rvals = oracle.saps_mask_compact(n, p, seed_t, ref)
+        oracle.saps_peer_average(ref, rvals, ridx, np.array(pairs, np.int32))
+        oracle.easgd_step(ref, alpha, beta, rc)
+        torch.cuda.synchronize()
+        scale = np.maximum(scale, np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc))
+        for w in range(W):
+            assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w} round {t}")
+        assert_close(host_f32(center), rc, scale, what=f"center round {t}")

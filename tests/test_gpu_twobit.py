@@ -46,9 +46,9 @@ def test_quantize_bit_exact_over_steps(n, dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_quantize_many_tiles_per_warp(dtype):
-    """Larger than one tile per resident warp, so the grid-stride loop runs
-    several iterations per warp; ragged tail of 23 elements."""
+def test_quantize_many_tiles(dtype):
+    """10,240 full tiles (many more than there are resident warps) and a
+    ragged tail of 23 elements."""
     n = 5 * 1024 * 1024 + 23
     t = 1e-3
     r = torch.zeros(n, dtype=torch.float32, device=DEV)
@@ -207,3 +207,68 @@ def test_cdsgd_chain_k4(n, dtype):
         for q in range(W):
             np.testing.assert_array_equal(host_f32(res[q]).view(np.uint32), res_ref[q].view(np.uint32))
         assert_close(host_f32(w), w_ref, scale, what=f"weights step {step}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_batched_quantize_matches_oracle(dtype):
+    """Buffers of different sizes (ragged tails, an empty one, several tiles)
+    quantised by one launch, over three steps."""
+    sizes = [100_003, 0, 1, 512, 4097, 1_000_000, 17]
+    t = 0.5
+    res = [guarded(n, torch.float32) for n in sizes]
+    for r, n in zip(res, sizes):
+        r[:n].zero_()
+    codes = [guarded(gc.code_words(n), torch.int32) for n in sizes]
+    r_ref = [np.zeros(n, np.float32) for n in sizes]
+    for step in range(3):
+        grads = [wl.normal(n, 0.7, seed=500 + 10 * step + b, device=DEV, dtype=dtype)
+                 for b, n in enumerate(sizes)]
+        gc.gc_2bit_quantize_batched(grads, [r[:n] for r, n in zip(res, sizes)],
+                                    [c[:gc.code_words(n)] for c, n in zip(codes, sizes)], t)
+        refs = [oracle.twobit_quantize(_grad_host(g), r_ref[b], t) for b, g in enumerate(grads)]
+        torch.cuda.synchronize()
+        for b, n in enumerate(sizes):
+            np.testing.assert_array_equal(host_u32(codes[b][:gc.code_words(n)]), refs[b])
+            np.testing.assert_array_equal(host_f32(res[b][:n]).view(np.uint32), r_ref[b].view(np.uint32))
+    for b, n in enumerate(sizes):
+        check_guard(res[b], n)
+        check_guard(codes[b], gc.code_words(n))
+
+
+def test_batched_config_twobit_dq_sgd_sampled():
+    """The 8-worker, 25,557,032-element workload through the batched quantiser
+    and the dequant-sum + SGD, 3 steps, checked on sampled chunks (every
+    element's chain is independent of the others)."""
+    from gpu_helpers import sample_chunks
+    cfg = wl.TWOBIT_DQ_SGD
+    n, W, t, lr = cfg.n, cfg.workers, cfg.threshold, cfg.lr
+    res = [torch.zeros(n, device=DEV) for _ in range(W)]
+    codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    w = wl.twobit_weights(cfg, device=DEV)
+    chunks = sample_chunks(n, 48, 4096, align=16, seed=3)
+    w0 = host_f32(w)
+    w_ref = {c: w0[c[0]:c[1]].astype(np.float64) for c in chunks}
+    r_ref = {(c, q): np.zeros(c[1] - c[0], np.float32) for c in chunks for q in range(W)}
+    scale = {c: np.abs(w_ref[c]).copy() for c in chunks}
+    for step in range(3):
+        grads = [wl.twobit_grad(cfg, step, q, device=DEV) for q in range(W)]
+        gc.gc_2bit_quantize_batched(grads, res, codes, t)
+        gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=w)
+        gh = [host_f32(g) for g in grads]
+        torch.cuda.synchronize()
+        hc = [host_u32(c) for c in codes]
+        for c in chunks:
+            lo, hi = c
+            cr = [oracle.twobit_quantize(np.ascontiguousarray(gh[q][lo:hi]), r_ref[(c, q)], t)
+                  for q in range(W)]
+            oracle.twobit_dequant_sum_update(cr, hi - lo, t, oracle.KIND_SGD, lr=lr, weights=w_ref[c])
+            scale[c] += lr * t
+            for q in range(W):
+                np.testing.assert_array_equal(hc[q][lo // 16:(hi + 15) // 16], cr[q])
+    hw = host_f32(w)
+    hr = [host_f32(r) for r in res]
+    for c in chunks:
+        lo, hi = c
+        for q in range(W):
+            np.testing.assert_array_equal(hr[q][lo:hi].view(np.uint32), r_ref[(c, q)].view(np.uint32))
+        assert_close(hw[lo:hi], w_ref[c], scale[c], what=f"weights {c}")
