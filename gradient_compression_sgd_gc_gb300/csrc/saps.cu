@@ -27,14 +27,17 @@ constexpr uint64_t kFlagPrefix = 2ull << 62;
 constexpr uint64_t kValueMask = (1ull << 62) - 1;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per look-back wait
 
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+// The look-back state word carries its own value (flag + count), and no
+// other data is published through it, so relaxed single-copy-atomic 64-bit
+// accesses at GPU scope are enough (no acquire/release fences).
+__device__ __forceinline__ uint64_t ld_state(const uint64_t* p) {
     uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+__device__ __forceinline__ void st_state(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -68,10 +71,10 @@ struct MaskArgs {
 // predecessors count as zero and GC_ERR_TIMEOUT is recorded.
 __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
     if (tile == 0) {
-        if (lane == 0) st_release(a.state, kFlagPrefix | agg);
+        if (lane == 0) st_state(a.state, kFlagPrefix | agg);
         return 0;
     }
-    if (lane == 0) st_release(a.state + tile, kFlagAgg | agg);
+    if (lane == 0) st_state(a.state + tile, kFlagAgg | agg);
     uint64_t excl = 0;
     int64_t end = tile - 1;
     const uint64_t t0 = global_ns();
@@ -82,7 +85,7 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int64_t j = end - (4 * lane + q);
-            st[q] = j >= 0 ? ld_acquire(a.state + j) : kFlagPrefix;
+            st[q] = j >= 0 ? ld_state(a.state + j) : kFlagPrefix;
         }
         unsigned polls = 0;
         while (true) {
@@ -99,11 +102,11 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
                     if ((st[q] >> 62) == 0) st[q] = kFlagAgg;   // unknown predecessor counts as 0
                 break;
             }
-            if (++polls > 8) __nanosleep(polls < 64 ? 64 : 512);
+            if (++polls > 32) __nanosleep(polls < 256 ? 32 : 256);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int64_t j = end - (4 * lane + q);
-                if ((st[q] >> 62) == 0) st[q] = ld_acquire(a.state + j);
+                if ((st[q] >> 62) == 0) st[q] = ld_state(a.state + j);
             }
         }
         // closest predecessor with a prefix: first lane that has one, then its first q
@@ -125,7 +128,7 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
         end -= 128;
     }
     if (lane == 0) {
-        st_release(a.state + tile, kFlagPrefix | (excl + agg));
+        st_state(a.state + tile, kFlagPrefix | (excl + agg));
         if (timed_out) atomicExch(a.d_status, GC_ERR_TIMEOUT);
     }
     return excl;
@@ -368,43 +371,61 @@ struct FusedArgs {
     int64_t capacity;
 };
 
+// Masked coordinates among the 4 elements of chunk i: the received peer
+// values are averaged into the registers m[].
+template <int MAXW>
+__device__ __forceinline__ void average_masked(const FusedArgs& a, float4 (&m)[MAXW], uint32_t bits,
+                                               uint32_t base, uint64_t usable) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (!((bits >> e) & 1u)) continue;
+        const uint32_t rank = base + __popc(bits & ((1u << e) - 1u));
+        if (rank >= usable) continue;
+        float recv[MAXW];
+#pragma unroll
+        for (int k = 0; k < MAXW; ++k)
+            if (k < a.W) recv[k] = __ldg(a.vals.p[a.partner[k]] + rank);
+#pragma unroll
+        for (int k = 0; k < MAXW; ++k) {
+            if (k < a.W) {
+                float* x = e == 0 ? &m[k].x : e == 1 ? &m[k].y : e == 2 ? &m[k].z : &m[k].w;
+                *x = __fmul_rn(__fadd_rn(*x, recv[k]), 0.5f);
+            }
+        }
+    }
+}
+
+// Grid-stride over float4 chunks with the next chunk's group tables loaded
+// one iteration ahead, so that the payload reads of a chunk are issued
+// together with its model loads instead of after a dependent round trip.
 template <int MAXW>
 __global__ void __launch_bounds__(kThreads, 2)
 k_saps_average_easgd(const FusedArgs a) {
     const uint64_t cnt = *a.d_count;
     const uint64_t usable = cnt < static_cast<uint64_t>(a.capacity) ? cnt : static_cast<uint64_t>(a.capacity);
     const int64_t nv = a.n >> 2;
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i < nv) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint32_t gm = 0, ge = 0;
+    if (first < nv) {
+        gm = __ldg(a.group_mask + ((4 * first) >> 5));
+        ge = __ldg(a.group_excl + ((4 * first) >> 5));
+    }
+    for (int64_t i = first; i < nv; i += stride) {
         float4 m[MAXW];
 #pragma unroll
         for (int k = 0; k < MAXW; ++k)
             if (k < a.W) m[k] = ld_f4(a.models.p[k] + 4 * i);
         const float4 c = ld_f4(a.center + 4 * i);
-        const int64_t g = (4 * i) >> 5;
-        const uint32_t sh = static_cast<uint32_t>((4 * i) & 31);
-        const uint32_t gm = __ldg(a.group_mask + g);
-        const uint32_t bits = (gm >> sh) & 15u;
-        if (bits) {
-            const uint32_t base = __ldg(a.group_excl + g) + __popc(gm & ((1u << sh) - 1u));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (!((bits >> e) & 1u)) continue;
-                const uint32_t rank = base + __popc(bits & ((1u << e) - 1u));
-                if (rank >= usable) continue;
-                float recv[MAXW];
-#pragma unroll
-                for (int k = 0; k < MAXW; ++k)
-                    if (k < a.W) recv[k] = __ldg(a.vals.p[a.partner[k]] + rank);
-#pragma unroll
-                for (int k = 0; k < MAXW; ++k) {
-                    if (k < a.W) {
-                        float* x = e == 0 ? &m[k].x : e == 1 ? &m[k].y : e == 2 ? &m[k].z : &m[k].w;
-                        *x = __fmul_rn(__fadd_rn(*x, recv[k]), 0.5f);
-                    }
-                }
-            }
+        const int64_t nxt = i + stride;
+        uint32_t gm_n = 0, ge_n = 0;
+        if (nxt < nv) {
+            gm_n = __ldg(a.group_mask + ((4 * nxt) >> 5));
+            ge_n = __ldg(a.group_excl + ((4 * nxt) >> 5));
         }
+        const uint32_t sh = static_cast<uint32_t>((4 * i) & 31);
+        const uint32_t bits = (gm >> sh) & 15u;
+        if (bits) average_masked<MAXW>(a, m, bits, ge + __popc(gm & ((1u << sh) - 1u)), usable);
         float4 sum = m[0];
 #pragma unroll
         for (int k = 1; k < MAXW; ++k)
@@ -422,13 +443,16 @@ k_saps_average_easgd(const FusedArgs a) {
         st_stream_f4(a.center + 4 * i,
                      make_float4(fmaf(a.beta, __fsub_rn(mean.x, c.x), c.x), fmaf(a.beta, __fsub_rn(mean.y, c.y), c.y),
                                  fmaf(a.beta, __fsub_rn(mean.z, c.z), c.z), fmaf(a.beta, __fsub_rn(mean.w, c.w), c.w)));
-    } else if (i == nv && (a.n & 3)) {
+        gm = gm_n;
+        ge = ge_n;
+    }
+    if (first == 0 && (a.n & 3)) {
         // the last n % 4 elements, one thread
         for (int64_t t = nv << 2; t < a.n; ++t) {
-            const uint32_t gm = __ldg(a.group_mask + (t >> 5));
+            const uint32_t gmt = __ldg(a.group_mask + (t >> 5));
             const uint32_t sh = static_cast<uint32_t>(t & 31);
-            const bool hit = (gm >> sh) & 1u;
-            const uint32_t rank = __ldg(a.group_excl + (t >> 5)) + __popc(gm & ((1u << sh) - 1u));
+            const bool hit = (gmt >> sh) & 1u;
+            const uint32_t rank = __ldg(a.group_excl + (t >> 5)) + __popc(gmt & ((1u << sh) - 1u));
             float v[GC_MAX_WORKERS];
             for (int k = 0; k < a.W; ++k) v[k] = a.models.p[k][t];
             if (hit && rank < usable)
@@ -619,7 +643,10 @@ int saps_average_easgd_step(float* const* models, const float* const* vals, cons
     a.capacity = capacity;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (W <= 16) {
-        const unsigned grid = static_cast<unsigned>(((n >> 2) + 1 + kThreads - 1) / kThreads);
+        const int64_t want = ((n >> 2) + kThreads - 1) / kThreads;
+        const int persistent = grid_for(2);
+        if (persistent <= 0) return GC_ERR_CUDA;
+        const unsigned grid = static_cast<unsigned>(want < persistent ? (want > 0 ? want : 1) : persistent);
         if (W <= 4)
             k_saps_average_easgd<4><<<grid, kThreads, 0, s>>>(a);
         else
