@@ -288,8 +288,9 @@ float orc_l2norm_fp32(const float *v, int64_t len)
  * slice of a long vector can be quantised on its own).  fp32 operation order
  * of the decision:
  *     S = s / norm,  a = |v_i| * S,  x = a + u,  level = min(floor(x), s)
- * (a NaN x, possible only when s / norm overflows, counts as s).  A bucket
- * with norm 0 gets level 0 everywhere.
+ * A NaN x arises only as 0 * inf (a zero coordinate in a bucket whose s / norm
+ * overflows fp32); Q_s scales |v_i|, so that coordinate gets level 0.  A
+ * bucket with norm 0 gets level 0 everywhere.
  * Codes are sign-magnitude: sign bit = (v_i < 0), set above the level bits.
  *   1 <= s <= 7   : 4-bit codes, two per byte, element 2j in the HIGH nibble
  *   8 <= s <= 127 : 8-bit codes, one per byte, bit 7 = sign
@@ -317,7 +318,9 @@ void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
                 float a = fabsf(v[i]) * S;
                 float u = (float)orc_uniform(seed_w ^ (uint64_t)(i0 + i));
                 float x = a + u;
-                if (x != x || x >= (float)s)
+                if (x != x)
+                    level = 0u;
+                else if (x >= (float)s)
                     level = (uint32_t)s;
                 else
                     level = (uint32_t)floorf(x);

@@ -225,3 +225,15 @@ def test_ragged_last_bucket_and_odd_n():
     assert norms.size == 5 and codes.size == (n + 1) // 2
     _exact_rounding_check(v[4 * d:], norms[4])
     assert codes[-1] & 0x0F == 0        # the unused low nibble of the last byte
+
+
+def test_tiny_norm_bucket_zero_coordinate_gets_level_zero():
+    """When s / norm overflows fp32 (a bucket of subnormal values), a zero
+    coordinate still quantises to level 0 (Q_s scales |v_i| = 0) and the
+    nonzero ones saturate at s."""
+    v = np.zeros(512, np.float32)
+    v[:8] = np.float32(1e-40)
+    norms, codes = oracle.qsgd_quantize(v, 512, 127, seed=4, worker=0)
+    assert np.isinf(np.float32(127) / norms[0])
+    sign, level = _parse_codes(codes, 512, 127)
+    assert np.all(level[8:] == 0) and np.all(level[:8] == 127)
