@@ -65,14 +65,14 @@ struct QArgs {
 
 // level = min(floor(|v| * S + u), s) in fp32, u = top24(hash) * 2^-24.
 // u is an exact multiple of 2^-24, so one fma rounds |v|*S + u exactly as the
-// separate add does.  For 0 <= y < 2^23, rounding y + 2^23 downwards leaves
-// floor(y) in the mantissa bits; a NaN y (s / norm overflowed) has all
-// mantissa bits set there, so the min with s maps it to s.
+// separate add does.  The floor runs on the conversion pipe (round toward
+// -inf to an unsigned integer; +inf saturates, so min() gives s); a NaN y
+// (0 * inf: a zero coordinate in a bucket whose s / norm overflows) converts
+// to 0, the level of a zero coordinate.
 __device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint64_t key) {
     const float a = __fmul_rn(fabsf(x), S);
     const float y = __fmaf_rn(__uint2float_rn(splitmix64_top24(key)), 5.9604644775390625e-8f, a);
-    const uint32_t fl = __float_as_uint(__fadd_rd(y, 8388608.0f)) & 0x7FFFFFu;
-    return min(fl, s);
+    return min(__float2uint_rd(y), s);
 }
 
 // One warp per bucket; the grid covers every bucket.
@@ -113,6 +113,7 @@ k_qsgd_quantize(const QArgs a) {
     }
     const float norm = warp_norm(hi, lo);
     if (lane == 0) a.norms[b] = norm;
+    // norm == 0 means every coordinate is +-0: sign bit 0, level 0, code 0
     const bool zero = !(norm > 0.0f);
     const float S = zero ? 0.0f : __fdiv_rn(s_f, norm);
 
@@ -122,11 +123,13 @@ k_qsgd_quantize(const QArgs a) {
         // e is a multiple of 4, so seed_w ^ (e + k) == (seed_w ^ e) ^ k
         const uint64_t kbase = a.seed_w ^ static_cast<uint64_t>(e);
         const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        uint32_t c[4];
+        uint32_t c[4] = {0u, 0u, 0u, 0u};
+        if (!zero) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t lvl = zero ? 0u : qlevel(xs[k], S, s_u, kbase ^ static_cast<uint64_t>(k));
-            c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t lvl = qlevel(xs[k], S, s_u, kbase ^ static_cast<uint64_t>(k));
+                c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
+            }
         }
         if (FOUR) {
             const uint32_t lo2 = (c[0] << 4) | c[1];

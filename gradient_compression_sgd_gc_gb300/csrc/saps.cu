@@ -65,9 +65,11 @@ struct MaskArgs {
 };
 
 // Exclusive prefix of tile `tile` whose own count is `agg`; run by one warp.
-// Publishes (aggregate) first, then walks back over its predecessors 128 at a
-// time (4 state words per lane) until it meets one that has published its
-// inclusive prefix.  Every wait is bounded: after kWaitLimitNs the missing
+// Publishes (aggregate) first, then walks back over its predecessors 32 at a
+// time (one coalesced 256-byte read of their state words) until it meets one
+// that has published its inclusive prefix.  Pending predecessors are polled
+// without sleeping (they publish their aggregate right after their own
+// block scan); every wait is bounded: after kWaitLimitNs the missing
 // predecessors count as zero and GC_ERR_TIMEOUT is recorded.
 __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
     if (tile == 0) {
@@ -80,52 +82,28 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
     const uint64_t t0 = global_ns();
     bool timed_out = false;
     while (true) {
-        // state of predecessor end - (4 * lane + q), q = 0..3
-        uint64_t st[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int64_t j = end - (4 * lane + q);
-            st[q] = j >= 0 ? ld_state(a.state + j) : kFlagPrefix;
-        }
-        unsigned polls = 0;
+        const int64_t j = end - lane;
+        uint64_t st = j >= 0 ? ld_state(a.state + j) : kFlagPrefix;
         while (true) {
-            bool pending = false;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) pending |= (st[q] >> 62) == 0;
+            const bool pending = (st >> 62) == 0;
             if (!__any_sync(0xffffffffu, pending)) break;
             // lane 0's clock decides, so the whole warp leaves together
             const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs, 0);
             if (expired) {
                 timed_out = true;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if ((st[q] >> 62) == 0) st[q] = kFlagAgg;   // unknown predecessor counts as 0
+                if (pending) st = kFlagAgg;   // unknown predecessor counts as 0
                 break;
             }
-            if (++polls > 32) __nanosleep(polls < 256 ? 32 : 256);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int64_t j = end - (4 * lane + q);
-                if ((st[q] >> 62) == 0) st[q] = ld_state(a.state + j);
-            }
+            if (pending) st = ld_state(a.state + j);
         }
-        // closest predecessor with a prefix: first lane that has one, then its first q
-        int myq = 4;
-#pragma unroll
-        for (int q = 3; q >= 0; --q)
-            if ((st[q] >> 62) == 2) myq = q;
-        const unsigned lanes = __ballot_sync(0xffffffffu, myq < 4);
-        const int f = lanes ? __ffs(lanes) - 1 : 32;
-        const int fq = lanes ? __shfl_sync(0xffffffffu, myq, f) : 4;
-        uint64_t v = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (lane < f || (lane == f && q <= fq)) v += st[q] & kValueMask;
+        const unsigned prefix_lanes = __ballot_sync(0xffffffffu, (st >> 62) == 2);
+        const int last = prefix_lanes ? __ffs(prefix_lanes) - 1 : 31;
+        uint64_t v = lane <= last ? (st & kValueMask) : 0;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         excl += v;
-        if (lanes) break;
-        end -= 128;
+        if (prefix_lanes) break;
+        end -= 32;
     }
     if (lane == 0) {
         st_state(a.state + tile, kFlagPrefix | (excl + agg));

@@ -148,3 +148,17 @@ def test_dequant_sum_parity(n, W, s):
     assert_close(host_f32(out[:n])[keep], ref[keep], (scale * terms)[keep], what="dequant-sum")
     check_guard(out, n)
     del mag
+
+
+def test_tiny_norm_bucket_matches_oracle():
+    v = torch.zeros(1024, device=DEV)
+    v[:8] = 1e-40
+    v[600:605] = -1e-40
+    for s in (7, 127):
+        norms = torch.empty(2, device=DEV)
+        codes = torch.empty(gc.qsgd_code_bytes(1024, s), dtype=torch.uint8, device=DEV)
+        gc.qsgd_quantize(v, 512, s, 4, 0, norms, codes)
+        rn, rc = oracle.qsgd_quantize(host_f32(v), 512, s, 4, 0)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_f32(norms), rn)
+        np.testing.assert_array_equal(codes.cpu().numpy(), rc)
