@@ -32,6 +32,29 @@ __device__ __forceinline__ void acc_square(float x, float& hi, float& lo) {
     lo = __fadd_rn(lo, __fadd_rn(e, q));
 }
 
+// Sum of squares of a double-float pair over the warp (every lane gets it).
+__device__ __forceinline__ void warp_sum2(float& hi, float& lo) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        float s, e;
+        two_sum(hi, h2, s, e);
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    }
+}
+
+// sqrt of the double-float X + Xl, rounded to nearest fp32.
+__device__ __forceinline__ float df_sqrt(float hi, float lo) {
+    const float X = __fadd_rn(hi, lo);
+    const float Xl = __fsub_rn(lo, __fsub_rn(X, hi));
+    if (!(X > 0.0f)) return 0.0f;
+    const float r = __fsqrt_rn(X);
+    const float rem = __fadd_rn(__fmaf_rn(-r, r, X), Xl);     // X + Xl - r^2
+    return __fmaf_rn(rem, __fdiv_rn(0.5f, r), r);             // r + rem / (2r)
+}
+
 // The bucket's l2 norm, rounded to nearest fp32 (equal to the correctly
 // rounded value unless sqrt(sum) lies within about 2^-40 relative of a
 // rounding midpoint).  Every lane returns the same value.
@@ -75,6 +98,15 @@ __device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint64_
     return min(__float2uint_rd(y), s);
 }
 
+// True when every value of the warp's bucket registers is +-0.
+template <int ROUNDS>
+__device__ __forceinline__ bool all_zero(const float4 (&v)[ROUNDS], int lane) {
+    bool nz = false;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) nz |= (v[j].x != 0.0f) | (v[j].y != 0.0f) | (v[j].z != 0.0f) | (v[j].w != 0.0f);
+    return !__any_sync(0xffffffffu, nz);
+}
+
 // One warp per bucket; the grid covers every bucket.
 template <int ROUNDS, bool FOUR>
 __global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
@@ -111,7 +143,34 @@ k_qsgd_quantize(const QArgs a) {
         acc_square(v[j].z, hi, lo);
         acc_square(v[j].w, hi, lo);
     }
-    const float norm = warp_norm(hi, lo);
+    float norm = warp_norm(hi, lo);
+    // A sum of squares below 2^-100 may have lost bits to underflow and one
+    // above 2^126 overflows: such buckets (subnormal-sized or huge gradients;
+    // the test is warp-uniform) are redone with every value scaled by the
+    // power of two that brings the bucket maximum to [0.5, 1), which is exact,
+    // and the norm scaled back.
+    const bool tiny = norm < 8.8817842e-16f;      // 2^-50: the sum of squares is below 2^-100
+    const bool huge = !(norm < 9.2233720e18f);    // 2^63, or inf / NaN
+    if (huge || (tiny && !all_zero(v, lane))) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j)
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int ex = 0;
+        frexpf(mx, &ex);
+        float h2 = 0.0f, l2 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j) {
+            acc_square(ldexpf(v[j].x, -ex), h2, l2);
+            acc_square(ldexpf(v[j].y, -ex), h2, l2);
+            acc_square(ldexpf(v[j].z, -ex), h2, l2);
+            acc_square(ldexpf(v[j].w, -ex), h2, l2);
+        }
+        warp_sum2(h2, l2);
+        norm = ldexpf(df_sqrt(h2, l2), ex);
+    }
     if (lane == 0) a.norms[b] = norm;
     // norm == 0 means every coordinate is +-0: sign bit 0, level 0, code 0
     const bool zero = !(norm > 0.0f);

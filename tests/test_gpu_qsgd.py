@@ -150,15 +150,24 @@ def test_dequant_sum_parity(n, W, s):
     del mag
 
 
-def test_tiny_norm_bucket_matches_oracle():
-    v = torch.zeros(1024, device=DEV)
-    v[:8] = 1e-40
-    v[600:605] = -1e-40
+@pytest.mark.parametrize("scale", [1e-40, 1e-25, 1e25])
+def test_tiny_and_huge_buckets_match_oracle(scale):
+    """Buckets whose squares underflow or overflow fp32 (subnormal-sized or
+    huge gradients): norms within rel 1e-5, codes equal up to boundary cases;
+    the subnormal case also exercises the s / norm overflow reading."""
+    n = 2048
+    rng = np.random.default_rng(5)
+    vh = (rng.normal(0, 1, n) * scale).astype(np.float32)
+    vh[512:520] = 0.0
+    vh[1024:1536] = 0.0
+    vh[1100] = np.float32(scale)
+    v = torch.from_numpy(vh).to(DEV)
     for s in (7, 127):
-        norms = torch.empty(2, device=DEV)
-        codes = torch.empty(gc.qsgd_code_bytes(1024, s), dtype=torch.uint8, device=DEV)
+        norms = torch.empty(4, device=DEV)
+        codes = torch.empty(gc.qsgd_code_bytes(n, s), dtype=torch.uint8, device=DEV)
         gc.qsgd_quantize(v, 512, s, 4, 0, norms, codes)
-        rn, rc = oracle.qsgd_quantize(host_f32(v), 512, s, 4, 0)
+        rn, rc = oracle.qsgd_quantize(vh, 512, s, 4, 0)
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(host_f32(norms), rn)
-        np.testing.assert_array_equal(codes.cpu().numpy(), rc)
+        assert_close(host_f32(norms), rn, np.abs(rn), what="norms")
+        assert host_f32(norms)[2] == rn[2]          # one nonzero value: |v| exactly
+        compare_codes(codes.cpu().numpy(), rc, vh, n, 512, s, 4, 0)
