@@ -248,66 +248,89 @@ __device__ __forceinline__ uint32_t code_of(uint32_t raw, int k) {
     return (raw >> (8 * k)) & 255u;
 }
 
-// One warp per bucket.  Workers are taken WC at a time with every code and
-// norm load of the group issued before any is decoded; each element's sum runs
-// in worker order.  The per-bucket unit is norm * (scale / s).
-template <int ROUNDS, bool FOUR>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 3)
+// One warp per NB consecutive buckets.  Workers are taken WC at a time
+// with every code and norm load of the group (all NB buckets) issued before
+// any is decoded, which keeps NB times more bytes in flight per warp than one
+// bucket would; each element's sum runs in worker order.  The per-bucket
+// unit is norm * (scale / s).
+template <int ROUNDS, bool FOUR, int NB>
+__global__ void __launch_bounds__(kThreads, 3)
 k_qsgd_dequant_sum(const DArgs a) {
-    constexpr int WC = ROUNDS >= 8 ? 1 : 4;      // workers whose loads are issued together
+    constexpr int WC = (ROUNDS * NB >= 8) ? 2 : 4;    // workers whose loads are issued together
     const int lane = threadIdx.x & 31;
-    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (b >= a.nbuckets) return;
+    const int64_t b_first = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * NB;
+    if (b_first >= a.nbuckets) return;
     constexpr int D = 128 * ROUNDS;
     constexpr uint32_t kLevelMask = FOUR ? 7u : 127u;
     constexpr uint32_t kSignBit = FOUR ? 8u : 128u;
 
-    const int64_t b0 = b * D;
-    const bool full = b0 + D <= a.n;
-    float sum[ROUNDS][4];
+    float sum[NB][ROUNDS][4];
 #pragma unroll
-    for (int j = 0; j < ROUNDS; ++j)
+    for (int bb = 0; bb < NB; ++bb)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sum[j][k] = 0.0f;
+        for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sum[bb][j][k] = 0.0f;
+    bool full[NB];
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) full[bb] = (b_first + bb + 1) * D <= a.n;
+
     for (int w0 = 0; w0 < a.W; w0 += WC) {
-        uint32_t raw[WC][ROUNDS];
-        float unit[WC];
+        uint32_t raw[WC][NB][ROUNDS];
+        float unit[WC][NB];
 #pragma unroll
         for (int q = 0; q < WC; ++q) {
             if (w0 + q < a.W) {
-                unit[q] = __ldg(a.norms.p[w0 + q] + b);
 #pragma unroll
-                for (int j = 0; j < ROUNDS; ++j)
-                    raw[q][j] = load_raw4<FOUR>(a.codes.p[w0 + q], b0 + 128 * j + 4 * lane, a.n, full);
+                for (int bb = 0; bb < NB; ++bb) {
+                    const int64_t b = b_first + bb;
+                    if (b < a.nbuckets) {
+                        unit[q][bb] = __ldg(a.norms.p[w0 + q] + b);
+#pragma unroll
+                        for (int j = 0; j < ROUNDS; ++j)
+                            raw[q][bb][j] = load_raw4<FOUR>(a.codes.p[w0 + q], b * D + 128 * j + 4 * lane, a.n,
+                                                             full[bb]);
+                    }
+                }
             }
         }
 #pragma unroll
         for (int q = 0; q < WC; ++q) {
             if (w0 + q < a.W) {
-                const float u = __fmul_rn(unit[q], a.unit_scale);
 #pragma unroll
-                for (int j = 0; j < ROUNDS; ++j)
+                for (int bb = 0; bb < NB; ++bb) {
+                    if (b_first + bb >= a.nbuckets) continue;
+                    const float u = __fmul_rn(unit[q][bb], a.unit_scale);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t c = code_of<FOUR>(raw[q][j], k);
-                        const float lf = __uint_as_float(0x4B000000u | (c & kLevelMask)) - 8388608.0f;
-                        const float term = __fmul_rn(u, lf);
-                        sum[j][k] = (c & kSignBit) ? __fsub_rn(sum[j][k], term) : __fadd_rn(sum[j][k], term);
-                    }
+                    for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t c = code_of<FOUR>(raw[q][bb][j], k);
+                            const float lf = __uint_as_float(0x4B000000u | (c & kLevelMask)) - 8388608.0f;
+                            const float term = __fmul_rn(u, lf);
+                            sum[bb][j][k] = (c & kSignBit) ? __fsub_rn(sum[bb][j][k], term)
+                                                           : __fadd_rn(sum[bb][j][k], term);
+                        }
+                }
             }
         }
     }
 #pragma unroll
-    for (int j = 0; j < ROUNDS; ++j) {
-        const int64_t e = b0 + 128 * j + 4 * lane;
-        const float4 o = make_float4(sum[j][0], sum[j][1], sum[j][2], sum[j][3]);
-        if (full) {
-            st_stream_f4(a.out + e, o);
-        } else {
-            if (e < a.n) a.out[e] = o.x;
-            if (e + 1 < a.n) a.out[e + 1] = o.y;
-            if (e + 2 < a.n) a.out[e + 2] = o.z;
-            if (e + 3 < a.n) a.out[e + 3] = o.w;
+    for (int bb = 0; bb < NB; ++bb) {
+        const int64_t b = b_first + bb;
+        if (b >= a.nbuckets) continue;
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j) {
+            const int64_t e = b * D + 128 * j + 4 * lane;
+            const float4 o = make_float4(sum[bb][j][0], sum[bb][j][1], sum[bb][j][2], sum[bb][j][3]);
+            if (full[bb]) {
+                st_stream_f4(a.out + e, o);
+            } else {
+                if (e < a.n) a.out[e] = o.x;
+                if (e + 1 < a.n) a.out[e + 1] = o.y;
+                if (e + 2 < a.n) a.out[e + 2] = o.z;
+                if (e + 3 < a.n) a.out[e + 3] = o.w;
+            }
         }
     }
 }
@@ -326,13 +349,16 @@ int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
 }
 
 template <bool FOUR>
-int launch_dequant(int rounds, const DArgs& a, unsigned grid, cudaStream_t s) {
+int launch_dequant(int rounds, const DArgs& a, cudaStream_t s) {
+    // buckets per warp: 2 for buckets of 512 elements or fewer, else 1
+    const unsigned g2 = blocks_for_tiles((a.nbuckets + 1) / 2);
+    const unsigned g1 = blocks_for_tiles(a.nbuckets);
     switch (rounds) {
-        case 1: k_qsgd_dequant_sum<1, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 2: k_qsgd_dequant_sum<2, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 4: k_qsgd_dequant_sum<4, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 8: k_qsgd_dequant_sum<8, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 16: k_qsgd_dequant_sum<16, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 1: k_qsgd_dequant_sum<1, FOUR, 2><<<g2, kThreads, 0, s>>>(a); break;
+        case 2: k_qsgd_dequant_sum<2, FOUR, 2><<<g2, kThreads, 0, s>>>(a); break;
+        case 4: k_qsgd_dequant_sum<4, FOUR, 2><<<g2, kThreads, 0, s>>>(a); break;
+        case 8: k_qsgd_dequant_sum<8, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
+        case 16: k_qsgd_dequant_sum<16, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
         default: return GC_ERR_INVALID;
     }
     return launch_status();
@@ -390,10 +416,9 @@ int qsgd_dequant_sum(const uint8_t* const* codes, const float* const* norms, int
     a.nbuckets = (n + bucket - 1) / bucket;
     a.unit_scale = static_cast<float>(static_cast<double>(scale) / s_levels);
     a.out = out;
-    const unsigned grid = blocks_for_tiles(a.nbuckets);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return s_levels <= 7 ? launch_dequant<true>(bucket / 128, a, grid, s)
-                         : launch_dequant<false>(bucket / 128, a, grid, s);
+    return s_levels <= 7 ? launch_dequant<true>(bucket / 128, a, s)
+                         : launch_dequant<false>(bucket / 128, a, s);
 }
 
 }  // extern "C"
