@@ -248,13 +248,13 @@ __device__ __forceinline__ uint32_t code_of(uint32_t raw, int k) {
     return (raw >> (8 * k)) & 255u;
 }
 
-// One warp per NB consecutive buckets.  Workers are taken WC at a time
-// with every code and norm load of the group (all NB buckets) issued before
-// any is decoded, which keeps NB times more bytes in flight per warp than one
-// bucket would; each element's sum runs in worker order.  The per-bucket
-// unit is norm * (scale / s).
+// One warp per NB consecutive buckets (NB = 1 in use: a second bucket per
+// warp measured slower).  Workers are taken WC at a time with every code and
+// norm load of the group issued before any is decoded; each element's sum
+// runs in worker order, every term added by one fma of the level with the
+// signed unit norm * (scale / s).
 template <int ROUNDS, bool FOUR, int NB>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
 k_qsgd_dequant_sum(const DArgs a) {
     constexpr int WC = (ROUNDS * NB >= 8) ? 2 : 4;    // workers whose loads are issued together
     const int lane = threadIdx.x & 31;
@@ -301,15 +301,16 @@ k_qsgd_dequant_sum(const DArgs a) {
                 for (int bb = 0; bb < NB; ++bb) {
                     if (b_first + bb >= a.nbuckets) continue;
                     const float u = __fmul_rn(unit[q][bb], a.unit_scale);
+                    const float nu = -u;
 #pragma unroll
                     for (int j = 0; j < ROUNDS; ++j)
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint32_t c = code_of<FOUR>(raw[q][bb][j], k);
+                            // level as an exact float (2^23 + level, minus 2^23); the
+                            // signed unit times the level is added with one rounding
                             const float lf = __uint_as_float(0x4B000000u | (c & kLevelMask)) - 8388608.0f;
-                            const float term = __fmul_rn(u, lf);
-                            sum[bb][j][k] = (c & kSignBit) ? __fsub_rn(sum[bb][j][k], term)
-                                                           : __fadd_rn(sum[bb][j][k], term);
+                            sum[bb][j][k] = __fmaf_rn(lf, (c & kSignBit) ? nu : u, sum[bb][j][k]);
                         }
                 }
             }
@@ -350,13 +351,11 @@ int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
 
 template <bool FOUR>
 int launch_dequant(int rounds, const DArgs& a, cudaStream_t s) {
-    // buckets per warp: 2 for buckets of 512 elements or fewer, else 1
-    const unsigned g2 = blocks_for_tiles((a.nbuckets + 1) / 2);
     const unsigned g1 = blocks_for_tiles(a.nbuckets);
     switch (rounds) {
-        case 1: k_qsgd_dequant_sum<1, FOUR, 2><<<g2, kThreads, 0, s>>>(a); break;
-        case 2: k_qsgd_dequant_sum<2, FOUR, 2><<<g2, kThreads, 0, s>>>(a); break;
-        case 4: k_qsgd_dequant_sum<4, FOUR, 2><<<g2, kThreads, 0, s>>>(a); break;
+        case 1: k_qsgd_dequant_sum<1, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
+        case 2: k_qsgd_dequant_sum<2, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
+        case 4: k_qsgd_dequant_sum<4, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
         case 8: k_qsgd_dequant_sum<8, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
         case 16: k_qsgd_dequant_sum<16, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
         default: return GC_ERR_INVALID;

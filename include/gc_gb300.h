@@ -203,8 +203,8 @@ GC_API int qsgd_quantize(const float *grad, int64_t n, int bucket, int s_levels,
  * qsgd_dequant_sum -- QSGD Knowl 2 (decode the tuple: value = norm * sign *
  * level / s) and Knowl 3 (sum the K decoded messages; scale = 1/K gives
  * their average).
- *   out[i] = scale * sum_w sgn_w(i) * (norms[w][b] / s_levels) * level_w(i),
- *   summed in fp32 in worker order.
+ *   out[i] = sum_w sgn_w(i) * (norms[w][b] * (scale / s_levels)) * level_w(i),
+ *   summed in fp32 in worker order (one fma per term).
  *
  *   codes, norms  host arrays of W device pointers laid out as qsgd_quantize
  *                 writes them
