@@ -273,7 +273,7 @@ def headline(args, dev, rank, world, pg):
 def e2e(args, dev):
     """Same metric through the public API with host buffers: every step copies
     the 8 gradients from pinned host memory, runs the path, and reads the 8
-    packed code buffers back.  Uploads run on two copy streams so that worker
+    packed code buffers back.  Uploads run on a copy stream so that worker
     w+1's upload overlaps worker w's quantisation; events order each kernel
     after its own upload."""
     import torch
@@ -283,7 +283,8 @@ def e2e(args, dev):
     cfg = wl.TWOBIT_DQ_SGD
     n, W, t, lr = cfg.n, cfg.workers, cfg.threshold, cfg.lr
     stream = torch.cuda.current_stream(dev)
-    copies = [torch.cuda.Stream(dev) for _ in range(2)]
+    # one copy stream: measured fastest here (more streams split the host link)
+    copies = [torch.cuda.Stream(dev)]
     host_g = [wl.twobit_grad(cfg, 0, w, device="cpu").pin_memory() for w in range(W)]
     host_c = [torch.empty(gc.code_words(n), dtype=torch.int32).pin_memory() for _ in range(W)]
     dev_g = [torch.empty(n, device=dev) for _ in range(W)]
@@ -296,16 +297,13 @@ def e2e(args, dev):
                                           stream=stream, prepare=True)
     up = [[torch.cuda.Event() for _ in copies] for _ in range(W)]
     used = [torch.cuda.Event() for _ in range(W)]
-    half = n // 2
 
     def step():
-        # each upload is split over two copy streams (two copy engines)
         for w in range(W):
             for h, cs in enumerate(copies):
                 cs.wait_event(used[w])        # the previous step's kernel has read dev_g[w]
-                sl = slice(0, half) if h == 0 else slice(half, n)
                 with torch.cuda.stream(cs):
-                    dev_g[w][sl].copy_(host_g[w][sl], non_blocking=True)
+                    dev_g[w].copy_(host_g[w], non_blocking=True)
                 up[w][h].record(cs)
         for w in range(W):
             for h in range(len(copies)):

@@ -106,11 +106,15 @@ def _stream(stream, t: torch.Tensor | None = None):
     return ctypes.c_void_p(int(stream))
 
 
-def _dev(t: torch.Tensor, name: str, dtype=None, numel: int | None = None) -> int:
+def _dev(t: torch.Tensor, name: str, dtype=None, numel: int | None = None,
+         pinned_ok: bool = False) -> int:
+    """Address of a contiguous tensor the GPU can read.  ``pinned_ok`` also
+    accepts page-locked host tensors (read in place by the kernel over the
+    host link; the address is the same on both sides with unified addressing)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name}: expected a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_cuda and not (pinned_ok and t.is_pinned()):
+        raise ValueError(f"{name}: must be a CUDA tensor" + (" or pinned host tensor" if pinned_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -120,8 +124,9 @@ def _dev(t: torch.Tensor, name: str, dtype=None, numel: int | None = None) -> in
     return t.data_ptr()
 
 
-def _ptrs(ts, name, dtype=None, numel=None):
-    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]", dtype, numel) for i, t in enumerate(ts)])
+def _ptrs(ts, name, dtype=None, numel=None, pinned_ok=False):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]", dtype, numel, pinned_ok)
+                                         for i, t in enumerate(ts)])
 
 
 def _check(status: int, where: str) -> None:
@@ -188,9 +193,9 @@ def gc_2bit_quantize(grad: torch.Tensor, residual: torch.Tensor, codes: torch.Te
                      threshold: float, stream=None, prepare: bool = False):
     n = grad.numel()
     lib = load()
-    args = (_dev(grad, "grad"), _gdtype(grad), _dev(residual, "residual", torch.float32, n),
+    args = (_dev(grad, "grad", pinned_ok=True), _gdtype(grad), _dev(residual, "residual", torch.float32, n),
             _dev(codes, "codes", torch.int32, code_words(n)), n, float(threshold),
-            _stream(stream, grad))
+            _stream(stream, residual))
     return _invoke(lib.gc_2bit_quantize, args, "gc_2bit_quantize", prepare, (grad, residual, codes))
 
 
@@ -204,10 +209,10 @@ def gc_2bit_quantize_batched(grads, residuals, codes, threshold: float, stream=N
     dt = _gdtype(grads[0])
     ns = [g.numel() for g in grads]
     n_arr = (ctypes.c_int64 * B)(*ns)
-    args = (_ptrs(grads, "grads", grads[0].dtype),
+    args = (_ptrs(grads, "grads", grads[0].dtype, pinned_ok=True),
             dt, (ctypes.c_void_p * B)(*[_dev(r, f"residuals[{i}]", torch.float32, ns[i]) for i, r in enumerate(residuals)]),
             (ctypes.c_void_p * B)(*[_dev(c, f"codes[{i}]", torch.int32, code_words(ns[i])) for i, c in enumerate(codes)]),
-            n_arr, B, float(threshold), _stream(stream, grads[0]))
+            n_arr, B, float(threshold), _stream(stream, residuals[0]))
     return _invoke(lib.gc_2bit_quantize_batched, args, "gc_2bit_quantize_batched", prepare,
                    (list(grads), list(residuals), list(codes), n_arr))
 

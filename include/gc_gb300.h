@@ -96,7 +96,9 @@ GC_API int gc_version(void);
  * of word k (first element in the most significant bits); the unused bits of
  * the last word are zero.
  *
- *   grad       device, n elements of type `dtype` (fp32 or bf16), read only
+ *   grad       n elements of type `dtype` (fp32 or bf16), read only; device
+ *              memory, or page-locked host memory the GPU addresses directly
+ *              (read in place over the host link)
  *   residual   device fp32 [n], in/out (the error-feedback memory)
  *   codes      device uint32 [ceil(n/16)], written
  *   threshold  finite, > 0
@@ -112,7 +114,8 @@ GC_API int gc_2bit_quantize(const void *grad, gc_dtype dtype, float *residual,
  * (the W workers held on this GPU, or the many gradient tensors of one
  * worker); same rule, layout and residual update per buffer.
  *
- *   grads      host array of B device pointers, n[b] elements of `dtype`
+ *   grads      host array of B pointers, n[b] elements of `dtype` each, in
+ *              device memory or GPU-addressable page-locked host memory
  *   residuals  host array of B device pointers, fp32 [n[b]], in/out
  *   codes      host array of B device pointers, uint32 [ceil(n[b]/16)]
  *   n          host array of B sizes (0 allowed: that buffer is skipped)
