@@ -86,6 +86,8 @@ def load():
             "easgd_step": (i32, [vp, i32, i64, f32, f32, vp, vp]),
             "saps_average_easgd_step": (i32, [vp, vp, vp, vp, i32, i64, i64, f32, f32, vp, vp, sz, vp]),
             "saps_mask_compact_noalloc": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, vp]),
+            "gc_testing_saps_mask_compact_withhold": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz,
+                                                            vp, i64, u64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

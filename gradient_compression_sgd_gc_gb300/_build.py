@@ -36,7 +36,8 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
-        os.path.join(ROOT, "include", "gc_gb300.h"), os.path.abspath(__file__)]
+        os.path.join(ROOT, "include", "gc_gb300.h"), os.path.join(ROOT, "include", "gc_gb300_testing.h"),
+        os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:

@@ -11,6 +11,7 @@
 // "Single-pass Parallel Prefix Scan with Decoupled Look-back" (NVIDIA
 // technical report NVR-2016-002).
 #include "gc_common.cuh"
+#include "../../include/gc_gb300_testing.h"
 
 namespace gc {
 namespace {
@@ -25,7 +26,6 @@ constexpr size_t kWsHeader = 64;                   // tile counter + padding
 constexpr uint64_t kFlagAgg = 1ull << 62;
 constexpr uint64_t kFlagPrefix = 2ull << 62;
 constexpr uint64_t kValueMask = (1ull << 62) - 1;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per look-back wait
 
 // The look-back state word carries its own value (flag + count), and no
 // other data is published through it, so relaxed single-copy-atomic 64-bit
@@ -62,6 +62,8 @@ struct MaskArgs {
     int* d_status;
     uint32_t* group_mask = nullptr;  // per 32 elements: the mask bits (workspace), or null
     uint32_t* group_excl = nullptr;  // per 32 elements: masked entries before them, or null
+    uint64_t wait_ns = 1000000000ull;  // bound on each look-back wait
+    int64_t withhold_tile = -1;        // test hook: this tile never publishes (-1: none)
 };
 
 // Exclusive prefix of tile `tile` whose own count is `agg`; run by one warp.
@@ -69,14 +71,15 @@ struct MaskArgs {
 // time (one coalesced 256-byte read of their state words) until it meets one
 // that has published its inclusive prefix.  Pending predecessors are polled
 // without sleeping (they publish their aggregate right after their own
-// block scan); every wait is bounded: after kWaitLimitNs the missing
+// block scan); every wait is bounded: after a.wait_ns the missing
 // predecessors count as zero and GC_ERR_TIMEOUT is recorded.
 __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
+    const bool publish = tile != a.withhold_tile;
     if (tile == 0) {
-        if (lane == 0) st_state(a.state, kFlagPrefix | agg);
+        if (lane == 0 && publish) st_state(a.state, kFlagPrefix | agg);
         return 0;
     }
-    if (lane == 0) st_state(a.state + tile, kFlagAgg | agg);
+    if (lane == 0 && publish) st_state(a.state + tile, kFlagAgg | agg);
     uint64_t excl = 0;
     int64_t end = tile - 1;
     const uint64_t t0 = global_ns();
@@ -88,7 +91,7 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
             const bool pending = (st >> 62) == 0;
             if (!__any_sync(0xffffffffu, pending)) break;
             // lane 0's clock decides, so the whole warp leaves together
-            const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs, 0);
+            const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > a.wait_ns, 0);
             if (expired) {
                 timed_out = true;
                 if (pending) st = kFlagAgg;   // unknown predecessor counts as 0
@@ -106,7 +109,7 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
         end -= 32;
     }
     if (lane == 0) {
-        st_state(a.state + tile, kFlagPrefix | (excl + agg));
+        if (publish) st_state(a.state + tile, kFlagPrefix | (excl + agg));
         if (timed_out) atomicExch(a.d_status, GC_ERR_TIMEOUT);
     }
     return excl;
@@ -503,9 +506,10 @@ size_t saps_workspace_bytes(int64_t n) {
            2 * sizeof(uint32_t) * static_cast<size_t>(ws_groups(n));
 }
 
-int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* models, int W,
-                      uint32_t* idx, float* const* vals, int64_t capacity, uint64_t* d_count,
-                      void* workspace, size_t workspace_bytes, int* d_status, gc_stream_t stream) {
+static int mask_compact_impl(int64_t n, double p, uint64_t seed_t, const float* const* models, int W,
+                             uint32_t* idx, float* const* vals, int64_t capacity, uint64_t* d_count,
+                             void* workspace, size_t workspace_bytes, int* d_status, gc_stream_t stream,
+                             int64_t withhold_tile, uint64_t wait_ns) {
     if (n < 0 || n > 0xFFFFFFFFll || W < 1 || W > GC_MAX_WORKERS || capacity < 0) return GC_ERR_INVALID;
     if (!(p > 0.0 && p <= 1.0)) return GC_ERR_INVALID;
     if (!d_count || !workspace || !d_status || !models || (capacity > 0 && (!idx || !vals)))
@@ -538,6 +542,8 @@ int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* 
     a.d_status = d_status;
     a.group_mask = ws_group_mask(workspace, n);
     a.group_excl = ws_group_excl(workspace, n);
+    a.withhold_tile = withhold_tile;
+    a.wait_ns = wait_ns;
     // the counter and look-back states must start at zero; the group tables
     // are written in full by the kernel
     if (cudaMemsetAsync(workspace, 0, kWsHeader + sizeof(uint64_t) * static_cast<size_t>(a.ntiles), s) !=
@@ -545,6 +551,23 @@ int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* 
         return GC_ERR_CUDA;
     k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles), kThreads, 0, s>>>(a);
     return launch_status();
+}
+
+int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* models, int W,
+                      uint32_t* idx, float* const* vals, int64_t capacity, uint64_t* d_count,
+                      void* workspace, size_t workspace_bytes, int* d_status, gc_stream_t stream) {
+    return mask_compact_impl(n, p, seed_t, models, W, idx, vals, capacity, d_count, workspace,
+                             workspace_bytes, d_status, stream, -1, 1000000000ull);
+}
+
+int gc_testing_saps_mask_compact_withhold(int64_t n, double p, uint64_t seed_t,
+                                          const float* const* models, int W, uint32_t* idx,
+                                          float* const* vals, int64_t capacity, uint64_t* d_count,
+                                          void* workspace, size_t workspace_bytes, int* d_status,
+                                          int64_t withhold_tile, uint64_t wait_ns, gc_stream_t stream) {
+    if (wait_ns == 0 || wait_ns > 1000000000ull) return GC_ERR_INVALID;
+    return mask_compact_impl(n, p, seed_t, models, W, idx, vals, capacity, d_count, workspace,
+                             workspace_bytes, d_status, stream, withhold_tile, wait_ns);
 }
 
 int saps_peer_average(float* const* models, const float* const* vals, const uint32_t* idx,

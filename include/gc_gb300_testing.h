@@ -1,0 +1,37 @@
+/*
+ * gc_gb300_testing.h -- test hooks of libgc_gb300.so.  Not part of the
+ * production ABI; they exist so that the failure paths of the library can be
+ * exercised without faulting, trapping or hanging a GPU.
+ */
+#ifndef GC_GB300_TESTING_H
+#define GC_GB300_TESTING_H
+
+#include "gc_gb300.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * gc_testing_saps_mask_compact_withhold -- saps_mask_compact in which tile
+ * `withhold_tile` (4096 elements per tile) never publishes its look-back
+ * state, and every look-back wait is bounded by `wait_ns` nanoseconds
+ * (1 .. 10^9).  Its successors' waits run out, they count the silent tile as
+ * empty, record GC_ERR_TIMEOUT in *d_status and finish; the kernel returns
+ * and the CUDA context stays usable.  Arguments otherwise as
+ * saps_mask_compact (SAPS section II-B; the bounded decoupled look-back).
+ * Errors: as saps_mask_compact, and GC_ERR_INVALID for wait_ns out of range.
+ */
+GC_API int gc_testing_saps_mask_compact_withhold(int64_t n, double p, uint64_t seed_t,
+                                                 const float *const *models, int W,
+                                                 uint32_t *idx, float *const *vals,
+                                                 int64_t capacity, uint64_t *d_count,
+                                                 void *workspace, size_t workspace_bytes,
+                                                 int *d_status, int64_t withhold_tile,
+                                                 uint64_t wait_ns, gc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GC_GB300_TESTING_H */

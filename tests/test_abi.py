@@ -17,7 +17,8 @@ HEADER = os.path.join(ROOT, "include", "gc_gb300.h")
 
 
 def _declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^GC_API\s+[a-z0-9_ ]+?\**\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
     return sorted(set(names))
@@ -183,3 +184,12 @@ def test_fused_average_easgd_validation():
     assert with_(9, MISALIGNED) == gc.GC_ERR_ALIGN                          # center
     assert with_(7, float("nan")) == gc.GC_ERR_INVALID
     assert with_(5, 0) == gc.GC_OK                                          # n == 0 no-op
+
+
+def test_testing_hook_validates_its_wait_bound():
+    f = "gc_testing_saps_mask_compact_withhold"
+    ws = gc.saps_workspace_bytes(1000)
+    p1 = _ptrs(FAKE)
+    for bad in (0, 2_000_000_000):
+        assert _call(f, 1000, 0.01, 5, p1, 1, FAKE, p1, 100, FAKE, FAKE, ws, FAKE, 3, bad,
+                     None) == gc.GC_ERR_INVALID
