@@ -1,0 +1,155 @@
+"""Parity at the workloads' full sizes, on sampled outputs.
+
+Every output element's chain depends only on that element's inputs (2-bit,
+CD-SGD, EASGD), on its bucket (QSGD) or on its index's mask bit and the round's
+matching (SAPS), so the oracle runs on sampled chunks -- bucket-aligned,
+including the first and the ragged last one -- while the GPU runs the whole
+workload in the launch configuration bench.py times.  The SAPS counts are
+also checked against the oracle's full-size mask every round.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_compression_sgd_gc_gb300 as gc
+from gradient_compression_sgd_gc_gb300 import workloads as wl
+import oracle
+from gpu_helpers import assert_close, host_bf16_bits, host_f32, host_u32, sample_chunks
+from test_gpu_qsgd import compare_codes
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("cfg", [wl.QSGD_S7, wl.QSGD_S127], ids=lambda c: c.name)
+def test_qsgd_full_size_sampled(cfg):
+    n, W, d, s = cfg.n, cfg.workers, cfg.bucket, cfg.s
+    nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
+    vs = [wl.qsgd_grad(cfg, w, device=DEV) for w in range(W)]
+    norms = [torch.empty(nb, device=DEV) for _ in range(W)]
+    codes = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    for w in range(W):
+        gc.qsgd_quantize(vs[w], d, s, cfg.seed, w, norms[w], codes[w])
+    out = torch.empty(n, device=DEV)
+    gc.qsgd_dequant_sum(codes, norms, n, d, s, 1.0 / W, out)
+    torch.cuda.synchronize()
+    chunks = sample_chunks(n, 40, 4 * d, align=d, seed=11)
+    assert chunks[-1][1] == n and (n - chunks[-1][0]) % d == 296 % d
+    hn = [host_f32(x) for x in norms]
+    hc = [x.cpu().numpy() for x in codes]
+    ho = host_f32(out)
+    mism = 0
+    for lo, hi in chunks:
+        bad_any = np.zeros(hi - lo, bool)
+        rcs, rns = [], []
+        for w in range(W):
+            v = host_f32(vs[w][lo:hi])
+            rn, rc = oracle.qsgd_quantize(v, d, s, cfg.seed, w, i0=lo)
+            assert_close(hn[w][lo // d:(hi + d - 1) // d], rn, np.abs(rn), what="norms")
+            if s <= 7:
+                gcodes = hc[w][lo // 2:(hi + 1) // 2]
+            else:
+                gcodes = hc[w][lo:hi]
+            m, bad = compare_codes(gcodes, rc, v, hi - lo, d, s, cfg.seed, w, i0=lo)
+            mism += m
+            bad_any |= bad
+            rcs.append(rc)
+            rns.append(rn)
+        ref = oracle.qsgd_dequant_sum(rcs, rns, hi - lo, d, s, 1.0 / W)
+        terms = sum(np.abs(oracle.qsgd_dequant_sum([rcs[w]], [rns[w]], hi - lo, d, s)) for w in range(W)) / W
+        keep = ~bad_any
+        assert_close(ho[lo:hi][keep], ref[keep], terms[keep], what="dequant-sum")
+    print(f"{cfg.name}: level mismatches at boundaries in {len(chunks)} sampled chunks: {mism}")
+
+
+def test_cdsgd_full_size_sampled():
+    """4 workers x 1.3e9 bf16, 8 steps, k = 4: steps 1-3 and 5-7 quantise each
+    worker and apply the averaged dequantised sum, steps 4 and 8 apply the
+    residual-compensated full-precision average."""
+    cfg = wl.CDSGD
+    n, W, t, lr, k = cfg.n, cfg.workers, cfg.threshold, cfg.lr, cfg.correction_every
+    res = [torch.zeros(n, device=DEV) for _ in range(W)]
+    codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    wts = wl.twobit_weights(cfg, device=DEV, seed=8)
+    chunks = sample_chunks(n, 24, 8192, align=16, seed=5)
+    w_ref = {c: host_f32(wts[c[0]:c[1]]).astype(np.float64) for c in chunks}
+    scale = {c: np.abs(w_ref[c]).copy() for c in chunks}
+    r_ref = {(c, q): np.zeros(c[1] - c[0], np.float32) for c in chunks for q in range(W)}
+    for step in range(1, 9):
+        grads = [wl.twobit_grad(cfg, step, q, device=DEV) for q in range(W)]
+        gh = {(c, q): host_bf16_bits(grads[q][c[0]:c[1]]) for c in chunks for q in range(W)}
+        if step % k:
+            gc.gc_2bit_quantize_batched(grads, res, codes, t)
+            gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=wts)
+        else:
+            gc.gc_compensated_sum_update(grads, res, lr, wts)
+        torch.cuda.synchronize()
+        hc = codes
+        for c in chunks:
+            lo, hi = c
+            if step % k:
+                cr = [oracle.twobit_quantize(gh[(c, q)], r_ref[(c, q)], t) for q in range(W)]
+                oracle.twobit_dequant_sum_update(cr, hi - lo, t, oracle.KIND_SGD, lr=lr, weights=w_ref[c])
+                scale[c] += lr * t
+                for q in range(W):
+                    np.testing.assert_array_equal(host_u32(hc[q][lo // 16:(hi + 15) // 16]), cr[q])
+            else:
+                mag = sum(np.abs(r_ref[(c, q)].astype(np.float64))
+                          + np.abs((gh[(c, q)].astype(np.uint32) << 16).view(np.float32)) for q in range(W))
+                oracle.compensated_sum_update([gh[(c, q)] for q in range(W)],
+                                              [r_ref[(c, q)] for q in range(W)], lr, w_ref[c])
+                scale[c] += lr * mag / W
+        del grads
+    for c in chunks:
+        lo, hi = c
+        for q in range(W):
+            np.testing.assert_array_equal(host_f32(res[q][lo:hi]).view(np.uint32),
+                                          r_ref[(c, q)].view(np.uint32))
+        assert_close(host_f32(wts[lo:hi]), w_ref[c], scale[c], what=f"weights {c}")
+
+
+@pytest.mark.parametrize("cfg", [wl.SAPS_P01, wl.SAPS_P001], ids=lambda c: c.name)
+def test_saps_full_size_50_rounds_sampled(cfg):
+    """16 workers x 25,557,032, 50 rounds of mask + compaction, fused pair
+    average + elastic step, against the oracle on sampled chunks; the masked
+    count of every round against the oracle's full-size mask."""
+    n, W = cfg.n, cfg.workers
+    models = wl.saps_models(cfg, device=DEV)
+    center = wl.saps_initial_center(models)
+    cap = int(n * cfg.p * 1.2 + 10_000)
+    idx = torch.empty(cap, dtype=torch.int32, device=DEV)
+    vals = [torch.empty(cap, device=DEV) for _ in range(W)]
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    chunks = sample_chunks(n, 16, 4096, align=32, seed=9)
+    ref = {c: [host_f32(m[c[0]:c[1]]).astype(np.float64) for m in models] for c in chunks}
+    rc = {c: host_f32(center[c[0]:c[1]]).astype(np.float64) for c in chunks}
+    scale = {c: np.max(np.abs(np.stack(ref[c])), axis=0) + np.abs(rc[c]) for c in chunks}
+    for t in range(cfg.rounds):
+        seed_t = gc.saps_round_seed(cfg.base_seed, t)
+        pairs = gc.saps_matching(seed_t, W)
+        gc.saps_mask_compact(n, cfg.p, seed_t, models, idx, vals, cnt, ws, st)
+        gc.saps_average_easgd_step(models, vals, cnt, pairs, cfg.alpha, cfg.beta, center, ws)
+        for c in chunks:
+            lo, hi = c
+            Kc, ridx, rvals = oracle.saps_mask_compact(hi - lo, cfg.p, seed_t, ref[c], i0=lo)
+            oracle.saps_peer_average(ref[c], rvals, ridx - np.uint32(lo), np.array(pairs, np.int32))
+            oracle.easgd_step(ref[c], cfg.alpha, cfg.beta, rc[c])
+            scale[c] = np.maximum(scale[c], np.max(np.abs(np.stack(ref[c])), axis=0) + np.abs(rc[c]))
+        if t in (0, cfg.rounds - 1):
+            torch.cuda.synchronize()
+            Kfull = _full_mask_count(n, cfg.p, seed_t)
+            assert int(cnt.item()) == Kfull and int(st.item()) == 0
+    torch.cuda.synchronize()
+    for c in chunks:
+        lo, hi = c
+        for w in range(W):
+            assert_close(host_f32(models[w][lo:hi]), ref[c][w], scale[c], what=f"model {w} {c}")
+        assert_close(host_f32(center[lo:hi]), rc[c], scale[c], what=f"center {c}")
+
+
+def _full_mask_count(n, p, seed_t):
+    """The oracle's masked count over all n indices (one worker of zeros)."""
+    K, _, _ = oracle.saps_mask_compact(n, p, seed_t, [np.zeros(n)], capacity=0)
+    return K
