@@ -423,6 +423,24 @@ def rows(args, dev, peak):
                                     tm.ms("d"), peak, n)
     del g, r, c, o
 
+    # config 2 as one fused launch per step vs the two-launch path of the headline
+    cfg2 = wl.TWOBIT_DQ_SGD
+    n, W = cfg2.n, cfg2.workers
+    g2 = [wl.twobit_grad(cfg2, 0, w, device=dev) for w in range(W)]
+    r2 = [torch.zeros(n, device=dev) for _ in range(W)]
+    c2 = [torch.empty(gc.code_words(n), dtype=torch.int32, device=dev) for _ in range(W)]
+    w2 = wl.twobit_weights(cfg2, device=dev)
+    pf = gc.gc_2bit_step(g2, r2, c2, cfg2.threshold, gc.GC_UPD_SGD, lr=cfg2.lr, weights=w2, stream=stream,
+                         prepare=True)
+    tm = Timer(stream)
+    for i in range(reps + 3):
+        tm.around("f" if i >= 3 else "w", pf)
+    torch.cuda.synchronize(dev)
+    out["twobit_dq_sgd.fused_step"] = _row("twobit_dq_sgd", "gc_2bit_step (quantise 8 workers + dequant-sum + SGD)",
+                                           (W * 12.25 + 8) * n, tm.ms("f"), peak, W * n,
+                                           {"input_gradient_GBps": round(W * n * 4 / (_median(tm.ms("f")) * 1e-3) / 1e9, 1)})
+    del g2, r2, c2, w2
+
     # config 3: QSGD, 4 workers x 61,100,840, bucket 512, s = 7 and s = 127
     for qcfg in (wl.QSGD_S7, wl.QSGD_S127):
         n, W, s = qcfg.n, qcfg.workers, qcfg.s
@@ -509,13 +527,20 @@ def rows(args, dev, peak):
         pd = gc.gc_2bit_dequant_sum_update(codes, n, ccfg.threshold, gc.GC_UPD_SGD, lr=ccfg.lr, weights=wts,
                                            stream=stream, prepare=True)
         pc = gc.gc_compensated_sum_update(grads, res, ccfg.lr, wts, stream=stream, prepare=True)
+        local = [torch.empty(n, device=dev) for _ in range(W)]
+        pl = gc.gc_2bit_quantize_local(grads, res, codes, wts, local, ccfg.threshold, 0.1, stream=stream,
+                                       prepare=True)
         for i in range(5):
             k = "" if i >= 1 else "w"
             for w in range(W):
                 tm.around("q" + k, pq[w])
             tm.around("d" + k, pd)
             tm.around("c" + k, pc)
+            tm.around("l" + k, pl)
         torch.cuda.synchronize(dev)
+        out["cdsgd.quantize_local_update"] = _row("cdsgd", "gc_2bit_quantize_local bf16 W=4 (eq. 11 local weights)",
+                                                  (W * (2 + 8 + 0.25 + 4) + 4) * n, tm.ms("l"), peak, W * n)
+        del local
         out["cdsgd.quantize_bf16"] = _row("cdsgd", "gc_2bit_quantize bf16", 10.25 * n, tm.ms("q"), peak, n)
         out["cdsgd.dequant_sum_sgd"] = _row("cdsgd", "gc_2bit_dequant_sum_update SGD W=4", (W * 0.25 + 8) * n,
                                             tm.ms("d"), peak, n)
@@ -627,7 +652,7 @@ def reference_arm(args, rank, world, pg):
 
 # ----------------------------------------------------------------------------- profiling cases
 
-CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
+CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated")
 
 
@@ -654,6 +679,14 @@ def run_case(name: str, n: int):
         rs = [torch.zeros(m, device=dev) for _ in range(W)]
         cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(W)]
         fn = lambda: gc.gc_2bit_quantize_batched(gs, rs, cs, 2e-3)
+    elif name == "step_fused":
+        W = 8
+        m = n // W
+        gs = [wl.normal(m, 1e-3, 1 + w, device=dev) for w in range(W)]
+        rs = [torch.zeros(m, device=dev) for _ in range(W)]
+        cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(W)]
+        wt = torch.zeros(m, device=dev)
+        fn = lambda: gc.gc_2bit_step(gs, rs, cs, 2e-3, gc.GC_UPD_SGD, lr=0.1, weights=wt)
     elif name == "dqsum_sgd":
         W = 8
         cs = [torch.randint(-2 ** 31, 2 ** 31 - 1, (gc.code_words(n),), dtype=torch.int32, device=dev)

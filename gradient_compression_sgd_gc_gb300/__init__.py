@@ -8,7 +8,8 @@ no CPU or PyTorch fallback: if the library cannot be built or loaded, every
 call raises.
 
 Entry points (same names as the C ABI):
-  gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update,
+  gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update, gc_2bit_step,
+  gc_2bit_quantize_local,
   gc_compensated_sum_update,
   qsgd_quantize, qsgd_dequant_sum,
   saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
@@ -35,6 +36,7 @@ __all__ = [
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
+    "gc_2bit_step", "gc_2bit_quantize_local",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -74,6 +76,8 @@ def load():
             "gc_version": (i32, []),
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
             "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
+            "gc_2bit_step": (i32, [vp, i32, vp, vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
+            "gc_2bit_quantize_local": (i32, [vp, i32, vp, vp, vp, vp, i32, i64, f32, f32, vp]),
             "gc_2bit_dequant_sum_update": (i32, [vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
             "gc_compensated_sum_update": (i32, [vp, i32, vp, i32, i64, f32, vp, vp]),
             "qsgd_quantize": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
@@ -217,6 +221,41 @@ def gc_2bit_quantize_batched(grads, residuals, codes, threshold: float, stream=N
             n_arr, B, float(threshold), _stream(stream, residuals[0]))
     return _invoke(lib.gc_2bit_quantize_batched, args, "gc_2bit_quantize_batched", prepare,
                    (list(grads), list(residuals), list(codes), n_arr))
+
+
+def gc_2bit_step(grads, residuals, codes, threshold: float, kind: int = GC_UPD_SGD, lr: float = 0.0,
+                 alpha: float = 0.0, center=None, weights=None, out=None, stream=None,
+                 prepare: bool = False):
+    """Quantise W equal-sized fp32 gradients and apply the dequant-sum update in
+    one pass (bit-identical to gc_2bit_quantize_batched + gc_2bit_dequant_sum_update)."""
+    lib = load()
+    W = len(grads)
+    n = grads[0].numel()
+    args = (_ptrs(grads, "grads", torch.float32, n, pinned_ok=True), GC_F32,
+            _ptrs(residuals, "residuals", torch.float32, n), _ptrs(codes, "codes", torch.int32, code_words(n)),
+            W, n, float(threshold), int(kind), float(lr), float(alpha),
+            _dev(center, "center", torch.float32, n) if center is not None else None,
+            _dev(weights, "weights", torch.float32, n) if weights is not None else None,
+            _dev(out, "out", torch.float32, n) if out is not None else None,
+            _stream(stream, residuals[0]))
+    return _invoke(lib.gc_2bit_step, args, "gc_2bit_step", prepare,
+                   (list(grads), list(residuals), list(codes), center, weights, out))
+
+
+def gc_2bit_quantize_local(grads, residuals, codes, weights: torch.Tensor, local_weights,
+                           threshold: float, local_lr: float, stream=None, prepare: bool = False):
+    """gc_2bit_quantize on B workers plus CD-SGD eq. 11 local weights
+    local_weights[b] = weights - local_lr * grads[b], one launch."""
+    lib = load()
+    B = len(grads)
+    n = weights.numel()
+    dt = _gdtype(grads[0])
+    args = (_ptrs(grads, "grads", grads[0].dtype, n, pinned_ok=True), dt,
+            _ptrs(residuals, "residuals", torch.float32, n), _ptrs(codes, "codes", torch.int32, code_words(n)),
+            _dev(weights, "weights", torch.float32, n), _ptrs(local_weights, "local_weights", torch.float32, n),
+            B, n, float(threshold), float(local_lr), _stream(stream, weights))
+    return _invoke(lib.gc_2bit_quantize_local, args, "gc_2bit_quantize_local", prepare,
+                   (list(grads), list(residuals), list(codes), weights, list(local_weights)))
 
 
 def gc_2bit_dequant_sum_update(codes, n: int, threshold: float, kind: int = GC_UPD_NONE,

@@ -391,6 +391,272 @@ k_2bit_dqsum(const DqArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ K1+K2 fused
+
+// The whole 2-bit step of W workers held on this GPU in one pass: for every
+// 512-element tile a warp quantises the tile of each worker in turn (codes
+// and residuals written as gc_2bit_quantize does), keeps each element's
+// decoded sum in registers instead of re-reading the codes, and applies the
+// update as gc_2bit_dequant_sum_update does -- the outputs are bit-identical
+// to those two calls.  Worker w+1's gradient and residual loads are issued
+// before worker w's tile is processed.
+struct StepArgs {
+    PtrTable<const void*> grads;
+    PtrTable<float*> res;
+    PtrTable<uint32_t*> codes;
+    int W;
+    int64_t n;
+    float t;
+    float k_out, k_lr, alpha;
+    const float* center;
+    float* weights;
+    float* out;
+};
+
+template <int KIND>
+__device__ __forceinline__ void step_apply(const StepArgs& a, int64_t e0, const float (&cnt)[4], float4 w,
+                                           float4 c) {
+    if (KIND == GC_UPD_NONE) {
+        st_stream_f4(a.out + e0, make_float4(cnt[0] * a.k_out, cnt[1] * a.k_out, cnt[2] * a.k_out,
+                                             cnt[3] * a.k_out));
+    } else {
+        float4 nw;
+        nw.x = fmaf(-cnt[0], a.k_lr, w.x);
+        nw.y = fmaf(-cnt[1], a.k_lr, w.y);
+        nw.z = fmaf(-cnt[2], a.k_lr, w.z);
+        nw.w = fmaf(-cnt[3], a.k_lr, w.w);
+        if (KIND == GC_UPD_EASGD) {
+            nw.x = fmaf(-a.alpha, w.x - c.x, nw.x);
+            nw.y = fmaf(-a.alpha, w.y - c.y, nw.y);
+            nw.z = fmaf(-a.alpha, w.z - c.z, nw.z);
+            nw.w = fmaf(-a.alpha, w.w - c.w, nw.w);
+        }
+        st_stream_f4(a.weights + e0, nw);
+    }
+}
+
+// fp32 quantise of one float4 that also returns the decoded values (+1/-1/0)
+__device__ __forceinline__ uint32_t quantize4_dec(float4& r, const float4 g, float t, int (&d)[4]) {
+    uint32_t c0 = quantize1(r.x, g.x, t), c1 = quantize1(r.y, g.y, t);
+    uint32_t c2 = quantize1(r.z, g.z, t), c3 = quantize1(r.w, g.w, t);
+    d[0] = (c0 == 3u) - (c0 == 2u);
+    d[1] = (c1 == 3u) - (c1 == 2u);
+    d[2] = (c2 == 3u) - (c2 == 2u);
+    d[3] = (c3 == 3u) - (c3 == 2u);
+    return (c0 << 6) | (c1 << 4) | (c2 << 2) | c3;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 2)
+k_2bit_step_f32(const StepArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nfull = a.n / kTile;
+    if (tile < nfull) {
+        const int64_t base = tile * kTile + 4 * lane;
+        float4 wv[4], cv[4];
+        if (KIND != GC_UPD_NONE) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wv[j] = ld_f4(a.weights + base + 128 * j);
+        }
+        if (KIND == GC_UPD_EASGD) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cv[j] = ld_stream_f4(a.center + base + 128 * j);
+        }
+        int cnt[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cnt[j][k] = 0;
+        float4 ga[4], ra[4];
+        {
+            const float* g = static_cast<const float*>(a.grads.p[0]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ga[j] = ld_stream_f4(g + base + 128 * j);
+                ra[j] = ld_f4(a.res.p[0] + base + 128 * j);
+            }
+        }
+        for (int w = 0; w < a.W; ++w) {
+            float4 gb[4], rb[4];
+            if (w + 1 < a.W) {
+                const float* g = static_cast<const float*>(a.grads.p[w + 1]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    gb[j] = ld_stream_f4(g + base + 128 * j);
+                    rb[j] = ld_f4(a.res.p[w + 1] + base + 128 * j);
+                }
+            }
+            float* r = a.res.p[w];
+            uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[w]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                int d[4];
+                const uint32_t c = quantize4_dec(ra[j], ga[j], a.t, d);
+                st_stream_f4(r + base + 128 * j, ra[j]);
+                cb[code_byte(base + 128 * j)] = static_cast<uint8_t>(c);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cnt[j][k] += d[k];
+            }
+            if (w + 1 < a.W) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ga[j] = gb[j];
+                    ra[j] = rb[j];
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float cf[4] = {static_cast<float>(cnt[j][0]), static_cast<float>(cnt[j][1]),
+                                 static_cast<float>(cnt[j][2]), static_cast<float>(cnt[j][3])};
+            step_apply<KIND>(a, base + 128 * j, cf, wv[j], cv[j]);
+        }
+    } else if (tile == nfull && a.n % kTile != 0) {
+        // partial last tile: element by element
+        const int64_t nwords = (a.n + 15) >> 4;
+        for (int j = 0; j < 4; ++j) {
+            const int64_t e0 = nfull * kTile + 128 * j + 4 * lane;
+            int cnt[4] = {0, 0, 0, 0};
+            for (int w = 0; w < a.W; ++w) {
+                const float* g = static_cast<const float*>(a.grads.p[w]);
+                float* r = a.res.p[w];
+                uint32_t cbits = 0;
+                for (int k = 0; k < 4; ++k) {
+                    const int64_t e = e0 + k;
+                    if (e < a.n) {
+                        float rr = r[e];
+                        const uint32_t c = quantize1(rr, g[e], a.t);
+                        r[e] = rr;
+                        cbits |= c << (6 - 2 * k);
+                        cnt[k] += (c == 3u) - (c == 2u);
+                    }
+                }
+                if ((e0 >> 4) < nwords) reinterpret_cast<uint8_t*>(a.codes.p[w])[code_byte(e0)] = static_cast<uint8_t>(cbits);
+            }
+            for (int k = 0; k < 4; ++k) {
+                const int64_t e = e0 + k;
+                if (e >= a.n) break;
+                const float cf = static_cast<float>(cnt[k]);
+                if (KIND == GC_UPD_NONE) {
+                    a.out[e] = cf * a.k_out;
+                } else {
+                    const float wo = a.weights[e];
+                    float nw = fmaf(-cf, a.k_lr, wo);
+                    if (KIND == GC_UPD_EASGD) nw = fmaf(-a.alpha, wo - a.center[e], nw);
+                    a.weights[e] = nw;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ K1 + CD-SGD local update
+
+// CD-SGD eq. 11: while worker w's gradient is in registers for the 2-bit
+// quantiser, its local weights W_loc[w] = W - local_lr * g are written too
+// (W = the global weights, shared by all workers).  The grid visits the B
+// workers of one tile on adjacent warps, so the B reads of a W tile meet in L2.
+struct LocalArgs {
+    PtrTable<const void*> grads;
+    PtrTable<float*> res;
+    PtrTable<uint32_t*> codes;
+    PtrTable<float*> local;
+    const float* weights;
+    int B;
+    int64_t n;
+    float t, local_lr;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads)
+k_2bit_quantize_local(const LocalArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t T = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t ntiles = (a.n + kTile - 1) / kTile;
+    if (T >= ntiles * a.B) return;
+    const int64_t tile = T / a.B;
+    const int b = static_cast<int>(T - tile * a.B);
+    const int64_t nfull = a.n / kTile;
+    float* __restrict__ r = a.res.p[b];
+    float* __restrict__ wl = a.local.p[b];
+    const float t = a.t, lr = a.local_lr;
+    if (tile < nfull) {
+        const int64_t base = tile * kTile + (BF16 ? 8 : 4) * lane;
+        if (!BF16) {
+            const float* __restrict__ g = static_cast<const float*>(a.grads.p[b]);
+            uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[b]);
+            float4 gv[4], rv[4], wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                gv[j] = ld_stream_f4(g + base + 128 * j);
+                rv[j] = ld_f4(r + base + 128 * j);
+                wv[j] = __ldg(reinterpret_cast<const float4*>(a.weights + base + 128 * j));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                st_stream_f4(wl + base + 128 * j,
+                             make_float4(fmaf(-lr, gv[j].x, wv[j].x), fmaf(-lr, gv[j].y, wv[j].y),
+                                         fmaf(-lr, gv[j].z, wv[j].z), fmaf(-lr, gv[j].w, wv[j].w)));
+                const uint32_t c = quantize4(rv[j], gv[j], t);
+                st_stream_f4(r + base + 128 * j, rv[j]);
+                cb[code_byte(base + 128 * j)] = static_cast<uint8_t>(c);
+            }
+        } else {
+            const uint16_t* __restrict__ g = static_cast<const uint16_t*>(a.grads.p[b]);
+            uint16_t* ch = reinterpret_cast<uint16_t*>(a.codes.p[b]);
+            uint4 gv[2];
+            float4 rv[4], wv[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                gv[j] = ld_stream_u4(g + base + 256 * j);
+                rv[2 * j] = ld_f4(r + base + 256 * j);
+                rv[2 * j + 1] = ld_f4(r + base + 256 * j + 4);
+                wv[2 * j] = __ldg(reinterpret_cast<const float4*>(a.weights + base + 256 * j));
+                wv[2 * j + 1] = __ldg(reinterpret_cast<const float4*>(a.weights + base + 256 * j + 4));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float4 g0 = make_float4(bf16lo(gv[j].x), bf16hi(gv[j].x), bf16lo(gv[j].y), bf16hi(gv[j].y));
+                const float4 g1 = make_float4(bf16lo(gv[j].z), bf16hi(gv[j].z), bf16lo(gv[j].w), bf16hi(gv[j].w));
+                st_stream_f4(wl + base + 256 * j,
+                             make_float4(fmaf(-lr, g0.x, wv[2 * j].x), fmaf(-lr, g0.y, wv[2 * j].y),
+                                         fmaf(-lr, g0.z, wv[2 * j].z), fmaf(-lr, g0.w, wv[2 * j].w)));
+                st_stream_f4(wl + base + 256 * j + 4,
+                             make_float4(fmaf(-lr, g1.x, wv[2 * j + 1].x), fmaf(-lr, g1.y, wv[2 * j + 1].y),
+                                         fmaf(-lr, g1.z, wv[2 * j + 1].z), fmaf(-lr, g1.w, wv[2 * j + 1].w)));
+                const uint32_t c = (quantize4(rv[2 * j], g0, t) << 8) | quantize4(rv[2 * j + 1], g1, t);
+                st_stream_f4(r + base + 256 * j, rv[2 * j]);
+                st_stream_f4(r + base + 256 * j + 4, rv[2 * j + 1]);
+                const int64_t e = base + 256 * j;
+                ch[2 * (e >> 4) + 1 - ((e >> 3) & 1)] = static_cast<uint16_t>(c);
+            }
+        }
+    } else {
+        // partial last tile
+        const int64_t t0 = nfull * kTile;
+        const int64_t nwords = (a.n + 15) >> 4;
+        uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[b]);
+        for (int j = 0; j < 4; ++j) {
+            const int64_t e0 = t0 + 128 * j + 4 * lane;
+            uint32_t cbits = 0;
+            for (int k = 0; k < 4; ++k) {
+                const int64_t e = e0 + k;
+                if (e < a.n) {
+                    const float gval = BF16 ? __uint_as_float(static_cast<uint32_t>(
+                                                  static_cast<const uint16_t*>(a.grads.p[b])[e]) << 16)
+                                            : static_cast<const float*>(a.grads.p[b])[e];
+                    wl[e] = fmaf(-lr, gval, a.weights[e]);
+                    float rr = r[e];
+                    cbits |= quantize1(rr, gval, t) << (6 - 2 * k);
+                    r[e] = rr;
+                }
+            }
+            if ((e0 >> 4) < nwords) cb[code_byte(e0)] = static_cast<uint8_t>(cbits);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ K3
 
 struct CompArgs {
@@ -595,6 +861,85 @@ int gc_2bit_dequant_sum_update(const uint32_t* const* codes, int W, int64_t n, f
         case GC_UPD_SGD: k_2bit_dqsum<GC_UPD_SGD><<<grid, kThreads, 0, s>>>(a); break;
         default: k_2bit_dqsum<GC_UPD_EASGD><<<grid, kThreads, 0, s>>>(a); break;
     }
+    return launch_status();
+}
+
+int gc_2bit_step(const void* const* grads, gc_dtype dtype, float* const* residuals, uint32_t* const* codes,
+                 int W, int64_t n, float threshold, gc_update kind, float lr, float alpha,
+                 const float* center, float* weights, float* out, gc_stream_t stream) {
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !finite_pos(threshold) || dtype != GC_F32) return GC_ERR_INVALID;
+    if (kind != GC_UPD_NONE && kind != GC_UPD_SGD && kind != GC_UPD_EASGD) return GC_ERR_INVALID;
+    if (!isfinite(lr) || !isfinite(alpha)) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grads || !residuals || !codes) return GC_ERR_INVALID;
+    StepArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!grads[w] || !residuals[w] || !codes[w]) return GC_ERR_INVALID;
+        if (!aligned16(grads[w]) || !aligned16(residuals[w]) || !aligned16(codes[w])) return GC_ERR_ALIGN;
+        a.grads.p[w] = grads[w];
+        a.res.p[w] = residuals[w];
+        a.codes.p[w] = codes[w];
+    }
+    if (kind == GC_UPD_NONE) {
+        if (!out) return GC_ERR_INVALID;
+        if (!aligned16(out)) return GC_ERR_ALIGN;
+    } else {
+        if (!weights) return GC_ERR_INVALID;
+        if (!aligned16(weights)) return GC_ERR_ALIGN;
+        if (kind == GC_UPD_EASGD) {
+            if (!center) return GC_ERR_INVALID;
+            if (!aligned16(center)) return GC_ERR_ALIGN;
+        }
+    }
+    a.W = W;
+    a.n = n;
+    a.t = threshold;
+    a.k_out = static_cast<float>(static_cast<double>(threshold) / W);
+    a.k_lr = static_cast<float>(static_cast<double>(lr) * threshold / W);
+    a.alpha = alpha;
+    a.center = center;
+    a.weights = weights;
+    a.out = out;
+    const unsigned grid = blocks_for_tiles((n + 511) / 512);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (kind) {
+        case GC_UPD_NONE: k_2bit_step_f32<GC_UPD_NONE><<<grid, kThreads, 0, s>>>(a); break;
+        case GC_UPD_SGD: k_2bit_step_f32<GC_UPD_SGD><<<grid, kThreads, 0, s>>>(a); break;
+        default: k_2bit_step_f32<GC_UPD_EASGD><<<grid, kThreads, 0, s>>>(a); break;
+    }
+    return launch_status();
+}
+
+int gc_2bit_quantize_local(const void* const* grads, gc_dtype dtype, float* const* residuals,
+                           uint32_t* const* codes, const float* weights, float* const* local_weights,
+                           int B, int64_t n, float threshold, float local_lr, gc_stream_t stream) {
+    if (n < 0 || B < 1 || B > GC_MAX_WORKERS || !finite_pos(threshold) || !isfinite(local_lr) ||
+        (dtype != GC_F32 && dtype != GC_BF16))
+        return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grads || !residuals || !codes || !weights || !local_weights) return GC_ERR_INVALID;
+    if (!aligned16(weights)) return GC_ERR_ALIGN;
+    LocalArgs a;
+    for (int b = 0; b < B; ++b) {
+        if (!grads[b] || !residuals[b] || !codes[b] || !local_weights[b]) return GC_ERR_INVALID;
+        if (!aligned16(grads[b]) || !aligned16(residuals[b]) || !aligned16(codes[b]) || !aligned16(local_weights[b]))
+            return GC_ERR_ALIGN;
+        a.grads.p[b] = grads[b];
+        a.res.p[b] = residuals[b];
+        a.codes.p[b] = codes[b];
+        a.local.p[b] = local_weights[b];
+    }
+    a.weights = weights;
+    a.B = B;
+    a.n = n;
+    a.t = threshold;
+    a.local_lr = local_lr;
+    const unsigned grid = blocks_for_tiles((n + 511) / 512 * B);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == GC_F32)
+        k_2bit_quantize_local<false><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_2bit_quantize_local<true><<<grid, kThreads, 0, s>>>(a);
     return launch_status();
 }
 

@@ -153,6 +153,44 @@ GC_API int gc_2bit_dequant_sum_update(const uint32_t *const *codes, int W, int64
                                float *weights, float *out, gc_stream_t stream);
 
 /*
+ * gc_2bit_step -- gc_2bit_quantize_batched over W equal-sized fp32 buffers
+ * followed by gc_2bit_dequant_sum_update, in one pass: each element's
+ * decoded sum is formed while its codes are produced, so the codes are
+ * written but not read back.  Codes, residuals and the update are
+ * bit-identical to the two separate calls.  (MXNet PR #8662 "Local kvstore":
+ * every device quantises, one sums the dequantised values; CD-SGD eq. 10.)
+ *
+ *   grads, residuals, codes   host arrays of W pointers as in the batched
+ *                             quantiser (fp32 gradients only)
+ *   kind, lr, alpha, center, weights, out
+ *                             as gc_2bit_dequant_sum_update
+ * Errors: GC_ERR_INVALID (also dtype other than GC_F32), GC_ERR_ALIGN,
+ * GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_step(const void *const *grads, gc_dtype dtype,
+                        float *const *residuals, uint32_t *const *codes, int W,
+                        int64_t n, float threshold, gc_update kind, float lr,
+                        float alpha, const float *center, float *weights,
+                        float *out, gc_stream_t stream);
+
+/*
+ * gc_2bit_quantize_local -- gc_2bit_quantize on B workers' gradients (one
+ * launch), each also producing the worker's local weights of CD-SGD eq. 11
+ * (Algorithm 1 line 24): local_weights[b][i] = weights[i] - local_lr *
+ * grad[b][i] (one fma), from the global weights before this step's update.
+ *
+ *   weights        device fp32 [n], the global weights, read only
+ *   local_weights  host array of B device pointers, fp32 [n], written
+ *   other arguments as gc_2bit_quantize_batched, with one size n for all
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_quantize_local(const void *const *grads, gc_dtype dtype,
+                                  float *const *residuals, uint32_t *const *codes,
+                                  const float *weights, float *const *local_weights,
+                                  int B, int64_t n, float threshold, float local_lr,
+                                  gc_stream_t stream);
+
+/*
  * gc_compensated_sum_update -- CD-SGD, Algorithm 1 (the branch taken every
  * k-th step, where the 32-bit gradient is pushed uncompressed) and section
  * 3.1 (k-step correction).  Reading: the pushed message is the

@@ -62,6 +62,7 @@ def _load():
             "orc_2bit_quantize": (None, [vp, i32, vp, vp, i64, f32]),
             "orc_2bit_dequant_sum_update": (None, [vp, i32, i64, f32, i32, f64, f64, vp, vp, vp]),
             "orc_compensated_sum_update": (None, [vp, i32, vp, i32, i64, f64, vp]),
+            "orc_cdsgd_local_update": (None, [vp, i32, vp, vp, i64, f64]),
             "orc_l2norm_fp32": (f32, [vp, i64]),
             "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_qsgd_scaled_values": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
@@ -178,6 +179,16 @@ def compensated_sum_update(grads, residuals, lr: float, weights: np.ndarray) -> 
     _check(weights, np.float64, "weights", n)
     _load().orc_compensated_sum_update(_ptr_array(grads), kind, _ptr_array(residuals), W, n,
                                        float(np.float32(lr)), _ptr(weights))
+
+
+def cdsgd_local_update(grad: np.ndarray, weights: np.ndarray, lr: float) -> np.ndarray:
+    """CD-SGD eq. 11: local weights = weights - lr * grad (fp64)."""
+    n = grad.size
+    kind = _grad_kind(grad)
+    _check(weights, np.float64, "weights", n)
+    out = np.zeros(n, dtype=np.float64)
+    _load().orc_cdsgd_local_update(_ptr(grad), kind, _ptr(weights), _ptr(out), n, float(np.float32(lr)))
+    return out
 
 
 # --------------------------------------------------------------------------

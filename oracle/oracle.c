@@ -183,6 +183,18 @@ void orc_compensated_sum_update(const void *const *grads, int is_bf16,
     }
 }
 
+/*
+ * [CD] eq. 11 and Algorithm 1 line 24: each worker's local weights are the
+ * global weights of the previous step moved by its own uncompressed
+ * gradient, W_loc = W - eta_loc * grad (fp64).
+ */
+void orc_cdsgd_local_update(const void *grad, int is_bf16, const double *w,
+                            double *local, int64_t n, double lr)
+{
+    for (int64_t i = 0; i < n; ++i)
+        local[i] = w[i] - lr * (double)grad_at(grad, is_bf16, i);
+}
+
 /* ------------------------------------------------------------------------ */
 /* [QS] QSGD stochastic quantisation                                        */
 /* ------------------------------------------------------------------------ */

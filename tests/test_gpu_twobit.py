@@ -292,3 +292,58 @@ def test_quantize_reads_pinned_host_gradients_in_place():
     c_ref = oracle.twobit_quantize(g_host.numpy(), r_ref, t)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(host_u32(codes), c_ref)
+
+
+@pytest.mark.parametrize("kind", [gc.GC_UPD_NONE, gc.GC_UPD_SGD, gc.GC_UPD_EASGD])
+@pytest.mark.parametrize("n,W", [(1, 1), (513, 3), (100_003, 8), (262_144, 2)])
+def test_fused_step_is_bitwise_the_two_calls(kind, n, W):
+    t, lr, alpha = 2e-3, 0.1, 0.9
+    grads = [wl.normal(n, 1e-3, 60 + w, device=DEV) for w in range(W)]
+    r0 = [wl.normal(n, 1e-3, 80 + w, device=DEV) for w in range(W)]
+    w0 = wl.uniform(n, 0.05, 7, device=DEV)
+    c0 = wl.uniform(n, 0.05, 9, device=DEV)
+    ra, rb = [x.clone() for x in r0], [x.clone() for x in r0]
+    ca = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    cb = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    wa, wb = w0.clone(), w0.clone()
+    oa, ob = torch.empty(n, device=DEV), torch.empty(n, device=DEV)
+    kw = dict(lr=lr, alpha=alpha, center=c0 if kind == gc.GC_UPD_EASGD else None,
+              weights=None if kind == gc.GC_UPD_NONE else None)
+    gc.gc_2bit_quantize_batched(grads, ra, ca, t)
+    gc.gc_2bit_dequant_sum_update(ca, n, t, kind, lr=lr, alpha=alpha, center=kw["center"],
+                                  weights=wa if kind != gc.GC_UPD_NONE else None,
+                                  out=oa if kind == gc.GC_UPD_NONE else None)
+    gc.gc_2bit_step(grads, rb, cb, t, kind, lr=lr, alpha=alpha, center=kw["center"],
+                    weights=wb if kind != gc.GC_UPD_NONE else None, out=ob if kind == gc.GC_UPD_NONE else None)
+    torch.cuda.synchronize()
+    for w in range(W):
+        assert torch.equal(ra[w].view(torch.int32), rb[w].view(torch.int32))
+        assert torch.equal(ca[w], cb[w])
+    if kind == gc.GC_UPD_NONE:
+        assert torch.equal(oa.view(torch.int32), ob.view(torch.int32))
+    else:
+        assert torch.equal(wa.view(torch.int32), wb.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n,B", [(1, 1), (517, 2), (100_003, 4)])
+def test_quantize_with_local_update(n, B, dtype):
+    t, lr_loc = 1e-3, 0.1
+    grads = [wl.normal(n, 5e-4, 90 + b, device=DEV, dtype=dtype) for b in range(B)]
+    res = [torch.zeros(n, device=DEV) for _ in range(B)]
+    codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(B)]
+    weights = wl.uniform(n, 0.05, 8, device=DEV)
+    local = [guarded(n, torch.float32) for _ in range(B)]
+    gc.gc_2bit_quantize_local(grads, res, codes, weights, [x[:n] for x in local], t, lr_loc)
+    torch.cuda.synchronize()
+    wh = host_f32(weights).astype(np.float64)
+    for b in range(B):
+        gh = _grad_host(grads[b])
+        r_ref = np.zeros(n, np.float32)
+        c_ref = oracle.twobit_quantize(gh, r_ref, t)
+        np.testing.assert_array_equal(host_u32(codes[b]), c_ref)
+        np.testing.assert_array_equal(host_f32(res[b]).view(np.uint32), r_ref.view(np.uint32))
+        l_ref = oracle.cdsgd_local_update(gh, wh, lr_loc)
+        gf = gh if dtype == torch.float32 else (gh.astype(np.uint32) << 16).view(np.float32)
+        assert_close(host_f32(local[b][:n]), l_ref, np.abs(wh) + lr_loc * np.abs(gf), what="local weights")
+        check_guard(local[b], n)

@@ -273,3 +273,20 @@ def test_correction_with_bf16_gradients():
     oracle.compensated_sum_update(bits, ra, 0.01, wa)
     oracle.compensated_sum_update(asf, rb, 0.01, wb)
     np.testing.assert_array_equal(wa, wb)
+
+
+def test_local_update_pins():
+    """CD-SGD eq. 11: lr = 0 or g = 0 leaves the local copy equal to the
+    global weights; on dyadic inputs (w - local) / lr is the gradient exactly;
+    bf16 bits give the same as their fp32 values."""
+    rng = np.random.default_rng(12)
+    n = 400
+    w = _dyadic(rng, n).astype(np.float64)
+    g = _dyadic(rng, n)
+    np.testing.assert_array_equal(oracle.cdsgd_local_update(g, w, 0.0), w)
+    np.testing.assert_array_equal(oracle.cdsgd_local_update(np.zeros(n, np.float32), w, 0.1), w)
+    loc = oracle.cdsgd_local_update(g, w, 0.125)
+    np.testing.assert_array_equal((w - loc) / 0.125, g.astype(np.float64))
+    bits = (g.view(np.uint32) >> 16).astype(np.uint16)
+    asf = (bits.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_array_equal(oracle.cdsgd_local_update(bits, w, 0.1), oracle.cdsgd_local_update(asf, w, 0.1))
