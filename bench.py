@@ -463,6 +463,14 @@ def rows(args, dev, peak):
                                             peak, n)
         out[f"{qcfg.name}.dequant_sum"] = _row(qcfg.name, "qsgd_dequant_sum", W * (cb + 4 * nb) + 4 * n,
                                                tm.ms("d"), peak, W * n)
+        pm = [gc.qsgd_quantize_maxnorm(vs[w], qcfg.bucket, s, qcfg.seed, w, norms[w], codes[w], stream=stream,
+                                       prepare=True) for w in range(W)]
+        for i in range(6):
+            for w in range(W):
+                tm.around("m" if i >= 2 else "w", pm[w])
+        torch.cuda.synchronize(dev)
+        out[f"{qcfg.name}.quantize_maxnorm"] = _row(qcfg.name, "qsgd_quantize_maxnorm", n * 4 + cb + 4 * nb,
+                                                    tm.ms("m"), peak, n)
         del vs, norms, codes, outq
 
     # config 5: SAPS + EASGD, 16 workers x 25,557,032, p = 0.01 and 0.001

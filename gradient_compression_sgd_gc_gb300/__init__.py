@@ -11,7 +11,7 @@ Entry points (same names as the C ABI):
   gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update, gc_2bit_step,
   gc_2bit_quantize_local,
   gc_compensated_sum_update,
-  qsgd_quantize, qsgd_dequant_sum,
+  qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum,
   saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
   saps_peer_average, saps_average_easgd_step, easgd_step, gc_status_string,
   gc_version
@@ -36,7 +36,7 @@ __all__ = [
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
-    "gc_2bit_step", "gc_2bit_quantize_local",
+    "gc_2bit_step", "gc_2bit_quantize_local", "qsgd_quantize_maxnorm",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -82,6 +82,7 @@ def load():
             "gc_compensated_sum_update": (i32, [vp, i32, vp, i32, i64, f32, vp, vp]),
             "qsgd_quantize": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
             "qsgd_dequant_sum": (i32, [vp, vp, i32, i64, i32, i32, f32, vp, vp]),
+            "qsgd_quantize_maxnorm": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
             "saps_round_seed": (u64, [u64, u64]),
             "saps_matching": (i32, [u64, i32, vp]),
             "saps_workspace_bytes": (sz, [i64]),
@@ -297,6 +298,18 @@ def qsgd_quantize(grad: torch.Tensor, bucket: int, s_levels: int, seed: int, wor
             _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
             _stream(stream, grad))
     return _invoke(lib.qsgd_quantize, args, "qsgd_quantize", prepare, (grad, norms, codes))
+
+
+def qsgd_quantize_maxnorm(grad: torch.Tensor, bucket: int, s_levels: int, seed: int, worker: int,
+                          scales: torch.Tensor, codes: torch.Tensor, stream=None, prepare: bool = False):
+    """QSGD with each bucket scaled by its max |v| (Knowl 8)."""
+    lib = load()
+    n = grad.numel()
+    args = (_dev(grad, "grad", torch.float32), n, int(bucket), int(s_levels),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, int(worker),
+            _dev(scales, "scales", torch.float32, qsgd_num_buckets(n, bucket)),
+            _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)), _stream(stream, grad))
+    return _invoke(lib.qsgd_quantize_maxnorm, args, "qsgd_quantize_maxnorm", prepare, (grad, scales, codes))
 
 
 def qsgd_dequant_sum(codes, norms, n: int, bucket: int, s_levels: int, scale: float,

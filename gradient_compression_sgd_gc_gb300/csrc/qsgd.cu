@@ -108,7 +108,7 @@ __device__ __forceinline__ bool all_zero(const float4 (&v)[ROUNDS], int lane) {
 }
 
 // One warp per bucket; the grid covers every bucket.
-template <int ROUNDS, bool FOUR>
+template <int ROUNDS, bool FOUR, bool MAXNORM>
 __global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
 k_qsgd_quantize(const QArgs a) {
     const int lane = threadIdx.x & 31;
@@ -135,6 +135,17 @@ k_qsgd_quantize(const QArgs a) {
             v[j].w = e + 3 < a.n ? a.v[e + 3] : 0.0f;
         }
     }
+    float norm;
+    if (MAXNORM) {
+        // QSGD Knowl 8 max-norm scaling: the bucket's largest |v| (exact)
+        float mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < ROUNDS; ++j)
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        norm = mx;
+    } else {
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
@@ -143,7 +154,7 @@ k_qsgd_quantize(const QArgs a) {
         acc_square(v[j].z, hi, lo);
         acc_square(v[j].w, hi, lo);
     }
-    float norm = warp_norm(hi, lo);
+    norm = warp_norm(hi, lo);
     // A sum of squares below 2^-100 may have lost bits to underflow and one
     // above 2^126 overflows: such buckets (subnormal-sized or huge gradients;
     // the test is warp-uniform) are redone with every value scaled by the
@@ -170,6 +181,7 @@ k_qsgd_quantize(const QArgs a) {
         }
         warp_sum2(h2, l2);
         norm = ldexpf(df_sqrt(h2, l2), ex);
+    }
     }
     if (lane == 0) a.norms[b] = norm;
     // norm == 0 means every coordinate is +-0: sign bit 0, level 0, code 0
@@ -336,14 +348,14 @@ k_qsgd_dequant_sum(const DArgs a) {
     }
 }
 
-template <bool FOUR>
+template <bool FOUR, bool MAXNORM>
 int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
     switch (rounds) {
-        case 1: k_qsgd_quantize<1, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 2: k_qsgd_quantize<2, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 4: k_qsgd_quantize<4, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 8: k_qsgd_quantize<8, FOUR><<<grid, kThreads, 0, s>>>(a); break;
-        case 16: k_qsgd_quantize<16, FOUR><<<grid, kThreads, 0, s>>>(a); break;
+        case 1: k_qsgd_quantize<1, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 2: k_qsgd_quantize<2, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 4: k_qsgd_quantize<4, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 8: k_qsgd_quantize<8, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 16: k_qsgd_quantize<16, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
         default: return GC_ERR_INVALID;
     }
     return launch_status();
@@ -374,8 +386,8 @@ using namespace gc;
 
 extern "C" {
 
-int qsgd_quantize(const float* grad, int64_t n, int bucket, int s_levels, uint64_t seed, int worker,
-                  float* norms, uint8_t* codes, gc_stream_t stream) {
+static int qsgd_quantize_impl(const float* grad, int64_t n, int bucket, int s_levels, uint64_t seed,
+                              int worker, float* norms, uint8_t* codes, gc_stream_t stream, bool maxnorm) {
     if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127 || worker < 0)
         return GC_ERR_INVALID;
     if (n == 0) return GC_OK;
@@ -391,8 +403,21 @@ int qsgd_quantize(const float* grad, int64_t n, int bucket, int s_levels, uint64
     a.codes = codes;
     const unsigned grid = blocks_for_tiles(a.nbuckets);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return s_levels <= 7 ? launch_quantize<true>(bucket / 128, a, grid, s)
-                         : launch_quantize<false>(bucket / 128, a, grid, s);
+    if (maxnorm)
+        return s_levels <= 7 ? launch_quantize<true, true>(bucket / 128, a, grid, s)
+                             : launch_quantize<false, true>(bucket / 128, a, grid, s);
+    return s_levels <= 7 ? launch_quantize<true, false>(bucket / 128, a, grid, s)
+                         : launch_quantize<false, false>(bucket / 128, a, grid, s);
+}
+
+int qsgd_quantize(const float* grad, int64_t n, int bucket, int s_levels, uint64_t seed, int worker,
+                  float* norms, uint8_t* codes, gc_stream_t stream) {
+    return qsgd_quantize_impl(grad, n, bucket, s_levels, seed, worker, norms, codes, stream, false);
+}
+
+int qsgd_quantize_maxnorm(const float* grad, int64_t n, int bucket, int s_levels, uint64_t seed, int worker,
+                          float* scales, uint8_t* codes, gc_stream_t stream) {
+    return qsgd_quantize_impl(grad, n, bucket, s_levels, seed, worker, scales, codes, stream, true);
 }
 
 int qsgd_dequant_sum(const uint8_t* const* codes, const float* const* norms, int W, int64_t n,

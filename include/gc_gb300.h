@@ -241,6 +241,17 @@ GC_API int qsgd_quantize(const float *grad, int64_t n, int bucket, int s_levels,
                   gc_stream_t stream);
 
 /*
+ * qsgd_quantize_maxnorm -- QSGD Knowl 8, max-norm scaling: as qsgd_quantize
+ * but each bucket is scaled by its largest coordinate magnitude ||v||_inf
+ * (stored exactly in scales[b]) instead of its l2 norm; qsgd_dequant_sum
+ * decodes the result unchanged (scales in place of norms).
+ * Errors: as qsgd_quantize.
+ */
+GC_API int qsgd_quantize_maxnorm(const float *grad, int64_t n, int bucket,
+                                 int s_levels, uint64_t seed, int worker,
+                                 float *scales, uint8_t *codes, gc_stream_t stream);
+
+/*
  * qsgd_dequant_sum -- QSGD Knowl 2 (decode the tuple: value = norm * sign *
  * level / s) and Knowl 3 (sum the K decoded messages; scale = 1/K gives
  * their average).

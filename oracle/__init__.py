@@ -66,6 +66,7 @@ def _load():
             "orc_l2norm_fp32": (f32, [vp, i64]),
             "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_qsgd_scaled_values": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
+            "orc_qsgd_quantize_maxnorm": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_qsgd_dequant_sum": (None, [vp, vp, i32, i64, i64, i32, f64, vp]),
             "orc_saps_mask_compact": (i64, [i64, f64, u64, vp, i32, i64, vp, vp, i64]),
             "orc_saps_matching": (i32, [u64, i32, vp]),
@@ -213,6 +214,17 @@ def qsgd_quantize(v: np.ndarray, bucket: int, s: int, seed: int, worker: int, i0
     codes = np.zeros(qsgd_code_bytes(n, s), dtype=np.uint8)
     _load().orc_qsgd_quantize(_ptr(v), n, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker, i0,
                               _ptr(norms), _ptr(codes))
+    return norms, codes
+
+
+def qsgd_quantize_maxnorm(v: np.ndarray, bucket: int, s: int, seed: int, worker: int, i0: int = 0):
+    """QSGD with each bucket scaled by max |v| (Knowl 8).  Returns (scales, codes)."""
+    _check(v, np.float32, "v")
+    n = v.size
+    norms = np.zeros((n + bucket - 1) // bucket, dtype=np.float32)
+    codes = np.zeros(qsgd_code_bytes(n, s), dtype=np.uint8)
+    _load().orc_qsgd_quantize_maxnorm(_ptr(v), n, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker, i0,
+                                      _ptr(norms), _ptr(codes))
     return norms, codes
 
 

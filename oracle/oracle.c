@@ -308,9 +308,41 @@ float orc_l2norm_fp32(const float *v, int64_t len)
  *   8 <= s <= 127 : 8-bit codes, one per byte, bit 7 = sign
  * Outputs: norms[ceil(n/d)] (fp32) and codes (ceil(n/2) or n bytes).
  */
+static void qsgd_quantize_impl(const float *v, int64_t n, int64_t d, int s,
+                               uint64_t seed, int worker, int64_t i0,
+                               int maxnorm, float *norms, uint8_t *codes);
+
 void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
                        uint64_t seed, int worker, int64_t i0, float *norms,
                        uint8_t *codes)
+{
+    qsgd_quantize_impl(v, n, d, s, seed, worker, i0, 0, norms, codes);
+}
+
+/*
+ * [QS] Knowl 8, max-norm scaling: each bucket is scaled by its largest
+ * coordinate magnitude ||v||_inf instead of its l2 norm; everything else as
+ * orc_qsgd_quantize (the stored scale is the max, exactly).
+ */
+void orc_qsgd_quantize_maxnorm(const float *v, int64_t n, int64_t d, int s,
+                               uint64_t seed, int worker, int64_t i0,
+                               float *norms, uint8_t *codes)
+{
+    qsgd_quantize_impl(v, n, d, s, seed, worker, i0, 1, norms, codes);
+}
+
+static float max_abs(const float *v, int64_t len)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < len; ++i)
+        if (fabsf(v[i]) > m)
+            m = fabsf(v[i]);
+    return m;
+}
+
+static void qsgd_quantize_impl(const float *v, int64_t n, int64_t d, int s,
+                               uint64_t seed, int worker, int64_t i0,
+                               int maxnorm, float *norms, uint8_t *codes)
 {
     int four_bit = (s <= 7);
     int64_t nbuckets = (n + d - 1) / d;
@@ -321,7 +353,7 @@ void orc_qsgd_quantize(const float *v, int64_t n, int64_t d, int s,
     for (int64_t b = 0; b < nbuckets; ++b) {
         int64_t lo = b * d;
         int64_t hi = lo + d < n ? lo + d : n;
-        float norm = orc_l2norm_fp32(v + lo, hi - lo);
+        float norm = maxnorm ? max_abs(v + lo, hi - lo) : orc_l2norm_fp32(v + lo, hi - lo);
         norms[b] = norm;
         float S = norm > 0.0f ? (float)s / norm : 0.0f;
         for (int64_t i = lo; i < hi; ++i) {

@@ -171,3 +171,28 @@ def test_tiny_and_huge_buckets_match_oracle(scale):
         assert_close(host_f32(norms), rn, np.abs(rn), what="norms")
         assert host_f32(norms)[2] == rn[2]          # one nonzero value: |v| exactly
         compare_codes(codes.cpu().numpy(), rc, vh, n, 512, s, 4, 0)
+
+
+@pytest.mark.parametrize("s", [1, 7, 22, 127])
+@pytest.mark.parametrize("n,bucket", [(1, 512), (5 * 512 + 297, 512), (100_001, 128), (70_000, 2048)])
+def test_maxnorm_quantize_parity(n, bucket, s):
+    """Knowl 8 max-norm scaling (and the s = 1 ternary and s ~ sqrt(d) dense
+    level counts): the scale is a max, exact on both sides, so scales and
+    codes are bit-exact; the dequant-sum within tolerance."""
+    cfg = wl.scaled(wl.QSGD_S7, n)
+    v = wl.qsgd_grad(cfg, 2, device=DEV)
+    nb, cb = gc.qsgd_num_buckets(n, bucket), gc.qsgd_code_bytes(n, s)
+    scales = guarded(nb, torch.float32)
+    codes = guarded(cb, torch.uint8)
+    gc.qsgd_quantize_maxnorm(v, bucket, s, 42, 2, scales[:nb], codes[:cb])
+    out = torch.empty(n, device=DEV)
+    gc.qsgd_dequant_sum([codes[:cb]], [scales[:nb]], n, bucket, s, 1.0, out)
+    vh = host_f32(v)
+    rs, rc = oracle.qsgd_quantize_maxnorm(vh, bucket, s, 42, 2)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_f32(scales[:nb]), rs)
+    np.testing.assert_array_equal(codes[:cb].cpu().numpy(), rc)
+    check_guard(scales, nb)
+    check_guard(codes, cb)
+    ref = oracle.qsgd_dequant_sum([rc], [rs], n, bucket, s)
+    assert_close(host_f32(out), ref, np.abs(ref), what="maxnorm dequant")

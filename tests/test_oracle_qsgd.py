@@ -238,3 +238,34 @@ def test_tiny_norm_bucket_zero_coordinate_gets_level_zero():
         assert np.isinf(np.float32(127) / norms[0])
     sign, level = _parse_codes(codes, 512, 127)
     assert np.all(level[8:] == 0) and np.all(level[:8] == 127)
+
+
+@pytest.mark.parametrize("s", [7, 127])
+def test_maxnorm_scale_levels_and_unbiasedness(s):
+    """Knowl 8 max-norm scaling: the stored scale is max |v| of the bucket,
+    the largest coordinate gets level s or s-1, no level exceeds s, and the
+    decoded vector is unbiased over 10^4 seeds (3 sigma, as for the l2 form)."""
+    rng = np.random.default_rng(77 + s)
+    d, nb, T = 512, 2, 10_000
+    v = rng.normal(0, 1e-2, d * nb).astype(np.float32)
+    v[rng.random(v.size) < 0.01] *= 100
+    scales, codes = oracle.qsgd_quantize_maxnorm(v, d, s, seed=1, worker=0)
+    for b in range(nb):
+        np.testing.assert_array_equal(scales[b], np.max(np.abs(v[b * d:(b + 1) * d])))
+    sign, level = _parse_codes(codes, v.size, s)
+    assert level.max() <= s
+    for b in range(nb):
+        j = b * d + int(np.argmax(np.abs(v[b * d:(b + 1) * d])))
+        assert level[j] in (s - 1, s)
+    acc = np.zeros(v.size)
+    for seed in range(T):
+        sc, c = oracle.qsgd_quantize_maxnorm(v, d, s, seed=seed, worker=0)
+        acc += oracle.qsgd_dequant_sum([c], [sc], v.size, d, s)
+    mean = acc / T
+    scl = np.repeat(scales.astype(np.float64), d)
+    a = np.abs(v.astype(np.float64)) / scl * s
+    p = a - np.floor(a)
+    sigma = scl / s * np.sqrt(p * (1 - p) / T)
+    mask = sigma > 0
+    z = (mean[mask] - v.astype(np.float64)[mask]) / sigma[mask]
+    assert np.mean(np.abs(z) <= 3) >= 0.99
