@@ -67,6 +67,9 @@ def _load():
             "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_qsgd_scaled_values": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
             "orc_qsgd_quantize_maxnorm": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
+            "orc_elias_omega_bits": (i32, [ctypes.c_uint32, ctypes.c_char_p]),
+            "orc_qsgd_elias_encode": (i64, [vp, vp, i64, i64, i32, vp, vp]),
+            "orc_qsgd_elias_decode": (None, [vp, vp, i64, i64, i32, vp, vp]),
             "orc_qsgd_dequant_sum": (None, [vp, vp, i32, i64, i64, i32, f64, vp]),
             "orc_saps_mask_compact": (i64, [i64, f64, u64, vp, i32, i64, vp, vp, i64]),
             "orc_saps_matching": (i32, [u64, i32, vp]),
@@ -249,6 +252,42 @@ def qsgd_dequant_sum(codes_list, norms_list, n: int, bucket: int, s: int,
     _load().orc_qsgd_dequant_sum(_ptr_array(codes_list), _ptr_array(norms_list), W, n, bucket,
                                  s, float(np.float32(scale)), _ptr(out))
     return out
+
+
+def elias_omega(N: int) -> str:
+    """The Elias omega codeword of N >= 1 as a string of '0'/'1'."""
+    buf = ctypes.create_string_buffer(64)
+    length = _load().orc_elias_omega_bits(int(N), buf)
+    return buf.value.decode()[:length]
+
+
+def qsgd_elias_max_words(n: int, bucket: int) -> int:
+    """Upper bound on the encoded words: 32 norm bits + at most 15 bits per
+    coordinate (Elias-omega of 128 is 14 bits, plus the sign), per bucket."""
+    nb = (n + bucket - 1) // bucket
+    return nb * (1 + (15 * bucket + 31) // 32) + 1
+
+
+def qsgd_elias_encode(codes: np.ndarray, norms: np.ndarray, n: int, bucket: int, s: int):
+    """Returns (words uint32 [total], offsets uint32 [nbuckets + 1])."""
+    _check(codes, np.uint8, "codes", qsgd_code_bytes(n, s))
+    nb = (n + bucket - 1) // bucket
+    _check(norms, np.float32, "norms", nb)
+    words = np.zeros(qsgd_elias_max_words(n, bucket), dtype=np.uint32)
+    offsets = np.zeros(nb + 1, dtype=np.uint32)
+    total = int(_load().orc_qsgd_elias_encode(_ptr(codes), _ptr(norms), n, bucket, s, _ptr(words),
+                                              _ptr(offsets)))
+    return words[:total].copy(), offsets
+
+
+def qsgd_elias_decode(words: np.ndarray, offsets: np.ndarray, n: int, bucket: int, s: int):
+    """Returns (codes uint8, norms fp32)."""
+    _check(words, np.uint32, "words")
+    _check(offsets, np.uint32, "offsets", (n + bucket - 1) // bucket + 1)
+    codes = np.zeros(qsgd_code_bytes(n, s), dtype=np.uint8)
+    norms = np.zeros((n + bucket - 1) // bucket, dtype=np.float32)
+    _load().orc_qsgd_elias_decode(_ptr(words), _ptr(offsets), n, bucket, s, _ptr(codes), _ptr(norms))
+    return codes, norms
 
 
 # --------------------------------------------------------------------------

@@ -547,3 +547,147 @@ void orc_easgd_step(double *const *models, int W, int64_t n, double alpha,
         center[i] = (1.0 - beta) * c + beta * mean;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* [QS] Knowl 2: lossless Elias-omega coding of the (norm, sign, level)     */
+/* tuple, dense regime ("offset Elias coding": Elias'(k) = Elias(k + 1)).    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bit stream: bit k of the stream is bit (31 - k % 32) of word k / 32 (most
+ * significant bit first).  Reading used for the format (the page gives the
+ * tuple and the per-coordinate code, not the layout): every bucket starts on
+ * a word boundary; it holds the 32 bits of its fp32 norm, then for each
+ * coordinate in order Elias-omega(level + 1) followed by one sign bit
+ * (1 = negative) when level > 0; unused bits of its last word are 0.
+ * offsets[b] is the first word of bucket b, offsets[nbuckets] the total.
+ */
+typedef struct {
+    uint32_t *words;
+    int64_t pos; /* bit position */
+} orc_bitwriter;
+
+static void put_bit(orc_bitwriter *w, int bit)
+{
+    if (bit)
+        w->words[w->pos / 32] |= 1u << (31 - (int)(w->pos % 32));
+    w->pos++;
+}
+
+/*
+ * Elias omega code of N >= 1 (Elias, "Universal codeword sets and
+ * representations of the integers", IEEE Trans. Inf. Theory 21(2), 1975):
+ * write the final 0; while N > 1, prepend the binary form of N and set N to
+ * (its number of digits) - 1.
+ */
+int orc_elias_omega_bits(uint32_t N, char *out)
+{
+    char buf[64];
+    int len = 0;
+    buf[len++] = '0';
+    while (N > 1) {
+        char grp[33];
+        int L = 0;
+        for (uint32_t m = N; m; m >>= 1)
+            grp[L++] = (char)('0' + (m & 1u));
+        /* grp holds the digits least significant first; prepend reversed */
+        memmove(buf + L, buf, (size_t)len);
+        for (int i = 0; i < L; ++i)
+            buf[i] = grp[L - 1 - i];
+        len += L;
+        N = (uint32_t)(L - 1);
+    }
+    memcpy(out, buf, (size_t)len);
+    out[len] = '\0';
+    return len;
+}
+
+static void put_omega(orc_bitwriter *w, uint32_t N)
+{
+    char bits[64];
+    int len = orc_elias_omega_bits(N, bits);
+    for (int i = 0; i < len; ++i)
+        put_bit(w, bits[i] == '1');
+}
+
+/* Returns the total number of words. */
+int64_t orc_qsgd_elias_encode(const uint8_t *codes, const float *norms, int64_t n,
+                              int64_t d, int s, uint32_t *words, uint32_t *offsets)
+{
+    int64_t nbuckets = (n + d - 1) / d;
+    orc_bitwriter w = {words, 0};
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        offsets[b] = (uint32_t)(w.pos / 32);
+        uint32_t nb;
+        memcpy(&nb, &norms[b], sizeof nb);
+        for (int i = 31; i >= 0; --i)
+            put_bit(&w, (int)((nb >> i) & 1u));
+        int64_t hi = (b + 1) * d < n ? (b + 1) * d : n;
+        for (int64_t i = b * d; i < hi; ++i) {
+            int sign, level;
+            qsgd_code_at(codes, i, s, &sign, &level);
+            put_omega(&w, (uint32_t)level + 1u);
+            if (level > 0)
+                put_bit(&w, sign);
+        }
+        w.pos = (w.pos + 31) / 32 * 32; /* next bucket on a word boundary */
+    }
+    offsets[nbuckets] = (uint32_t)(w.pos / 32);
+    return w.pos / 32;
+}
+
+typedef struct {
+    const uint32_t *words;
+    int64_t pos;
+} orc_bitreader;
+
+static int get_bit(orc_bitreader *r)
+{
+    int bit = (int)((r->words[r->pos / 32] >> (31 - (int)(r->pos % 32))) & 1u);
+    r->pos++;
+    return bit;
+}
+
+static uint32_t get_omega(orc_bitreader *r)
+{
+    uint32_t N = 1;
+    while (get_bit(r)) {
+        uint32_t v = 1;
+        for (uint32_t i = 0; i < N; ++i)
+            v = 2 * v + (uint32_t)get_bit(r);
+        N = v;
+    }
+    return N;
+}
+
+/*
+ * Inverse of orc_qsgd_elias_encode.  Codes come back in the same
+ * sign-magnitude layout; a level-0 coordinate carries no sign in the stream
+ * and comes back with sign 0.
+ */
+void orc_qsgd_elias_decode(const uint32_t *words, const uint32_t *offsets, int64_t n,
+                           int64_t d, int s, uint8_t *codes, float *norms)
+{
+    int64_t nbuckets = (n + d - 1) / d;
+    if (s <= 7)
+        for (int64_t k = 0; k < (n + 1) / 2; ++k)
+            codes[k] = 0;
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        orc_bitreader r = {words, (int64_t)offsets[b] * 32};
+        uint32_t nb = 0;
+        for (int i = 0; i < 32; ++i)
+            nb = (nb << 1) | (uint32_t)get_bit(&r);
+        memcpy(&norms[b], &nb, sizeof nb);
+        int64_t hi = (b + 1) * d < n ? (b + 1) * d : n;
+        for (int64_t i = b * d; i < hi; ++i) {
+            uint32_t level = get_omega(&r) - 1u;
+            uint32_t sign = level > 0 ? (uint32_t)get_bit(&r) : 0u;
+            if (s <= 7) {
+                uint32_t code = (sign << 3) | level;
+                codes[i / 2] |= (uint8_t)(i % 2 == 0 ? code << 4 : code);
+            } else {
+                codes[i] = (uint8_t)((sign << 7) | level);
+            }
+        }
+    }
+}
