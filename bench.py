@@ -471,7 +471,34 @@ def rows(args, dev, peak):
         torch.cuda.synchronize(dev)
         out[f"{qcfg.name}.quantize_maxnorm"] = _row(qcfg.name, "qsgd_quantize_maxnorm", n * 4 + cb + 4 * nb,
                                                     tm.ms("m"), peak, n)
-        del vs, norms, codes, outq
+        # Elias-omega stream of each worker's (l2-norm) codes, and its decode
+        for w in range(W):
+            pq[w]()
+        cap = gc.qsgd_elias_max_words(n, qcfg.bucket, s)
+        words = [torch.empty(cap, dtype=torch.int32, device=dev) for _ in range(W)]
+        offs = [torch.empty(nb + 1, dtype=torch.int32, device=dev) for _ in range(W)]
+        ews = torch.empty(gc.qsgd_elias_workspace_bytes(n, qcfg.bucket), dtype=torch.uint8, device=dev)
+        dcodes = torch.empty(cb, dtype=torch.uint8, device=dev)
+        dnorms = torch.empty(nb, device=dev)
+        pe = [gc.qsgd_elias_encode(codes[w], norms[w], n, qcfg.bucket, s, words[w], offs[w], ews, stream=stream,
+                                   prepare=True) for w in range(W)]
+        px = [gc.qsgd_elias_decode(words[w], offs[w], n, qcfg.bucket, s, dcodes, dnorms, stream=stream,
+                                   prepare=True) for w in range(W)]
+        for i in range(6):
+            for w in range(W):
+                tm.around("e" if i >= 2 else "w", pe[w])
+            for w in range(W):
+                tm.around("x" if i >= 2 else "w", px[w])
+        torch.cuda.synchronize(dev)
+        total = sum(int(o[nb].item()) for o in offs) / W
+        bits = {"bits_per_coord": round(32 * total / n, 4),
+                "bits_per_coord_with_offsets": round(32 * (total + nb + 1) / n, 4)}
+        out[f"{qcfg.name}.elias_encode"] = _row(qcfg.name, "qsgd_elias_encode (count + encode)",
+                                                cb + 4 * nb + 4 * total + 4 * (nb + 1), tm.ms("e"), peak, n,
+                                                bits)
+        out[f"{qcfg.name}.elias_decode"] = _row(qcfg.name, "qsgd_elias_decode",
+                                                4 * total + 4 * (nb + 1) + cb + 4 * nb, tm.ms("x"), peak, n)
+        del vs, norms, codes, outq, words, offs, ews, dcodes, dnorms
 
     # config 5: SAPS + EASGD, 16 workers x 25,557,032, p = 0.01 and 0.001
     for scfg in (wl.SAPS_P01, wl.SAPS_P001):
@@ -661,7 +688,8 @@ def reference_arm(args, rank, world, pg):
 # ----------------------------------------------------------------------------- profiling cases
 
 CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
-         "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated")
+         "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated",
+         "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127")
 
 
 def run_case(name: str, n: int):
@@ -716,6 +744,23 @@ def run_case(name: str, n: int):
         nms = [torch.rand(nb, device=dev) for _ in range(W)]
         out = torch.empty(n, device=dev)
         fn = lambda: gc.qsgd_dequant_sum(cs, nms, n, 512, s, 0.25, out)
+    elif name.startswith("elias_"):
+        s = 7 if name.endswith("s7") else 127
+        v = wl.qsgd_grad(wl.scaled(wl.QSGD_S7, n), 0, device=dev)
+        nb = gc.qsgd_num_buckets(n, 512)
+        nm = torch.empty(nb, device=dev)
+        c = torch.empty(gc.qsgd_code_bytes(n, s), dtype=torch.uint8, device=dev)
+        gc.qsgd_quantize(v, 512, s, 42, 0, nm, c)
+        words = torch.empty(gc.qsgd_elias_max_words(n, 512, s), dtype=torch.int32, device=dev)
+        offs = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+        ews = torch.empty(gc.qsgd_elias_workspace_bytes(n, 512), dtype=torch.uint8, device=dev)
+        gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews)
+        if name.startswith("elias_encode"):
+            fn = lambda: gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews)
+        else:
+            dc = torch.empty_like(c)
+            dn = torch.empty_like(nm)
+            fn = lambda: gc.qsgd_elias_decode(words, offs, n, 512, s, dc, dn)
     elif name in ("saps_mask", "saps_avg", "easgd", "saps_fused"):
         cfg = wl.scaled(wl.SAPS_P01, n if name not in ("easgd", "saps_fused") else n // 4)
         models = wl.saps_models(cfg, device=dev)

@@ -37,9 +37,12 @@ __all__ = [
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
     "gc_2bit_step", "gc_2bit_quantize_local", "qsgd_quantize_maxnorm",
+    "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
+    "qsgd_elias_workspace_bytes",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+GC_ERR_CORRUPT = -6
 GC_F32, GC_BF16 = 0, 1
 GC_UPD_NONE, GC_UPD_SGD, GC_UPD_EASGD = 0, 1, 2
 GC_MAX_WORKERS = 64
@@ -83,6 +86,10 @@ def load():
             "qsgd_quantize": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
             "qsgd_dequant_sum": (i32, [vp, vp, i32, i64, i32, i32, f32, vp, vp]),
             "qsgd_quantize_maxnorm": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
+            "qsgd_elias_encode": (i32, [vp, vp, i64, i32, i32, vp, u64, vp, vp, sz, vp]),
+            "qsgd_elias_max_words": (u64, [i64, i32, i32]),
+            "qsgd_elias_workspace_bytes": (sz, [i64, i32]),
+            "qsgd_elias_decode": (i32, [vp, vp, i64, i32, i32, vp, vp, vp, vp]),
             "saps_round_seed": (u64, [u64, u64]),
             "saps_matching": (i32, [u64, i32, vp]),
             "saps_workspace_bytes": (sz, [i64]),
@@ -321,6 +328,47 @@ def qsgd_dequant_sum(codes, norms, n: int, bucket: int, s_levels: int, scale: fl
             W, n, int(bucket), int(s_levels), float(scale),
             _dev(out, "out", torch.float32, n), _stream(stream, out))
     return _invoke(lib.qsgd_dequant_sum, args, "qsgd_dequant_sum", prepare, (list(codes), list(norms), out))
+
+
+def qsgd_elias_max_words(n: int, bucket: int, s_levels: int) -> int:
+    """Words the Elias stream of n coordinates can take at most."""
+    return int(load().qsgd_elias_max_words(int(n), int(bucket), int(s_levels)))
+
+
+def qsgd_elias_workspace_bytes(n: int, bucket: int) -> int:
+    return int(load().qsgd_elias_workspace_bytes(int(n), int(bucket)))
+
+
+def qsgd_elias_encode(codes: torch.Tensor, norms: torch.Tensor, n: int, bucket: int, s_levels: int,
+                      words: torch.Tensor, offsets: torch.Tensor, workspace: torch.Tensor,
+                      stream=None, prepare: bool = False):
+    """Elias-omega stream of QSGD codes (Knowl 2).  words/offsets are int32
+    tensors holding uint32 bit patterns; offsets[nbuckets] is the length."""
+    lib = load()
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _dev(norms, "norms", torch.float32, nb), int(n), int(bucket), int(s_levels),
+            _dev(words, "words", torch.int32), words.numel(),
+            _dev(offsets, "offsets", torch.int32, nb + 1),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream, codes))
+    return _invoke(lib.qsgd_elias_encode, args, "qsgd_elias_encode", prepare,
+                   (codes, norms, words, offsets, workspace))
+
+
+def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket: int, s_levels: int,
+                      codes: torch.Tensor, norms: torch.Tensor, status: torch.Tensor | None = None,
+                      stream=None, prepare: bool = False):
+    """Inverse of qsgd_elias_encode; ``status`` (device int32 [1]) receives
+    GC_ERR_CORRUPT for a stream that does not decode."""
+    lib = load()
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_dev(words, "words", torch.int32), _dev(offsets, "offsets", torch.int32, nb + 1),
+            int(n), int(bucket), int(s_levels),
+            _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _dev(norms, "norms", torch.float32, nb),
+            None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words))
+    keep = (words, offsets, codes, norms) + (() if status is None else (status,))
+    return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
 
 
 def saps_round_seed(base_seed: int, t: int) -> int:

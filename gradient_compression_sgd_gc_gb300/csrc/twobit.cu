@@ -766,6 +766,7 @@ const char* gc_status_string(int status) {
         case GC_ERR_CUDA: return "GC_ERR_CUDA: CUDA launch or runtime error";
         case GC_ERR_CAPACITY: return "GC_ERR_CAPACITY: more masked entries than capacity";
         case GC_ERR_TIMEOUT: return "GC_ERR_TIMEOUT: bounded device wait ran out";
+        case GC_ERR_CORRUPT: return "GC_ERR_CORRUPT: coded stream does not decode";
         default: return "unknown status";
     }
 }

@@ -63,7 +63,8 @@ enum {
     GC_ERR_ALIGN = -2,    /* a data pointer is not 16-byte aligned           */
     GC_ERR_CUDA = -3,     /* a CUDA launch or runtime call failed            */
     GC_ERR_CAPACITY = -4, /* device: more masked entries than the capacity   */
-    GC_ERR_TIMEOUT = -5   /* device: a bounded wait in the compaction ran out */
+    GC_ERR_TIMEOUT = -5,  /* device: a bounded wait in the compaction ran out */
+    GC_ERR_CORRUPT = -6   /* device: a coded stream does not decode           */
 };
 
 /* Gradient element type. */
@@ -266,6 +267,66 @@ GC_API int qsgd_quantize_maxnorm(const float *grad, int64_t n, int bucket,
 GC_API int qsgd_dequant_sum(const uint8_t *const *codes, const float *const *norms,
                      int W, int64_t n, int bucket, int s_levels, float scale,
                      float *out, gc_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* QSGD Elias-omega coding                                                */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * qsgd_elias_encode -- "QSGD: Communication-Efficient SGD via Gradient
+ * Quantization and Encoding", Knowl 2, dense regime: the lossless code of the
+ * quantised tuple (norm, signs, levels) that qsgd_quantize writes.  Per bucket
+ * b, in a stream of 32-bit words read most significant bit first:
+ *   the 32 bits of norms[b], then for each coordinate in order
+ *   Elias-omega(level + 1) (Elias, IEEE Trans. Inf. Theory 21(2), 1975),
+ *   followed by its sign bit (1 = negative) when level > 0;
+ *   the bucket's last word is padded with zero bits.
+ * Every bucket starts on a word boundary; offsets[b] is its first word and
+ * offsets[nbuckets] the number of words written, so that the receiver
+ * decodes the buckets in parallel (side information not on the pages: 32
+ * bits per bucket).  The sign of a level-0 coordinate is not sent.
+ *
+ *   codes, norms   device, as qsgd_quantize writes them (read only)
+ *   words          device uint32 [capacity_words]; capacity_words must be at
+ *                  least qsgd_elias_max_words(n, bucket, s_levels)
+ *   offsets        device uint32 [ceil(n/bucket) + 1], written
+ *   workspace      device, qsgd_elias_workspace_bytes(n, bucket) bytes
+ *                  (contents need not be preserved between calls)
+ * Two kernel launches and one memset on `stream`; the total length is
+ * offsets[nbuckets] on the device.
+ * Errors: GC_ERR_INVALID (bad bucket or s_levels, n < 0, NULL, workspace too
+ * small, a bound above 2^32 - 1 words), GC_ERR_CAPACITY (capacity_words below
+ * the bound), GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_elias_encode(const uint8_t *codes, const float *norms, int64_t n,
+                             int bucket, int s_levels, uint32_t *words,
+                             uint64_t capacity_words, uint32_t *offsets,
+                             void *workspace, size_t ws_bytes, gc_stream_t stream);
+
+/*
+ * Upper bound on the words qsgd_elias_encode writes, whatever the codes:
+ * per bucket of L coordinates 1 + ceil(L * c / 32) with c = 8 bits for 4-bit
+ * codes (level 7) and c = 15 for 8-bit codes (level 127).  0 for invalid
+ * arguments.
+ */
+GC_API uint64_t qsgd_elias_max_words(int64_t n, int bucket, int s_levels);
+
+/* Bytes of device workspace qsgd_elias_encode needs (0 for invalid arguments). */
+GC_API size_t qsgd_elias_workspace_bytes(int64_t n, int bucket);
+
+/*
+ * qsgd_elias_decode -- the inverse of qsgd_elias_encode (Knowl 2: decode the
+ * tuple): norms and codes in qsgd_quantize's layout; a level-0 coordinate
+ * comes back with sign 0.  Bucket b reads only words[offsets[b] ..
+ * offsets[b+1]); missing bits read as zeros.
+ *   d_status   device int or NULL; set to GC_ERR_CORRUPT when a bucket's
+ *              codewords run past its words, a level exceeds s_levels (it is
+ *              written as s_levels) or a bucket has no norm word
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_elias_decode(const uint32_t *words, const uint32_t *offsets, int64_t n,
+                             int bucket, int s_levels, uint8_t *codes, float *norms,
+                             int *d_status, gc_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* SAPS sparsified gossip + EASGD                                         */

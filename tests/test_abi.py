@@ -46,7 +46,7 @@ def test_library_is_the_in_tree_build():
 
 
 def test_status_strings():
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         s = gc.gc_status_string(code)
         assert s and (code != 0 or s == "GC_OK")
     assert gc.gc_status_string(12345) == "unknown status"
@@ -104,6 +104,32 @@ def test_qsgd_validation():
     assert _call(g, _ptrs(FAKE), _ptrs(FAKE), 1, 100, 512, 7, float("nan"), FAKE,
                  None) == gc.GC_ERR_INVALID
     assert _call(g, _ptrs(FAKE), _ptrs(FAKE), 0, 100, 512, 7, 1.0, FAKE, None) == gc.GC_ERR_INVALID
+
+
+def test_elias_sizes_and_validation():
+    assert gc.qsgd_elias_max_words(1024, 512, 7) == 2 * (1 + 512 * 8 // 32)
+    assert gc.qsgd_elias_max_words(1024 + 3, 512, 127) == 2 * (1 + 512 * 15 // 32) + 1 + 2
+    assert gc.qsgd_elias_max_words(100, 500, 7) == 0
+    assert gc.qsgd_elias_workspace_bytes(100, 500) == 0
+    ws = gc.qsgd_elias_workspace_bytes(10_000, 512)
+    assert ws >= 4 * 20 and ws % 16 == 0
+    f = "qsgd_elias_encode"
+    cap = gc.qsgd_elias_max_words(10_000, 512, 7)
+    assert _call(f, FAKE, FAKE, 10_000, 500, 7, FAKE, cap, FAKE, FAKE, ws, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, FAKE, 10_000, 512, 0, FAKE, cap, FAKE, FAKE, ws, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, FAKE, 10_000, 512, 7, FAKE, cap - 1, FAKE, FAKE, ws, None) == gc.GC_ERR_CAPACITY
+    assert _call(f, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, FAKE, ws - 1, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, None, FAKE, ws, None) == gc.GC_ERR_INVALID
+    assert _call(f, FAKE, FAKE, 10_000, 512, 7, MISALIGNED, cap, FAKE, FAKE, ws, None) == gc.GC_ERR_ALIGN
+    # offsets must stay 32-bit: a stream bound above 2^32 - 1 words is refused
+    big = 1 << 34
+    assert _call(f, FAKE, FAKE, big, 512, 127, FAKE, 1 << 40, FAKE, FAKE, 1 << 40, None) == gc.GC_ERR_INVALID
+    g = "qsgd_elias_decode"
+    assert _call(g, FAKE, FAKE, 10_000, 512, 128, FAKE, FAKE, None, None) == gc.GC_ERR_INVALID
+    assert _call(g, None, FAKE, 10_000, 512, 7, FAKE, FAKE, None, None) == gc.GC_ERR_INVALID
+    assert _call(g, FAKE, FAKE, 10_000, 512, 7, FAKE, MISALIGNED, None, None) == gc.GC_ERR_ALIGN
+    assert _call(g, FAKE, FAKE, 10_000, 512, 7, FAKE, FAKE, MISALIGNED + 1, None) == gc.GC_ERR_ALIGN
+    assert _call(g, None, None, 0, 512, 7, None, None, None, None) == gc.GC_OK
 
 
 def test_saps_validation():

@@ -1,0 +1,214 @@
+"""GPU parity of the QSGD Elias-omega codec (Knowl 2) against the oracle.
+
+The encoder's input codes and norms come from the oracle's quantiser on the
+seeded workload recipe, so the GPU stream must equal the oracle's stream word
+for word (integer work: bit-exact), offsets included; the decoder must give
+back the oracle decoder's codes and norms exactly.  Sizes span several CTAs of
+64 buckets and a ragged last bucket; the full-size cases use the QSGD
+workload (61,100,840 coordinates, buckets of 512).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_compression_sgd_gc_gb300 as gc
+from gradient_compression_sgd_gc_gb300 import workloads as wl
+import oracle
+from gpu_helpers import check_guard, guarded, host_f32, host_u32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _oracle_codes(cfg, n, bucket, s, worker=0):
+    v = wl.qsgd_grad(wl.scaled(cfg, n), worker, device="cpu").numpy()
+    norms, codes = oracle.qsgd_quantize(v, bucket, s, cfg.seed, worker)
+    return v, norms, codes
+
+
+def _encode_gpu(codes_h, norms_h, n, bucket, s):
+    nb = gc.qsgd_num_buckets(n, bucket)
+    cap = gc.qsgd_elias_max_words(n, bucket, s)
+    codes = torch.from_numpy(codes_h).to(DEV)
+    norms = torch.from_numpy(norms_h).to(DEV)
+    words = guarded(cap, torch.int32)
+    offsets = guarded(nb + 1, torch.int32)
+    ws = torch.empty(max(16, gc.qsgd_elias_workspace_bytes(n, bucket)), dtype=torch.uint8, device=DEV)
+    ws.fill_(0xA5)                 # the workspace needs no initialisation
+    gc.qsgd_elias_encode(codes, norms, n, bucket, s, words[:cap], offsets[:nb + 1], ws)
+    torch.cuda.synchronize()
+    check_guard(offsets, nb + 1)
+    check_guard(words, cap)
+    return words, offsets
+
+
+def _decode_gpu(words, offsets, n, bucket, s):
+    nb = gc.qsgd_num_buckets(n, bucket)
+    cb = gc.qsgd_code_bytes(n, s)
+    codes = guarded(cb, torch.uint8)
+    codes[:cb].fill_(0xEE)       # every byte must be written
+    norms = guarded(nb, torch.float32)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gc.qsgd_elias_decode(words, offsets, n, bucket, s, codes[:cb], norms[:nb], st)
+    torch.cuda.synchronize()
+    check_guard(codes, cb)
+    check_guard(norms, nb)
+    return codes[:cb].cpu().numpy(), host_f32(norms[:nb]), int(st.item())
+
+
+CASES = [
+    (wl.QSGD_S7, 512 * 150 + 297, 512, 7),       # 151 buckets: 3 CTAs, ragged odd tail
+    (wl.QSGD_S7, 128 * 400 + 77, 128, 7),
+    (wl.QSGD_S7, 256 * 70, 256, 1),              # s = 1 (ternary)
+    (wl.QSGD_S127, 512 * 130 + 1, 512, 127),
+    (wl.QSGD_S127, 2048 * 70 + 1001, 2048, 127),
+    (wl.QSGD_S127, 512 * 129 + 400, 512, 22),    # s = floor(sqrt(512)): the dense regime
+    (wl.QSGD_S7, 1024 * 65, 1024, 5),
+    (wl.QSGD_S7, 300, 512, 7),                   # one short bucket
+    (wl.QSGD_S127, 1, 128, 127),
+]
+
+
+@pytest.mark.parametrize("cfg,n,bucket,s", CASES, ids=lambda x: getattr(x, "name", str(x)))
+def test_encode_decode_parity(cfg, n, bucket, s):
+    _, norms, codes = _oracle_codes(cfg, n, bucket, s)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    words, offsets = _encode_gpu(codes, norms, n, bucket, s)
+    nb = gc.qsgd_num_buckets(n, bucket)
+    np.testing.assert_array_equal(host_u32(offsets[:nb + 1]), ref_off)
+    total = int(ref_off[-1])
+    np.testing.assert_array_equal(host_u32(words[:total]), ref_w)
+    dc, dn, st = _decode_gpu(words, offsets, n, bucket, s)
+    rc, rn = oracle.qsgd_elias_decode(ref_w, ref_off, n, bucket, s)
+    assert st == 0
+    np.testing.assert_array_equal(dc, rc)
+    np.testing.assert_array_equal(dn.view(np.uint32), rn.view(np.uint32))
+
+
+def test_empty():
+    offsets = torch.full((4,), 7, dtype=torch.int32, device=DEV)
+    words = torch.zeros(4, dtype=torch.int32, device=DEV)
+    codes = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    norms = torch.zeros(4, device=DEV)
+    ws = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    gc.qsgd_elias_encode(codes, norms, 0, 512, 7, words, offsets, ws)
+    gc.qsgd_elias_decode(words, offsets, 0, 512, 7, codes, norms)
+    torch.cuda.synchronize()
+    assert host_u32(offsets).tolist() == [0, 7, 7, 7]
+
+
+@pytest.mark.parametrize("s", [7, 127])
+def test_worst_case_fills_the_bound(s):
+    """Every coordinate at the top level with sign -: each codeword takes the
+    longest form, and the stream is exactly qsgd_elias_max_words long."""
+    n, bucket = 512 * 70 + 33, 512
+    nb = gc.qsgd_num_buckets(n, bucket)
+    cb = gc.qsgd_code_bytes(n, s)
+    top = 0x8 | s if s <= 7 else 0x80 | s
+    codes = np.full(cb, (top << 4) | top if s <= 7 else top, np.uint8)
+    if s <= 7 and n % 2:
+        codes[-1] &= 0xF0
+    norms = np.linspace(0.5, 2.0, nb).astype(np.float32)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    assert ref_w.size == gc.qsgd_elias_max_words(n, bucket, s)
+    words, offsets = _encode_gpu(codes, norms, n, bucket, s)
+    np.testing.assert_array_equal(host_u32(offsets[:nb + 1]), ref_off)
+    np.testing.assert_array_equal(host_u32(words[:ref_w.size]), ref_w)
+    dc, dn, st = _decode_gpu(words, offsets, n, bucket, s)
+    assert st == 0
+    np.testing.assert_array_equal(dc, codes)
+
+
+def test_all_zero_buckets():
+    """Norm 0: level 0 everywhere, one bit per coordinate; negative zeros and
+    negative values in a zero-norm bucket send no sign."""
+    n, bucket, s = 512 * 66, 512, 7
+    v = np.zeros(n, np.float32)
+    v[::3] = -0.0
+    v[512 * 10:512 * 11] = np.linspace(-1, 1, 512, dtype=np.float32)
+    norms, codes = oracle.qsgd_quantize(v, bucket, s, seed=1, worker=0)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    words, offsets = _encode_gpu(codes, norms, n, bucket, s)
+    np.testing.assert_array_equal(host_u32(offsets[:67]), ref_off)
+    np.testing.assert_array_equal(host_u32(words[:ref_w.size]), ref_w)
+    assert int(ref_off[1]) == 1 + 512 // 32
+
+
+def test_roundtrip_through_dequant_sum():
+    """quantise -> encode -> decode -> dequant-sum on the GPU equals quantise ->
+    dequant-sum: the codec is lossless for everything the decoder reads."""
+    cfg, n, bucket = wl.QSGD_S7, 512 * 300 + 5, 512
+    for s in (7, 127):
+        W = 3
+        nb, cb = gc.qsgd_num_buckets(n, bucket), gc.qsgd_code_bytes(n, s)
+        cap = gc.qsgd_elias_max_words(n, bucket, s)
+        ws = torch.empty(gc.qsgd_elias_workspace_bytes(n, bucket), dtype=torch.uint8, device=DEV)
+        codes, norms, dcodes, dnorms = [], [], [], []
+        for w in range(W):
+            v = wl.qsgd_grad(wl.scaled(cfg, n), w, device=DEV)
+            c = torch.empty(cb, dtype=torch.uint8, device=DEV)
+            nr = torch.empty(nb, device=DEV)
+            gc.qsgd_quantize(v, bucket, s, cfg.seed, w, nr, c)
+            words = torch.empty(cap, dtype=torch.int32, device=DEV)
+            offs = torch.empty(nb + 1, dtype=torch.int32, device=DEV)
+            gc.qsgd_elias_encode(c, nr, n, bucket, s, words, offs, ws)
+            dc = torch.empty(cb, dtype=torch.uint8, device=DEV)
+            dn = torch.empty(nb, device=DEV)
+            gc.qsgd_elias_decode(words, offs, n, bucket, s, dc, dn)
+            codes.append(c), norms.append(nr), dcodes.append(dc), dnorms.append(dn)
+        a = torch.empty(n, device=DEV)
+        b = torch.empty(n, device=DEV)
+        gc.qsgd_dequant_sum(codes, norms, n, bucket, s, 1.0 / W, a)
+        gc.qsgd_dequant_sum(dcodes, dnorms, n, bucket, s, 1.0 / W, b)
+        torch.cuda.synchronize()
+        assert bool((a == b).all())
+        for w in range(W):
+            assert torch.equal(norms[w], dnorms[w])
+
+
+def test_corrupt_streams_are_reported():
+    """Streams that cannot be the encoder's output: the decoder stays inside
+    each bucket's words and reports GC_ERR_CORRUPT."""
+    cfg, n, bucket, s = wl.QSGD_S127, 512 * 8, 512, 127
+    _, norms, codes = _oracle_codes(cfg, n, bucket, s)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    words = torch.from_numpy(ref_w.view(np.int32)).to(DEV)
+    # (a) bucket 3 cut to its norm word alone
+    # (bucket 4 then starts inside bucket 3's codewords; every read stays
+    # below offsets[nbuckets])
+    trunc_off = ref_off.copy()
+    trunc_off[4] = ref_off[3] + 1
+    _, _, st = _decode_gpu(words, torch.from_numpy(trunc_off.view(np.int32)).to(DEV),
+                           n, bucket, s)
+    assert st == gc.GC_ERR_CORRUPT
+    # (b) levels above s: an s = 127 stream decoded as s = 22
+    offsets = torch.from_numpy(ref_off.view(np.int32)).to(DEV)
+    assert int((codes & 127).max()) > 22
+    _, _, st = _decode_gpu(words, offsets, n, bucket, 22)
+    assert st == gc.GC_ERR_CORRUPT
+    # the untouched stream decodes cleanly
+    _, _, st = _decode_gpu(words, offsets, n, bucket, s)
+    assert st == 0
+
+
+@pytest.mark.parametrize("cfg", [wl.QSGD_S7, wl.QSGD_S127], ids=lambda c: c.name)
+def test_full_size_stream_bit_exact(cfg):
+    """The QSGD workload at full size (61,100,840 coordinates, 119,338
+    buckets, last 296): the whole GPU stream equals the oracle's, and the
+    GPU decoder returns the oracle decoder's codes."""
+    n, d, s = cfg.n, cfg.bucket, cfg.s
+    v = wl.qsgd_grad(cfg, 1, device="cpu").numpy()
+    norms, codes = oracle.qsgd_quantize(v, d, s, cfg.seed, 1)
+    del v
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, d, s)
+    words, offsets = _encode_gpu(codes, norms, n, d, s)
+    nb = gc.qsgd_num_buckets(n, d)
+    np.testing.assert_array_equal(host_u32(offsets[:nb + 1]), ref_off)
+    np.testing.assert_array_equal(host_u32(words[:ref_w.size]), ref_w)
+    dc, dn, st = _decode_gpu(words, offsets, n, d, s)
+    rc, rn = oracle.qsgd_elias_decode(ref_w, ref_off, n, d, s)
+    assert st == 0
+    np.testing.assert_array_equal(dc, rc)
+    np.testing.assert_array_equal(dn.view(np.uint32), rn.view(np.uint32))
+    print(f"{cfg.name}: {32 * ref_w.size / n:.3f} bits/coordinate, "
+          f"{32 * (ref_w.size + nb + 1) / n:.3f} with offsets")
