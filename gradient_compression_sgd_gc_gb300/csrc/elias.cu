@@ -25,7 +25,6 @@ namespace gc {
 namespace {
 
 constexpr int kChunk = 64;                          // buckets per CTA
-constexpr int kBucketsPerWarp = kChunk / kWarpsPerBlock;
 constexpr size_t kTicketBytes = 16;
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -189,6 +188,53 @@ __device__ __forceinline__ void emit(uint32_t* stage, uint32_t pos, uint64_t acc
     if (x2) atomicOr(stage + w0 + 2, x2);
 }
 
+// ---------------------------------------------------------------- full buckets
+
+// A full bucket is Bb = d/2 (4-bit) or d (8-bit) code bytes, a multiple of
+// 64, read as P = Bb/16 pieces of 16 bytes.  G = min(P, 32) consecutive
+// lanes share a bucket; a warp covers 32/G buckets per pass and a bucket
+// takes P/G rounds.
+struct Geometry {
+    int Bb, P, G;
+};
+
+template <bool FOUR>
+__device__ __forceinline__ Geometry geometry(int d) {
+    Geometry g;
+    g.Bb = FOUR ? d / 2 : d;
+    g.P = g.Bb / 16;
+    g.G = g.P < 32 ? g.P : 32;
+    return g;
+}
+
+// Coded bits of 16 code bytes.
+__device__ __forceinline__ uint32_t piece_bits(const uint4& v, const uint32_t* lut) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t bits = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bits += lut[(w[i] >> (8 * j)) & 255u] & 31u;
+    return bits;
+}
+
+// Coded bits of a ragged bucket (the last one, when n is not a multiple of
+// d), by one warp, byte by byte at the edge.
+template <bool FOUR>
+__device__ uint32_t ragged_bits(const uint8_t* codes, int64_t n, int d, int64_t b, const uint32_t* lut,
+                                int lane) {
+    const BucketBytes bb = bucket_bytes<FOUR>(codes, n, d, b);
+    const int nw_in = (bb.valid + 3) >> 2;
+    int bits = 0;
+    for (int k = lane; k < nw_in; k += 32) {
+        uint64_t acc;
+        bits += word_bits<FOUR>(bb, k, lut, acc);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
+    return static_cast<uint32_t>(bits);
+}
+
 // ---------------------------------------------------------------- count
 
 struct CountArgs {
@@ -202,34 +248,63 @@ struct CountArgs {
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_count(CountArgs a) {
     __shared__ uint32_t lut[256];
+    __shared__ uint32_t bits_s[kChunk];
     __shared__ uint32_t wsum[kWarpsPerBlock];
     __shared__ uint32_t scan_carry;
     __shared__ bool is_last;
     build_lut<FOUR>(lut);
+    if (threadIdx.x < kChunk) bits_s[threadIdx.x] = 0u;
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t warp_words = 0;
-    for (int j = 0; j < kBucketsPerWarp; ++j) {
-        const int64_t b = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kBucketsPerWarp + j;
-        if (b >= a.nbuckets) break;
-        const BucketBytes bb = bucket_bytes<FOUR>(a.codes, a.n, a.d, b);
-        const int nw_in = (bb.valid + 3) >> 2;
-        int bits = 0;
-        for (int k = lane; k < nw_in; k += 32) {
-            uint64_t acc;
-            bits += word_bits<FOUR>(bb, k, lut, acc);
+    const Geometry g = geometry<FOUR>(a.d);
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
+    const bool ragged = (a.n % a.d) != 0 && b0 + nbc == a.nbuckets;
+    const int nfull = nbc - (ragged ? 1 : 0);
+    const uint4* src = reinterpret_cast<const uint4*>(a.codes + b0 * g.Bb);
+    const int npieces = nfull * g.P;
+    // four pieces per thread in flight, then their lengths
+    constexpr int kBatch = 4;
+    for (int q0 = warp * 32; q0 < npieces; q0 += kBatch * kThreads) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int q = q0 + i * kThreads + lane;
+            v[i] = q < npieces ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int o = 16; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
-        const uint32_t nw = static_cast<uint32_t>((32 + bits + 31) >> 5);
-        if (lane == 0) a.ws.counts[b] = nw;
-        warp_words += nw;
+        for (int i = 0; i < kBatch; ++i) {
+            const int q = q0 + i * kThreads + lane;
+            uint32_t bits = q < npieces ? piece_bits(v[i], lut) : 0u;
+            for (int o = g.G >> 1; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
+            if ((lane & (g.G - 1)) == 0 && q < npieces) {
+                if (g.P <= 32)
+                    bits_s[q / g.P] = bits;
+                else
+                    atomicAdd(bits_s + q / g.P, bits);
+            }
+        }
     }
-    if (lane == 0) wsum[warp] = warp_words;
+    if (ragged && warp == kWarpsPerBlock - 1) {
+        const uint32_t bits = ragged_bits<FOUR>(a.codes, a.n, a.d, b0 + nfull, lut, lane);
+        if (lane == 0) bits_s[nfull] = bits;
+    }
+    __syncthreads();
+    if (warp < kChunk / 32) {
+        const int t = threadIdx.x;
+        uint32_t nw = 0;
+        if (t < nbc) {
+            nw = (32u + bits_s[t] + 31u) >> 5;
+            a.ws.counts[b0 + t] = nw;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) nw += __shfl_xor_sync(0xffffffffu, nw, o);
+        if (lane == 0) wsum[warp] = nw;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t t = 0;
-        for (int w = 0; w < kWarpsPerBlock; ++w) t += wsum[w];
+        for (int w = 0; w < kChunk / 32; ++w) t += wsum[w];
         a.ws.chunk[blockIdx.x] = t;
         __threadfence();
         is_last = atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1;
@@ -273,17 +348,41 @@ struct EncodeArgs {
     Ws ws;
     uint32_t* words;
     uint32_t* offsets;
-    int stage_stride;   // staging words per warp
+    int stage_stride;   // staging words per bucket slot
+    int slots;          // bucket slots per warp (32 / G)
 };
+
+// The stream bits of 16 code bytes (table entries e[]) OR-ed into the
+// staging words from bit position `start`: a 64-bit shift register (hi:lo)
+// collects the bits and hands over every completed word.
+__device__ __forceinline__ void emit_piece(uint32_t* stage, uint32_t start, const uint32_t (&e)[16]) {
+    uint32_t wi = start >> 5;
+    int nacc = static_cast<int>(start & 31u);
+    uint32_t hi = 0u, lo = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int l = static_cast<int>(e[j] & 31u);
+        hi = __funnelshift_l(lo, hi, l);
+        lo = (lo << l) | (e[j] >> 5);
+        nacc += l;
+        if (nacc >= 32) {
+            atomicOr(stage + wi, __funnelshift_r(lo, hi, nacc - 32));
+            ++wi;
+            nacc -= 32;
+        }
+    }
+    if (nacc > 0) atomicOr(stage + wi, lo << (32 - nacc));
+}
 
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_encode(EncodeArgs a) {
     extern __shared__ uint32_t smem[];
     uint32_t* lut = smem;
     uint32_t* offs = smem + 256;                       // [kChunk]
-    uint32_t* stage_all = smem + 256 + kChunk;
+    uint32_t* stages = smem + 256 + kChunk;            // [kWarpsPerBlock * slots][stage_stride]
     build_lut<FOUR>(lut);
-    for (int i = threadIdx.x; i < kWarpsPerBlock * a.stage_stride; i += kThreads) stage_all[i] = 0u;
+    const int nstage = kWarpsPerBlock * a.slots * a.stage_stride;
+    for (int i = threadIdx.x; i < nstage; i += kThreads) stages[i] = 0u;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
     if (warp == 0) {
@@ -299,30 +398,93 @@ __global__ void __launch_bounds__(kThreads) k_elias_encode(EncodeArgs a) {
         if (blockIdx.x == gridDim.x - 1 && lane == 0) a.offsets[a.nbuckets] = a.ws.chunk[gridDim.x];
     }
     __syncthreads();
-    uint32_t* stage = stage_all + warp * a.stage_stride;
-    for (int j = 0; j < kBucketsPerWarp; ++j) {
-        const int local = warp * kBucketsPerWarp + j;
-        const int64_t b = b0 + local;
-        if (b >= a.nbuckets) break;
+    const Geometry g = geometry<FOUR>(a.d);
+    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
+    const bool ragged = (a.n % a.d) != 0 && b0 + nbc == a.nbuckets;
+    const int nfull = nbc - (ragged ? 1 : 0);
+    const int grp = lane / g.G, gl = lane % g.G;
+    uint32_t* stage = stages + (warp * a.slots + grp) * a.stage_stride;
+    const uint4* src = reinterpret_cast<const uint4*>(a.codes + b0 * g.Bb);
+    // Items = (bucket pass j, round r); the next item's 16 bytes and norm are
+    // loaded while the current one is coded.
+    const int R = g.P / g.G;
+    const int first = warp * a.slots, step = kWarpsPerBlock * a.slots;
+    const int passes = nfull > first ? (nfull - first + step - 1) / step : 0;
+    const int items = passes * R;
+    auto load_item = [&](int it, uint4& v, float& nrm) {
+        const int lb = first + (it / R) * step + grp;
+        if (lb < nfull) {
+            v = __ldg(src + lb * g.P + (it % R) * g.G + gl);
+            nrm = __ldg(a.norms + b0 + lb);
+        }
+    };
+    uint4 vn = make_uint4(0u, 0u, 0u, 0u);
+    float nn = 0.0f;
+    if (items) load_item(0, vn, nn);
+    uint32_t pos = 32;
+    for (int it = 0; it < items; ++it) {
+        const int r = it % R;
+        const int lb = first + (it / R) * step + grp;
+        const bool active = lb < nfull;
+        const uint4 v = vn;
+        const float nrm = nn;
+        if (it + 1 < items) load_item(it + 1, vn, nn);
+        if (r == 0) {
+            pos = 32;
+            if (active && gl == 0) stage[0] = __float_as_uint(nrm);
+        }
+        uint32_t e[16];
+        uint32_t len = 0;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                e[4 * i + j] = lut[(w[i] >> (8 * j)) & 255u];
+                len += e[4 * i + j] & 31u;
+            }
+        if (!active) len = 0;
+        uint32_t incl = len;
+        for (int o = 1; o < g.G; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (gl >= o) incl += t;
+        }
+        if (active) emit_piece(stage, pos + incl - len, e);
+        pos += __shfl_sync(0xffffffffu, incl, grp * g.G + g.G - 1);
+        if (r == R - 1) {
+            __syncwarp();
+            if (active) {
+                const int nw = static_cast<int>((pos + 31) >> 5);
+                uint32_t* dst = a.words + offs[lb];
+                for (int k = gl; k < nw; k += g.G) {
+                    dst[k] = stage[k];
+                    stage[k] = 0u;
+                }
+            }
+            __syncwarp();
+        }
+    }
+    if (ragged && warp == kWarpsPerBlock - 1) {
+        // the ragged last bucket, by one warp in slot 0 of this warp
+        const int lb = nfull;
+        const int64_t b = b0 + lb;
         const BucketBytes bb = bucket_bytes<FOUR>(a.codes, a.n, a.d, b);
         const int nw_in = (bb.valid + 3) >> 2;
-        if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
+        uint32_t* st0 = stages + warp * a.slots * a.stage_stride;
+        __syncwarp();
+        if (lane == 0) st0[0] = __float_as_uint(__ldg(a.norms + b));
         uint32_t pos = 32;
         for (int k0 = 0; k0 < nw_in; k0 += 32) {
             uint64_t acc;
             const int len = word_bits<FOUR>(bb, k0 + lane, lut, acc);
             const int incl = warp_incl_sum(len, lane);
-            emit(stage, pos + static_cast<uint32_t>(incl - len), acc, len);
+            emit(st0, pos + static_cast<uint32_t>(incl - len), acc, len);
             pos += static_cast<uint32_t>(__shfl_sync(0xffffffffu, incl, 31));
         }
         __syncwarp();
         const int nw = static_cast<int>((pos + 31) >> 5);
-        uint32_t* dst = a.words + offs[local];
-        for (int k = lane; k < nw; k += 32) {
-            dst[k] = stage[k];
-            stage[k] = 0u;
-        }
-        __syncwarp();
+        uint32_t* dst = a.words + offs[lb];
+        for (int k = lane; k < nw; k += 32) dst[k] = st0[k];
     }
 }
 
@@ -340,9 +502,9 @@ struct DecodeArgs {
     int* status;
 };
 
-// Lookahead table: the codeword (+ sign) at the top of an 8-bit window, as
-// (level << 5) | (sign << 4) | length, or 0 when it does not end inside the
-// window.
+// Single-codeword table: the codeword (+ sign) at the top of an 8-bit
+// window, as (level << 5) | (sign << 4) | length, or 0 when it does not end
+// inside the window.
 __device__ __forceinline__ uint32_t decode_entry(uint32_t x) {
     int pos = 0;
     uint32_t N = 1;
@@ -366,101 +528,168 @@ __device__ __forceinline__ uint32_t decode_entry(uint32_t x) {
     return (level << 5) | (sign << 4) | static_cast<uint32_t>(pos);
 }
 
+// Multi-codeword table: every whole codeword (+ sign) at the front of an
+// 8-bit window, up to KMAX of them and stopping before a level above s:
+// x = (count << 4) | bits used, y = their codes in the output layout
+// (4-bit or 8-bit sign-magnitude), the first one most significant.
+template <bool FOUR>
+__device__ __forceinline__ uint2 multi_entry(uint32_t x, uint32_t s) {
+    constexpr int KMAX = FOUR ? 8 : 4;
+    uint32_t used = 0, k = 0, packed = 0;
+    while (k < KMAX && used < 8) {
+        const uint32_t t = decode_entry((x << used) & 255u);
+        const uint32_t len = t & 15u;
+        if (!t || used + len > 8) break;
+        const uint32_t level = t >> 5, sign = (t >> 4) & 1u;
+        if (level > s) break;
+        packed = FOUR ? (packed << 4) | (sign << 3) | level : (packed << 8) | (sign << 7) | level;
+        used += len;
+        ++k;
+    }
+    return make_uint2((k << 4) | used, packed);
+}
+
+// Output side of the decoder: codes arrive in units of 4 or 8 bits, first
+// code most significant, and leave as 16-byte stores.
+template <bool FOUR>
+struct CodeWriter {
+    static constexpr int kUnit = FOUR ? 4 : 8;
+    static constexpr int kPerWord = 32 / kUnit;
+    uint32_t ahi = 0, alo = 0;   // pending units, right-aligned
+    int pend = 0;
+    uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;   // completed words, newest in b3
+    int nbuf = 0;
+    uint32_t* out;               // 16-byte aligned
+
+    __device__ __forceinline__ void put(uint32_t packed, int k) {
+        const int sh = k * kUnit;                    // <= 32
+        ahi = __funnelshift_lc(alo, ahi, sh);
+        alo = __funnelshift_lc(0u, alo, sh) | packed;
+        pend += k;
+        if (pend >= kPerWord) {
+            pend -= kPerWord;
+            const uint32_t w = __funnelshift_r(alo, ahi, pend * kUnit);
+            b0 = b1;
+            b1 = b2;
+            b2 = b3;
+            b3 = __byte_perm(w, 0u, 0x0123);
+            if (++nbuf == 4) {
+                *reinterpret_cast<uint4*>(out) = make_uint4(b0, b1, b2, b3);
+                out += 4;
+                nbuf = 0;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish() {
+        if (nbuf == 3) {
+            out[0] = b1;
+            out[1] = b2;
+            out[2] = b3;
+        } else if (nbuf == 2) {
+            out[0] = b2;
+            out[1] = b3;
+        } else if (nbuf == 1) {
+            out[0] = b3;
+        }
+        if (pend) {
+            const uint32_t w = __byte_perm(alo << (32 - pend * kUnit), 0u, 0x0123);
+            uint8_t* tail = reinterpret_cast<uint8_t*>(out + nbuf);
+            const int nbytes = (pend * kUnit + 7) / 8;
+            for (int j = 0; j < nbytes; ++j) tail[j] = static_cast<uint8_t>(w >> (8 * j));
+        }
+    }
+};
+
+// One thread per bucket: its stream is walked with a 64-bit window (whi:wlo,
+// `have` valid bits from the top, the next word waiting in `pre`).
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
-    __shared__ uint32_t lut[256];
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = decode_entry(static_cast<uint32_t>(i));
+    constexpr int KMAX = FOUR ? 8 : 4;
+    __shared__ uint2 multi[256];
+    __shared__ uint32_t single[256];
+    const uint32_t smax = static_cast<uint32_t>(a.s);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        multi[i] = multi_entry<FOUR>(static_cast<uint32_t>(i), smax);
+        single[i] = decode_entry(static_cast<uint32_t>(i));
+    }
     __syncthreads();
     const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (b >= a.nbuckets) return;
     const int64_t lo = b * a.d;
-    const int len = static_cast<int>((a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d)));
+    const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
     const uint32_t w_lo = a.offsets[b], w_hi = a.offsets[b + 1];
     const uint32_t* src = a.words + w_lo;
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
     bool bad = avail == 0;
-    a.norms[b] = __uint_as_float(avail ? __ldg(src) : 0u);
-    int64_t next = 1;
-    uint64_t win = 0;   // left-aligned
-    int have = 0;
-    auto refill = [&]() {
-        const uint32_t w = next < avail ? __ldg(src + next) : 0u;
-        win |= static_cast<uint64_t>(w) << (32 - have);
-        have += 32;
-        ++next;
+    auto word = [&](int64_t i) { return i < avail ? __ldg(src + i) : 0u; };
+    a.norms[b] = __uint_as_float(word(0));
+    uint32_t whi = word(1), wlo = word(2), pre = word(3);
+    int64_t next = 4;
+    int have = 64;
+    CodeWriter<FOUR> wr;
+    wr.out = reinterpret_cast<uint32_t*>(a.codes + (FOUR ? lo / 2 : lo));
+    auto consume = [&](int l) {
+        whi = __funnelshift_l(wlo, whi, l);
+        wlo <<= l;
+        have -= l;
+        if (have <= 32) {
+            whi |= __funnelshift_rc(pre, 0u, have);
+            wlo |= pre << (32 - have);
+            have += 32;
+            pre = word(next);
+            ++next;
+        }
     };
-    refill();
-    refill();
-    int64_t used = 32;                 // stream bits consumed, norm included
-    const uint32_t smax = static_cast<uint32_t>(a.s);
-    uint8_t* out = a.codes + (FOUR ? lo / 2 : lo);
-    uint32_t acc = 0;
-    for (int e = 0; e < len; ++e) {
-        if (have <= 32) refill();
-        uint32_t level, sign;
-        int clen;
-        const uint32_t t = lut[win >> 56];
-        if (t) {
-            clen = static_cast<int>(t & 15u);
-            sign = (t >> 4) & 1u;
-            level = t >> 5;
-        } else {
-            // codeword longer than 8 bits (levels of 15 and above)
-            uint32_t N = 1;
-            int p = 0;
-            for (;;) {
-                const uint32_t bit = static_cast<uint32_t>((win << p) >> 63);
-                ++p;
-                if (!bit) break;
-                if (N > 7) {                 // a level above 127: not a stream of codes
-                    bad = true;
-                    N = 1;
-                    break;
-                }
-                const uint32_t v = static_cast<uint32_t>((win << (p - 1)) >> (64 - (N + 1)));
-                p += static_cast<int>(N);
-                N = v;
-            }
-            level = N - 1u;
-            sign = 0u;
-            if (level) {
-                sign = static_cast<uint32_t>((win << p) >> 63);
-                ++p;
-            }
-            clen = p;
-        }
-        win <<= clen;
-        have -= clen;
-        used += clen;
-        if (level > smax) {
+    // A codeword longer than 8 bits in a valid stream is omega(N) for N of
+    // k = 5..8 binary digits: the groups "10" and binary(k - 1) = "1xx", then
+    // N itself, the final 0 and the sign bit (k + 7 bits in all).  Anything
+    // else at this point -- or a level above s -- is not the encoder's
+    // output: it is flagged, and decoding goes on with a clamped level.
+    auto long_code = [&](uint32_t& code, int& l) {
+        const uint32_t top5 = whi >> 27;
+        const uint32_t k = 5u + (top5 & 3u);
+        const uint32_t N = (whi >> (27u - k)) & ((1u << k) - 1u);
+        uint32_t level = N - 1u;
+        const uint32_t sign = (whi >> (25u - k)) & 1u;
+        const bool ok = (top5 >> 2) == 5u && ((whi >> (26u - k)) & 1u) == 0u && (N >> (k - 1u)) == 1u &&
+                        level <= smax;
+        if (!ok) {
             bad = true;
-            level = smax;
+            level = level < smax ? level : smax;
         }
-        if (!level) sign = 0u;
-        if (FOUR) {
-            const uint32_t code = (sign << 3) | level;
-            acc |= code << (8 * ((e >> 1) & 3) + ((e & 1) ? 0 : 4));
-            if ((e & 7) == 7) {
-                reinterpret_cast<uint32_t*>(out)[e >> 3] = acc;
-                acc = 0u;
-            }
-        } else {
-            acc |= ((sign << 7) | level) << (8 * (e & 3));
-            if ((e & 3) == 3) {
-                reinterpret_cast<uint32_t*>(out)[e >> 2] = acc;
-                acc = 0u;
-            }
+        code = FOUR ? (sign << 3) | (level & 7u) : (sign << 7) | level;
+        l = static_cast<int>(k) + 7;
+    };
+    int e = 0;
+    while (len - e >= KMAX) {
+        const uint2 t = multi[whi >> 24];
+        int k = static_cast<int>(t.x >> 4);
+        int l = static_cast<int>(t.x & 15u);
+        uint32_t packed = t.y;
+        if (k == 0) {
+            long_code(packed, l);
+            k = 1;
         }
+        consume(l);
+        wr.put(packed, k);
+        e += k;
     }
-    // the partial last word of a ragged bucket, byte by byte
-    const int per_word = FOUR ? 8 : 4;
-    const int rem = len % per_word;
-    if (rem) {
-        const int nbytes = FOUR ? (rem + 1) / 2 : rem;
-        uint8_t* tail = out + (len / per_word) * 4;
-        for (int j = 0; j < nbytes; ++j) tail[j] = static_cast<uint8_t>(acc >> (8 * j));
+    for (; e < len; ++e) {
+        const uint32_t t = single[whi >> 24];
+        int l = static_cast<int>(t & 15u);
+        const uint32_t level = t >> 5, sign = level ? (t >> 4) & 1u : 0u;
+        uint32_t code;
+        if (t && level <= smax)
+            code = FOUR ? (sign << 3) | level : (sign << 7) | level;
+        else
+            long_code(code, l);
+        consume(l);
+        wr.put(code, 1);
     }
-    if (used > avail * 32) bad = true;
+    wr.finish();
+    // bits consumed: the words fetched (norm included, `pre` not) minus those still in the window
+    if (32 * (next - 1) - have > 32 * avail) bad = true;
     if (bad && a.status) *a.status = GC_ERR_CORRUPT;
 }
 
@@ -510,9 +739,11 @@ int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int b
     else
         k_elias_count<false><<<grid, kThreads, 0, s>>>(ca);
     if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
+    const int P = (four ? bucket / 2 : bucket) / 16;
     EncodeArgs ea{codes, norms, n, bucket, nb, ws, words, offsets,
-                  static_cast<int>(bucket_max_words(bucket, four)) + 2};
-    const size_t smem = sizeof(uint32_t) * (256 + kChunk + static_cast<size_t>(kWarpsPerBlock) * ea.stage_stride);
+                  static_cast<int>(bucket_max_words(bucket, four)) + 2, P < 32 ? 32 / P : 1};
+    const size_t smem = sizeof(uint32_t) *
+                        (256 + kChunk + static_cast<size_t>(kWarpsPerBlock) * ea.slots * ea.stage_stride);
     if (four)
         k_elias_encode<true><<<grid, kThreads, smem, s>>>(ea);
     else
