@@ -689,7 +689,8 @@ def reference_arm(args, rank, world, pg):
 
 CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated",
-         "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127")
+         "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127",
+         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127")
 
 
 def run_case(name: str, n: int):
@@ -729,6 +730,21 @@ def run_case(name: str, n: int):
               for _ in range(W)]
         w = torch.zeros(n, device=dev)
         fn = lambda: gc.gc_2bit_dequant_sum_update(cs, n, 2e-3, gc.GC_UPD_SGD, lr=0.1, weights=w)
+    elif name == "quantize_local":
+        W = 4
+        m = n // W
+        gs = [wl.normal(m, 5e-4, 1 + w, device=dev, dtype=torch.bfloat16) for w in range(W)]
+        rs = [torch.zeros(m, device=dev) for _ in range(W)]
+        cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(W)]
+        wt = torch.zeros(m, device=dev)
+        loc = [torch.empty(m, device=dev) for _ in range(W)]
+        fn = lambda: gc.gc_2bit_quantize_local(gs, rs, cs, wt, loc, 1e-3, 0.1)
+    elif name.startswith("qsgd_maxnorm"):
+        s = 7 if name.endswith("s7") else 127
+        v = wl.qsgd_grad(wl.scaled(wl.QSGD_S7, n), 0, device=dev)
+        nm = torch.empty(gc.qsgd_num_buckets(n, 512), device=dev)
+        c = torch.empty(gc.qsgd_code_bytes(n, s), dtype=torch.uint8, device=dev)
+        fn = lambda: gc.qsgd_quantize_maxnorm(v, 512, s, 42, 0, nm, c)
     elif name.startswith("qsgd_quantize"):
         s = 7 if name.endswith("s7") else 127
         v = wl.qsgd_grad(wl.scaled(wl.QSGD_S7, n), 0, device=dev)

@@ -50,7 +50,9 @@ def compare_codes(gpu_codes, ref_codes, v, n, bucket, s, seed, worker, i0=0):
 
 
 CASES = [(n, b, s) for n in (1, 2, 511, 512, 513, 5 * 512 + 297, 100_001) for b in (128, 512, 2048)
-         for s in (7, 127)] + [(3, 512, 1), (1000, 256, 3), (4097, 1024, 64)]
+         for s in (7, 127)] + [(3, 512, 1), (1000, 256, 3), (4097, 1024, 64)] + [
+    # s = 1 (ternary) and s = floor(sqrt(d)), the dense regime, per bucket size
+    (100_001, 512, 1), (100_001, 512, 22), (5 * 512 + 297, 128, 11), (70_000, 2048, 45)]
 
 
 @pytest.mark.parametrize("n,bucket,s", CASES)
