@@ -512,7 +512,7 @@ def rows(args, dev, peak):
         ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         tm = Timer(stream)
-        rounds = 22
+        rounds = 32
         for rd in range(rounds):
             seed_t = gc.saps_round_seed(scfg.base_seed, rd)
             pairs = gc.saps_matching(seed_t, W)
@@ -523,8 +523,13 @@ def rows(args, dev, peak):
             pe = gc.easgd_step(models, scfg.alpha, scfg.beta, center, stream=stream, prepare=True)
             pf = gc.saps_average_easgd_step(models, vals, cnt, pairs, scfg.alpha, scfg.beta, center, ws,
                                             stream=stream, prepare=True)
+            pr = gc.saps_round(n, scfg.p, seed_t, models, pairs, scfg.alpha, scfg.beta, center, idx, vals,
+                               cnt, ws, st, stream=stream, prepare=True)
+            if rd % 3 == 2:
+                tm.around("r" + k, pr)
+                continue
             tm.around("m" + k, pm)
-            if rd % 2 == 0:
+            if rd % 3 == 0:
                 tm.around("a" + k, pa)
                 tm.around("e" + k, pe)
             else:
@@ -546,6 +551,10 @@ def rows(args, dev, peak):
         out[f"{scfg.name}.round"] = {"ms": round(round_ms, 4), "bytes": int(round_bytes),
                                      "kernels": "saps_mask_compact + saps_average_easgd_step",
                                      "frac": round(round_bytes / (round_ms * 1e-3) / 1e9 / peak, 3)}
+        one_pass_bytes = 4 * K + W * 4 * K + (2 * W + 2) * 4 * n
+        out[f"{scfg.name}.round_one_pass"] = _row(scfg.name, "saps_round (mask + compaction + pair average + "
+                                                  "elastic step, one pass)", one_pass_bytes, tm.ms("r"), peak,
+                                                  W * n, {"masked": K})
         del models, center, vals, idx
 
     # config 4: CD-SGD, 4 workers x 1.3e9 bf16
@@ -690,7 +699,7 @@ def reference_arm(args, rank, world, pg):
 CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated",
          "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127",
-         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127")
+         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001")
 
 
 def run_case(name: str, n: int):
@@ -777,8 +786,9 @@ def run_case(name: str, n: int):
             dc = torch.empty_like(c)
             dn = torch.empty_like(nm)
             fn = lambda: gc.qsgd_elias_decode(words, offs, n, 512, s, dc, dn)
-    elif name in ("saps_mask", "saps_avg", "easgd", "saps_fused"):
-        cfg = wl.scaled(wl.SAPS_P01, n if name not in ("easgd", "saps_fused") else n // 4)
+    elif name in ("saps_mask", "saps_mask_p001", "saps_avg", "easgd", "saps_fused"):
+        base = wl.SAPS_P001 if name == "saps_mask_p001" else wl.SAPS_P01
+        cfg = wl.scaled(base, n if name not in ("easgd", "saps_fused") else n // 4)
         models = wl.saps_models(cfg, device=dev)
         cap = int(cfg.n * cfg.p * 1.2 + 10_000)
         idx = torch.empty(cap, dtype=torch.int32, device=dev)
@@ -790,7 +800,7 @@ def run_case(name: str, n: int):
         seed_t = gc.saps_round_seed(5, 0)
         pairs = gc.saps_matching(seed_t, cfg.workers)
         gc.saps_mask_compact(cfg.n, cfg.p, seed_t, models, idx, vals, cnt, ws, st)
-        if name == "saps_mask":
+        if name in ("saps_mask", "saps_mask_p001"):
             fn = lambda: gc.saps_mask_compact(cfg.n, cfg.p, seed_t, models, idx, vals, cnt, ws, st)
         elif name == "saps_avg":
             fn = lambda: gc.saps_peer_average(models, vals, idx, cnt, pairs)

@@ -38,7 +38,7 @@ __all__ = [
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
     "gc_2bit_step", "gc_2bit_quantize_local", "qsgd_quantize_maxnorm",
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
-    "qsgd_elias_workspace_bytes",
+    "qsgd_elias_workspace_bytes", "saps_round",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -97,6 +97,9 @@ def load():
             "saps_peer_average": (i32, [vp, vp, vp, vp, vp, i32, i64, vp]),
             "easgd_step": (i32, [vp, i32, i64, f32, f32, vp, vp]),
             "saps_average_easgd_step": (i32, [vp, vp, vp, vp, i32, i64, i64, f32, f32, vp, vp, sz, vp]),
+            "saps_round": (i32, [i64, f64, u64, vp, i32, vp, f32, f32, vp, vp, vp, i64, vp, vp, sz, vp, vp]),
+            "gc_testing_saps_round_one_pass": (i32, [i64, f64, u64, vp, i32, vp, f32, f32, vp, vp, vp, i64, vp,
+                                                     vp, sz, vp, vp]),
             "saps_mask_compact_noalloc": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, vp]),
             "gc_testing_saps_mask_compact_withhold": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz,
                                                             vp, i64, u64, vp]),
@@ -433,6 +436,28 @@ def saps_average_easgd_step(models, vals, d_count: torch.Tensor, pairs, alpha: f
             _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream, center))
     return _invoke(lib.saps_average_easgd_step, args, "saps_average_easgd_step", prepare,
                    (list(models), list(vals), d_count, center, workspace, pairs_arr))
+
+
+def saps_round(n: int, p: float, seed_t: int, models, pairs, alpha: float, beta: float,
+               center: torch.Tensor, idx: torch.Tensor, vals, d_count: torch.Tensor,
+               workspace: torch.Tensor, d_status: torch.Tensor, stream=None, prepare: bool = False,
+               _one_pass: bool = False):
+    """One SAPS round in one pass: saps_mask_compact + saps_peer_average +
+    easgd_step, bit for bit while the count fits idx.numel().  ``_one_pass``
+    (tests only) forces the one-pass kernel whatever p is."""
+    lib = load()
+    fn = lib.gc_testing_saps_round_one_pass if _one_pass else lib.saps_round
+    W = len(models)
+    capacity = idx.numel()
+    pairs_arr = (ctypes.c_int * W)(*[int(q) for q in pairs])
+    args = (int(n), float(p), int(seed_t) & 0xFFFFFFFFFFFFFFFF,
+            _ptrs(models, "models", torch.float32, n), W, pairs_arr, float(alpha), float(beta),
+            _dev(center, "center", torch.float32, n), _dev(idx, "idx", torch.int32),
+            _ptrs(vals, "vals", torch.float32, capacity), capacity,
+            _dev(d_count, "d_count", torch.int64, 1), _dev(workspace, "workspace", torch.uint8),
+            workspace.numel(), _dev(d_status, "d_status", torch.int32, 1), _stream(stream, center))
+    return _invoke(fn, args, "saps_round", prepare,
+                   (list(models), center, idx, list(vals), d_count, workspace, d_status, pairs_arr))
 
 
 def easgd_step(models, alpha: float, beta: float, center: torch.Tensor, stream=None,

@@ -73,13 +73,11 @@ struct MaskArgs {
 // without sleeping (they publish their aggregate right after their own
 // block scan); every wait is bounded: after a.wait_ns the missing
 // predecessors count as zero and GC_ERR_TIMEOUT is recorded.
-__device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
+// Walk back from tile `tile` (whose aggregate is already published) and
+// publish its inclusive prefix; returns the exclusive prefix.
+__device__ uint64_t walk_back(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
     const bool publish = tile != a.withhold_tile;
-    if (tile == 0) {
-        if (lane == 0 && publish) st_state(a.state, kFlagPrefix | agg);
-        return 0;
-    }
-    if (lane == 0 && publish) st_state(a.state + tile, kFlagAgg | agg);
+    if (tile == 0) return 0;
     uint64_t excl = 0;
     int64_t end = tile - 1;
     const uint64_t t0 = global_ns();
@@ -113,6 +111,17 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
         if (timed_out) atomicExch(a.d_status, GC_ERR_TIMEOUT);
     }
     return excl;
+}
+
+// Publishes tile `tile`'s aggregate (its inclusive prefix for tile 0).
+__device__ __forceinline__ void publish_aggregate(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
+    if (lane == 0 && tile != a.withhold_tile)
+        st_state(a.state + tile, (tile == 0 ? kFlagPrefix : kFlagAgg) | agg);
+}
+
+__device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
+    publish_aggregate(a, tile, agg, lane);
+    return walk_back(a, tile, agg, lane);
 }
 
 // K6: one CTA per 4096-element tile, tiles taken in launch order from a
@@ -315,6 +324,244 @@ k_easgd_wide(const EasgdArgs a) {
         for (int k = 0; k < a.W; ++k) sum = __fadd_rn(sum, a.models.p[k][i]);
         for (int k = 0; k < a.W; ++k) a.models.p[k][i] = elastic(a.models.p[k][i], c, a.alpha);
         a.center[i] = fmaf(a.beta, __fsub_rn(__fmul_rn(sum, a.inv_w), c), c);
+    }
+}
+
+// ------------------------------------------------------------------ one-pass round
+
+// A whole SAPS round in one pass over the models: the round's mask and its
+// compaction (idx, vals) with the decoupled look-back above, the pair
+// average of the masked coordinates and the EASGD elastic step.  Each CTA
+// takes a 4096-element tile from the dynamic counter, issues its first
+// round of loads (one float4 of every worker and of the center per thread;
+// four rounds of 1024 elements), hashes all 4096 elements, ranks the masked
+// ones with one block scan and publishes the tile's aggregate at once.  Then
+// it streams the four rounds without further barriers: a masked
+// coordinate's pre-average values go to a shared-memory stash (the
+// compacted output) and to a per-thread scratch row from which each worker
+// reads its partner's value for the pair average; the elastic step and the
+// center update are written back.  Last the CTA walks back for its
+// exclusive prefix -- its predecessors have streamed their tiles by then --
+// and writes idx and vals from the stash.  A tile with more masked
+// coordinates than the stash holds walks back first and writes them
+// directly.  Results equal saps_mask_compact + saps_peer_average +
+// easgd_step bit for bit while the count fits the capacity.
+constexpr int kStash = 384;                      // masked entries kept per tile
+constexpr int kRoundElems = 4 * kThreads;        // elements per round (1024)
+
+struct RoundArgs {
+    MaskArgs m;                                  // mask, compaction, look-back
+    PtrTable<float*> models;
+    int partner[GC_MAX_WORKERS];
+    float alpha, beta, inv_w;
+    float* center;
+};
+
+// Round r's float4 of every worker and of the center for element i0.
+template <int MAXW>
+__device__ __forceinline__ void round_load(const RoundArgs& a, int64_t i0, float4 (&v)[MAXW], float4& c) {
+#pragma unroll
+    for (int k = 0; k < MAXW; ++k)
+        if (k < a.m.W) v[k] = ld_f4(a.models.p[k] + i0);
+    c = ld_f4(a.center + i0);
+}
+
+template <int MAXW>
+__global__ void __launch_bounds__(kThreads, 2)
+k_saps_round(const RoundArgs a) {
+    constexpr int kRounds = kTileElems / kRoundElems;      // 4
+    __shared__ float s_stash[kStash * MAXW];
+    __shared__ uint32_t s_sidx[kStash];
+    __shared__ float s_scratch[kThreads * MAXW];
+    __shared__ uint32_t s_wsum[2][kWarpsPerBlock];
+    __shared__ unsigned long long s_tile;
+    __shared__ uint64_t s_excl;
+    const MaskArgs& m = a.m;
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_tile = atomicAdd(m.counter, 1ull);
+    __syncthreads();
+    const int64_t tile = static_cast<int64_t>(s_tile);
+    const int64_t base = tile * kTileElems;
+    const int W = m.W;
+    const uint64_t cap = static_cast<uint64_t>(m.capacity);
+    float* scratch = s_scratch + threadIdx.x * MAXW;
+
+    // round 0's loads go out before the hashing
+    float4 v[MAXW];
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t first = base + 4 * threadIdx.x;
+    if (first + 4 <= m.n) round_load<MAXW>(a, first, v, c);
+    // the mask of all four rounds: 4 bits per round in `bits`
+    uint32_t bits = 0;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t i = base + static_cast<int64_t>(r) * kRoundElems + 4 * threadIdx.x + e;
+            bits |= (i < m.n && splitmix64_top24(m.seed_t ^ static_cast<uint64_t>(i)) < m.thr ? 1u : 0u)
+                    << (4 * r + e);
+        }
+    // per-round block scans, two rounds per 32-bit word (16-bit fields)
+    const uint32_t c01 = __popc(bits & 0xFu) | (__popc(bits & 0xF0u) << 16);
+    const uint32_t c23 = __popc(bits & 0xF00u) | (__popc(bits & 0xF000u) << 16);
+    uint32_t i01 = c01, i23 = c23;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t01 = __shfl_up_sync(0xffffffffu, i01, o);
+        const uint32_t t23 = __shfl_up_sync(0xffffffffu, i23, o);
+        if (lane >= o) {
+            i01 += t01;
+            i23 += t23;
+        }
+    }
+    if (lane == 31) {
+        s_wsum[0][wib] = i01;
+        s_wsum[1][wib] = i23;
+    }
+    __syncthreads();
+    uint32_t b01 = 0, b23 = 0, t01 = 0, t23 = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerBlock; ++w) {
+        const uint32_t x01 = s_wsum[0][w], x23 = s_wsum[1][w];
+        b01 += w < wib ? x01 : 0u;
+        b23 += w < wib ? x23 : 0u;
+        t01 += x01;
+        t23 += x23;
+    }
+    // exclusive rank of this thread's first masked element in each round
+    const uint32_t tot[kRounds] = {t01 & 0xFFFFu, t01 >> 16, t23 & 0xFFFFu, t23 >> 16};
+    const uint32_t e01 = b01 + i01 - c01, e23 = b23 + i23 - c23;
+    uint32_t rank_base[kRounds] = {e01 & 0xFFFFu, e01 >> 16, e23 & 0xFFFFu, e23 >> 16};
+    rank_base[1] += tot[0];
+    rank_base[2] += tot[0] + tot[1];
+    rank_base[3] += tot[0] + tot[1] + tot[2];
+    const uint32_t agg = tot[0] + tot[1] + tot[2] + tot[3];
+    const bool big = agg > static_cast<uint32_t>(kStash);
+    if (wib == 0) {
+        publish_aggregate(m, tile, agg, lane);
+        if (big) {
+            const uint64_t ex = walk_back(m, tile, agg, lane);
+            if (lane == 0) s_excl = ex;
+        }
+    }
+    if (big) __syncthreads();                    // block-uniform
+    const uint64_t excl_big = big ? s_excl : 0;
+
+#pragma unroll 1
+    for (int r = 0; r < kRounds; ++r) {
+        const int64_t i0 = base + static_cast<int64_t>(r) * kRoundElems + 4 * threadIdx.x;
+        if (i0 >= m.n) break;
+        const uint32_t rb = (bits >> (4 * r)) & 15u;
+        const uint32_t rank0 = rank_base[r];
+        if (i0 + 4 <= m.n) {
+            if (r > 0) round_load<MAXW>(a, i0, v, c);
+            if (rb) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (!((rb >> e) & 1u)) continue;
+                    const uint32_t rank = rank0 + __popc(rb & ((1u << e) - 1u));
+#pragma unroll
+                    for (int k = 0; k < MAXW; ++k)
+                        if (k < W) scratch[k] = e == 0 ? v[k].x : e == 1 ? v[k].y : e == 2 ? v[k].z : v[k].w;
+                    if (!big) {
+                        s_sidx[rank] = static_cast<uint32_t>(i0 + e);
+#pragma unroll
+                        for (int k = 0; k < MAXW; ++k)
+                            if (k < W) s_stash[rank * MAXW + k] = scratch[k];
+                    } else if (excl_big + rank < cap) {
+                        m.idx[excl_big + rank] = static_cast<uint32_t>(i0 + e);
+#pragma unroll
+                        for (int k = 0; k < MAXW; ++k)
+                            if (k < W) m.vals.p[k][excl_big + rank] = scratch[k];
+                    }
+#pragma unroll
+                    for (int k = 0; k < MAXW; ++k) {
+                        if (k < W) {
+                            float* dst = e == 0 ? &v[k].x : e == 1 ? &v[k].y : e == 2 ? &v[k].z : &v[k].w;
+                            *dst = __fmul_rn(__fadd_rn(scratch[k], scratch[a.partner[k]]), 0.5f);
+                        }
+                    }
+                }
+            }
+            float4 sum = v[0];
+#pragma unroll
+            for (int k = 1; k < MAXW; ++k)
+                if (k < W) sum = f4_add(sum, v[k]);
+#pragma unroll
+            for (int k = 0; k < MAXW; ++k) {
+                if (k < W) {
+                    st_stream_f4(a.models.p[k] + i0,
+                                 make_float4(elastic(v[k].x, c.x, a.alpha), elastic(v[k].y, c.y, a.alpha),
+                                             elastic(v[k].z, c.z, a.alpha), elastic(v[k].w, c.w, a.alpha)));
+                }
+            }
+            const float4 mean = make_float4(__fmul_rn(sum.x, a.inv_w), __fmul_rn(sum.y, a.inv_w),
+                                            __fmul_rn(sum.z, a.inv_w), __fmul_rn(sum.w, a.inv_w));
+            st_stream_f4(a.center + i0,
+                         make_float4(fmaf(a.beta, __fsub_rn(mean.x, c.x), c.x), fmaf(a.beta, __fsub_rn(mean.y, c.y), c.y),
+                                     fmaf(a.beta, __fsub_rn(mean.z, c.z), c.z), fmaf(a.beta, __fsub_rn(mean.w, c.w), c.w)));
+        } else {
+            // the last n % 4 elements, element by element
+            for (int e = 0; i0 + e < m.n; ++e) {
+                const int64_t i = i0 + e;
+#pragma unroll
+                for (int k = 0; k < MAXW; ++k)
+                    if (k < W) scratch[k] = a.models.p[k][i];
+                const float ce = a.center[i];
+                const bool hit = (rb >> e) & 1u;
+                if (hit) {
+                    const uint32_t rank = rank0 + __popc(rb & ((1u << e) - 1u));
+                    if (!big) {
+                        s_sidx[rank] = static_cast<uint32_t>(i);
+#pragma unroll
+                        for (int k = 0; k < MAXW; ++k)
+                            if (k < W) s_stash[rank * MAXW + k] = scratch[k];
+                    } else if (excl_big + rank < cap) {
+                        m.idx[excl_big + rank] = static_cast<uint32_t>(i);
+#pragma unroll
+                        for (int k = 0; k < MAXW; ++k)
+                            if (k < W) m.vals.p[k][excl_big + rank] = scratch[k];
+                    }
+                }
+                float y[MAXW];
+#pragma unroll
+                for (int k = 0; k < MAXW; ++k)
+                    if (k < W) y[k] = hit ? __fmul_rn(__fadd_rn(scratch[k], scratch[a.partner[k]]), 0.5f) : scratch[k];
+                float sum = y[0];
+#pragma unroll
+                for (int k = 1; k < MAXW; ++k)
+                    if (k < W) sum = __fadd_rn(sum, y[k]);
+#pragma unroll
+                for (int k = 0; k < MAXW; ++k)
+                    if (k < W) a.models.p[k][i] = elastic(y[k], ce, a.alpha);
+                a.center[i] = fmaf(a.beta, __fsub_rn(__fmul_rn(sum, a.inv_w), ce), ce);
+            }
+        }
+    }
+
+    // C. the exclusive prefix (predecessors have long published), then idx
+    // and vals from the stash
+    if (!big && wib == 0) {
+        const uint64_t ex = walk_back(m, tile, agg, lane);
+        if (lane == 0) s_excl = ex;
+    }
+    __syncthreads();
+    const uint64_t excl = s_excl;
+    if (!big) {
+        const uint32_t kept = cap > excl ? static_cast<uint32_t>(min(static_cast<uint64_t>(agg), cap - excl)) : 0u;
+        for (uint32_t k = threadIdx.x; k < kept; k += kThreads) m.idx[excl + k] = s_sidx[k];
+        const uint32_t pairs = kept * static_cast<uint32_t>(W);
+        for (uint32_t q = threadIdx.x; q < pairs; q += kThreads) {
+            const uint32_t w = q / kept;
+            const uint32_t k = q - w * kept;
+            m.vals.p[w][excl + k] = s_stash[k * MAXW + w];
+        }
+    }
+    if (threadIdx.x == 0 && tile == m.ntiles - 1) {
+        const uint64_t total = excl + agg;
+        *m.d_count = total;
+        if (total > cap) atomicExch(m.d_status, GC_ERR_CAPACITY);
     }
 }
 
@@ -657,6 +904,94 @@ int saps_average_easgd_step(float* const* models, const float* const* vals, cons
         k_saps_average_easgd_wide<<<grid, kThreads, 0, s>>>(a);
     }
     return launch_status();
+}
+
+static int saps_round_impl(int64_t n, double p, uint64_t seed_t, float* const* models, int W, const int* pairs,
+                           float alpha, float beta, float* center, uint32_t* idx, float* const* vals,
+                           int64_t capacity, uint64_t* d_count, void* workspace, size_t workspace_bytes,
+                           int* d_status, gc_stream_t stream, bool force_one_pass) {
+    if (n < 0 || n > 0xFFFFFFFFll || W < 2 || W > GC_MAX_WORKERS || (W & 1) || capacity < 0 ||
+        !(p > 0.0 && p <= 1.0) || !isfinite(alpha) || !isfinite(beta))
+        return GC_ERR_INVALID;
+    if (!models || !pairs || !center || !d_count || !d_status || !workspace || (capacity > 0 && (!idx || !vals)))
+        return GC_ERR_INVALID;
+    if (workspace_bytes < saps_workspace_bytes(n)) return GC_ERR_INVALID;
+    if (!aligned16(workspace) || !aligned16(d_count) || !aligned16(center) || (capacity > 0 && !aligned16(idx)))
+        return GC_ERR_ALIGN;
+    RoundArgs a;
+    bool seen[GC_MAX_WORKERS] = {false};
+    for (int w = 0; w < W; ++w) {
+        const int q = pairs[w];
+        if (q < 0 || q >= W || seen[q]) return GC_ERR_INVALID;
+        seen[q] = true;
+    }
+    for (int q = 0; q < W / 2; ++q) {
+        a.partner[pairs[2 * q]] = pairs[2 * q + 1];
+        a.partner[pairs[2 * q + 1]] = pairs[2 * q];
+    }
+    for (int w = 0; w < W; ++w) {
+        if (!models[w] || (capacity > 0 && !vals[w])) return GC_ERR_INVALID;
+        if (!aligned16(models[w]) || (capacity > 0 && !aligned16(vals[w]))) return GC_ERR_ALIGN;
+    }
+    // The one-pass kernel while a tile's expected masked count (4096 p) stays
+    // well inside its stash; otherwise, and for W > 16, the compaction and
+    // then the fused pair average + elastic step.
+    if (W > 16 || (!force_one_pass && p * kTileElems > 0.75 * kStash)) {
+        if (force_one_pass) return GC_ERR_INVALID;
+        const int rc = saps_mask_compact(n, p, seed_t, models, W, idx, vals, capacity, d_count, workspace,
+                                         workspace_bytes, d_status, stream);
+        if (rc != GC_OK) return rc;
+        return saps_average_easgd_step(models, vals, d_count, pairs, W, n, capacity, alpha, beta, center,
+                                       workspace, workspace_bytes, stream);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n == 0) return cudaMemsetAsync(d_count, 0, sizeof(uint64_t), s) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    MaskArgs& m = a.m;
+    for (int w = 0; w < W; ++w) {
+        a.models.p[w] = models[w];
+        m.models.p[w] = models[w];
+        m.vals.p[w] = capacity > 0 ? vals[w] : nullptr;
+    }
+    m.n = n;
+    m.seed_t = seed_t;
+    m.thr = static_cast<uint32_t>(ceil(p * 16777216.0));
+    m.W = W;
+    m.idx = idx;
+    m.capacity = capacity;
+    m.d_count = d_count;
+    m.counter = static_cast<unsigned long long*>(workspace);
+    m.state = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) + kWsHeader);
+    m.ntiles = mask_tiles(n);
+    m.d_status = d_status;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.inv_w = static_cast<float>(1.0 / W);
+    a.center = center;
+    if (cudaMemsetAsync(workspace, 0, kWsHeader + sizeof(uint64_t) * static_cast<size_t>(m.ntiles), s) !=
+        cudaSuccess)
+        return GC_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>(m.ntiles);
+    if (W <= 4)
+        k_saps_round<4><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_saps_round<16><<<grid, kThreads, 0, s>>>(a);
+    return launch_status();
+}
+
+int saps_round(int64_t n, double p, uint64_t seed_t, float* const* models, int W, const int* pairs,
+               float alpha, float beta, float* center, uint32_t* idx, float* const* vals, int64_t capacity,
+               uint64_t* d_count, void* workspace, size_t workspace_bytes, int* d_status,
+               gc_stream_t stream) {
+    return saps_round_impl(n, p, seed_t, models, W, pairs, alpha, beta, center, idx, vals, capacity, d_count,
+                           workspace, workspace_bytes, d_status, stream, false);
+}
+
+int gc_testing_saps_round_one_pass(int64_t n, double p, uint64_t seed_t, float* const* models, int W,
+                                   const int* pairs, float alpha, float beta, float* center, uint32_t* idx,
+                                   float* const* vals, int64_t capacity, uint64_t* d_count, void* workspace,
+                                   size_t workspace_bytes, int* d_status, gc_stream_t stream) {
+    return saps_round_impl(n, p, seed_t, models, W, pairs, alpha, beta, center, idx, vals, capacity, d_count,
+                           workspace, workspace_bytes, d_status, stream, true);
 }
 
 int easgd_step(float* const* models, int W, int64_t n, float alpha, float beta, float* center,

@@ -426,6 +426,27 @@ GC_API int saps_average_easgd_step(float *const *models, const float *const *val
                                    size_t workspace_bytes, gc_stream_t stream);
 
 /*
+ * saps_round -- one whole SAPS round (section II: mask, sparsified exchange,
+ * single-peer gossip average; EASGD elastic step from the IMerge notes) in
+ * one pass over the models: the results of
+ *   saps_mask_compact(...); saps_peer_average(...); easgd_step(...)
+ * bit for bit (idx, vals, d_count, models, center), as long as the masked
+ * count fits the capacity.  When it does not, d_status gets GC_ERR_CAPACITY,
+ * idx/vals hold the first `capacity` entries and every masked coordinate is
+ * still averaged (the pair's values are at hand in the pass).
+ *
+ *   pairs      host int [W], a permutation of 0..W-1 (as saps_matching)
+ *   others     as saps_mask_compact and easgd_step; W even, 2 <= W <= 64
+ *              (W > 16 runs saps_mask_compact + saps_average_easgd_step)
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int saps_round(int64_t n, double p, uint64_t seed_t, float *const *models, int W,
+                      const int *pairs, float alpha, float beta, float *center,
+                      uint32_t *idx, float *const *vals, int64_t capacity,
+                      uint64_t *d_count, void *workspace, size_t workspace_bytes,
+                      int *d_status, gc_stream_t stream);
+
+/*
  * easgd_step -- EASGD local and global updates (IMerge design notes,
  * "Interleaved Communication Scheduling"), without a gradient term:
  *   mean_i = (sum_k models[k][i]) / W                (values before the step)

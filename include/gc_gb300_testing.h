@@ -30,6 +30,22 @@ GC_API int gc_testing_saps_mask_compact_withhold(int64_t n, double p, uint64_t s
                                                  int *d_status, int64_t withhold_tile,
                                                  uint64_t wait_ns, gc_stream_t stream);
 
+/*
+ * gc_testing_saps_round_one_pass -- saps_round with the one-pass kernel
+ * whatever p is (saps_round itself takes the two-launch path when a tile's
+ * expected masked count would not fit the kernel's shared-memory stash), so
+ * that the kernel's own overflow path -- a tile whose stash fills fetches
+ * its prefix mid-tile and writes the rest directly -- can be tested.
+ * W <= 16.  Arguments and errors as saps_round.
+ */
+GC_API int gc_testing_saps_round_one_pass(int64_t n, double p, uint64_t seed_t,
+                                          float *const *models, int W, const int *pairs,
+                                          float alpha, float beta, float *center,
+                                          uint32_t *idx, float *const *vals, int64_t capacity,
+                                          uint64_t *d_count, void *workspace,
+                                          size_t workspace_bytes, int *d_status,
+                                          gc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

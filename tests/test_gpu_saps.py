@@ -210,3 +210,90 @@ def test_saps_rounds_chain_fused():
         for w in range(W):
             assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w} round {t}")
         assert_close(host_f32(center), rc, scale, what=f"center round {t}")
+
+
+@pytest.mark.parametrize("one_pass", [False, True], ids=["public", "one-pass-kernel"])
+@pytest.mark.parametrize("W", [2, 4, 16, 18])
+@pytest.mark.parametrize("n,p", [(1, 0.5), (33, 1.0), (4097, 0.01), (100_003, 0.01), (100_003, 0.001),
+                                 (3 * 4096 + 5, 0.3), (50_001, 0.9), (40_000, 0.09)])
+def test_one_pass_round_is_bitwise_the_three_calls(one_pass, W, n, p):
+    """saps_round == saps_mask_compact + saps_peer_average + easgd_step, bit for
+    bit: count, idx, vals, models and center.  With the one-pass kernel forced,
+    p = 0.09, 0.3 and 0.9 fill a tile's stash (the mid-tile prefix path)."""
+    if one_pass and W > 16:
+        pytest.skip("the one-pass kernel takes W <= 16")
+    base = [wl.normal(n, 0.05, 700 + w, device=DEV) for w in range(W)]
+    c0 = wl.saps_initial_center(base)
+    ma = [b.clone() for b in base]
+    mb = [b.clone() for b in base]
+    ca, cb = c0.clone(), c0.clone()
+    seed_t = gc.saps_round_seed(13, n + W)
+    pairs = gc.saps_matching(seed_t, W)
+    comp = Compactor(n, W, n)
+    comp.run(p, seed_t, ma)
+    gc.saps_peer_average(ma, [v[:n] for v in comp.vals], comp.idx[:n], comp.count[:1], pairs)
+    gc.easgd_step(ma, 0.9, 0.6, ca)
+    K, idx, vals, st = comp.result()
+    r = Compactor(n, W, n)
+    gc.saps_round(n, p, seed_t, mb, pairs, 0.9, 0.6, cb, r.idx[:n], [v[:n] for v in r.vals], r.count[:1],
+                  r.ws, r.status, _one_pass=one_pass)
+    K2, idx2, vals2, st2 = r.result()
+    assert (K2, st2) == (K, st) == (K, 0)
+    np.testing.assert_array_equal(idx2, idx)
+    for w in range(W):
+        np.testing.assert_array_equal(vals2[w].view(np.uint32), vals[w].view(np.uint32))
+        assert torch.equal(ma[w].view(torch.int32), mb[w].view(torch.int32)), f"worker {w}"
+    assert torch.equal(ca.view(torch.int32), cb.view(torch.int32))
+    check_guard(r.idx, n)
+    for v in r.vals:
+        check_guard(v, n)
+
+
+@pytest.mark.parametrize("p", [0.05, 0.2])
+def test_one_pass_round_capacity_overflow(p):
+    """More masked entries than capacity: GC_ERR_CAPACITY, the true count, and
+    the first `capacity` entries of idx/vals as the compaction writes them."""
+    n, W, cap = 60_000, 4, 1000
+    base = [wl.normal(n, 0.05, 300 + w, device=DEV) for w in range(W)]
+    seed_t = gc.saps_round_seed(2, 9)
+    pairs = gc.saps_matching(seed_t, W)
+    comp = Compactor(n, W, cap)
+    comp.run(p, seed_t, [b.clone() for b in base])
+    K, idx, vals, st = comp.result()
+    r = Compactor(n, W, cap)
+    center = wl.saps_initial_center(base)
+    gc.saps_round(n, p, seed_t, [b.clone() for b in base], pairs, 0.9, 0.9, center, r.idx[:cap],
+                  [v[:cap] for v in r.vals], r.count[:1], r.ws, r.status, _one_pass=True)
+    K2, idx2, vals2, st2 = r.result()
+    assert K2 == K > cap and st2 == gc.GC_ERR_CAPACITY
+    np.testing.assert_array_equal(idx2, idx)
+    for w in range(W):
+        np.testing.assert_array_equal(vals2[w].view(np.uint32), vals[w].view(np.uint32))
+    check_guard(r.idx, cap)
+
+
+def test_one_pass_rounds_chain_against_oracle():
+    """Six rounds of saps_round on 16 workers against the oracle's fp64 chain."""
+    n, W, p, alpha, beta = 150_011, 16, 0.01, 0.9, 0.9
+    cfg = wl.scaled(wl.SAPS_P01, n)
+    models = wl.saps_models(cfg, device=DEV)
+    center = wl.saps_initial_center(models)
+    ref = [host_f32(m).astype(np.float64) for m in models]
+    rc = host_f32(center).astype(np.float64)
+    r = Compactor(n, W, n)
+    scale = np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc)
+    for t in range(6):
+        seed_t = gc.saps_round_seed(cfg.base_seed, t)
+        pairs = gc.saps_matching(seed_t, W)
+        gc.saps_round(n, p, seed_t, models, pairs, alpha, beta, center, r.idx[:n], [v[:n] for v in r.vals],
+                      r.count[:1], r.ws, r.status)
+        rK, ridx, rvals = oracle.saps_mask_compact(n, p, seed_t, ref)
+        oracle.saps_peer_average(ref, rvals, ridx, np.array(pairs, np.int32))
+        oracle.easgd_step(ref, alpha, beta, rc)
+        K, idx, vals, st = r.result()
+        assert K == rK and st == 0
+        np.testing.assert_array_equal(idx, ridx)
+        scale = np.maximum(scale, np.max(np.abs(np.stack(ref)), axis=0) + np.abs(rc))
+        for w in range(W):
+            assert_close(host_f32(models[w]), ref[w], scale, what=f"model {w} round {t}")
+        assert_close(host_f32(center), rc, scale, what=f"center round {t}")
