@@ -699,7 +699,7 @@ def reference_arm(args, rank, world, pg):
 CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated",
          "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127",
-         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001")
+         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001", "saps_round")
 
 
 def run_case(name: str, n: int):
@@ -786,9 +786,9 @@ def run_case(name: str, n: int):
             dc = torch.empty_like(c)
             dn = torch.empty_like(nm)
             fn = lambda: gc.qsgd_elias_decode(words, offs, n, 512, s, dc, dn)
-    elif name in ("saps_mask", "saps_mask_p001", "saps_avg", "easgd", "saps_fused"):
+    elif name in ("saps_mask", "saps_mask_p001", "saps_avg", "easgd", "saps_fused", "saps_round"):
         base = wl.SAPS_P001 if name == "saps_mask_p001" else wl.SAPS_P01
-        cfg = wl.scaled(base, n if name not in ("easgd", "saps_fused") else n // 4)
+        cfg = wl.scaled(base, n if name not in ("easgd", "saps_fused", "saps_round") else n // 4)
         models = wl.saps_models(cfg, device=dev)
         cap = int(cfg.n * cfg.p * 1.2 + 10_000)
         idx = torch.empty(cap, dtype=torch.int32, device=dev)
@@ -806,6 +806,8 @@ def run_case(name: str, n: int):
             fn = lambda: gc.saps_peer_average(models, vals, idx, cnt, pairs)
         elif name == "saps_fused":
             fn = lambda: gc.saps_average_easgd_step(models, vals, cnt, pairs, 0.9, 0.9, center, ws)
+        elif name == "saps_round":
+            fn = lambda: gc.saps_round(cfg.n, cfg.p, seed_t, models, pairs, 0.9, 0.9, center, idx, vals, cnt, ws, st)
         else:
             fn = lambda: gc.easgd_step(models, 0.9, 0.9, center)
     elif name == "compensated":
