@@ -100,18 +100,40 @@ def source_sha(rel: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+def ncu_entry(kernel: str):
+    """The committed ncu summary of a kernel (DRAM bytes and warp instructions
+    per launch, scaled to the launch bench.py times), or None when the kernel
+    source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)[kernel]
         if d.get("source_sha") != source_sha(d["source"]):
             return None
-        return float(d["bytes_per_launch"])
+        return d
     except Exception:
         return None
+
+
+def ncu_traffic(kernel: str):
+    d = ncu_entry(kernel)
+    return float(d["bytes_per_launch"]) if d else None
+
+
+# Issue roofline for kernels bound by instruction issue rather than HBM:
+# 152 SMs x 4 schedulers x 1 warp instruction per clock at the 2070 MHz
+# maximum SM clock.
+ISSUE_PEAK = 152 * 4 * 2070e6
+
+
+def issue_roofline(kernel: str, ms_list):
+    d = ncu_entry(kernel)
+    if not d or "warp_inst_per_launch" not in d or not ms_list:
+        return None
+    rate = float(d["warp_inst_per_launch"]) / (_median(ms_list) * 1e-3)
+    return {"bound": "issue", "achieved": round(rate / 1e12, 4), "peak": round(ISSUE_PEAK / 1e12, 4),
+            "unit": "T warp instructions/s", "frac": round(rate / ISSUE_PEAK, 3),
+            "warp_inst_per_launch": int(d["warp_inst_per_launch"])}
 
 
 class ClockSampler:
@@ -460,7 +482,7 @@ def rows(args, dev, peak):
             tm.around("d" if i >= 2 else "w", pd)
         torch.cuda.synchronize(dev)
         out[f"{qcfg.name}.quantize"] = _row(qcfg.name, "qsgd_quantize", n * 4 + cb + 4 * nb, tm.ms("q"),
-                                            peak, n)
+                                            peak, n, {"issue": issue_roofline(f"qsgd_quantize_s{s}", tm.ms("q"))})
         out[f"{qcfg.name}.dequant_sum"] = _row(qcfg.name, "qsgd_dequant_sum", W * (cb + 4 * nb) + 4 * n,
                                                tm.ms("d"), peak, W * n)
         pm = [gc.qsgd_quantize_maxnorm(vs[w], qcfg.bucket, s, qcfg.seed, w, norms[w], codes[w], stream=stream,
@@ -470,7 +492,18 @@ def rows(args, dev, peak):
                 tm.around("m" if i >= 2 else "w", pm[w])
         torch.cuda.synchronize(dev)
         out[f"{qcfg.name}.quantize_maxnorm"] = _row(qcfg.name, "qsgd_quantize_maxnorm", n * 4 + cb + 4 * nb,
-                                                    tm.ms("m"), peak, n)
+                                                    tm.ms("m"), peak, n,
+                                                    {"issue": issue_roofline(f"qsgd_maxnorm_s{s}", tm.ms("m"))})
+        # every worker's quantisation + the dequant-sum in one pass
+        pst = gc.qsgd_step(vs, qcfg.bucket, s, qcfg.seed, norms, codes, 1.0 / W, outq, stream=stream,
+                           prepare=True)
+        for i in range(6):
+            tm.around("t" if i >= 2 else "w", pst)
+        torch.cuda.synchronize(dev)
+        sep_ms = W * _median(tm.ms("q")) + _median(tm.ms("d"))
+        out[f"{qcfg.name}.step_one_pass"] = _row(qcfg.name, "qsgd_step (4 workers quantised + dequant-sum, one pass)",
+                                                 W * (n * 4 + cb + 4 * nb) + 4 * n, tm.ms("t"), peak, W * n,
+                                                 {"separate_calls_ms": round(sep_ms, 5)})
         # Elias-omega stream of each worker's (l2-norm) codes, and its decode
         for w in range(W):
             pq[w]()
@@ -492,12 +525,14 @@ def rows(args, dev, peak):
         torch.cuda.synchronize(dev)
         total = sum(int(o[nb].item()) for o in offs) / W
         bits = {"bits_per_coord": round(32 * total / n, 4),
-                "bits_per_coord_with_offsets": round(32 * (total + nb + 1) / n, 4)}
+                "bits_per_coord_with_offsets": round(32 * (total + nb + 1) / n, 4),
+                "issue": issue_roofline(f"elias_encode_s{s}", tm.ms("e"))}
         out[f"{qcfg.name}.elias_encode"] = _row(qcfg.name, "qsgd_elias_encode (count + encode)",
                                                 cb + 4 * nb + 4 * total + 4 * (nb + 1), tm.ms("e"), peak, n,
                                                 bits)
         out[f"{qcfg.name}.elias_decode"] = _row(qcfg.name, "qsgd_elias_decode",
-                                                4 * total + 4 * (nb + 1) + cb + 4 * nb, tm.ms("x"), peak, n)
+                                                4 * total + 4 * (nb + 1) + cb + 4 * nb, tm.ms("x"), peak, n,
+                                                {"issue": issue_roofline(f"elias_decode_s{s}", tm.ms("x"))})
         del vs, norms, codes, outq, words, offs, ews, dcodes, dnorms
 
     # config 5: SAPS + EASGD, 16 workers x 25,557,032, p = 0.01 and 0.001

@@ -38,7 +38,7 @@ __all__ = [
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
     "gc_2bit_step", "gc_2bit_quantize_local", "qsgd_quantize_maxnorm",
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
-    "qsgd_elias_workspace_bytes", "saps_round",
+    "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -86,6 +86,7 @@ def load():
             "qsgd_quantize": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
             "qsgd_dequant_sum": (i32, [vp, vp, i32, i64, i32, i32, f32, vp, vp]),
             "qsgd_quantize_maxnorm": (i32, [vp, i64, i32, i32, u64, i32, vp, vp, vp]),
+            "qsgd_step": (i32, [vp, i32, i64, i32, i32, u64, i32, vp, vp, f32, vp, vp]),
             "qsgd_elias_encode": (i32, [vp, vp, i64, i32, i32, vp, u64, vp, vp, sz, vp]),
             "qsgd_elias_max_words": (u64, [i64, i32, i32]),
             "qsgd_elias_workspace_bytes": (sz, [i64, i32]),
@@ -372,6 +373,21 @@ def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket
             None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words))
     keep = (words, offsets, codes, norms) + (() if status is None else (status,))
     return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
+
+
+def qsgd_step(grads, bucket: int, s_levels: int, seed: int, norms, codes, scale: float,
+              out: torch.Tensor, maxnorm: bool = False, stream=None, prepare: bool = False):
+    """Every worker's qsgd_quantize (worker index = position) and the
+    dequant-sum, in one pass; bit-identical to the separate calls."""
+    lib = load()
+    W = len(grads)
+    n = out.numel()
+    args = (_ptrs(grads, "grads", torch.float32, n), W, n, int(bucket), int(s_levels),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, 1 if maxnorm else 0,
+            _ptrs(norms, "norms", torch.float32, qsgd_num_buckets(n, bucket)),
+            _ptrs(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)), float(scale),
+            _dev(out, "out", torch.float32, n), _stream(stream, out))
+    return _invoke(lib.qsgd_step, args, "qsgd_step", prepare, (list(grads), list(norms), list(codes), out))
 
 
 def saps_round_seed(base_seed: int, t: int) -> int:

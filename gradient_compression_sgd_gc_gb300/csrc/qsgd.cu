@@ -107,13 +107,14 @@ __device__ __forceinline__ bool all_zero(const float4 (&v)[ROUNDS], int lane) {
     return !__any_sync(0xffffffffu, nz);
 }
 
-// One warp per bucket; the grid covers every bucket.
-template <int ROUNDS, bool FOUR, bool MAXNORM>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
-k_qsgd_quantize(const QArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (b >= a.nbuckets) return;
+// One bucket of one worker, by one warp: the bucket's norm (written by lane
+// 0), its codes (written), and -- when SUM -- every element's dequantised
+// term added to sum[j][k] exactly as k_qsgd_dequant_sum adds it (one fma of
+// the level with the signed norm * unit_scale), so that a fused pass over
+// all workers equals the quantise calls followed by the dequant-sum.
+template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM>
+__device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int lane, float unit_scale,
+                                                float (&sum)[ROUNDS][4]) {
     constexpr int D = 128 * ROUNDS;
     constexpr uint32_t kSignShift = FOUR ? 3 : 7;
     const float s_f = static_cast<float>(a.s);
@@ -202,6 +203,14 @@ k_qsgd_quantize(const QArgs a) {
                 c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
             }
         }
+        if (SUM) {
+            const float u = __fmul_rn(norm, unit_scale);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float lf = __uint_as_float(0x4B000000u | (c[k] & (FOUR ? 7u : 127u))) - 8388608.0f;
+                sum[j][k] = __fmaf_rn(lf, (c[k] >> kSignShift) ? -u : u, sum[j][k]);
+            }
+        }
         if (FOUR) {
             const uint32_t lo2 = (c[0] << 4) | c[1];
             const uint32_t hi2 = (c[2] << 4) | c[3];
@@ -219,6 +228,67 @@ k_qsgd_quantize(const QArgs a) {
                 for (int k = 0; k < 4; ++k)
                     if (e + k < a.n) a.codes[e + k] = static_cast<uint8_t>(c[k]);
             }
+        }
+    }
+}
+
+// One warp per bucket; the grid covers every bucket.
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+k_qsgd_quantize(const QArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= a.nbuckets) return;
+    float unused[ROUNDS][4];
+    quantize_bucket<ROUNDS, FOUR, MAXNORM, false>(a, b, lane, 0.0f, unused);
+}
+
+// Every worker's quantisation and the dequant-sum in one pass: one warp per
+// bucket runs the W workers in order and keeps the sum in registers.
+struct StepArgs {
+    PtrTable<const float*> v;
+    PtrTable<float*> norms;
+    PtrTable<uint8_t*> codes;
+    QArgs q;              // per-worker fields (v, seed_w, norms, codes) set in the loop
+    int W;
+    uint64_t seed;
+    float unit_scale;
+    float* out;
+};
+
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 3)
+k_qsgd_step(const StepArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= a.q.nbuckets) return;
+    constexpr int D = 128 * ROUNDS;
+    float sum[ROUNDS][4];
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sum[j][k] = 0.0f;
+    for (int w = 0; w < a.W; ++w) {
+        QArgs q = a.q;
+        q.v = a.v.p[w];
+        q.seed_w = a.seed ^ (static_cast<uint64_t>(static_cast<uint32_t>(w)) << 48);
+        q.norms = a.norms.p[w];
+        q.codes = a.codes.p[w];
+        quantize_bucket<ROUNDS, FOUR, MAXNORM, true>(q, b, lane, a.unit_scale, sum);
+    }
+    const int64_t b0 = b * D;
+    const bool full = b0 + D <= a.q.n;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+        const int64_t e = b0 + 128 * j + 4 * lane;
+        const float4 o = make_float4(sum[j][0], sum[j][1], sum[j][2], sum[j][3]);
+        if (full) {
+            st_stream_f4(a.out + e, o);
+        } else {
+            if (e < a.q.n) a.out[e] = o.x;
+            if (e + 1 < a.q.n) a.out[e + 1] = o.y;
+            if (e + 2 < a.q.n) a.out[e + 2] = o.z;
+            if (e + 3 < a.q.n) a.out[e + 3] = o.w;
         }
     }
 }
@@ -361,6 +431,19 @@ int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
     return launch_status();
 }
 
+template <bool FOUR, bool MAXNORM>
+int launch_step(int rounds, const StepArgs& a, unsigned grid, cudaStream_t s) {
+    switch (rounds) {
+        case 1: k_qsgd_step<1, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 2: k_qsgd_step<2, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 4: k_qsgd_step<4, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 8: k_qsgd_step<8, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 16: k_qsgd_step<16, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        default: return GC_ERR_INVALID;
+    }
+    return launch_status();
+}
+
 template <bool FOUR>
 int launch_dequant(int rounds, const DArgs& a, cudaStream_t s) {
     const unsigned g1 = blocks_for_tiles(a.nbuckets);
@@ -443,6 +526,43 @@ int qsgd_dequant_sum(const uint8_t* const* codes, const float* const* norms, int
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return s_levels <= 7 ? launch_dequant<true>(bucket / 128, a, s)
                          : launch_dequant<false>(bucket / 128, a, s);
+}
+
+int qsgd_step(const float* const* grads, int W, int64_t n, int bucket, int s_levels, uint64_t seed,
+              int maxnorm, float* const* norms, uint8_t* const* codes, float scale, float* out,
+              gc_stream_t stream) {
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127 ||
+        !isfinite(scale) || (maxnorm != 0 && maxnorm != 1))
+        return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grads || !norms || !codes || !out) return GC_ERR_INVALID;
+    StepArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!grads[w] || !norms[w] || !codes[w]) return GC_ERR_INVALID;
+        if (!aligned16(grads[w]) || !aligned16(norms[w]) || !aligned16(codes[w])) return GC_ERR_ALIGN;
+        a.v.p[w] = grads[w];
+        a.norms.p[w] = norms[w];
+        a.codes.p[w] = codes[w];
+    }
+    if (!aligned16(out)) return GC_ERR_ALIGN;
+    a.q.v = nullptr;
+    a.q.n = n;
+    a.q.nbuckets = (n + bucket - 1) / bucket;
+    a.q.seed_w = 0;
+    a.q.s = s_levels;
+    a.q.norms = nullptr;
+    a.q.codes = nullptr;
+    a.W = W;
+    a.seed = seed;
+    a.unit_scale = static_cast<float>(static_cast<double>(scale) / s_levels);
+    a.out = out;
+    const unsigned grid = blocks_for_tiles(a.q.nbuckets);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (maxnorm)
+        return s_levels <= 7 ? launch_step<true, true>(bucket / 128, a, grid, s)
+                             : launch_step<false, true>(bucket / 128, a, grid, s);
+    return s_levels <= 7 ? launch_step<true, false>(bucket / 128, a, grid, s)
+                         : launch_step<false, false>(bucket / 128, a, grid, s);
 }
 
 }  // extern "C"

@@ -268,6 +268,24 @@ GC_API int qsgd_dequant_sum(const uint8_t *const *codes, const float *const *nor
                      int W, int64_t n, int bucket, int s_levels, float scale,
                      float *out, gc_stream_t stream);
 
+/*
+ * qsgd_step -- synchronous parallel QSGD's compression and aggregation for W
+ * simulated workers in one pass (Knowl 3: each worker quantises its
+ * gradient; the decoded messages are summed): the results of
+ *   qsgd_quantize(grads[w], n, bucket, s_levels, seed, w, norms[w], codes[w])
+ *   for w = 0 .. W-1 (qsgd_quantize_maxnorm when maxnorm = 1), then
+ *   qsgd_dequant_sum(codes, norms, W, n, bucket, s_levels, scale, out)
+ * bit for bit, with each bucket's W gradients read once and the sum kept in
+ * registers (the codes and norms are still written: they are the messages).
+ *   grads      host array of W device pointers, fp32 [n], read only
+ *   norms, codes   host arrays of W device pointers, written as qsgd_quantize
+ *   out        device fp32 [n], written
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_step(const float *const *grads, int W, int64_t n, int bucket, int s_levels,
+                     uint64_t seed, int maxnorm, float *const *norms, uint8_t *const *codes,
+                     float scale, float *out, gc_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* QSGD Elias-omega coding                                                */
 /* ---------------------------------------------------------------------- */

@@ -198,3 +198,32 @@ def test_maxnorm_quantize_parity(n, bucket, s):
     check_guard(codes, cb)
     ref = oracle.qsgd_dequant_sum([rc], [rs], n, bucket, s)
     assert_close(host_f32(out), ref, np.abs(ref), what="maxnorm dequant")
+
+
+@pytest.mark.parametrize("maxnorm", [False, True], ids=["l2", "maxnorm"])
+@pytest.mark.parametrize("s", [1, 7, 22, 127])
+@pytest.mark.parametrize("n,bucket,W", [(1, 512, 1), (5 * 512 + 297, 512, 4), (100_001, 128, 3),
+                                         (70_000, 2048, 2), (4096 * 3 + 1, 256, 9)])
+def test_one_pass_step_is_bitwise_the_separate_calls(n, bucket, W, s, maxnorm):
+    """qsgd_step == W x qsgd_quantize (or _maxnorm) + qsgd_dequant_sum, bit for
+    bit: codes, norms and the sum."""
+    cfg = wl.scaled(wl.QSGD_S7, n)
+    vs = [wl.qsgd_grad(cfg, w, device=DEV) for w in range(W)]
+    nb, cb = gc.qsgd_num_buckets(n, bucket), gc.qsgd_code_bytes(n, s)
+    n1 = [torch.empty(nb, device=DEV) for _ in range(W)]
+    c1 = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    q = gc.qsgd_quantize_maxnorm if maxnorm else gc.qsgd_quantize
+    for w in range(W):
+        q(vs[w], bucket, s, 77, w, n1[w], c1[w])
+    o1 = torch.empty(n, device=DEV)
+    gc.qsgd_dequant_sum(c1, n1, n, bucket, s, 1.0 / W, o1)
+    n2 = [torch.full((nb,), 7.0, device=DEV) for _ in range(W)]
+    c2 = [torch.full((cb,), 0xEE, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    o2 = guarded(n, torch.float32)
+    gc.qsgd_step(vs, bucket, s, 77, n2, c2, 1.0 / W, o2[:n], maxnorm=maxnorm)
+    torch.cuda.synchronize()
+    check_guard(o2, n)
+    for w in range(W):
+        assert torch.equal(n1[w].view(torch.int32), n2[w].view(torch.int32))
+        assert torch.equal(c1[w], c2[w])
+    assert torch.equal(o1.view(torch.int32), o2[:n].view(torch.int32))
