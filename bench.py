@@ -503,7 +503,8 @@ def rows(args, dev, peak):
         sep_ms = W * _median(tm.ms("q")) + _median(tm.ms("d"))
         out[f"{qcfg.name}.step_one_pass"] = _row(qcfg.name, "qsgd_step (4 workers quantised + dequant-sum, one pass)",
                                                  W * (n * 4 + cb + 4 * nb) + 4 * n, tm.ms("t"), peak, W * n,
-                                                 {"separate_calls_ms": round(sep_ms, 5)})
+                                                 {"separate_calls_ms": round(sep_ms, 5),
+                                                  "issue": issue_roofline(f"qsgd_step_s{s}", tm.ms("t"))})
         # Elias-omega stream of each worker's (l2-norm) codes, and its decode
         for w in range(W):
             pq[w]()
@@ -574,7 +575,8 @@ def rows(args, dev, peak):
         assert int(st.item()) == 0
         rm = tm.ms("m")
         out[f"{scfg.name}.mask_compact"] = _row(scfg.name, "saps_mask_compact", 4 * K + W * 8 * K, rm, peak, n,
-                                                {"bound": "alu", "masked": K})
+                                                {"masked": K, "issue": issue_roofline(
+                                                    "saps_mask" if scfg.p >= 0.01 else "saps_mask_p001", rm)})
         out[f"{scfg.name}.peer_average"] = _row(scfg.name, "saps_peer_average", (W // 2) * 20 * K,
                                                 tm.ms("a"), peak, None)
         out[f"{scfg.name}.easgd"] = _row(scfg.name, "easgd_step", (2 * W + 2) * 4 * n, tm.ms("e"), peak, W * n)
@@ -734,7 +736,8 @@ def reference_arm(args, rank, world, pg):
 CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqsum_sgd", "saps_fused", "qsgd_quantize_s7", "qsgd_quantize_s127",
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated",
          "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127",
-         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001", "saps_round")
+         "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001", "saps_round",
+         "qsgd_step_s7", "qsgd_step_s127")
 
 
 def run_case(name: str, n: int):
@@ -783,6 +786,15 @@ def run_case(name: str, n: int):
         wt = torch.zeros(m, device=dev)
         loc = [torch.empty(m, device=dev) for _ in range(W)]
         fn = lambda: gc.gc_2bit_quantize_local(gs, rs, cs, wt, loc, 1e-3, 0.1)
+    elif name.startswith("qsgd_step"):
+        s = 7 if name.endswith("s7") else 127
+        W = 4
+        m = n // W
+        vs = [wl.qsgd_grad(wl.scaled(wl.QSGD_S7, m), w, device=dev) for w in range(W)]
+        nms = [torch.empty(gc.qsgd_num_buckets(m, 512), device=dev) for _ in range(W)]
+        cs = [torch.empty(gc.qsgd_code_bytes(m, s), dtype=torch.uint8, device=dev) for _ in range(W)]
+        out = torch.empty(m, device=dev)
+        fn = lambda: gc.qsgd_step(vs, 512, s, 42, nms, cs, 0.25, out)
     elif name.startswith("qsgd_maxnorm"):
         s = 7 if name.endswith("s7") else 127
         v = wl.qsgd_grad(wl.scaled(wl.QSGD_S7, n), 0, device=dev)
