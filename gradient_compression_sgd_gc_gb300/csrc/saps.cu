@@ -22,6 +22,7 @@ constexpr int kItems = 16;                         // rounds of 32 elements per 
 constexpr int kWarpSpan = 32 * kItems;             // 512 elements per warp
 constexpr int kTileElems = kWarpsPerBlock * kWarpSpan;   // 4096 elements per CTA tile
 constexpr size_t kWsHeader = 64;                   // tile counter + padding
+constexpr int kGatherStash = 512;                  // gathered values staged per tile (entries x W)
 
 constexpr uint64_t kFlagAgg = 1ull << 62;
 constexpr uint64_t kFlagPrefix = 2ull << 62;
@@ -135,6 +136,7 @@ __device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int 
 __global__ void __launch_bounds__(kThreads)
 k_saps_mask_compact(const MaskArgs a) {
     __shared__ uint32_t s_list[kTileElems];
+    __shared__ float s_vals[kGatherStash];
     __shared__ uint32_t s_warp_excl[kWarpsPerBlock];
     __shared__ uint32_t s_warp_tot[kWarpsPerBlock];
     __shared__ unsigned long long s_tile;
@@ -177,26 +179,14 @@ k_saps_mask_compact(const MaskArgs a) {
         }
         if (lane < kWarpsPerBlock) s_warp_excl[lane] = vi - v;
         const uint32_t agg = __shfl_sync(0xffffffffu, vi, kWarpsPerBlock - 1);
-        const uint64_t excl = lookback(a, tile, agg, lane);
-        if (lane == 0) {
-            s_excl = excl;
-            s_agg = agg;
-        }
+        publish_aggregate(a, tile, agg, lane);
+        if (lane == 0) s_agg = agg;
     }
     __syncthreads();
 
     const uint32_t wex = s_warp_excl[wib];
-    const uint64_t excl = s_excl;
     const uint32_t agg = s_agg;
     const uint32_t lt = (1u << lane) - 1u;
-    // per 32-element group: mask bits and the masked count before the group
-    if (a.group_mask != nullptr && lane < kItems) {
-        const int64_t g = (wbase >> 5) + lane;
-        if (g * 32 < a.n) {
-            a.group_mask[g] = my_mask;
-            a.group_excl[g] = static_cast<uint32_t>(excl + wex + round_excl);
-        }
-    }
 #pragma unroll 4
     for (int r = 0; r < kItems; ++r) {
         const uint32_t m = __shfl_sync(0xffffffffu, my_mask, r);
@@ -205,8 +195,35 @@ k_saps_mask_compact(const MaskArgs a) {
     }
     __syncthreads();
 
-    // indices, then one (entry, worker) pair per thread so that every random
-    // read of the gather is in flight at once; stores stay coalesced per worker
+    // Warp 0 walks back for the prefix while the other warps gather the
+    // tile's values into shared memory (when they fit), so the gather's
+    // random reads and the look-back's round trips overlap.
+    const uint32_t all_pairs = agg * static_cast<uint32_t>(a.W);
+    const bool staged = all_pairs <= static_cast<uint32_t>(kGatherStash);
+    if (wib == 0) {
+        const uint64_t ex = walk_back(a, tile, agg, lane);
+        if (lane == 0) s_excl = ex;
+    } else if (staged) {
+        for (uint32_t q = threadIdx.x - 32; q < all_pairs; q += kThreads - 32) {
+            const uint32_t w = q / agg;
+            const uint32_t k = q - w * agg;
+            s_vals[q] = __ldg(a.models.p[w] + s_list[k]);
+        }
+    }
+    __syncthreads();
+    const uint64_t excl = s_excl;
+
+    // per 32-element group: mask bits and the masked count before the group
+    if (a.group_mask != nullptr && lane < kItems) {
+        const int64_t g = (wbase >> 5) + lane;
+        if (g * 32 < a.n) {
+            a.group_mask[g] = my_mask;
+            a.group_excl[g] = static_cast<uint32_t>(excl + wex + round_excl);
+        }
+    }
+    // indices, then the values: from the stash, or one (entry, worker) pair
+    // per thread so that every random read is in flight at once; stores stay
+    // coalesced per worker
     const uint32_t kept = static_cast<uint64_t>(a.capacity) > excl
         ? static_cast<uint32_t>(min(static_cast<uint64_t>(agg), static_cast<uint64_t>(a.capacity) - excl)) : 0u;
     for (uint32_t k = threadIdx.x; k < kept; k += kThreads) a.idx[excl + k] = s_list[k];
@@ -214,7 +231,7 @@ k_saps_mask_compact(const MaskArgs a) {
     for (uint32_t q = threadIdx.x; q < pairs; q += kThreads) {
         const uint32_t w = q / kept;
         const uint32_t k = q - w * kept;
-        a.vals.p[w][excl + k] = __ldg(a.models.p[w] + s_list[k]);
+        a.vals.p[w][excl + k] = staged ? s_vals[w * agg + k] : __ldg(a.models.p[w] + s_list[k]);
     }
     if (threadIdx.x == 0 && tile == a.ntiles - 1) {
         const uint64_t total = excl + agg;
