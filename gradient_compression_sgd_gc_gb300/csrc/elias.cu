@@ -208,13 +208,31 @@ __device__ __forceinline__ Geometry geometry(int d) {
 }
 
 // Coded bits of 16 code bytes.
+// For 4-bit codes the length follows from three comparisons of the level
+// (omega(level + 1) + sign is 1, 4, 7 or 8 bits for level 0, 1-2, 3-6, 7):
+// L = 1 + 3 [level >= 1] + 3 [level >= 3] + [level = 7], counted for the
+// eight codes of a word at once with bit tricks on the 3-bit level fields.
+template <bool FOUR>
 __device__ __forceinline__ uint32_t piece_bits(const uint4& v, const uint32_t* lut) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t bits = 0;
+    if (FOUR) {
+        uint32_t ge1 = 0, ge3 = 0, eq7 = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lv = w[i] & 0x77777777u;
+            const uint32_t b1 = lv >> 1, b2 = lv >> 2;
+            ge1 += __popc((lv | b1 | b2) & 0x11111111u);
+            ge3 += __popc((b2 | (b1 & lv)) & 0x11111111u);
+            eq7 += __popc(b2 & b1 & lv & 0x11111111u);
+        }
+        bits = 32u + 3u * (ge1 + ge3) + eq7;
+    } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) bits += lut[(w[i] >> (8 * j)) & 255u] & 31u;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bits += lut[(w[i] >> (8 * j)) & 255u] & 31u;
+    }
     return bits;
 }
 
@@ -250,7 +268,6 @@ __global__ void __launch_bounds__(kThreads) k_elias_count(CountArgs a) {
     __shared__ uint32_t lut[256];
     __shared__ uint32_t bits_s[kChunk];
     __shared__ uint32_t wsum[kWarpsPerBlock];
-    __shared__ uint32_t scan_carry;
     __shared__ bool is_last;
     build_lut<FOUR>(lut);
     if (threadIdx.x < kChunk) bits_s[threadIdx.x] = 0u;
@@ -275,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_count(CountArgs a) {
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
             const int q = q0 + i * kThreads + lane;
-            uint32_t bits = q < npieces ? piece_bits(v[i], lut) : 0u;
+            uint32_t bits = q < npieces ? piece_bits<FOUR>(v[i], lut) : 0u;
             for (int o = g.G >> 1; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
             if ((lane & (g.G - 1)) == 0 && q < npieces) {
                 if (g.P <= 32)
@@ -313,26 +330,33 @@ __global__ void __launch_bounds__(kThreads) k_elias_count(CountArgs a) {
     if (!is_last) return;
     // The last CTA: exclusive prefix of the per-CTA totals, in place, and
     // the grand total after them.  Every other CTA fenced its total before
-    // taking its ticket; the totals are read from L2.
+    // taking its ticket; the totals are read from L2.  Thread t scans the
+    // contiguous run [t*per, (t+1)*per) with all its loads in flight, then
+    // one block scan of the run totals gives each run its base.
     __threadfence();
     const int nchunks = static_cast<int>(gridDim.x);
-    if (threadIdx.x == 0) scan_carry = 0;
+    const int per = (nchunks + kThreads - 1) / kThreads;
+    const int lo = threadIdx.x * per;
+    const int hi = lo + per < nchunks ? lo + per : nchunks;
+    uint32_t run = 0;
+    for (int i = lo; i < hi; ++i) run += __ldcg(a.ws.chunk + i);
+    const int incl = warp_incl_sum(static_cast<int>(run), lane);
+    if (lane == 31) wsum[warp] = static_cast<uint32_t>(incl);
     __syncthreads();
-    for (int base = 0; base < nchunks; base += kThreads) {
-        const int i = base + threadIdx.x;
-        const uint32_t v = i < nchunks ? __ldcg(a.ws.chunk + i) : 0u;
-        const int incl = warp_incl_sum(static_cast<int>(v), lane);
-        if (lane == 31) wsum[warp] = static_cast<uint32_t>(incl);
-        __syncthreads();
-        uint32_t before = scan_carry;
-        for (int w = 0; w < warp; ++w) before += wsum[w];
-        if (i < nchunks) a.ws.chunk[i] = before + static_cast<uint32_t>(incl) - v;
-        __syncthreads();
-        if (threadIdx.x == kThreads - 1) scan_carry = before + static_cast<uint32_t>(incl);
-        __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerBlock; ++w) {
+        before += w < warp ? wsum[w] : 0u;
+        total += wsum[w];
+    }
+    uint32_t acc = before + static_cast<uint32_t>(incl) - run;
+    for (int i = lo; i < hi; ++i) {
+        const uint32_t v = __ldcg(a.ws.chunk + i);
+        a.ws.chunk[i] = acc;
+        acc += v;
     }
     if (threadIdx.x == 0) {
-        a.ws.chunk[nchunks] = scan_carry;
+        a.ws.chunk[nchunks] = total;
         *a.ws.ticket = 0u;
     }
 }
