@@ -637,8 +637,37 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
         multi[i] = multi_entry<FOUR>(static_cast<uint32_t>(i), smax);
         single[i] = decode_entry(static_cast<uint32_t>(i));
     }
+    // The CTA's 256 buckets are handed to its threads in order of stream
+    // length (a counting sort on the word count), so that the threads of a
+    // warp walk streams of about the same length instead of idling on the
+    // warp's longest one.
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_wsum[kWarpsPerBlock];
+    __shared__ uint16_t s_order[kThreads];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    s_hist[threadIdx.x] = 0u;
     __syncthreads();
-    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t bb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint32_t key = 255u;
+    if (bb < a.nbuckets) {
+        const uint32_t nw = a.offsets[bb + 1] - a.offsets[bb];
+        key = nw < 255u ? nw : 255u;
+    }
+    const uint32_t pos = atomicAdd(s_hist + key, 1u);
+    __syncthreads();
+    const uint32_t h = s_hist[threadIdx.x];
+    const int incl = warp_incl_sum(static_cast<int>(h), lane);
+    if (lane == 31) s_wsum[warp] = static_cast<uint32_t>(incl);
+    __syncthreads();
+    uint32_t start = static_cast<uint32_t>(incl) - h;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerBlock; ++w) start += w < warp ? s_wsum[w] : 0u;
+    __syncthreads();
+    s_hist[threadIdx.x] = start;                 // bin starts
+    __syncthreads();
+    s_order[s_hist[key] + pos] = static_cast<uint16_t>(threadIdx.x);
+    __syncthreads();
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + s_order[threadIdx.x];
     if (b >= a.nbuckets) return;
     const int64_t lo = b * a.d;
     const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
