@@ -227,3 +227,34 @@ def test_one_pass_step_is_bitwise_the_separate_calls(n, bucket, W, s, maxnorm):
         assert torch.equal(n1[w].view(torch.int32), n2[w].view(torch.int32))
         assert torch.equal(c1[w], c2[w])
     assert torch.equal(o1.view(torch.int32), o2[:n].view(torch.int32))
+
+
+@pytest.mark.parametrize("s", [7, 127])
+@pytest.mark.parametrize("n,W", [(5 * 512 + 297, 4), (100_001, 3)])
+def test_one_pass_step_against_oracle(n, W, s):
+    """qsgd_step element by element against the oracle: norms within rel 1e-5
+    (bit-equal in practice), codes up to boundary cases, the average within
+    the float tolerance away from those cases."""
+    cfg = wl.scaled(wl.QSGD_S7, n)
+    d = 512
+    vs = [wl.qsgd_grad(cfg, w, device=DEV) for w in range(W)]
+    nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
+    norms = [torch.empty(nb, device=DEV) for _ in range(W)]
+    codes = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    out = torch.empty(n, device=DEV)
+    gc.qsgd_step(vs, d, s, 31, norms, codes, 1.0 / W, out)
+    torch.cuda.synchronize()
+    rcs, rns = [], []
+    bad_any = np.zeros(n, bool)
+    for w in range(W):
+        vh = host_f32(vs[w])
+        rn, rc = oracle.qsgd_quantize(vh, d, s, 31, w)
+        assert_close(host_f32(norms[w]), rn, np.abs(rn), what="norms")
+        _, bad = compare_codes(codes[w].cpu().numpy(), rc, vh, n, d, s, 31, w)
+        bad_any |= bad
+        rcs.append(rc)
+        rns.append(rn)
+    ref = oracle.qsgd_dequant_sum(rcs, rns, n, d, s, 1.0 / W)
+    terms = sum(np.abs(oracle.qsgd_dequant_sum([rcs[w]], [rns[w]], n, d, s)) for w in range(W)) / W
+    keep = ~bad_any
+    assert_close(host_f32(out)[keep], ref[keep], terms[keep], what="average")

@@ -347,3 +347,25 @@ def test_quantize_with_local_update(n, B, dtype):
         gf = gh if dtype == torch.float32 else (gh.astype(np.uint32) << 16).view(np.float32)
         assert_close(host_f32(local[b][:n]), l_ref, np.abs(wh) + lr_loc * np.abs(gf), what="local weights")
         check_guard(local[b], n)
+
+
+@pytest.mark.parametrize("n,W", [(517, 3), (100_003, 8)])
+def test_fused_step_against_oracle(n, W):
+    """gc_2bit_step (SGD) element by element against the oracle: every worker's
+    codes and residual bit-exact, the weights within the float tolerance."""
+    t, lr = 2e-3, 0.1
+    grads = [wl.normal(n, 1e-3, 160 + w, device=DEV) for w in range(W)]
+    res = [wl.normal(n, 1e-3, 180 + w, device=DEV) for w in range(W)]
+    r_ref = [host_f32(r).copy() for r in res]
+    codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    w0 = wl.uniform(n, 0.05, 17, device=DEV)
+    w_ref = host_f32(w0).astype(np.float64)
+    gc.gc_2bit_step(grads, res, codes, t, gc.GC_UPD_SGD, lr=lr, weights=w0)
+    torch.cuda.synchronize()
+    c_ref = [oracle.twobit_quantize(host_f32(grads[w]), r_ref[w], t) for w in range(W)]
+    scale = np.abs(w_ref) + lr * t
+    oracle.twobit_dequant_sum_update(c_ref, n, t, oracle.KIND_SGD, lr=lr, weights=w_ref)
+    for w in range(W):
+        np.testing.assert_array_equal(host_u32(codes[w]), c_ref[w])
+        np.testing.assert_array_equal(host_f32(res[w]).view(np.uint32), r_ref[w].view(np.uint32))
+    assert_close(host_f32(w0), w_ref, scale, what="weights")
