@@ -360,33 +360,72 @@ def e2e(args, dev):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline_twobit(seconds: float, m: int | None = None):
-    """The oracle as it stands (one thread, plain C) on a bounded sample of the
-    headline workload: 8 workers x m elements per step, quantise + dequant-sum
-    + SGD, repeated for about `seconds`."""
+def _oracle_twobit_chunk(job):
+    """One host process of the CPU baseline: the oracle, as it stands, on its
+    own chunk of m elements per worker of the headline workload (the 2-bit
+    step is elementwise, so chunks are independent).  Runs `warmup` steps,
+    then `steps` timed steps, or -- with steps = 0 -- as many as fit in
+    `seconds`.  Returns (timed steps, seconds)."""
+    chunk, m, warmup, steps, seconds = job
     import numpy as np
     import oracle
     from gradient_compression_sgd_gc_gb300 import workloads as wl
 
     cfg = wl.TWOBIT_DQ_SGD
     W, t, lr = cfg.workers, cfg.threshold, cfg.lr
-    m = m or (1 << 21)
-    grads = [wl.normal(m, cfg.grad_std, 1000 + w).numpy() for w in range(W)]
+    grads = [wl.normal(m, cfg.grad_std, 1000 + 16 * chunk + w).numpy() for w in range(W)]
     res = [np.zeros(m, np.float32) for _ in range(W)]
-    w64 = wl.uniform(m, 0.05, 7).numpy().astype(np.float64)
-    steps = 0
-    t0 = time.perf_counter()
-    while True:
+    w64 = wl.uniform(m, 0.05, 7 + chunk).numpy().astype(np.float64)
+
+    def step():
         codes = [oracle.twobit_quantize(grads[q], res[q], t) for q in range(W)]
         oracle.twobit_dequant_sum_update(codes, m, t, oracle.KIND_SGD, lr=lr, weights=w64)
-        steps += 1
+
+    for _ in range(warmup):
+        step()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        step()
+        done += 1
         el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": round(W * m * 4 * steps / el / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{steps} steps of the 8-worker 2-bit step on {m} elements per worker "
-                      f"({el:.1f} s, single-threaded C oracle)"}
+        if (steps and done >= steps) or (not steps and el >= seconds):
+            return done, el
+
+
+def _host_cores() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except Exception:
+        return max(1, os.cpu_count() or 1)
+
+
+def _run_chunks(jobs):
+    """The chunk jobs on a process pool of one process per job (started with
+    spawn: this process has initialised CUDA)."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()                      # once, before the children load it
+    if len(jobs) == 1:
+        return [_oracle_twobit_chunk(jobs[0])]
+    with mp.get_context("spawn").Pool(len(jobs)) as pool:
+        return pool.map(_oracle_twobit_chunk, jobs)
+
+
+def cpu_baseline_twobit(seconds: float, m: int | None = None):
+    """The oracle as it stands (plain C, one thread per process) on every host
+    core at once, each process on its own bounded chunk of the headline
+    workload: 8 workers x m elements per step, quantise + dequant-sum + SGD,
+    repeated for about `seconds`."""
+    cfg_W = 8
+    m = m or (1 << 20)
+    cores = _host_cores()
+    out = _run_chunks([(c, m, 1, 0, seconds) for c in range(cores)])
+    rate = sum(cfg_W * m * 4 * st / el for st, el in out)
+    steps = sum(st for st, _ in out)
+    return {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes, each the 8-worker 2-bit step on its own {m} elements per worker "
+                      f"({steps} steps in about {seconds:.0f} s, single-threaded C oracle per process)"}
 
 
 # ----------------------------------------------------------------------------- rows
@@ -692,40 +731,25 @@ def reference_arm(args, rank, world, pg):
     total_steps = args.steps + args.warmup
     budget = 90.0
     per_step = min(1.0, budget / max(1, total_steps))
-    # calibrate the sample size so one step takes about per_step seconds
+    cores = _host_cores()
+    # calibrate each process's chunk so that one step takes about per_step
+    # seconds (one process, then every core running the same size)
     m = 1 << 14
-    grads = [wl.normal(m, cfg.grad_std, 1000 + w).numpy() for w in range(W)]
-    res = [np.zeros(m, np.float32) for _ in range(W)]
-    w64 = np.zeros(m)
-
-    def step(mm, gg, rr, ww):
-        codes = [oracle.twobit_quantize(gg[q], rr[q], t) for q in range(W)]
-        oracle.twobit_dequant_sum_update(codes, mm, t, oracle.KIND_SGD, lr=lr, weights=ww)
-
-    t0 = time.perf_counter()
-    for _ in range(3):
-        step(m, grads, res, w64)
-    one = (time.perf_counter() - t0) / 3
-    m = int(max(1 << 10, min(cfg.n, m * per_step / max(one, 1e-6)))) // 16 * 16
-    grads = [wl.normal(m, cfg.grad_std, 1000 + w).numpy() for w in range(W)]
-    res = [np.zeros(m, np.float32) for _ in range(W)]
-    w64 = wl.uniform(m, 0.05, 7).numpy().astype(np.float64)
-    for _ in range(args.warmup):
-        step(m, grads, res, w64)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step(m, grads, res, w64)
-    el = time.perf_counter() - t0
-    ms = el / args.steps * 1e3
-    value = W * m * 4 / (ms * 1e-3) / 1e9
-    sample = f"{m} of {cfg.n} elements per worker per step, single-threaded C oracle"
+    st, el = _oracle_twobit_chunk((0, m, 1, 3, 0.0))
+    one = el / st
+    m = int(max(1 << 10, min(cfg.n // cores, m * per_step / max(one, 1e-6)))) // 16 * 16
+    out = _run_chunks([(c, m, args.warmup, args.steps, 0.0) for c in range(cores)])
+    ms = max(el / st for st, el in out) * 1e3
+    value = cores * W * m * 4 / (ms * 1e-3) / 1e9
+    sample = (f"{cores} x {m} of {cfg.n} elements per worker per step, one single-threaded C oracle "
+              f"process per host core")
     return {"impl": "reference", "metric": HEADLINE_METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "twobit_dq_sgd: 8 workers x 25,557,032 fp32, t=2e-3, lr=0.1 (sampled)",
-                       "sample_elements_per_worker": m},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                       "sample_elements_per_worker": cores * m},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
