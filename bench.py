@@ -482,7 +482,38 @@ def rows(args, dev, peak):
                                         tm.ms("qh"), peak, n)
     out["twobit_w1.dequant"] = _row("twobit_w1", "gc_2bit_dequant_sum_update NONE W=1", 4.25 * n,
                                     tm.ms("d"), peak, n)
-    del g, r, c, o
+    # the configuration's ten steps (fresh gradient each step, residual
+    # carried, codes dequantised) captured once as a CUDA graph: 20 launches
+    # replayed without host launch overhead, against the same calls eagerly
+    gs = [wl.twobit_grad(cfg, st, 0, device=dev) for st in range(cfg.steps)]
+    cs = [torch.empty(gc.code_words(n), dtype=torch.int32, device=dev) for _ in range(cfg.steps)]
+    os_ = [torch.empty(n, device=dev) for _ in range(cfg.steps)]
+
+    def ten_steps():
+        for st in range(cfg.steps):
+            gc.gc_2bit_quantize(gs[st], r, cs[st], cfg.threshold)
+            gc.gc_2bit_dequant_sum_update([cs[st]], n, cfg.threshold, gc.GC_UPD_NONE, out=os_[st])
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        ten_steps()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ten_steps()
+    tm = Timer(stream)
+    for i in range(reps + 3):
+        flush_l2(flush)
+        tm.around("g" if i >= 3 else "w", graph.replay)
+        flush_l2(flush)
+        tm.around("e" if i >= 3 else "w", ten_steps)
+    torch.cuda.synchronize(dev)
+    ten_bytes = cfg.steps * (12.25 + 4.25) * n
+    out["twobit_w1.ten_steps_graph"] = _row("twobit_w1", "10 x (gc_2bit_quantize + dequant) as one CUDA graph "
+                                            "(L2 flushed before each replay)", ten_bytes, tm.ms("g"), peak,
+                                            cfg.steps * n, {"eager_ms": round(_median(tm.ms("e")), 5)})
+    del g, r, c, o, gs, cs, os_, graph
 
     # config 2 as one fused launch per step vs the two-launch path of the headline
     cfg2 = wl.TWOBIT_DQ_SGD
