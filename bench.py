@@ -494,18 +494,28 @@ def rows(args, dev, peak):
             gc.gc_2bit_quantize(gs[st], r, cs[st], cfg.threshold)
             gc.gc_2bit_dequant_sum_update([cs[st]], n, cfg.threshold, gc.GC_UPD_NONE, out=os_[st])
 
-    side = torch.cuda.Stream(dev)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        ten_steps()
-    stream.wait_stream(side)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        ten_steps()
+    def ten_fused():
+        # one launch per step: gc_2bit_step with one worker quantises and
+        # writes the dequantised values (update kind NONE)
+        for st in range(cfg.steps):
+            gc.gc_2bit_step([gs[st]], [r], [cs[st]], cfg.threshold, gc.GC_UPD_NONE, out=os_[st])
+
+    graphs = {}
+    for key, fn in (("g", ten_steps), ("f", ten_fused)):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        graphs[key] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graphs[key]):
+            fn()
     tm = Timer(stream)
     for i in range(reps + 3):
         flush_l2(flush)
-        tm.around("g" if i >= 3 else "w", graph.replay)
+        tm.around("g" if i >= 3 else "w", graphs["g"].replay)
+        flush_l2(flush)
+        tm.around("f" if i >= 3 else "w", graphs["f"].replay)
         flush_l2(flush)
         tm.around("e" if i >= 3 else "w", ten_steps)
     torch.cuda.synchronize(dev)
@@ -513,7 +523,10 @@ def rows(args, dev, peak):
     out["twobit_w1.ten_steps_graph"] = _row("twobit_w1", "10 x (gc_2bit_quantize + dequant) as one CUDA graph "
                                             "(L2 flushed before each replay)", ten_bytes, tm.ms("g"), peak,
                                             cfg.steps * n, {"eager_ms": round(_median(tm.ms("e")), 5)})
-    del g, r, c, o, gs, cs, os_, graph
+    out["twobit_w1.ten_fused_steps_graph"] = _row("twobit_w1", "10 x gc_2bit_step (W=1, NONE: quantise + "
+                                                  "dequant in one launch) as one CUDA graph (L2 flushed)",
+                                                  ten_bytes, tm.ms("f"), peak, cfg.steps * n)
+    del g, r, c, o, gs, cs, os_, graphs
 
     # config 2 as one fused launch per step vs the two-launch path of the headline
     cfg2 = wl.TWOBIT_DQ_SGD

@@ -67,15 +67,14 @@ struct MaskArgs {
     int64_t withhold_tile = -1;        // test hook: this tile never publishes (-1: none)
 };
 
-// Exclusive prefix of tile `tile` whose own count is `agg`; run by one warp.
-// Publishes (aggregate) first, then walks back over its predecessors 32 at a
-// time (one coalesced 256-byte read of their state words) until it meets one
-// that has published its inclusive prefix.  Pending predecessors are polled
-// without sleeping (they publish their aggregate right after their own
-// block scan); every wait is bounded: after a.wait_ns the missing
-// predecessors count as zero and GC_ERR_TIMEOUT is recorded.
-// Walk back from tile `tile` (whose aggregate is already published) and
-// publish its inclusive prefix; returns the exclusive prefix.
+// Exclusive prefix of tile `tile` whose own count `agg` it has already
+// published (publish_aggregate); run by one warp.  Walks back over its
+// predecessors 32 at a time (one coalesced 256-byte read of their state
+// words) until it meets one that has published its inclusive prefix, then
+// publishes its own.  Pending predecessors are polled without sleeping
+// (they publish their aggregate as soon as their mask is counted); every
+// wait is bounded: after a.wait_ns the missing predecessors count as zero
+// and GC_ERR_TIMEOUT is recorded.
 __device__ uint64_t walk_back(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
     const bool publish = tile != a.withhold_tile;
     if (tile == 0) return 0;
@@ -120,10 +119,6 @@ __device__ __forceinline__ void publish_aggregate(const MaskArgs& a, int64_t til
         st_state(a.state + tile, (tile == 0 ? kFlagPrefix : kFlagAgg) | agg);
 }
 
-__device__ uint64_t lookback(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
-    publish_aggregate(a, tile, agg, lane);
-    return walk_back(a, tile, agg, lane);
-}
 
 // K6: one CTA per 4096-element tile, tiles taken in launch order from a
 // dynamic counter so every predecessor is already running.  Warp w hashes
@@ -252,18 +247,42 @@ struct AvgArgs {
     int64_t capacity;
 };
 
+// Every received value of entry k is loaded before any model is written
+// (for up to MAXP pairs), so that all of an entry's reads and its 2 * (W/2)
+// scattered writes are in flight together.
+template <int MAXP>
 __global__ void __launch_bounds__(kThreads)
 k_saps_peer_average(const AvgArgs a) {
     const uint64_t cnt = *a.d_count;
     const int64_t count = cnt < static_cast<uint64_t>(a.capacity) ? static_cast<int64_t>(cnt) : a.capacity;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int P = a.W / 2;
     for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < count; k += stride) {
         const uint32_t e = a.idx[k];
-        for (int q = 0; q < a.W / 2; ++q) {
-            const int pa = a.pairs[2 * q], pb = a.pairs[2 * q + 1];
-            const float v = __fmul_rn(__fadd_rn(__ldg(a.vals.p[pa] + k), __ldg(a.vals.p[pb] + k)), 0.5f);
-            a.models.p[pa][e] = v;
-            a.models.p[pb][e] = v;
+        if (MAXP > 0) {
+            float va[MAXP > 0 ? MAXP : 1], vb[MAXP > 0 ? MAXP : 1];
+#pragma unroll
+            for (int q = 0; q < MAXP; ++q) {
+                if (q < P) {
+                    va[q] = __ldg(a.vals.p[a.pairs[2 * q]] + k);
+                    vb[q] = __ldg(a.vals.p[a.pairs[2 * q + 1]] + k);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < MAXP; ++q) {
+                if (q < P) {
+                    const float v = __fmul_rn(__fadd_rn(va[q], vb[q]), 0.5f);
+                    a.models.p[a.pairs[2 * q]][e] = v;
+                    a.models.p[a.pairs[2 * q + 1]][e] = v;
+                }
+            }
+        } else {
+            for (int q = 0; q < P; ++q) {
+                const int pa = a.pairs[2 * q], pb = a.pairs[2 * q + 1];
+                const float v = __fmul_rn(__fadd_rn(__ldg(a.vals.p[pa] + k), __ldg(a.vals.p[pb] + k)), 0.5f);
+                a.models.p[pa][e] = v;
+                a.models.p[pb][e] = v;
+            }
         }
     }
 }
@@ -862,7 +881,11 @@ int saps_peer_average(float* const* models, const float* const* vals, const uint
     if (grid <= 0) return GC_ERR_CUDA;
     const int64_t need = (capacity + kThreads - 1) / kThreads;
     if (need < grid) grid = static_cast<int>(need);
-    k_saps_peer_average<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (W <= 16)
+        k_saps_peer_average<8><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_saps_peer_average<0><<<grid, kThreads, 0, s>>>(a);
     return launch_status();
 }
 
