@@ -339,12 +339,19 @@ template <int ROUNDS, bool FOUR, int NB>
 __global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
 k_qsgd_dequant_sum(const DArgs a) {
     constexpr int WC = (ROUNDS * NB >= 8) ? 2 : 4;    // workers whose loads are issued together
+    // code -> signed level as an exact float: (-1)^sign * level; one table
+    // load replaces the level extraction, its conversion and the sign select
+    constexpr int kCodes = FOUR ? 16 : 256;
+    __shared__ float s_signed_level[kCodes];
+    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) {
+        const float l = static_cast<float>(c & (FOUR ? 7 : 127));
+        s_signed_level[c] = (c & (FOUR ? 8 : 128)) ? -l : l;
+    }
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t b_first = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * NB;
     if (b_first >= a.nbuckets) return;
     constexpr int D = 128 * ROUNDS;
-    constexpr uint32_t kLevelMask = FOUR ? 7u : 127u;
-    constexpr uint32_t kSignBit = FOUR ? 8u : 128u;
 
     float sum[NB][ROUNDS][4];
 #pragma unroll
@@ -383,16 +390,14 @@ k_qsgd_dequant_sum(const DArgs a) {
                 for (int bb = 0; bb < NB; ++bb) {
                     if (b_first + bb >= a.nbuckets) continue;
                     const float u = __fmul_rn(unit[q][bb], a.unit_scale);
-                    const float nu = -u;
 #pragma unroll
                     for (int j = 0; j < ROUNDS; ++j)
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
+                            // (+-level) * unit added with one rounding: the same
+                            // value as level * (+-unit)
                             const uint32_t c = code_of<FOUR>(raw[q][bb][j], k);
-                            // level as an exact float (2^23 + level, minus 2^23); the
-                            // signed unit times the level is added with one rounding
-                            const float lf = __uint_as_float(0x4B000000u | (c & kLevelMask)) - 8388608.0f;
-                            sum[bb][j][k] = __fmaf_rn(lf, (c & kSignBit) ? nu : u, sum[bb][j][k]);
+                            sum[bb][j][k] = __fmaf_rn(s_signed_level[c], u, sum[bb][j][k]);
                         }
                 }
             }
