@@ -126,6 +126,19 @@ def ncu_traffic(kernel: str):
 ISSUE_PEAK = 152 * 4 * 2070e6
 
 
+def dram_roofline(kernel: str, ms_list, peak: float):
+    """DRAM bytes the kernel really moves (committed ncu capture, scaled to the
+    bench launch) over its measured time: the roofline for kernels whose
+    algorithmic bytes are far below their unavoidable traffic (random 4-byte
+    gathers and scatters move whole DRAM sectors or lines)."""
+    d = ncu_entry(kernel)
+    if not d or not ms_list:
+        return None
+    gbps = float(d["bytes_per_launch"]) / (_median(ms_list) * 1e-3) / 1e9
+    return {"bound": "hbm (DRAM bytes moved)", "bytes": int(d["bytes_per_launch"]), "achieved": round(gbps, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(gbps / peak, 3)}
+
+
 def issue_roofline(kernel: str, ms_list):
     d = ncu_entry(kernel)
     if not d or "warp_inst_per_launch" not in d or not ms_list:
@@ -657,11 +670,14 @@ def rows(args, dev, peak):
         K = int(cnt.item())
         assert int(st.item()) == 0
         rm = tm.ms("m")
+        mkey = "saps_mask" if scfg.p >= 0.01 else "saps_mask_p001"
         out[f"{scfg.name}.mask_compact"] = _row(scfg.name, "saps_mask_compact", 4 * K + W * 8 * K, rm, peak, n,
-                                                {"masked": K, "issue": issue_roofline(
-                                                    "saps_mask" if scfg.p >= 0.01 else "saps_mask_p001", rm)})
+                                                {"masked": K, "issue": issue_roofline(mkey, rm),
+                                                 "dram": dram_roofline(mkey, rm, peak)})
         out[f"{scfg.name}.peer_average"] = _row(scfg.name, "saps_peer_average", (W // 2) * 20 * K,
-                                                tm.ms("a"), peak, None)
+                                                tm.ms("a"), peak, None,
+                                                {"dram": dram_roofline("saps_avg", tm.ms("a"), peak)
+                                                 if scfg.p >= 0.01 else None})
         out[f"{scfg.name}.easgd"] = _row(scfg.name, "easgd_step", (2 * W + 2) * 4 * n, tm.ms("e"), peak, W * n)
         out[f"{scfg.name}.average_easgd_fused"] = _row(scfg.name, "saps_average_easgd_step",
                                                        (2 * W + 2) * 4 * n + W * 4 * K + n // 4,
