@@ -370,20 +370,22 @@ k_easgd_wide(const EasgdArgs a) {
 // average of the masked coordinates and the EASGD elastic step.  Each CTA
 // takes a 4096-element tile from the dynamic counter, issues its first
 // round of loads (one float4 of every worker and of the center per thread;
-// four rounds of 1024 elements), hashes all 4096 elements, ranks the masked
-// ones with one block scan and publishes the tile's aggregate at once.  Then
-// it streams the four rounds without further barriers: a masked
-// coordinate's pre-average values go to a shared-memory stash (the
-// compacted output) and to a per-thread scratch row from which each worker
-// reads its partner's value for the pair average; the elastic step and the
-// center update are written back.  Last the CTA walks back for its
-// exclusive prefix -- its predecessors have streamed their tiles by then --
-// and writes idx and vals from the stash.  A tile with more masked
-// coordinates than the stash holds walks back first and writes them
+// the tile is streamed in rounds of 4 x NT elements), hashes all 4096
+// elements, ranks the masked ones with one block scan per pair of rounds and
+// publishes the tile's aggregate at once.  Then it streams the rounds
+// without further barriers: a masked coordinate's pre-average values go to a
+// shared-memory stash (the compacted output) and to a per-thread scratch row
+// from which each worker reads its partner's value for the pair average; the
+// elastic step and the center update are written back.  Last the CTA walks
+// back for its exclusive prefix -- its predecessors have streamed their
+// tiles by then -- and writes idx and vals from the stash.  A tile with more
+// masked coordinates than the stash holds walks back first and writes them
 // directly.  Results equal saps_mask_compact + saps_peer_average +
 // easgd_step bit for bit while the count fits the capacity.
 constexpr int kStash = 384;                      // masked entries kept per tile
-constexpr int kRoundElems = 4 * kThreads;        // elements per round (1024)
+// Threads per CTA of the one-pass round: 256 (two CTAs per SM) measured
+// ahead of 128 (four per SM; 553 against 541 us at p = 0.01).
+constexpr int kRoundThreads = 256;
 
 struct RoundArgs {
     MaskArgs m;                                  // mask, compaction, look-back
@@ -402,14 +404,18 @@ __device__ __forceinline__ void round_load(const RoundArgs& a, int64_t i0, float
     c = ld_f4(a.center + i0);
 }
 
-template <int MAXW>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int MAXW, int NT>
+__global__ void __launch_bounds__(NT, 512 / NT)
 k_saps_round(const RoundArgs a) {
-    constexpr int kRounds = kTileElems / kRoundElems;      // 4
+    constexpr int kRoundN = 4 * NT;                   // elements per round
+    constexpr int kRounds = kTileElems / kRoundN;     // 4 (256 threads) or 8 (128)
+    constexpr int kPairs = kRounds / 2;               // round counts packed two per word
+    constexpr int kNW = NT / 32;
+    static_assert(kRounds * 4 <= 32 && kRounds % 2 == 0, "4 mask bits per round in one word");
     __shared__ float s_stash[kStash * MAXW];
     __shared__ uint32_t s_sidx[kStash];
-    __shared__ float s_scratch[kThreads * MAXW];
-    __shared__ uint32_t s_wsum[2][kWarpsPerBlock];
+    __shared__ float s_scratch[NT * MAXW];
+    __shared__ uint32_t s_wsum[kPairs][kNW];
     __shared__ unsigned long long s_tile;
     __shared__ uint64_t s_excl;
     const MaskArgs& m = a.m;
@@ -428,51 +434,54 @@ k_saps_round(const RoundArgs a) {
     float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
     const int64_t first = base + 4 * threadIdx.x;
     if (first + 4 <= m.n) round_load<MAXW>(a, first, v, c);
-    // the mask of all four rounds: 4 bits per round in `bits`
+    // the mask of every round: 4 bits per round in `bits`
     uint32_t bits = 0;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int64_t i = base + static_cast<int64_t>(r) * kRoundElems + 4 * threadIdx.x + e;
+            const int64_t i = base + static_cast<int64_t>(r) * kRoundN + 4 * threadIdx.x + e;
             bits |= (i < m.n && splitmix64_top24(m.seed_t ^ static_cast<uint64_t>(i)) < m.thr ? 1u : 0u)
                     << (4 * r + e);
         }
     // per-round block scans, two rounds per 32-bit word (16-bit fields)
-    const uint32_t c01 = __popc(bits & 0xFu) | (__popc(bits & 0xF0u) << 16);
-    const uint32_t c23 = __popc(bits & 0xF00u) | (__popc(bits & 0xF000u) << 16);
-    uint32_t i01 = c01, i23 = c23;
+    uint32_t cw[kPairs], iw[kPairs];
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q) {
+        cw[q] = __popc((bits >> (8 * q)) & 0xFu) | (__popc((bits >> (8 * q + 4)) & 0xFu) << 16);
+        iw[q] = cw[q];
+    }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t01 = __shfl_up_sync(0xffffffffu, i01, o);
-        const uint32_t t23 = __shfl_up_sync(0xffffffffu, i23, o);
-        if (lane >= o) {
-            i01 += t01;
-            i23 += t23;
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, iw[q], o);
+            if (lane >= o) iw[q] += t;
         }
     }
     if (lane == 31) {
-        s_wsum[0][wib] = i01;
-        s_wsum[1][wib] = i23;
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) s_wsum[q][wib] = iw[q];
     }
     __syncthreads();
-    uint32_t b01 = 0, b23 = 0, t01 = 0, t23 = 0;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerBlock; ++w) {
-        const uint32_t x01 = s_wsum[0][w], x23 = s_wsum[1][w];
-        b01 += w < wib ? x01 : 0u;
-        b23 += w < wib ? x23 : 0u;
-        t01 += x01;
-        t23 += x23;
-    }
     // exclusive rank of this thread's first masked element in each round
-    const uint32_t tot[kRounds] = {t01 & 0xFFFFu, t01 >> 16, t23 & 0xFFFFu, t23 >> 16};
-    const uint32_t e01 = b01 + i01 - c01, e23 = b23 + i23 - c23;
-    uint32_t rank_base[kRounds] = {e01 & 0xFFFFu, e01 >> 16, e23 & 0xFFFFu, e23 >> 16};
-    rank_base[1] += tot[0];
-    rank_base[2] += tot[0] + tot[1];
-    rank_base[3] += tot[0] + tot[1] + tot[2];
-    const uint32_t agg = tot[0] + tot[1] + tot[2] + tot[3];
+    uint32_t rank_base[kRounds];
+    uint32_t agg = 0;
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q) {
+        uint32_t before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) {
+            const uint32_t x = s_wsum[q][w];
+            before += w < wib ? x : 0u;
+            total += x;
+        }
+        const uint32_t ex = before + iw[q] - cw[q];
+        rank_base[2 * q] = agg + (ex & 0xFFFFu);
+        agg += total & 0xFFFFu;
+        rank_base[2 * q + 1] = agg + (ex >> 16);
+        agg += total >> 16;
+    }
     const bool big = agg > static_cast<uint32_t>(kStash);
     if (wib == 0) {
         publish_aggregate(m, tile, agg, lane);
@@ -486,7 +495,7 @@ k_saps_round(const RoundArgs a) {
 
 #pragma unroll 1
     for (int r = 0; r < kRounds; ++r) {
-        const int64_t i0 = base + static_cast<int64_t>(r) * kRoundElems + 4 * threadIdx.x;
+        const int64_t i0 = base + static_cast<int64_t>(r) * kRoundN + 4 * threadIdx.x;
         if (i0 >= m.n) break;
         const uint32_t rb = (bits >> (4 * r)) & 15u;
         const uint32_t rank0 = rank_base[r];
@@ -586,9 +595,9 @@ k_saps_round(const RoundArgs a) {
     const uint64_t excl = s_excl;
     if (!big) {
         const uint32_t kept = cap > excl ? static_cast<uint32_t>(min(static_cast<uint64_t>(agg), cap - excl)) : 0u;
-        for (uint32_t k = threadIdx.x; k < kept; k += kThreads) m.idx[excl + k] = s_sidx[k];
+        for (uint32_t k = threadIdx.x; k < kept; k += NT) m.idx[excl + k] = s_sidx[k];
         const uint32_t pairs = kept * static_cast<uint32_t>(W);
-        for (uint32_t q = threadIdx.x; q < pairs; q += kThreads) {
+        for (uint32_t q = threadIdx.x; q < pairs; q += NT) {
             const uint32_t w = q / kept;
             const uint32_t k = q - w * kept;
             m.vals.p[w][excl + k] = s_stash[k * MAXW + w];
@@ -1012,9 +1021,9 @@ static int saps_round_impl(int64_t n, double p, uint64_t seed_t, float* const* m
         return GC_ERR_CUDA;
     const unsigned grid = static_cast<unsigned>(m.ntiles);
     if (W <= 4)
-        k_saps_round<4><<<grid, kThreads, 0, s>>>(a);
+        k_saps_round<4, kRoundThreads><<<grid, kRoundThreads, 0, s>>>(a);
     else
-        k_saps_round<16><<<grid, kThreads, 0, s>>>(a);
+        k_saps_round<16, kRoundThreads><<<grid, kRoundThreads, 0, s>>>(a);
     return launch_status();
 }
 
