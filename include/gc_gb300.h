@@ -412,7 +412,9 @@ GC_API int saps_mask_compact(int64_t n, double p, uint64_t seed_t,
  *   v = (vals[a][k] + vals[b][k]) * 0.5;  models[a][idx[k]] = models[b][idx[k]] = v
  *
  *   models     host array of W device pointers, fp32 [n], in/out
- *   vals, idx  as written by saps_mask_compact
+ *   vals, idx  as written by saps_mask_compact; the indices are used as they
+ *              are (the call has no n to check them against), so they must
+ *              come from a compaction over these models
  *   d_count    device uint64 written by saps_mask_compact
  *   pairs      host int [W], a perfect matching of 0..W-1 (saps_matching)
  * Errors: GC_ERR_INVALID (W odd, pairs not a permutation, NULL),
