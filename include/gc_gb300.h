@@ -8,23 +8,28 @@
  *     dequantise-sum fused with an SGD or EASGD update, and CD-SGD's periodic
  *     full-precision correction step;
  *   - QSGD bucketed stochastic quantisation to 4- or 8-bit sign-magnitude
- *     codes, and its dequantise-sum;
+ *     codes, its dequantise-sum, and the lossless Elias-omega coding of the
+ *     codes;
  *   - SAPS seeded random-mask sparsification compacted to (index, value)
  *     pairs, peer averaging over a random perfect matching, and the EASGD
- *     elastic step.
+ *     elastic step;
+ *   - one-pass forms of each method's step (gc_2bit_step, qsgd_step,
+ *     saps_round), bit-identical to the separate calls.
  *
  * Conventions shared by every entry point
  *   Ownership   The caller allocates and owns every buffer.  The library
- *               allocates no memory, holds no state between calls and never
- *               synchronises the device.
+ *               allocates no memory, holds no state between calls (except
+ *               the fixed scratch array of saps_mask_compact_noalloc) and
+ *               never synchronises the device.
  *   Execution   Each call validates its arguments on the host, enqueues its
  *               kernels on `stream` (a cudaStream_t; NULL is the legacy
  *               default stream) and returns.  Results are valid once the
  *               stream reaches that point.
  *   Status      The return value is GC_OK or a negative GC_ERR_* code from
  *               host validation, or GC_ERR_CUDA when a launch failed.  Errors
- *               found on the device (compaction capacity, look-back timeout)
- *               are written to the caller's device int `d_status`.
+ *               found on the device (compaction capacity, look-back timeout,
+ *               a coded stream that does not decode) are written to the
+ *               caller's device int `d_status`.
  *   Pointers    "device" pointers are CUDA device memory of the current
  *               device; pointer arrays (const float* const* ...) are HOST
  *               arrays of device pointers, read during the call only.
