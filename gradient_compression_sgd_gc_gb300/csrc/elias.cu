@@ -377,17 +377,20 @@ struct EncodeArgs {
 };
 
 // The stream bits of 16 code bytes (table entries e[]) OR-ed into the
-// staging words from bit position `start`: a 64-bit shift register (hi:lo)
-// collects the bits and hands over every completed word.
+// staging words from bit position `start`: the entries are joined two at a
+// time (at most 16 + 16 bits), and a 64-bit shift register (hi:lo) collects
+// the pairs and hands over every completed word (at most one per pair).
 __device__ __forceinline__ void emit_piece(uint32_t* stage, uint32_t start, const uint32_t (&e)[16]) {
     uint32_t wi = start >> 5;
     int nacc = static_cast<int>(start & 31u);
     uint32_t hi = 0u, lo = 0u;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int l = static_cast<int>(e[j] & 31u);
-        hi = __funnelshift_l(lo, hi, l);
-        lo = (lo << l) | (e[j] >> 5);
+    for (int j = 0; j < 16; j += 2) {
+        const int l1 = static_cast<int>(e[j + 1] & 31u);
+        const int l = static_cast<int>(e[j] & 31u) + l1;                 // <= 32
+        const uint32_t pat = ((e[j] >> 5) << l1) | (e[j + 1] >> 5);
+        hi = __funnelshift_lc(lo, hi, l);
+        lo = __funnelshift_lc(0u, lo, l) | pat;
         nacc += l;
         if (nacc >= 32) {
             atomicOr(stage + wi, __funnelshift_r(lo, hi, nacc - 32));
