@@ -449,7 +449,8 @@ def _median(xs):
 
 def _row(name, kernel, bytes_per_launch, ms_list, peak, unit_elems=None, extra=None):
     ms = _median(ms_list)
-    d = {"kernel": kernel, "ms": round(ms, 5), "bytes": int(bytes_per_launch),
+    d = {"kernel": kernel, "ms": round(ms, 5), "ms_min": round(min(ms_list), 5), "reps": len(ms_list),
+         "bytes": int(bytes_per_launch),
          "GBps": round(bytes_per_launch / (ms * 1e-3) / 1e9, 1),
          "frac": round(bytes_per_launch / (ms * 1e-3) / 1e9 / peak, 3)}
     if unit_elems:
