@@ -1,0 +1,125 @@
+"""Key-value style gradient compression on top of the C ABI.
+
+"2bit gradient compression" (MXNet PR #8662), sections "Usage" and "Backend
+API": the user sets the compression once as a dict of parameters,
+``{'type': '2bit', 'threshold': t}``; the threshold has no default; every
+gradient (one per key) carries its own residual; the receiver dequantises
+every worker's codes and averages them.  Switching compression off after it
+was on is an error; changing the threshold is allowed, and codes produced
+with the old threshold are then decoded with the new one (the page warns of
+that transient).
+
+This module keeps the per-key residuals and code buffers as device tensors
+and calls the library for all arithmetic; it holds no fallback.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import (GC_UPD_EASGD, GC_UPD_NONE, GC_UPD_SGD, code_words, gc_2bit_dequant_sum_update,
+               gc_2bit_quantize, gc_2bit_step)
+
+__all__ = ["GradientCompression"]
+
+_TYPES = ("none", "2bit")
+
+
+def _check_params(params) -> dict:
+    if not isinstance(params, dict):
+        raise TypeError("compression params must be a dict such as {'type': '2bit', 'threshold': 0.5}")
+    unknown = set(params) - {"type", "threshold"}
+    if unknown:
+        raise ValueError(f"unknown compression parameters: {sorted(unknown)}")
+    kind = params.get("type")
+    if kind not in _TYPES:
+        raise ValueError(f"compression type must be one of {_TYPES}, got {kind!r}")
+    if kind == "2bit":
+        if "threshold" not in params:
+            raise ValueError("2bit compression needs a threshold (there is no default)")
+        t = float(params["threshold"])
+        if not (math.isfinite(t) and t > 0.0):
+            raise ValueError(f"threshold must be finite and positive, got {params['threshold']!r}")
+        return {"type": "2bit", "threshold": t}
+    if "threshold" in params:
+        raise ValueError("'none' compression takes no threshold")
+    return {"type": "none"}
+
+
+class GradientCompression:
+    """Per-key 2-bit compression state: residuals and codes on the device."""
+
+    def __init__(self, params):
+        self._params = _check_params(params)
+        self._residual: dict = {}
+        self._codes: dict = {}
+        self._used = False
+
+    @property
+    def params(self) -> dict:
+        return dict(self._params)
+
+    @property
+    def threshold(self) -> float | None:
+        return self._params.get("threshold")
+
+    def set_params(self, params) -> None:
+        """Re-configure.  Turning compression off once it has compressed a
+        gradient raises; a new threshold applies from the next call."""
+        new = _check_params(params)
+        if self._used and self._params["type"] == "2bit" and new["type"] == "none":
+            raise ValueError("compression cannot be switched off after it has been used")
+        self._params = new
+
+    def _state(self, key, grad: torch.Tensor):
+        n = grad.numel()
+        r = self._residual.get(key)
+        if r is None or r.numel() != n or r.device != grad.device:
+            r = torch.zeros(n, dtype=torch.float32, device=grad.device)
+            self._residual[key] = r
+            self._codes[key] = torch.empty(code_words(n), dtype=torch.int32, device=grad.device)
+        return r, self._codes[key]
+
+    def residual(self, key) -> torch.Tensor | None:
+        return self._residual.get(key)
+
+    def compress(self, key, grad: torch.Tensor) -> torch.Tensor:
+        """The packed codes of ``grad`` (fp32 or bf16), the key's residual
+        carried over; for 'none' the gradient itself, untouched."""
+        if self._params["type"] == "none":
+            return grad
+        r, c = self._state(key, grad)
+        gc_2bit_quantize(grad.reshape(-1), r, c, self._params["threshold"])
+        self._used = True
+        return c
+
+    def decompress(self, codes, n: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        """The average of the workers' dequantised codes (one code buffer per
+        worker), as the receiver forms it.  With 'none' there is nothing to
+        decode: the caller reduces the uncompressed gradients itself."""
+        if self._params["type"] == "none":
+            raise ValueError("no compression configured: reduce the uncompressed gradients directly")
+        out = out if out is not None else torch.empty(n, dtype=torch.float32, device=codes[0].device)
+        gc_2bit_dequant_sum_update(list(codes), n, self._params["threshold"], GC_UPD_NONE, out=out)
+        return out
+
+    def apply(self, codes, weights: torch.Tensor, lr: float, alpha: float = 0.0,
+              center: torch.Tensor | None = None) -> None:
+        """weights -= lr * (average of the dequantised codes), and the EASGD
+        elastic term when ``center`` is given (2bit only)."""
+        if self._params["type"] != "2bit":
+            raise ValueError("apply() needs 2bit compression")
+        kind = GC_UPD_EASGD if center is not None else GC_UPD_SGD
+        gc_2bit_dequant_sum_update(list(codes), weights.numel(), self._params["threshold"], kind, lr=lr,
+                                   alpha=alpha, center=center, weights=weights)
+
+    def step(self, keys, grads, weights: torch.Tensor, lr: float) -> None:
+        """Every worker's compression (one key per worker) and the averaged
+        SGD update in one pass over the data (fp32 gradients of one size)."""
+        if self._params["type"] != "2bit":
+            raise ValueError("step() needs 2bit compression")
+        res, codes = zip(*[self._state(k, g) for k, g in zip(keys, grads)])
+        gc_2bit_step([g.reshape(-1) for g in grads], list(res), list(codes), self._params["threshold"],
+                     GC_UPD_SGD, lr=lr, weights=weights)
+        self._used = True

@@ -1,0 +1,71 @@
+"""The key-value compression front end: parameter rules of "2bit gradient
+compression" (MXNet PR #8662, "Usage": a dict {'type', 'threshold'}; no
+default threshold; switching compression off after use is an error) on the
+host, and on the GPU its calls against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gradient_compression_sgd_gc_gb300.compression import GradientCompression
+import gradient_compression_sgd_gc_gb300 as gc
+from gradient_compression_sgd_gc_gb300 import workloads as wl
+import oracle
+
+
+def test_params_rules():
+    with pytest.raises(ValueError):
+        GradientCompression({"type": "2bit"})                      # no default threshold
+    with pytest.raises(ValueError):
+        GradientCompression({"type": "2bit", "threshold": 0.0})
+    with pytest.raises(ValueError):
+        GradientCompression({"type": "2bit", "threshold": float("nan")})
+    with pytest.raises(ValueError):
+        GradientCompression({"type": "1bit", "threshold": 0.5})
+    with pytest.raises(ValueError):
+        GradientCompression({"type": "2bit", "threshold": 0.5, "bits": 2})
+    with pytest.raises(TypeError):
+        GradientCompression("2bit")
+    c = GradientCompression({"type": "2bit", "threshold": 0.5})
+    assert c.params == {"type": "2bit", "threshold": 0.5}
+    c.set_params({"type": "2bit", "threshold": 0.25})             # allowed at any time
+    assert c.threshold == 0.25
+    c.set_params({"type": "none"})                                 # never used yet: allowed
+    assert c.params == {"type": "none"}
+    g = torch.ones(3)
+    assert c.compress("w", g) is g                                 # untouched
+    with pytest.raises(ValueError):
+        c.decompress([g], 3)
+
+
+@pytest.mark.gpu
+def test_keys_against_oracle_and_no_switch_off_after_use():
+    dev = "cuda"
+    n, W, t, lr = 70_001, 3, 2e-3, 0.1
+    comp = GradientCompression({"type": "2bit", "threshold": t})
+    grads = [wl.normal(n, 1e-3, 300 + w, device=dev) for w in range(W)]
+    codes = [comp.compress(("layer0", w), grads[w]) for w in range(W)]
+    avg = comp.decompress(codes, n)
+    weights = wl.uniform(n, 0.05, 3, device=dev)
+    w_ref = weights.cpu().numpy().astype(np.float64)
+    comp.apply(codes, weights, lr)
+    torch.cuda.synchronize()
+    r_ref = [np.zeros(n, np.float32) for _ in range(W)]
+    c_ref = [oracle.twobit_quantize(grads[w].cpu().numpy(), r_ref[w], t) for w in range(W)]
+    for w in range(W):
+        np.testing.assert_array_equal(codes[w].cpu().numpy().view(np.uint32), c_ref[w])
+        np.testing.assert_array_equal(comp.residual(("layer0", w)).cpu().numpy().view(np.uint32),
+                                      r_ref[w].view(np.uint32))
+    a_ref = oracle.twobit_dequant_sum_update(c_ref, n, t, oracle.KIND_NONE)
+    np.testing.assert_allclose(avg.cpu().numpy(), a_ref, rtol=0, atol=1e-5 * t)
+    oracle.twobit_dequant_sum_update(c_ref, n, t, oracle.KIND_SGD, lr=lr, weights=w_ref)
+    np.testing.assert_allclose(weights.cpu().numpy(), w_ref, rtol=1e-5, atol=1e-5 * lr * t)
+    with pytest.raises(ValueError):
+        comp.set_params({"type": "none"})
+    # the fused step keeps the same per-key residuals
+    weights2 = wl.uniform(n, 0.05, 4, device=dev)
+    comp.step([("layer0", w) for w in range(W)], grads, weights2, lr)
+    torch.cuda.synchronize()
+    c2 = [oracle.twobit_quantize(grads[w].cpu().numpy(), r_ref[w], t) for w in range(W)]
+    for w in range(W):
+        np.testing.assert_array_equal(comp.residual(("layer0", w)).cpu().numpy().view(np.uint32),
+                                      r_ref[w].view(np.uint32))
