@@ -21,7 +21,7 @@ import torch
 from . import (GC_UPD_EASGD, GC_UPD_NONE, GC_UPD_SGD, code_words, gc_2bit_dequant_sum_update,
                gc_2bit_quantize, gc_2bit_step)
 
-__all__ = ["GradientCompression"]
+__all__ = ["GradientCompression", "QSGD", "SAPSGossip"]
 
 _TYPES = ("none", "2bit")
 
@@ -123,3 +123,81 @@ class GradientCompression:
         gc_2bit_step([g.reshape(-1) for g in grads], list(res), list(codes), self._params["threshold"],
                      GC_UPD_SGD, lr=lr, weights=weights)
         self._used = True
+
+
+class QSGD:
+    """QSGD for W workers held on this GPU ("QSGD: Communication-Efficient SGD
+    via Gradient Quantization and Encoding", Knowl 1-3 and 8): bucketed
+    stochastic quantisation with s levels (4-bit codes for s <= 7, else
+    8-bit), optional max-norm scaling, the average of the decoded messages,
+    and the Elias-omega stream of a worker's message (Knowl 2)."""
+
+    def __init__(self, n: int, workers: int, bucket: int = 512, s: int = 7, seed: int = 0,
+                 maxnorm: bool = False, device="cuda"):
+        from . import qsgd_code_bytes, qsgd_num_buckets
+        if not (1 <= s <= 127) or bucket not in (128, 256, 512, 1024, 2048) or workers < 1:
+            raise ValueError("need 1 <= s <= 127, bucket in {128, ..., 2048} and at least one worker")
+        self.n, self.W, self.bucket, self.s, self.seed, self.maxnorm = n, workers, bucket, s, seed, maxnorm
+        nb, cb = qsgd_num_buckets(n, bucket), qsgd_code_bytes(n, s)
+        self.norms = [torch.empty(nb, dtype=torch.float32, device=device) for _ in range(workers)]
+        self.codes = [torch.empty(cb, dtype=torch.uint8, device=device) for _ in range(workers)]
+
+    def step(self, grads, out: torch.Tensor) -> torch.Tensor:
+        """Every worker's message (worker w quantises grads[w] with its own
+        draws) and their average into ``out``, in one pass."""
+        from . import qsgd_step
+        if len(grads) != self.W:
+            raise ValueError(f"expected {self.W} gradients")
+        qsgd_step(list(grads), self.bucket, self.s, self.seed, self.norms, self.codes, 1.0 / self.W, out,
+                  maxnorm=self.maxnorm)
+        return out
+
+    def encode(self, worker: int):
+        """The Elias-omega stream of a worker's last message: (words, offsets),
+        offsets[-1] being its length in 32-bit words."""
+        from . import qsgd_elias_encode, qsgd_elias_max_words, qsgd_elias_workspace_bytes, qsgd_num_buckets
+        dev = self.codes[worker].device
+        words = torch.empty(qsgd_elias_max_words(self.n, self.bucket, self.s), dtype=torch.int32, device=dev)
+        offsets = torch.empty(qsgd_num_buckets(self.n, self.bucket) + 1, dtype=torch.int32, device=dev)
+        ws = torch.empty(max(16, qsgd_elias_workspace_bytes(self.n, self.bucket)), dtype=torch.uint8, device=dev)
+        qsgd_elias_encode(self.codes[worker], self.norms[worker], self.n, self.bucket, self.s, words, offsets, ws)
+        return words, offsets
+
+    def decode(self, words: torch.Tensor, offsets: torch.Tensor, worker: int) -> None:
+        """Replace a worker's message by the decoded stream."""
+        from . import qsgd_elias_decode
+        qsgd_elias_decode(words, offsets, self.n, self.bucket, self.s, self.codes[worker], self.norms[worker])
+
+
+class SAPSGossip:
+    """SAPS rounds for W workers held on this GPU ("Communication-Efficient
+    Decentralized Learning with Sparsification and Adaptive Peer Selection",
+    section II, with the EASGD elastic step): round t draws its shared seed
+    from the base seed, the seeded perfect matching, the Bernoulli(p) mask,
+    the compacted (index, value) messages, the pair averages and the elastic
+    step -- one pass over the models."""
+
+    def __init__(self, models, center: torch.Tensor, p: float, alpha: float, beta: float,
+                 base_seed: int = 0, capacity: int | None = None):
+        from . import saps_workspace_bytes
+        self.models, self.center = list(models), center
+        self.W, self.n = len(self.models), center.numel()
+        if self.W < 2 or self.W % 2:
+            raise ValueError("SAPS pairs the workers: W must be even")
+        self.p, self.alpha, self.beta, self.base_seed = p, alpha, beta, base_seed
+        dev = center.device
+        cap = capacity if capacity is not None else self.n
+        self.idx = torch.empty(cap, dtype=torch.int32, device=dev)
+        self.vals = [torch.empty(cap, dtype=torch.float32, device=dev) for _ in range(self.W)]
+        self.count = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = torch.empty(saps_workspace_bytes(self.n), dtype=torch.uint8, device=dev)
+
+    def round(self, t: int):
+        """Run round t; returns its matching (host list)."""
+        from . import saps_matching, saps_round, saps_round_seed
+        seed_t = saps_round_seed(self.base_seed, t)
+        pairs = saps_matching(seed_t, self.W)
+        saps_round(self.n, self.p, seed_t, self.models, pairs, self.alpha, self.beta, self.center, self.idx,
+                   self.vals, self.count, self.workspace, self.status)
+        return pairs

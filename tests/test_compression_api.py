@@ -69,3 +69,57 @@ def test_keys_against_oracle_and_no_switch_off_after_use():
     for w in range(W):
         np.testing.assert_array_equal(comp.residual(("layer0", w)).cpu().numpy().view(np.uint32),
                                       r_ref[w].view(np.uint32))
+
+
+@pytest.mark.gpu
+def test_qsgd_front_end_round_trip():
+    from gradient_compression_sgd_gc_gb300.compression import QSGD
+    dev = "cuda"
+    n, W = 100_003, 3
+    q = QSGD(n, W, bucket=512, s=22, seed=5)
+    cfg = wl.scaled(wl.QSGD_S127, n)
+    grads = [wl.qsgd_grad(cfg, w, device=dev) for w in range(W)]
+    out = torch.empty(n, device=dev)
+    q.step(grads, out)
+    n1 = [x.clone() for x in q.norms]
+    c1 = [x.clone() for x in q.codes]
+    words, offsets = q.encode(1)
+    q.codes[1].zero_()
+    q.norms[1].zero_()
+    q.decode(words, offsets, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(q.norms[1], n1[1])
+    lv = lambda c: c & 127
+    assert torch.equal(lv(q.codes[1]), lv(c1[1]))
+    ref = torch.empty(n, device=dev)
+    gc.qsgd_dequant_sum(c1, n1, n, 512, 22, 1.0 / W, ref)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.gpu
+def test_saps_front_end_rounds_equal_the_calls():
+    from gradient_compression_sgd_gc_gb300.compression import SAPSGossip
+    dev = "cuda"
+    n, W, p = 60_001, 4, 0.01
+    base = [wl.normal(n, 0.05, 70 + w, device=dev) for w in range(W)]
+    c0 = wl.saps_initial_center(base)
+    ga = SAPSGossip([b.clone() for b in base], c0.clone(), p, 0.9, 0.9, base_seed=11)
+    mb, cb = [b.clone() for b in base], c0.clone()
+    idx = torch.empty(n, dtype=torch.int32, device=dev)
+    vals = [torch.empty(n, device=dev) for _ in range(W)]
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    for t in range(3):
+        pairs = ga.round(t)
+        seed_t = gc.saps_round_seed(11, t)
+        assert pairs == gc.saps_matching(seed_t, W)
+        gc.saps_mask_compact(n, p, seed_t, mb, idx, vals, cnt, ws, st)
+        gc.saps_peer_average(mb, vals, idx, cnt, pairs)
+        gc.easgd_step(mb, 0.9, 0.9, cb)
+    torch.cuda.synchronize()
+    for w in range(W):
+        assert torch.equal(ga.models[w], mb[w])
+    assert torch.equal(ga.center, cb)
+    assert int(ga.status.item()) == 0
