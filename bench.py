@@ -305,12 +305,13 @@ def headline(args, dev, rank, world, pg):
             "launches": args.steps * 2, "n": n, "W": W}
 
 
-def e2e(args, dev):
+def e2e(args, dev, pg=None, world: int = 1):
     """Same metric through the public API with host buffers: every step copies
     the 8 gradients from pinned host memory, runs the path, and reads the 8
     packed code buffers back.  Uploads run on a copy stream so that worker
     w+1's upload overlaps worker w's quantisation; events order each kernel
-    after its own upload."""
+    after its own upload.  Every rank runs it (each GPU has its own host
+    link); the slowest rank's time sets the whole-job value."""
     import torch
     import gradient_compression_sgd_gc_gb300 as gc
     from gradient_compression_sgd_gc_gb300 import workloads as wl
@@ -354,6 +355,7 @@ def e2e(args, dev):
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
+    barrier(pg, dev)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -363,10 +365,11 @@ def e2e(args, dev):
         step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / args.e2e_steps
+    barrier(pg, dev)
+    ms = max_over_ranks(pg, a.elapsed_time(b) / args.e2e_steps, dev)
     h2d = W * n * 4
     d2h = W * gc.code_words(n) * 4
-    return {"value": round(W * n * 4 / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(world * W * n * 4 / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
             "h2d_GBps": round(h2d / (ms * 1e-3) / 1e9, 1)}
 
@@ -1019,8 +1022,9 @@ def main():
         "gpu_launches": h["launches"],
         "clocks": h["clocks"],
     }
+    e2e_line = e2e(args, dev, pg, world)
     if rank == 0:
-        line["e2e"] = e2e(args, dev)
+        line["e2e"] = e2e_line
         if world == 1 and not args.no_rows:
             line["rows"] = rows(args, dev, peak)
         if world == 1 and not args.no_cpu:
