@@ -223,3 +223,40 @@ def test_testing_hook_validates_its_wait_bound():
     for bad in (0, 2_000_000_000):
         assert _call(f, 1000, 0.01, 5, p1, 1, FAKE, p1, 100, FAKE, FAKE, ws, FAKE, 3, bad,
                      None) == gc.GC_ERR_INVALID
+
+
+def test_one_pass_entry_validation():
+    f = "qsgd_step"
+    g3 = _ptrs(FAKE, FAKE, FAKE)
+    assert _call(f, g3, 3, 1000, 500, 7, 1, 0, g3, g3, 1.0, FAKE, None) == gc.GC_ERR_INVALID    # bucket
+    assert _call(f, g3, 3, 1000, 512, 0, 1, 0, g3, g3, 1.0, FAKE, None) == gc.GC_ERR_INVALID    # s
+    assert _call(f, g3, 3, 1000, 512, 7, 1, 2, g3, g3, 1.0, FAKE, None) == gc.GC_ERR_INVALID    # maxnorm flag
+    assert _call(f, g3, 0, 1000, 512, 7, 1, 0, g3, g3, 1.0, FAKE, None) == gc.GC_ERR_INVALID    # W
+    assert _call(f, g3, 3, 1000, 512, 7, 1, 0, g3, g3, float("inf"), FAKE, None) == gc.GC_ERR_INVALID
+    assert _call(f, g3, 3, 1000, 512, 7, 1, 0, g3, g3, 1.0, MISALIGNED, None) == gc.GC_ERR_ALIGN
+    assert _call(f, _ptrs(FAKE, MISALIGNED, FAKE), 3, 1000, 512, 7, 1, 0, g3, g3, 1.0, FAKE, None) == gc.GC_ERR_ALIGN
+    assert _call(f, g3, 3, 0, 512, 7, 1, 0, g3, g3, 1.0, FAKE, None) == gc.GC_OK               # n == 0
+    r = "saps_round"
+    ws = gc.saps_workspace_bytes(1000)
+    m4, v4 = _ptrs(FAKE, FAKE, FAKE, FAKE), _ptrs(FAKE, FAKE, FAKE, FAKE)
+    pairs = (ctypes.c_int * 4)(0, 1, 2, 3)
+    bad_pairs = (ctypes.c_int * 4)(0, 0, 2, 3)
+    ok_args = dict(n=1000, p=0.01, seed=1, models=m4, W=4, pairs=pairs, alpha=0.9, beta=0.9, center=FAKE,
+                   idx=FAKE, vals=v4, cap=1000, cnt=FAKE, ws=FAKE, wsb=ws, st=FAKE)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return _call(r, a["n"], a["p"], a["seed"], a["models"], a["W"], a["pairs"], a["alpha"], a["beta"],
+                     a["center"], a["idx"], a["vals"], a["cap"], a["cnt"], a["ws"], a["wsb"], a["st"], None)
+
+    assert call(W=3) == gc.GC_ERR_INVALID
+    assert call(pairs=bad_pairs) == gc.GC_ERR_INVALID
+    assert call(p=0.0) == gc.GC_ERR_INVALID
+    assert call(p=1.5) == gc.GC_ERR_INVALID
+    assert call(alpha=float("nan")) == gc.GC_ERR_INVALID
+    assert call(wsb=ws - 1) == gc.GC_ERR_INVALID
+    assert call(st=None) == gc.GC_ERR_INVALID
+    assert call(n=1 << 33) == gc.GC_ERR_INVALID
+    assert call(center=MISALIGNED) == gc.GC_ERR_ALIGN
+    assert call(models=_ptrs(FAKE, MISALIGNED, FAKE, FAKE)) == gc.GC_ERR_ALIGN
+
