@@ -34,6 +34,22 @@ inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
+// Launches `kernel` (kThreads threads per CTA, no dynamic shared memory) on
+// as many CTAs as are resident on the current device at once, at most
+// `want`: the kernel strides over its work.
+template <typename Args>
+int launch_persistent(void (*kernel)(Args), int64_t want, cudaStream_t s, const Args& a) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess)
+        return GC_ERR_CUDA;
+    const int64_t resident = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    const int64_t grid = want < resident ? (want > 0 ? want : 1) : resident;
+    kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(a);
+    return launch_status();
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline bool finite_pos(float x) { return isfinite(x) && x > 0.0f; }

@@ -330,27 +330,15 @@ __device__ __forceinline__ uint32_t code_of(uint32_t raw, int k) {
     return (raw >> (8 * k)) & 255u;
 }
 
-// One warp per NB consecutive buckets (NB = 1 in use: a second bucket per
-// warp measured slower).  Workers are taken WC at a time with every code and
-// norm load of the group issued before any is decoded; each element's sum
-// runs in worker order, every term added by one fma of the level with the
-// signed unit norm * (scale / s).
+// NB consecutive buckets by one warp (NB = 1 in use: a second bucket per warp
+// measured slower).  Workers are taken WC at a time with every code and norm
+// load of the group issued before any is decoded; each element's sum runs in
+// worker order, every term added by one fma of the level with the signed unit
+// norm * (scale / s).
 template <int ROUNDS, bool FOUR, int NB>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
-k_qsgd_dequant_sum(const DArgs a) {
+__device__ __forceinline__ void dequant_buckets(const DArgs& a, int64_t b_first, int lane,
+                                                const float* s_signed_level) {
     constexpr int WC = (ROUNDS * NB >= 8) ? 2 : 4;    // workers whose loads are issued together
-    // code -> signed level as an exact float: (-1)^sign * level; one table
-    // load replaces the level extraction, its conversion and the sign select
-    constexpr int kCodes = FOUR ? 16 : 256;
-    __shared__ float s_signed_level[kCodes];
-    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) {
-        const float l = static_cast<float>(c & (FOUR ? 7 : 127));
-        s_signed_level[c] = (c & (FOUR ? 8 : 128)) ? -l : l;
-    }
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int64_t b_first = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * NB;
-    if (b_first >= a.nbuckets) return;
     constexpr int D = 128 * ROUNDS;
 
     float sum[NB][ROUNDS][4];
@@ -423,6 +411,28 @@ k_qsgd_dequant_sum(const DArgs a) {
     }
 }
 
+// Persistent grid (as many CTAs as fit on the GPU at once): each warp strides
+// over the buckets, so a CTA builds its code table once rather than once per
+// 8 buckets (measured 8-15% faster than one CTA per 8 buckets).
+template <int ROUNDS, bool FOUR, int NB>
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+k_qsgd_dequant_sum(const DArgs a) {
+    // code -> signed level as an exact float: (-1)^sign * level; one table
+    // load replaces the level extraction, its conversion and the sign select
+    constexpr int kCodes = FOUR ? 16 : 256;
+    __shared__ float s_signed_level[kCodes];
+    for (int c = threadIdx.x; c < kCodes; c += blockDim.x) {
+        const float l = static_cast<float>(c & (FOUR ? 7 : 127));
+        s_signed_level[c] = (c & (FOUR ? 8 : 128)) ? -l : l;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = ((static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) * NB;
+    for (int64_t b_first = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * NB;
+         b_first < a.nbuckets; b_first += stride)
+        dequant_buckets<ROUNDS, FOUR, NB>(a, b_first, lane, s_signed_level);
+}
+
 template <bool FOUR, bool MAXNORM>
 int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
     switch (rounds) {
@@ -451,13 +461,13 @@ int launch_step(int rounds, const StepArgs& a, unsigned grid, cudaStream_t s) {
 
 template <bool FOUR>
 int launch_dequant(int rounds, const DArgs& a, cudaStream_t s) {
-    const unsigned g1 = blocks_for_tiles(a.nbuckets);
+    const int64_t want = blocks_for_tiles(a.nbuckets);
     switch (rounds) {
-        case 1: k_qsgd_dequant_sum<1, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
-        case 2: k_qsgd_dequant_sum<2, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
-        case 4: k_qsgd_dequant_sum<4, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
-        case 8: k_qsgd_dequant_sum<8, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
-        case 16: k_qsgd_dequant_sum<16, FOUR, 1><<<g1, kThreads, 0, s>>>(a); break;
+        case 1: return launch_persistent(k_qsgd_dequant_sum<1, FOUR, 1>, want, s, a);
+        case 2: return launch_persistent(k_qsgd_dequant_sum<2, FOUR, 1>, want, s, a);
+        case 4: return launch_persistent(k_qsgd_dequant_sum<4, FOUR, 1>, want, s, a);
+        case 8: return launch_persistent(k_qsgd_dequant_sum<8, FOUR, 1>, want, s, a);
+        case 16: return launch_persistent(k_qsgd_dequant_sum<16, FOUR, 1>, want, s, a);
         default: return GC_ERR_INVALID;
     }
     return launch_status();

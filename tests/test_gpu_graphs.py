@@ -57,7 +57,7 @@ def test_twobit_steps_in_a_graph():
     _replay_equals_eager(make, run)
 
 
-def test_qsgd_step_and_elias_in_a_graph():
+def test_qsgd_step_elias_and_dequant_in_a_graph():
     n, W, d, s = 70_001, 3, 512, 127
     cfg = wl.scaled(wl.QSGD_S127, n)
     vs = [wl.qsgd_grad(cfg, w, device=DEV) for w in range(W)]
@@ -70,14 +70,16 @@ def test_qsgd_step_and_elias_in_a_graph():
                 + [torch.zeros(n, device=DEV), torch.zeros(cap, dtype=torch.int32, device=DEV),
                    torch.zeros(nb + 1, dtype=torch.int32, device=DEV),
                    torch.zeros(gc.qsgd_elias_workspace_bytes(n, d), dtype=torch.uint8, device=DEV),
-                   torch.zeros(cb, dtype=torch.uint8, device=DEV), torch.zeros(nb, device=DEV)])
+                   torch.zeros(cb, dtype=torch.uint8, device=DEV), torch.zeros(nb, device=DEV),
+                   torch.zeros(n, device=DEV)])
 
     def run(st):
         norms, codes = st[:W], st[W:2 * W]
-        out, words, offs, ws, dc, dn = st[2 * W:]
+        out, words, offs, ws, dc, dn, total = st[2 * W:]
         gc.qsgd_step(vs, d, s, 9, norms, codes, 1.0 / W, out)
         gc.qsgd_elias_encode(codes[0], norms[0], n, d, s, words, offs, ws)
         gc.qsgd_elias_decode(words, offs, n, d, s, dc, dn)
+        gc.qsgd_dequant_sum(codes, norms, n, d, s, 1.0, total)
 
     _replay_equals_eager(make, run)
 
