@@ -22,7 +22,6 @@ constexpr int kItems = 16;                         // rounds of 32 elements per 
 constexpr int kWarpSpan = 32 * kItems;             // 512 elements per warp
 constexpr int kTileElems = kWarpsPerBlock * kWarpSpan;   // 4096 elements per CTA tile
 constexpr size_t kWsHeader = 64;                   // tile counter + padding
-constexpr int kGatherStash = 512;                  // gathered values staged per tile (entries x W)
 
 constexpr uint64_t kFlagAgg = 1ull << 62;
 constexpr uint64_t kFlagPrefix = 2ull << 62;
@@ -119,120 +118,197 @@ __device__ __forceinline__ void publish_aggregate(const MaskArgs& a, int64_t til
         st_state(a.state + tile, (tile == 0 ? kFlagPrefix : kFlagAgg) | agg);
 }
 
+constexpr int kListCap = 1024;                // masked indices kept for a tile's deferred write
+constexpr int kGroups = kTileElems / 32;      // 32-element groups per tile
 
-// K6: one CTA per 4096-element tile, tiles taken in launch order from a
-// dynamic counter so every predecessor is already running.  Warp w hashes
-// elements tile*4096 + 512w + 32r + lane (r < 16) and keeps the ballot of
-// round r in lane r.  After the scan the CTA lists its masked indices in
-// shared memory and writes idx[] and every worker's vals[] with coalesced
-// stores.  When the workspace has room it also records, per 32 elements,
-// the mask bits and the number of masked entries before them, which the
-// fused pair-average + elastic step uses to find each entry's rank.
-__global__ void __launch_bounds__(kThreads)
-k_saps_mask_compact(const MaskArgs a) {
-    __shared__ uint32_t s_list[kTileElems];
-    __shared__ float s_vals[kGatherStash];
-    __shared__ uint32_t s_warp_excl[kWarpsPerBlock];
-    __shared__ uint32_t s_warp_tot[kWarpsPerBlock];
-    __shared__ unsigned long long s_tile;
-    __shared__ uint64_t s_excl;
-    __shared__ uint32_t s_agg;
+struct TileStage {
+    uint32_t gmask[kGroups];    // mask bits of each group
+    uint32_t gex[kGroups];      // masked entries of the tile before each group
+    int64_t tile;
+    uint32_t agg;               // masked entries of the tile
+};
 
-    const int lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
-    if (threadIdx.x == 0) s_tile = atomicAdd(a.counter, 1ull);
-    __syncthreads();
-    const int64_t tile = static_cast<int64_t>(s_tile);
-    const int64_t wbase = tile * kTileElems + static_cast<int64_t>(wib) * kWarpSpan;
-
+template <bool CHECK>
+__device__ __forceinline__ uint32_t hash_rounds(const MaskArgs& a, int64_t wbase, int lane) {
     uint32_t my_mask = 0;
 #pragma unroll 4
     for (int r = 0; r < kItems; ++r) {
         const int64_t e = wbase + 32 * r + lane;
-        const bool hit = e < a.n && splitmix64_top24(a.seed_t ^ static_cast<uint64_t>(e)) < a.thr;
+        bool hit = splitmix64_top24(a.seed_t ^ static_cast<uint64_t>(e)) < a.thr;
+        if (CHECK) hit = hit && e < a.n;
         const uint32_t m = __ballot_sync(0xffffffffu, hit);
         if (lane == r) my_mask = m;
     }
-    const uint32_t cnt = __popc(my_mask);
-    uint32_t incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    const uint32_t round_excl = incl - cnt;
-    if (lane == 31) s_warp_tot[wib] = incl;
-    __syncthreads();
+    return my_mask;
+}
 
-    if (wib == 0) {
-        const uint32_t v = lane < kWarpsPerBlock ? s_warp_tot[lane] : 0u;
-        uint32_t vi = v;
-#pragma unroll
-        for (int o = 1; o < kWarpsPerBlock; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, vi, o);
-            if (lane >= o) vi += t;
-        }
-        if (lane < kWarpsPerBlock) s_warp_excl[lane] = vi - v;
-        const uint32_t agg = __shfl_sync(0xffffffffu, vi, kWarpsPerBlock - 1);
-        publish_aggregate(a, tile, agg, lane);
-        if (lane == 0) s_agg = agg;
-    }
-    __syncthreads();
-
-    const uint32_t wex = s_warp_excl[wib];
-    const uint32_t agg = s_agg;
-    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll 4
-    for (int r = 0; r < kItems; ++r) {
-        const uint32_t m = __shfl_sync(0xffffffffu, my_mask, r);
-        const uint32_t re = __shfl_sync(0xffffffffu, round_excl, r);
-        if (m & (1u << lane)) s_list[wex + re + __popc(m & lt)] = static_cast<uint32_t>(wbase + 32 * r + lane);
-    }
-    __syncthreads();
-
-    // Warp 0 walks back for the prefix while the other warps gather the
-    // tile's values into shared memory (when they fit), so the gather's
-    // random reads and the look-back's round trips overlap.
-    const uint32_t all_pairs = agg * static_cast<uint32_t>(a.W);
-    const bool staged = all_pairs <= static_cast<uint32_t>(kGatherStash);
-    if (wib == 0) {
-        const uint64_t ex = walk_back(a, tile, agg, lane);
-        if (lane == 0) s_excl = ex;
-    } else if (staged) {
-        for (uint32_t q = threadIdx.x - 32; q < all_pairs; q += kThreads - 32) {
-            const uint32_t w = q / agg;
-            const uint32_t k = q - w * agg;
-            s_vals[q] = __ldg(a.models.p[w] + s_list[k]);
-        }
-    }
-    __syncthreads();
-    const uint64_t excl = s_excl;
-
-    // per 32-element group: mask bits and the masked count before the group
-    if (a.group_mask != nullptr && lane < kItems) {
-        const int64_t g = (wbase >> 5) + lane;
-        if (g * 32 < a.n) {
-            a.group_mask[g] = my_mask;
-            a.group_excl[g] = static_cast<uint32_t>(excl + wex + round_excl);
-        }
-    }
-    // indices, then the values: from the stash, or one (entry, worker) pair
-    // per thread so that every random read is in flight at once; stores stay
-    // coalesced per worker
-    const uint32_t kept = static_cast<uint64_t>(a.capacity) > excl
-        ? static_cast<uint32_t>(min(static_cast<uint64_t>(agg), static_cast<uint64_t>(a.capacity) - excl)) : 0u;
-    for (uint32_t k = threadIdx.x; k < kept; k += kThreads) a.idx[excl + k] = s_list[k];
-    const uint32_t pairs = kept * static_cast<uint32_t>(a.W);
-    for (uint32_t q = threadIdx.x; q < pairs; q += kThreads) {
-        const uint32_t w = q / kept;
-        const uint32_t k = q - w * kept;
-        a.vals.p[w][excl + k] = staged ? s_vals[w * agg + k] : __ldg(a.models.p[w] + s_list[k]);
-    }
+// The total count, written by the CTA that writes the last tile.
+__device__ __forceinline__ void finish_count(const MaskArgs& a, int64_t tile, uint64_t excl, uint32_t agg) {
     if (threadIdx.x == 0 && tile == a.ntiles - 1) {
         const uint64_t total = excl + agg;
         *a.d_count = total;
         if (total > static_cast<uint64_t>(a.capacity)) atomicExch(a.d_status, GC_ERR_CAPACITY);
     }
+}
+
+// The group tables of a tile whose exclusive prefix is `excl`.
+__device__ __forceinline__ void write_groups(const MaskArgs& a, const TileStage& st, uint64_t excl) {
+    if (a.group_mask == nullptr) return;
+    const int64_t g0 = st.tile * kGroups;
+    for (int g = threadIdx.x; g < kGroups; g += kThreads) {
+        if ((g0 + g) * 32 < a.n) {
+            a.group_mask[g0 + g] = st.gmask[g];
+            a.group_excl[g0 + g] = static_cast<uint32_t>(excl + st.gex[g]);
+        }
+    }
+}
+
+// Output positions start .. start+count-1 from a list of indices: idx, then
+// every worker's vals with one (entry, worker) pair per thread, so that all
+// the random reads are in flight at once; stores stay coalesced per worker.
+// Positions at or above the capacity are dropped.
+__device__ void write_list(const MaskArgs& a, const uint32_t* list, uint64_t start, uint32_t count) {
+    const uint64_t cap = static_cast<uint64_t>(a.capacity);
+    const uint32_t kept = cap > start ? static_cast<uint32_t>(min(static_cast<uint64_t>(count), cap - start)) : 0u;
+    for (uint32_t k = threadIdx.x; k < kept; k += kThreads) a.idx[start + k] = list[k];
+    const uint32_t pairs = kept * static_cast<uint32_t>(a.W);
+    for (uint32_t q = threadIdx.x; q < pairs; q += kThreads) {
+        const uint32_t w = q / kept;
+        const uint32_t k = q - w * kept;
+        a.vals.p[w][start + k] = __ldg(a.models.p[w] + list[k]);
+    }
+}
+
+// K6: a persistent grid; each CTA takes 4096-element tiles in order from a
+// dynamic counter, so every predecessor of a claimed tile is held by a
+// running CTA.  Warp w hashes elements tile*4096 + 512w + 32r + lane (r < 16)
+// and keeps the ballot of round r in lane r; one block scan gives the tile's
+// count, which is published at once.  The tile's masked indices are listed in
+// shared memory and its prefix is only looked up after the CTA has hashed and
+// published its NEXT tile: by then the predecessors have long published, so
+// the look-back is short and its round trips overlap other work.  Then idx[],
+// every worker's vals[] and the per-group tables (mask bits and the masked
+// count before each 32-element group, used by the fused pair-average +
+// elastic step) are written.  A tile with more masked entries than one list
+// holds takes its prefix at once and is written in chunks through both lists.
+__global__ void __launch_bounds__(kThreads)
+k_saps_mask_compact(const MaskArgs a) {
+    __shared__ uint32_t s_list[2 * kListCap];   // one list per stage; both for a dense tile
+    __shared__ TileStage s_stage[2];
+    __shared__ uint32_t s_warp_excl[kWarpsPerBlock];
+    __shared__ uint32_t s_warp_tot[kWarpsPerBlock];
+    __shared__ unsigned long long s_tile;
+    __shared__ uint64_t s_excl;
+
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    int cur = 0;              // stage (and list) of the tile being hashed
+    bool have_prev = false;   // stage cur ^ 1 holds a tile waiting for its prefix
+    // Every condition below that guards a barrier is uniform over the CTA.
+    while (true) {
+        if (threadIdx.x == 0) s_tile = atomicAdd(a.counter, 1ull);
+        __syncthreads();
+        const int64_t tile = static_cast<int64_t>(s_tile);
+        const bool have = tile < a.ntiles;
+        TileStage& st = s_stage[cur];
+        uint32_t* list = s_list + cur * kListCap;
+        const int64_t wbase = tile * kTileElems + static_cast<int64_t>(wib) * kWarpSpan;
+        uint32_t my_mask = 0, round_excl = 0;
+        if (have) {
+            my_mask = wbase + kWarpSpan <= a.n ? hash_rounds<false>(a, wbase, lane)
+                                               : hash_rounds<true>(a, wbase, lane);
+            const uint32_t cnt = __popc(my_mask);
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < kItems; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            round_excl = incl - cnt;
+            if (lane == kItems - 1) s_warp_tot[wib] = incl;
+        }
+        __syncthreads();
+        if (have && wib == 0) {
+            const uint32_t v = lane < kWarpsPerBlock ? s_warp_tot[lane] : 0u;
+            uint32_t vi = v;
+#pragma unroll
+            for (int o = 1; o < kWarpsPerBlock; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, vi, o);
+                if (lane >= o) vi += t;
+            }
+            if (lane < kWarpsPerBlock) s_warp_excl[lane] = vi - v;
+            const uint32_t agg = __shfl_sync(0xffffffffu, vi, kWarpsPerBlock - 1);
+            publish_aggregate(a, tile, agg, lane);
+            if (lane == 0) {
+                st.agg = agg;
+                st.tile = tile;
+            }
+        }
+        __syncthreads();
+        // tile entries before round `lane` of this warp (lanes < kItems)
+        const uint32_t before = have ? s_warp_excl[wib] + round_excl : 0u;
+        const uint32_t agg = have ? st.agg : 0u;
+        const uint32_t eb = static_cast<uint32_t>(wbase) + 32u * static_cast<uint32_t>(lane);
+        if (have) {
+            if (lane < kItems) {
+                st.gmask[wib * kItems + lane] = my_mask;
+                st.gex[wib * kItems + lane] = before;
+            }
+            if (agg <= static_cast<uint32_t>(kListCap)) {
+                uint32_t pos = before;
+                for (uint32_t mm = my_mask; mm != 0; mm &= mm - 1) list[pos++] = eb + (__ffs(mm) - 1);
+            }
+        }
+        if (have_prev) {
+            const TileStage& pv = s_stage[cur ^ 1];
+            if (wib == 0) {
+                const uint64_t ex = walk_back(a, pv.tile, pv.agg, lane);
+                if (lane == 0) s_excl = ex;
+            }
+            __syncthreads();
+            const uint64_t ex = s_excl;
+            write_groups(a, pv, ex);
+            write_list(a, s_list + (cur ^ 1) * kListCap, ex, pv.agg);
+            finish_count(a, pv.tile, ex, pv.agg);
+        }
+        if (!have) break;
+        if (agg > static_cast<uint32_t>(kListCap)) {
+            __syncthreads();                  // s_excl and the previous tile's list are free
+            if (wib == 0) {
+                const uint64_t ex = walk_back(a, tile, agg, lane);
+                if (lane == 0) s_excl = ex;
+            }
+            __syncthreads();
+            const uint64_t ex = s_excl;
+            write_groups(a, st, ex);
+            for (uint32_t c0 = 0; c0 < agg; c0 += 2 * kListCap) {
+                uint32_t pos = before;
+                for (uint32_t mm = my_mask; mm != 0; mm &= mm - 1, ++pos)
+                    if (pos - c0 < static_cast<uint32_t>(2 * kListCap)) s_list[pos - c0] = eb + (__ffs(mm) - 1);
+                __syncthreads();
+                write_list(a, s_list, ex + c0, min(agg - c0, static_cast<uint32_t>(2 * kListCap)));
+                __syncthreads();
+            }
+            finish_count(a, tile, ex, agg);
+            have_prev = false;
+        } else {
+            have_prev = true;
+            cur ^= 1;
+        }
+    }
+}
+
+// Grid of the compaction: as many CTAs as are resident at once, at most one
+// per tile.
+int launch_mask(const MaskArgs& a, cudaStream_t s) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_saps_mask_compact, kThreads, 0) != cudaSuccess)
+        return GC_ERR_CUDA;
+    const int64_t resident = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles < resident ? a.ntiles : resident), kThreads, 0, s>>>(a);
+    return launch_status();
 }
 
 // ------------------------------------------------------------------ K7
@@ -841,8 +917,7 @@ static int mask_compact_impl(int64_t n, double p, uint64_t seed_t, const float* 
     if (cudaMemsetAsync(workspace, 0, kWsHeader + sizeof(uint64_t) * static_cast<size_t>(a.ntiles), s) !=
         cudaSuccess)
         return GC_ERR_CUDA;
-    k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles), kThreads, 0, s>>>(a);
-    return launch_status();
+    return launch_mask(a, s);
 }
 
 int saps_mask_compact(int64_t n, double p, uint64_t seed_t, const float* const* models, int W,
@@ -1176,6 +1251,5 @@ extern "C" int saps_mask_compact_noalloc(int64_t n, double p, uint64_t seed_t,
     a.d_status = d_status;
     const size_t used = kWsHeader + sizeof(uint64_t) * static_cast<size_t>(a.ntiles);
     if (cudaMemsetAsync(scratch, 0, used, s) != cudaSuccess) return GC_ERR_CUDA;
-    k_saps_mask_compact<<<static_cast<unsigned>(a.ntiles), kThreads, 0, s>>>(a);
-    return launch_status();
+    return launch_mask(a, s);
 }

@@ -40,8 +40,11 @@ class Compactor:
 
 
 @pytest.mark.parametrize("n", [1, 100, 4095, 4096, 4097, 3 * 4096 + 5, 1_000_003])
-@pytest.mark.parametrize("p", [0.001, 0.01, 0.5, 1.0])
+@pytest.mark.parametrize("p", [0.001, 0.01, 0.25, 0.5, 1.0])
 def test_mask_compact_parity(n, p):
+    """p = 0.25 puts about half the 4096-element tiles above the 1024 entries
+    a tile stages for its deferred write (the rest take their prefix at once),
+    so both paths alternate in one launch."""
     W = 3
     models = [wl.normal(n, 0.05, 4000 + w, device=DEV) for w in range(W)]
     seed_t = oracle.round_seed(5, n % 7)
@@ -76,17 +79,24 @@ def test_mask_compact_sixteen_workers_and_repeat_calls():
             np.testing.assert_array_equal(vals[w].astype(np.float64), rvals[w])
 
 
-def test_capacity_overflow_reports_and_truncates():
+@pytest.mark.parametrize("p,cap", [(0.1, 100), (0.5, 100), (0.5, 3000), (0.25, 1500)])
+def test_capacity_overflow_reports_and_truncates(p, cap):
+    """The capacity cut lands inside a staged tile (p = 0.1), inside a dense
+    tile written at once (p = 0.5), or where both kinds alternate."""
     n, W = 50_000, 2
     models = [wl.normal(n, 1.0, w, device=DEV) for w in range(W)]
-    comp = Compactor(n, W, 100)
-    comp.run(0.1, 99, models)
+    comp = Compactor(n, W, cap)
+    comp.run(p, 99, models)
     K, idx, vals, status = comp.result()
-    rK, ridx, _ = oracle.saps_mask_compact(n, 0.1, 99, [host_f32(m).astype(np.float64) for m in models])
-    assert K == rK > 100
+    rK, ridx, rvals = oracle.saps_mask_compact(n, p, 99, [host_f32(m).astype(np.float64) for m in models])
+    assert K == rK > cap
     assert status == gc.GC_ERR_CAPACITY
-    np.testing.assert_array_equal(idx, ridx[:100])
-    check_guard(comp.idx, 100)
+    np.testing.assert_array_equal(idx, ridx[:cap])
+    for w in range(W):
+        np.testing.assert_array_equal(vals[w].astype(np.float64), rvals[w][:cap])
+    check_guard(comp.idx, cap)
+    for v in comp.vals:
+        check_guard(v, cap)
 
 
 def test_saps_rounds_chain():
@@ -161,7 +171,7 @@ def test_easgd_step_parity(W, n):
 
 @pytest.mark.parametrize("W", [2, 4, 16, 18])
 @pytest.mark.parametrize("n,p,cap", [(1, 0.5, None), (33, 0.5, None), (4097, 0.01, None),
-                                     (100_003, 0.01, None), (100_003, 0.3, 5000)])
+                                     (100_003, 0.01, None), (100_003, 0.25, None), (100_003, 0.3, 5000)])
 def test_fused_average_easgd_is_bitwise_the_two_calls(W, n, p, cap):
     """saps_average_easgd_step == saps_peer_average then easgd_step, bit for
     bit, including a capacity overflow (entries beyond capacity not averaged)."""
