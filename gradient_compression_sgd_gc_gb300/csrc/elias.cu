@@ -17,8 +17,9 @@
 // scan of bit lengths per 32 code words, then shared-memory atomicOr of at
 // most three words per lane) and stores it with coalesced 32-bit writes.
 // Decode: one thread per bucket walks its stream with a 64-bit window; an
-// 8-bit lookahead table decodes every codeword of up to 8 bits (all of them
-// for 4-bit codes) in one step.
+// 11-bit (4-bit codes) or 12-bit (8-bit codes) lookahead table, built by the
+// compiler, decodes up to 8 or 4 whole codewords per step, and an 8-bit one
+// the rest.
 #include "gc_common.cuh"
 
 namespace gc {
@@ -529,52 +530,81 @@ struct DecodeArgs {
     int* status;
 };
 
-// Single-codeword table: the codeword (+ sign) at the top of an 8-bit
-// window, as (level << 5) | (sign << 4) | length, or 0 when it does not end
-// inside the window.
-__device__ __forceinline__ uint32_t decode_entry(uint32_t x) {
+// Lookahead bits of the multi-codeword table: 11 for 4-bit codes, 12 for
+// 8-bit ones (measured fastest of 10-12 on the QSGD workloads).
+template <bool FOUR>
+__host__ __device__ constexpr int win_bits() { return FOUR ? 11 : 12; }
+
+// The codeword (+ sign) at the top of a W-bit window x, as
+// (level << 5) | (sign << 4) | length, or 0 when it does not end inside the
+// window.  W = 8 gives the single-codeword table; evaluable at compile time.
+template <int W>
+__host__ __device__ constexpr uint32_t window_entry(uint32_t x) {
+    constexpr uint32_t kMask = (1u << W) - 1u;
     int pos = 0;
     uint32_t N = 1;
     for (;;) {
-        if (pos >= 8) return 0u;
-        const uint32_t bit = (x >> (7 - pos)) & 1u;
+        if (pos >= W) return 0u;
+        const uint32_t bit = (x >> (W - 1 - pos)) & 1u;
         ++pos;
         if (!bit) break;
-        if (pos + static_cast<int>(N) > 8) return 0u;
-        const uint32_t v = ((x << (pos - 1)) & 255u) >> (8 - (N + 1));
+        if (pos + static_cast<int>(N) > W) return 0u;
+        const uint32_t v = ((x << (pos - 1)) & kMask) >> (W - (N + 1));
         pos += static_cast<int>(N);
         N = v;
     }
     const uint32_t level = N - 1u;
     uint32_t sign = 0u;
     if (level) {
-        if (pos >= 8) return 0u;
-        sign = (x >> (7 - pos)) & 1u;
+        if (pos >= W) return 0u;
+        sign = (x >> (W - 1 - pos)) & 1u;
         ++pos;
     }
     return (level << 5) | (sign << 4) | static_cast<uint32_t>(pos);
 }
 
-// Multi-codeword table: every whole codeword (+ sign) at the front of an
-// 8-bit window, up to KMAX of them and stopping before a level above s:
-// x = (count << 4) | bits used, y = their codes in the output layout
-// (4-bit or 8-bit sign-magnitude), the first one most significant.
+// Multi-codeword table entry: every whole codeword (+ sign) at the front of a
+// win_bits()-bit window, up to KMAX of them (the codes that fill 32 bits) and
+// stopping before a level the code width cannot hold.  Bits 0-3: bits used;
+// 4-7: codeword count (0 when the first codeword is longer than the window);
+// 8-14: the largest level (checked against s at run time); 32-63: the codes
+// in the output layout, first one most significant.
 template <bool FOUR>
-__device__ __forceinline__ uint2 multi_entry(uint32_t x, uint32_t s) {
-    constexpr int KMAX = FOUR ? 8 : 4;
-    uint32_t used = 0, k = 0, packed = 0;
-    while (k < KMAX && used < 8) {
-        const uint32_t t = decode_entry((x << used) & 255u);
+__host__ __device__ constexpr uint64_t multi_window_entry(uint32_t x) {
+    constexpr uint32_t KMAX = FOUR ? 8 : 4;
+    constexpr uint32_t kMaxLevel = FOUR ? 7 : 127;
+    constexpr int W = win_bits<FOUR>();
+    constexpr uint32_t kMask = (1u << W) - 1u;
+    uint32_t used = 0, k = 0, packed = 0, top = 0;
+    while (k < KMAX && used < static_cast<uint32_t>(W)) {
+        const uint32_t t = window_entry<W>((x << used) & kMask);
         const uint32_t len = t & 15u;
-        if (!t || used + len > 8) break;
+        if (!t || used + len > static_cast<uint32_t>(W)) break;
         const uint32_t level = t >> 5, sign = (t >> 4) & 1u;
-        if (level > s) break;
+        if (level > kMaxLevel) break;
         packed = FOUR ? (packed << 4) | (sign << 3) | level : (packed << 8) | (sign << 7) | level;
+        top = level > top ? level : top;
         used += len;
         ++k;
     }
-    return make_uint2((k << 4) | used, packed);
+    return (static_cast<uint64_t>(packed) << 32) | (top << 8) | (k << 4) | used;
 }
+
+template <bool FOUR>
+struct MultiTable {
+    uint64_t e[1 << win_bits<FOUR>()];
+};
+
+template <bool FOUR>
+constexpr MultiTable<FOUR> make_multi_table() {
+    MultiTable<FOUR> t{};
+    for (uint32_t x = 0; x < (1u << win_bits<FOUR>()); ++x) t.e[x] = multi_window_entry<FOUR>(x);
+    return t;
+}
+
+// Built by the compiler; each decoding CTA copies its table to shared memory.
+__device__ const MultiTable<true> kMulti4 = make_multi_table<true>();
+__device__ const MultiTable<false> kMulti8 = make_multi_table<false>();
 
 // Output side of the decoder: codes arrive in units of 4 or 8 bits, first
 // code most significant, and leave as 16-byte stores.
@@ -633,13 +663,16 @@ struct CodeWriter {
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     constexpr int KMAX = FOUR ? 8 : 4;
-    __shared__ uint2 multi[256];
+    constexpr int W = win_bits<FOUR>();
+    __shared__ __align__(16) uint64_t multi[1 << W];
     __shared__ uint32_t single[256];
     const uint32_t smax = static_cast<uint32_t>(a.s);
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-        multi[i] = multi_entry<FOUR>(static_cast<uint32_t>(i), smax);
-        single[i] = decode_entry(static_cast<uint32_t>(i));
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(FOUR ? kMulti4.e : kMulti8.e);
+        uint4* dst = reinterpret_cast<uint4*>(multi);
+        for (int i = threadIdx.x; i < (1 << W) / 2; i += blockDim.x) dst[i] = __ldg(src + i);
     }
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) single[i] = window_entry<8>(static_cast<uint32_t>(i));
     // The CTA's 256 buckets are handed to its threads in order of stream
     // length (a counting sort on the word count), so that the threads of a
     // warp walk streams of about the same length instead of idling on the
@@ -717,14 +750,25 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
         code = FOUR ? (sign << 3) | (level & 7u) : (sign << 7) | level;
         l = static_cast<int>(k) + 7;
     };
+    // One codeword through the 8-bit table, or the long-codeword formula.
+    auto one_code = [&](uint32_t& code, int& l) {
+        const uint32_t t = single[whi >> 24];
+        l = static_cast<int>(t & 15u);
+        const uint32_t level = t >> 5, sign = level ? (t >> 4) & 1u : 0u;
+        if (t && level <= smax)
+            code = FOUR ? (sign << 3) | level : (sign << 7) | level;
+        else
+            long_code(code, l);
+    };
     int e = 0;
     while (len - e >= KMAX) {
-        const uint2 t = multi[whi >> 24];
-        int k = static_cast<int>(t.x >> 4);
-        int l = static_cast<int>(t.x & 15u);
-        uint32_t packed = t.y;
-        if (k == 0) {
-            long_code(packed, l);
+        const uint64_t t = multi[whi >> (32 - W)];
+        int k = static_cast<int>((t >> 4) & 15u);
+        int l = static_cast<int>(t & 15u);
+        uint32_t packed = static_cast<uint32_t>(t >> 32);
+        if (k == 0 || ((t >> 8) & 127u) > smax) {
+            // a codeword longer than the window, or a level above s
+            one_code(packed, l);
             k = 1;
         }
         consume(l);
@@ -732,14 +776,9 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
         e += k;
     }
     for (; e < len; ++e) {
-        const uint32_t t = single[whi >> 24];
-        int l = static_cast<int>(t & 15u);
-        const uint32_t level = t >> 5, sign = level ? (t >> 4) & 1u : 0u;
         uint32_t code;
-        if (t && level <= smax)
-            code = FOUR ? (sign << 3) | level : (sign << 7) | level;
-        else
-            long_code(code, l);
+        int l;
+        one_code(code, l);
         consume(l);
         wr.put(code, 1);
     }
