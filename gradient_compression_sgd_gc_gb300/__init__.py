@@ -11,10 +11,12 @@ Entry points (same names as the C ABI):
   gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update, gc_2bit_step,
   gc_2bit_quantize_local,
   gc_compensated_sum_update,
-  qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum,
+  qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum, qsgd_step,
+  qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_max_words, qsgd_elias_workspace_bytes,
   saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
-  saps_peer_average, saps_average_easgd_step, easgd_step, gc_status_string,
-  gc_version
+  saps_mask_compact_noalloc, saps_peer_average, saps_average_easgd_step, easgd_step,
+  saps_round, gc_status_string, gc_version
+Front ends over them (per-key state, parameter rules): ``compression.py``.
 """
 from __future__ import annotations
 
@@ -145,6 +147,14 @@ def _dev(t: torch.Tensor, name: str, dtype=None, numel: int | None = None,
 def _ptrs(ts, name, dtype=None, numel=None, pinned_ok=False):
     return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]", dtype, numel, pinned_ok)
                                          for i, t in enumerate(ts)])
+
+
+def _pairs(pairs, W: int, where: str):
+    """Host int array of the matching (pairs (p[2q], p[2q+1])); the library
+    checks that it is a permutation of 0..W-1."""
+    if len(pairs) != W:
+        raise ValueError(f"{where}: pairs must list all {W} workers, got {len(pairs)} entries")
+    return (ctypes.c_int * W)(*[int(q) for q in pairs])
 
 
 def _check(status: int, where: str) -> None:
@@ -427,7 +437,7 @@ def saps_peer_average(models, vals, idx: torch.Tensor, d_count: torch.Tensor, pa
                       stream=None, prepare: bool = False):
     lib = load()
     W = len(models)
-    pairs_arr = (ctypes.c_int * W)(*[int(p) for p in pairs])
+    pairs_arr = _pairs(pairs, W, "saps_peer_average")
     capacity = idx.numel()
     args = (_ptrs(models, "models", torch.float32), _ptrs(vals, "vals", torch.float32, capacity),
             _dev(idx, "idx", torch.int32), _dev(d_count, "d_count", torch.int64, 1),
@@ -445,7 +455,7 @@ def saps_average_easgd_step(models, vals, d_count: torch.Tensor, pairs, alpha: f
     W = len(models)
     n = center.numel()
     capacity = vals[0].numel() if vals else 0
-    pairs_arr = (ctypes.c_int * W)(*[int(p) for p in pairs])
+    pairs_arr = _pairs(pairs, W, "saps_average_easgd_step")
     args = (_ptrs(models, "models", torch.float32, n), _ptrs(vals, "vals", torch.float32, capacity),
             _dev(d_count, "d_count", torch.int64, 1), pairs_arr, W, n, capacity, float(alpha),
             float(beta), _dev(center, "center", torch.float32, n),
@@ -465,7 +475,7 @@ def saps_round(n: int, p: float, seed_t: int, models, pairs, alpha: float, beta:
     fn = lib.gc_testing_saps_round_one_pass if _one_pass else lib.saps_round
     W = len(models)
     capacity = idx.numel()
-    pairs_arr = (ctypes.c_int * W)(*[int(q) for q in pairs])
+    pairs_arr = _pairs(pairs, W, "saps_round")
     args = (int(n), float(p), int(seed_t) & 0xFFFFFFFFFFFFFFFF,
             _ptrs(models, "models", torch.float32, n), W, pairs_arr, float(alpha), float(beta),
             _dev(center, "center", torch.float32, n), _dev(idx, "idx", torch.int32),

@@ -260,3 +260,21 @@ def test_one_pass_entry_validation():
     assert call(center=MISALIGNED) == gc.GC_ERR_ALIGN
     assert call(models=_ptrs(FAKE, MISALIGNED, FAKE, FAKE)) == gc.GC_ERR_ALIGN
 
+
+
+def test_binding_wants_the_whole_matching():
+    """A matching shorter than the worker list is refused on the host (a short
+    list padded with zeros could still be a permutation)."""
+    import torch
+    models = [torch.zeros(4) for _ in range(4)]
+    for call in (lambda: gc.saps_peer_average(models, models, torch.zeros(4, dtype=torch.int32),
+                                              torch.zeros(1, dtype=torch.int64), [1, 2, 3]),
+                 lambda: gc.saps_average_easgd_step(models, models, torch.zeros(1, dtype=torch.int64),
+                                                    [1, 2, 3], 0.9, 0.9, torch.zeros(4),
+                                                    torch.zeros(16, dtype=torch.uint8)),
+                 lambda: gc.saps_round(4, 0.5, 1, models, [1, 2, 3], 0.9, 0.9, torch.zeros(4),
+                                       torch.zeros(4, dtype=torch.int32), models,
+                                       torch.zeros(1, dtype=torch.int64), torch.zeros(16, dtype=torch.uint8),
+                                       torch.zeros(1, dtype=torch.int32))):
+        with pytest.raises(ValueError, match="pairs must list all 4 workers"):
+            call()
