@@ -232,9 +232,12 @@ __device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int l
     }
 }
 
-// One warp per bucket; the grid covers every bucket.
+// One warp per bucket; the grid covers every bucket.  For buckets of up to
+// 512 the register bound allows 8 CTAs (64 warps) per SM: the quantiser is
+// issue- and latency-bound, and full occupancy measured 5-6% faster than 4
+// CTAs per SM despite a few spilled registers.
 template <int ROUNDS, bool FOUR, bool MAXNORM>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 8)
 k_qsgd_quantize(const QArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -257,7 +260,7 @@ struct StepArgs {
 };
 
 template <int ROUNDS, bool FOUR, bool MAXNORM>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
 k_qsgd_step(const StepArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
