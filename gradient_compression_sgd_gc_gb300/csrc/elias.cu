@@ -264,8 +264,9 @@ struct CountArgs {
     Ws ws;
 };
 
+// Register bound for 8 CTAs per SM (measured fastest with the encoder below).
 template <bool FOUR>
-__global__ void __launch_bounds__(kThreads) k_elias_count(CountArgs a) {
+__global__ void __launch_bounds__(kThreads, 8) k_elias_count(CountArgs a) {
     __shared__ uint32_t lut[256];
     __shared__ uint32_t bits_s[kChunk];
     __shared__ uint32_t wsum[kWarpsPerBlock];
@@ -402,8 +403,10 @@ __device__ __forceinline__ void emit_piece(uint32_t* stage, uint32_t start, cons
     if (nacc > 0) atomicOr(stage + wi, lo << (32 - nacc));
 }
 
+// Register bound for 5 CTAs per SM (48 registers, no spills): 3-8% faster
+// than the 4 that 54-58 registers allow.
 template <bool FOUR>
-__global__ void __launch_bounds__(kThreads) k_elias_encode(EncodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
     extern __shared__ uint32_t smem[];
     uint32_t* lut = smem;
     uint32_t* offs = smem + 256;                       // [kChunk]
