@@ -32,6 +32,48 @@ __device__ __forceinline__ void acc_square(float x, float& hi, float& lo) {
     lo = __fadd_rn(lo, __fadd_rn(e, q));
 }
 
+// Two fp32 lanes in one 64-bit register, for the packed (f32x2) arithmetic of
+// sm_100+: one instruction does the same IEEE round-to-nearest operation on
+// both halves.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// acc_square on two independent accumulators at once (the even and the odd
+// elements of a pair): the same operations, each rounded as there.  The
+// square is formed as fma(x, x, +0) (the same value as x*x): a packed multiply
+// feeding the packed add of the TwoSum was measured to be contracted into one
+// fma by the assembler, which loses the error term this sum relies on.
+__device__ __forceinline__ void acc_square2(uint64_t x, uint64_t& hi, uint64_t& lo) {
+    const uint64_t p = fma2(x, x, 0ull);
+    const uint64_t q = fma2(x, x, sub2(0ull, p));     // x*x - p, exactly
+    const uint64_t s = add2(hi, p);                    // TwoSum(hi, p)
+    const uint64_t bp = sub2(s, hi);
+    const uint64_t e = add2(sub2(hi, sub2(s, bp)), sub2(p, bp));
+    hi = s;
+    lo = add2(lo, add2(e, q));
+}
+
 // Sum of squares of a double-float pair over the warp (every lane gets it).
 __device__ __forceinline__ void warp_sum2(float& hi, float& lo) {
 #pragma unroll
@@ -147,14 +189,19 @@ __device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int l
         for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         norm = mx;
     } else {
-    float hi = 0.0f, lo = 0.0f;
+    // two double-float accumulators (even and odd elements) in packed fp32
+    // pairs, joined by one TwoSum: the same accuracy as one accumulator
+    uint64_t hi2 = 0ull, lo2 = 0ull;
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
-        acc_square(v[j].x, hi, lo);
-        acc_square(v[j].y, hi, lo);
-        acc_square(v[j].z, hi, lo);
-        acc_square(v[j].w, hi, lo);
+        acc_square2(pack2(v[j].x, v[j].y), hi2, lo2);
+        acc_square2(pack2(v[j].z, v[j].w), hi2, lo2);
     }
+    float ha, hb, la, lb, hi, e;
+    unpack2(hi2, ha, hb);
+    unpack2(lo2, la, lb);
+    two_sum(ha, hb, hi, e);
+    const float lo = __fadd_rn(__fadd_rn(la, lb), e);
     norm = warp_norm(hi, lo);
     // A sum of squares below 2^-100 may have lost bits to underflow and one
     // above 2^126 overflows: such buckets (subnormal-sized or huge gradients;
