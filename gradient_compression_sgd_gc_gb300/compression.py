@@ -18,10 +18,11 @@ import math
 
 import torch
 
-from . import (GC_UPD_EASGD, GC_UPD_NONE, GC_UPD_SGD, code_words, gc_2bit_dequant_sum_update,
-               gc_2bit_quantize, gc_2bit_step)
+from . import (GC_MAX_WORKERS, GC_UPD_EASGD, GC_UPD_NONE, GC_UPD_SGD, code_words,
+               gc_2bit_dequant_sum_update, gc_2bit_quantize, gc_2bit_quantize_batched,
+               gc_2bit_quantize_local, gc_2bit_step, gc_compensated_sum_update)
 
-__all__ = ["GradientCompression", "QSGD", "SAPSGossip"]
+__all__ = ["GradientCompression", "CDSGD", "QSGD", "SAPSGossip"]
 
 _TYPES = ("none", "2bit")
 
@@ -123,6 +124,57 @@ class GradientCompression:
         gc_2bit_step([g.reshape(-1) for g in grads], list(res), list(codes), self._params["threshold"],
                      GC_UPD_SGD, lr=lr, weights=weights)
         self._used = True
+
+
+class CDSGD:
+    """CD-SGD's step schedule for W workers held on this GPU ("CD-SGD:
+    Distributed Stochastic Gradient Descent with Compression and Delay
+    Compensation", Algorithm 1, eq. 10 and eq. 11).  Steps are counted from 1;
+    every k-th step is a correction step: each worker sends its
+    residual-compensated full-precision gradient r + g (its residual is then
+    zeroed) and the weights take their average; every other step each worker
+    2-bit quantises its gradient with its residual and the weights take the
+    dequantised average.  With ``local_lr`` set, a compressed step also writes
+    each worker's local weights W - local_lr * g (eq. 11) from the weights
+    before the update.  Gradients are fp32 or bf16, one size for all."""
+
+    def __init__(self, n: int, workers: int, threshold: float, lr: float, k: int = 4,
+                 local_lr: float | None = None, device="cuda"):
+        if not (1 <= workers <= GC_MAX_WORKERS):
+            raise ValueError(f"need 1 <= workers <= {GC_MAX_WORKERS}")
+        if int(k) != k or k < 1:
+            raise ValueError("the correction period k must be a positive integer")
+        if not (math.isfinite(threshold) and threshold > 0.0):
+            raise ValueError("threshold must be finite and positive")
+        if not math.isfinite(lr) or (local_lr is not None and not math.isfinite(local_lr)):
+            raise ValueError("learning rates must be finite")
+        self.n, self.W, self.k = int(n), int(workers), int(k)
+        self.threshold, self.lr, self.local_lr = float(threshold), float(lr), local_lr
+        self.residuals = [torch.zeros(self.n, dtype=torch.float32, device=device) for _ in range(self.W)]
+        self.codes = [torch.empty(code_words(self.n), dtype=torch.int32, device=device) for _ in range(self.W)]
+        self.t = 0
+
+    def is_correction(self, t: int) -> bool:
+        """Whether step t (1-based) sends full precision."""
+        return t % self.k == 0
+
+    def step(self, grads, weights: torch.Tensor, local_weights=None) -> bool:
+        """One step; returns True for a correction step."""
+        if len(grads) != self.W:
+            raise ValueError(f"expected {self.W} gradients")
+        if self.local_lr is not None and local_weights is None and not self.is_correction(self.t + 1):
+            raise ValueError("local_lr is set: pass one local-weights buffer per worker")
+        self.t += 1
+        if self.is_correction(self.t):
+            gc_compensated_sum_update(list(grads), self.residuals, self.lr, weights)
+            return True
+        if self.local_lr is not None:
+            gc_2bit_quantize_local(list(grads), self.residuals, self.codes, weights, list(local_weights),
+                                   self.threshold, self.local_lr)
+        else:
+            gc_2bit_quantize_batched(list(grads), self.residuals, self.codes, self.threshold)
+        gc_2bit_dequant_sum_update(self.codes, self.n, self.threshold, GC_UPD_SGD, lr=self.lr, weights=weights)
+        return False
 
 
 class QSGD:

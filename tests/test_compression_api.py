@@ -123,3 +123,61 @@ def test_saps_front_end_rounds_equal_the_calls():
         assert torch.equal(ga.models[w], mb[w])
     assert torch.equal(ga.center, cb)
     assert int(ga.status.item()) == 0
+
+
+def test_cdsgd_rules():
+    from gradient_compression_sgd_gc_gb300.compression import CDSGD
+    for kw in ({"k": 0}, {"k": 2.5}, {"threshold": 0.0}, {"threshold": float("nan")},
+               {"workers": 0}, {"workers": 65}, {"lr": float("inf")}, {"local_lr": float("nan")}):
+        args = {"n": 10, "workers": 2, "threshold": 1e-3, "lr": 0.01, "device": "cpu"}
+        args.update(kw)
+        with pytest.raises(ValueError):
+            CDSGD(**args)
+    c = CDSGD(10, 2, 1e-3, 0.01, k=4, local_lr=0.1, device="cpu")
+    # Algorithm 1 with the counter starting at 1: steps 4 and 8 are full precision
+    assert [t for t in range(1, 9) if c.is_correction(t)] == [4, 8]
+    with pytest.raises(ValueError):
+        c.step([torch.zeros(10)], torch.zeros(10))                 # one gradient for two workers
+    with pytest.raises(ValueError):
+        c.step([torch.zeros(10)] * 2, torch.zeros(10))              # local_lr set, no local weights
+    assert c.t == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_cdsgd_eight_steps_against_oracle(dtype):
+    """k = 4: steps 1-3 and 5-7 compressed (with eq. 11 local weights),
+    steps 4 and 8 residual-compensated full precision; codes and residuals
+    bit-exact, weights and local weights within the float tolerance."""
+    from gradient_compression_sgd_gc_gb300.compression import CDSGD
+    dev = "cuda"
+    n, W, t, lr, llr = 70_001, 3, 1e-3, 0.01, 0.1
+    cd = CDSGD(n, W, t, lr, k=4, local_lr=llr, device=dev)
+    weights = wl.uniform(n, 0.05, 11, device=dev)
+    w_ref = weights.cpu().numpy().astype(np.float64)
+    r_ref = [np.zeros(n, np.float32) for _ in range(W)]
+    local = [torch.empty(n, device=dev) for _ in range(W)]
+    for step in range(1, 9):
+        grads = [wl.normal(n, 5e-4, 100 * step + w, device=dev, dtype=dtype) for w in range(W)]
+        hg = [(g.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == torch.bfloat16 else g.cpu().numpy())
+              for g in grads]
+        w_before = w_ref.copy()
+        corr = cd.step(grads, weights, local)
+        torch.cuda.synchronize()
+        assert corr == (step % 4 == 0)
+        if corr:
+            oracle.compensated_sum_update(hg, r_ref, lr, w_ref)
+            for w in range(W):
+                assert not cd.residuals[w].any()
+        else:
+            c_ref = [oracle.twobit_quantize(hg[w], r_ref[w], t) for w in range(W)]
+            for w in range(W):
+                np.testing.assert_array_equal(cd.codes[w].cpu().numpy().view(np.uint32), c_ref[w])
+                loc = oracle.cdsgd_local_update(hg[w], w_before, llr)
+                got = local[w].cpu().numpy()
+                assert np.max(np.abs(got - loc) / (np.abs(loc) + llr * 1e-3)) < 1e-5
+            oracle.twobit_dequant_sum_update(c_ref, n, t, oracle.KIND_SGD, lr=lr, weights=w_ref)
+        for w in range(W):
+            np.testing.assert_array_equal(cd.residuals[w].cpu().numpy().view(np.uint32), r_ref[w].view(np.uint32))
+        got = weights.cpu().numpy()
+        assert np.max(np.abs(got - w_ref) / (np.abs(w_ref) + lr * t)) < 1e-5, f"weights after step {step}"
