@@ -576,7 +576,7 @@ def rows(args, dev, peak):
         pq = [gc.qsgd_quantize(vs[w], qcfg.bucket, s, qcfg.seed, w, norms[w], codes[w], stream=stream,
                                prepare=True) for w in range(W)]
         pd = gc.qsgd_dequant_sum(codes, norms, n, qcfg.bucket, s, 1.0 / W, outq, stream=stream, prepare=True)
-        for i in range(8):
+        for i in range(22):
             for w in range(W):
                 tm.around("q" if i >= 2 else "w", pq[w])
             tm.around("d" if i >= 2 else "w", pd)
@@ -587,7 +587,7 @@ def rows(args, dev, peak):
                                                tm.ms("d"), peak, W * n)
         pm = [gc.qsgd_quantize_maxnorm(vs[w], qcfg.bucket, s, qcfg.seed, w, norms[w], codes[w], stream=stream,
                                        prepare=True) for w in range(W)]
-        for i in range(6):
+        for i in range(7):
             for w in range(W):
                 tm.around("m" if i >= 2 else "w", pm[w])
         torch.cuda.synchronize(dev)
@@ -597,7 +597,7 @@ def rows(args, dev, peak):
         # every worker's quantisation + the dequant-sum in one pass
         pst = gc.qsgd_step(vs, qcfg.bucket, s, qcfg.seed, norms, codes, 1.0 / W, outq, stream=stream,
                            prepare=True)
-        for i in range(6):
+        for i in range(22):
             tm.around("t" if i >= 2 else "w", pst)
         torch.cuda.synchronize(dev)
         sep_ms = W * _median(tm.ms("q")) + _median(tm.ms("d"))
@@ -618,7 +618,7 @@ def rows(args, dev, peak):
                                    prepare=True) for w in range(W)]
         px = [gc.qsgd_elias_decode(words[w], offs[w], n, qcfg.bucket, s, dcodes, dnorms, stream=stream,
                                    prepare=True) for w in range(W)]
-        for i in range(6):
+        for i in range(7):
             for w in range(W):
                 tm.around("e" if i >= 2 else "w", pe[w])
             for w in range(W):
@@ -648,7 +648,7 @@ def rows(args, dev, peak):
         ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
         tm = Timer(stream)
-        rounds = 32
+        rounds = 62
         for rd in range(rounds):
             seed_t = gc.saps_round_seed(scfg.base_seed, rd)
             pairs = gc.saps_matching(seed_t, W)
@@ -714,7 +714,7 @@ def rows(args, dev, peak):
         local = [torch.empty(n, device=dev) for _ in range(W)]
         pl = gc.gc_2bit_quantize_local(grads, res, codes, wts, local, ccfg.threshold, 0.1, stream=stream,
                                        prepare=True)
-        for i in range(5):
+        for i in range(21):
             k = "" if i >= 1 else "w"
             for w in range(W):
                 tm.around("q" + k, pq[w])
