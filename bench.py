@@ -634,7 +634,18 @@ def rows(args, dev, peak):
         out[f"{qcfg.name}.elias_decode"] = _row(qcfg.name, "qsgd_elias_decode",
                                                 4 * total + 4 * (nb + 1) + cb + 4 * nb, tm.ms("x"), peak, n,
                                                 {"issue": issue_roofline(f"elias_decode_s{s}", tm.ms("x"))})
-        del vs, norms, codes, outq, words, offs, ews, dcodes, dnorms
+        # the W workers' streams in one launch (the receiver's decode before the sum)
+        bcodes = [torch.empty(cb, dtype=torch.uint8, device=dev) for _ in range(W)]
+        bnorms = [torch.empty(nb, device=dev) for _ in range(W)]
+        pb = gc.qsgd_elias_decode_batched(words, offs, n, qcfg.bucket, s, bcodes, bnorms, stream=stream,
+                                          prepare=True)
+        for i in range(22):
+            tm.around("b" if i >= 2 else "w", pb)
+        torch.cuda.synchronize(dev)
+        out[f"{qcfg.name}.elias_decode_batched"] = _row(
+            qcfg.name, f"qsgd_elias_decode_batched ({W} streams, one launch)",
+            W * (4 * total + 4 * (nb + 1) + cb + 4 * nb), tm.ms("b"), peak, W * n)
+        del vs, norms, codes, outq, words, offs, ews, dcodes, dnorms, bcodes, bnorms
 
     # config 5: SAPS + EASGD, 16 workers x 25,557,032, p = 0.01 and 0.001
     for scfg in (wl.SAPS_P01, wl.SAPS_P001):

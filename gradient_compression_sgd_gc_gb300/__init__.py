@@ -12,7 +12,8 @@ Entry points (same names as the C ABI):
   gc_2bit_quantize_local,
   gc_compensated_sum_update,
   qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum, qsgd_step,
-  qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_max_words, qsgd_elias_workspace_bytes,
+  qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_decode_batched, qsgd_elias_max_words,
+  qsgd_elias_workspace_bytes,
   saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
   saps_mask_compact_noalloc, saps_peer_average, saps_average_easgd_step, easgd_step,
   saps_round, gc_status_string, gc_version
@@ -40,7 +41,7 @@ __all__ = [
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
     "gc_2bit_step", "gc_2bit_quantize_local", "qsgd_quantize_maxnorm",
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
-    "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step",
+    "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step", "qsgd_elias_decode_batched",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -93,6 +94,7 @@ def load():
             "qsgd_elias_max_words": (u64, [i64, i32, i32]),
             "qsgd_elias_workspace_bytes": (sz, [i64, i32]),
             "qsgd_elias_decode": (i32, [vp, vp, i64, i32, i32, vp, vp, vp, vp]),
+            "qsgd_elias_decode_batched": (i32, [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp]),
             "saps_round_seed": (u64, [u64, u64]),
             "saps_matching": (i32, [u64, i32, vp]),
             "saps_workspace_bytes": (sz, [i64]),
@@ -384,6 +386,23 @@ def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket
     keep = (words, offsets, codes, norms) + (() if status is None else (status,))
     return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
 
+
+
+def qsgd_elias_decode_batched(words, offsets, n: int, bucket: int, s_levels: int, codes, norms,
+                              status: torch.Tensor | None = None, stream=None, prepare: bool = False):
+    """qsgd_elias_decode of W streams (lists of equal length) in one launch."""
+    lib = load()
+    W = len(words)
+    if not (len(offsets) == len(codes) == len(norms) == W) or W == 0:
+        raise ValueError("words, offsets, codes and norms must be non-empty lists of equal length")
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_ptrs(words, "words", torch.int32), _ptrs(offsets, "offsets", torch.int32, nb + 1), W,
+            int(n), int(bucket), int(s_levels),
+            _ptrs(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _ptrs(norms, "norms", torch.float32, nb),
+            None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words[0]))
+    keep = (list(words), list(offsets), list(codes), list(norms)) + (() if status is None else (status,))
+    return _invoke(lib.qsgd_elias_decode_batched, args, "qsgd_elias_decode_batched", prepare, keep)
 
 def qsgd_step(grads, bucket: int, s_levels: int, seed: int, norms, codes, scale: float,
               out: torch.Tensor, maxnorm: bool = False, stream=None, prepare: bool = False):

@@ -521,15 +521,18 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
 
 // ---------------------------------------------------------------- decode
 
+// One launch decodes W streams (blockIdx.y = stream): a decoding thread owns
+// one bucket, so a single stream of 61 M coordinates fills only about a
+// quarter of the GPU's warp slots; W streams fill W times more.
 struct DecodeArgs {
-    const uint32_t* words;
-    const uint32_t* offsets;
+    PtrTable<const uint32_t*> words;
+    PtrTable<const uint32_t*> offsets;
+    PtrTable<uint8_t*> codes;
+    PtrTable<float*> norms;
     int64_t n;
     int d;
     int64_t nbuckets;
     int s;
-    uint8_t* codes;
-    float* norms;
     int* status;
 };
 
@@ -686,10 +689,12 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     s_hist[threadIdx.x] = 0u;
     __syncthreads();
+    const int stream = blockIdx.y;
+    const uint32_t* offsets = a.offsets.p[stream];
     const int64_t bb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     uint32_t key = 255u;
     if (bb < a.nbuckets) {
-        const uint32_t nw = a.offsets[bb + 1] - a.offsets[bb];
+        const uint32_t nw = offsets[bb + 1] - offsets[bb];
         key = nw < 255u ? nw : 255u;
     }
     const uint32_t pos = atomicAdd(s_hist + key, 1u);
@@ -710,17 +715,17 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     if (b >= a.nbuckets) return;
     const int64_t lo = b * a.d;
     const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
-    const uint32_t w_lo = a.offsets[b], w_hi = a.offsets[b + 1];
-    const uint32_t* src = a.words + w_lo;
+    const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
+    const uint32_t* src = a.words.p[stream] + w_lo;
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
     bool bad = avail == 0;
     auto word = [&](int64_t i) { return i < avail ? __ldg(src + i) : 0u; };
-    a.norms[b] = __uint_as_float(word(0));
+    a.norms.p[stream][b] = __uint_as_float(word(0));
     uint32_t whi = word(1), wlo = word(2), pre = word(3);
     int64_t next = 4;
     int have = 64;
     CodeWriter<FOUR> wr;
-    wr.out = reinterpret_cast<uint32_t*>(a.codes + (FOUR ? lo / 2 : lo));
+    wr.out = reinterpret_cast<uint32_t*>(a.codes.p[stream] + (FOUR ? lo / 2 : lo));
     auto consume = [&](int l) {
         whi = __funnelshift_l(wlo, whi, l);
         wlo <<= l;
@@ -849,23 +854,42 @@ int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int b
     return launch_status();
 }
 
-int qsgd_elias_decode(const uint32_t* words, const uint32_t* offsets, int64_t n, int bucket, int s_levels,
-                      uint8_t* codes, float* norms, int* d_status, gc_stream_t stream) {
-    if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127) return GC_ERR_INVALID;
+int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* const* offsets, int W,
+                              int64_t n, int bucket, int s_levels, uint8_t* const* codes,
+                              float* const* norms, int* d_status, gc_stream_t stream) {
+    if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127 || W < 1 || W > GC_MAX_WORKERS)
+        return GC_ERR_INVALID;
     if (n == 0) return GC_OK;
     if (!words || !offsets || !codes || !norms) return GC_ERR_INVALID;
-    if (!aligned16(words) || !aligned16(offsets) || !aligned16(codes) || !aligned16(norms) ||
-        (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)))
-        return GC_ERR_ALIGN;
+    if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return GC_ERR_ALIGN;
+    DecodeArgs a;
+    for (int w = 0; w < W; ++w) {
+        if (!words[w] || !offsets[w] || !codes[w] || !norms[w]) return GC_ERR_INVALID;
+        if (!aligned16(words[w]) || !aligned16(offsets[w]) || !aligned16(codes[w]) || !aligned16(norms[w]))
+            return GC_ERR_ALIGN;
+        a.words.p[w] = words[w];
+        a.offsets.p[w] = offsets[w];
+        a.codes.p[w] = codes[w];
+        a.norms.p[w] = norms[w];
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t nb = div_up(n, bucket);
-    DecodeArgs a{words, offsets, n, bucket, nb, s_levels, codes, norms, d_status};
-    const unsigned grid = static_cast<unsigned>(div_up(nb, kThreads));
+    a.n = n;
+    a.d = bucket;
+    a.nbuckets = nb;
+    a.s = s_levels;
+    a.status = d_status;
+    const dim3 grid(static_cast<unsigned>(div_up(nb, kThreads)), static_cast<unsigned>(W));
     if (s_levels <= 7)
         k_elias_decode<true><<<grid, kThreads, 0, s>>>(a);
     else
         k_elias_decode<false><<<grid, kThreads, 0, s>>>(a);
     return launch_status();
+}
+
+int qsgd_elias_decode(const uint32_t* words, const uint32_t* offsets, int64_t n, int bucket, int s_levels,
+                      uint8_t* codes, float* norms, int* d_status, gc_stream_t stream) {
+    return qsgd_elias_decode_batched(&words, &offsets, 1, n, bucket, s_levels, &codes, &norms, d_status, stream);
 }
 
 }  // extern "C"

@@ -351,6 +351,24 @@ GC_API int qsgd_elias_decode(const uint32_t *words, const uint32_t *offsets, int
                              int bucket, int s_levels, uint8_t *codes, float *norms,
                              int *d_status, gc_stream_t stream);
 
+/*
+ * qsgd_elias_decode_batched -- qsgd_elias_decode of W streams of the same n,
+ * bucket and s_levels (the W workers' messages a receiver decodes before
+ * their sum, Knowl 3) in one launch; stream w's results are those of
+ * qsgd_elias_decode on (words[w], offsets[w]).  The decoder gives one thread
+ * to each bucket, so W streams keep W times more of the GPU busy.
+ *   words, offsets, codes, norms   host arrays of W device pointers, each as
+ *                                  in qsgd_elias_decode
+ *   W          1 .. GC_MAX_WORKERS
+ *   d_status   device int or NULL, shared by the W streams
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_elias_decode_batched(const uint32_t *const *words,
+                                     const uint32_t *const *offsets, int W, int64_t n,
+                                     int bucket, int s_levels, uint8_t *const *codes,
+                                     float *const *norms, int *d_status,
+                                     gc_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* SAPS sparsified gossip + EASGD                                         */
 /* ---------------------------------------------------------------------- */

@@ -134,6 +134,14 @@ def test_elias_sizes_and_validation():
     assert _call(g, FAKE, FAKE, 10_000, 512, 7, FAKE, MISALIGNED, None, None) == gc.GC_ERR_ALIGN
     assert _call(g, FAKE, FAKE, 10_000, 512, 7, FAKE, FAKE, MISALIGNED + 1, None) == gc.GC_ERR_ALIGN
     assert _call(g, None, None, 0, 512, 7, None, None, None, None) == gc.GC_OK
+    h = "qsgd_elias_decode_batched"
+    two = _ptrs(FAKE, FAKE)
+    assert _call(h, two, two, 0, 10_000, 512, 7, two, two, None, None) == gc.GC_ERR_INVALID       # W = 0
+    assert _call(h, two, two, 65, 10_000, 512, 7, two, two, None, None) == gc.GC_ERR_INVALID      # W > 64
+    assert _call(h, two, _ptrs(FAKE, None), 2, 10_000, 512, 7, two, two, None, None) == gc.GC_ERR_INVALID
+    assert _call(h, two, two, 2, 10_000, 512, 7, _ptrs(FAKE, MISALIGNED), two, None, None) == gc.GC_ERR_ALIGN
+    assert _call(h, two, two, 2, 10_000, 500, 7, two, two, None, None) == gc.GC_ERR_INVALID
+    assert _call(h, None, None, 2, 0, 512, 7, None, None, None, None) == gc.GC_OK
 
 
 def test_saps_validation():

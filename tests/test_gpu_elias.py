@@ -85,6 +85,44 @@ def test_encode_decode_parity(cfg, n, bucket, s):
     np.testing.assert_array_equal(dn.view(np.uint32), rn.view(np.uint32))
 
 
+@pytest.mark.parametrize("cfg,n,bucket,s", [CASES[0], CASES[3], CASES[5]], ids=lambda x: getattr(x, "name", str(x)))
+def test_batched_decode_equals_the_single_decodes(cfg, n, bucket, s):
+    """Three workers' streams decoded in one launch: each equals the oracle's
+    decode of that worker's stream; a corrupt third stream flags the shared
+    status without changing the other two."""
+    nb = gc.qsgd_num_buckets(n, bucket)
+    cb = gc.qsgd_code_bytes(n, s)
+    streams, refs = [], []
+    for w in range(3):
+        _, norms, codes = _oracle_codes(cfg, n, bucket, s, worker=w)
+        ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+        words, offsets = _encode_gpu(codes, norms, n, bucket, s)
+        streams.append((words, offsets))
+        refs.append(oracle.qsgd_elias_decode(ref_w, ref_off, n, bucket, s))
+    out_c = [guarded(cb, torch.uint8) for _ in range(3)]
+    out_n = [guarded(nb, torch.float32) for _ in range(3)]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gc.qsgd_elias_decode_batched([w for w, _ in streams], [o[:nb + 1] for _, o in streams], n, bucket, s,
+                                 [c[:cb] for c in out_c], [m[:nb] for m in out_n], st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for w in range(3):
+        np.testing.assert_array_equal(out_c[w][:cb].cpu().numpy(), refs[w][0])
+        np.testing.assert_array_equal(host_f32(out_n[w][:nb]).view(np.uint32), refs[w][1].view(np.uint32))
+        check_guard(out_c[w], cb)
+        check_guard(out_n[w], nb)
+    # truncate the third stream's first bucket to its norm word: corrupt
+    bad_off = streams[2][1][:nb + 1].clone()
+    bad_off[1] = bad_off[0] + 1
+    bad_off[2:] = torch.maximum(bad_off[2:], bad_off[1])
+    gc.qsgd_elias_decode_batched([w for w, _ in streams], [streams[0][1][:nb + 1], streams[1][1][:nb + 1], bad_off],
+                                 n, bucket, s, [c[:cb] for c in out_c], [m[:nb] for m in out_n], st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == gc.GC_ERR_CORRUPT
+    for w in range(2):
+        np.testing.assert_array_equal(out_c[w][:cb].cpu().numpy(), refs[w][0])
+
+
 def test_empty():
     offsets = torch.full((4,), 7, dtype=torch.int32, device=DEV)
     words = torch.zeros(4, dtype=torch.int32, device=DEV)
