@@ -220,6 +220,15 @@ class QSGD:
         from . import qsgd_elias_decode
         qsgd_elias_decode(words, offsets, self.n, self.bucket, self.s, self.codes[worker], self.norms[worker])
 
+    def decode_all(self, streams) -> None:
+        """Replace every worker's message by its decoded stream, streams[w] =
+        (words, offsets), in one launch."""
+        from . import qsgd_elias_decode_batched
+        if len(streams) != self.W:
+            raise ValueError(f"expected {self.W} streams")
+        qsgd_elias_decode_batched([w for w, _ in streams], [o for _, o in streams], self.n, self.bucket, self.s,
+                                  self.codes, self.norms)
+
 
 class SAPSGossip:
     """SAPS rounds for W workers held on this GPU ("Communication-Efficient

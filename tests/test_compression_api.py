@@ -95,6 +95,15 @@ def test_qsgd_front_end_round_trip():
     gc.qsgd_dequant_sum(c1, n1, n, 512, 22, 1.0 / W, ref)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+    # every worker's stream decoded in one launch
+    streams = [q.encode(w) for w in range(W)]
+    for x in q.codes + q.norms:
+        x.zero_()
+    q.decode_all(streams)
+    torch.cuda.synchronize()
+    for w in range(W):
+        assert torch.equal(q.norms[w], n1[w])
+        assert torch.equal(lv(q.codes[w]), lv(c1[w]))
 
 
 @pytest.mark.gpu
