@@ -153,15 +153,16 @@ def test_cdsgd_rules():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_cdsgd_eight_steps_against_oracle(dtype):
+@pytest.mark.parametrize("dtype,k", [(torch.float32, 4), (torch.bfloat16, 4), (torch.float32, 3), (torch.float32, 1)])
+def test_cdsgd_eight_steps_against_oracle(dtype, k):
     """k = 4: steps 1-3 and 5-7 compressed (with eq. 11 local weights),
-    steps 4 and 8 residual-compensated full precision; codes and residuals
-    bit-exact, weights and local weights within the float tolerance."""
+    steps 4 and 8 residual-compensated full precision (k = 3: steps 3 and 6;
+    k = 1: every step); codes and residuals bit-exact, weights and local
+    weights within the float tolerance."""
     from gradient_compression_sgd_gc_gb300.compression import CDSGD
     dev = "cuda"
     n, W, t, lr, llr = 70_001, 3, 1e-3, 0.01, 0.1
-    cd = CDSGD(n, W, t, lr, k=4, local_lr=llr, device=dev)
+    cd = CDSGD(n, W, t, lr, k=k, local_lr=llr, device=dev)
     weights = wl.uniform(n, 0.05, 11, device=dev)
     w_ref = weights.cpu().numpy().astype(np.float64)
     r_ref = [np.zeros(n, np.float32) for _ in range(W)]
@@ -173,7 +174,7 @@ def test_cdsgd_eight_steps_against_oracle(dtype):
         w_before = w_ref.copy()
         corr = cd.step(grads, weights, local)
         torch.cuda.synchronize()
-        assert corr == (step % 4 == 0)
+        assert corr == (step % k == 0)
         if corr:
             oracle.compensated_sum_update(hg, r_ref, lr, w_ref)
             for w in range(W):

@@ -123,6 +123,32 @@ def test_batched_decode_equals_the_single_decodes(cfg, n, bucket, s):
         np.testing.assert_array_equal(out_c[w][:cb].cpu().numpy(), refs[w][0])
 
 
+def test_batched_decode_of_sixty_four_streams():
+    """The largest batch (GC_MAX_WORKERS streams) of short ragged streams."""
+    cfg, n, bucket, s = wl.QSGD_S7, 2 * 128 + 37, 128, 7
+    nb = gc.qsgd_num_buckets(n, bucket)
+    cb = gc.qsgd_code_bytes(n, s)
+    words, offs, refs = [], [], []
+    for w in range(gc.GC_MAX_WORKERS):
+        _, norms, codes = _oracle_codes(cfg, n, bucket, s, worker=w)
+        ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+        words.append(torch.from_numpy(ref_w.view(np.int32)).to(DEV))
+        offs.append(torch.from_numpy(ref_off.view(np.int32)).to(DEV))
+        refs.append(oracle.qsgd_elias_decode(ref_w, ref_off, n, bucket, s))
+    out_c = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(gc.GC_MAX_WORKERS)]
+    out_n = [torch.empty(nb, device=DEV) for _ in range(gc.GC_MAX_WORKERS)]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gc.qsgd_elias_decode_batched(words, offs, n, bucket, s, out_c, out_n, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for w in range(gc.GC_MAX_WORKERS):
+        np.testing.assert_array_equal(out_c[w].cpu().numpy(), refs[w][0])
+        np.testing.assert_array_equal(host_f32(out_n[w]).view(np.uint32), refs[w][1].view(np.uint32))
+    with pytest.raises(gc.GcError):
+        gc.qsgd_elias_decode_batched(words + words[:1], offs + offs[:1], n, bucket, s, out_c + out_c[:1],
+                                     out_n + out_n[:1], st)
+
+
 def test_empty():
     offsets = torch.full((4,), 7, dtype=torch.int32, device=DEV)
     words = torch.zeros(4, dtype=torch.int32, device=DEV)
