@@ -134,10 +134,40 @@ struct QArgs {
 // -inf to an unsigned integer; +inf saturates, so min() gives s); a NaN y
 // (0 * inf: a zero coordinate in a bucket whose s / norm overflows) converts
 // to 0, the level of a zero coordinate.
-__device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint64_t key) {
+__device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint32_t top24) {
     const float a = __fmul_rn(fabsf(x), S);
-    const float y = __fmaf_rn(__uint2float_rn(splitmix64_top24(key)), 5.9604644775390625e-8f, a);
+    const float y = __fmaf_rn(__uint2float_rn(top24), 5.9604644775390625e-8f, a);
     return min(__float2uint_rd(y), s);
+}
+
+// splitmix64_top24 of the four keys kbase ^ k (k = 0..3), sharing what the
+// four have in common: they differ only in their low two bits, so
+// x_k = x0 + j_k with x0 = kbase & ~3 and j_k = (kbase & 3) ^ k.  While
+// z0 = x0 + golden has no carry out of its low word for j_k <= 3, the four z
+// have the same high word, and so does the high word of z ^ (z >> 30); its
+// share of the first product is computed once.  A group whose low word would
+// carry takes the plain function (one group in about 2^30).
+__device__ __forceinline__ void hash4_top24(uint64_t kbase, uint32_t (&t)[4]) {
+    constexpr uint64_t kC1 = 0xBF58476D1CE4E5B9ull;
+    constexpr uint64_t kC2 = 0x94D049BB133111EBull;
+    const uint64_t z0 = (kbase & ~3ull) + 0x9E3779B97F4A7C15ull;
+    const uint32_t z0l = static_cast<uint32_t>(z0), zh = static_cast<uint32_t>(z0 >> 32);
+    const uint32_t jb = static_cast<uint32_t>(kbase) & 3u;
+    if (z0l > 0xFFFFFFFCu) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] = splitmix64_top24(kbase ^ static_cast<uint64_t>(k));
+        return;
+    }
+    const uint32_t yh = zh ^ (zh >> 30);                               // high word of z ^ (z >> 30)
+    const uint64_t yh_part = static_cast<uint64_t>(yh * static_cast<uint32_t>(kC1)) << 32;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t zl = z0l + (jb ^ static_cast<uint32_t>(k));
+        const uint32_t yl = zl ^ __funnelshift_r(zl, zh, 30);              // low word of z ^ (z >> 30)
+        const uint64_t p = static_cast<uint64_t>(yl) * kC1 + yh_part;      // (yh:yl) * C1 mod 2^64
+        const uint64_t q = p ^ (p >> 27);
+        t[k] = static_cast<uint32_t>((q * kC2) >> 40);
+    }
 }
 
 // True when every value of the warp's bucket registers is +-0.
@@ -244,9 +274,11 @@ __device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int l
         const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
         uint32_t c[4] = {0u, 0u, 0u, 0u};
         if (!zero) {
+            uint32_t t[4];
+            hash4_top24(kbase, t);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint32_t lvl = qlevel(xs[k], S, s_u, kbase ^ static_cast<uint64_t>(k));
+                const uint32_t lvl = qlevel(xs[k], S, s_u, t[k]);
                 c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
             }
         }
@@ -280,11 +312,11 @@ __device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int l
 }
 
 // One warp per bucket; the grid covers every bucket.  For buckets of up to
-// 512 the register bound allows 8 CTAs (64 warps) per SM: the quantiser is
-// issue- and latency-bound, and full occupancy measured 5-6% faster than 4
-// CTAs per SM despite a few spilled registers.
+// 512 the register bound allows 6 CTAs (48 warps) per SM with no spills: the
+// quantiser is bound by the integer ALU pipe and latency, and 6 measured
+// ahead of 4 (56 registers) and of 8 (32 registers and spills).
 template <int ROUNDS, bool FOUR, bool MAXNORM>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 8)
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 6)
 k_qsgd_quantize(const QArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
