@@ -140,6 +140,36 @@ __device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint32_
     return min(__float2uint_rd(y), s);
 }
 
+// splitmix64_top24 of the four keys kbase ^ k (k = 0..3), sharing what the
+// four have in common: they differ only in their low two bits, so
+// x_k = x0 + j_k with x0 = kbase & ~3 and j_k = (kbase & 3) ^ k.  While
+// z0 = x0 + golden has no carry out of its low word for j_k <= 3, the four z
+// have the same high word, and so does the high word of z ^ (z >> 30); its
+// share of the first product is computed once.  A group whose low word would
+// carry takes the plain function (one group in about 2^30).
+__device__ __forceinline__ void hash4_top24(uint64_t kbase, uint32_t (&t)[4]) {
+    constexpr uint64_t kC1 = 0xBF58476D1CE4E5B9ull;
+    constexpr uint64_t kC2 = 0x94D049BB133111EBull;
+    const uint64_t z0 = (kbase & ~3ull) + 0x9E3779B97F4A7C15ull;
+    const uint32_t z0l = static_cast<uint32_t>(z0), zh = static_cast<uint32_t>(z0 >> 32);
+    const uint32_t jb = static_cast<uint32_t>(kbase) & 3u;
+    if (z0l > 0xFFFFFFFCu) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] = splitmix64_top24(kbase ^ static_cast<uint64_t>(k));
+        return;
+    }
+    const uint32_t yh = zh ^ (zh >> 30);                               // high word of z ^ (z >> 30)
+    const uint64_t yh_part = static_cast<uint64_t>(yh * static_cast<uint32_t>(kC1)) << 32;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t zl = z0l + (jb ^ static_cast<uint32_t>(k));
+        const uint32_t yl = zl ^ __funnelshift_r(zl, zh, 30);              // low word of z ^ (z >> 30)
+        const uint64_t p = static_cast<uint64_t>(yl) * kC1 + yh_part;      // (yh:yl) * C1 mod 2^64
+        const uint64_t q = p ^ (p >> 27);
+        t[k] = static_cast<uint32_t>((q * kC2) >> 40);
+    }
+}
+
 // True when every value of the warp's bucket registers is +-0.
 template <int ROUNDS>
 __device__ __forceinline__ bool all_zero(const float4 (&v)[ROUNDS], int lane) {
