@@ -139,14 +139,17 @@ def dram_roofline(kernel: str, ms_list, peak: float):
             "peak": peak, "unit": "GB/s", "frac": round(gbps / peak, 3)}
 
 
-def issue_roofline(kernel: str, ms_list):
+def issue_roofline(kernel: str, ms_list, mult: int = 1):
+    """Issue rate of a launch doing `mult` times the captured kernel's work
+    (e.g. a batched call over `mult` streams)."""
     d = ncu_entry(kernel)
     if not d or "warp_inst_per_launch" not in d or not ms_list:
         return None
-    rate = float(d["warp_inst_per_launch"]) / (_median(ms_list) * 1e-3)
+    inst = mult * float(d["warp_inst_per_launch"])
+    rate = inst / (_median(ms_list) * 1e-3)
     return {"bound": "issue", "achieved": round(rate / 1e12, 4), "peak": round(ISSUE_PEAK / 1e12, 4),
             "unit": "T warp instructions/s", "frac": round(rate / ISSUE_PEAK, 3),
-            "warp_inst_per_launch": int(d["warp_inst_per_launch"])}
+            "warp_inst_per_launch": int(inst)}
 
 
 class ClockSampler:
@@ -644,7 +647,8 @@ def rows(args, dev, peak):
         torch.cuda.synchronize(dev)
         out[f"{qcfg.name}.elias_decode_batched"] = _row(
             qcfg.name, f"qsgd_elias_decode_batched ({W} streams, one launch)",
-            W * (4 * total + 4 * (nb + 1) + cb + 4 * nb), tm.ms("b"), peak, W * n)
+            W * (4 * total + 4 * (nb + 1) + cb + 4 * nb), tm.ms("b"), peak, W * n,
+            {"issue": issue_roofline(f"elias_decode_s{s}", tm.ms("b"), mult=W)})
         del vs, norms, codes, outq, words, offs, ews, dcodes, dnorms, bcodes, bnorms
 
     # config 5: SAPS + EASGD, 16 workers x 25,557,032, p = 0.01 and 0.001
