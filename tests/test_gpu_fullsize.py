@@ -153,3 +153,44 @@ def _full_mask_count(n, p, seed_t):
     """The oracle's masked count over all n indices (one worker of zeros)."""
     K, _, _ = oracle.saps_mask_compact(n, p, seed_t, [np.zeros(n)], capacity=0)
     return K
+
+
+def test_indices_beyond_two_to_the_32():
+    """64-bit indexing: 2^32 + 3000 elements (17 GB per fp32 buffer).  The QSGD
+    buckets and the 2-bit words just below and above element 2^32, and the last
+    ones, equal the oracle's at their global indices (the hash keys' high words
+    change there)."""
+    n = (1 << 32) + 3000
+    free, _ = torch.cuda.mem_get_info()
+    if free < (48 << 30):
+        pytest.skip("needs about 48 GB of free device memory")
+    v = torch.empty(n, device=DEV)
+    chunk = 1 << 28
+    for i, c0 in enumerate(range(0, n, chunk)):
+        c1 = min(n, c0 + chunk)
+        wl.normal(c1 - c0, 1e-2, 9000 + i, device=DEV, out=v[c0:c1])
+    d, s, seed, worker = 512, 127, 77, 1
+    nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
+    norms = torch.empty(nb, device=DEV)
+    codes = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    gc.qsgd_quantize(v, d, s, seed, worker, norms, codes)
+    torch.cuda.synchronize()
+    for b0 in ((1 << 32) // d - 3, nb - 4):
+        lo, hi = b0 * d, min(n, (b0 + 6) * d)
+        vh = host_f32(v[lo:hi])
+        rn, rc = oracle.qsgd_quantize(vh, d, s, seed, worker, i0=lo)
+        np.testing.assert_array_equal(host_f32(norms[b0:b0 + rn.size]).view(np.uint32), rn.view(np.uint32))
+        compare_codes(codes[lo:hi].cpu().numpy(), rc, vh, hi - lo, d, s, seed, worker, i0=lo)
+    del norms, codes
+    t = 1e-2
+    res = torch.zeros(n, device=DEV)
+    words = torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV)
+    gc.gc_2bit_quantize(v, res, words, t)
+    torch.cuda.synchronize()
+    for lo, hi in (((1 << 32) - 1024, (1 << 32) + 1024), (n - 1000 - (n - 1000) % 16, n)):
+        r_ref = np.zeros(hi - lo, np.float32)
+        c_ref = oracle.twobit_quantize(host_f32(v[lo:hi]), r_ref, t)
+        np.testing.assert_array_equal(host_u32(words[lo // 16:lo // 16 + c_ref.size]), c_ref)
+        np.testing.assert_array_equal(host_f32(res[lo:hi]).view(np.uint32), r_ref.view(np.uint32))
+    del res, words, v
+    torch.cuda.empty_cache()
