@@ -194,3 +194,44 @@ def test_indices_beyond_two_to_the_32():
         np.testing.assert_array_equal(host_f32(res[lo:hi]).view(np.uint32), r_ref.view(np.uint32))
     del res, words, v
     torch.cuda.empty_cache()
+
+
+def test_saps_mask_at_the_largest_n():
+    """n = 2^32 - 1, the largest count uint32 indices allow (two workers of
+    17 GB): indices stay ascending and below n, and every sampled range --
+    the first, the last and ones in between -- holds exactly the oracle's
+    indices and gathered values for that range."""
+    n, W, p = (1 << 32) - 1, 2, 1e-4
+    free, _ = torch.cuda.mem_get_info()
+    if free < (40 << 30):
+        pytest.skip("needs about 40 GB of free device memory")
+    models = [torch.empty(n, device=DEV) for _ in range(W)]
+    chunk = 1 << 28
+    for w in range(W):
+        for i, c0 in enumerate(range(0, n, chunk)):
+            c1 = min(n, c0 + chunk)
+            wl.normal(c1 - c0, 0.05, 7000 + 100 * w + i, device=DEV, out=models[w][c0:c1])
+    cap = int(n * p * 1.2) + 10_000
+    idx = torch.empty(cap, dtype=torch.int32, device=DEV)
+    vals = [torch.empty(cap, device=DEV) for _ in range(W)]
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(gc.saps_workspace_bytes(n), dtype=torch.uint8, device=DEV)
+    seed_t = gc.saps_round_seed(11, 3)
+    gc.saps_mask_compact(n, p, seed_t, models, idx, vals, cnt, ws, st)
+    torch.cuda.synchronize()
+    K = int(cnt.item())
+    assert int(st.item()) == 0 and 0 < K <= cap
+    gi = host_u32(idx[:K]).astype(np.int64)
+    assert np.all(np.diff(gi) > 0) and gi[-1] < n
+    gv = [host_f32(v[:K]) for v in vals]
+    for lo, hi in sample_chunks(n, 6, 1 << 22, align=4096, seed=5):
+        ref = [host_f32(m[lo:hi]).astype(np.float64) for m in models]
+        Kc, ridx, rvals = oracle.saps_mask_compact(hi - lo, p, seed_t, ref, i0=lo)
+        a, b = np.searchsorted(gi, lo), np.searchsorted(gi, hi)
+        assert b - a == Kc
+        np.testing.assert_array_equal(gi[a:b], ridx.astype(np.int64))
+        for w in range(W):
+            np.testing.assert_array_equal(gv[w][a:b].astype(np.float64), rvals[w])
+    del models, idx, vals, ws
+    torch.cuda.empty_cache()
