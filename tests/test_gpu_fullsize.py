@@ -235,3 +235,48 @@ def test_saps_mask_at_the_largest_n():
             np.testing.assert_array_equal(gv[w][a:b].astype(np.float64), rvals[w])
     del models, idx, vals, ws
     torch.cuda.empty_cache()
+
+
+def test_elias_beyond_two_to_the_32():
+    """The Elias codec on 2^32 + 3000 QSGD s=7 coordinates: offsets stay
+    32-bit word indices; sampled buckets' words equal the oracle's encoding
+    of the same codes; the decode gives the levels back everywhere."""
+    n, d, s = (1 << 32) + 3000, 512, 7
+    free, _ = torch.cuda.mem_get_info()
+    if free < (40 << 30):
+        pytest.skip("needs about 40 GB of free device memory")
+    nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
+    codes = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    norms = torch.empty(nb, device=DEV)
+    v = torch.empty(1 << 28, device=DEV)
+    for i, c0 in enumerate(range(0, n, 1 << 28)):       # quantise in slices: v is not kept whole
+        c1 = min(n, c0 + (1 << 28))
+        wl.normal(c1 - c0, 1e-2, 9500 + i, device=DEV, out=v[:c1 - c0])
+        gc.qsgd_quantize(v[:c1 - c0], d, s, 5, 0, norms[c0 // d:(c1 + d - 1) // d], codes[c0 // 2:(c1 + 1) // 2])
+    del v
+    cap = gc.qsgd_elias_max_words(n, d, s)
+    words = torch.empty(cap, dtype=torch.int32, device=DEV)
+    offs = torch.empty(nb + 1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(gc.qsgd_elias_workspace_bytes(n, d), dtype=torch.uint8, device=DEV)
+    gc.qsgd_elias_encode(codes, norms, n, d, s, words, offs, ws)
+    torch.cuda.synchronize()
+    ho = host_u32(offs).astype(np.int64)
+    assert np.all(np.diff(ho) >= 2)
+    for b0 in (0, (1 << 32) // d - 2, nb - 3):
+        b1 = min(nb, b0 + 3)
+        lo, hi = b0 * d, min(n, b1 * d)
+        rc = codes[lo // 2:(hi + 1) // 2].cpu().numpy()
+        rn = host_f32(norms[b0:b1])
+        ref_w, ref_off = oracle.qsgd_elias_encode(rc, rn, hi - lo, d, s)
+        np.testing.assert_array_equal(ho[b0:b1 + 1] - ho[b0], ref_off.astype(np.int64))
+        np.testing.assert_array_equal(host_u32(words[int(ho[b0]):int(ho[b1])]), ref_w)
+    dc = torch.empty_like(codes)
+    dn = torch.empty_like(norms)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gc.qsgd_elias_decode(words, offs, n, d, s, dc, dn, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(dn, norms)
+    assert torch.equal(dc & 0x77, codes & 0x77)          # levels; a level-0 code comes back with sign 0
+    del codes, norms, words, offs, ws, dc, dn
+    torch.cuda.empty_cache()
