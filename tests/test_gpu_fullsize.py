@@ -187,12 +187,22 @@ def test_indices_beyond_two_to_the_32():
     words = torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV)
     gc.gc_2bit_quantize(v, res, words, t)
     torch.cuda.synchronize()
-    for lo, hi in (((1 << 32) - 1024, (1 << 32) + 1024), (n - 1000 - (n - 1000) % 16, n)):
+    ranges = (((1 << 32) - 1024, (1 << 32) + 1024), (n - 1000 - (n - 1000) % 16, n))
+    refs = []
+    for lo, hi in ranges:
         r_ref = np.zeros(hi - lo, np.float32)
         c_ref = oracle.twobit_quantize(host_f32(v[lo:hi]), r_ref, t)
         np.testing.assert_array_equal(host_u32(words[lo // 16:lo // 16 + c_ref.size]), c_ref)
         np.testing.assert_array_equal(host_f32(res[lo:hi]).view(np.uint32), r_ref.view(np.uint32))
-    del res, words, v
+        refs.append(c_ref)
+    del v
+    # the dequantised values (one worker) into the residual buffer
+    gc.gc_2bit_dequant_sum_update([words], n, t, gc.GC_UPD_NONE, out=res)
+    torch.cuda.synchronize()
+    for (lo, hi), c_ref in zip(ranges, refs):
+        a_ref = oracle.twobit_dequant_sum_update([c_ref], hi - lo, t, oracle.KIND_NONE)
+        assert_close(host_f32(res[lo:hi]), a_ref, np.full(hi - lo, t), what="dequantised")
+    del res, words
     torch.cuda.empty_cache()
 
 
