@@ -19,7 +19,9 @@
 // Decode: one thread per bucket walks its stream with a 64-bit window; an
 // 11-bit (4-bit codes) or 12-bit (8-bit codes) lookahead table, built by the
 // compiler, decodes up to 8 or 4 whole codewords per step, and an 8-bit one
-// the rest.
+// the rest; each CTA first copies its buckets' words to shared memory.
+#include <atomic>
+
 #include "gc_common.cuh"
 
 namespace gc {
@@ -534,6 +536,7 @@ struct DecodeArgs {
     int64_t nbuckets;
     int s;
     int* status;
+    uint32_t stage_cap;   // stream words a CTA stages in shared memory
 };
 
 // Lookahead bits of the multi-codeword table: 11 for 4-bit codes, 12 for
@@ -668,6 +671,7 @@ struct CodeWriter {
 // `have` valid bits from the top, the next word waiting in `pre`).
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
+    extern __shared__ uint32_t s_words[];   // a.stage_cap words
     constexpr int KMAX = FOUR ? 8 : 4;
     constexpr int W = win_bits<FOUR>();
     __shared__ __align__(16) uint64_t multi[1 << W];
@@ -676,7 +680,16 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     {
         const uint4* src = reinterpret_cast<const uint4*>(FOUR ? kMulti4.e : kMulti8.e);
         uint4* dst = reinterpret_cast<uint4*>(multi);
-        for (int i = threadIdx.x; i < (1 << W) / 2; i += blockDim.x) dst[i] = __ldg(src + i);
+        // A window holding a level above s gets count 0, which sends it to
+        // the one-codeword path (where that level is flagged): the main loop
+        // then tests only the count.  Entries are (packed << 32) | meta, meta
+        // = (max level << 8) | (count << 4) | bits.
+        for (int i = threadIdx.x; i < (1 << W) / 2; i += blockDim.x) {
+            uint4 v = __ldg(src + i);
+            if (((v.x >> 8) & 127u) > smax) v.x &= ~0xF0u;
+            if (((v.z >> 8) & 127u) > smax) v.z &= ~0xF0u;
+            dst[i] = v;
+        }
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x) single[i] = window_entry<8>(static_cast<uint32_t>(i));
     // The CTA's 256 buckets are handed to its threads in order of stream
@@ -710,16 +723,37 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     s_hist[threadIdx.x] = start;                 // bin starts
     __syncthreads();
     s_order[s_hist[key] + pos] = static_cast<uint16_t>(threadIdx.x);
+    // The CTA's words, offsets[b0] .. offsets[b0 + cnt) (at most stage_cap of
+    // them), are copied to shared memory with coalesced loads, so that the
+    // walks below read from there.  Every word of that range lies inside the
+    // range of one of the CTA's buckets, whatever the offsets: the copy reads
+    // nothing a bucket would not.
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * blockDim.x;
+    const int64_t cnt = a.nbuckets - b0 < kThreads ? a.nbuckets - b0 : kThreads;
+    const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
+    const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
+    const uint32_t* gwords = a.words.p[stream];
+    for (uint32_t i = threadIdx.x; i < nst; i += 4 * kThreads) {
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = i + j * kThreads < nst ? __ldg(gwords + base + i + j * kThreads) : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (i + j * kThreads < nst) s_words[i + j * kThreads] = v[j];
+    }
     __syncthreads();
-    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + s_order[threadIdx.x];
+    const int64_t b = b0 + s_order[threadIdx.x];
     if (b >= a.nbuckets) return;
     const int64_t lo = b * a.d;
     const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
     const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
-    const uint32_t* src = a.words.p[stream] + w_lo;
+    // a bucket wholly inside the staged words reads shared memory (through a
+    // generic pointer), any other bucket global memory
+    const bool staged = w_lo - base <= nst && w_hi - base <= nst;
+    const uint32_t* src = staged ? s_words + (w_lo - base) : gwords + w_lo;
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
     bool bad = avail == 0;
-    auto word = [&](int64_t i) { return i < avail ? __ldg(src + i) : 0u; };
+    auto word = [&](int64_t i) { return i < avail ? src[i] : 0u; };
     a.norms.p[stream][b] = __uint_as_float(word(0));
     uint32_t whi = word(1), wlo = word(2), pre = word(3);
     int64_t next = 4;
@@ -774,7 +808,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
         int k = static_cast<int>((t >> 4) & 15u);
         int l = static_cast<int>(t & 15u);
         uint32_t packed = static_cast<uint32_t>(t >> 32);
-        if (k == 0 || ((t >> 8) & 127u) > smax) {
+        if (k == 0) {
             // a codeword longer than the window, or a level above s
             one_code(packed, l);
             k = 1;
@@ -794,6 +828,42 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     // bits consumed: the words fetched (norm included, `pre` not) minus those still in the window
     if (32 * (next - 1) - have > 32 * avail) bad = true;
     if (bad && a.status) *a.status = GC_ERR_CORRUPT;
+}
+
+// Stream words one decoding CTA stages: the shared memory left, after the
+// kernel's static tables and the per-CTA reservation, when four CTAs share an
+// SM (one stream of 61 M coordinates needs 3.4 CTAs per SM of the 152).
+// Computed once per device, which also raises the kernel's dynamic
+// shared-memory limit there.
+constexpr int kDecodeCtasPerSm = 4;
+constexpr int kMaxDevices = 64;
+
+template <bool FOUR>
+int decode_stage_words(uint32_t* cap) {
+    static std::atomic<uint32_t> cached[kMaxDevices];   // words + 1; 0 = not yet known
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GC_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const uint32_t c = cached[dev].load(std::memory_order_relaxed);
+        if (c) {
+            *cap = c - 1;
+            return GC_OK;
+        }
+    }
+    int per_sm = 0, reserved = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, k_elias_decode<FOUR>) != cudaSuccess)
+        return GC_ERR_CUDA;
+    int64_t bytes = static_cast<int64_t>(per_sm) / kDecodeCtasPerSm - reserved - static_cast<int64_t>(fa.sharedSizeBytes);
+    bytes = bytes > 0 ? bytes & ~static_cast<int64_t>(15) : 0;
+    if (cudaFuncSetAttribute(k_elias_decode<FOUR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes)) != cudaSuccess)
+        return GC_ERR_CUDA;
+    *cap = static_cast<uint32_t>(bytes / sizeof(uint32_t));
+    if (dev >= 0 && dev < kMaxDevices) cached[dev].store(*cap + 1, std::memory_order_relaxed);
+    return GC_OK;
 }
 
 }  // namespace
@@ -880,10 +950,14 @@ int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* cons
     a.s = s_levels;
     a.status = d_status;
     const dim3 grid(static_cast<unsigned>(div_up(nb, kThreads)), static_cast<unsigned>(W));
-    if (s_levels <= 7)
-        k_elias_decode<true><<<grid, kThreads, 0, s>>>(a);
+    const bool four = s_levels <= 7;
+    const int rc = four ? decode_stage_words<true>(&a.stage_cap) : decode_stage_words<false>(&a.stage_cap);
+    if (rc != GC_OK) return rc;
+    const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
+    if (four)
+        k_elias_decode<true><<<grid, kThreads, dyn, s>>>(a);
     else
-        k_elias_decode<false><<<grid, kThreads, 0, s>>>(a);
+        k_elias_decode<false><<<grid, kThreads, dyn, s>>>(a);
     return launch_status();
 }
 
