@@ -792,15 +792,23 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
         code = FOUR ? (sign << 3) | (level & 7u) : (sign << 7) | level;
         l = static_cast<int>(k) + 7;
     };
-    // One codeword through the 8-bit table, or the long-codeword formula.
+    // One codeword through the 8-bit table, or the long-codeword formula.  A
+    // level above s is flagged and written as s; its codeword's own length is
+    // consumed, so that the codes after it still decode in step.
     auto one_code = [&](uint32_t& code, int& l) {
         const uint32_t t = single[whi >> 24];
-        l = static_cast<int>(t & 15u);
-        const uint32_t level = t >> 5, sign = level ? (t >> 4) & 1u : 0u;
-        if (t && level <= smax)
+        if (t) {
+            l = static_cast<int>(t & 15u);
+            uint32_t level = t >> 5;
+            const uint32_t sign = level ? (t >> 4) & 1u : 0u;
+            if (level > smax) {
+                bad = true;
+                level = smax;
+            }
             code = FOUR ? (sign << 3) | level : (sign << 7) | level;
-        else
+        } else {
             long_code(code, l);
+        }
     };
     int e = 0;
     while (len - e >= KMAX) {

@@ -344,7 +344,10 @@ GC_API size_t qsgd_elias_workspace_bytes(int64_t n, int bucket);
  * offsets[b+1]); missing bits read as zeros.
  *   d_status   device int or NULL; set to GC_ERR_CORRUPT when a bucket's
  *              codewords run past its words, a level exceeds s_levels (it is
- *              written as s_levels) or a bucket has no norm word
+ *              written as s_levels, with its sign, and the codes after it
+ *              decode as they would otherwise), a codeword is not an
+ *              Elias-omega codeword of at most 8 binary digits, or a bucket
+ *              has no norm word
  * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
  */
 GC_API int qsgd_elias_decode(const uint32_t *words, const uint32_t *offsets, int64_t n,

@@ -255,6 +255,86 @@ def test_corrupt_streams_are_reported():
     assert st == 0
 
 
+def _levels_signs(codes, n, s):
+    """Per-coordinate (level, sign) of a code array in qsgd_quantize's layout."""
+    if s <= 7:
+        c = np.empty(n, dtype=np.uint8)
+        c[0::2] = codes[:(n + 1) // 2] >> 4
+        c[1::2] = codes[:n // 2] & 15
+        return c & 7, c >> 3
+    return codes[:n] & 127, codes[:n] >> 7
+
+
+def _pack(level, sign, s):
+    level = level.astype(np.uint8)
+    sign = sign.astype(np.uint8)
+    n = level.size
+    if s <= 7:
+        c = (sign << 3) | level
+        out = (c[0::2] << 4).astype(np.uint8)
+        out[:n // 2] |= c[1::2]
+        return out
+    return (sign << 7) | level
+
+
+@pytest.mark.parametrize("cfg,n,bucket,s,s_dec", [
+    (wl.QSGD_S127, 512 * 40 + 77, 512, 127, 22),
+    (wl.QSGD_S127, 512 * 40 + 77, 512, 127, 7),    # 8-bit stream into 4-bit codes
+    (wl.QSGD_S127, 256 * 50 + 3, 256, 127, 1),
+    (wl.QSGD_S7, 512 * 40 + 77, 512, 7, 3),
+    (wl.QSGD_S7, 128 * 90 + 1, 128, 7, 1),
+], ids=lambda x: getattr(x, "name", str(x)))
+def test_levels_above_s_are_clamped_in_step(cfg, n, bucket, s, s_dec):
+    """A stream decoded with a smaller s: every level above it is written as
+    s (sign kept), the status says GC_ERR_CORRUPT, and every other code is
+    the oracle's -- the decoder stays in step with the codewords.  The
+    expected codes are the oracle decoder's, clamped."""
+    _, norms, codes = _oracle_codes(cfg, n, bucket, s)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    ref_codes, ref_norms = oracle.qsgd_elias_decode(ref_w, ref_off, n, bucket, s)
+    level, sign = _levels_signs(ref_codes, n, s)
+    assert int(level.max()) > s_dec
+    want = _pack(np.minimum(level, s_dec), sign, s_dec)
+    words = torch.from_numpy(ref_w.view(np.int32)).to(DEV)
+    offsets = torch.from_numpy(ref_off.view(np.int32)).to(DEV)
+    dc, dn, st = _decode_gpu(words, offsets, n, bucket, s_dec)
+    assert st == gc.GC_ERR_CORRUPT
+    np.testing.assert_array_equal(dn.view(np.uint32), ref_norms.view(np.uint32))
+    np.testing.assert_array_equal(dc, want)
+
+
+@pytest.mark.parametrize("cfg,n,bucket,s,most", [
+    (wl.QSGD_S7, 512 * 600 + 41, 512, 7, 40),      # 3 CTAs of 256 buckets
+    (wl.QSGD_S127, 512 * 600 + 41, 512, 127, 40),
+    (wl.QSGD_S127, 128 * 1500 + 9, 128, 127, 300),  # CTAs whose words outgrow the shared copy
+], ids=lambda x: getattr(x, "name", str(x)))
+def test_words_after_a_bucket_are_ignored(cfg, n, bucket, s, most):
+    """Buckets followed by 0..most random words (offsets still mark each
+    bucket's first word): the decoder reads only what the codewords need, so
+    codes, norms and status are those of the packed stream -- whichever
+    buckets of a CTA its shared-memory copy holds."""
+    _, norms, codes = _oracle_codes(cfg, n, bucket, s)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    ref_codes, ref_norms = oracle.qsgd_elias_decode(ref_w, ref_off, n, bucket, s)
+    rng = np.random.default_rng(11)
+    nb = ref_off.size - 1
+    pad = rng.integers(0, most + 1, size=nb)
+    parts, offs, pos = [], [0], 0
+    for b in range(nb):
+        body = ref_w[ref_off[b]:ref_off[b + 1]]
+        junk = rng.integers(0, 2**32, size=int(pad[b]), dtype=np.uint64).astype(np.uint32)
+        parts += [body, junk]
+        pos += body.size + junk.size
+        offs.append(pos)
+    words_h = np.concatenate(parts)
+    off_h = np.asarray(offs, dtype=np.uint32)
+    dc, dn, st = _decode_gpu(torch.from_numpy(words_h.view(np.int32)).to(DEV),
+                             torch.from_numpy(off_h.view(np.int32)).to(DEV), n, bucket, s)
+    assert st == 0
+    np.testing.assert_array_equal(dn.view(np.uint32), ref_norms.view(np.uint32))
+    np.testing.assert_array_equal(dc, ref_codes)
+
+
 @pytest.mark.parametrize("cfg", [wl.QSGD_S7, wl.QSGD_S127], ids=lambda c: c.name)
 def test_full_size_stream_bit_exact(cfg):
     """The QSGD workload at full size (61,100,840 coordinates, 119,338
