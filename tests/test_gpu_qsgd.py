@@ -116,7 +116,20 @@ def test_norms_bit_identical_on_heavy_tails():
 @pytest.mark.parametrize("s", [7, 127])
 @pytest.mark.parametrize("n,W", [(1, 1), (513, 2), (5 * 512 + 297, 4), (100_001, 4), (4096, 9)])
 def test_dequant_sum_parity(n, W, s):
-    bucket = 512
+    _dequant_sum_case(n, W, s, 512)
+
+
+@pytest.mark.parametrize("n,W,s,bucket", [
+    (3_000_017, 4, 7, 128), (3_000_017, 9, 127, 128), (3_000_017, 8, 7, 512), (3_000_017, 3, 100, 256),
+    (12_000_013, 5, 7, 2048), (12_000_013, 9, 127, 2048), (12_000_013, 4, 127, 512)])
+def test_dequant_sum_many_buckets_per_warp(n, W, s, bucket):
+    """Sizes at which every warp of the persistent grid walks several
+    buckets, so the shared-memory stages of the copy pipeline are reused and
+    worker groups of 1..4 alternate; the ragged last bucket included."""
+    _dequant_sum_case(n, W, s, bucket)
+
+
+def _dequant_sum_case(n, W, s, bucket):
     cfg = wl.scaled(wl.QSGD_S7, n)
     nb = gc.qsgd_num_buckets(n, bucket)
     cb = gc.qsgd_code_bytes(n, s)
