@@ -95,9 +95,37 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source without its comments, every run of whitespace folded to
+    one space: the part of a file that decides what the compiler builds."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_sha(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel source's code (comments and layout excluded), which
+    ties a committed ncu capture to the code it was taken on."""
+    with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+        return hashlib.sha256(code_only(f.read()).encode()).hexdigest()[:16]
 
 
 def ncu_entry(kernel: str):
