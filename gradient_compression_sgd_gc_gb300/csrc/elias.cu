@@ -840,7 +840,8 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
 
 // Stream words one decoding CTA stages: the shared memory left, after the
 // kernel's static tables and the per-CTA reservation, when four CTAs share an
-// SM (one stream of 61 M coordinates needs 3.4 CTAs per SM of the 152).
+// SM (one stream of 61 M coordinates needs 3.4 CTAs per SM of the 152; five
+// or six CTAs per SM for 4-bit codes measured no faster on four streams).
 // Computed once per device, which also raises the kernel's dynamic
 // shared-memory limit there.
 constexpr int kDecodeCtasPerSm = 4;
