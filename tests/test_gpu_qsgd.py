@@ -121,11 +121,13 @@ def test_dequant_sum_parity(n, W, s):
 
 @pytest.mark.parametrize("n,W,s,bucket", [
     (3_000_017, 4, 7, 128), (3_000_017, 9, 127, 128), (3_000_017, 8, 7, 512), (3_000_017, 3, 100, 256),
-    (12_000_013, 5, 7, 2048), (12_000_013, 9, 127, 2048), (12_000_013, 4, 127, 512)])
+    (12_000_013, 5, 7, 2048), (12_000_013, 9, 127, 2048), (12_000_013, 4, 127, 512),
+    (200_003, 64, 7, 128), (200_003, 64, 127, 512)])
 def test_dequant_sum_many_buckets_per_warp(n, W, s, bucket):
     """Sizes at which every warp of the persistent grid walks several
-    buckets, so the shared-memory stages of the copy pipeline are reused and
-    worker groups of 1..4 alternate; the ragged last bucket included."""
+    buckets (or, at 64 workers, 16 worker groups of one bucket), so the
+    shared-memory stages of the copy pipeline are reused and worker groups of
+    1..4 alternate; the ragged last bucket included."""
     _dequant_sum_case(n, W, s, bucket)
 
 
