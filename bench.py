@@ -780,6 +780,87 @@ def rows(args, dev, peak):
     return out
 
 
+def qsgd_level_mismatches(dev, chunks_per_worker: int = 16, chunk: int = 1 << 20):
+    """Part of the oracle leg (outside every timed region): the full-size QSGD
+    configurations are quantised on the GPU, and on a bounded sample of each
+    worker's vector (``chunks_per_worker`` bucket-aligned chunks of ``chunk``
+    elements, the first and last included) the GPU's codes are compared with
+    the oracle's.  A level that differs by one where the oracle's deciding
+    value x = |v| * (s / norm) + u lies within 1e-6 of an integer is a
+    boundary mismatch (counted); any other difference, or a sign difference,
+    is a violation (must be 0)."""
+    import numpy as np
+    import torch
+    import gradient_compression_sgd_gc_gb300 as gc
+    from gradient_compression_sgd_gc_gb300 import workloads as wl
+    import oracle
+
+    def levels(codes, n, s):
+        if s <= 7:
+            c = np.empty(2 * codes.size, np.uint8)
+            c[0::2], c[1::2] = codes >> 4, codes & 0xF
+            c = c[:n]
+            return c >> 3, c & 7
+        return codes[:n] >> 7, codes[:n] & 0x7F
+
+    out = {}
+    for qcfg in (wl.QSGD_S7, wl.QSGD_S127):
+        n, W, s, d = qcfg.n, qcfg.workers, qcfg.s, qcfg.bucket
+        rng = np.random.default_rng(1234 + s)
+        starts = {0, (n - 1) // chunk * chunk}
+        starts |= {int(x) // d * d for x in rng.integers(0, n, chunks_per_worker - 2)}
+        mism = viol = norms_diff = elems = 0
+        t0 = time.time()
+        for w in range(W):
+            v = wl.qsgd_grad(qcfg, w, device=dev)
+            nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
+            norms = torch.empty(nb, device=dev)
+            codes = torch.empty(cb, dtype=torch.uint8, device=dev)
+            gc.qsgd_quantize(v, d, s, qcfg.seed, w, norms, codes)
+            torch.cuda.synchronize(dev)
+            for lo in sorted(starts):
+                hi = min(n, lo + chunk)
+                vh = v[lo:hi].cpu().numpy()
+                rn, rc = oracle.qsgd_quantize(vh, d, s, qcfg.seed, w, i0=lo)
+                gn = norms[lo // d:(hi + d - 1) // d].cpu().numpy()
+                norms_diff += int((gn != rn).sum())
+                gcodes = (codes[lo // 2:(hi + 1) // 2] if s <= 7 else codes[lo:hi]).cpu().numpy()
+                elems += hi - lo
+                if np.array_equal(gcodes, rc):
+                    continue
+                gs, gl = levels(gcodes, hi - lo, s)
+                rs, rl = levels(rc, hi - lo, s)
+                viol += int((gs != rs).sum())
+                bad = gl != rl
+                x = oracle.qsgd_scaled_values(vh, d, s, qcfg.seed, w, i0=lo)[bad].astype(np.float64)
+                k = np.maximum(gl[bad], rl[bad]).astype(np.float64)
+                near = (np.abs(gl[bad].astype(int) - rl[bad].astype(int)) == 1) & (np.abs(x - k) <= 1e-6)
+                mism += int(near.sum())
+                viol += int((~near).sum())
+            del v, norms, codes
+        out[f"s{s}"] = {"mismatches": mism, "violations": viol, "norms_differing": norms_diff,
+                        "elements_checked": elems,
+                        "sample": f"{len(starts)} chunks of {chunk} elements per worker x {W} workers "
+                                  f"(n = {n}, bucket {d}), first and last included",
+                        "oracle_s": round(time.time() - t0, 1)}
+    torch.cuda.empty_cache()
+    return out
+
+
+def row_fracs(rows_: dict) -> dict:
+    """Compact per-row fractions, [HBM frac of measured peak, issue frac,
+    DRAM-bytes frac] (null where a roofline does not apply)."""
+    out = {}
+    for k, r in rows_.items():
+        if not isinstance(r, dict) or "frac" not in r:
+            continue
+        iss = r.get("issue")
+        dram = r.get("dram")
+        out[k] = [r["frac"], iss.get("frac") if isinstance(iss, dict) else None,
+                  dram.get("frac") if isinstance(dram, dict) else None]
+    return out
+
+
 def cpu_rows(seconds_each: float = 1.5):
     """The oracle timed on bounded samples of each row's workload (one thread)."""
     import numpy as np
@@ -1074,6 +1155,10 @@ def main():
             line["cpu_baseline"] = cpu_baseline_twobit(args.cpu_seconds)
             if not args.no_rows:
                 line["cpu_rows"] = cpu_rows()
+                line["qsgd_level_mismatches"] = qsgd_level_mismatches(dev)
+        if "rows" in line:
+            # last key: the record of a run keeps only the end of stdout
+            line["row_fracs"] = row_fracs(line["rows"])
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

@@ -1174,12 +1174,13 @@ int easgd_step(float* const* models, int W, int64_t n, float alpha, float beta, 
 // order them on one stream or with events.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// names a host-side stand-in), so the first call on each device looks the
-// address up with cudaGetSymbolAddress, with that device current, and keeps
-// it for later calls.  Make that first call before any stream capture.
+// names a host-side stand-in), so every call looks the address up with
+// cudaGetSymbolAddress, with the device current, and passes it to the kernel.
+// Looking it up per call keeps no pointer across a context teardown and
+// re-creation; the first call on a device may also load the module, so make
+// that first call before any stream capture.  The stream must belong to the
+// current device: the array and the SM count both come from that device.
 // ---------------------------------------------------------------------------
-
-#include <mutex>
 
 namespace gc {
 namespace {
@@ -1187,10 +1188,6 @@ namespace {
 constexpr int64_t kNoAllocMaxN = int64_t(1) << 26;                  // 67,108,864 elements
 constexpr int64_t kNoAllocMaxTiles = kNoAllocMaxN / kTileElems;    // 16,384 tiles
 constexpr size_t kNoAllocWords = kWsHeader / sizeof(uint64_t) + kNoAllocMaxTiles;
-constexpr int kMaxDevices = 64;
-
-std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -1199,19 +1196,25 @@ static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocWo
 
 namespace {
 
-int noalloc_scratch_address(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GC_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return GC_ERR_CUDA;
-        }
-        g_noalloc_addr[dev] = p;
+// The current device's copy of the scratch array, after checking that
+// `stream` runs on that device.
+int noalloc_scratch_address(cudaStream_t stream, void** out) {
+    int dev = -1, sdev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GC_ERR_CUDA;
     }
-    *out = g_noalloc_addr[dev];
+    if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
+        cudaGetLastError();
+        return GC_ERR_CUDA;
+    }
+    if (sdev != dev) return GC_ERR_INVALID;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return GC_ERR_CUDA;
+    }
+    *out = p;
     return GC_OK;
 }
 
@@ -1241,7 +1244,7 @@ extern "C" int saps_mask_compact_noalloc(int64_t n, double p, uint64_t seed_t,
         return GC_OK;
     }
     void* scratch = nullptr;
-    const int st = noalloc_scratch_address(&scratch);
+    const int st = noalloc_scratch_address(s, &scratch);
     if (st != GC_OK) return st;
     a.n = n;
     a.seed_t = seed_t;

@@ -518,11 +518,14 @@ GC_API int easgd_step(float *const *models, int W, int64_t n, float alpha, float
  *
  *   n          0 .. GC_NOALLOC_MAX_N; larger n returns GC_ERR_INVALID
  *   other arguments as saps_mask_compact
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call on a device shares the array and
- * clears the part it uses on `stream`; calls that overlap on the GPU race and
- * must be ordered (one stream, or events).
+ *   stream     must belong to the current device (the array used is that
+ *              device's copy); a stream of another device returns
+ *              GC_ERR_INVALID
+ * Every call looks up the current device's copy of the array
+ * (cudaGetSymbolAddress); the first call on a device may load the module,
+ * so make that first call before any stream capture.  Every call on a device
+ * shares the array and clears the part it uses on `stream`; calls that
+ * overlap on the GPU race and must be ordered (one stream, or events).
  * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
  */
 #define GC_NOALLOC_MAX_N (1LL << 26)

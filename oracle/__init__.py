@@ -66,6 +66,7 @@ def _load():
             "orc_l2norm_fp32": (f32, [vp, i64]),
             "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_qsgd_scaled_values": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
+            "orc_qsgd_scaled_values_maxnorm": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
             "orc_qsgd_quantize_maxnorm": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_elias_omega_bits": (i32, [ctypes.c_uint32, ctypes.c_char_p]),
             "orc_qsgd_elias_encode": (i64, [vp, vp, i64, i64, i32, vp, vp]),
@@ -232,12 +233,13 @@ def qsgd_quantize_maxnorm(v: np.ndarray, bucket: int, s: int, seed: int, worker:
 
 
 def qsgd_scaled_values(v: np.ndarray, bucket: int, s: int, seed: int, worker: int,
-                       i0: int = 0) -> np.ndarray:
-    """fp32 x = |v| * (s / norm) + u whose floor decides each level (0 in zero buckets)."""
+                       i0: int = 0, maxnorm: bool = False) -> np.ndarray:
+    """fp32 x = |v| * (s / scale) + u whose floor decides each level (0 where
+    the bucket's scale is 0); scale = the l2 norm, or max |v| with ``maxnorm``."""
     _check(v, np.float32, "v")
     x = np.zeros(v.size, dtype=np.float32)
-    _load().orc_qsgd_scaled_values(_ptr(v), v.size, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker,
-                                   i0, _ptr(x))
+    fn = _load().orc_qsgd_scaled_values_maxnorm if maxnorm else _load().orc_qsgd_scaled_values
+    fn(_ptr(v), v.size, bucket, s, seed & 0xFFFFFFFFFFFFFFFF, worker, i0, _ptr(x))
     return x
 
 

@@ -387,18 +387,21 @@ static void qsgd_quantize_impl(const float *v, int64_t n, int64_t d, int s,
 
 /*
  * The fp32 value x = |v_i| * S + u whose floor decides each level above
- * (0 where the bucket norm is 0).  Used by the tests to tell a level that
- * sits on a rounding boundary from a wrong one.
+ * (0 where the bucket's scale is 0), with S taken from the l2 norm or, when
+ * maxnorm is set, from max |v_i| ([QS] Knowl 8).  The level written by the
+ * quantiser is min(floor(x), s), and 0 where x is NaN.  Used by the tests to
+ * tell a level that sits on a rounding boundary from a wrong one.
  */
-void orc_qsgd_scaled_values(const float *v, int64_t n, int64_t d, int s,
-                            uint64_t seed, int worker, int64_t i0, float *x_out)
+static void qsgd_scaled_values_impl(const float *v, int64_t n, int64_t d, int s,
+                                    uint64_t seed, int worker, int64_t i0,
+                                    int maxnorm, float *x_out)
 {
     int64_t nbuckets = (n + d - 1) / d;
     uint64_t seed_w = seed ^ ((uint64_t)(uint32_t)worker << 48);
     for (int64_t b = 0; b < nbuckets; ++b) {
         int64_t lo = b * d;
         int64_t hi = lo + d < n ? lo + d : n;
-        float norm = orc_l2norm_fp32(v + lo, hi - lo);
+        float norm = maxnorm ? max_abs(v + lo, hi - lo) : orc_l2norm_fp32(v + lo, hi - lo);
         float S = norm > 0.0f ? (float)s / norm : 0.0f;
         for (int64_t i = lo; i < hi; ++i) {
             if (norm > 0.0f) {
@@ -410,6 +413,19 @@ void orc_qsgd_scaled_values(const float *v, int64_t n, int64_t d, int s,
             }
         }
     }
+}
+
+void orc_qsgd_scaled_values(const float *v, int64_t n, int64_t d, int s,
+                            uint64_t seed, int worker, int64_t i0, float *x_out)
+{
+    qsgd_scaled_values_impl(v, n, d, s, seed, worker, i0, 0, x_out);
+}
+
+void orc_qsgd_scaled_values_maxnorm(const float *v, int64_t n, int64_t d, int s,
+                                    uint64_t seed, int worker, int64_t i0,
+                                    float *x_out)
+{
+    qsgd_scaled_values_impl(v, n, d, s, seed, worker, i0, 1, x_out);
 }
 
 /* Sign and level of element i from a code buffer written as above. */

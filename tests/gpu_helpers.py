@@ -1,6 +1,11 @@
 """Helpers shared by the GPU parity tests: host views of device buffers,
 sentinel-guarded allocations and the float tolerance used throughout.
 
+QSGD levels: both sides decide a level in fp32 from the same deciding value
+x = |v| * (s / norm) + u; a level may differ from the oracle's only where x
+lies within QSGD_BOUNDARY (absolute) of an integer, and those cases are
+counted.
+
 Float tolerance: the floating-point outputs (sums, averages, weight updates,
 dequantised values, elastic averaging) must agree with the fp64 oracle within
 a relative 1e-5 of the magnitude of the terms that form them,
@@ -12,7 +17,10 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import oracle
+
 REL = 1e-5
+QSGD_BOUNDARY = 1e-6
 SENTINEL = 0x5A5A5A5A
 
 
@@ -80,3 +88,49 @@ def sample_chunks(n: int, count: int, size: int, align: int = 16, seed: int = 0)
         else:
             merged.append((lo, hi))
     return merged
+
+
+def qsgd_levels(codes: np.ndarray, n: int, s: int):
+    """(sign, level) arrays of n elements from packed QSGD codes (4-bit codes
+    two per byte, element 2j in the high nibble; 8-bit codes, bit 7 = sign)."""
+    if s <= 7:
+        hi = (codes >> 4) & 0xF
+        lo = codes & 0xF
+        c = np.empty(2 * codes.size, np.uint8)
+        c[0::2], c[1::2] = hi, lo
+        c = c[:n]
+        return c >> 3, c & 7
+    return codes[:n] >> 7, codes[:n] & 0x7F
+
+
+def compare_codes(gpu_codes, ref_codes, v, n, bucket, s, seed, worker, i0=0, maxnorm=False):
+    """Asserts the GPU's QSGD codes equal the oracle's except for levels that
+    differ by one where the oracle's deciding value x lies within
+    QSGD_BOUNDARY of the integer between them; signs must agree everywhere.
+    Returns (mismatch count, boolean mask of the mismatched elements)."""
+    if np.array_equal(gpu_codes, ref_codes):
+        return 0, np.zeros(n, bool)
+    gs, gl = qsgd_levels(gpu_codes, n, s)
+    rs, rl = qsgd_levels(ref_codes, n, s)
+    assert np.array_equal(gs, rs), "sign bits differ"
+    bad = gl != rl
+    x = oracle.qsgd_scaled_values(v, bucket, s, seed, worker, i0, maxnorm=maxnorm)[bad]
+    k = np.maximum(gl[bad], rl[bad]).astype(np.float64)
+    assert np.all(np.abs(gl[bad].astype(int) - rl[bad].astype(int)) == 1), "levels differ by more than one"
+    assert np.all(np.abs(x.astype(np.float64) - k) <= QSGD_BOUNDARY), \
+        "a level differs where the deciding value is not within 1e-6 of a rounding boundary"
+    if s <= 7 and n % 2:
+        assert gpu_codes[-1] & 0xF == 0
+    return int(bad.sum()), bad
+
+
+def qsgd_sum_reference(codes_list, norms_list, n: int, bucket: int, s: int, scale: float):
+    """The oracle's dequantise-sum of the given (host) codes and norms, and the
+    tolerance scale: scale * sum over workers of |each worker's decoded value|.
+    The GPU tests pass the GPU's own codes and norms, so every element of the
+    GPU sum is compared, boundary-case levels included."""
+    ref = oracle.qsgd_dequant_sum(codes_list, norms_list, n, bucket, s, scale)
+    terms = np.zeros(n)
+    for c, nm in zip(codes_list, norms_list):
+        terms += np.abs(oracle.qsgd_dequant_sum([c], [nm], n, bucket, s))
+    return ref, abs(float(np.float32(scale))) * terms

@@ -14,8 +14,8 @@ import torch
 import gradient_compression_sgd_gc_gb300 as gc
 from gradient_compression_sgd_gc_gb300 import workloads as wl
 import oracle
-from gpu_helpers import assert_close, host_bf16_bits, host_f32, host_u32, sample_chunks
-from test_gpu_qsgd import compare_codes
+from gpu_helpers import (assert_close, compare_codes, host_bf16_bits, host_f32, host_u32,
+                         qsgd_sum_reference, sample_chunks)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -40,25 +40,21 @@ def test_qsgd_full_size_sampled(cfg):
     ho = host_f32(out)
     mism = 0
     for lo, hi in chunks:
-        bad_any = np.zeros(hi - lo, bool)
-        rcs, rns = [], []
+        gcs, gns = [], []
         for w in range(W):
             v = host_f32(vs[w][lo:hi])
             rn, rc = oracle.qsgd_quantize(v, d, s, cfg.seed, w, i0=lo)
-            assert_close(hn[w][lo // d:(hi + d - 1) // d], rn, np.abs(rn), what="norms")
+            gn = hn[w][lo // d:(hi + d - 1) // d]
+            assert_close(gn, rn, np.abs(rn), what="norms")
             if s <= 7:
                 gcodes = hc[w][lo // 2:(hi + 1) // 2]
             else:
                 gcodes = hc[w][lo:hi]
-            m, bad = compare_codes(gcodes, rc, v, hi - lo, d, s, cfg.seed, w, i0=lo)
-            mism += m
-            bad_any |= bad
-            rcs.append(rc)
-            rns.append(rn)
-        ref = oracle.qsgd_dequant_sum(rcs, rns, hi - lo, d, s, 1.0 / W)
-        terms = sum(np.abs(oracle.qsgd_dequant_sum([rcs[w]], [rns[w]], hi - lo, d, s)) for w in range(W)) / W
-        keep = ~bad_any
-        assert_close(ho[lo:hi][keep], ref[keep], terms[keep], what="dequant-sum")
+            mism += compare_codes(gcodes, rc, v, hi - lo, d, s, cfg.seed, w, i0=lo)[0]
+            gcs.append(np.ascontiguousarray(gcodes))
+            gns.append(np.ascontiguousarray(gn))
+        ref, terms = qsgd_sum_reference(gcs, gns, hi - lo, d, s, 1.0 / W)
+        assert_close(ho[lo:hi], ref, terms, what="dequant-sum")
     print(f"{cfg.name}: level mismatches at boundaries in {len(chunks)} sampled chunks: {mism}")
 
 

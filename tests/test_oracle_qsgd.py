@@ -269,3 +269,78 @@ def test_maxnorm_scale_levels_and_unbiasedness(s):
     mask = sigma > 0
     z = (mean[mask] - v.astype(np.float64)[mask]) / sigma[mask]
     assert np.mean(np.abs(z) <= 3) >= 0.99
+
+
+# ---------------------------------------------------------------- deciding value
+
+def _levels_from_scaled(x: np.ndarray, s: int) -> np.ndarray:
+    """Knowl 1's level from the deciding value: min(floor(x), s), and 0 where
+    x is NaN (0 * inf: a zero coordinate in a bucket whose s / scale overflows)."""
+    lv = np.zeros(x.size, np.int64)
+    ok = ~np.isnan(x)
+    lv[ok] = np.minimum(np.floor(x[ok].astype(np.float64)), s).astype(np.int64)
+    return lv
+
+
+def _mixed_buckets(rng, d: int) -> np.ndarray:
+    """Five buckets and a ragged tail: Gaussian, heavy-tailed, all zero,
+    subnormal (s / scale overflows fp32, zeros inside), huge values, and a
+    short last bucket of 37 elements."""
+    parts = [rng.normal(0, 1, d),
+             rng.normal(0, 1e-2, d) * np.where(rng.random(d) < 0.05, 100, 1),
+             np.zeros(d),
+             np.where(np.arange(d) % 3 == 0, 0.0, 1e-42 * rng.integers(1, 9, d)),
+             rng.normal(0, 1e30, d),
+             rng.normal(0, 3, 37)]
+    return np.concatenate(parts).astype(np.float32)
+
+
+@pytest.mark.parametrize("maxnorm", [False, True], ids=["l2", "maxnorm"])
+@pytest.mark.parametrize("s", [1, 7, 22, 127])
+def test_scaled_values_decide_every_written_level(s, maxnorm):
+    """The deciding value the GPU tests use to excuse a level that sits on a
+    rounding boundary must be the one the quantiser floors: on every element
+    of buckets of every kind (zero norm, overflowing s / norm, huge values,
+    ragged tail), for a nonzero worker and a bucket-aligned slice at i0 != 0,
+    min(floor(x), s) (0 for NaN) equals the level written.  A dropped u, a
+    wrong index offset, a worker missing from the seed or the other scale
+    would each move levels and fail here."""
+    rng = np.random.default_rng(900 + s)
+    d = 512
+    v = _mixed_buckets(rng, d)
+    q = oracle.qsgd_quantize_maxnorm if maxnorm else oracle.qsgd_quantize
+    for worker, i0 in ((0, 0), (3, 7 * d), (1, (1 << 33) + 5 * d)):
+        x = oracle.qsgd_scaled_values(v, d, s, 42, worker, i0, maxnorm=maxnorm)
+        _, codes = q(v, d, s, 42, worker, i0)
+        _, level = _parse_codes(codes, v.size, s)
+        np.testing.assert_array_equal(_levels_from_scaled(x, s), level.astype(np.int64))
+        assert np.all(x[2 * d:3 * d] == 0)                      # the all-zero bucket
+        assert np.isnan(x[3 * d]) and level[3 * d] == 0          # 0 * inf in the subnormal bucket
+        sub = slice(3 * d + 1, 4 * d)
+        assert np.all(np.isinf(x[sub][v[sub] != 0])) and np.all(level[sub][v[sub] != 0] == s)
+
+
+def test_scaled_values_of_a_slice_equal_the_whole():
+    """A bucket-aligned slice decided at its global index i0 gives the same
+    deciding values as the same elements of the whole vector."""
+    rng = np.random.default_rng(31)
+    d = 256
+    v = rng.normal(0, 1, 9 * d + 11).astype(np.float32)
+    whole = oracle.qsgd_scaled_values(v, d, 7, 5, 2)
+    part = oracle.qsgd_scaled_values(v[4 * d:], d, 7, 5, 2, i0=4 * d)
+    np.testing.assert_array_equal(part, whole[4 * d:])
+
+
+def test_scaled_values_single_nonzero_bucket_closed_form():
+    """One nonzero coordinate c in a bucket: the l2 norm and the max are |c|
+    exactly, so x = fl(|c| * fl(s / |c|)) + u lies within one ulp of s + u,
+    and every zero coordinate has x = u, the uniform draw of its own index."""
+    d, s = 512, 127
+    v = np.zeros(d, np.float32)
+    v[100] = np.float32(-0.3)
+    for maxnorm in (False, True):
+        x = oracle.qsgd_scaled_values(v, d, s, 9, 0, maxnorm=maxnorm)
+        u = np.array([oracle.uniform(9 ^ i) for i in range(d)], np.float32)
+        zero = np.arange(d) != 100
+        np.testing.assert_array_equal(x[zero], u[zero])
+        assert abs(float(x[100]) - (s + float(u[100]))) <= 2 * np.spacing(np.float32(s + 1))
