@@ -757,6 +757,12 @@ def rows(args, dev, peak):
         local = [torch.empty(n, device=dev) for _ in range(W)]
         pl = gc.gc_2bit_quantize_local(grads, res, codes, wts, local, ccfg.threshold, 0.1, stream=stream,
                                        prepare=True)
+        # the compressed step in one pass: all 4 workers quantised + dequant-sum
+        # + SGD (gc_2bit_step), and the same with eq. 11 local weights
+        ps = gc.gc_2bit_step(grads, res, codes, ccfg.threshold, gc.GC_UPD_SGD, lr=ccfg.lr, weights=wts,
+                             stream=stream, prepare=True)
+        psl = gc.gc_2bit_step(grads, res, codes, ccfg.threshold, gc.GC_UPD_SGD, lr=ccfg.lr, weights=wts,
+                              stream=stream, prepare=True, local_weights=local, local_lr=0.1)
         for i in range(21):
             k = "" if i >= 1 else "w"
             for w in range(W):
@@ -764,7 +770,15 @@ def rows(args, dev, peak):
             tm.around("d" + k, pd)
             tm.around("c" + k, pc)
             tm.around("l" + k, pl)
+            tm.around("s" + k, ps)
+            tm.around("t" + k, psl)
         torch.cuda.synchronize(dev)
+        out["cdsgd.step_one_pass"] = _row("cdsgd", "gc_2bit_step bf16 W=4 (quantise all + dequant-sum + SGD, one pass)",
+                                          (W * 10.25 + 8) * n, tm.ms("s"), peak, W * n,
+                                          {"separate_calls_ms": round(W * _median(tm.ms("q")) + _median(tm.ms("d")), 5)})
+        out["cdsgd.step_one_pass_local"] = _row("cdsgd", "gc_2bit_step_local bf16 W=4 (+ eq. 11 local weights)",
+                                                (W * 14.25 + 8) * n, tm.ms("t"), peak, W * n,
+                                                {"separate_calls_ms": round(_median(tm.ms("l")) + _median(tm.ms("d")), 5)})
         out["cdsgd.quantize_local_update"] = _row("cdsgd", "gc_2bit_quantize_local bf16 W=4 (eq. 11 local weights)",
                                                   (W * (2 + 8 + 0.25 + 4) + 4) * n, tm.ms("l"), peak, W * n)
         del local

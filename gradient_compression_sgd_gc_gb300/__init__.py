@@ -9,7 +9,7 @@ call raises.
 
 Entry points (same names as the C ABI):
   gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update, gc_2bit_step,
-  gc_2bit_quantize_local,
+  gc_2bit_quantize_local, gc_2bit_step_local (through gc_2bit_step with local_weights),
   gc_compensated_sum_update,
   qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum, qsgd_step,
   qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_decode_batched, qsgd_elias_max_words,
@@ -83,6 +83,8 @@ def load():
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
             "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
             "gc_2bit_step": (i32, [vp, i32, vp, vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
+            "gc_2bit_step_local": (i32, [vp, i32, vp, vp, vp, f32, i32, i64, f32, i32, f32, f32, vp, vp, vp,
+                                         vp]),
             "gc_2bit_quantize_local": (i32, [vp, i32, vp, vp, vp, vp, i32, i64, f32, f32, vp]),
             "gc_2bit_dequant_sum_update": (i32, [vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
             "gc_compensated_sum_update": (i32, [vp, i32, vp, i32, i64, f32, vp, vp]),
@@ -249,21 +251,30 @@ def gc_2bit_quantize_batched(grads, residuals, codes, threshold: float, stream=N
 
 def gc_2bit_step(grads, residuals, codes, threshold: float, kind: int = GC_UPD_SGD, lr: float = 0.0,
                  alpha: float = 0.0, center=None, weights=None, out=None, stream=None,
-                 prepare: bool = False):
-    """Quantise W equal-sized fp32 gradients and apply the dequant-sum update in
-    one pass (bit-identical to gc_2bit_quantize_batched + gc_2bit_dequant_sum_update)."""
+                 prepare: bool = False, local_weights=None, local_lr: float = 0.0):
+    """Quantise W equal-sized fp32 or bf16 gradients and apply the dequant-sum
+    update in one pass (bit-identical to gc_2bit_quantize_batched +
+    gc_2bit_dequant_sum_update).  With ``local_weights`` (W fp32 tensors) the
+    CD-SGD eq. 11 local weights weights - local_lr * grads[w] are written too
+    (gc_2bit_step_local)."""
     lib = load()
     W = len(grads)
     n = grads[0].numel()
-    args = (_ptrs(grads, "grads", torch.float32, n, pinned_ok=True), GC_F32,
-            _ptrs(residuals, "residuals", torch.float32, n), _ptrs(codes, "codes", torch.int32, code_words(n)),
-            W, n, float(threshold), int(kind), float(lr), float(alpha),
+    dt = _gdtype(grads[0])
+    head = (_ptrs(grads, "grads", grads[0].dtype, n, pinned_ok=True), dt,
+            _ptrs(residuals, "residuals", torch.float32, n), _ptrs(codes, "codes", torch.int32, code_words(n)))
+    tail = (W, n, float(threshold), int(kind), float(lr), float(alpha),
             _dev(center, "center", torch.float32, n) if center is not None else None,
             _dev(weights, "weights", torch.float32, n) if weights is not None else None,
             _dev(out, "out", torch.float32, n) if out is not None else None,
             _stream(stream, residuals[0]))
-    return _invoke(lib.gc_2bit_step, args, "gc_2bit_step", prepare,
-                   (list(grads), list(residuals), list(codes), center, weights, out))
+    keep = (list(grads), list(residuals), list(codes), center, weights, out)
+    if local_weights is None:
+        return _invoke(lib.gc_2bit_step, head + tail, "gc_2bit_step", prepare, keep)
+    if len(local_weights) != W:
+        raise ValueError("gc_2bit_step: one local weight buffer per worker")
+    args = head + (_ptrs(local_weights, "local_weights", torch.float32, n), float(local_lr)) + tail
+    return _invoke(lib.gc_2bit_step_local, args, "gc_2bit_step_local", prepare, keep + (list(local_weights),))
 
 
 def gc_2bit_quantize_local(grads, residuals, codes, weights: torch.Tensor, local_weights,

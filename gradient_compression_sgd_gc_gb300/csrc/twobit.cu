@@ -399,15 +399,18 @@ k_2bit_dqsum(const DqArgs a) {
 // decoded sum in registers instead of re-reading the codes, and applies the
 // update as gc_2bit_dequant_sum_update does -- the outputs are bit-identical
 // to those two calls.  Worker w+1's gradient and residual loads are issued
-// before worker w's tile is processed.
+// before worker w's tile is processed.  With LOCAL, each worker's CD-SGD
+// eq. 11 local weights W_loc = W - local_lr * g are written from the global
+// weights as read before the update (as gc_2bit_quantize_local writes them).
 struct StepArgs {
     PtrTable<const void*> grads;
     PtrTable<float*> res;
     PtrTable<uint32_t*> codes;
+    PtrTable<float*> local;
     int W;
     int64_t n;
     float t;
-    float k_out, k_lr, alpha;
+    float k_out, k_lr, alpha, local_lr;
     const float* center;
     float* weights;
     float* out;
@@ -446,71 +449,121 @@ __device__ __forceinline__ uint32_t quantize4_dec(float4& r, const float4 g, flo
     return (c0 << 6) | (c1 << 4) | (c2 << 2) | c3;
 }
 
-template <int KIND>
+// Element offset, within a lane's share of a full tile, of its q-th group of
+// four consecutive elements (q = 0..3).  fp32: lane l owns 4l + 128q (one
+// float4 per round, as the fp32 quantiser); bf16: lane l owns 8l + 256(q/2)
+// + 4(q%2) (one 16-byte vector of 8 bf16 per round, as the bf16 quantiser).
+template <bool BF16>
+__device__ __forceinline__ int64_t step_group(int lane, int q) {
+    return BF16 ? 8 * lane + 256 * (q >> 1) + 4 * (q & 1) : 4 * lane + 128 * q;
+}
+
+// One worker's gradient for a lane's 16 elements of a full tile, raw: four
+// float4 (fp32) or two 16-byte vectors of 8 bf16 in the first two slots.
+template <bool BF16>
+__device__ __forceinline__ void step_load_grad(const void* g, int64_t tbase, int lane, uint4 (&raw)[4]) {
+    if (BF16) {
+        const uint16_t* gh = static_cast<const uint16_t*>(g) + tbase + 8 * lane;
+        raw[0] = ld_stream_u4(gh);
+        raw[1] = ld_stream_u4(gh + 256);
+    } else {
+        const float* gf = static_cast<const float*>(g) + tbase + 4 * lane;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) raw[q] = ld_stream_u4(gf + 128 * q);
+    }
+}
+
+// Gradient values of group q from the raw registers (bf16 widened exactly).
+template <bool BF16>
+__device__ __forceinline__ float4 step_grad(const uint4 (&raw)[4], int q) {
+    if (BF16) {
+        const uint4 u = raw[q >> 1];
+        return (q & 1) ? make_float4(bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w))
+                       : make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+    }
+    return make_float4(__uint_as_float(raw[q].x), __uint_as_float(raw[q].y), __uint_as_float(raw[q].z),
+                       __uint_as_float(raw[q].w));
+}
+
+template <int KIND, bool BF16, bool LOCAL>
 __global__ void __launch_bounds__(kThreads, 2)
-k_2bit_step_f32(const StepArgs a) {
+k_2bit_step(const StepArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nfull = a.n / kTile;
     if (tile < nfull) {
-        const int64_t base = tile * kTile + 4 * lane;
+        const int64_t tbase = tile * kTile;
         float4 wv[4], cv[4];
-        if (KIND != GC_UPD_NONE) {
+        if (KIND != GC_UPD_NONE || LOCAL) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wv[j] = ld_f4(a.weights + base + 128 * j);
+            for (int q = 0; q < 4; ++q) wv[q] = ld_f4(a.weights + tbase + step_group<BF16>(lane, q));
         }
         if (KIND == GC_UPD_EASGD) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) cv[j] = ld_stream_f4(a.center + base + 128 * j);
+            for (int q = 0; q < 4; ++q) cv[q] = ld_stream_f4(a.center + tbase + step_group<BF16>(lane, q));
         }
         int cnt[4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cnt[j][k] = 0;
-        float4 ga[4], ra[4];
-        {
-            const float* g = static_cast<const float*>(a.grads.p[0]);
+            for (int k = 0; k < 4; ++k) cnt[q][k] = 0;
+        uint4 ga[4];
+        float4 ra[4];
+        step_load_grad<BF16>(a.grads.p[0], tbase, lane, ga);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                ga[j] = ld_stream_f4(g + base + 128 * j);
-                ra[j] = ld_f4(a.res.p[0] + base + 128 * j);
-            }
-        }
+        for (int q = 0; q < 4; ++q) ra[q] = ld_f4(a.res.p[0] + tbase + step_group<BF16>(lane, q));
         for (int w = 0; w < a.W; ++w) {
-            float4 gb[4], rb[4];
+            uint4 gb[4];
+            float4 rb[4];
             if (w + 1 < a.W) {
-                const float* g = static_cast<const float*>(a.grads.p[w + 1]);
+                step_load_grad<BF16>(a.grads.p[w + 1], tbase, lane, gb);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    gb[j] = ld_stream_f4(g + base + 128 * j);
-                    rb[j] = ld_f4(a.res.p[w + 1] + base + 128 * j);
-                }
+                for (int q = 0; q < 4; ++q) rb[q] = ld_f4(a.res.p[w + 1] + tbase + step_group<BF16>(lane, q));
             }
             float* r = a.res.p[w];
-            uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[w]);
+            uint32_t c[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int q = 0; q < 4; ++q) {
+                const int64_t e = tbase + step_group<BF16>(lane, q);
+                const float4 g = step_grad<BF16>(ga, q);
+                if (LOCAL)
+                    st_stream_f4(a.local.p[w] + e,
+                                 make_float4(fmaf(-a.local_lr, g.x, wv[q].x), fmaf(-a.local_lr, g.y, wv[q].y),
+                                             fmaf(-a.local_lr, g.z, wv[q].z), fmaf(-a.local_lr, g.w, wv[q].w)));
                 int d[4];
-                const uint32_t c = quantize4_dec(ra[j], ga[j], a.t, d);
-                st_stream_f4(r + base + 128 * j, ra[j]);
-                cb[code_byte(base + 128 * j)] = static_cast<uint8_t>(c);
+                c[q] = quantize4_dec(ra[q], g, a.t, d);
+                st_stream_f4(r + e, ra[q]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) cnt[j][k] += d[k];
+                for (int k = 0; k < 4; ++k) cnt[q][k] += d[k];
+            }
+            if (BF16) {
+                // elements e..e+7 (e = tbase + 8 lane + 256 j) are the high half
+                // of word e/16 when e % 16 == 0, its low half otherwise
+                uint16_t* ch = reinterpret_cast<uint16_t*>(a.codes.p[w]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int64_t e = tbase + 8 * lane + 256 * j;
+                    ch[2 * (e >> 4) + 1 - ((e >> 3) & 1)] = static_cast<uint16_t>((c[2 * j] << 8) | c[2 * j + 1]);
+                }
+            } else {
+                uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[w]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    cb[code_byte(tbase + step_group<BF16>(lane, q))] = static_cast<uint8_t>(c[q]);
             }
             if (w + 1 < a.W) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ga[j] = gb[j];
-                    ra[j] = rb[j];
+                for (int q = 0; q < 4; ++q) {
+                    ga[q] = gb[q];
+                    ra[q] = rb[q];
                 }
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float cf[4] = {static_cast<float>(cnt[j][0]), static_cast<float>(cnt[j][1]),
-                                 static_cast<float>(cnt[j][2]), static_cast<float>(cnt[j][3])};
-            step_apply<KIND>(a, base + 128 * j, cf, wv[j], cv[j]);
+        for (int q = 0; q < 4; ++q) {
+            const float cf[4] = {static_cast<float>(cnt[q][0]), static_cast<float>(cnt[q][1]),
+                                 static_cast<float>(cnt[q][2]), static_cast<float>(cnt[q][3])};
+            step_apply<KIND>(a, tbase + step_group<BF16>(lane, q), cf, wv[q], cv[q]);
         }
     } else if (tile == nfull && a.n % kTile != 0) {
         // partial last tile: element by element
@@ -519,14 +572,17 @@ k_2bit_step_f32(const StepArgs a) {
             const int64_t e0 = nfull * kTile + 128 * j + 4 * lane;
             int cnt[4] = {0, 0, 0, 0};
             for (int w = 0; w < a.W; ++w) {
-                const float* g = static_cast<const float*>(a.grads.p[w]);
                 float* r = a.res.p[w];
                 uint32_t cbits = 0;
                 for (int k = 0; k < 4; ++k) {
                     const int64_t e = e0 + k;
                     if (e < a.n) {
+                        const float gval = BF16 ? __uint_as_float(static_cast<uint32_t>(
+                                                      static_cast<const uint16_t*>(a.grads.p[w])[e]) << 16)
+                                                : static_cast<const float*>(a.grads.p[w])[e];
+                        if (LOCAL) a.local.p[w][e] = fmaf(-a.local_lr, gval, a.weights[e]);
                         float rr = r[e];
-                        const uint32_t c = quantize1(rr, g[e], a.t);
+                        const uint32_t c = quantize1(rr, gval, a.t);
                         r[e] = rr;
                         cbits |= c << (6 - 2 * k);
                         cnt[k] += (c == 3u) - (c == 2u);
@@ -548,6 +604,15 @@ k_2bit_step_f32(const StepArgs a) {
                 }
             }
         }
+    }
+}
+
+template <bool BF16, bool LOCAL>
+void launch_step(gc_update kind, unsigned grid, cudaStream_t s, const StepArgs& a) {
+    switch (kind) {
+        case GC_UPD_NONE: k_2bit_step<GC_UPD_NONE, BF16, LOCAL><<<grid, kThreads, 0, s>>>(a); break;
+        case GC_UPD_SGD: k_2bit_step<GC_UPD_SGD, BF16, LOCAL><<<grid, kThreads, 0, s>>>(a); break;
+        default: k_2bit_step<GC_UPD_EASGD, BF16, LOCAL><<<grid, kThreads, 0, s>>>(a); break;
     }
 }
 
@@ -865,32 +930,42 @@ int gc_2bit_dequant_sum_update(const uint32_t* const* codes, int W, int64_t n, f
     return launch_status();
 }
 
-int gc_2bit_step(const void* const* grads, gc_dtype dtype, float* const* residuals, uint32_t* const* codes,
-                 int W, int64_t n, float threshold, gc_update kind, float lr, float alpha,
-                 const float* center, float* weights, float* out, gc_stream_t stream) {
-    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !finite_pos(threshold) || dtype != GC_F32) return GC_ERR_INVALID;
+}  // extern "C"
+
+namespace {
+
+int step_entry(const void* const* grads, gc_dtype dtype, float* const* residuals, uint32_t* const* codes,
+               float* const* local_weights, float local_lr, int W, int64_t n, float threshold,
+               gc_update kind, float lr, float alpha, const float* center, float* weights, float* out,
+               gc_stream_t stream) {
+    const bool local = local_weights != nullptr;
+    if (n < 0 || W < 1 || W > GC_MAX_WORKERS || !finite_pos(threshold)) return GC_ERR_INVALID;
+    if (dtype != GC_F32 && dtype != GC_BF16) return GC_ERR_INVALID;
     if (kind != GC_UPD_NONE && kind != GC_UPD_SGD && kind != GC_UPD_EASGD) return GC_ERR_INVALID;
-    if (!isfinite(lr) || !isfinite(alpha)) return GC_ERR_INVALID;
+    if (!isfinite(lr) || !isfinite(alpha) || !isfinite(local_lr)) return GC_ERR_INVALID;
     if (n == 0) return GC_OK;
     if (!grads || !residuals || !codes) return GC_ERR_INVALID;
     StepArgs a;
     for (int w = 0; w < W; ++w) {
-        if (!grads[w] || !residuals[w] || !codes[w]) return GC_ERR_INVALID;
+        if (!grads[w] || !residuals[w] || !codes[w] || (local && !local_weights[w])) return GC_ERR_INVALID;
         if (!aligned16(grads[w]) || !aligned16(residuals[w]) || !aligned16(codes[w])) return GC_ERR_ALIGN;
+        if (local && !aligned16(local_weights[w])) return GC_ERR_ALIGN;
         a.grads.p[w] = grads[w];
         a.res.p[w] = residuals[w];
         a.codes.p[w] = codes[w];
+        a.local.p[w] = local ? local_weights[w] : nullptr;
     }
     if (kind == GC_UPD_NONE) {
         if (!out) return GC_ERR_INVALID;
         if (!aligned16(out)) return GC_ERR_ALIGN;
-    } else {
+    }
+    if (kind != GC_UPD_NONE || local) {
         if (!weights) return GC_ERR_INVALID;
         if (!aligned16(weights)) return GC_ERR_ALIGN;
-        if (kind == GC_UPD_EASGD) {
-            if (!center) return GC_ERR_INVALID;
-            if (!aligned16(center)) return GC_ERR_ALIGN;
-        }
+    }
+    if (kind == GC_UPD_EASGD) {
+        if (!center) return GC_ERR_INVALID;
+        if (!aligned16(center)) return GC_ERR_ALIGN;
     }
     a.W = W;
     a.n = n;
@@ -898,17 +973,38 @@ int gc_2bit_step(const void* const* grads, gc_dtype dtype, float* const* residua
     a.k_out = static_cast<float>(static_cast<double>(threshold) / W);
     a.k_lr = static_cast<float>(static_cast<double>(lr) * threshold / W);
     a.alpha = alpha;
+    a.local_lr = local_lr;
     a.center = center;
     a.weights = weights;
     a.out = out;
     const unsigned grid = blocks_for_tiles((n + 511) / 512);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    switch (kind) {
-        case GC_UPD_NONE: k_2bit_step_f32<GC_UPD_NONE><<<grid, kThreads, 0, s>>>(a); break;
-        case GC_UPD_SGD: k_2bit_step_f32<GC_UPD_SGD><<<grid, kThreads, 0, s>>>(a); break;
-        default: k_2bit_step_f32<GC_UPD_EASGD><<<grid, kThreads, 0, s>>>(a); break;
+    if (dtype == GC_BF16) {
+        if (local) launch_step<true, true>(kind, grid, s, a); else launch_step<true, false>(kind, grid, s, a);
+    } else {
+        if (local) launch_step<false, true>(kind, grid, s, a); else launch_step<false, false>(kind, grid, s, a);
     }
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int gc_2bit_step(const void* const* grads, gc_dtype dtype, float* const* residuals, uint32_t* const* codes,
+                 int W, int64_t n, float threshold, gc_update kind, float lr, float alpha,
+                 const float* center, float* weights, float* out, gc_stream_t stream) {
+    return step_entry(grads, dtype, residuals, codes, nullptr, 0.0f, W, n, threshold, kind, lr, alpha, center,
+                      weights, out, stream);
+}
+
+int gc_2bit_step_local(const void* const* grads, gc_dtype dtype, float* const* residuals,
+                       uint32_t* const* codes, float* const* local_weights, float local_lr, int W, int64_t n,
+                       float threshold, gc_update kind, float lr, float alpha, const float* center,
+                       float* weights, float* out, gc_stream_t stream) {
+    if (!local_weights) return GC_ERR_INVALID;
+    return step_entry(grads, dtype, residuals, codes, local_weights, local_lr, W, n, threshold, kind, lr, alpha,
+                      center, weights, out, stream);
 }
 
 int gc_2bit_quantize_local(const void* const* grads, gc_dtype dtype, float* const* residuals,

@@ -159,25 +159,48 @@ GC_API int gc_2bit_dequant_sum_update(const uint32_t *const *codes, int W, int64
                                float *weights, float *out, gc_stream_t stream);
 
 /*
- * gc_2bit_step -- gc_2bit_quantize_batched over W equal-sized fp32 buffers
- * followed by gc_2bit_dequant_sum_update, in one pass: each element's
- * decoded sum is formed while its codes are produced, so the codes are
- * written but not read back.  Codes, residuals and the update are
+ * gc_2bit_step -- gc_2bit_quantize_batched over W equal-sized gradient
+ * buffers followed by gc_2bit_dequant_sum_update, in one pass: each
+ * element's decoded sum is formed while its codes are produced, so the codes
+ * are written but not read back.  Codes, residuals and the update are
  * bit-identical to the two separate calls.  (MXNet PR #8662 "Local kvstore":
- * every device quantises, one sums the dequantised values; CD-SGD eq. 10.)
+ * every device quantises, one sums the dequantised values; CD-SGD eq. 10 and
+ * Algorithm 1's compressed iteration.)
  *
- *   grads, residuals, codes   host arrays of W pointers as in the batched
- *                             quantiser (fp32 gradients only)
+ *   grads      host array of W device pointers, fp32 or bf16 (dtype) [n]
+ *   residuals, codes
+ *              host arrays of W pointers as in the batched quantiser
  *   kind, lr, alpha, center, weights, out
- *                             as gc_2bit_dequant_sum_update
- * Errors: GC_ERR_INVALID (also dtype other than GC_F32), GC_ERR_ALIGN,
- * GC_ERR_CUDA.
+ *              as gc_2bit_dequant_sum_update
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
  */
 GC_API int gc_2bit_step(const void *const *grads, gc_dtype dtype,
                         float *const *residuals, uint32_t *const *codes, int W,
                         int64_t n, float threshold, gc_update kind, float lr,
                         float alpha, const float *center, float *weights,
                         float *out, gc_stream_t stream);
+
+/*
+ * gc_2bit_step_local -- gc_2bit_step that also writes each worker's CD-SGD
+ * local weights (eq. 11 and Algorithm 1's local step):
+ *   local_weights[w][i] = weights[i] - local_lr * g_w[i]
+ * from the weights as they are before this call's update, i.e. the same
+ * values gc_2bit_quantize_local writes; everything else as gc_2bit_step.
+ * Bit-identical to gc_2bit_quantize_local followed by
+ * gc_2bit_dequant_sum_update.
+ *
+ *   local_weights  host array of W device pointers, fp32 [n], out (must not
+ *                  alias weights or each other)
+ *   local_lr       eta_loc, finite
+ *   weights        required (read for the local weights) for every kind
+ * Errors: GC_ERR_INVALID (also local_weights NULL), GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_step_local(const void *const *grads, gc_dtype dtype,
+                              float *const *residuals, uint32_t *const *codes,
+                              float *const *local_weights, float local_lr, int W,
+                              int64_t n, float threshold, gc_update kind, float lr,
+                              float alpha, const float *center, float *weights,
+                              float *out, gc_stream_t stream);
 
 /*
  * gc_2bit_quantize_local -- gc_2bit_quantize on B workers' gradients (one

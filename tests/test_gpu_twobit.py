@@ -325,6 +325,81 @@ def test_fused_step_is_bitwise_the_two_calls(kind, n, W):
         assert torch.equal(wa.view(torch.int32), wb.view(torch.int32))
 
 
+@pytest.mark.parametrize("local", [False, True], ids=["plain", "local"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("kind", [gc.GC_UPD_NONE, gc.GC_UPD_SGD, gc.GC_UPD_EASGD])
+@pytest.mark.parametrize("n,W", [(1, 1), (513, 3), (100_003, 4), (262_144 + 16, 2)])
+def test_fused_step_dtypes_and_local_weights_are_bitwise_the_separate_calls(kind, dtype, local, n, W):
+    """gc_2bit_step on fp32 or bf16 gradients, optionally writing the CD-SGD
+    eq. 11 local weights (gc_2bit_step_local), equals bit for bit the batched
+    quantiser (or gc_2bit_quantize_local) followed by the dequant-sum update:
+    codes, residuals, local weights and the updated weights (or output)."""
+    t, lr, alpha, llr = 1e-3, 0.01, 0.9, 0.1
+    grads = [wl.normal(n, 5e-4, 260 + w, device=DEV, dtype=dtype) for w in range(W)]
+    r0 = [wl.normal(n, 5e-4, 280 + w, device=DEV) for w in range(W)]
+    w0 = wl.uniform(n, 0.05, 27, device=DEV)
+    c0 = wl.uniform(n, 0.05, 29, device=DEV)
+    ra, rb = [x.clone() for x in r0], [x.clone() for x in r0]
+    ca = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    cb = [torch.full((gc.code_words(n),), 7, dtype=torch.int32, device=DEV) for _ in range(W)]
+    wa, wb = w0.clone(), w0.clone()
+    oa, ob = torch.empty(n, device=DEV), guarded(n, torch.float32)
+    la = [torch.empty(n, device=DEV) for _ in range(W)]
+    lb = [guarded(n, torch.float32) for _ in range(W)]
+    center = c0 if kind == gc.GC_UPD_EASGD else None
+    upd = dict(lr=lr, alpha=alpha, center=center, weights=wa if kind != gc.GC_UPD_NONE else None,
+               out=oa if kind == gc.GC_UPD_NONE else None)
+    if local:
+        gc.gc_2bit_quantize_local(grads, ra, ca, wa, la, t, llr)
+    else:
+        gc.gc_2bit_quantize_batched(grads, ra, ca, t)
+    gc.gc_2bit_dequant_sum_update(ca, n, t, kind, **upd)
+    gc.gc_2bit_step(grads, rb, cb, t, kind, lr=lr, alpha=alpha, center=center,
+                    weights=wb if (kind != gc.GC_UPD_NONE or local) else None,
+                    out=ob[:n] if kind == gc.GC_UPD_NONE else None,
+                    local_weights=[x[:n] for x in lb] if local else None, local_lr=llr)
+    torch.cuda.synchronize()
+    for w in range(W):
+        assert torch.equal(ra[w].view(torch.int32), rb[w].view(torch.int32)), "residuals"
+        assert torch.equal(ca[w], cb[w]), "codes"
+        if local:
+            assert torch.equal(la[w].view(torch.int32), lb[w][:n].view(torch.int32)), "local weights"
+            check_guard(lb[w], n)
+    if kind == gc.GC_UPD_NONE:
+        assert torch.equal(oa.view(torch.int32), ob[:n].view(torch.int32))
+        check_guard(ob, n)
+    else:
+        assert torch.equal(wa.view(torch.int32), wb.view(torch.int32))
+
+
+@pytest.mark.parametrize("n,W", [(517, 3), (100_003, 4)])
+def test_fused_bf16_step_with_local_weights_against_oracle(n, W):
+    """The configured CD-SGD compressed step (bf16 gradients, fp32 residuals,
+    SGD on the averaged dequantised sum) with eq. 11 local weights, in one
+    pass, element by element against the oracle."""
+    t, lr, llr = 1e-3, 0.01, 0.1
+    grads = [wl.normal(n, 5e-4, 360 + w, device=DEV, dtype=torch.bfloat16) for w in range(W)]
+    res = [wl.normal(n, 5e-4, 380 + w, device=DEV) for w in range(W)]
+    r_ref = [host_f32(r).copy() for r in res]
+    codes = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(W)]
+    w0 = wl.uniform(n, 0.05, 37, device=DEV)
+    w_ref = host_f32(w0).astype(np.float64)
+    local = [torch.empty(n, device=DEV) for _ in range(W)]
+    gc.gc_2bit_step(grads, res, codes, t, gc.GC_UPD_SGD, lr=lr, weights=w0, local_weights=local, local_lr=llr)
+    torch.cuda.synchronize()
+    gh = [_grad_host(g) for g in grads]
+    l_ref = [oracle.cdsgd_local_update(gh[w], w_ref, llr) for w in range(W)]
+    c_ref = [oracle.twobit_quantize(gh[w], r_ref[w], t) for w in range(W)]
+    scale = np.abs(w_ref) + lr * t
+    lscale = [np.abs(w_ref) + llr * np.abs((gh[w].astype(np.uint32) << 16).view(np.float32)) for w in range(W)]
+    oracle.twobit_dequant_sum_update(c_ref, n, t, oracle.KIND_SGD, lr=lr, weights=w_ref)
+    for w in range(W):
+        np.testing.assert_array_equal(host_u32(codes[w]), c_ref[w])
+        np.testing.assert_array_equal(host_f32(res[w]).view(np.uint32), r_ref[w].view(np.uint32))
+        assert_close(host_f32(local[w]), l_ref[w], lscale[w], what="local weights")
+    assert_close(host_f32(w0), w_ref, scale, what="weights")
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("n,B", [(1, 1), (517, 2), (100_003, 4)])
 def test_quantize_with_local_update(n, B, dtype):
