@@ -8,13 +8,14 @@ no CPU or PyTorch fallback: if the library cannot be built or loaded, every
 call raises.
 
 Entry points (same names as the C ABI):
-  gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_dequant_sum_update, gc_2bit_step,
+  gc_2bit_quantize, gc_2bit_quantize_batched, gc_2bit_quantize_steps, gc_2bit_dequant_sum_update,
+  gc_2bit_step,
   gc_2bit_quantize_local, gc_2bit_step_local (through gc_2bit_step with local_weights),
   gc_compensated_sum_update,
   qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum, qsgd_step,
   qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_decode_batched, qsgd_elias_max_words,
   qsgd_elias_workspace_bytes,
-  saps_round_seed, saps_matching, saps_workspace_bytes, saps_mask_compact,
+  saps_round_seed, saps_matching, saps_matching_bandwidth, saps_workspace_bytes, saps_mask_compact,
   saps_mask_compact_noalloc, saps_peer_average, saps_average_easgd_step, easgd_step,
   saps_round, gc_status_string, gc_version
 Front ends over them (per-key state, parameter rules): ``compression.py``.
@@ -35,11 +36,11 @@ __all__ = [
     "GC_UPD_NONE", "GC_UPD_SGD", "GC_UPD_EASGD", "GC_MAX_WORKERS",
     "gc_status_string", "gc_version", "gc_2bit_quantize", "gc_2bit_quantize_batched",
     "gc_2bit_dequant_sum_update",
-    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed",
+    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed", "saps_matching_bandwidth", "gossip_matrix", "NEVER",
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
-    "gc_2bit_step", "gc_2bit_quantize_local", "qsgd_quantize_maxnorm",
+    "gc_2bit_step", "gc_2bit_quantize_local", "gc_2bit_quantize_steps", "qsgd_quantize_maxnorm",
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
     "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step", "qsgd_elias_decode_batched",
 ]
@@ -83,6 +84,8 @@ def load():
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
             "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
             "gc_2bit_step": (i32, [vp, i32, vp, vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
+            "saps_matching_bandwidth": (i32, [i32, vp, f64, vp, i64, i64, u64, vp]),
+            "gc_2bit_quantize_steps": (i32, [vp, i32, vp, vp, vp, i32, i64, f32, vp]),
             "gc_2bit_step_local": (i32, [vp, i32, vp, vp, vp, f32, i32, i64, f32, i32, f32, f32, vp, vp, vp,
                                          vp]),
             "gc_2bit_quantize_local": (i32, [vp, i32, vp, vp, vp, vp, i32, i64, f32, f32, vp]),
@@ -277,6 +280,25 @@ def gc_2bit_step(grads, residuals, codes, threshold: float, kind: int = GC_UPD_S
     return _invoke(lib.gc_2bit_step_local, args, "gc_2bit_step_local", prepare, keep + (list(local_weights),))
 
 
+def gc_2bit_quantize_steps(grads, residual: torch.Tensor, codes, threshold: float, out=None, stream=None,
+                           prepare: bool = False):
+    """S successive 2-bit steps of one worker in one launch: grads[s] quantised
+    into codes[s] with the residual carried; with ``out`` (S fp32 tensors) the
+    dequantised values of each step too."""
+    lib = load()
+    S = len(grads)
+    n = residual.numel()
+    if len(codes) != S or (out is not None and len(out) != S):
+        raise ValueError("gc_2bit_quantize_steps: one code (and out) buffer per step")
+    args = (_ptrs(grads, "grads", grads[0].dtype, n, pinned_ok=True), _gdtype(grads[0]),
+            _dev(residual, "residual", torch.float32, n),
+            _ptrs(codes, "codes", torch.int32, code_words(n)),
+            _ptrs(out, "out", torch.float32, n) if out is not None else None,
+            S, n, float(threshold), _stream(stream, residual))
+    return _invoke(lib.gc_2bit_quantize_steps, args, "gc_2bit_quantize_steps", prepare,
+                   (list(grads), residual, list(codes), list(out) if out is not None else None))
+
+
 def gc_2bit_quantize_local(grads, residuals, codes, weights: torch.Tensor, local_weights,
                            threshold: float, local_lr: float, stream=None, prepare: bool = False):
     """gc_2bit_quantize on B workers plus CD-SGD eq. 11 local weights
@@ -438,6 +460,40 @@ def saps_matching(seed_t: int, W: int) -> list[int]:
     buf = (ctypes.c_int * max(W, 1))()
     _check(load().saps_matching(int(seed_t) & 0xFFFFFFFFFFFFFFFF, int(W), buf), "saps_matching")
     return list(buf)[:W]
+
+
+NEVER = -(1 << 63)
+
+
+def saps_matching_bandwidth(bandwidth, b_thres: float, last_round, t: int, t_thres: int,
+                            seed_t: int) -> list[int]:
+    """SAPS Algorithm 3 (host): the round's perfect matching from the W x W
+    bandwidth matrix.  ``last_round`` is a W x W int64 numpy array updated in
+    place (the rounds pairs were last matched; NEVER for never)."""
+    import numpy as np
+    B = np.ascontiguousarray(bandwidth, dtype=np.float64)
+    W = B.shape[0]
+    if B.shape != (W, W) or not isinstance(last_round, np.ndarray) or last_round.shape != (W, W) \
+            or last_round.dtype != np.int64 or not last_round.flags.c_contiguous:
+        raise ValueError("saps_matching_bandwidth: bandwidth and last_round must be W x W "
+                         "(last_round a C-contiguous int64 array)")
+    buf = (ctypes.c_int * max(W, 1))()
+    _check(load().saps_matching_bandwidth(int(W), B.ctypes.data, float(b_thres), last_round.ctypes.data,
+                                          int(t), int(t_thres), int(seed_t) & 0xFFFFFFFFFFFFFFFF, buf),
+           "saps_matching_bandwidth")
+    return list(buf)[:W]
+
+
+def gossip_matrix(pairs):
+    """The doubly stochastic W x W gossip matrix of a perfect matching given as
+    pairs (pairs[2q], pairs[2q+1]): 1/2 on i,i / i,j / j,i / j,j per pair."""
+    import numpy as np
+    W = len(pairs)
+    M = np.zeros((W, W))
+    for q in range(0, W, 2):
+        a, b = pairs[q], pairs[q + 1]
+        M[a, a] = M[b, b] = M[a, b] = M[b, a] = 0.5
+    return M
 
 
 def saps_workspace_bytes(n: int) -> int:

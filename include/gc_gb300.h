@@ -203,6 +203,28 @@ GC_API int gc_2bit_step_local(const void *const *grads, gc_dtype dtype,
                               float *out, gc_stream_t stream);
 
 /*
+ * gc_2bit_quantize_steps -- S successive 2-bit steps of one worker in one
+ * launch (MXNet PR #8662 "Two bit quantization": the residual carries what
+ * was not sent to the next step).  Step s (0-based) quantises grads[s] with
+ * the residual left by step s-1 and writes codes[s]; with `out`, also the
+ * dequantised values out[s][i] = +t, -t or 0 (the W = 1 dequant-sum).  The
+ * residual is read once and written once, after the last step.
+ * Bit-identical to S calls of gc_2bit_quantize (each followed by
+ * gc_2bit_dequant_sum_update with W = 1 and GC_UPD_NONE when out is given).
+ *
+ *   grads      host array of S device pointers, fp32 or bf16 (dtype) [n]
+ *   residual   device fp32 [n], in/out
+ *   codes      host array of S device pointers, uint32 [ceil(n/16)], out
+ *   out        host array of S device pointers, fp32 [n], out; or NULL
+ *   S          1 .. GC_MAX_WORKERS
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int gc_2bit_quantize_steps(const void *const *grads, gc_dtype dtype,
+                                  float *residual, uint32_t *const *codes,
+                                  float *const *out, int S, int64_t n,
+                                  float threshold, gc_stream_t stream);
+
+/*
  * gc_2bit_quantize_local -- gc_2bit_quantize on B workers' gradients (one
  * launch), each also producing the worker's local weights of CD-SGD eq. 11
  * (Algorithm 1 line 24): local_weights[b][i] = weights[i] - local_lr *
@@ -418,6 +440,43 @@ GC_API uint64_t saps_round_seed(uint64_t base_seed, uint64_t t);
  * Errors: GC_ERR_INVALID (W not even, W < 2, W > GC_MAX_WORKERS, NULL).
  */
 GC_API int saps_matching(uint64_t seed_t, int W, int *pairs_out);
+
+/*
+ * saps_matching_bandwidth -- the round's gossip partners chosen from link
+ * bandwidths, as the coordinator of SAPS section II-C (Algorithm 3) does.
+ * Host only.  Steps, in the page's order:
+ *   - B_ij = B_ji = min(B_ij, B_ji) (the slower direction bounds the link);
+ *   - B*: the pairs with B_ij > b_thres (section II-A's filtered matrix);
+ *   - "recently connected" (RC) pairs: last_round[i][j] > t - t_thres;
+ *   - if the RC pairs connect every worker, the candidate pairs are B*;
+ *     otherwise they are the links (B_ij > 0) between different connected
+ *     components of the RC graph;
+ *   - a maximum matching of the candidates (Edmonds' blossom algorithm on a
+ *     general graph), searched from a relabelling of the workers drawn from
+ *     seed_t (the page's "RandomlyMaxMatch");
+ *   - workers still unmatched are paired among themselves in an order drawn
+ *     from seed_t, without regard to bandwidth;
+ *   - last_round[i][j] = last_round[j][i] = t for every pair chosen.
+ * The result is a perfect matching, so the gossip matrix (1/2 on i,i / i,j /
+ * j,i / j,j of each pair) is doubly stochastic.  Reading: "maximum match" is
+ * a matching of maximum cardinality (the blossom algorithm the page cites);
+ * bandwidth enters through b_thres and through the bridging rule.
+ *
+ *   W           even, 2 .. GC_MAX_WORKERS
+ *   bandwidth   host double [W*W], row-major, >= 0 and finite (0 = no link);
+ *               the diagonal is ignored
+ *   b_thres     B_thres (not NaN)
+ *   last_round  host int64 [W*W], row-major, in/out: the round each pair was
+ *               last matched (INT64_MIN, or any value <= t - t_thres, for
+ *               never)
+ *   t, t_thres  the round number and T_thres >= 1
+ *   pairs_out   host int [W]; pairs (pairs_out[2q], pairs_out[2q+1]), the
+ *               smaller worker first, pairs ordered by their first worker
+ * Errors: GC_ERR_INVALID.
+ */
+GC_API int saps_matching_bandwidth(int W, const double *bandwidth, double b_thres,
+                                   int64_t *last_round, int64_t t, int64_t t_thres,
+                                   uint64_t seed_t, int *pairs_out);
 
 /* Bytes of device workspace saps_mask_compact needs for n elements. */
 GC_API size_t saps_workspace_bytes(int64_t n);
