@@ -558,6 +558,9 @@ def rows(args, dev, peak):
         graphs[key] = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graphs[key]):
             fn()
+    # the ten steps in one launch: the residual stays in registers across steps
+    r_ms = torch.zeros(n, device=dev)
+    pms = gc.gc_2bit_quantize_steps(gs, r_ms, cs, cfg.threshold, out=os_, stream=stream, prepare=True)
     tm = Timer(stream)
     for i in range(reps + 3):
         flush_l2(flush)
@@ -566,15 +569,22 @@ def rows(args, dev, peak):
         tm.around("f" if i >= 3 else "w", graphs["f"].replay)
         flush_l2(flush)
         tm.around("e" if i >= 3 else "w", ten_steps)
+        flush_l2(flush)
+        tm.around("m" if i >= 3 else "w", pms)
     torch.cuda.synchronize(dev)
     ten_bytes = cfg.steps * (12.25 + 4.25) * n
+    one_launch_bytes = (cfg.steps * (4 + 0.25 + 4) + 8) * n
+    out["twobit_w1.ten_steps_one_launch"] = _row(
+        "twobit_w1", "gc_2bit_quantize_steps: 10 steps (codes + dequantised values) in one launch, residual "
+        "read and written once (L2 flushed)", one_launch_bytes, tm.ms("m"), peak, cfg.steps * n,
+        {"ten_steps_unfused_bytes_frac": round(ten_bytes / (_median(tm.ms("m")) * 1e-3) / 1e9 / peak, 3)})
     out["twobit_w1.ten_steps_graph"] = _row("twobit_w1", "10 x (gc_2bit_quantize + dequant) as one CUDA graph "
                                             "(L2 flushed before each replay)", ten_bytes, tm.ms("g"), peak,
                                             cfg.steps * n, {"eager_ms": round(_median(tm.ms("e")), 5)})
     out["twobit_w1.ten_fused_steps_graph"] = _row("twobit_w1", "10 x gc_2bit_step (W=1, NONE: quantise + "
                                                   "dequant in one launch) as one CUDA graph (L2 flushed)",
                                                   ten_bytes, tm.ms("f"), peak, cfg.steps * n)
-    del g, r, c, o, gs, cs, os_, graphs
+    del g, r, c, o, gs, cs, os_, graphs, r_ms
 
     # config 2 as one fused launch per step vs the two-launch path of the headline
     cfg2 = wl.TWOBIT_DQ_SGD

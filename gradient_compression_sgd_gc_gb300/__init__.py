@@ -16,7 +16,7 @@ Entry points (same names as the C ABI):
   qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_decode_batched, qsgd_elias_max_words,
   qsgd_elias_workspace_bytes,
   saps_round_seed, saps_matching, saps_matching_bandwidth, saps_workspace_bytes, saps_mask_compact,
-  saps_mask_compact_noalloc, saps_peer_average, saps_average_easgd_step, easgd_step,
+  saps_mask_compact_noalloc, saps_peer_average, saps_pair_average_remote, easgd_step_from_sum, saps_average_easgd_step, easgd_step,
   saps_round, gc_status_string, gc_version
 Front ends over them (per-key state, parameter rules): ``compression.py``.
 """
@@ -36,7 +36,7 @@ __all__ = [
     "GC_UPD_NONE", "GC_UPD_SGD", "GC_UPD_EASGD", "GC_MAX_WORKERS",
     "gc_status_string", "gc_version", "gc_2bit_quantize", "gc_2bit_quantize_batched",
     "gc_2bit_dequant_sum_update",
-    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed", "saps_matching_bandwidth", "gossip_matrix", "NEVER",
+    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed", "saps_matching_bandwidth", "saps_pair_average_remote", "easgd_step_from_sum", "gossip_matrix", "NEVER",
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
@@ -84,6 +84,8 @@ def load():
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
             "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
             "gc_2bit_step": (i32, [vp, i32, vp, vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
+            "saps_pair_average_remote": (i32, [vp, vp, vp, vp, vp, i64, vp]),
+            "easgd_step_from_sum": (i32, [vp, vp, i32, i64, f32, f32, vp, vp]),
             "saps_matching_bandwidth": (i32, [i32, vp, f64, vp, i64, i64, u64, vp]),
             "gc_2bit_quantize_steps": (i32, [vp, i32, vp, vp, vp, i32, i64, f32, vp]),
             "gc_2bit_step_local": (i32, [vp, i32, vp, vp, vp, f32, i32, i64, f32, i32, f32, f32, vp, vp, vp,
@@ -494,6 +496,29 @@ def gossip_matrix(pairs):
         a, b = pairs[q], pairs[q + 1]
         M[a, a] = M[b, b] = M[a, b] = M[b, a] = 0.5
     return M
+
+
+def saps_pair_average_remote(model: torch.Tensor, idx: torch.Tensor, d_count: torch.Tensor,
+                             mine: torch.Tensor, peer: torch.Tensor, stream=None, prepare: bool = False):
+    """Pair average for a worker whose peer is another process: model[idx[k]] =
+    (mine[k] + peer[k]) / 2 for k < min(count, capacity)."""
+    lib = load()
+    cap = idx.numel()
+    args = (_dev(model, "model", torch.float32), _dev(idx, "idx", torch.int32, cap),
+            _dev(d_count, "d_count", torch.int64, 1), _dev(mine, "mine", torch.float32, cap),
+            _dev(peer, "peer", torch.float32, cap), cap, _stream(stream, model))
+    return _invoke(lib.saps_pair_average_remote, args, "saps_pair_average_remote", prepare,
+                   (model, idx, d_count, mine, peer))
+
+
+def easgd_step_from_sum(model: torch.Tensor, model_sum: torch.Tensor, W: int, alpha: float, beta: float,
+                        center: torch.Tensor, stream=None, prepare: bool = False):
+    """Elastic step of one worker from the sum of all W workers' models."""
+    lib = load()
+    n = model.numel()
+    args = (_dev(model, "model", torch.float32, n), _dev(model_sum, "model_sum", torch.float32, n), int(W), n,
+            float(alpha), float(beta), _dev(center, "center", torch.float32, n), _stream(stream, model))
+    return _invoke(lib.easgd_step_from_sum, args, "easgd_step_from_sum", prepare, (model, model_sum, center))
 
 
 def saps_workspace_bytes(n: int) -> int:

@@ -92,13 +92,24 @@ __device__ __forceinline__ void warp_sum2(float& hi, float& lo) {
 }
 
 // sqrt of the double-float X + Xl, rounded to nearest fp32.
+// 1 / (2r) for the Newton correction below: the hardware reciprocal refined by
+// one step of Newton's method for 1/x (relative error near 2^-24, which the correction -- itself
+// at most half an ulp of r -- scales down to about 2^-48 of the result).
+__device__ __forceinline__ float half_recip(float r) {
+    float c0;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(c0) : "f"(r));
+    c0 = __fmul_rn(0.5f, c0);
+    const float e = __fmaf_rn(__fmul_rn(-2.0f, r), c0, 1.0f);
+    return __fmaf_rn(c0, e, c0);
+}
+
 __device__ __forceinline__ float df_sqrt(float hi, float lo) {
     const float X = __fadd_rn(hi, lo);
     const float Xl = __fsub_rn(lo, __fsub_rn(X, hi));
     if (!(X > 0.0f)) return 0.0f;
     const float r = __fsqrt_rn(X);
     const float rem = __fadd_rn(__fmaf_rn(-r, r, X), Xl);     // X + Xl - r^2
-    return __fmaf_rn(rem, __fdiv_rn(0.5f, r), r);             // r + rem / (2r)
+    return __fmaf_rn(rem, half_recip(r), r);                  // r + rem / (2r)
 }
 
 // The bucket's l2 norm, rounded to nearest fp32 (equal to the correctly
@@ -114,12 +125,7 @@ __device__ __forceinline__ float warp_norm(float hi, float lo) {
         hi = s;
         lo = __fadd_rn(__fadd_rn(lo, l2), e);
     }
-    const float X = __fadd_rn(hi, lo);
-    const float Xl = __fsub_rn(lo, __fsub_rn(X, hi));
-    if (!(X > 0.0f)) return 0.0f;
-    const float r = __fsqrt_rn(X);
-    const float rem = __fadd_rn(__fmaf_rn(-r, r, X), Xl);     // X + Xl - r^2
-    return __fmaf_rn(rem, __fdiv_rn(0.5f, r), r);             // r + rem / (2r)
+    return df_sqrt(hi, lo);
 }
 
 struct QArgs {
@@ -188,16 +194,48 @@ __device__ __forceinline__ bool all_zero(const float4 (&v)[ROUNDS], int lane) {
 // term added to sum[j][k] exactly as k_qsgd_dequant_sum adds it (one fma of
 // the level with the signed norm * unit_scale), so that a fused pass over
 // all workers equals the quantise calls followed by the dequant-sum.
-template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM>
-__device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int lane, float unit_scale,
-                                                float (&sum)[ROUNDS][4]) {
+template <int ROUNDS>
+struct BucketRegs {
+    float4 v[ROUNDS];
+};
+
+// A sum of squares below 2^-100 may have lost bits to underflow and one above
+// 2^126 overflows: such buckets (subnormal-sized or huge gradients) are redone
+// with every value scaled by the power of two that brings the bucket maximum
+// to [0.5, 1), which is exact, and the norm scaled back.  Out of line: the
+// rare path would otherwise cost the common one registers and scheduling.
+template <int ROUNDS>
+__device__ __noinline__ float rescued_norm(const BucketRegs<ROUNDS> r) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(r.v[j].x), fabsf(r.v[j].y)), fmaxf(fabsf(r.v[j].z), fabsf(r.v[j].w))));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int ex = 0;
+    frexpf(mx, &ex);
+    float h2 = 0.0f, l2 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+        acc_square(ldexpf(r.v[j].x, -ex), h2, l2);
+        acc_square(ldexpf(r.v[j].y, -ex), h2, l2);
+        acc_square(ldexpf(r.v[j].z, -ex), h2, l2);
+        acc_square(ldexpf(r.v[j].w, -ex), h2, l2);
+    }
+    warp_sum2(h2, l2);
+    return ldexpf(df_sqrt(h2, l2), ex);
+}
+
+template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM, bool RAGGED>
+__device__ __forceinline__ void quantize_bucket_body(const QArgs& a, int64_t b, int lane, float unit_scale,
+                                                     float (&sum)[ROUNDS][4]) {
     constexpr int D = 128 * ROUNDS;
     constexpr uint32_t kSignShift = FOUR ? 3 : 7;
     const float s_f = static_cast<float>(a.s);
     const uint32_t s_u = static_cast<uint32_t>(a.s);
 
     const int64_t b0 = b * D;
-    const bool full = b0 + D <= a.n;
+    const bool full = !RAGGED;
     float4 v[ROUNDS];
     if (full) {
 #pragma unroll
@@ -237,32 +275,13 @@ __device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int l
     two_sum(ha, hb, hi, e);
     const float lo = __fadd_rn(__fadd_rn(la, lb), e);
     norm = warp_norm(hi, lo);
-    // A sum of squares below 2^-100 may have lost bits to underflow and one
-    // above 2^126 overflows: such buckets (subnormal-sized or huge gradients;
-    // the test is warp-uniform) are redone with every value scaled by the
-    // power of two that brings the bucket maximum to [0.5, 1), which is exact,
-    // and the norm scaled back.
     const bool tiny = norm < 8.8817842e-16f;      // 2^-50: the sum of squares is below 2^-100
     const bool huge = !(norm < 9.2233720e18f);    // 2^63, or inf / NaN
-    if (huge || (tiny && !all_zero(v, lane))) {
-        float mx = 0.0f;
+    if (huge || (tiny && !all_zero(v, lane))) {   // warp-uniform
+        BucketRegs<ROUNDS> r;
 #pragma unroll
-        for (int j = 0; j < ROUNDS; ++j)
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        int ex = 0;
-        frexpf(mx, &ex);
-        float h2 = 0.0f, l2 = 0.0f;
-#pragma unroll
-        for (int j = 0; j < ROUNDS; ++j) {
-            acc_square(ldexpf(v[j].x, -ex), h2, l2);
-            acc_square(ldexpf(v[j].y, -ex), h2, l2);
-            acc_square(ldexpf(v[j].z, -ex), h2, l2);
-            acc_square(ldexpf(v[j].w, -ex), h2, l2);
-        }
-        warp_sum2(h2, l2);
-        norm = ldexpf(df_sqrt(h2, l2), ex);
+        for (int j = 0; j < ROUNDS; ++j) r.v[j] = v[j];
+        norm = rescued_norm<ROUNDS>(r);
     }
     }
     if (lane == 0) a.norms[b] = norm;
@@ -313,6 +332,22 @@ __device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int l
             }
         }
     }
+}
+
+// The partial last bucket (bounds-checked loads and stores), out of line.
+template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM>
+__device__ __noinline__ void quantize_bucket_ragged(const QArgs& a, int64_t b, int lane, float unit_scale,
+                                                    float (&sum)[ROUNDS][4]) {
+    quantize_bucket_body<ROUNDS, FOUR, MAXNORM, SUM, true>(a, b, lane, unit_scale, sum);
+}
+
+template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM>
+__device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int lane, float unit_scale,
+                                                float (&sum)[ROUNDS][4]) {
+    if ((b + 1) * (128 * ROUNDS) <= a.n)
+        quantize_bucket_body<ROUNDS, FOUR, MAXNORM, SUM, false>(a, b, lane, unit_scale, sum);
+    else
+        quantize_bucket_ragged<ROUNDS, FOUR, MAXNORM, SUM>(a, b, lane, unit_scale, sum);
 }
 
 // One warp per bucket; the grid covers every bucket.  For buckets of up to

@@ -845,6 +845,66 @@ k_saps_average_easgd_wide(const FusedArgs a) {
 
 
 
+// ---------------------------------------------------------------- one rank per worker
+
+// The pair average of a worker whose peer runs in another process: the peer's
+// gathered values arrive in `peer` (same order as idx), and the masked
+// coordinates become fl(fl(mine + peer) * 0.5) -- the same value the peer
+// computes (fp addition commutes), and the value k_saps_peer_average writes.
+struct RemoteAvgArgs {
+    float* model;
+    const uint32_t* idx;
+    const uint64_t* d_count;
+    const float* mine;
+    const float* peer;
+    int64_t capacity;
+};
+
+__global__ void __launch_bounds__(kThreads)
+k_saps_pair_average_remote(const RemoteAvgArgs a) {
+    const uint64_t cnt = *a.d_count;
+    const int64_t count = cnt < static_cast<uint64_t>(a.capacity) ? static_cast<int64_t>(cnt) : a.capacity;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < count; k += stride)
+        a.model[a.idx[k]] = __fmul_rn(__fadd_rn(__ldg(a.mine + k), __ldg(a.peer + k)), 0.5f);
+}
+
+// The elastic step of one worker given the sum of all W workers' models
+// (formed by an all-reduce across processes): w <- w - alpha (w - c), and
+// c <- c + beta (sum / W - c), as k_easgd does with the sum formed locally.
+struct EasgdSumArgs {
+    float* model;
+    const float* sum;
+    float* center;
+    int64_t n;
+    float alpha, beta, inv_w;
+};
+
+__global__ void __launch_bounds__(kThreads)
+k_easgd_from_sum(const EasgdSumArgs a) {
+    const int64_t nv = a.n >> 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i = gtid; i < nv; i += stride) {
+        const float4 m = ld_f4(a.model + 4 * i);
+        const float4 c = ld_f4(a.center + 4 * i);
+        const float4 sm = ld_stream_f4(a.sum + 4 * i);
+        st_stream_f4(a.model + 4 * i, make_float4(elastic(m.x, c.x, a.alpha), elastic(m.y, c.y, a.alpha),
+                                                  elastic(m.z, c.z, a.alpha), elastic(m.w, c.w, a.alpha)));
+        st_stream_f4(a.center + 4 * i,
+                     make_float4(fmaf(a.beta, __fsub_rn(__fmul_rn(sm.x, a.inv_w), c.x), c.x),
+                                 fmaf(a.beta, __fsub_rn(__fmul_rn(sm.y, a.inv_w), c.y), c.y),
+                                 fmaf(a.beta, __fsub_rn(__fmul_rn(sm.z, a.inv_w), c.z), c.z),
+                                 fmaf(a.beta, __fsub_rn(__fmul_rn(sm.w, a.inv_w), c.w), c.w)));
+    }
+    const int64_t t = (nv << 2) + gtid;
+    if (gtid < (a.n & 3)) {
+        const float c = a.center[t];
+        a.model[t] = elastic(a.model[t], c, a.alpha);
+        a.center[t] = fmaf(a.beta, __fsub_rn(__fmul_rn(a.sum[t], a.inv_w), c), c);
+    }
+}
+
 }  // namespace
 }  // namespace gc
 
@@ -1151,6 +1211,34 @@ int easgd_step(float* const* models, int W, int64_t n, float alpha, float beta, 
         k_easgd<16><<<grid, kThreads, 0, s>>>(a);
     else
         k_easgd_wide<<<grid, kThreads, 0, s>>>(a);
+    return launch_status();
+}
+
+int saps_pair_average_remote(float* model, const uint32_t* idx, const uint64_t* d_count, const float* mine,
+                             const float* peer, int64_t capacity, gc_stream_t stream) {
+    if (capacity < 0) return GC_ERR_INVALID;
+    if (capacity == 0) return GC_OK;
+    if (!model || !idx || !d_count || !mine || !peer) return GC_ERR_INVALID;
+    if (!aligned16(model) || !aligned16(idx) || !aligned16(d_count) || !aligned16(mine) || !aligned16(peer))
+        return GC_ERR_ALIGN;
+    RemoteAvgArgs a{model, idx, d_count, mine, peer, capacity};
+    const int64_t want = (capacity + kThreads - 1) / kThreads;
+    const int64_t cap_grid = static_cast<int64_t>(grid_for(8));
+    const unsigned grid = static_cast<unsigned>(want < cap_grid ? want : (cap_grid > 0 ? cap_grid : 1));
+    k_saps_pair_average_remote<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return launch_status();
+}
+
+int easgd_step_from_sum(float* model, const float* model_sum, int W, int64_t n, float alpha, float beta,
+                        float* center, gc_stream_t stream) {
+    if (n < 0 || W < 1 || !isfinite(alpha) || !isfinite(beta)) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!model || !model_sum || !center) return GC_ERR_INVALID;
+    if (!aligned16(model) || !aligned16(model_sum) || !aligned16(center)) return GC_ERR_ALIGN;
+    EasgdSumArgs a{model, model_sum, center, n, alpha, beta, static_cast<float>(1.0 / W)};
+    const int64_t items = (n >> 2) + 1;
+    const unsigned grid = static_cast<unsigned>((items + kThreads - 1) / kThreads);
+    k_easgd_from_sum<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
     return launch_status();
 }
 

@@ -438,15 +438,18 @@ __device__ __forceinline__ void step_apply(const StepArgs& a, int64_t e0, const 
     }
 }
 
-// fp32 quantise of one float4 that also returns the decoded values (+1/-1/0)
-__device__ __forceinline__ uint32_t quantize4_dec(float4& r, const float4 g, float t, int (&d)[4]) {
-    uint32_t c0 = quantize1(r.x, g.x, t), c1 = quantize1(r.y, g.y, t);
-    uint32_t c2 = quantize1(r.z, g.z, t), c3 = quantize1(r.w, g.w, t);
-    d[0] = (c0 == 3u) - (c0 == 2u);
-    d[1] = (c1 == 3u) - (c1 == 2u);
-    d[2] = (c2 == 3u) - (c2 == 2u);
-    d[3] = (c3 == 3u) - (c3 == 2u);
-    return (c0 << 6) | (c1 << 4) | (c2 << 2) | c3;
+// fp32 quantise of one float4 that also adds each element's decoded value
+// + 1 (0, 1 or 2) to byte k of `cnt` (element k of the four); after W workers
+// byte k holds (decoded sum + W) <= 2 * 64.
+__device__ __forceinline__ uint32_t quantize4_count(float4& r, const float4 g, float t, uint32_t& cnt) {
+    const uint32_t c0 = quantize1(r.x, g.x, t), c1 = quantize1(r.y, g.y, t);
+    const uint32_t c2 = quantize1(r.z, g.z, t), c3 = quantize1(r.w, g.w, t);
+    // code 11 -> 2, 10 -> 0, 00 -> 1: (c >> 1) ? (c & 1) * 2 : 1
+    const uint32_t c = (c0 << 6) | (c1 << 4) | (c2 << 2) | c3;
+    const uint32_t h = c >> 1;
+    const uint32_t f = (((h & c & 0x55u) << 1) | (~h & 0x55u));   // four (value + 1) fields, element 0 on top
+    cnt += ((f >> 6) & 3u) | (((f >> 4) & 3u) << 8) | (((f >> 2) & 3u) << 16) | ((f & 3u) << 24);
+    return c;
 }
 
 // Element offset, within a lane's share of a full tile, of its q-th group of
@@ -485,8 +488,13 @@ __device__ __forceinline__ float4 step_grad(const uint4 (&raw)[4], int q) {
                        __uint_as_float(raw[q].w));
 }
 
+// Registers bound the occupancy here: per lane the current and the next
+// worker's gradient and residual (the next one's loads are in flight while
+// the current one is quantised), the per-element counts packed four to a
+// register, and -- only with LOCAL, which needs them in the loop -- the
+// weights; otherwise weights and center are loaded after the worker loop.
 template <int KIND, bool BF16, bool LOCAL>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, (BF16 && !LOCAL) ? 3 : 2)
 k_2bit_step(const StepArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -494,19 +502,11 @@ k_2bit_step(const StepArgs a) {
     if (tile < nfull) {
         const int64_t tbase = tile * kTile;
         float4 wv[4], cv[4];
-        if (KIND != GC_UPD_NONE || LOCAL) {
+        if (LOCAL) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) wv[q] = ld_f4(a.weights + tbase + step_group<BF16>(lane, q));
         }
-        if (KIND == GC_UPD_EASGD) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) cv[q] = ld_stream_f4(a.center + tbase + step_group<BF16>(lane, q));
-        }
-        int cnt[4][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) cnt[q][k] = 0;
+        uint32_t cnt[4] = {0u, 0u, 0u, 0u};
         uint4 ga[4];
         float4 ra[4];
         step_load_grad<BF16>(a.grads.p[0], tbase, lane, ga);
@@ -530,11 +530,8 @@ k_2bit_step(const StepArgs a) {
                     st_stream_f4(a.local.p[w] + e,
                                  make_float4(fmaf(-a.local_lr, g.x, wv[q].x), fmaf(-a.local_lr, g.y, wv[q].y),
                                              fmaf(-a.local_lr, g.z, wv[q].z), fmaf(-a.local_lr, g.w, wv[q].w)));
-                int d[4];
-                c[q] = quantize4_dec(ra[q], g, a.t, d);
+                c[q] = quantize4_count(ra[q], g, a.t, cnt[q]);
                 st_stream_f4(r + e, ra[q]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cnt[q][k] += d[k];
             }
             if (BF16) {
                 // elements e..e+7 (e = tbase + 8 lane + 256 j) are the high half
@@ -559,10 +556,21 @@ k_2bit_step(const StepArgs a) {
                 }
             }
         }
+        if (KIND != GC_UPD_NONE && !LOCAL) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) wv[q] = ld_f4(a.weights + tbase + step_group<BF16>(lane, q));
+        }
+        if (KIND == GC_UPD_EASGD) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) cv[q] = ld_stream_f4(a.center + tbase + step_group<BF16>(lane, q));
+        }
+        const float bias = static_cast<float>(a.W);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float cf[4] = {static_cast<float>(cnt[q][0]), static_cast<float>(cnt[q][1]),
-                                 static_cast<float>(cnt[q][2]), static_cast<float>(cnt[q][3])};
+            const float cf[4] = {static_cast<float>(cnt[q] & 255u) - bias,
+                                 static_cast<float>((cnt[q] >> 8) & 255u) - bias,
+                                 static_cast<float>((cnt[q] >> 16) & 255u) - bias,
+                                 static_cast<float>(cnt[q] >> 24) - bias};
             step_apply<KIND>(a, tbase + step_group<BF16>(lane, q), cf, wv[q], cv[q]);
         }
     } else if (tile == nfull && a.n % kTile != 0) {
@@ -613,6 +621,105 @@ void launch_step(gc_update kind, unsigned grid, cudaStream_t s, const StepArgs& 
         case GC_UPD_NONE: k_2bit_step<GC_UPD_NONE, BF16, LOCAL><<<grid, kThreads, 0, s>>>(a); break;
         case GC_UPD_SGD: k_2bit_step<GC_UPD_SGD, BF16, LOCAL><<<grid, kThreads, 0, s>>>(a); break;
         default: k_2bit_step<GC_UPD_EASGD, BF16, LOCAL><<<grid, kThreads, 0, s>>>(a); break;
+    }
+}
+
+// ------------------------------------------------------------------ K1 (+K2 NONE) over S steps
+
+// S successive steps of one worker in one launch: step s quantises gradient
+// g_s into codes_s with the residual carried from step s-1 and, when out is
+// given, writes the dequantised values out_s (+t, -t, 0).  The residual stays
+// in registers between steps and is read and written once.  Bit-identical to
+// S calls of gc_2bit_quantize (+ gc_2bit_dequant_sum_update NONE with W = 1).
+struct StepsArgs {
+    PtrTable<const void*> grads;
+    PtrTable<uint32_t*> codes;
+    PtrTable<float*> out;
+    float* res;
+    int S;
+    bool has_out;
+    int64_t n;
+    float t;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads)
+k_2bit_steps(const StepsArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t tile = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nfull = a.n / kTile;
+    if (tile < nfull) {
+        const int64_t tbase = tile * kTile;
+        float4 ra[4];
+        uint4 ga[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ra[q] = ld_f4(a.res + tbase + step_group<BF16>(lane, q));
+        step_load_grad<BF16>(a.grads.p[0], tbase, lane, ga);
+        for (int st = 0; st < a.S; ++st) {
+            uint4 gb[4];
+            if (st + 1 < a.S) step_load_grad<BF16>(a.grads.p[st + 1], tbase, lane, gb);
+            uint32_t c[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                int d[4];
+                const float4 g = step_grad<BF16>(ga, q);
+                uint32_t cnt = 0u;
+                c[q] = quantize4_count(ra[q], g, a.t, cnt);
+                d[0] = static_cast<int>(cnt & 255u) - 1;
+                d[1] = static_cast<int>((cnt >> 8) & 255u) - 1;
+                d[2] = static_cast<int>((cnt >> 16) & 255u) - 1;
+                d[3] = static_cast<int>(cnt >> 24) - 1;
+                if (a.has_out)
+                    st_stream_f4(a.out.p[st] + tbase + step_group<BF16>(lane, q),
+                                 make_float4(static_cast<float>(d[0]) * a.t, static_cast<float>(d[1]) * a.t,
+                                             static_cast<float>(d[2]) * a.t, static_cast<float>(d[3]) * a.t));
+            }
+            if (BF16) {
+                uint16_t* ch = reinterpret_cast<uint16_t*>(a.codes.p[st]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int64_t e = tbase + 8 * lane + 256 * j;
+                    ch[2 * (e >> 4) + 1 - ((e >> 3) & 1)] = static_cast<uint16_t>((c[2 * j] << 8) | c[2 * j + 1]);
+                }
+            } else {
+                uint8_t* cb = reinterpret_cast<uint8_t*>(a.codes.p[st]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    cb[code_byte(tbase + step_group<BF16>(lane, q))] = static_cast<uint8_t>(c[q]);
+            }
+            if (st + 1 < a.S) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ga[q] = gb[q];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            st_stream_f4(a.res + tbase + step_group<BF16>(lane, q), ra[q]);
+    } else if (tile == nfull && a.n % kTile != 0) {
+        const int64_t nwords = (a.n + 15) >> 4;
+        float* r = a.res;
+        for (int j = 0; j < 4; ++j) {
+            const int64_t e0 = nfull * kTile + 128 * j + 4 * lane;
+            float rr[4];
+            for (int k = 0; k < 4; ++k) rr[k] = e0 + k < a.n ? r[e0 + k] : 0.0f;
+            for (int st = 0; st < a.S; ++st) {
+                uint32_t cbits = 0;
+                for (int k = 0; k < 4; ++k) {
+                    const int64_t e = e0 + k;
+                    if (e < a.n) {
+                        const float gval = BF16 ? __uint_as_float(static_cast<uint32_t>(
+                                                      static_cast<const uint16_t*>(a.grads.p[st])[e]) << 16)
+                                                : static_cast<const float*>(a.grads.p[st])[e];
+                        const uint32_t c = quantize1(rr[k], gval, a.t);
+                        cbits |= c << (6 - 2 * k);
+                        if (a.has_out) a.out.p[st][e] = static_cast<float>((c == 3u) - (c == 2u)) * a.t;
+                    }
+                }
+                if ((e0 >> 4) < nwords) reinterpret_cast<uint8_t*>(a.codes.p[st])[code_byte(e0)] = static_cast<uint8_t>(cbits);
+            }
+            for (int k = 0; k < 4; ++k)
+                if (e0 + k < a.n) r[e0 + k] = rr[k];
+        }
     }
 }
 
@@ -1005,6 +1112,35 @@ int gc_2bit_step_local(const void* const* grads, gc_dtype dtype, float* const* r
     if (!local_weights) return GC_ERR_INVALID;
     return step_entry(grads, dtype, residuals, codes, local_weights, local_lr, W, n, threshold, kind, lr, alpha,
                       center, weights, out, stream);
+}
+
+int gc_2bit_quantize_steps(const void* const* grads, gc_dtype dtype, float* residual, uint32_t* const* codes,
+                           float* const* out, int S, int64_t n, float threshold, gc_stream_t stream) {
+    if (n < 0 || S < 1 || S > GC_MAX_WORKERS || !finite_pos(threshold)) return GC_ERR_INVALID;
+    if (dtype != GC_F32 && dtype != GC_BF16) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!grads || !residual || !codes) return GC_ERR_INVALID;
+    if (!aligned16(residual)) return GC_ERR_ALIGN;
+    StepsArgs a;
+    for (int st = 0; st < S; ++st) {
+        if (!grads[st] || !codes[st] || (out && !out[st])) return GC_ERR_INVALID;
+        if (!aligned16(grads[st]) || !aligned16(codes[st]) || (out && !aligned16(out[st]))) return GC_ERR_ALIGN;
+        a.grads.p[st] = grads[st];
+        a.codes.p[st] = codes[st];
+        a.out.p[st] = out ? out[st] : nullptr;
+    }
+    a.res = residual;
+    a.S = S;
+    a.has_out = out != nullptr;
+    a.n = n;
+    a.t = threshold;
+    const unsigned grid = blocks_for_tiles((n + 511) / 512);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == GC_BF16)
+        k_2bit_steps<true><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_2bit_steps<false><<<grid, kThreads, 0, s>>>(a);
+    return launch_status();
 }
 
 int gc_2bit_quantize_local(const void* const* grads, gc_dtype dtype, float* const* residuals,

@@ -589,6 +589,41 @@ GC_API int easgd_step(float *const *models, int W, int64_t n, float alpha, float
                float *center, gc_stream_t stream);
 
 /*
+ * saps_pair_average_remote -- the SAPS pair average (section II-B/II-C: the
+ * masked coordinates of both peers become their average) for a worker whose
+ * peer lives in another process: after the two have exchanged their gathered
+ * values (K floats each way, the indices being the same on both sides),
+ *   model[idx[k]] = fl(fl(mine[k] + peer[k]) * 0.5)   for k < min(*d_count, capacity)
+ * -- the value the peer writes on its side and saps_peer_average writes.
+ *
+ *   model      device fp32 [n], in/out
+ *   idx        device uint32 [capacity], from saps_mask_compact (unchecked)
+ *   d_count    device uint64, the masked count
+ *   mine, peer device fp32 [capacity]: this worker's and the peer's values
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int saps_pair_average_remote(float *model, const uint32_t *idx,
+                                    const uint64_t *d_count, const float *mine,
+                                    const float *peer, int64_t capacity,
+                                    gc_stream_t stream);
+
+/*
+ * easgd_step_from_sum -- easgd_step for one worker when the W workers'
+ * models live in different processes: model_sum holds the elementwise sum of
+ * all W pre-step models (e.g. an all-reduce of a copy of each model), and
+ *   model[i]  = model[i] - alpha * (model[i] - center[i])
+ *   center[i] = center[i] + beta * (model_sum[i] / W - center[i])
+ * with the same fp32 operations as easgd_step (the sum's order is the
+ * all-reduce's).  IMerge design notes, EASGD local and global updates.
+ *
+ *   model, center  device fp32 [n], in/out;  model_sum device fp32 [n]
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int easgd_step_from_sum(float *model, const float *model_sum, int W, int64_t n,
+                               float alpha, float beta, float *center,
+                               gc_stream_t stream);
+
+/*
  * saps_mask_compact_noalloc -- no counterpart on the pages: the same
  * compaction as saps_mask_compact, for callers that cannot provide or
  * allocate a workspace (a plug-in inside a host framework whose device

@@ -66,6 +66,7 @@ def _load():
             "orc_l2norm_fp32": (f32, [vp, i64]),
             "orc_qsgd_quantize": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_qsgd_scaled_values": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
+            "orc_easgd_step_from_sum": (None, [vp, vp, i32, i64, f64, f64, vp]),
             "orc_qsgd_scaled_values_maxnorm": (None, [vp, i64, i64, i32, u64, i32, i64, vp]),
             "orc_qsgd_quantize_maxnorm": (None, [vp, i64, i64, i32, u64, i32, i64, vp, vp]),
             "orc_elias_omega_bits": (i32, [ctypes.c_uint32, ctypes.c_char_p]),
@@ -342,3 +343,14 @@ def easgd_step(models, alpha: float, beta: float, center: np.ndarray) -> None:
     _check(center, np.float64, "center", n)
     _load().orc_easgd_step(_ptr_array(models), W, n, float(np.float32(alpha)),
                            float(np.float32(beta)), _ptr(center))
+
+
+def easgd_step_from_sum(model: np.ndarray, model_sum: np.ndarray, W: int, alpha: float, beta: float,
+                        center: np.ndarray) -> None:
+    """One worker's EASGD step given the sum of all W workers' models (fp64, in place)."""
+    n = center.size
+    _check(model, np.float64, "model", n)
+    _check(model_sum, np.float64, "model_sum", n)
+    _check(center, np.float64, "center", n)
+    _load().orc_easgd_step_from_sum(_ptr(model), _ptr(model_sum), int(W), n, float(np.float32(alpha)),
+                                    float(np.float32(beta)), _ptr(center))

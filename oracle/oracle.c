@@ -564,6 +564,22 @@ void orc_easgd_step(double *const *models, int W, int64_t n, double alpha,
     }
 }
 
+/*
+ * [EA] the same two updates for one worker when the other workers' models
+ * are only known through their elementwise sum (one process per worker):
+ * mean = sum / W; model <- model - alpha (model - c); c <- (1-beta) c + beta mean.
+ */
+void orc_easgd_step_from_sum(double *model, const double *sum, int W, int64_t n,
+                             double alpha, double beta, double *center)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        double mean = sum[i] / (double)W;
+        double c = center[i];
+        model[i] = model[i] - alpha * (model[i] - c);
+        center[i] = (1.0 - beta) * c + beta * mean;
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* [QS] Knowl 2: lossless Elias-omega coding of the (norm, sign, level)     */
 /* tuple, dense regime ("offset Elias coding": Elias'(k) = Elias(k + 1)).    */

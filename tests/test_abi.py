@@ -270,6 +270,39 @@ def test_one_pass_entry_validation():
 
 
 
+def test_step_and_multistep_validation():
+    """gc_2bit_step takes fp32 and bf16; gc_2bit_step_local needs its local
+    weight pointers and the weights; gc_2bit_quantize_steps checks S, the
+    residual and every step's buffers.  Host validation only (no launch)."""
+    p2 = _ptrs(FAKE, FAKE)
+    f = "gc_2bit_step"
+    #      grads dtype res codes W  n     t    kind lr   alpha center weights out  stream
+    assert _call(f, p2, 2, p2, p2, 2, 1000, 0.5, 1, 0.1, 0.0, None, FAKE, None, None) == gc.GC_ERR_INVALID   # dtype
+    assert _call(f, p2, 1, p2, p2, 2, 1000, 0.5, 1, 0.1, 0.0, None, None, None, None) == gc.GC_ERR_INVALID   # weights
+    assert _call(f, p2, 1, p2, p2, 2, 0, 0.5, 1, 0.1, 0.0, None, FAKE, None, None) == gc.GC_OK            # bf16, n == 0
+    g = "gc_2bit_step_local"
+    assert _call(g, p2, 1, p2, p2, None, 0.1, 2, 1000, 0.5, 1, 0.1, 0.0, None, FAKE, None, None) == gc.GC_ERR_INVALID
+    assert _call(g, p2, 1, p2, p2, _ptrs(FAKE, 0), 0.1, 2, 1000, 0.5, 1, 0.1, 0.0, None, FAKE, None,
+                 None) == gc.GC_ERR_INVALID
+    assert _call(g, p2, 1, p2, p2, _ptrs(FAKE, MISALIGNED), 0.1, 2, 1000, 0.5, 1, 0.1, 0.0, None, FAKE, None,
+                 None) == gc.GC_ERR_ALIGN
+    assert _call(g, p2, 1, p2, p2, p2, float("nan"), 2, 1000, 0.5, 1, 0.1, 0.0, None, FAKE, None,
+                 None) == gc.GC_ERR_INVALID
+    # kind NONE with local weights still needs the weights (read for W_loc)
+    assert _call(g, p2, 1, p2, p2, p2, 0.1, 2, 1000, 0.5, 0, 0.0, 0.0, None, None, FAKE, None) == gc.GC_ERR_INVALID
+    h = "gc_2bit_quantize_steps"
+    #      grads dtype residual codes out S  n     t
+    assert _call(h, p2, 0, FAKE, p2, None, 0, 1000, 0.5, None) == gc.GC_ERR_INVALID        # S
+    assert _call(h, p2, 0, FAKE, p2, None, 65, 1000, 0.5, None) == gc.GC_ERR_INVALID       # S > 64
+    assert _call(h, p2, 0, None, p2, None, 2, 1000, 0.5, None) == gc.GC_ERR_INVALID        # residual
+    assert _call(h, p2, 0, MISALIGNED, p2, None, 2, 1000, 0.5, None) == gc.GC_ERR_ALIGN
+    assert _call(h, p2, 0, FAKE, _ptrs(FAKE, 0), None, 2, 1000, 0.5, None) == gc.GC_ERR_INVALID
+    assert _call(h, p2, 0, FAKE, p2, _ptrs(FAKE, MISALIGNED), 2, 1000, 0.5, None) == gc.GC_ERR_ALIGN
+    assert _call(h, p2, 0, FAKE, p2, None, 2, 1000, -0.5, None) == gc.GC_ERR_INVALID       # threshold
+    assert _call(h, p2, 3, FAKE, p2, None, 2, 1000, 0.5, None) == gc.GC_ERR_INVALID        # dtype
+    assert _call(h, p2, 0, FAKE, p2, None, 2, 0, 0.5, None) == gc.GC_OK                    # n == 0
+
+
 def test_binding_wants_the_whole_matching():
     """A matching shorter than the worker list is refused on the host (a short
     list padded with zeros could still be a permutation)."""

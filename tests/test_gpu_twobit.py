@@ -444,3 +444,51 @@ def test_fused_step_against_oracle(n, W):
         np.testing.assert_array_equal(host_u32(codes[w]), c_ref[w])
         np.testing.assert_array_equal(host_f32(res[w]).view(np.uint32), r_ref[w].view(np.uint32))
     assert_close(host_f32(w0), w_ref, scale, what="weights")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("n,S", [(1, 1), (517, 3), (1 << 20, 10), (100_003, 7)])
+def test_multi_step_quantize_bit_exact_against_oracle(n, S, dtype):
+    """gc_2bit_quantize_steps: S successive steps of one worker in one launch
+    (the configured ten steps of 2^20 elements at t = 0.5 among them), each
+    step's codes and dequantised values and the final residual bit-exact with
+    the oracle run step by step."""
+    t = 0.5
+    grads = [wl.normal(n, 1.0, 400 + st, device=DEV, dtype=dtype) for st in range(S)]
+    r = wl.normal(n, 0.2, 420, device=DEV)
+    r_ref = host_f32(r).copy()
+    codes = [guarded(gc.code_words(n), torch.int32) for _ in range(S)]
+    outs = [guarded(n, torch.float32) for _ in range(S)]
+    gc.gc_2bit_quantize_steps(grads, r, [c[:gc.code_words(n)] for c in codes], t, out=[o[:n] for o in outs])
+    torch.cuda.synchronize()
+    for st in range(S):
+        c_ref = oracle.twobit_quantize(_grad_host(grads[st]), r_ref, t)
+        np.testing.assert_array_equal(host_u32(codes[st][:gc.code_words(n)]), c_ref)
+        d_ref = oracle.twobit_dequant_sum_update([c_ref], n, t, oracle.KIND_NONE)
+        np.testing.assert_array_equal(host_f32(outs[st][:n]).astype(np.float64), d_ref)
+        check_guard(codes[st], gc.code_words(n))
+        check_guard(outs[st], n)
+    np.testing.assert_array_equal(host_f32(r).view(np.uint32), r_ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("with_out", [False, True], ids=["codes", "codes+out"])
+def test_multi_step_equals_separate_calls(with_out):
+    n, S, t = 262_144 + 37, 5, 2e-3
+    grads = [wl.normal(n, 1e-3, 440 + st, device=DEV) for st in range(S)]
+    r0 = wl.normal(n, 1e-3, 460, device=DEV)
+    ra, rb = r0.clone(), r0.clone()
+    ca = [torch.empty(gc.code_words(n), dtype=torch.int32, device=DEV) for _ in range(S)]
+    cb = [torch.full((gc.code_words(n),), 9, dtype=torch.int32, device=DEV) for _ in range(S)]
+    oa = [torch.empty(n, device=DEV) for _ in range(S)]
+    ob = [torch.empty(n, device=DEV) for _ in range(S)]
+    for st in range(S):
+        gc.gc_2bit_quantize(grads[st], ra, ca[st], t)
+        if with_out:
+            gc.gc_2bit_dequant_sum_update([ca[st]], n, t, gc.GC_UPD_NONE, out=oa[st])
+    gc.gc_2bit_quantize_steps(grads, rb, cb, t, out=ob if with_out else None)
+    torch.cuda.synchronize()
+    assert torch.equal(ra.view(torch.int32), rb.view(torch.int32))
+    for st in range(S):
+        assert torch.equal(ca[st], cb[st])
+        if with_out:
+            assert torch.equal(oa[st].view(torch.int32), ob[st].view(torch.int32))

@@ -166,3 +166,30 @@ def test_easgd_hand_example():
     c = np.array([0.0])
     oracle.easgd_step(m, 0.5, 0.25, c)
     assert m[0][0] == 0.5 and m[1][0] == 1.5 and c[0] == 0.5
+
+
+def test_easgd_from_sum_equals_the_all_worker_step():
+    """The one-worker form used when workers are separate processes: given the
+    elementwise sum of the W pre-step models (summed in worker order, as the
+    all-worker step sums), each worker's update and the center equal the
+    all-worker EASGD step; alpha = 0 leaves the model, beta = 1 makes the
+    center the mean."""
+    rng = np.random.default_rng(12)
+    W, n = 5, 777
+    models = [rng.normal(0, 0.05, n) for _ in range(W)]
+    center = rng.normal(0, 0.05, n)
+    total = np.zeros(n)
+    for m in models:
+        total = total + m
+    ref = [m.copy() for m in models]
+    rc = center.copy()
+    oracle.easgd_step(ref, 0.9, 0.5, rc)
+    for k in range(W):
+        m, c = models[k].copy(), center.copy()
+        oracle.easgd_step_from_sum(m, total, W, 0.9, 0.5, c)
+        np.testing.assert_array_equal(m, ref[k])
+        np.testing.assert_array_equal(c, rc)
+    m, c = models[0].copy(), center.copy()
+    oracle.easgd_step_from_sum(m, total, W, 0.0, 1.0, c)
+    np.testing.assert_array_equal(m, models[0])
+    np.testing.assert_array_equal(c, total / W)
