@@ -72,6 +72,8 @@ def _load():
             "orc_elias_omega_bits": (i32, [ctypes.c_uint32, ctypes.c_char_p]),
             "orc_qsgd_elias_encode": (i64, [vp, vp, i64, i64, i32, vp, vp]),
             "orc_qsgd_elias_decode": (None, [vp, vp, i64, i64, i32, vp, vp]),
+            "orc_qsgd_elias_encode_sparse": (i64, [vp, vp, i64, i64, i32, vp, vp]),
+            "orc_qsgd_elias_decode_sparse": (i64, [vp, vp, i64, i64, i32, vp, vp]),
             "orc_qsgd_dequant_sum": (None, [vp, vp, i32, i64, i64, i32, f64, vp]),
             "orc_saps_mask_compact": (i64, [i64, f64, u64, vp, i32, i64, vp, vp, i64]),
             "orc_saps_matching": (i32, [u64, i32, vp]),
@@ -354,3 +356,36 @@ def easgd_step_from_sum(model: np.ndarray, model_sum: np.ndarray, W: int, alpha:
     _check(center, np.float64, "center", n)
     _load().orc_easgd_step_from_sum(_ptr(model), _ptr(model_sum), int(W), n, float(np.float32(alpha)),
                                     float(np.float32(beta)), _ptr(center))
+
+
+def qsgd_elias_sparse_max_words(n: int, bucket: int) -> int:
+    """Upper bound on the sparse-regime stream: per bucket 32 norm bits plus
+    at most 18 bits per coordinate (distances sum to the bucket length and
+    |omega(g)| <= g + 2; sign 1 bit; omega(level) <= 14 bits) and 2 bits."""
+    nb = (n + bucket - 1) // bucket
+    return nb * (1 + (18 * bucket + 2 + 31) // 32) + 1
+
+
+def qsgd_elias_encode_sparse(codes: np.ndarray, norms: np.ndarray, n: int, bucket: int, s: int):
+    """Knowl 2 sparse regime (distances between non-zero coordinates).
+    Returns (words uint32 [total], offsets uint32 [nbuckets + 1])."""
+    _check(codes, np.uint8, "codes", qsgd_code_bytes(n, s))
+    nb = (n + bucket - 1) // bucket
+    _check(norms, np.float32, "norms", nb)
+    words = np.zeros(qsgd_elias_sparse_max_words(n, bucket), dtype=np.uint32)
+    offsets = np.zeros(nb + 1, dtype=np.uint32)
+    total = int(_load().orc_qsgd_elias_encode_sparse(_ptr(codes), _ptr(norms), n, bucket, s, _ptr(words),
+                                                     _ptr(offsets)))
+    return words[:total].copy(), offsets
+
+
+def qsgd_elias_decode_sparse(words: np.ndarray, offsets: np.ndarray, n: int, bucket: int, s: int):
+    """Inverse of qsgd_elias_encode_sparse: (codes, norms, overshooting buckets)."""
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.uint32)
+    nb = (n + bucket - 1) // bucket
+    codes = np.zeros(qsgd_code_bytes(n, s), dtype=np.uint8)
+    norms = np.zeros(nb, dtype=np.float32)
+    bad = int(_load().orc_qsgd_elias_decode_sparse(_ptr(words), _ptr(offsets), n, bucket, s, _ptr(codes),
+                                                   _ptr(norms)))
+    return codes, norms, bad

@@ -723,3 +723,97 @@ void orc_qsgd_elias_decode(const uint32_t *words, const uint32_t *offsets, int64
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* [QS] Knowl 2, sparse regimes: only the non-zero coordinates are sent.    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Items 1 (s >= 2) and 1' (s = 1) of Knowl 2: the distances between
+ * non-zero coordinates are coded with Elias omega.  Reading used for the
+ * format (the page gives what is coded, not the layout), with the stream
+ * conventions of the dense code above (most significant bit first, every
+ * bucket on a word boundary, its fp32 norm first, an offsets table):
+ *   for each coordinate i of the bucket (0-based within it) whose level is
+ *   not 0, in order:  Elias-omega(i - p)  (p = the previous such i, or -1),
+ *                     one sign bit (1 = negative),
+ *                     Elias-omega(level)  (only when s >= 2; for s = 1 every
+ *                                          sent level is 1);
+ *   then Elias-omega(len - p) with len the bucket's length: the running
+ *   position reaches len exactly, which ends the bucket.
+ * A level-0 coordinate carries nothing and decodes with sign 0.
+ */
+int64_t orc_qsgd_elias_encode_sparse(const uint8_t *codes, const float *norms, int64_t n,
+                                     int64_t d, int s, uint32_t *words, uint32_t *offsets)
+{
+    int64_t nbuckets = (n + d - 1) / d;
+    orc_bitwriter w = {words, 0};
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        offsets[b] = (uint32_t)(w.pos / 32);
+        uint32_t nb;
+        memcpy(&nb, &norms[b], sizeof nb);
+        for (int i = 31; i >= 0; --i)
+            put_bit(&w, (int)((nb >> i) & 1u));
+        int64_t lo = b * d;
+        int64_t len = (b + 1) * d < n ? d : n - lo;
+        int64_t p = -1;
+        for (int64_t i = 0; i < len; ++i) {
+            int sign, level;
+            qsgd_code_at(codes, lo + i, s, &sign, &level);
+            if (level == 0)
+                continue;
+            put_omega(&w, (uint32_t)(i - p));
+            put_bit(&w, sign);
+            if (s >= 2)
+                put_omega(&w, (uint32_t)level);
+            p = i;
+        }
+        put_omega(&w, (uint32_t)(len - p));
+        w.pos = (w.pos + 31) / 32 * 32;
+    }
+    offsets[nbuckets] = (uint32_t)(w.pos / 32);
+    return w.pos / 32;
+}
+
+/*
+ * Inverse of orc_qsgd_elias_encode_sparse.  Returns the number of buckets
+ * whose distances overshoot the bucket (a stream this encoder did not
+ * write); such a bucket keeps the coordinates decoded before the overshoot.
+ */
+int64_t orc_qsgd_elias_decode_sparse(const uint32_t *words, const uint32_t *offsets, int64_t n,
+                                     int64_t d, int s, uint8_t *codes, float *norms)
+{
+    int64_t nbuckets = (n + d - 1) / d;
+    int64_t bad = 0;
+    int64_t nbytes = s <= 7 ? (n + 1) / 2 : n;
+    for (int64_t k = 0; k < nbytes; ++k)
+        codes[k] = 0;
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        orc_bitreader r = {words, (int64_t)offsets[b] * 32};
+        uint32_t nb = 0;
+        for (int i = 0; i < 32; ++i)
+            nb = (nb << 1) | (uint32_t)get_bit(&r);
+        memcpy(&norms[b], &nb, sizeof nb);
+        int64_t lo = b * d;
+        int64_t len = (b + 1) * d < n ? d : n - lo;
+        int64_t p = -1;
+        for (;;) {
+            p += (int64_t)get_omega(&r);
+            if (p >= len) {
+                if (p > len)
+                    ++bad;
+                break;
+            }
+            uint32_t sign = (uint32_t)get_bit(&r);
+            uint32_t level = s >= 2 ? get_omega(&r) : 1u;
+            int64_t i = lo + p;
+            if (s <= 7) {
+                uint32_t code = (sign << 3) | (level & 7u);
+                codes[i / 2] |= (uint8_t)(i % 2 == 0 ? code << 4 : code);
+            } else {
+                codes[i] = (uint8_t)((sign << 7) | (level & 127u));
+            }
+        }
+    }
+    return bad;
+}

@@ -61,6 +61,10 @@ def test_easgd_from_sum_against_oracle(n, W):
     gc.easgd_step(ref_m, 0.9, 0.9, ref_c)
     hm = [host_f32(m).astype(np.float64) for m in models]
     hc = host_f32(center).astype(np.float64)
+    # the terms of w - alpha (w - c): w, alpha w, alpha c; and of
+    # c + beta (sum / W - c): c, beta |w_k| / W summed, beta c
+    scale = [np.abs(m) + 0.9 * (np.abs(m) + np.abs(hc)) for m in hm]
+    cscale = np.abs(hc) + 0.9 * (sum(np.abs(m) for m in hm) / W + np.abs(hc))
     oracle.easgd_step(hm, 0.9, 0.9, hc)
     for k in range(W):
         m, c = models[k].clone(), center.clone()
@@ -68,8 +72,8 @@ def test_easgd_from_sum_against_oracle(n, W):
         torch.cuda.synchronize()
         assert torch.equal(m.view(torch.int32), ref_m[k].view(torch.int32))
         assert torch.equal(c.view(torch.int32), ref_c.view(torch.int32))
-        assert_close(host_f32(m), hm[k], np.abs(hm[k]) + 0.9 * np.abs(hc), what="model")
-    assert_close(host_f32(ref_c), hc, np.abs(hc) + 1.0, what="center")
+        assert_close(host_f32(m), hm[k], scale[k], what="model")
+    assert_close(host_f32(ref_c), hc, cscale, what="center")
 
 
 @pytest.fixture
