@@ -675,6 +675,26 @@ def rows(args, dev, peak):
         out[f"{qcfg.name}.elias_decode"] = _row(qcfg.name, "qsgd_elias_decode",
                                                 4 * total + 4 * (nb + 1) + cb + 4 * nb, tm.ms("x"), peak, n,
                                                 {"issue": issue_roofline(f"elias_decode_s{s}", tm.ms("x"))})
+        # the sparse-regime code (distances between non-zero coordinates) of the
+        # same codes, and its decode
+        scap = gc.qsgd_elias_sparse_max_words(n, qcfg.bucket)
+        swords = torch.empty(scap, dtype=torch.int32, device=dev)
+        soffs = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+        pse = gc.qsgd_elias_encode_sparse(codes[0], norms[0], n, qcfg.bucket, s, swords, soffs, ews, stream=stream,
+                                          prepare=True)
+        psd = gc.qsgd_elias_decode_sparse(swords, soffs, n, qcfg.bucket, s, dcodes, dnorms, stream=stream,
+                                          prepare=True)
+        for i in range(22):
+            tm.around("se" if i >= 2 else "w", pse)
+            tm.around("sd" if i >= 2 else "w", psd)
+        torch.cuda.synchronize(dev)
+        stotal = int(soffs[nb].item())
+        out[f"{qcfg.name}.elias_sparse_encode"] = _row(
+            qcfg.name, "qsgd_elias_encode_sparse (count + encode)", cb + 4 * nb + 4 * stotal + 4 * (nb + 1),
+            tm.ms("se"), peak, n, {"bits_per_coord": round(32 * stotal / n, 4)})
+        out[f"{qcfg.name}.elias_sparse_decode"] = _row(
+            qcfg.name, "qsgd_elias_decode_sparse", 4 * stotal + 4 * (nb + 1) + cb + 4 * nb, tm.ms("sd"), peak, n)
+        del swords, soffs
         # the W workers' streams in one launch (the receiver's decode before the sum)
         bcodes = [torch.empty(cb, dtype=torch.uint8, device=dev) for _ in range(W)]
         bnorms = [torch.empty(nb, device=dev) for _ in range(W)]

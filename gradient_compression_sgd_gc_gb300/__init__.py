@@ -14,6 +14,7 @@ Entry points (same names as the C ABI):
   gc_compensated_sum_update,
   qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum, qsgd_step,
   qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_decode_batched, qsgd_elias_max_words,
+  qsgd_elias_encode_sparse, qsgd_elias_decode_sparse, qsgd_elias_sparse_max_words,
   qsgd_elias_workspace_bytes,
   saps_round_seed, saps_matching, saps_matching_bandwidth, saps_workspace_bytes, saps_mask_compact,
   saps_mask_compact_noalloc, saps_peer_average, saps_pair_average_remote, easgd_step_from_sum, saps_average_easgd_step, easgd_step,
@@ -36,7 +37,8 @@ __all__ = [
     "GC_UPD_NONE", "GC_UPD_SGD", "GC_UPD_EASGD", "GC_MAX_WORKERS",
     "gc_status_string", "gc_version", "gc_2bit_quantize", "gc_2bit_quantize_batched",
     "gc_2bit_dequant_sum_update",
-    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed", "saps_matching_bandwidth", "saps_pair_average_remote", "easgd_step_from_sum", "gossip_matrix", "NEVER",
+    "gc_compensated_sum_update", "qsgd_quantize", "qsgd_dequant_sum", "saps_round_seed", "saps_matching_bandwidth", "qsgd_elias_encode_sparse", "qsgd_elias_decode_sparse",
+    "qsgd_elias_sparse_max_words", "saps_pair_average_remote", "easgd_step_from_sum", "gossip_matrix", "NEVER",
     "saps_matching", "saps_workspace_bytes", "saps_mask_compact", "saps_peer_average",
     "easgd_step", "code_words", "qsgd_code_bytes", "qsgd_num_buckets",
     "saps_mask_compact_noalloc", "GC_NOALLOC_MAX_N", "PreparedCall", "saps_average_easgd_step",
@@ -84,6 +86,9 @@ def load():
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
             "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
             "gc_2bit_step": (i32, [vp, i32, vp, vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
+            "qsgd_elias_encode_sparse": (i32, [vp, vp, i64, i32, i32, vp, u64, vp, vp, sz, vp]),
+            "qsgd_elias_sparse_max_words": (u64, [i64, i32]),
+            "qsgd_elias_decode_sparse": (i32, [vp, vp, i64, i32, i32, vp, vp, vp, vp]),
             "saps_pair_average_remote": (i32, [vp, vp, vp, vp, vp, i64, vp]),
             "easgd_step_from_sum": (i32, [vp, vp, i32, i64, f32, f32, vp, vp]),
             "saps_matching_bandwidth": (i32, [i32, vp, f64, vp, i64, i64, u64, vp]),
@@ -421,6 +426,41 @@ def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket
     keep = (words, offsets, codes, norms) + (() if status is None else (status,))
     return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
 
+
+
+def qsgd_elias_sparse_max_words(n: int, bucket: int) -> int:
+    return int(load().qsgd_elias_sparse_max_words(int(n), int(bucket)))
+
+
+def qsgd_elias_encode_sparse(codes: torch.Tensor, norms: torch.Tensor, n: int, bucket: int, s_levels: int,
+                             words: torch.Tensor, offsets: torch.Tensor, workspace: torch.Tensor,
+                             stream=None, prepare: bool = False):
+    """Sparse-regime Elias stream of QSGD codes (Knowl 2 items 1 and 1'):
+    distances between non-zero coordinates, signs, and levels when s >= 2."""
+    lib = load()
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _dev(norms, "norms", torch.float32, nb), int(n), int(bucket), int(s_levels),
+            _dev(words, "words", torch.int32), words.numel(),
+            _dev(offsets, "offsets", torch.int32, nb + 1),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream, codes))
+    return _invoke(lib.qsgd_elias_encode_sparse, args, "qsgd_elias_encode_sparse", prepare,
+                   (codes, norms, words, offsets, workspace))
+
+
+def qsgd_elias_decode_sparse(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket: int, s_levels: int,
+                             codes: torch.Tensor, norms: torch.Tensor, status: torch.Tensor | None = None,
+                             stream=None, prepare: bool = False):
+    """Inverse of qsgd_elias_encode_sparse; ``status`` receives GC_ERR_CORRUPT."""
+    lib = load()
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_dev(words, "words", torch.int32), _dev(offsets, "offsets", torch.int32, nb + 1),
+            int(n), int(bucket), int(s_levels),
+            _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _dev(norms, "norms", torch.float32, nb),
+            None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words))
+    keep = (words, offsets, codes, norms) + (() if status is None else (status,))
+    return _invoke(lib.qsgd_elias_decode_sparse, args, "qsgd_elias_decode_sparse", prepare, keep)
 
 
 def qsgd_elias_decode_batched(words, offsets, n: int, bucket: int, s_levels: int, codes, norms,

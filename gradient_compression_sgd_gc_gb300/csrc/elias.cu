@@ -875,6 +875,329 @@ int decode_stage_words(uint32_t* cap) {
     return GC_OK;
 }
 
+// ================================================================ sparse regimes
+//
+// QSGD Knowl 2, items 1 (s >= 2) and 1' (s = 1): only the non-zero
+// coordinates are sent.  Per bucket: the 32 norm bits, then for each
+// coordinate i (0-based within the bucket) whose level is not 0, in order,
+// Elias-omega(i - p) (p the previous such i, or -1), one sign bit and, when
+// s >= 2, Elias-omega(level); then Elias-omega(len - p) closes the bucket.
+// Same stream conventions as the dense code above (most significant bit
+// first, buckets on word boundaries, an offsets table).
+//
+// Encode = count + encode launches as for the dense code: one warp per
+// bucket, lane l owning coordinates [l d/32, (l+1) d/32); a lane's distances
+// need the last non-zero coordinate before its range, which a warp max-scan
+// supplies.  Decode: one thread per bucket, after its CTA has zeroed the
+// code bytes of its buckets.
+
+// Length of Elias-omega(N), N >= 1.
+__device__ __forceinline__ int omega_len(uint32_t N) {
+    int len = 1;
+    while (N > 1) {
+        const int L = 32 - __clz(N);
+        len += L;
+        N = static_cast<uint32_t>(L - 1);
+    }
+    return len;
+}
+
+// Words of a sparse-coded bucket of len coordinates, whatever its codes: 32
+// norm bits and at most 18 bits per coordinate (the distances sum to len and
+// |omega(g)| <= g + 2; one sign bit; omega(level) <= 14 bits) plus 2.
+inline int64_t sparse_bucket_max_words(int64_t len) { return 1 + div_up(18 * len + 2, 32); }
+
+template <bool FOUR>
+__device__ __forceinline__ void code_at(const uint8_t* codes, int64_t i, uint32_t& sign, uint32_t& level) {
+    if (FOUR) {
+        const uint32_t byte = __ldg(codes + (i >> 1));
+        const uint32_t c = (i & 1) ? (byte & 15u) : (byte >> 4);
+        sign = c >> 3;
+        level = c & 7u;
+    } else {
+        const uint32_t c = __ldg(codes + i);
+        sign = c >> 7;
+        level = c & 127u;
+    }
+}
+
+// The warp's view of one bucket: each lane's coded bits (its first distance
+// included), the last non-zero coordinate before each lane's range, and the
+// bucket's total bits.
+struct SparseBucket {
+    int64_t lo;          // first coordinate of the bucket
+    int len, c0, c1;     // bucket length; this lane's range [c0, c1)
+    int before;          // last non-zero coordinate before c0, or -1
+    int last_all;        // last non-zero coordinate of the bucket, or -1
+    uint32_t lane_bits;  // this lane's bits
+    uint32_t lane_pos;   // this lane's first bit within the bucket
+    uint32_t total;      // the bucket's bits, norm and closing distance included
+};
+
+template <bool FOUR>
+__device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, int64_t b, bool levels, int lane) {
+    SparseBucket r;
+    r.lo = b * d;
+    r.len = static_cast<int>(n - r.lo < d ? n - r.lo : static_cast<int64_t>(d));
+    const int cpl = d / 32;
+    r.c0 = min(r.len, lane * cpl);
+    r.c1 = min(r.len, r.c0 + cpl);
+    int first = -1, prev = -1;
+    uint32_t bits = 0;
+    for (int c = r.c0; c < r.c1; ++c) {
+        uint32_t sg, lv;
+        code_at<FOUR>(codes, r.lo + c, sg, lv);
+        if (!lv) continue;
+        if (prev >= 0) bits += omega_len(static_cast<uint32_t>(c - prev));
+        else first = c;
+        bits += 1 + (levels ? omega_len(lv) : 0);
+        prev = c;
+    }
+    int incl = prev;      // inclusive max-scan of the lanes' last non-zero coordinates
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl = max(incl, t);
+    }
+    const int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    r.before = lane ? excl : -1;
+    r.last_all = __shfl_sync(0xffffffffu, incl, 31);
+    if (first >= 0) bits += omega_len(static_cast<uint32_t>(first - r.before));
+    r.lane_bits = bits;
+    const int in = warp_incl_sum(static_cast<int>(bits), lane);
+    r.lane_pos = 32u + static_cast<uint32_t>(in) - bits;
+    const uint32_t all = static_cast<uint32_t>(__shfl_sync(0xffffffffu, in, 31));
+    r.total = 32u + all + static_cast<uint32_t>(omega_len(static_cast<uint32_t>(r.len - r.last_all)));
+    return r;
+}
+
+struct SparseArgs {
+    const uint8_t* codes;
+    const float* norms;
+    int64_t n;
+    int d;
+    int64_t nbuckets;
+    bool levels;          // s >= 2
+    Ws ws;
+    uint32_t* words;
+    uint32_t* offsets;
+    int stage_words;      // staging words per warp
+};
+
+// Count: words of each bucket and the exclusive prefix of the per-CTA totals
+// (the last CTA to finish turns the totals into it, as k_elias_count does).
+template <bool FOUR>
+__global__ void __launch_bounds__(kThreads) k_elias_sparse_count(SparseArgs a) {
+    __shared__ uint32_t wsum[kWarpsPerBlock];
+    __shared__ bool is_last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
+    uint32_t mine = 0;
+    for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
+        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b0 + lb, a.levels, lane);
+        const uint32_t nw = (sb.total + 31u) >> 5;
+        if (lane == 0) a.ws.counts[b0 + lb] = nw;
+        mine += nw;
+    }
+    if (lane == 0) wsum[warp] = mine;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = 0;
+        for (int w = 0; w < kWarpsPerBlock; ++w) t += wsum[w];
+        a.ws.chunk[blockIdx.x] = t;
+        __threadfence();
+        is_last = atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int nchunks = static_cast<int>(gridDim.x);
+    const int per = (nchunks + kThreads - 1) / kThreads;
+    const int lo = threadIdx.x * per;
+    const int hi = lo + per < nchunks ? lo + per : nchunks;
+    uint32_t run = 0;
+    for (int i = lo; i < hi; ++i) run += __ldcg(a.ws.chunk + i);
+    const int incl = warp_incl_sum(static_cast<int>(run), lane);
+    __syncthreads();
+    if (lane == 31) wsum[warp] = static_cast<uint32_t>(incl);
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerBlock; ++w) {
+        before += w < warp ? wsum[w] : 0u;
+        total += wsum[w];
+    }
+    uint32_t acc = before + static_cast<uint32_t>(incl) - run;
+    for (int i = lo; i < hi; ++i) {
+        const uint32_t v = __ldcg(a.ws.chunk + i);
+        a.ws.chunk[i] = acc;
+        acc += v;
+    }
+    if (threadIdx.x == 0) {
+        a.ws.chunk[nchunks] = total;
+        *a.ws.ticket = 0u;
+    }
+}
+
+// Encode: each warp assembles one bucket at a time in its shared staging
+// words (shared-memory atomicOr of each entry's bits) and copies it out.
+template <bool FOUR>
+__global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) {
+    extern __shared__ uint32_t smem[];
+    uint32_t* offs = smem;                       // [kChunk]
+    uint32_t* stages = smem + kChunk;            // [kWarpsPerBlock][stage_words]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    for (int i = threadIdx.x; i < kWarpsPerBlock * a.stage_words; i += kThreads) stages[i] = 0u;
+    if (warp == 0) {
+        const int64_t ba = b0 + 2 * lane, bb = ba + 1;
+        const uint32_t c0 = ba < a.nbuckets ? a.ws.counts[ba] : 0u;
+        const uint32_t c1 = bb < a.nbuckets ? a.ws.counts[bb] : 0u;
+        const int incl = warp_incl_sum(static_cast<int>(c0 + c1), lane);
+        const uint32_t o0 = a.ws.chunk[blockIdx.x] + static_cast<uint32_t>(incl) - c0 - c1;
+        offs[2 * lane] = o0;
+        offs[2 * lane + 1] = o0 + c0;
+        if (ba < a.nbuckets) a.offsets[ba] = o0;
+        if (bb < a.nbuckets) a.offsets[bb] = o0 + c0;
+        if (blockIdx.x == gridDim.x - 1 && lane == 0) a.offsets[a.nbuckets] = a.ws.chunk[gridDim.x];
+    }
+    __syncthreads();
+    uint32_t* stage = stages + warp * a.stage_words;
+    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
+    for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
+        const int64_t b = b0 + lb;
+        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b, a.levels, lane);
+        if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
+        uint32_t pos = sb.lane_pos;
+        int prev = sb.before;
+        for (int c = sb.c0; c < sb.c1; ++c) {
+            uint32_t sg, lv;
+            code_at<FOUR>(a.codes, sb.lo + c, sg, lv);
+            if (!lv) continue;
+            uint32_t gpat, lpat = 0;
+            const int glen = omega(static_cast<uint32_t>(c - prev), &gpat);
+            const int llen = a.levels ? omega(lv, &lpat) : 0;
+            const uint64_t acc = ((((static_cast<uint64_t>(gpat) << 1) | sg) << llen) | lpat);
+            const int len = glen + 1 + llen;
+            emit(stage, pos, acc, len);
+            pos += static_cast<uint32_t>(len);
+            prev = c;
+        }
+        if (lane == 0) {
+            uint32_t tpat;
+            const int tlen = omega(static_cast<uint32_t>(sb.len - sb.last_all), &tpat);
+            emit(stage, sb.total - static_cast<uint32_t>(tlen), tpat, tlen);
+        }
+        __syncwarp();
+        const int nw = static_cast<int>((sb.total + 31u) >> 5);
+        uint32_t* dst = a.words + offs[lb];
+        for (int k = lane; k < nw; k += 32) {
+            dst[k] = stage[k];
+            stage[k] = 0u;
+        }
+        __syncwarp();
+    }
+}
+
+// Decode: one thread per bucket.  The CTA first zeroes the code bytes of its
+// buckets (coalesced), then each thread walks its bucket's words with a
+// 64-bit window and sets the codes of the non-zero coordinates.  A stream
+// this encoder did not write -- a distance past the bucket's end, a read past
+// its words, a level above s or an impossible codeword -- sets the status to
+// GC_ERR_CORRUPT.
+template <bool FOUR>
+__global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) {
+    const int stream = blockIdx.y;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kThreads;
+    const int64_t cnt = a.nbuckets - b0 < kThreads ? a.nbuckets - b0 : kThreads;
+    uint8_t* codes = a.codes.p[stream];
+    {
+        const int64_t bpb = FOUR ? a.d / 2 : a.d;                 // bytes per whole bucket (>= 64)
+        const int64_t total = FOUR ? (a.n + 1) / 2 : a.n;
+        const int64_t start = b0 * bpb;
+        int64_t end = (b0 + cnt) * bpb;
+        if (end > total) end = total;
+        const int64_t nvec = (end - start) / 16;
+        uint4* v = reinterpret_cast<uint4*>(codes + start);
+        for (int64_t i = threadIdx.x; i < nvec; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int64_t i = start + nvec * 16 + threadIdx.x; i < end; i += kThreads) codes[i] = 0;
+    }
+    __syncthreads();
+    const int64_t b = b0 + threadIdx.x;
+    if (b >= a.nbuckets) return;
+    const uint32_t* offsets = a.offsets.p[stream];
+    const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
+    const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
+    const uint32_t* src = a.words.p[stream] + w_lo;
+    const int64_t lo = b * a.d;
+    const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
+    bool bad = avail == 0;
+    int64_t next = 0;
+    uint64_t win = 0;
+    int have = 0;
+    // the window may hold zero words read ahead past the bucket; only taking
+    // bits beyond its last word makes the stream corrupt
+    const int64_t limit = avail > 0 ? 32 * (avail - 1) : 0;
+    int64_t used = 0;
+    auto refill = [&]() {
+        while (have <= 32) {
+            const uint32_t w = next < avail ? __ldg(src + next) : 0u;
+            ++next;
+            win |= static_cast<uint64_t>(w) << (32 - have);
+            have += 32;
+        }
+    };
+    auto take = [&](int k) -> uint32_t {       // k in 1..31
+        refill();
+        const uint32_t v = static_cast<uint32_t>(win >> (64 - k));
+        win <<= k;
+        have -= k;
+        used += k;
+        bad |= used > limit;
+        return v;
+    };
+    auto get_omega = [&]() -> uint32_t {
+        uint32_t N = 1;
+        while (take(1)) {
+            if (N > 16) {                      // no distance or level of a valid stream is this long
+                bad = true;
+                return 0u;
+            }
+            N = (1u << N) | take(static_cast<int>(N));
+        }
+        return N;
+    };
+    a.norms.p[stream][b] = __uint_as_float(avail ? __ldg(src) : 0u);
+    next = 1;
+    const uint32_t smax = static_cast<uint32_t>(a.s);
+    int64_t p = -1;
+    for (int guard = 0; guard <= len && !bad; ++guard) {
+        const uint32_t g = get_omega();
+        if (bad) break;
+        p += g;
+        if (p >= len) {
+            bad |= p > len;
+            break;
+        }
+        const uint32_t sign = take(1);
+        uint32_t level = a.s >= 2 ? get_omega() : 1u;
+        if (bad) break;
+        if (level > smax) {
+            bad = true;
+            level = smax;
+        }
+        const int64_t i = lo + p;
+        if (FOUR) {
+            const uint8_t code = static_cast<uint8_t>((sign << 3) | level);
+            codes[i >> 1] = static_cast<uint8_t>(codes[i >> 1] | ((i & 1) ? code : (code << 4)));
+        } else {
+            codes[i] = static_cast<uint8_t>((sign << 7) | level);
+        }
+    }
+    if (bad && a.status) *a.status = GC_ERR_CORRUPT;
+}
+
 }  // namespace
 }  // namespace gc
 
@@ -973,6 +1296,74 @@ int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* cons
 int qsgd_elias_decode(const uint32_t* words, const uint32_t* offsets, int64_t n, int bucket, int s_levels,
                       uint8_t* codes, float* norms, int* d_status, gc_stream_t stream) {
     return qsgd_elias_decode_batched(&words, &offsets, 1, n, bucket, s_levels, &codes, &norms, d_status, stream);
+}
+
+uint64_t qsgd_elias_sparse_max_words(int64_t n, int bucket) {
+    if (n < 0 || !valid_bucket(bucket)) return 0;
+    const int64_t full = n / bucket, rest = n % bucket;
+    return static_cast<uint64_t>(full * sparse_bucket_max_words(bucket) +
+                                 (rest ? sparse_bucket_max_words(rest) : 0));
+}
+
+int qsgd_elias_encode_sparse(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels,
+                             uint32_t* words, uint64_t capacity_words, uint32_t* offsets, void* workspace,
+                             size_t ws_bytes, gc_stream_t stream) {
+    if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127) return GC_ERR_INVALID;
+    if (!offsets || (n > 0 && (!codes || !norms || !words || !workspace))) return GC_ERR_INVALID;
+    const uint64_t need = qsgd_elias_sparse_max_words(n, bucket);
+    if (need > 0xFFFFFFFFull) return GC_ERR_INVALID;
+    if (capacity_words < need) return GC_ERR_CAPACITY;
+    if (ws_bytes < qsgd_elias_workspace_bytes(n, bucket)) return GC_ERR_INVALID;
+    if ((codes && !aligned16(codes)) || (norms && !aligned16(norms)) || (words && !aligned16(words)) ||
+        !aligned16(offsets) || (workspace && !aligned16(workspace)))
+        return GC_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n == 0) return cudaMemsetAsync(offsets, 0, sizeof(uint32_t), s) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    const bool four = s_levels <= 7;
+    const int64_t nb = div_up(n, bucket), nchunks = div_up(nb, kChunk);
+    const Ws ws = ws_layout(workspace, nchunks);
+    if (cudaMemsetAsync(ws.ticket, 0, kTicketBytes, s) != cudaSuccess) return GC_ERR_CUDA;
+    SparseArgs a{codes, norms, n, bucket, nb, s_levels >= 2, ws, words, offsets,
+                 static_cast<int>(sparse_bucket_max_words(bucket)) + 2};
+    const unsigned grid = static_cast<unsigned>(nchunks);
+    if (four)
+        k_elias_sparse_count<true><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_elias_sparse_count<false><<<grid, kThreads, 0, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
+    const size_t smem = sizeof(uint32_t) * (kChunk + static_cast<size_t>(kWarpsPerBlock) * a.stage_words);
+    if (four)
+        k_elias_sparse_encode<true><<<grid, kThreads, smem, s>>>(a);
+    else
+        k_elias_sparse_encode<false><<<grid, kThreads, smem, s>>>(a);
+    return launch_status();
+}
+
+int qsgd_elias_decode_sparse(const uint32_t* words, const uint32_t* offsets, int64_t n, int bucket, int s_levels,
+                             uint8_t* codes, float* norms, int* d_status, gc_stream_t stream) {
+    if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!words || !offsets || !codes || !norms) return GC_ERR_INVALID;
+    if (!aligned16(words) || !aligned16(offsets) || !aligned16(codes) || !aligned16(norms)) return GC_ERR_ALIGN;
+    if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return GC_ERR_ALIGN;
+    DecodeArgs a;
+    a.words.p[0] = words;
+    a.offsets.p[0] = offsets;
+    a.codes.p[0] = codes;
+    a.norms.p[0] = norms;
+    a.n = n;
+    a.d = bucket;
+    a.nbuckets = div_up(n, bucket);
+    a.s = s_levels;
+    a.status = d_status;
+    a.stage_cap = 0;
+    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads)), 1u);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (s_levels <= 7)
+        k_elias_decode_sparse<true><<<grid, kThreads, 0, s>>>(a);
+    else
+        k_elias_decode_sparse<false><<<grid, kThreads, 0, s>>>(a);
+    return launch_status();
 }
 
 }  // extern "C"

@@ -194,22 +194,29 @@ __device__ __forceinline__ bool all_zero(const float4 (&v)[ROUNDS], int lane) {
 // term added to sum[j][k] exactly as k_qsgd_dequant_sum adds it (one fma of
 // the level with the signed norm * unit_scale), so that a fused pass over
 // all workers equals the quantise calls followed by the dequant-sum.
-template <int ROUNDS>
-struct BucketRegs {
-    float4 v[ROUNDS];
-};
+// Programmatic dependent launch: the fix-up kernels are launched with the
+// programmatic-serialisation attribute, so they can be scheduled while the
+// main kernel's last CTAs drain instead of after a full launch gap.  The
+// main kernel allows it at its start; the fix-up waits (griddepcontrol.wait)
+// until the main grid has completed and its writes are visible before it
+// reads a norm.  Launched without the attribute, the wait returns at once.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // A sum of squares below 2^-100 may have lost bits to underflow and one above
 // 2^126 overflows: such buckets (subnormal-sized or huge gradients) are redone
 // with every value scaled by the power of two that brings the bucket maximum
-// to [0.5, 1), which is exact, and the norm scaled back.  Out of line: the
-// rare path would otherwise cost the common one registers and scheduling.
+// to [0.5, 1), which is exact, and the norm scaled back.
 template <int ROUNDS>
-__device__ __noinline__ float rescued_norm(const BucketRegs<ROUNDS> r) {
+__device__ __forceinline__ float rescued_norm(const float4 (&v)[ROUNDS]) {
     float mx = 0.0f;
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j)
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(r.v[j].x), fabsf(r.v[j].y)), fmaxf(fabsf(r.v[j].z), fabsf(r.v[j].w))));
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     int ex = 0;
@@ -217,16 +224,37 @@ __device__ __noinline__ float rescued_norm(const BucketRegs<ROUNDS> r) {
     float h2 = 0.0f, l2 = 0.0f;
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
-        acc_square(ldexpf(r.v[j].x, -ex), h2, l2);
-        acc_square(ldexpf(r.v[j].y, -ex), h2, l2);
-        acc_square(ldexpf(r.v[j].z, -ex), h2, l2);
-        acc_square(ldexpf(r.v[j].w, -ex), h2, l2);
+        acc_square(ldexpf(v[j].x, -ex), h2, l2);
+        acc_square(ldexpf(v[j].y, -ex), h2, l2);
+        acc_square(ldexpf(v[j].z, -ex), h2, l2);
+        acc_square(ldexpf(v[j].w, -ex), h2, l2);
     }
     warp_sum2(h2, l2);
     return ldexpf(df_sqrt(h2, l2), ex);
 }
 
-template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM, bool RAGGED>
+// The four sign bits of a float4 at bit 7 of each byte (element k in byte k),
+// set where the value is below zero: +0 is added first (packed), which turns
+// -0 into +0 and leaves every other number as it is, then the top byte of
+// each float is picked out.  (A NaN never reaches here: its bucket is flagged.)
+__device__ __forceinline__ uint32_t sign_bytes(const float4 x) {
+    const uint64_t p01 = add2(pack2(x.x, x.y), 0ull), p23 = add2(pack2(x.z, x.w), 0ull);
+    const uint32_t lo = __byte_perm(static_cast<uint32_t>(p01), static_cast<uint32_t>(p01 >> 32), 0x0073);
+    const uint32_t hi = __byte_perm(static_cast<uint32_t>(p23), static_cast<uint32_t>(p23 >> 32), 0x0073);
+    return __byte_perm(lo, hi, 0x5410) & 0x80808080u;
+}
+
+// One bucket of one worker, by one warp: the bucket's norm (written by lane
+// 0), its codes (written), and -- when SUM -- every element's dequantised
+// term added to sum[j][k] exactly as k_qsgd_dequant_sum adds it (one fma of
+// the level with the signed norm * unit_scale), so that a fused pass over
+// all workers equals the quantise calls followed by the dequant-sum.
+// RAGGED: the partial last bucket (bounds-checked loads and stores).
+// FLAG: a bucket whose l2 norm needs the rescue above is not finished here:
+// its norm is written as -1 (no norm is negative) and a second, small kernel
+// redoes it with FLAG off.  Keeping the rare path out of the main kernel
+// measured 10% faster than carrying it inline or as a call.
+template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM, bool RAGGED, bool FLAG>
 __device__ __forceinline__ void quantize_bucket_body(const QArgs& a, int64_t b, int lane, float unit_scale,
                                                      float (&sum)[ROUNDS][4]) {
     constexpr int D = 128 * ROUNDS;
@@ -235,9 +263,8 @@ __device__ __forceinline__ void quantize_bucket_body(const QArgs& a, int64_t b, 
     const uint32_t s_u = static_cast<uint32_t>(a.s);
 
     const int64_t b0 = b * D;
-    const bool full = !RAGGED;
     float4 v[ROUNDS];
-    if (full) {
+    if (!RAGGED) {
 #pragma unroll
         for (int j = 0; j < ROUNDS; ++j) v[j] = ld_stream_f4(a.v + b0 + 128 * j + 4 * lane);
     } else {
@@ -261,31 +288,32 @@ __device__ __forceinline__ void quantize_bucket_body(const QArgs& a, int64_t b, 
         for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         norm = mx;
     } else {
-    // two double-float accumulators (even and odd elements) in packed fp32
-    // pairs, joined by one TwoSum: the same accuracy as one accumulator
-    uint64_t hi2 = 0ull, lo2 = 0ull;
+        // two double-float accumulators (even and odd elements) in packed fp32
+        // pairs, joined by one TwoSum: the same accuracy as one accumulator
+        uint64_t hi2 = 0ull, lo2 = 0ull;
 #pragma unroll
-    for (int j = 0; j < ROUNDS; ++j) {
-        acc_square2(pack2(v[j].x, v[j].y), hi2, lo2);
-        acc_square2(pack2(v[j].z, v[j].w), hi2, lo2);
-    }
-    float ha, hb, la, lb, hi, e;
-    unpack2(hi2, ha, hb);
-    unpack2(lo2, la, lb);
-    two_sum(ha, hb, hi, e);
-    const float lo = __fadd_rn(__fadd_rn(la, lb), e);
-    norm = warp_norm(hi, lo);
-    const bool tiny = norm < 8.8817842e-16f;      // 2^-50: the sum of squares is below 2^-100
-    const bool huge = !(norm < 9.2233720e18f);    // 2^63, or inf / NaN
-    if (huge || (tiny && !all_zero(v, lane))) {   // warp-uniform
-        BucketRegs<ROUNDS> r;
-#pragma unroll
-        for (int j = 0; j < ROUNDS; ++j) r.v[j] = v[j];
-        norm = rescued_norm<ROUNDS>(r);
-    }
+        for (int j = 0; j < ROUNDS; ++j) {
+            acc_square2(pack2(v[j].x, v[j].y), hi2, lo2);
+            acc_square2(pack2(v[j].z, v[j].w), hi2, lo2);
+        }
+        float ha, hb, la, lb, hi, e;
+        unpack2(hi2, ha, hb);
+        unpack2(lo2, la, lb);
+        two_sum(ha, hb, hi, e);
+        const float lo = __fadd_rn(__fadd_rn(la, lb), e);
+        norm = warp_norm(hi, lo);
+        const bool tiny = norm < 8.8817842e-16f;      // 2^-50: the sum of squares is below 2^-100
+        const bool huge = !(norm < 9.2233720e18f);    // 2^63, or inf / NaN
+        if (huge || (tiny && !all_zero(v, lane))) {   // warp-uniform
+            if (FLAG)
+                norm = -1.0f;
+            else
+                norm = rescued_norm<ROUNDS>(v);
+        }
     }
     if (lane == 0) a.norms[b] = norm;
     // norm == 0 means every coordinate is +-0: sign bit 0, level 0, code 0
+    // (a flagged norm of -1 gives level 0 everywhere; the codes are rewritten)
     const bool zero = !(norm > 0.0f);
     const float S = zero ? 0.0f : __fdiv_rn(s_f, norm);
 
@@ -295,73 +323,91 @@ __device__ __forceinline__ void quantize_bucket_body(const QArgs& a, int64_t b, 
         // e is a multiple of 4, so seed_w ^ (e + k) == (seed_w ^ e) ^ k
         const uint64_t kbase = a.seed_w ^ static_cast<uint64_t>(e);
         const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        uint32_t c[4] = {0u, 0u, 0u, 0u};
+        uint32_t lv[4] = {0u, 0u, 0u, 0u};
         if (!zero) {
             uint32_t t[4];
             hash4_top24(kbase, t);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t lvl = qlevel(xs[k], S, s_u, t[k]);
-                c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lvl;
-            }
+            for (int k = 0; k < 4; ++k) lv[k] = qlevel(xs[k], S, s_u, t[k]);
         }
         if (SUM) {
             const float u = __fmul_rn(norm, unit_scale);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float lf = __uint_as_float(0x4B000000u | (c[k] & (FOUR ? 7u : 127u))) - 8388608.0f;
-                sum[j][k] = __fmaf_rn(lf, (c[k] >> kSignShift) ? -u : u, sum[j][k]);
+                const float lf = __uint_as_float(0x4B000000u | lv[k]) - 8388608.0f;
+                sum[j][k] = __fmaf_rn(lf, xs[k] < 0.0f ? -u : u, sum[j][k]);
             }
         }
         if (FOUR) {
+            uint32_t c[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) c[k] = ((xs[k] < 0.0f ? 1u : 0u) << kSignShift) | lv[k];
             const uint32_t lo2 = (c[0] << 4) | c[1];
             const uint32_t hi2 = (c[2] << 4) | c[3];
-            if (full) {
+            if (!RAGGED) {
                 *reinterpret_cast<uint16_t*>(a.codes + (e >> 1)) = static_cast<uint16_t>(lo2 | (hi2 << 8));
             } else {
                 if (e < a.n) a.codes[e >> 1] = static_cast<uint8_t>(e + 1 < a.n ? lo2 : (c[0] << 4));
                 if (e + 2 < a.n) a.codes[(e >> 1) + 1] = static_cast<uint8_t>(e + 3 < a.n ? hi2 : (c[2] << 4));
             }
         } else {
-            if (full) {
-                *reinterpret_cast<uint32_t*>(a.codes + e) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+            // levels into bytes (element k in byte k), sign bits from the floats
+            const uint32_t L = __byte_perm(__byte_perm(lv[0], lv[1], 0x0040), __byte_perm(lv[2], lv[3], 0x0040), 0x5410);
+            const uint32_t word = L | sign_bytes(v[j]);
+            if (!RAGGED) {
+                *reinterpret_cast<uint32_t*>(a.codes + e) = word;
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    if (e + k < a.n) a.codes[e + k] = static_cast<uint8_t>(c[k]);
+                    if (e + k < a.n) a.codes[e + k] = static_cast<uint8_t>(word >> (8 * k));
             }
         }
     }
 }
 
-// The partial last bucket (bounds-checked loads and stores), out of line.
-template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM>
-__device__ __noinline__ void quantize_bucket_ragged(const QArgs& a, int64_t b, int lane, float unit_scale,
-                                                    float (&sum)[ROUNDS][4]) {
-    quantize_bucket_body<ROUNDS, FOUR, MAXNORM, SUM, true>(a, b, lane, unit_scale, sum);
-}
-
-template <int ROUNDS, bool FOUR, bool MAXNORM, bool SUM>
-__device__ __forceinline__ void quantize_bucket(const QArgs& a, int64_t b, int lane, float unit_scale,
-                                                float (&sum)[ROUNDS][4]) {
-    if ((b + 1) * (128 * ROUNDS) <= a.n)
-        quantize_bucket_body<ROUNDS, FOUR, MAXNORM, SUM, false>(a, b, lane, unit_scale, sum);
-    else
-        quantize_bucket_ragged<ROUNDS, FOUR, MAXNORM, SUM>(a, b, lane, unit_scale, sum);
-}
-
-// One warp per bucket; the grid covers every bucket.  For buckets of up to
-// 512 the register bound allows 6 CTAs (48 warps) per SM with no spills: the
-// quantiser is bound by the integer ALU pipe and latency, and 6 measured
-// ahead of 4 (56 registers) and of 8 (32 registers and spills).
+// One warp per whole bucket; the grid covers the whole buckets.  For buckets
+// of up to 512 the register bound allows 6 CTAs (48 warps) per SM with no
+// spills: the quantiser is bound by instruction issue and the integer ALU
+// pipe, and 6 measured ahead of 4 (56 registers) and of 8 (32 registers and
+// spills).  The partial last bucket and flagged buckets: k_qsgd_fixup.
 template <int ROUNDS, bool FOUR, bool MAXNORM>
 __global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 6)
 k_qsgd_quantize(const QArgs a) {
+    constexpr int D = 128 * ROUNDS;
+    allow_dependent_launch();
     const int lane = threadIdx.x & 31;
     const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (b >= a.nbuckets) return;
+    if (b >= a.n / D) return;
     float unused[ROUNDS][4];
-    quantize_bucket<ROUNDS, FOUR, MAXNORM, false>(a, b, lane, 0.0f, unused);
+    quantize_bucket_body<ROUNDS, FOUR, MAXNORM, false, false, !MAXNORM>(a, b, lane, 0.0f, unused);
+}
+
+// After k_qsgd_quantize: each warp scans 32 norms at a time and redoes, with
+// the rescue, every bucket flagged there (norm -1); the first warp also does
+// the partial last bucket.
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+__global__ void __launch_bounds__(kThreads)
+k_qsgd_fixup(const QArgs a) {
+    constexpr int D = 128 * ROUNDS;
+    wait_for_primary();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nfull = a.n / D;
+    float unused[ROUNDS][4];
+    if (!MAXNORM) {
+        for (int64_t g0 = gw * 32; g0 < nfull; g0 += nw * 32) {
+            const int64_t b = g0 + lane;
+            uint32_t m = __ballot_sync(0xffffffffu, b < nfull && a.norms[b] < 0.0f);
+            while (m) {
+                const int i = __ffs(m) - 1;
+                m &= m - 1;
+                quantize_bucket_body<ROUNDS, FOUR, false, false, false, false>(a, g0 + i, lane, 0.0f, unused);
+            }
+        }
+    }
+    if (gw == 0 && nfull * D < a.n)
+        quantize_bucket_body<ROUNDS, FOUR, MAXNORM, false, true, false>(a, nfull, lane, 0.0f, unused);
 }
 
 // Every worker's quantisation and the dequant-sum in one pass: one warp per
@@ -377,12 +423,10 @@ struct StepArgs {
     float* out;
 };
 
-template <int ROUNDS, bool FOUR, bool MAXNORM>
-__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
-k_qsgd_step(const StepArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (b >= a.q.nbuckets) return;
+// All workers' quantisation of bucket b and the sum of their terms, written
+// to out (FLAG and RAGGED as in quantize_bucket_body).
+template <int ROUNDS, bool FOUR, bool MAXNORM, bool RAGGED, bool FLAG>
+__device__ __forceinline__ void step_bucket(const StepArgs& a, int64_t b, int lane) {
     constexpr int D = 128 * ROUNDS;
     float sum[ROUNDS][4];
 #pragma unroll
@@ -395,15 +439,14 @@ k_qsgd_step(const StepArgs a) {
         q.seed_w = a.seed ^ (static_cast<uint64_t>(static_cast<uint32_t>(w)) << 48);
         q.norms = a.norms.p[w];
         q.codes = a.codes.p[w];
-        quantize_bucket<ROUNDS, FOUR, MAXNORM, true>(q, b, lane, a.unit_scale, sum);
+        quantize_bucket_body<ROUNDS, FOUR, MAXNORM, true, RAGGED, FLAG>(q, b, lane, a.unit_scale, sum);
     }
     const int64_t b0 = b * D;
-    const bool full = b0 + D <= a.q.n;
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
         const int64_t e = b0 + 128 * j + 4 * lane;
         const float4 o = make_float4(sum[j][0], sum[j][1], sum[j][2], sum[j][3]);
-        if (full) {
+        if (!RAGGED) {
             st_stream_f4(a.out + e, o);
         } else {
             if (e < a.q.n) a.out[e] = o.x;
@@ -412,6 +455,46 @@ k_qsgd_step(const StepArgs a) {
             if (e + 3 < a.q.n) a.out[e + 3] = o.w;
         }
     }
+}
+
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+__global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4)
+k_qsgd_step(const StepArgs a) {
+    constexpr int D = 128 * ROUNDS;
+    allow_dependent_launch();
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (b >= a.q.n / D) return;
+    step_bucket<ROUNDS, FOUR, MAXNORM, false, !MAXNORM>(a, b, lane);
+}
+
+// After k_qsgd_step: every bucket in which some worker was flagged is redone
+// for all workers (norms, codes and the sum); the first warp also does the
+// partial last bucket.
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+__global__ void __launch_bounds__(kThreads)
+k_qsgd_step_fixup(const StepArgs a) {
+    constexpr int D = 128 * ROUNDS;
+    wait_for_primary();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t nfull = a.q.n / D;
+    if (!MAXNORM) {
+        for (int64_t g0 = gw * 32; g0 < nfull; g0 += nw * 32) {
+            const int64_t b = g0 + lane;
+            bool f = false;
+            if (b < nfull)
+                for (int w = 0; w < a.W; ++w) f |= a.norms.p[w][b] < 0.0f;
+            uint32_t m = __ballot_sync(0xffffffffu, f);
+            while (m) {
+                const int i = __ffs(m) - 1;
+                m &= m - 1;
+                step_bucket<ROUNDS, FOUR, false, false, false>(a, g0 + i, lane);
+            }
+        }
+    }
+    if (gw == 0 && nfull * D < a.q.n) step_bucket<ROUNDS, FOUR, MAXNORM, true, false>(a, nfull, lane);
 }
 
 struct DArgs {
@@ -675,30 +758,80 @@ __global__ void __launch_bounds__(kThreads, ROUNDS >= 8 ? 2 : 4) k_qsgd_dequant_
     if (nfull < a.nbuckets && wid == nfull % nw) dequant_bucket_direct<ROUNDS, FOUR>(a, nfull, lane, lane_base);
 }
 
-template <bool FOUR, bool MAXNORM>
-int launch_quantize(int rounds, const QArgs& a, unsigned grid, cudaStream_t s) {
-    switch (rounds) {
-        case 1: k_qsgd_quantize<1, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 2: k_qsgd_quantize<2, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 4: k_qsgd_quantize<4, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 8: k_qsgd_quantize<8, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 16: k_qsgd_quantize<16, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        default: return GC_ERR_INVALID;
+// Launches a fix-up kernel after the kernel just enqueued on s, as a
+// programmatic dependent launch (see wait_for_primary).
+template <typename Args>
+cudaError_t launch_after(void (*kernel)(Args), unsigned grid, cudaStream_t s, const Args& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// The fix-up grid: one warp per 32 whole buckets (their norms scanned with
+// one coalesced load), at most two CTAs per SM; one CTA when only the
+// partial last bucket can need it (max-norm scaling flags nothing).
+inline unsigned fixup_grid(int64_t nfull, bool flags) {
+    if (!flags) return 1u;
+    const int64_t want = (nfull / 32 + kWarpsPerBlock) / kWarpsPerBlock;
+    const int64_t cap = grid_for(2) > 0 ? grid_for(2) : 1;
+    return static_cast<unsigned>(want < cap ? want : cap);
+}
+
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+int launch_quantize_r(const QArgs& a, cudaStream_t s) {
+    constexpr int D = 128 * ROUNDS;
+    const int64_t nfull = a.n / D;
+    if (nfull > 0) k_qsgd_quantize<ROUNDS, FOUR, MAXNORM><<<blocks_for_tiles(nfull), kThreads, 0, s>>>(a);
+    if (!MAXNORM || nfull * D < a.n) {
+        if (launch_after<QArgs>(k_qsgd_fixup<ROUNDS, FOUR, MAXNORM>, fixup_grid(nfull, !MAXNORM), s, a) != cudaSuccess)
+            return GC_ERR_CUDA;
     }
     return launch_status();
 }
 
 template <bool FOUR, bool MAXNORM>
-int launch_step(int rounds, const StepArgs& a, unsigned grid, cudaStream_t s) {
+int launch_quantize(int rounds, const QArgs& a, cudaStream_t s) {
     switch (rounds) {
-        case 1: k_qsgd_step<1, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 2: k_qsgd_step<2, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 4: k_qsgd_step<4, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 8: k_qsgd_step<8, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
-        case 16: k_qsgd_step<16, FOUR, MAXNORM><<<grid, kThreads, 0, s>>>(a); break;
+        case 1: return launch_quantize_r<1, FOUR, MAXNORM>(a, s);
+        case 2: return launch_quantize_r<2, FOUR, MAXNORM>(a, s);
+        case 4: return launch_quantize_r<4, FOUR, MAXNORM>(a, s);
+        case 8: return launch_quantize_r<8, FOUR, MAXNORM>(a, s);
+        case 16: return launch_quantize_r<16, FOUR, MAXNORM>(a, s);
         default: return GC_ERR_INVALID;
     }
+}
+
+template <int ROUNDS, bool FOUR, bool MAXNORM>
+int launch_step_r(const StepArgs& a, cudaStream_t s) {
+    constexpr int D = 128 * ROUNDS;
+    const int64_t nfull = a.q.n / D;
+    if (nfull > 0) k_qsgd_step<ROUNDS, FOUR, MAXNORM><<<blocks_for_tiles(nfull), kThreads, 0, s>>>(a);
+    if (!MAXNORM || nfull * D < a.q.n) {
+        if (launch_after<StepArgs>(k_qsgd_step_fixup<ROUNDS, FOUR, MAXNORM>, fixup_grid(nfull, !MAXNORM), s, a) !=
+            cudaSuccess)
+            return GC_ERR_CUDA;
+    }
     return launch_status();
+}
+
+template <bool FOUR, bool MAXNORM>
+int launch_step(int rounds, const StepArgs& a, cudaStream_t s) {
+    switch (rounds) {
+        case 1: return launch_step_r<1, FOUR, MAXNORM>(a, s);
+        case 2: return launch_step_r<2, FOUR, MAXNORM>(a, s);
+        case 4: return launch_step_r<4, FOUR, MAXNORM>(a, s);
+        case 8: return launch_step_r<8, FOUR, MAXNORM>(a, s);
+        case 16: return launch_step_r<16, FOUR, MAXNORM>(a, s);
+        default: return GC_ERR_INVALID;
+    }
 }
 
 constexpr int kMaxDevices = 64;
@@ -793,13 +926,12 @@ static int qsgd_quantize_impl(const float* grad, int64_t n, int bucket, int s_le
     a.s = s_levels;
     a.norms = norms;
     a.codes = codes;
-    const unsigned grid = blocks_for_tiles(a.nbuckets);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (maxnorm)
-        return s_levels <= 7 ? launch_quantize<true, true>(bucket / 128, a, grid, s)
-                             : launch_quantize<false, true>(bucket / 128, a, grid, s);
-    return s_levels <= 7 ? launch_quantize<true, false>(bucket / 128, a, grid, s)
-                         : launch_quantize<false, false>(bucket / 128, a, grid, s);
+        return s_levels <= 7 ? launch_quantize<true, true>(bucket / 128, a, s)
+                             : launch_quantize<false, true>(bucket / 128, a, s);
+    return s_levels <= 7 ? launch_quantize<true, false>(bucket / 128, a, s)
+                         : launch_quantize<false, false>(bucket / 128, a, s);
 }
 
 int qsgd_quantize(const float* grad, int64_t n, int bucket, int s_levels, uint64_t seed, int worker,
@@ -865,13 +997,12 @@ int qsgd_step(const float* const* grads, int W, int64_t n, int bucket, int s_lev
     a.seed = seed;
     a.unit_scale = static_cast<float>(static_cast<double>(scale) / s_levels);
     a.out = out;
-    const unsigned grid = blocks_for_tiles(a.q.nbuckets);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (maxnorm)
-        return s_levels <= 7 ? launch_step<true, true>(bucket / 128, a, grid, s)
-                             : launch_step<false, true>(bucket / 128, a, grid, s);
-    return s_levels <= 7 ? launch_step<true, false>(bucket / 128, a, grid, s)
-                         : launch_step<false, false>(bucket / 128, a, grid, s);
+        return s_levels <= 7 ? launch_step<true, true>(bucket / 128, a, s)
+                             : launch_step<false, true>(bucket / 128, a, s);
+    return s_levels <= 7 ? launch_step<true, false>(bucket / 128, a, s)
+                         : launch_step<false, false>(bucket / 128, a, s);
 }
 
 }  // extern "C"

@@ -417,6 +417,48 @@ GC_API int qsgd_elias_decode_batched(const uint32_t *const *words,
                                      float *const *norms, int *d_status,
                                      gc_stream_t stream);
 
+/*
+ * qsgd_elias_encode_sparse -- QSGD's Elias coding in the sparse regimes
+ * ("QSGD ..." summary page, Knowl 2 items 1 (s >= 2) and 1' (s = 1)): only
+ * the coordinates whose level is not 0 are sent, each as Elias-omega of its
+ * distance from the previous one (the first from -1), one sign bit and, when
+ * s_levels >= 2, Elias-omega(level); Elias-omega(bucket length - last index)
+ * closes each bucket.  Stream conventions as qsgd_elias_encode: 32-bit words
+ * read most significant bit first, every bucket on a word boundary behind
+ * its fp32 norm, offsets[b] its first word, offsets[nbuckets] the length.
+ * Worth it where most levels are 0 (s = 1, small s on peaked gradients).
+ *
+ *   codes, norms, n, bucket, s_levels, offsets, workspace, ws_bytes
+ *                  as qsgd_elias_encode (same workspace size)
+ *   words          device uint32 [capacity_words], at least
+ *                  qsgd_elias_sparse_max_words(n, bucket)
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CAPACITY, GC_ERR_CUDA.
+ */
+GC_API int qsgd_elias_encode_sparse(const uint8_t *codes, const float *norms, int64_t n,
+                                    int bucket, int s_levels, uint32_t *words,
+                                    uint64_t capacity_words, uint32_t *offsets,
+                                    void *workspace, size_t ws_bytes, gc_stream_t stream);
+
+/* Upper bound on the words qsgd_elias_encode_sparse writes: per bucket of
+ * len coordinates 1 + ceil((18 len + 2) / 32) (0 for invalid arguments). */
+GC_API uint64_t qsgd_elias_sparse_max_words(int64_t n, int bucket);
+
+/*
+ * qsgd_elias_decode_sparse -- the inverse of qsgd_elias_encode_sparse: norms
+ * and codes in qsgd_quantize's layout, every coordinate not in the stream
+ * (and the sign of every level-0 coordinate) 0.  Bucket b reads only
+ * words[offsets[b] .. offsets[b+1]).
+ *   d_status   device int or NULL; set to GC_ERR_CORRUPT when a distance
+ *              runs past the bucket's end, a bucket's codewords run past its
+ *              words, a level exceeds s_levels (written as s_levels), a
+ *              codeword is longer than any valid one, or a bucket has no
+ *              norm word
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_elias_decode_sparse(const uint32_t *words, const uint32_t *offsets, int64_t n,
+                                    int bucket, int s_levels, uint8_t *codes, float *norms,
+                                    int *d_status, gc_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* SAPS sparsified gossip + EASGD                                         */
 /* ---------------------------------------------------------------------- */

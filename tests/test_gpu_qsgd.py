@@ -238,3 +238,80 @@ def test_one_pass_step_against_oracle(n, W, s):
     ref, terms = qsgd_sum_reference([c.cpu().numpy() for c in codes], [host_f32(x) for x in norms],
                                     n, d, s, 1.0 / W)
     assert_close(host_f32(out), ref, terms, what="average")
+
+
+def _mixed_scale_vector(n, seed):
+    """Buckets of 512 cycling through normal, subnormal-sized (flagged: the
+    sum of squares underflows), huge (flagged: it overflows) and all-zero
+    values, with a ragged tail."""
+    rng = np.random.default_rng(seed)
+    v = rng.normal(0, 1, n)
+    for b in range((n + 511) // 512):
+        kind = b % 4
+        sl = slice(512 * b, min(n, 512 * b + 512))
+        if kind == 1:
+            v[sl] *= 1e-41
+        elif kind == 2:
+            v[sl] *= 1e25
+        elif kind == 3:
+            v[sl] = 0.0
+    return v.astype(np.float32)
+
+
+@pytest.mark.parametrize("s", [7, 127])
+@pytest.mark.parametrize("n", [512 * 37 + 111, 512 * 300])
+def test_flagged_buckets_are_redone(n, s):
+    """Buckets whose sum of squares under- or overflows are finished by the
+    fix-up launch: half of all buckets here, spread over many 32-bucket scan
+    groups, plus zero buckets and the ragged tail; norms and codes against
+    the oracle, and the dequantised sum of the GPU's codes."""
+    vh = _mixed_scale_vector(n, 17 + s)
+    v = torch.from_numpy(vh).to(DEV)
+    nb, cb = gc.qsgd_num_buckets(n, 512), gc.qsgd_code_bytes(n, s)
+    norms = guarded(nb, torch.float32)
+    codes = guarded(cb, torch.uint8)
+    gc.qsgd_quantize(v, 512, s, 11, 2, norms[:nb], codes[:cb])
+    rn, rc = oracle.qsgd_quantize(vh, 512, s, 11, 2)
+    torch.cuda.synchronize()
+    gn = host_f32(norms[:nb])
+    assert np.all(gn >= 0), "a flagged norm was left behind"
+    assert_close(gn, rn, np.abs(rn), what="norms")
+    compare_codes(codes[:cb].cpu().numpy(), rc, vh, n, 512, s, 11, 2)
+    check_guard(norms, nb)
+    check_guard(codes, cb)
+    out = torch.empty(n, device=DEV)
+    gc.qsgd_dequant_sum([codes[:cb]], [norms[:nb]], n, 512, s, 1.0, out)
+    ref, terms = qsgd_sum_reference([codes[:cb].cpu().numpy()], [gn], n, 512, s, 1.0)
+    torch.cuda.synchronize()
+    assert_close(host_f32(out), ref, terms, what="dequant")
+
+
+@pytest.mark.parametrize("s", [7, 127])
+def test_one_pass_step_with_flagged_buckets(s):
+    """qsgd_step when some workers' buckets are flagged (their whole bucket is
+    redone for every worker by the step's fix-up): bit for bit the separate
+    calls, and the oracle's codes."""
+    n, W = 512 * 41 + 7, 3
+    vhs = [_mixed_scale_vector(n, 40 + w + s) for w in range(W)]
+    vhs[1][512 * 4:512 * 8] = np.random.default_rng(3).normal(0, 1, 2048).astype(np.float32)
+    vs = [torch.from_numpy(x).to(DEV) for x in vhs]
+    nb, cb = gc.qsgd_num_buckets(n, 512), gc.qsgd_code_bytes(n, s)
+    n1 = [torch.empty(nb, device=DEV) for _ in range(W)]
+    c1 = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    for w in range(W):
+        gc.qsgd_quantize(vs[w], 512, s, 5, w, n1[w], c1[w])
+    o1 = torch.empty(n, device=DEV)
+    gc.qsgd_dequant_sum(c1, n1, n, 512, s, 1.0 / W, o1)
+    n2 = [torch.full((nb,), 3.0, device=DEV) for _ in range(W)]
+    c2 = [torch.full((cb,), 0x5A, dtype=torch.uint8, device=DEV) for _ in range(W)]
+    o2 = guarded(n, torch.float32)
+    gc.qsgd_step(vs, 512, s, 5, n2, c2, 1.0 / W, o2[:n])
+    torch.cuda.synchronize()
+    check_guard(o2, n)
+    for w in range(W):
+        assert torch.equal(n1[w].view(torch.int32), n2[w].view(torch.int32))
+        assert torch.equal(c1[w], c2[w])
+        rn, rc = oracle.qsgd_quantize(vhs[w], 512, s, 5, w)
+        assert_close(host_f32(n2[w]), rn, np.abs(rn), what="norms")
+        compare_codes(c2[w].cpu().numpy(), rc, vhs[w], n, 512, s, 5, w)
+    assert torch.equal(o1.view(torch.int32), o2[:n].view(torch.int32))
