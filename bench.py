@@ -993,7 +993,8 @@ CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqs
          "qsgd_dequant_s7", "qsgd_dequant_s127", "saps_mask", "saps_avg", "easgd", "compensated",
          "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127",
          "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001", "saps_round",
-         "qsgd_step_s7", "qsgd_step_s127")
+         "qsgd_step_s7", "qsgd_step_s127", "step_bf16", "multi_step", "elias_sparse_encode_s7",
+         "elias_sparse_encode_s127", "elias_sparse_decode_s7", "elias_sparse_decode_s127")
 
 
 def run_case(name: str, n: int):
@@ -1027,6 +1028,22 @@ def run_case(name: str, n: int):
         cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(W)]
         wt = torch.zeros(m, device=dev)
         fn = lambda: gc.gc_2bit_step(gs, rs, cs, 2e-3, gc.GC_UPD_SGD, lr=0.1, weights=wt)
+    elif name == "step_bf16":
+        W = 4
+        m = n // W
+        gs = [wl.normal(m, 5e-4, 1 + w, device=dev, dtype=torch.bfloat16) for w in range(W)]
+        rs = [torch.zeros(m, device=dev) for _ in range(W)]
+        cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(W)]
+        wt = torch.zeros(m, device=dev)
+        fn = lambda: gc.gc_2bit_step(gs, rs, cs, 1e-3, gc.GC_UPD_SGD, lr=0.01, weights=wt)
+    elif name == "multi_step":
+        S = 10
+        m = n // S
+        gs = [wl.normal(m, 1.0, st, device=dev) for st in range(S)]
+        r = torch.zeros(m, device=dev)
+        cs = [torch.empty(gc.code_words(m), dtype=torch.int32, device=dev) for _ in range(S)]
+        os_ = [torch.empty(m, device=dev) for _ in range(S)]
+        fn = lambda: gc.gc_2bit_quantize_steps(gs, r, cs, 0.5, out=os_)
     elif name == "dqsum_sgd":
         W = 8
         cs = [torch.randint(-2 ** 31, 2 ** 31 - 1, (gc.code_words(n),), dtype=torch.int32, device=dev)
@@ -1083,7 +1100,16 @@ def run_case(name: str, n: int):
         offs = torch.empty(nb + 1, dtype=torch.int32, device=dev)
         ews = torch.empty(gc.qsgd_elias_workspace_bytes(n, 512), dtype=torch.uint8, device=dev)
         gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews)
-        if name.startswith("elias_encode"):
+        if name.startswith("elias_sparse"):
+            sw = torch.empty(gc.qsgd_elias_sparse_max_words(n, 512), dtype=torch.int32, device=dev)
+            gc.qsgd_elias_encode_sparse(c, nm, n, 512, s, sw, offs, ews)
+            if name.startswith("elias_sparse_encode"):
+                fn = lambda: gc.qsgd_elias_encode_sparse(c, nm, n, 512, s, sw, offs, ews)
+            else:
+                dc = torch.empty_like(c)
+                dn = torch.empty_like(nm)
+                fn = lambda: gc.qsgd_elias_decode_sparse(sw, offs, n, 512, s, dc, dn)
+        elif name.startswith("elias_encode"):
             fn = lambda: gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews)
         else:
             dc = torch.empty_like(c)

@@ -934,6 +934,47 @@ struct SparseBucket {
     uint32_t total;      // the bucket's bits, norm and closing distance included
 };
 
+// Calls f(c, sign, level) for each coordinate c in [c0, c1) of the bucket
+// starting at coordinate lo whose level is not 0, in order.  A whole bucket's
+// lane range is read a word (or, for 2-byte lane ranges, a half-word) at a
+// time and only non-zero codes are visited; the ragged last bucket reads
+// byte by byte so that nothing past the codes is touched.
+template <bool FOUR, typename F>
+__device__ __forceinline__ void for_nonzero(const uint8_t* codes, int64_t lo, int c0, int c1, bool whole, F f) {
+    if (!whole) {
+        for (int c = c0; c < c1; ++c) {
+            uint32_t sg, lv;
+            code_at<FOUR>(codes, lo + c, sg, lv);
+            if (lv) f(c, sg, lv);
+        }
+        return;
+    }
+    constexpr int kPerWord = FOUR ? 8 : 4;
+    const int ncodes = c1 - c0;
+    const uint8_t* base = codes + (FOUR ? (lo + c0) / 2 : lo + c0);
+    for (int k = 0; k < ncodes; k += kPerWord) {
+        uint32_t w;
+        if (FOUR && ncodes < 8) w = __ldg(reinterpret_cast<const uint16_t*>(base));   // 4 codes, 2 bytes
+        else w = __ldg(reinterpret_cast<const uint32_t*>(base) + k / kPerWord);
+        uint32_t nz;
+        if (FOUR) {
+            // element e of the word in nibble e (low nibble first): swap the
+            // nibbles of each byte (the first code of a byte is its high nibble)
+            w = ((w >> 4) & 0x0F0F0F0Fu) | ((w & 0x0F0F0F0Fu) << 4);
+            nz = (w | (w >> 1) | (w >> 2)) & 0x11111111u;
+        } else {
+            nz = ((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
+        }
+        while (nz) {
+            const int bit = __ffs(nz) - 1;
+            nz &= nz - 1;
+            const int e = FOUR ? (bit >> 2) : (bit >> 3);
+            const uint32_t code = FOUR ? (w >> (4 * e)) & 15u : (w >> (8 * e)) & 255u;
+            f(c0 + k + e, FOUR ? code >> 3 : code >> 7, FOUR ? code & 7u : code & 127u);
+        }
+    }
+}
+
 template <bool FOUR>
 __device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, int64_t b, bool levels, int lane) {
     SparseBucket r;
@@ -944,15 +985,12 @@ __device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, in
     r.c1 = min(r.len, r.c0 + cpl);
     int first = -1, prev = -1;
     uint32_t bits = 0;
-    for (int c = r.c0; c < r.c1; ++c) {
-        uint32_t sg, lv;
-        code_at<FOUR>(codes, r.lo + c, sg, lv);
-        if (!lv) continue;
+    for_nonzero<FOUR>(codes, r.lo, r.c0, r.c1, r.len == d, [&](int c, uint32_t, uint32_t lv) {
         if (prev >= 0) bits += omega_len(static_cast<uint32_t>(c - prev));
         else first = c;
         bits += 1 + (levels ? omega_len(lv) : 0);
         prev = c;
-    }
+    });
     int incl = prev;      // inclusive max-scan of the lanes' last non-zero coordinates
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1069,21 +1107,40 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
         const int64_t b = b0 + lb;
         const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b, a.levels, lane);
         if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
-        uint32_t pos = sb.lane_pos;
+        // This lane's bits fill [lane_pos, lane_pos + lane_bits): words are
+        // assembled in a register; a completed word is stored plainly unless
+        // it is the lane's first word and the previous lane's bits end in it,
+        // and the last, partial word is OR-ed (the next lane may share it).
+        uint32_t wi = sb.lane_pos >> 5;
+        int fill = static_cast<int>(sb.lane_pos & 31u);
+        const bool shared_first = fill != 0;
+        const uint32_t first_wi = wi;
+        uint32_t cur = 0u;
         int prev = sb.before;
-        for (int c = sb.c0; c < sb.c1; ++c) {
-            uint32_t sg, lv;
-            code_at<FOUR>(a.codes, sb.lo + c, sg, lv);
-            if (!lv) continue;
+        const bool levels = a.levels;
+        for_nonzero<FOUR>(a.codes, sb.lo, sb.c0, sb.c1, sb.len == a.d, [&](int c, uint32_t sg, uint32_t lv) {
             uint32_t gpat, lpat = 0;
             const int glen = omega(static_cast<uint32_t>(c - prev), &gpat);
-            const int llen = a.levels ? omega(lv, &lpat) : 0;
-            const uint64_t acc = ((((static_cast<uint64_t>(gpat) << 1) | sg) << llen) | lpat);
-            const int len = glen + 1 + llen;
-            emit(stage, pos, acc, len);
-            pos += static_cast<uint32_t>(len);
+            const int llen = levels ? omega(lv, &lpat) : 0;
+            uint64_t piece = ((((static_cast<uint64_t>(gpat) << 1) | sg) << llen) | lpat);
+            int len = glen + 1 + llen;                       // <= 34
+            while (len > 0) {
+                const int t = min(len, 32 - fill);
+                const uint32_t top = static_cast<uint32_t>(piece >> (len - t)) & (0xFFFFFFFFu >> (32 - t));
+                cur |= top << (32 - fill - t);
+                fill += t;
+                len -= t;
+                if (fill == 32) {
+                    if (shared_first && wi == first_wi) atomicOr(stage + wi, cur);
+                    else stage[wi] = cur;
+                    ++wi;
+                    cur = 0u;
+                    fill = 0;
+                }
+            }
             prev = c;
-        }
+        });
+        if (fill > 0) atomicOr(stage + wi, cur);
         if (lane == 0) {
             uint32_t tpat;
             const int tlen = omega(static_cast<uint32_t>(sb.len - sb.last_all), &tpat);
@@ -1106,8 +1163,31 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
 // this encoder did not write -- a distance past the bucket's end, a read past
 // its words, a level above s or an impossible codeword -- sets the status to
 // GC_ERR_CORRUPT.
+// Elias-omega codewords that end inside a 12-bit window (values up to 63),
+// looked up as (value << 4) | length, 0 when the codeword is longer.
+constexpr int kOmegaWin = 12;
+
+__device__ __forceinline__ uint32_t omega_window_entry(uint32_t x) {
+    int pos = 0;
+    uint32_t N = 1;
+    for (;;) {
+        if (pos >= kOmegaWin) return 0u;
+        const uint32_t bit = (x >> (kOmegaWin - 1 - pos)) & 1u;
+        ++pos;
+        if (!bit) break;
+        if (pos + static_cast<int>(N) > kOmegaWin) return 0u;
+        const uint32_t v = (x >> (kOmegaWin - pos - static_cast<int>(N))) & ((1u << N) - 1u);
+        pos += static_cast<int>(N);
+        N = (1u << N) | v;
+    }
+    return (N << 4) | static_cast<uint32_t>(pos);
+}
+
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) {
+    __shared__ uint16_t otab[1 << kOmegaWin];
+    for (int i = threadIdx.x; i < (1 << kOmegaWin); i += kThreads)
+        otab[i] = static_cast<uint16_t>(omega_window_entry(static_cast<uint32_t>(i)));
     const int stream = blockIdx.y;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kThreads;
     const int64_t cnt = a.nbuckets - b0 < kThreads ? a.nbuckets - b0 : kThreads;
@@ -1158,6 +1238,16 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) 
         return v;
     };
     auto get_omega = [&]() -> uint32_t {
+        refill();
+        const uint32_t e = otab[static_cast<uint32_t>(win >> (64 - kOmegaWin))];
+        if (e) {
+            const int l = static_cast<int>(e & 15u);
+            win <<= l;
+            have -= l;
+            used += l;
+            bad |= used > limit;
+            return e >> 4;
+        }
         uint32_t N = 1;
         while (take(1)) {
             if (N > 16) {                      // no distance or level of a valid stream is this long

@@ -382,19 +382,23 @@ k_qsgd_quantize(const QArgs a) {
     quantize_bucket_body<ROUNDS, FOUR, MAXNORM, false, false, !MAXNORM>(a, b, lane, 0.0f, unused);
 }
 
-// After k_qsgd_quantize: each warp scans 32 norms at a time and redoes, with
-// the rescue, every bucket flagged there (norm -1); the first warp also does
-// the partial last bucket.
+// After k_qsgd_quantize: the first warp does the partial last bucket, then
+// each warp scans 32 norms at a time and redoes, with the rescue, every
+// bucket flagged there (norm -1).
 template <int ROUNDS, bool FOUR, bool MAXNORM>
 __global__ void __launch_bounds__(kThreads)
 k_qsgd_fixup(const QArgs a) {
     constexpr int D = 128 * ROUNDS;
-    wait_for_primary();
     const int lane = threadIdx.x & 31;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t nfull = a.n / D;
     float unused[ROUNDS][4];
+    // the partial last bucket touches nothing the main kernel writes: done
+    // before waiting for it
+    if (gw == 0 && nfull * D < a.n)
+        quantize_bucket_body<ROUNDS, FOUR, MAXNORM, false, true, false>(a, nfull, lane, 0.0f, unused);
+    wait_for_primary();
     if (!MAXNORM) {
         for (int64_t g0 = gw * 32; g0 < nfull; g0 += nw * 32) {
             const int64_t b = g0 + lane;
@@ -406,8 +410,6 @@ k_qsgd_fixup(const QArgs a) {
             }
         }
     }
-    if (gw == 0 && nfull * D < a.n)
-        quantize_bucket_body<ROUNDS, FOUR, MAXNORM, false, true, false>(a, nfull, lane, 0.0f, unused);
 }
 
 // Every worker's quantisation and the dequant-sum in one pass: one warp per
@@ -468,18 +470,19 @@ k_qsgd_step(const StepArgs a) {
     step_bucket<ROUNDS, FOUR, MAXNORM, false, !MAXNORM>(a, b, lane);
 }
 
-// After k_qsgd_step: every bucket in which some worker was flagged is redone
-// for all workers (norms, codes and the sum); the first warp also does the
-// partial last bucket.
+// After k_qsgd_step: the first warp does the partial last bucket, then every
+// bucket in which some worker was flagged is redone for all workers (norms,
+// codes and the sum).
 template <int ROUNDS, bool FOUR, bool MAXNORM>
 __global__ void __launch_bounds__(kThreads)
 k_qsgd_step_fixup(const StepArgs a) {
     constexpr int D = 128 * ROUNDS;
-    wait_for_primary();
     const int lane = threadIdx.x & 31;
     const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t nfull = a.q.n / D;
+    if (gw == 0 && nfull * D < a.q.n) step_bucket<ROUNDS, FOUR, MAXNORM, true, false>(a, nfull, lane);
+    wait_for_primary();
     if (!MAXNORM) {
         for (int64_t g0 = gw * 32; g0 < nfull; g0 += nw * 32) {
             const int64_t b = g0 + lane;
@@ -494,7 +497,6 @@ k_qsgd_step_fixup(const StepArgs a) {
             }
         }
     }
-    if (gw == 0 && nfull * D < a.q.n) step_bucket<ROUNDS, FOUR, MAXNORM, true, false>(a, nfull, lane);
 }
 
 struct DArgs {
