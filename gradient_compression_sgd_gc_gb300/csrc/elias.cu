@@ -902,6 +902,31 @@ __device__ __forceinline__ int omega_len(uint32_t N) {
     return len;
 }
 
+// Elias-omega codewords of 1..255 as (pattern << 5) | length (at most 14
+// bits), built per CTA in shared memory; longer values take omega().
+constexpr int kOmegaLut = 256;
+
+__device__ __forceinline__ void build_omega_lut(uint32_t* lut) {
+    for (int i = threadIdx.x; i < kOmegaLut; i += blockDim.x) {
+        uint32_t pat = 0;
+        const int len = i ? omega(static_cast<uint32_t>(i), &pat) : 0;
+        lut[i] = (pat << 5) | static_cast<uint32_t>(len);
+    }
+}
+
+__device__ __forceinline__ int omega_len_lut(const uint32_t* lut, uint32_t N) {
+    return N < kOmegaLut ? static_cast<int>(lut[N] & 31u) : omega_len(N);
+}
+
+__device__ __forceinline__ int omega_lut(const uint32_t* lut, uint32_t N, uint32_t* pat) {
+    if (N < kOmegaLut) {
+        const uint32_t e = lut[N];
+        *pat = e >> 5;
+        return static_cast<int>(e & 31u);
+    }
+    return omega(N, pat);
+}
+
 // Words of a sparse-coded bucket of len coordinates, whatever its codes: 32
 // norm bits and at most 18 bits per coordinate (the distances sum to len and
 // |omega(g)| <= g + 2; one sign bit; omega(level) <= 14 bits) plus 2.
@@ -976,7 +1001,8 @@ __device__ __forceinline__ void for_nonzero(const uint8_t* codes, int64_t lo, in
 }
 
 template <bool FOUR>
-__device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, int64_t b, bool levels, int lane) {
+__device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, int64_t b, bool levels, int lane,
+                                      const uint32_t* lut) {
     SparseBucket r;
     r.lo = b * d;
     r.len = static_cast<int>(n - r.lo < d ? n - r.lo : static_cast<int64_t>(d));
@@ -986,9 +1012,9 @@ __device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, in
     int first = -1, prev = -1;
     uint32_t bits = 0;
     for_nonzero<FOUR>(codes, r.lo, r.c0, r.c1, r.len == d, [&](int c, uint32_t, uint32_t lv) {
-        if (prev >= 0) bits += omega_len(static_cast<uint32_t>(c - prev));
+        if (prev >= 0) bits += omega_len_lut(lut, static_cast<uint32_t>(c - prev));
         else first = c;
-        bits += 1 + (levels ? omega_len(lv) : 0);
+        bits += 1 + (levels ? omega_len_lut(lut, lv) : 0);
         prev = c;
     });
     int incl = prev;      // inclusive max-scan of the lanes' last non-zero coordinates
@@ -1000,12 +1026,12 @@ __device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, in
     const int excl = __shfl_up_sync(0xffffffffu, incl, 1);
     r.before = lane ? excl : -1;
     r.last_all = __shfl_sync(0xffffffffu, incl, 31);
-    if (first >= 0) bits += omega_len(static_cast<uint32_t>(first - r.before));
+    if (first >= 0) bits += omega_len_lut(lut, static_cast<uint32_t>(first - r.before));
     r.lane_bits = bits;
     const int in = warp_incl_sum(static_cast<int>(bits), lane);
     r.lane_pos = 32u + static_cast<uint32_t>(in) - bits;
     const uint32_t all = static_cast<uint32_t>(__shfl_sync(0xffffffffu, in, 31));
-    r.total = 32u + all + static_cast<uint32_t>(omega_len(static_cast<uint32_t>(r.len - r.last_all)));
+    r.total = 32u + all + static_cast<uint32_t>(omega_len_lut(lut, static_cast<uint32_t>(r.len - r.last_all)));
     return r;
 }
 
@@ -1027,13 +1053,16 @@ struct SparseArgs {
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_sparse_count(SparseArgs a) {
     __shared__ uint32_t wsum[kWarpsPerBlock];
+    __shared__ uint32_t lut[kOmegaLut];
     __shared__ bool is_last;
+    build_omega_lut(lut);
+    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
     const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
     uint32_t mine = 0;
     for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
-        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b0 + lb, a.levels, lane);
+        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b0 + lb, a.levels, lane, lut);
         const uint32_t nw = (sb.total + 31u) >> 5;
         if (lane == 0) a.ws.counts[b0 + lb] = nw;
         mine += nw;
@@ -1083,8 +1112,10 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_count(SparseArgs a) {
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) {
     extern __shared__ uint32_t smem[];
-    uint32_t* offs = smem;                       // [kChunk]
-    uint32_t* stages = smem + kChunk;            // [kWarpsPerBlock][stage_words]
+    uint32_t* lut = smem;                        // [kOmegaLut]
+    uint32_t* offs = smem + kOmegaLut;           // [kChunk]
+    uint32_t* stages = smem + kOmegaLut + kChunk;   // [kWarpsPerBlock][stage_words]
+    build_omega_lut(lut);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
     for (int i = threadIdx.x; i < kWarpsPerBlock * a.stage_words; i += kThreads) stages[i] = 0u;
@@ -1105,7 +1136,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
     const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
     for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
         const int64_t b = b0 + lb;
-        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b, a.levels, lane);
+        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b, a.levels, lane, lut);
         if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
         // This lane's bits fill [lane_pos, lane_pos + lane_bits): words are
         // assembled in a register; a completed word is stored plainly unless
@@ -1120,8 +1151,8 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
         const bool levels = a.levels;
         for_nonzero<FOUR>(a.codes, sb.lo, sb.c0, sb.c1, sb.len == a.d, [&](int c, uint32_t sg, uint32_t lv) {
             uint32_t gpat, lpat = 0;
-            const int glen = omega(static_cast<uint32_t>(c - prev), &gpat);
-            const int llen = levels ? omega(lv, &lpat) : 0;
+            const int glen = omega_lut(lut, static_cast<uint32_t>(c - prev), &gpat);
+            const int llen = levels ? omega_lut(lut, lv, &lpat) : 0;
             uint64_t piece = ((((static_cast<uint64_t>(gpat) << 1) | sg) << llen) | lpat);
             int len = glen + 1 + llen;                       // <= 34
             while (len > 0) {
@@ -1143,7 +1174,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
         if (fill > 0) atomicOr(stage + wi, cur);
         if (lane == 0) {
             uint32_t tpat;
-            const int tlen = omega(static_cast<uint32_t>(sb.len - sb.last_all), &tpat);
+            const int tlen = omega_lut(lut, static_cast<uint32_t>(sb.len - sb.last_all), &tpat);
             emit(stage, sb.total - static_cast<uint32_t>(tlen), tpat, tlen);
         }
         __syncwarp();
@@ -1421,7 +1452,7 @@ int qsgd_elias_encode_sparse(const uint8_t* codes, const float* norms, int64_t n
     else
         k_elias_sparse_count<false><<<grid, kThreads, 0, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
-    const size_t smem = sizeof(uint32_t) * (kChunk + static_cast<size_t>(kWarpsPerBlock) * a.stage_words);
+    const size_t smem = sizeof(uint32_t) * (kOmegaLut + kChunk + static_cast<size_t>(kWarpsPerBlock) * a.stage_words);
     if (four)
         k_elias_sparse_encode<true><<<grid, kThreads, smem, s>>>(a);
     else
