@@ -1119,9 +1119,12 @@ def run_case(name: str, n: int):
         ews = torch.empty(gc.qsgd_elias_workspace_bytes(n, 512), dtype=torch.uint8, device=dev)
         gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews)
         # the encoders read the codes twice (count, then encode); each call
-        # starts from a flushed L2 so that a capture without cache control sees
-        # the first read come from DRAM and the second from wherever it does
-        flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+        # starts from an L2 filled with other (clean) data -- a read of a
+        # buffer larger than L2, no write-back to come -- so that a capture
+        # without cache control sees the first read come from DRAM and the
+        # second from wherever it does in a real call
+        flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+        flush_l2 = lambda buf: buf.sum()
         if name.startswith("elias_sparse"):
             sw = torch.empty(gc.qsgd_elias_sparse_max_words(n, 512), dtype=torch.int32, device=dev)
             gc.qsgd_elias_encode_sparse(c, nm, n, 512, s, sw, offs, ews)

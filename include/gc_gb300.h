@@ -9,12 +9,15 @@
  *     full-precision correction step;
  *   - QSGD bucketed stochastic quantisation to 4- or 8-bit sign-magnitude
  *     codes, its dequantise-sum, and the lossless Elias-omega coding of the
- *     codes;
+ *     codes (dense and sparse regimes);
  *   - SAPS seeded random-mask sparsification compacted to (index, value)
- *     pairs, peer averaging over a random perfect matching, and the EASGD
- *     elastic step;
+ *     pairs, peer averaging over a random or bandwidth-aware perfect
+ *     matching, and the EASGD elastic step;
  *   - one-pass forms of each method's step (gc_2bit_step, qsgd_step,
- *     saps_round), bit-identical to the separate calls.
+ *     saps_round), bit-identical to the separate calls, and S successive
+ *     2-bit steps of one worker in one launch (gc_2bit_quantize_steps);
+ *   - per-worker forms of the SAPS exchange steps for workers that live in
+ *     different processes (saps_pair_average_remote, easgd_step_from_sum).
  *
  * Conventions shared by every entry point
  *   Ownership   The caller allocates and owns every buffer.  The library

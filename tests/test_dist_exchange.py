@@ -116,6 +116,10 @@ def _rank_main(rank, world, port, case, out):
             out[rank] = (o.numpy().copy(), ex.g_codes.numpy().copy(), ex.g_norms.numpy().copy())
         else:
             n, p = 20_011, 0.05
+            bandwidth = case == "saps_bw"
+            if bandwidth:
+                B = np.random.default_rng(77).uniform(1.0, 10.0, (world, world))
+                R = np.full((world, world), gc.NEVER, np.int64)
             ex = gdist.SAPSExchange(n, p, 5, 0.9, 0.9, "cpu", ops=OracleOps)
             rng = np.random.default_rng(4000 + rank)
             model = torch.from_numpy(rng.normal(0, 0.05, n).astype(np.float32).astype(np.float64))
@@ -123,7 +127,11 @@ def _rank_main(rank, world, port, case, out):
                        for k in range(world)]
             center = torch.from_numpy(sum(centers) / world)
             for t in range(3):
-                pairs = gc.saps_matching(gc.saps_round_seed(5, t), world)
+                seed_t = gc.saps_round_seed(5, t)
+                if bandwidth:   # every rank runs the coordinator's selection on its own copy of R
+                    pairs = gc.saps_matching_bandwidth(B, 5.0, R, t, 2, seed_t)
+                else:
+                    pairs = gc.saps_matching(seed_t, world)
                 ex.round(t, model, center, pairs)
             out[rank] = (model.numpy().copy(), center.numpy().copy())
     finally:
@@ -168,18 +176,26 @@ def test_qsgd_exchange_equals_single_process(world):
         np.testing.assert_array_equal(got[r][2], np.stack([nm for nm, _ in q]))
 
 
-@pytest.mark.parametrize("world", [2, 4])
-def test_saps_exchange_equals_single_process(world):
+@pytest.mark.parametrize("world,case", [(2, "saps"), (4, "saps"), (4, "saps_bw")])
+def test_saps_exchange_equals_single_process(world, case):
+    """SAPS rounds across ranks with the seeded uniform matching, and (saps_bw)
+    with the bandwidth-aware selection of Algorithm 3 run on every rank."""
     import oracle
     import gradient_compression_sgd_gc_gb300 as gc
-    got = _run(world, "saps")
+    got = _run(world, case)
     n, p = 20_011, 0.05
     models = [np.random.default_rng(4000 + k).normal(0, 0.05, n).astype(np.float32).astype(np.float64)
               for k in range(world)]
     center = sum(models) / world
+    if case == "saps_bw":
+        B = np.random.default_rng(77).uniform(1.0, 10.0, (world, world))
+        R = np.full((world, world), gc.NEVER, np.int64)
     for t in range(3):
         seed_t = gc.saps_round_seed(5, t)
-        pairs = np.array(gc.saps_matching(seed_t, world), np.int32)
+        if case == "saps_bw":
+            pairs = np.array(gc.saps_matching_bandwidth(B, 5.0, R, t, 2, seed_t), np.int32)
+        else:
+            pairs = np.array(gc.saps_matching(seed_t, world), np.int32)
         K, idx, vals = oracle.saps_mask_compact(n, p, seed_t, models)
         oracle.saps_peer_average(models, vals, idx, pairs)
         oracle.easgd_step(models, 0.9, 0.9, center)
