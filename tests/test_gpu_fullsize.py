@@ -21,17 +21,25 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+@pytest.mark.parametrize("one_pass", [False, True], ids=["separate", "one_pass"])
 @pytest.mark.parametrize("cfg", [wl.QSGD_S7, wl.QSGD_S127], ids=lambda c: c.name)
-def test_qsgd_full_size_sampled(cfg):
+def test_qsgd_full_size_sampled(cfg, one_pass):
+    """4 workers x 61,100,840, bucket 512: every worker quantised and the
+    average dequantised, by the separate calls or by qsgd_step in one pass;
+    sampled chunks against the oracle (norms, codes up to boundary cases, the
+    average of the GPU's own codes on every element of the chunks)."""
     n, W, d, s = cfg.n, cfg.workers, cfg.bucket, cfg.s
     nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
     vs = [wl.qsgd_grad(cfg, w, device=DEV) for w in range(W)]
     norms = [torch.empty(nb, device=DEV) for _ in range(W)]
     codes = [torch.empty(cb, dtype=torch.uint8, device=DEV) for _ in range(W)]
-    for w in range(W):
-        gc.qsgd_quantize(vs[w], d, s, cfg.seed, w, norms[w], codes[w])
     out = torch.empty(n, device=DEV)
-    gc.qsgd_dequant_sum(codes, norms, n, d, s, 1.0 / W, out)
+    if one_pass:
+        gc.qsgd_step(vs, d, s, cfg.seed, norms, codes, 1.0 / W, out)
+    else:
+        for w in range(W):
+            gc.qsgd_quantize(vs[w], d, s, cfg.seed, w, norms[w], codes[w])
+        gc.qsgd_dequant_sum(codes, norms, n, d, s, 1.0 / W, out)
     torch.cuda.synchronize()
     chunks = sample_chunks(n, 40, 4 * d, align=d, seed=11)
     assert chunks[-1][1] == n and (n - chunks[-1][0]) % d == 296 % d
@@ -58,9 +66,11 @@ def test_qsgd_full_size_sampled(cfg):
     print(f"{cfg.name}: level mismatches at boundaries in {len(chunks)} sampled chunks: {mism}")
 
 
-def test_cdsgd_full_size_sampled():
+@pytest.mark.parametrize("one_pass", [False, True], ids=["separate", "one_pass"])
+def test_cdsgd_full_size_sampled(one_pass):
     """4 workers x 1.3e9 bf16, 8 steps, k = 4: steps 1-3 and 5-7 quantise each
-    worker and apply the averaged dequantised sum, steps 4 and 8 apply the
+    worker and apply the averaged dequantised sum (the batched quantiser and
+    the dequant-sum, or gc_2bit_step in one pass), steps 4 and 8 apply the
     residual-compensated full-precision average."""
     cfg = wl.CDSGD
     n, W, t, lr, k = cfg.n, cfg.workers, cfg.threshold, cfg.lr, cfg.correction_every
@@ -74,7 +84,9 @@ def test_cdsgd_full_size_sampled():
     for step in range(1, 9):
         grads = [wl.twobit_grad(cfg, step, q, device=DEV) for q in range(W)]
         gh = {(c, q): host_bf16_bits(grads[q][c[0]:c[1]]) for c in chunks for q in range(W)}
-        if step % k:
+        if step % k and one_pass:
+            gc.gc_2bit_step(grads, res, codes, t, gc.GC_UPD_SGD, lr=lr, weights=wts)
+        elif step % k:
             gc.gc_2bit_quantize_batched(grads, res, codes, t)
             gc.gc_2bit_dequant_sum_update(codes, n, t, gc.GC_UPD_SGD, lr=lr, weights=wts)
         else:
@@ -286,3 +298,46 @@ def test_elias_beyond_two_to_the_32():
     assert torch.equal(dc & 0x77, codes & 0x77)          # levels; a level-0 code comes back with sign 0
     del codes, norms, words, offs, ws, dc, dn
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cfg", [wl.QSGD_S7, wl.QSGD_S127], ids=lambda c: c.name)
+def test_elias_sparse_full_size_sampled(cfg):
+    """The sparse-regime Elias stream of one worker's codes on the configured
+    61,100,840 coordinates: 48 sampled buckets (the first and the ragged last
+    among them) word for word against the oracle's encoding of the same
+    bucket, and the whole stream decoded back to the codes."""
+    n, d, s = cfg.n, cfg.bucket, cfg.s
+    v = wl.qsgd_grad(cfg, 0, device=DEV)
+    nb, cb = gc.qsgd_num_buckets(n, d), gc.qsgd_code_bytes(n, s)
+    norms = torch.empty(nb, device=DEV)
+    codes = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    gc.qsgd_quantize(v, d, s, cfg.seed, 0, norms, codes)
+    cap = gc.qsgd_elias_sparse_max_words(n, d)
+    words = torch.empty(cap, dtype=torch.int32, device=DEV)
+    offs = torch.empty(nb + 1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(gc.qsgd_elias_workspace_bytes(n, d), dtype=torch.uint8, device=DEV)
+    gc.qsgd_elias_encode_sparse(codes, norms, n, d, s, words, offs, ws)
+    dc = torch.empty_like(codes)
+    dn = torch.empty_like(norms)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gc.qsgd_elias_decode_sparse(words, offs, n, d, s, dc, dn, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    hc, hn = codes.cpu().numpy(), host_f32(norms)
+    ho, hw = host_u32(offs), host_u32(words)
+    rng = np.random.default_rng(9)
+    picks = sorted({0, nb - 1} | {int(b) for b in rng.integers(0, nb, 46)})
+    for b in picks:
+        lo = b * d
+        ln = min(d, n - lo)
+        cs = hc[lo // 2:(lo + ln + 1) // 2] if s <= 7 else hc[lo:lo + ln]
+        rw, ro = oracle.qsgd_elias_encode_sparse(np.ascontiguousarray(cs), hn[b:b + 1].copy(), ln, d, s)
+        np.testing.assert_array_equal(hw[ho[b]:ho[b + 1]], rw)
+    if s <= 7:
+        nib = np.stack([hc >> 4, hc & 15], axis=1).reshape(-1)
+        nib = np.where((nib & 7) == 0, 0, nib)
+        canon = ((nib[0::2] << 4) | nib[1::2]).astype(np.uint8)
+    else:
+        canon = np.where((hc & 127) == 0, 0, hc).astype(np.uint8)
+    np.testing.assert_array_equal(dc.cpu().numpy(), canon)
+    assert torch.equal(dn.view(torch.int32), norms.view(torch.int32))
