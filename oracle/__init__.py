@@ -72,6 +72,7 @@ def _load():
             "orc_elias_omega_bits": (i32, [ctypes.c_uint32, ctypes.c_char_p]),
             "orc_qsgd_elias_encode": (i64, [vp, vp, i64, i64, i32, vp, vp]),
             "orc_qsgd_elias_decode": (None, [vp, vp, i64, i64, i32, vp, vp]),
+            "orc_qsgd_elias_quarter_marks": (None, [vp, i64, i64, i32, vp]),
             "orc_qsgd_elias_encode_sparse": (i64, [vp, vp, i64, i64, i32, vp, vp]),
             "orc_qsgd_elias_decode_sparse": (i64, [vp, vp, i64, i64, i32, vp, vp]),
             "orc_qsgd_dequant_sum": (None, [vp, vp, i32, i64, i64, i32, f64, vp]),
@@ -389,3 +390,13 @@ def qsgd_elias_decode_sparse(words: np.ndarray, offsets: np.ndarray, n: int, buc
     bad = int(_load().orc_qsgd_elias_decode_sparse(_ptr(words), _ptr(offsets), n, bucket, s, _ptr(codes),
                                                    _ptr(norms)))
     return codes, norms, bad
+
+
+def qsgd_elias_quarter_marks(codes: np.ndarray, n: int, bucket: int, s: int) -> np.ndarray:
+    """uint16 [3 * nbuckets]: bit offset (from the bucket's first word) where the
+    codeword of each bucket's coordinate k*bucket/4 starts, k = 1..3."""
+    _check(codes, np.uint8, "codes", qsgd_code_bytes(n, s))
+    nb = (n + bucket - 1) // bucket
+    marks = np.zeros(3 * nb, dtype=np.uint16)
+    _load().orc_qsgd_elias_quarter_marks(_ptr(codes), n, bucket, s, _ptr(marks))
+    return marks

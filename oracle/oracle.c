@@ -817,3 +817,34 @@ int64_t orc_qsgd_elias_decode_sparse(const uint32_t *words, const uint32_t *offs
     }
     return bad;
 }
+
+/*
+ * Side information for decoding a dense-regime bucket in parallel (not on
+ * the pages; the per-bucket offsets table above is side information of the
+ * same kind): marks[3b + k - 1], k = 1..3, is the bit offset, counted from
+ * the first bit of bucket b's first word, at which the codeword of the
+ * bucket's coordinate k d/4 starts; a quarter that starts past the bucket's
+ * last coordinate (a short last bucket) gets the bucket's end.
+ */
+void orc_qsgd_elias_quarter_marks(const uint8_t *codes, int64_t n, int64_t d, int s,
+                                  uint16_t *marks)
+{
+    int64_t nbuckets = (n + d - 1) / d;
+    int64_t q = d / 4;
+    for (int64_t b = 0; b < nbuckets; ++b) {
+        int64_t lo = b * d;
+        int64_t len = (b + 1) * d < n ? d : n - lo;
+        int64_t pos = 32;
+        for (int64_t i = 0; i < len; ++i) {
+            if (i > 0 && i % q == 0)
+                marks[3 * b + i / q - 1] = (uint16_t)pos;
+            int sign, level;
+            qsgd_code_at(codes, lo + i, s, &sign, &level);
+            char bits[64];
+            pos += orc_elias_omega_bits((uint32_t)level + 1u, bits) + (level > 0 ? 1 : 0);
+        }
+        for (int64_t k = 1; k <= 3; ++k)
+            if (k * q >= len)
+                marks[3 * b + k - 1] = (uint16_t)pos;
+    }
+}

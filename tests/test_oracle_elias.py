@@ -196,3 +196,59 @@ def test_dense_regime_expected_length():
     assert abs(mean - expect) <= 4 * math.sqrt(var / seeds), (mean, expect)
     per_bucket = mean / nb
     assert per_bucket <= 1.05 * (2.8 * d + 32)
+
+
+def _read_codes_from(words, bitpos, count, table_inv):
+    """Decodes `count` dense-regime codewords (omega(level + 1), then a sign
+    bit when level > 0) from the stream bits starting at `bitpos`, with a
+    plain bit reader and the hand-written codeword table (independent of the
+    oracle's decoder).  Returns (sign, level) pairs."""
+    bits = "".join(format(int(w), "032b") for w in words)
+    out, p = [], bitpos
+    for _ in range(count):
+        for L in range(1, 20):
+            N = table_inv.get(bits[p:p + L])
+            if N is not None:
+                break
+        else:
+            raise AssertionError("no codeword")
+        p += L
+        level = N - 1
+        sign = 0
+        if level:
+            sign = int(bits[p])
+            p += 1
+        out.append((sign, level))
+    return out
+
+
+@pytest.mark.parametrize("s,d,n", [(7, 512, 3 * 512 + 201), (127, 128, 5 * 128 + 31), (22, 256, 2 * 256 + 3)])
+def test_quarter_marks_start_each_quarter(s, d, n):
+    """Decoding a bucket's stream from each quarter mark, with a reader that
+    knows only the codeword table, gives that quarter's codes; the marks of a
+    quarter past a short bucket's end equal the bucket's end."""
+    table = _codewords()
+    inv = {w: N for N, w in table.items()}
+    for N in range(1, 130):                      # every level + 1 up to 128
+        inv.setdefault(oracle.elias_omega(N), N)
+    rng = np.random.default_rng(d + s)
+    v = rng.standard_normal(n).astype(np.float32)
+    norms, codes = oracle.qsgd_quantize(v, d, s, seed=3, worker=0)
+    w, off = oracle.qsgd_elias_encode(codes, norms, n, d, s)
+    marks = oracle.qsgd_elias_quarter_marks(codes, n, d, s)
+    sg, lv = _unpack(codes, n, s)
+    q = d // 4
+    for b in range((n + d - 1) // d):
+        bw = w[off[b]:off[b + 1]]
+        ln = min(d, n - b * d)
+        for k in range(1, 4):
+            m = int(marks[3 * b + k - 1])
+            if k * q >= ln:
+                # the end of the bucket's codewords: the rest of its last word is padding
+                assert (32 * len(bw) - m) < 32 and all(c == "0" for c in "".join(format(int(x), "032b") for x in bw)[m:])
+                continue
+            cnt = min(q, ln - k * q)
+            got = _read_codes_from(bw, m, cnt, inv)
+            lo = b * d + k * q
+            exp = [(int(sg[i]) if lv[i] else 0, int(lv[i])) for i in range(lo, lo + cnt)]
+            assert got == exp
