@@ -693,6 +693,27 @@ def rows(args, dev, peak):
         out[f"{qcfg.name}.elias_decode"] = _row(qcfg.name, "qsgd_elias_decode",
                                                 4 * total + 4 * (nb + 1) + cb + 4 * nb, tm.ms("x"), peak, n,
                                                 {"issue": issue_roofline(f"elias_decode_s{s}", tm.ms("x"))})
+        # the quarter-marked stream of worker 0's codes (the same stream, plus 3
+        # marks per bucket) and its decode with one thread per quarter bucket
+        marks = torch.empty(3 * nb, dtype=torch.int16, device=dev)
+        pme = gc.qsgd_elias_encode_marked(codes[0], norms[0], n, qcfg.bucket, s, words[0], offs[0], marks, ews,
+                                          stream=stream, prepare=True)
+        pqd = gc.qsgd_elias_decode_quarters(words[0], offs[0], marks, n, qcfg.bucket, s, dcodes, dnorms,
+                                            stream=stream, prepare=True)
+        for i in range(22):
+            tm.around("me" if i >= 2 else "w", pme)
+            tm.around("qd" if i >= 2 else "w", pqd)
+        torch.cuda.synchronize(dev)
+        total0 = int(offs[0][nb].item())
+        out[f"{qcfg.name}.elias_encode_marked"] = _row(
+            qcfg.name, "qsgd_elias_encode_marked (count + encode + quarter marks)",
+            cb + 4 * nb + 4 * total0 + 4 * (nb + 1) + 6 * nb, tm.ms("me"), peak, n,
+            {"marks_bits_per_coord": round(48 * nb / n, 4)})
+        out[f"{qcfg.name}.elias_decode_quarters"] = _row(
+            qcfg.name, "qsgd_elias_decode_quarters (a thread per quarter bucket)",
+            4 * total0 + 4 * (nb + 1) + 6 * nb + cb + 4 * nb, tm.ms("qd"), peak, n,
+            {"issue": issue_roofline(f"elias_quarters_s{s}", tm.ms("qd"))})
+        del marks
         # the sparse-regime code (distances between non-zero coordinates) of the
         # same codes, and its decode
         scap = gc.qsgd_elias_sparse_max_words(n, qcfg.bucket)
@@ -1012,7 +1033,8 @@ CASES = ("quantize_f32", "quantize_bf16", "quantize_batched", "step_fused", "dqs
          "elias_encode_s7", "elias_encode_s127", "elias_decode_s7", "elias_decode_s127",
          "quantize_local", "qsgd_maxnorm_s7", "qsgd_maxnorm_s127", "saps_mask_p001", "saps_round",
          "qsgd_step_s7", "qsgd_step_s127", "step_bf16", "multi_step", "elias_sparse_encode_s7",
-         "elias_sparse_encode_s127", "elias_sparse_decode_s7", "elias_sparse_decode_s127")
+         "elias_sparse_encode_s127", "elias_sparse_decode_s7", "elias_sparse_decode_s127", "elias_quarters_s7",
+         "elias_quarters_s127")
 
 
 def run_case(name: str, n: int):
@@ -1134,6 +1156,12 @@ def run_case(name: str, n: int):
                 dc = torch.empty_like(c)
                 dn = torch.empty_like(nm)
                 fn = lambda: gc.qsgd_elias_decode_sparse(sw, offs, n, 512, s, dc, dn)
+        elif name.startswith("elias_quarters"):
+            marks = torch.empty(3 * nb, dtype=torch.int16, device=dev)
+            gc.qsgd_elias_encode_marked(c, nm, n, 512, s, words, offs, marks, ews)
+            dc = torch.empty_like(c)
+            dn = torch.empty_like(nm)
+            fn = lambda: gc.qsgd_elias_decode_quarters(words, offs, marks, n, 512, s, dc, dn)
         elif name.startswith("elias_encode"):
             fn = lambda: (flush_l2(flush), gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews))
         else:

@@ -14,6 +14,7 @@ Entry points (same names as the C ABI):
   gc_compensated_sum_update,
   qsgd_quantize, qsgd_quantize_maxnorm, qsgd_dequant_sum, qsgd_step,
   qsgd_elias_encode, qsgd_elias_decode, qsgd_elias_decode_batched, qsgd_elias_max_words,
+  qsgd_elias_encode_marked, qsgd_elias_decode_quarters,
   qsgd_elias_encode_sparse, qsgd_elias_decode_sparse, qsgd_elias_sparse_max_words,
   qsgd_elias_workspace_bytes,
   saps_round_seed, saps_matching, saps_matching_bandwidth, saps_workspace_bytes, saps_mask_compact,
@@ -45,6 +46,7 @@ __all__ = [
     "gc_2bit_step", "gc_2bit_quantize_local", "gc_2bit_quantize_steps", "qsgd_quantize_maxnorm",
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
     "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step", "qsgd_elias_decode_batched",
+    "qsgd_elias_encode_marked", "qsgd_elias_decode_quarters",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -107,6 +109,8 @@ def load():
             "qsgd_elias_workspace_bytes": (sz, [i64, i32]),
             "qsgd_elias_decode": (i32, [vp, vp, i64, i32, i32, vp, vp, vp, vp]),
             "qsgd_elias_decode_batched": (i32, [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp]),
+            "qsgd_elias_encode_marked": (i32, [vp, vp, i64, i32, i32, vp, u64, vp, vp, vp, sz, vp]),
+            "qsgd_elias_decode_quarters": (i32, [vp, vp, vp, i64, i32, i32, vp, vp, vp, vp]),
             "saps_round_seed": (u64, [u64, u64]),
             "saps_matching": (i32, [u64, i32, vp]),
             "saps_workspace_bytes": (sz, [i64]),
@@ -426,6 +430,37 @@ def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket
     keep = (words, offsets, codes, norms) + (() if status is None else (status,))
     return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
 
+
+def qsgd_elias_encode_marked(codes: torch.Tensor, norms: torch.Tensor, n: int, bucket: int, s_levels: int,
+                             words: torch.Tensor, offsets: torch.Tensor, marks: torch.Tensor,
+                             workspace: torch.Tensor, stream=None, prepare: bool = False):
+    """qsgd_elias_encode that also writes the quarter marks: an int16 tensor
+    [3 * nbuckets] holding uint16 bit positions (the start of each bucket's
+    quarters 1..3 within its stream)."""
+    lib = load()
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _dev(norms, "norms", torch.float32, nb), int(n), int(bucket), int(s_levels),
+            _dev(words, "words", torch.int32), words.numel(),
+            _dev(offsets, "offsets", torch.int32, nb + 1), _dev(marks, "marks", torch.int16, 3 * nb),
+            _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream, codes))
+    return _invoke(lib.qsgd_elias_encode_marked, args, "qsgd_elias_encode_marked", prepare,
+                   (codes, norms, words, offsets, marks, workspace))
+
+
+def qsgd_elias_decode_quarters(words: torch.Tensor, offsets: torch.Tensor, marks: torch.Tensor, n: int,
+                               bucket: int, s_levels: int, codes: torch.Tensor, norms: torch.Tensor,
+                               status: torch.Tensor | None = None, stream=None, prepare: bool = False):
+    """qsgd_elias_decode of a marked stream, one thread per quarter bucket."""
+    lib = load()
+    nb = qsgd_num_buckets(n, bucket)
+    args = (_dev(words, "words", torch.int32), _dev(offsets, "offsets", torch.int32, nb + 1),
+            _dev(marks, "marks", torch.int16, 3 * nb), int(n), int(bucket), int(s_levels),
+            _dev(codes, "codes", torch.uint8, qsgd_code_bytes(n, s_levels)),
+            _dev(norms, "norms", torch.float32, nb),
+            None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words))
+    keep = (words, offsets, marks, codes, norms) + (() if status is None else (status,))
+    return _invoke(lib.qsgd_elias_decode_quarters, args, "qsgd_elias_decode_quarters", prepare, keep)
 
 
 def qsgd_elias_sparse_max_words(n: int, bucket: int) -> int:

@@ -378,6 +378,7 @@ struct EncodeArgs {
     uint32_t* offsets;
     int stage_stride;   // staging words per bucket slot
     int slots;          // bucket slots per warp (32 / G)
+    uint16_t* marks;    // quarter marks [3 * nbuckets], or null
 };
 
 // The stream bits of 16 code bytes (table entries e[]) OR-ed into the
@@ -483,6 +484,12 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
             if (gl >= o) incl += t;
         }
         if (active) emit_piece(stage, pos + incl - len, e);
+        if (a.marks && active) {
+            // a piece that starts a quarter of the bucket records its start bit
+            const int c = (r * g.G + gl) * (FOUR ? 32 : 16);
+            const int q = a.d / 4;
+            if (c > 0 && c % q == 0) a.marks[3 * (b0 + lb) + c / q - 1] = static_cast<uint16_t>(pos + incl - len);
+        }
         pos += __shfl_sync(0xffffffffu, incl, grp * g.G + g.G - 1);
         if (r == R - 1) {
             __syncwarp();
@@ -507,13 +514,22 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
         __syncwarp();
         if (lane == 0) st0[0] = __float_as_uint(__ldg(a.norms + b));
         uint32_t pos = 32;
+        const int q = a.d / 4;
+        const int blen = static_cast<int>(a.n - b * a.d);
         for (int k0 = 0; k0 < nw_in; k0 += 32) {
             uint64_t acc;
             const int len = word_bits<FOUR>(bb, k0 + lane, lut, acc);
             const int incl = warp_incl_sum(len, lane);
             emit(st0, pos + static_cast<uint32_t>(incl - len), acc, len);
+            if (a.marks) {
+                const int c = (k0 + lane) * (FOUR ? 8 : 4);
+                if (c > 0 && c < blen && c % q == 0)
+                    a.marks[3 * b + c / q - 1] = static_cast<uint16_t>(pos + static_cast<uint32_t>(incl - len));
+            }
             pos += static_cast<uint32_t>(__shfl_sync(0xffffffffu, incl, 31));
         }
+        // quarters that start past the short bucket's end: the end
+        if (a.marks && lane < 3 && (lane + 1) * q >= blen) a.marks[3 * b + lane] = static_cast<uint16_t>(pos);
         __syncwarp();
         const int nw = static_cast<int>((pos + 31) >> 5);
         uint32_t* dst = a.words + offs[lb];
@@ -537,6 +553,7 @@ struct DecodeArgs {
     int s;
     int* status;
     uint32_t stage_cap;   // stream words a CTA stages in shared memory
+    const uint16_t* marks;   // quarter marks of stream 0 (segmented decode), else null
 };
 
 // Lookahead bits of the multi-codeword table: 11 for 4-bit codes, 12 for
@@ -669,9 +686,12 @@ struct CodeWriter {
 
 // One thread per bucket: its stream is walked with a 64-bit window (whi:wlo,
 // `have` valid bits from the top, the next word waiting in `pre`).
-template <bool FOUR>
+// SEG: each thread decodes one quarter of a bucket, from the bucket's quarter
+// mark (qsgd_elias_decode_quarters); a CTA then covers 64 buckets.
+template <bool FOUR, bool SEG>
 __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     extern __shared__ uint32_t s_words[];   // a.stage_cap words
+    constexpr int S = SEG ? 4 : 1;          // tasks per bucket
     constexpr int KMAX = FOUR ? 8 : 4;
     constexpr int W = win_bits<FOUR>();
     __shared__ __align__(16) uint64_t multi[1 << W];
@@ -704,10 +724,17 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     __syncthreads();
     const int stream = blockIdx.y;
     const uint32_t* offsets = a.offsets.p[stream];
-    const int64_t bb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    constexpr int kBucketsPerCta = kThreads / S;
+    const int64_t bb = static_cast<int64_t>(blockIdx.x) * kBucketsPerCta + threadIdx.x / S;
     uint32_t key = 255u;
     if (bb < a.nbuckets) {
-        const uint32_t nw = offsets[bb + 1] - offsets[bb];
+        uint32_t nw = offsets[bb + 1] - offsets[bb];
+        if (SEG) {
+            const int k = threadIdx.x % S;
+            const uint32_t sb = k ? a.marks[3 * bb + k - 1] : 32u;
+            const uint32_t eb = k < 3 ? a.marks[3 * bb + k] : 32u * nw;
+            nw = eb > sb ? (eb - sb + 31u) / 32u : 0u;
+        }
         key = nw < 255u ? nw : 255u;
     }
     const uint32_t pos = atomicAdd(s_hist + key, 1u);
@@ -728,8 +755,8 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     // walks below read from there.  Every word of that range lies inside the
     // range of one of the CTA's buckets, whatever the offsets: the copy reads
     // nothing a bucket would not.
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * blockDim.x;
-    const int64_t cnt = a.nbuckets - b0 < kThreads ? a.nbuckets - b0 : kThreads;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kBucketsPerCta;
+    const int64_t cnt = a.nbuckets - b0 < kBucketsPerCta ? a.nbuckets - b0 : kBucketsPerCta;
     const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
     const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
     const uint32_t* gwords = a.words.p[stream];
@@ -742,10 +769,17 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
             if (i + j * kThreads < nst) s_words[i + j * kThreads] = v[j];
     }
     __syncthreads();
-    const int64_t b = b0 + s_order[threadIdx.x];
+    const int task = s_order[threadIdx.x];
+    const int64_t b = b0 + task / S;
     if (b >= a.nbuckets) return;
-    const int64_t lo = b * a.d;
-    const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
+    const int kq = task % S;                    // the quarter (SEG), else 0
+    const int64_t blo = b * a.d;
+    const int blen = static_cast<int>(a.n - blo < a.d ? a.n - blo : static_cast<int64_t>(a.d));
+    const int q = a.d / S;
+    const int c0 = kq * q;                      // first coordinate of the task
+    if (c0 >= blen && kq > 0) return;           // a quarter past a short bucket's end
+    const int64_t lo = blo + c0;
+    const int len = min(blen - c0, q);
     const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
     // a bucket wholly inside the staged words reads shared memory (through a
     // generic pointer), any other bucket global memory
@@ -754,9 +788,12 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
     bool bad = avail == 0;
     auto word = [&](int64_t i) { return i < avail ? src[i] : 0u; };
-    a.norms.p[stream][b] = __uint_as_float(word(0));
-    uint32_t whi = word(1), wlo = word(2), pre = word(3);
-    int64_t next = 4;
+    if (kq == 0) a.norms.p[stream][b] = __uint_as_float(word(0));
+    // the task's first bit (after the norm, or its quarter mark)
+    const uint32_t sb = kq ? a.marks[3 * b + kq - 1] : 32u;
+    const int64_t w0 = sb >> 5;
+    uint32_t whi = word(w0), wlo = word(w0 + 1), pre = word(w0 + 2);
+    int64_t next = w0 + 3;
     int have = 64;
     CodeWriter<FOUR> wr;
     wr.out = reinterpret_cast<uint32_t*>(a.codes.p[stream] + (FOUR ? lo / 2 : lo));
@@ -810,6 +847,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
             long_code(code, l);
         }
     };
+    if (sb & 31u) consume(static_cast<int>(sb & 31u));
     int e = 0;
     while (len - e >= KMAX) {
         const uint64_t t = multi[whi >> (32 - W)];
@@ -834,7 +872,19 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     }
     wr.finish();
     // bits consumed: the words fetched (norm included, `pre` not) minus those still in the window
-    if (32 * (next - 1) - have > 32 * avail) bad = true;
+    const int64_t used = 32 * (next - 1) - have;
+    if (used > 32 * avail) bad = true;
+    // a quarter must end where the next one starts; the bucket's last
+    // quarter (of a short bucket: the last one holding coordinates) must end
+    // at every mark left, which the encoder sets to the bucket's end
+    if (SEG) {
+        if (c0 + q < blen) {
+            if (used != a.marks[3 * b + kq]) bad = true;
+        } else {
+            for (int k = kq; k < 3; ++k)
+                if (used != a.marks[3 * b + k]) bad = true;
+        }
+    }
     if (bad && a.status) *a.status = GC_ERR_CORRUPT;
 }
 
@@ -847,7 +897,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
 constexpr int kDecodeCtasPerSm = 4;
 constexpr int kMaxDevices = 64;
 
-template <bool FOUR>
+template <bool FOUR, bool SEG>
 int decode_stage_words(uint32_t* cap) {
     static std::atomic<uint32_t> cached[kMaxDevices];   // words + 1; 0 = not yet known
     int dev = 0;
@@ -863,11 +913,11 @@ int decode_stage_words(uint32_t* cap) {
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, k_elias_decode<FOUR>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, k_elias_decode<FOUR, SEG>) != cudaSuccess)
         return GC_ERR_CUDA;
     int64_t bytes = static_cast<int64_t>(per_sm) / kDecodeCtasPerSm - reserved - static_cast<int64_t>(fa.sharedSizeBytes);
     bytes = bytes > 0 ? bytes & ~static_cast<int64_t>(15) : 0;
-    if (cudaFuncSetAttribute(k_elias_decode<FOUR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_elias_decode<FOUR, SEG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes)) != cudaSuccess)
         return GC_ERR_CUDA;
     *cap = static_cast<uint32_t>(bytes / sizeof(uint32_t));
@@ -1340,9 +1390,13 @@ size_t qsgd_elias_workspace_bytes(int64_t n, int bucket) {
     return kTicketBytes + chunk_bytes(nchunks) + static_cast<size_t>(div_up(nb * 4, 16) * 16);
 }
 
-int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels,
-                      uint32_t* words, uint64_t capacity_words, uint32_t* offsets, void* workspace,
-                      size_t ws_bytes, gc_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int encode_dense(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels, uint32_t* words,
+                 uint64_t capacity_words, uint32_t* offsets, uint16_t* marks, void* workspace, size_t ws_bytes,
+                 gc_stream_t stream) {
     if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127) return GC_ERR_INVALID;
     if (!offsets || (n > 0 && (!codes || !norms || !words || !workspace))) return GC_ERR_INVALID;
     const uint64_t need = qsgd_elias_max_words(n, bucket, s_levels);
@@ -1367,7 +1421,7 @@ int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int b
     if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
     const int P = (four ? bucket / 2 : bucket) / 16;
     EncodeArgs ea{codes, norms, n, bucket, nb, ws, words, offsets,
-                  static_cast<int>(bucket_max_words(bucket, four)) + 2, P < 32 ? 32 / P : 1};
+                  static_cast<int>(bucket_max_words(bucket, four)) + 2, P < 32 ? 32 / P : 1, marks};
     const size_t smem = sizeof(uint32_t) *
                         (256 + kChunk + static_cast<size_t>(kWarpsPerBlock) * ea.slots * ea.stage_stride);
     if (four)
@@ -1375,6 +1429,26 @@ int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int b
     else
         k_elias_encode<false><<<grid, kThreads, smem, s>>>(ea);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels,
+                      uint32_t* words, uint64_t capacity_words, uint32_t* offsets, void* workspace,
+                      size_t ws_bytes, gc_stream_t stream) {
+    return encode_dense(codes, norms, n, bucket, s_levels, words, capacity_words, offsets, nullptr, workspace,
+                        ws_bytes, stream);
+}
+
+int qsgd_elias_encode_marked(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels,
+                             uint32_t* words, uint64_t capacity_words, uint32_t* offsets, uint16_t* marks,
+                             void* workspace, size_t ws_bytes, gc_stream_t stream) {
+    if (n > 0 && !marks) return GC_ERR_INVALID;
+    if (marks && !aligned16(marks)) return GC_ERR_ALIGN;
+    return encode_dense(codes, norms, n, bucket, s_levels, words, capacity_words, offsets, marks, workspace,
+                        ws_bytes, stream);
 }
 
 int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* const* offsets, int W,
@@ -1402,21 +1476,56 @@ int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* cons
     a.nbuckets = nb;
     a.s = s_levels;
     a.status = d_status;
+    a.marks = nullptr;
     const dim3 grid(static_cast<unsigned>(div_up(nb, kThreads)), static_cast<unsigned>(W));
     const bool four = s_levels <= 7;
-    const int rc = four ? decode_stage_words<true>(&a.stage_cap) : decode_stage_words<false>(&a.stage_cap);
+    const int rc = four ? decode_stage_words<true, false>(&a.stage_cap)
+                        : decode_stage_words<false, false>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     if (four)
-        k_elias_decode<true><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<true, false><<<grid, kThreads, dyn, s>>>(a);
     else
-        k_elias_decode<false><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<false, false><<<grid, kThreads, dyn, s>>>(a);
     return launch_status();
 }
 
 int qsgd_elias_decode(const uint32_t* words, const uint32_t* offsets, int64_t n, int bucket, int s_levels,
                       uint8_t* codes, float* norms, int* d_status, gc_stream_t stream) {
     return qsgd_elias_decode_batched(&words, &offsets, 1, n, bucket, s_levels, &codes, &norms, d_status, stream);
+}
+
+int qsgd_elias_decode_quarters(const uint32_t* words, const uint32_t* offsets, const uint16_t* marks, int64_t n,
+                               int bucket, int s_levels, uint8_t* codes, float* norms, int* d_status,
+                               gc_stream_t stream) {
+    if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127) return GC_ERR_INVALID;
+    if (n == 0) return GC_OK;
+    if (!words || !offsets || !marks || !codes || !norms) return GC_ERR_INVALID;
+    if (!aligned16(words) || !aligned16(offsets) || !aligned16(marks) || !aligned16(codes) || !aligned16(norms))
+        return GC_ERR_ALIGN;
+    if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return GC_ERR_ALIGN;
+    DecodeArgs a;
+    a.words.p[0] = words;
+    a.offsets.p[0] = offsets;
+    a.codes.p[0] = codes;
+    a.norms.p[0] = norms;
+    a.n = n;
+    a.d = bucket;
+    a.nbuckets = div_up(n, bucket);
+    a.s = s_levels;
+    a.status = d_status;
+    a.marks = marks;
+    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads / 4)), 1u);
+    const bool four = s_levels <= 7;
+    const int rc = four ? decode_stage_words<true, true>(&a.stage_cap) : decode_stage_words<false, true>(&a.stage_cap);
+    if (rc != GC_OK) return rc;
+    const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (four)
+        k_elias_decode<true, true><<<grid, kThreads, dyn, s>>>(a);
+    else
+        k_elias_decode<false, true><<<grid, kThreads, dyn, s>>>(a);
+    return launch_status();
 }
 
 uint64_t qsgd_elias_sparse_max_words(int64_t n, int bucket) {
@@ -1478,6 +1587,7 @@ int qsgd_elias_decode_sparse(const uint32_t* words, const uint32_t* offsets, int
     a.s = s_levels;
     a.status = d_status;
     a.stage_cap = 0;
+    a.marks = nullptr;
     const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads)), 1u);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (s_levels <= 7)

@@ -421,6 +421,45 @@ GC_API int qsgd_elias_decode_batched(const uint32_t *const *words,
                                      gc_stream_t stream);
 
 /*
+ * qsgd_elias_encode_marked -- qsgd_elias_encode that also writes each
+ * bucket's quarter marks: marks[3*b + k - 1], k = 1..3, is the bit (from the
+ * start of bucket b's first word, the norm's 32 bits included) at which the
+ * codeword of coordinate k*bucket/4 of that bucket begins; a quarter that
+ * starts at or past a short last bucket's end gets the bucket's total bits.
+ * The stream and offsets are those of qsgd_elias_encode, bit for bit.  The
+ * marks are side information not on the pages (48 bits per bucket, 0.09 bits
+ * per coordinate at bucket 512) that let a receiver decode a bucket's four
+ * quarters in parallel (qsgd_elias_decode_quarters).
+ *   marks   device uint16 [3 * ceil(n/bucket)], 16-byte aligned, written
+ *           (a bucket holds at most 32 + 2048 * 15 < 2^16 bits)
+ * Other arguments and errors as qsgd_elias_encode; GC_ERR_INVALID for a NULL
+ * marks with n > 0.
+ */
+GC_API int qsgd_elias_encode_marked(const uint8_t *codes, const float *norms, int64_t n,
+                                    int bucket, int s_levels, uint32_t *words,
+                                    uint64_t capacity_words, uint32_t *offsets,
+                                    uint16_t *marks, void *workspace, size_t ws_bytes,
+                                    gc_stream_t stream);
+
+/*
+ * qsgd_elias_decode_quarters -- qsgd_elias_decode of a stream written by
+ * qsgd_elias_encode_marked, with one decoding thread per quarter bucket
+ * (four times the parallelism of qsgd_elias_decode on one stream).  Same
+ * results as qsgd_elias_decode on (words, offsets).
+ *   marks      device uint16 [3 * ceil(n/bucket)], as the encoder wrote them
+ *   d_status   as in qsgd_elias_decode; also set to GC_ERR_CORRUPT when a
+ *              quarter's codewords do not end exactly at the next quarter's
+ *              mark, or the last quarter holding coordinates does not end
+ *              exactly at each mark after it (so that any marks other than
+ *              the encoder's are reported)
+ * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
+ */
+GC_API int qsgd_elias_decode_quarters(const uint32_t *words, const uint32_t *offsets,
+                                      const uint16_t *marks, int64_t n, int bucket,
+                                      int s_levels, uint8_t *codes, float *norms,
+                                      int *d_status, gc_stream_t stream);
+
+/*
  * qsgd_elias_encode_sparse -- QSGD's Elias coding in the sparse regimes
  * ("QSGD ..." summary page, Knowl 2 items 1 (s >= 2) and 1' (s = 1)): only
  * the coordinates whose level is not 0 are sent, each as Elias-omega of its

@@ -142,6 +142,17 @@ def test_elias_sizes_and_validation():
     assert _call(h, two, two, 2, 10_000, 512, 7, _ptrs(FAKE, MISALIGNED), two, None, None) == gc.GC_ERR_ALIGN
     assert _call(h, two, two, 2, 10_000, 500, 7, two, two, None, None) == gc.GC_ERR_INVALID
     assert _call(h, None, None, 2, 0, 512, 7, None, None, None, None) == gc.GC_OK
+    m = "qsgd_elias_encode_marked"
+    assert _call(m, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, None, FAKE, ws, None) == gc.GC_ERR_INVALID
+    assert _call(m, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, MISALIGNED, FAKE, ws, None) == gc.GC_ERR_ALIGN
+    assert _call(m, FAKE, FAKE, 10_000, 500, 7, FAKE, cap, FAKE, FAKE, FAKE, ws, None) == gc.GC_ERR_INVALID
+    assert _call(m, FAKE, FAKE, 10_000, 512, 7, FAKE, cap - 1, FAKE, FAKE, FAKE, ws, None) == gc.GC_ERR_CAPACITY
+    q = "qsgd_elias_decode_quarters"
+    assert _call(q, FAKE, FAKE, None, 10_000, 512, 7, FAKE, FAKE, None, None) == gc.GC_ERR_INVALID
+    assert _call(q, FAKE, FAKE, MISALIGNED, 10_000, 512, 7, FAKE, FAKE, None, None) == gc.GC_ERR_ALIGN
+    assert _call(q, FAKE, FAKE, FAKE, 10_000, 512, 0, FAKE, FAKE, None, None) == gc.GC_ERR_INVALID
+    assert _call(q, FAKE, FAKE, FAKE, 10_000, 512, 7, FAKE, FAKE, MISALIGNED + 1, None) == gc.GC_ERR_ALIGN
+    assert _call(q, None, None, None, 0, 512, 7, None, None, None, None) == gc.GC_OK
 
 
 def test_saps_validation():
