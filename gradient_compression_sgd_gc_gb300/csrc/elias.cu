@@ -686,12 +686,27 @@ struct CodeWriter {
 
 // One thread per bucket: its stream is walked with a 64-bit window (whi:wlo,
 // `have` valid bits from the top, the next word waiting in `pre`).
-// SEG: each thread decodes one quarter of a bucket, from the bucket's quarter
-// mark (qsgd_elias_decode_quarters); a CTA then covers 64 buckets.
-template <bool FOUR, bool SEG>
-__global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
+// S > 1: each thread decodes 1/S of a bucket (S = 2 or 4), from the
+// bucket's quarter marks (qsgd_elias_decode_quarters); a CTA then covers
+// 256 / S buckets.
+// Resident CTAs per SM the decoders size their shared staging for: one
+// stream of 61 M coordinates needs 3.4 CTAs per SM of the 152 at a bucket per
+// thread (five or six CTAs per SM for 4-bit codes measured no faster on four
+// streams); a quarter per thread stages a quarter of the words per CTA, so
+// six CTAs fit.
+template <bool FOUR, int S>
+constexpr int decode_ctas_per_sm() { return S > 1 ? 6 : 4; }
+
+// Parts per bucket in qsgd_elias_decode_quarters: 4-bit codes, a thread per
+// half bucket (the middle mark); 8-bit codes, whose streams are about twice
+// as long, a thread per quarter.
+constexpr int kPartsFour = 2, kPartsEight = 4;
+
+template <bool FOUR, int S>
+__global__ void __launch_bounds__(kThreads, (decode_ctas_per_sm<FOUR, S>())) k_elias_decode(DecodeArgs a) {
     extern __shared__ uint32_t s_words[];   // a.stage_cap words
-    constexpr int S = SEG ? 4 : 1;          // tasks per bucket
+    static_assert(S == 1 || S == 2 || S == 4, "a bucket splits at its quarter marks");
+    constexpr int QS = 4 / S;               // quarters per task
     constexpr int KMAX = FOUR ? 8 : 4;
     constexpr int W = win_bits<FOUR>();
     __shared__ __align__(16) uint64_t multi[1 << W];
@@ -703,11 +718,12 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
         // A window holding a level above s gets count 0, which sends it to
         // the one-codeword path (where that level is flagged): the main loop
         // then tests only the count.  Entries are (packed << 32) | meta, meta
-        // = (max level << 8) | (count << 4) | bits.
+        // = (max level << 8) | (count << 4) | bits; the shared copy drops the
+        // max level, so that the count is meta >> 4.
         for (int i = threadIdx.x; i < (1 << W) / 2; i += blockDim.x) {
             uint4 v = __ldg(src + i);
-            if (((v.x >> 8) & 127u) > smax) v.x &= ~0xF0u;
-            if (((v.z >> 8) & 127u) > smax) v.z &= ~0xF0u;
+            v.x = ((v.x >> 8) & 127u) > smax ? (v.x & 15u) : (v.x & 255u);
+            v.z = ((v.z >> 8) & 127u) > smax ? (v.z & 15u) : (v.z & 255u);
             dst[i] = v;
         }
     }
@@ -729,10 +745,10 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     uint32_t key = 255u;
     if (bb < a.nbuckets) {
         uint32_t nw = offsets[bb + 1] - offsets[bb];
-        if (SEG) {
+        if (S > 1) {
             const int k = threadIdx.x % S;
-            const uint32_t sb = k ? a.marks[3 * bb + k - 1] : 32u;
-            const uint32_t eb = k < 3 ? a.marks[3 * bb + k] : 32u * nw;
+            const uint32_t sb = k ? a.marks[3 * bb + k * QS - 1] : 32u;
+            const uint32_t eb = k < S - 1 ? a.marks[3 * bb + (k + 1) * QS - 1] : 32u * nw;
             nw = eb > sb ? (eb - sb + 31u) / 32u : 0u;
         }
         key = nw < 255u ? nw : 255u;
@@ -772,12 +788,12 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     const int task = s_order[threadIdx.x];
     const int64_t b = b0 + task / S;
     if (b >= a.nbuckets) return;
-    const int kq = task % S;                    // the quarter (SEG), else 0
+    const int kq = task % S;                    // the task's part of the bucket
     const int64_t blo = b * a.d;
     const int blen = static_cast<int>(a.n - blo < a.d ? a.n - blo : static_cast<int64_t>(a.d));
     const int q = a.d / S;
     const int c0 = kq * q;                      // first coordinate of the task
-    if (c0 >= blen && kq > 0) return;           // a quarter past a short bucket's end
+    if (c0 >= blen && kq > 0) return;           // a part past a short bucket's end
     const int64_t lo = blo + c0;
     const int len = min(blen - c0, q);
     const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
@@ -790,17 +806,19 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     auto word = [&](int64_t i) { return i < avail ? src[i] : 0u; };
     if (kq == 0) a.norms.p[stream][b] = __uint_as_float(word(0));
     // the task's first bit (after the norm, or its quarter mark)
-    const uint32_t sb = kq ? a.marks[3 * b + kq - 1] : 32u;
+    const uint32_t sb = kq ? a.marks[3 * b + kq * QS - 1] : 32u;
     const int64_t w0 = sb >> 5;
     uint32_t whi = word(w0), wlo = word(w0 + 1), pre = word(w0 + 2);
     int64_t next = w0 + 3;
     int have = 64;
     CodeWriter<FOUR> wr;
     wr.out = reinterpret_cast<uint32_t*>(a.codes.p[stream] + (FOUR ? lo / 2 : lo));
-    auto consume = [&](int l) {
+    auto shift_out = [&](int l) {
         whi = __funnelshift_l(wlo, whi, l);
         wlo <<= l;
         have -= l;
+    };
+    auto refill = [&]() {
         if (have <= 32) {
             whi |= __funnelshift_rc(pre, 0u, have);
             wlo |= pre << (32 - have);
@@ -808,6 +826,10 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
             pre = word(next);
             ++next;
         }
+    };
+    auto consume = [&](int l) {
+        shift_out(l);
+        refill();
     };
     // A codeword longer than 8 bits in a valid stream is omega(N) for N of
     // k = 5..8 binary digits: the groups "10" and binary(k - 1) = "1xx", then
@@ -849,9 +871,9 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     };
     if (sb & 31u) consume(static_cast<int>(sb & 31u));
     int e = 0;
-    while (len - e >= KMAX) {
+    auto table_step = [&]() {
         const uint64_t t = multi[whi >> (32 - W)];
-        int k = static_cast<int>((t >> 4) & 15u);
+        int k = static_cast<int>(static_cast<uint32_t>(t) >> 4);
         int l = static_cast<int>(t & 15u);
         uint32_t packed = static_cast<uint32_t>(t >> 32);
         if (k == 0) {
@@ -859,9 +881,21 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
             one_code(packed, l);
             k = 1;
         }
-        consume(l);
+        shift_out(l);
         wr.put(packed, k);
         e += k;
+    };
+    // After a refill the window holds more than 32 bits and a step takes at
+    // most 15 (the longest codeword with its sign), so two steps share one
+    // refill: the second still sees at least 18 valid bits.
+    while (len - e >= 2 * KMAX) {
+        table_step();
+        table_step();
+        refill();
+    }
+    while (len - e >= KMAX) {
+        table_step();
+        refill();
     }
     for (; e < len; ++e) {
         uint32_t code;
@@ -874,30 +908,27 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode(DecodeArgs a) {
     // bits consumed: the words fetched (norm included, `pre` not) minus those still in the window
     const int64_t used = 32 * (next - 1) - have;
     if (used > 32 * avail) bad = true;
-    // a quarter must end where the next one starts; the bucket's last
-    // quarter (of a short bucket: the last one holding coordinates) must end
-    // at every mark left, which the encoder sets to the bucket's end
-    if (SEG) {
+    // a part must end where the next one starts; the bucket's last part (of
+    // a short bucket: the last one holding coordinates) must end at the start
+    // mark of every part after it, which the encoder sets to the bucket's end
+    if (S > 1) {
         if (c0 + q < blen) {
-            if (used != a.marks[3 * b + kq]) bad = true;
+            if (used != a.marks[3 * b + (kq + 1) * QS - 1]) bad = true;
         } else {
-            for (int k = kq; k < 3; ++k)
-                if (used != a.marks[3 * b + k]) bad = true;
+            for (int k = kq + 1; k < S; ++k)
+                if (used != a.marks[3 * b + k * QS - 1]) bad = true;
         }
     }
     if (bad && a.status) *a.status = GC_ERR_CORRUPT;
 }
 
 // Stream words one decoding CTA stages: the shared memory left, after the
-// kernel's static tables and the per-CTA reservation, when four CTAs share an
-// SM (one stream of 61 M coordinates needs 3.4 CTAs per SM of the 152; five
-// or six CTAs per SM for 4-bit codes measured no faster on four streams).
-// Computed once per device, which also raises the kernel's dynamic
-// shared-memory limit there.
-constexpr int kDecodeCtasPerSm = 4;
+// kernel's static tables and the per-CTA reservation, when
+// decode_ctas_per_sm CTAs share an SM.  Computed once per device, which also
+// raises the kernel's dynamic shared-memory limit there.
 constexpr int kMaxDevices = 64;
 
-template <bool FOUR, bool SEG>
+template <bool FOUR, int S>
 int decode_stage_words(uint32_t* cap) {
     static std::atomic<uint32_t> cached[kMaxDevices];   // words + 1; 0 = not yet known
     int dev = 0;
@@ -913,11 +944,12 @@ int decode_stage_words(uint32_t* cap) {
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, k_elias_decode<FOUR, SEG>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, k_elias_decode<FOUR, S>) != cudaSuccess)
         return GC_ERR_CUDA;
-    int64_t bytes = static_cast<int64_t>(per_sm) / kDecodeCtasPerSm - reserved - static_cast<int64_t>(fa.sharedSizeBytes);
+    int64_t bytes = static_cast<int64_t>(per_sm) / decode_ctas_per_sm<FOUR, S>() - reserved -
+                    static_cast<int64_t>(fa.sharedSizeBytes);
     bytes = bytes > 0 ? bytes & ~static_cast<int64_t>(15) : 0;
-    if (cudaFuncSetAttribute(k_elias_decode<FOUR, SEG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_elias_decode<FOUR, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes)) != cudaSuccess)
         return GC_ERR_CUDA;
     *cap = static_cast<uint32_t>(bytes / sizeof(uint32_t));
@@ -1479,14 +1511,13 @@ int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* cons
     a.marks = nullptr;
     const dim3 grid(static_cast<unsigned>(div_up(nb, kThreads)), static_cast<unsigned>(W));
     const bool four = s_levels <= 7;
-    const int rc = four ? decode_stage_words<true, false>(&a.stage_cap)
-                        : decode_stage_words<false, false>(&a.stage_cap);
+    const int rc = four ? decode_stage_words<true, 1>(&a.stage_cap) : decode_stage_words<false, 1>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     if (four)
-        k_elias_decode<true, false><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<true, 1><<<grid, kThreads, dyn, s>>>(a);
     else
-        k_elias_decode<false, false><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<false, 1><<<grid, kThreads, dyn, s>>>(a);
     return launch_status();
 }
 
@@ -1515,16 +1546,18 @@ int qsgd_elias_decode_quarters(const uint32_t* words, const uint32_t* offsets, c
     a.s = s_levels;
     a.status = d_status;
     a.marks = marks;
-    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads / 4)), 1u);
     const bool four = s_levels <= 7;
-    const int rc = four ? decode_stage_words<true, true>(&a.stage_cap) : decode_stage_words<false, true>(&a.stage_cap);
+    const int S = four ? kPartsFour : kPartsEight;
+    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads / S)), 1u);
+    const int rc = four ? decode_stage_words<true, kPartsFour>(&a.stage_cap)
+                        : decode_stage_words<false, kPartsEight>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (four)
-        k_elias_decode<true, true><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<true, kPartsFour><<<grid, kThreads, dyn, s>>>(a);
     else
-        k_elias_decode<false, true><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<false, kPartsEight><<<grid, kThreads, dyn, s>>>(a);
     return launch_status();
 }
 

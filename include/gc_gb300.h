@@ -443,15 +443,18 @@ GC_API int qsgd_elias_encode_marked(const uint8_t *codes, const float *norms, in
 
 /*
  * qsgd_elias_decode_quarters -- qsgd_elias_decode of a stream written by
- * qsgd_elias_encode_marked, with one decoding thread per quarter bucket
- * (four times the parallelism of qsgd_elias_decode on one stream).  Same
- * results as qsgd_elias_decode on (words, offsets).
+ * qsgd_elias_encode_marked, with more decoding threads per bucket: for 8-bit
+ * codes (s_levels > 7) one per quarter bucket, starting at the quarter
+ * marks; for 4-bit codes, whose streams are about half as long, one per half
+ * bucket, starting at the middle mark (marks[3*b + 1]).  Same results as
+ * qsgd_elias_decode on (words, offsets).
  *   marks      device uint16 [3 * ceil(n/bucket)], as the encoder wrote them
  *   d_status   as in qsgd_elias_decode; also set to GC_ERR_CORRUPT when a
- *              quarter's codewords do not end exactly at the next quarter's
- *              mark, or the last quarter holding coordinates does not end
- *              exactly at each mark after it (so that any marks other than
- *              the encoder's are reported)
+ *              part's codewords do not end exactly at the mark the next part
+ *              starts from, or the last part holding coordinates of a short
+ *              bucket does not end exactly at the marks of the parts after
+ *              it (so that any mark the decoder starts from, other than the
+ *              encoder's, is reported)
  * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA.
  */
 GC_API int qsgd_elias_decode_quarters(const uint32_t *words, const uint32_t *offsets,

@@ -149,6 +149,23 @@ def test_extreme_buckets(s):
     np.testing.assert_array_equal(dc, rc)
 
 
+def test_corrupt_middle_mark_of_four_bit_streams():
+    """4-bit codes decode in halves from the middle mark (marks[3b + 1]): a
+    middle mark one bit off, or a short bucket's middle mark not at its end,
+    is reported."""
+    cfg, n, bucket, s = wl.QSGD_S7, 512 * 8 + 200, 512, 7
+    norms, codes = _oracle_codes(cfg, n, bucket, s)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, bucket, s)
+    ref_m = oracle.qsgd_elias_quarter_marks(codes, n, bucket, s)
+    words, offs = _dev_u32(ref_w), _dev_u32(ref_off)
+    assert _decode_quarters(words, offs, _dev_u16(ref_m), n, bucket, s)[2] == 0
+    for i in (1, 3 * 5 + 1, 3 * 8 + 1):           # buckets 0 and 5, and the short last bucket (200)
+        for delta in (1, -1):
+            m = ref_m.copy()
+            m[i] = np.uint16(int(m[i]) + delta)
+            assert _decode_quarters(words, offs, _dev_u16(m), n, bucket, s)[2] == gc.GC_ERR_CORRUPT
+
+
 def test_corrupt_marks_and_streams_are_reported():
     cfg, n, bucket, s = wl.QSGD_S127, 512 * 8 + 100, 512, 127
     norms, codes = _oracle_codes(cfg, n, bucket, s)
