@@ -58,6 +58,7 @@ def _load():
         sig = {
             "orc_splitmix64": (u64, [u64]),
             "orc_uniform": (f64, [u64]),
+            "orc_qsgd_dither": (f64, [u64, u64]),
             "orc_round_seed": (u64, [u64, u64]),
             "orc_2bit_quantize": (None, [vp, i32, vp, vp, i64, f32]),
             "orc_2bit_dequant_sum_update": (None, [vp, i32, i64, f32, i32, f64, f64, vp, vp, vp]),
@@ -116,6 +117,13 @@ def splitmix64(x: int) -> int:
 
 def uniform(key: int) -> float:
     return float(_load().orc_uniform(key & 0xFFFFFFFFFFFFFFFF))
+
+
+def qsgd_dither(seed: int, worker: int, i: int) -> float:
+    """QSGD's dither u of global element index i for (seed, worker): one
+    SplitMix64 output per pair of elements (see orc_qsgd_dither)."""
+    seed_w = (seed ^ ((worker & 0xFFFFFFFF) << 48)) & 0xFFFFFFFFFFFFFFFF
+    return float(_load().orc_qsgd_dither(seed_w, i & 0xFFFFFFFFFFFFFFFF))
 
 
 def round_seed(base: int, t: int) -> int:

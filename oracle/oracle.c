@@ -35,10 +35,10 @@
  *          random mask with a shared seed, single-peer gossip matrix).
  *   [EA]   IMerge design notes (blog), "Interleaved Communication Scheduling",
  *          EASGD local and global update equations.
- *   The counter-based hash (splitmix64 of seed XOR index, top 24 bits scaled
- *   to [0,1)) is not on the pages; it is the published SplitMix64 finaliser
- *   (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
- *   OOPSLA 2014).
+ *   The counter-based hash (splitmix64 of seed XOR index, 24-bit fields
+ *   scaled to [0,1)) is not on the pages; it is the published SplitMix64
+ *   finaliser (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ *   generators", OOPSLA 2014).
  */
 #include <math.h>
 #include <stdint.h>
@@ -62,6 +62,20 @@ uint64_t orc_splitmix64(uint64_t x)
 double orc_uniform(uint64_t key)
 {
     return (double)(orc_splitmix64(key) >> 40) / 16777216.0;
+}
+
+/*
+ * QSGD's dither for global element index i of the worker whose seed is
+ * seed_w: one SplitMix64 output serves a pair of elements,
+ *     z = splitmix64(seed_w ^ floor(i / 2)),
+ * the even element 2j taking bits 40..63 of z and the odd element 2j + 1
+ * bits 8..31 (two disjoint 24-bit fields), each scaled by 2^-24.
+ */
+double orc_qsgd_dither(uint64_t seed_w, uint64_t i)
+{
+    uint64_t z = orc_splitmix64(seed_w ^ (i >> 1));
+    uint64_t field = (i & 1u) ? (z >> 8) & 0xFFFFFFu : z >> 40;
+    return (double)field / 16777216.0;
 }
 
 /* Round seed for SAPS round t: seed_t = splitmix64(base + t). */
@@ -294,7 +308,7 @@ float orc_l2norm_fp32(const float *v, int64_t len)
  * [QS] Knowl 1 and Knowl 8: per bucket of d coordinates (the last one may be
  * shorter), Q_s(v_i) = ||v|| * sgn(v_i) * xi_i with xi_i in {l/s, (l+1)/s},
  * sgn(0) = +1 and Q_s(0) = 0.  The random choice is made as
- *     level = floor(|v_i| / ||v|| * s + u),   u = uniform(seed_w ^ i)
+ *     level = floor(|v_i| / ||v|| * s + u),   u = qsgd_dither(seed_w, i)
  * with the worker folded into the seed as seed_w = seed ^ (worker << 48) and
  * i the global element index (i0 + local index, so that a bucket-aligned
  * slice of a long vector can be quantised on its own).  fp32 operation order
@@ -360,7 +374,7 @@ static void qsgd_quantize_impl(const float *v, int64_t n, int64_t d, int s,
             uint32_t level = 0u;
             if (norm > 0.0f) {
                 float a = fabsf(v[i]) * S;
-                float u = (float)orc_uniform(seed_w ^ (uint64_t)(i0 + i));
+                float u = (float)orc_qsgd_dither(seed_w, (uint64_t)(i0 + i));
                 float x = a + u;
                 if (x != x)
                     level = 0u;
@@ -406,7 +420,7 @@ static void qsgd_scaled_values_impl(const float *v, int64_t n, int64_t d, int s,
         for (int64_t i = lo; i < hi; ++i) {
             if (norm > 0.0f) {
                 float a = fabsf(v[i]) * S;
-                float u = (float)orc_uniform(seed_w ^ (uint64_t)(i0 + i));
+                float u = (float)orc_qsgd_dither(seed_w, (uint64_t)(i0 + i));
                 x_out[i] = a + u;
             } else {
                 x_out[i] = 0.0f;

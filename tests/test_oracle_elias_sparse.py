@@ -87,7 +87,11 @@ def test_sparse_roundtrip_and_lengths(s, d, n):
     table = _codewords()
 
     def omega_len(g):
-        return len(table[1 << (int(g).bit_length() - 1)])
+        # from the table where it reaches; above it, omega(N) is the code of
+        # bitlength(N) - 1 followed by N's binary digits (Elias 1975)
+        bl = int(g).bit_length()
+        key = 1 << (bl - 1)
+        return len(table[key]) if key in table else bl + omega_len(bl - 1)
 
     _, lv = _unpack(codes, n, s)
     for b in range((n + d - 1) // d):

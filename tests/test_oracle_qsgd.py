@@ -38,6 +38,47 @@ def test_uniform_grid_mean_and_flatness():
     assert chi2 < 255 + 5 * math.sqrt(2 * 255)
 
 
+def test_qsgd_dither_fields_of_published_splitmix64_outputs():
+    """The pair (2j, 2j + 1) shares z = splitmix64(seed_w ^ j): bits 40..63
+    for the even element, bits 8..31 for the odd one.  SplitMix64 seeded with 0
+    gives 0xE220A8397B1DCDAF and then 0x6E789E6AA1B965F4 (Steele, Lea and
+    Flood 2014); as counters those are splitmix64(0) and
+    splitmix64(0x9E3779B97F4A7C15)."""
+    g = 0x9E3779B97F4A7C15
+    assert oracle.qsgd_dither(0, 0, 0) == 0xE220A8 / 2 ** 24
+    assert oracle.qsgd_dither(0, 0, 1) == 0x7B1DCD / 2 ** 24
+    assert oracle.qsgd_dither(g, 0, 0) == 0x6E789E / 2 ** 24
+    assert oracle.qsgd_dither(g, 0, 1) == 0xA1B965 / 2 ** 24
+    # index 2j and 2j + 1 use the counter seed_w ^ j: j = 1 with seed_w = g ^ 1
+    assert oracle.qsgd_dither(g ^ 1, 0, 2) == 0x6E789E / 2 ** 24
+    assert oracle.qsgd_dither(g ^ 1, 0, 3) == 0xA1B965 / 2 ** 24
+    # the worker is folded in at bit 48, indices above 2^32 keep their high bits
+    w, big = 3, (5 << 33) | 6
+    assert oracle.qsgd_dither(g ^ (w << 48) ^ (big >> 1), w, big) == 0x6E789E / 2 ** 24
+    assert oracle.qsgd_dither(g ^ (big >> 1), 0, big + 1) == 0xA1B965 / 2 ** 24
+
+
+def test_qsgd_dither_fields_uniform_and_independent():
+    """Both fields are uniform on the 2^-24 grid, and the two fields of one
+    output, and neighbouring pairs, are uncorrelated."""
+    n = 1 << 16
+    u = np.array([oracle.qsgd_dither(0x5EED, 2, i) for i in range(2 * n)])
+    assert np.all(u >= 0.0) and np.all(u < 1.0)
+    assert np.all(u * 2 ** 24 == np.floor(u * 2 ** 24))
+    for part in (u[0::2], u[1::2]):
+        assert abs(part.mean() - 0.5) < 5 * math.sqrt(1 / 12 / n)
+        hist = np.bincount((part * 256).astype(int), minlength=256)
+        chi2 = float(((hist - n / 256) ** 2 / (n / 256)).sum())
+        assert chi2 < 255 + 5 * math.sqrt(2 * 255)
+    for a, b in ((u[0::2], u[1::2]), (u[1:-1:2], u[2::2]), (u[:-2], u[2:])):
+        r = np.corrcoef(a, b)[0, 1]
+        assert abs(r) < 5 / math.sqrt(a.size)
+    # the joint distribution of the pair's fields: 16 x 16 cells
+    hist2 = np.bincount((u[0::2] * 16).astype(int) * 16 + (u[1::2] * 16).astype(int), minlength=256)
+    chi2 = float(((hist2 - n / 256) ** 2 / (n / 256)).sum())
+    assert chi2 < 255 + 5 * math.sqrt(2 * 255)
+
+
 # ---------------------------------------------------------------- norm
 
 def _exact_rounding_check(v: np.ndarray, r: np.float32) -> None:
@@ -339,8 +380,9 @@ def test_scaled_values_single_nonzero_bucket_closed_form():
     v = np.zeros(d, np.float32)
     v[100] = np.float32(-0.3)
     for maxnorm in (False, True):
-        x = oracle.qsgd_scaled_values(v, d, s, 9, 0, maxnorm=maxnorm)
-        u = np.array([oracle.uniform(9 ^ i) for i in range(d)], np.float32)
-        zero = np.arange(d) != 100
-        np.testing.assert_array_equal(x[zero], u[zero])
-        assert abs(float(x[100]) - (s + float(u[100]))) <= 2 * np.spacing(np.float32(s + 1))
+        for worker, i0 in ((0, 0), (3, 7 * d), (1, (1 << 33) + d)):
+            x = oracle.qsgd_scaled_values(v, d, s, 9, worker, i0=i0, maxnorm=maxnorm)
+            u = np.array([oracle.qsgd_dither(9, worker, i0 + i) for i in range(d)], np.float32)
+            zero = np.arange(d) != 100
+            np.testing.assert_array_equal(x[zero], u[zero])
+            assert abs(float(x[100]) - (s + float(u[100]))) <= 2 * np.spacing(np.float32(s + 1))
