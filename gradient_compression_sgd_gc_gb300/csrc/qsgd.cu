@@ -138,7 +138,7 @@ struct QArgs {
     uint8_t* codes;
 };
 
-// level = min(floor(|v| * S + u), s) in fp32, u = top24(hash) * 2^-24.
+// level = min(floor(|v| * S + u), s) in fp32, u = (24-bit dither field) * 2^-24.
 // u is an exact multiple of 2^-24, so one fma rounds |v|*S + u exactly as the
 // separate add does.  The floor runs on the conversion pipe (round toward
 // -inf to an unsigned integer; +inf saturates, so min() gives s); a NaN y
@@ -150,33 +150,47 @@ __device__ __forceinline__ uint32_t qlevel(float x, float S, uint32_t s, uint32_
     return min(__float2uint_rd(y), s);
 }
 
-// splitmix64_top24 of the four keys kbase ^ k (k = 0..3), sharing what the
-// four have in common: they differ only in their low two bits, so
-// x_k = x0 + j_k with x0 = kbase & ~3 and j_k = (kbase & 3) ^ k.  While
-// z0 = x0 + golden has no carry out of its low word for j_k <= 3, the four z
-// have the same high word, and so does the high word of z ^ (z >> 30); its
-// share of the first product is computed once.  A group whose low word would
-// carry takes the plain function (one group in about 2^30).
-__device__ __forceinline__ void hash4_top24(uint64_t kbase, uint32_t (&t)[4]) {
+// The dither fields of one SplitMix64 output: z = splitmix64(key); the even
+// element of the pair takes bits 40..63 of z, the odd one bits 8..31.
+__device__ __forceinline__ void splitmix64_fields(uint64_t key, uint32_t& even, uint32_t& odd) {
+    const uint64_t z = splitmix64(key);
+    even = static_cast<uint32_t>(z >> 40);
+    odd = (static_cast<uint32_t>(z) >> 8);
+}
+
+// Dither fields of four consecutive elements e .. e + 3 (e a multiple of 4):
+// the pairs use the keys kbase = seed_w ^ (e / 2) and kbase ^ 1.  The two
+// keys differ only in their low bit, so x_k = x0 + j_k with x0 = kbase & ~1
+// and j_k = (kbase & 1) ^ k.  While z0 = x0 + golden has no carry out of its
+// low word for j_k <= 1, both z have the same high word, and so does the
+// high word of z ^ (z >> 30); its share of the first product is computed
+// once.  A pair whose low word would carry takes the plain function (one in
+// about 2^31).  Of the last product r = q * C2 the even field needs bits
+// 40..63 (the final z ^ (z >> 31) leaves them as they are) and the odd field
+// bits 8..31 of r ^ (r >> 31).
+__device__ __forceinline__ void dither4_top24(uint64_t kbase, uint32_t (&t)[4]) {
     constexpr uint64_t kC1 = 0xBF58476D1CE4E5B9ull;
     constexpr uint64_t kC2 = 0x94D049BB133111EBull;
-    const uint64_t z0 = (kbase & ~3ull) + 0x9E3779B97F4A7C15ull;
+    const uint64_t z0 = (kbase & ~1ull) + 0x9E3779B97F4A7C15ull;
     const uint32_t z0l = static_cast<uint32_t>(z0), zh = static_cast<uint32_t>(z0 >> 32);
-    const uint32_t jb = static_cast<uint32_t>(kbase) & 3u;
-    if (z0l > 0xFFFFFFFCu) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) t[k] = splitmix64_top24(kbase ^ static_cast<uint64_t>(k));
+    const uint32_t jb = static_cast<uint32_t>(kbase) & 1u;
+    if (z0l == 0xFFFFFFFFu) {
+        splitmix64_fields(kbase, t[0], t[1]);
+        splitmix64_fields(kbase ^ 1ull, t[2], t[3]);
         return;
     }
     const uint32_t yh = zh ^ (zh >> 30);                               // high word of z ^ (z >> 30)
     const uint64_t yh_part = static_cast<uint64_t>(yh * static_cast<uint32_t>(kC1)) << 32;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 2; ++k) {
         const uint32_t zl = z0l + (jb ^ static_cast<uint32_t>(k));
         const uint32_t yl = zl ^ __funnelshift_r(zl, zh, 30);              // low word of z ^ (z >> 30)
         const uint64_t p = static_cast<uint64_t>(yl) * kC1 + yh_part;      // (yh:yl) * C1 mod 2^64
         const uint64_t q = p ^ (p >> 27);
-        t[k] = static_cast<uint32_t>((q * kC2) >> 40);
+        const uint64_t r = q * kC2;
+        const uint32_t rl = static_cast<uint32_t>(r), rh = static_cast<uint32_t>(r >> 32);
+        t[2 * k] = rh >> 8;
+        t[2 * k + 1] = (rl ^ __funnelshift_r(rl, rh, 31)) >> 8;
     }
 }
 
@@ -320,13 +334,14 @@ __device__ __forceinline__ void quantize_bucket_body(const QArgs& a, int64_t b, 
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
         const int64_t e = b0 + 128 * j + 4 * lane;
-        // e is a multiple of 4, so seed_w ^ (e + k) == (seed_w ^ e) ^ k
-        const uint64_t kbase = a.seed_w ^ static_cast<uint64_t>(e);
+        // e is a multiple of 4: elements e, e + 1 share the key seed_w ^ (e / 2),
+        // elements e + 2, e + 3 the key seed_w ^ (e / 2 + 1) == (seed_w ^ (e / 2)) ^ 1
+        const uint64_t kbase = a.seed_w ^ static_cast<uint64_t>(e >> 1);
         const float xs[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
         uint32_t lv[4] = {0u, 0u, 0u, 0u};
         if (!zero) {
             uint32_t t[4];
-            hash4_top24(kbase, t);
+            dither4_top24(kbase, t);
 #pragma unroll
             for (int k = 0; k < 4; ++k) lv[k] = qlevel(xs[k], S, s_u, t[k]);
         }

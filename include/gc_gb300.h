@@ -275,9 +275,12 @@ GC_API int gc_compensated_sum_update(const void *const *grads, gc_dtype dtype,
  *   norms[b] = the l2 norm of the bucket, rounded to nearest fp32
  *   S = s_levels / norms[b]                       (fp32 division)
  *   per element: a = |v| * S, x = a + u, level = min(floor(x), s_levels)
- *   with u = (splitmix64(seed_w ^ i) >> 40) * 2^-24, seed_w = seed ^
- *   ((uint64)worker << 48), i the global element index; a bucket whose norm
- *   is 0 has level 0 everywhere.  Sign bit = (v < 0), so sgn(0) = +1.
+ *   with u = f * 2^-24, f the 24-bit dither field of element i: with
+ *   z = splitmix64(seed_w ^ floor(i/2)), bits 40..63 of z for even i and
+ *   bits 8..31 for odd i (one SplitMix64 output per pair of elements),
+ *   seed_w = seed ^ ((uint64)worker << 48), i the global element index; a
+ *   bucket whose norm is 0 has level 0 everywhere.  Sign bit = (v < 0), so
+ *   sgn(0) = +1.
  * Codes are sign-magnitude:
  *   1 <= s_levels <= 7  : 4-bit codes (sign in bit 3), two per byte, element
  *                         2j in the HIGH nibble of byte j; codes has
