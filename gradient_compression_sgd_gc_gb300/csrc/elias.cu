@@ -689,13 +689,20 @@ struct CodeWriter {
 // S > 1: each thread decodes 1/S of a bucket (S = 2 or 4), from the
 // bucket's quarter marks (qsgd_elias_decode_quarters); a CTA then covers
 // 256 / S buckets.
-// Resident CTAs per SM the decoders size their shared staging for: one
-// stream of 61 M coordinates needs 3.4 CTAs per SM of the 152 at a bucket per
-// thread (five or six CTAs per SM for 4-bit codes measured no faster on four
-// streams); a quarter per thread stages a quarter of the words per CTA, so
-// six CTAs fit.
+// Threads per decoding CTA and the resident CTAs per SM its shared staging
+// is sized for.  Each CTA copies the codeword tables (19 KB for 4-bit codes,
+// 35 KB for 8-bit codes) to shared memory, so fewer, larger CTAs leave more
+// of it for staging stream words.  4-bit codes: 256 threads, 4 CTAs per SM a
+// bucket per thread (one stream of 61 M coordinates needs 3.4 of them per SM
+// of the 152), 6 with a part of a bucket per thread; 512- or 1024-thread
+// CTAs measured no faster.  8-bit codes: one 1024-thread CTA per SM a bucket
+// per thread (all its words staged: 87 -> 76 us for 61 M coordinates),
+// three 512-thread CTAs a part per thread (72 -> 70 us, 85 -> 76 us with L2
+// flushed).
 template <bool FOUR, int S>
-constexpr int decode_ctas_per_sm() { return S > 1 ? 6 : 4; }
+__host__ __device__ constexpr int decode_threads() { return FOUR ? 256 : (S == 1 ? 1024 : 512); }
+template <bool FOUR, int S>
+__host__ __device__ constexpr int decode_ctas_per_sm() { return FOUR ? (S > 1 ? 6 : 4) : (S == 1 ? 1 : 3); }
 
 // Parts per bucket in qsgd_elias_decode_quarters: 4-bit codes, a thread per
 // half bucket (the middle mark); 8-bit codes, whose streams are about twice
@@ -703,7 +710,10 @@ constexpr int decode_ctas_per_sm() { return S > 1 ? 6 : 4; }
 constexpr int kPartsFour = 2, kPartsEight = 4;
 
 template <bool FOUR, int S>
-__global__ void __launch_bounds__(kThreads, (decode_ctas_per_sm<FOUR, S>())) k_elias_decode(DecodeArgs a) {
+__global__ void __launch_bounds__((decode_threads<FOUR, S>()), (decode_ctas_per_sm<FOUR, S>()))
+k_elias_decode(DecodeArgs a) {
+    constexpr int NT = decode_threads<FOUR, S>();
+    static_assert(NT % 256 == 0 && NT <= 1024, "the length sort has 256 bins");
     extern __shared__ uint32_t s_words[];   // a.stage_cap words
     static_assert(S == 1 || S == 2 || S == 4, "a bucket splits at its quarter marks");
     constexpr int QS = 4 / S;               // quarters per task
@@ -728,19 +738,19 @@ __global__ void __launch_bounds__(kThreads, (decode_ctas_per_sm<FOUR, S>())) k_e
         }
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x) single[i] = window_entry<8>(static_cast<uint32_t>(i));
-    // The CTA's 256 buckets are handed to its threads in order of stream
-    // length (a counting sort on the word count), so that the threads of a
-    // warp walk streams of about the same length instead of idling on the
+    // The CTA's NT tasks are handed to its threads in order of stream length
+    // (a counting sort on the word count, 256 bins), so that the threads of
+    // a warp walk streams of about the same length instead of idling on the
     // warp's longest one.
     __shared__ uint32_t s_hist[256];
-    __shared__ uint32_t s_wsum[kWarpsPerBlock];
-    __shared__ uint16_t s_order[kThreads];
+    __shared__ uint32_t s_wsum[8];
+    __shared__ uint16_t s_order[NT];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    s_hist[threadIdx.x] = 0u;
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0u;
     __syncthreads();
     const int stream = blockIdx.y;
     const uint32_t* offsets = a.offsets.p[stream];
-    constexpr int kBucketsPerCta = kThreads / S;
+    constexpr int kBucketsPerCta = NT / S;
     const int64_t bb = static_cast<int64_t>(blockIdx.x) * kBucketsPerCta + threadIdx.x / S;
     uint32_t key = 255u;
     if (bb < a.nbuckets) {
@@ -755,15 +765,16 @@ __global__ void __launch_bounds__(kThreads, (decode_ctas_per_sm<FOUR, S>())) k_e
     }
     const uint32_t pos = atomicAdd(s_hist + key, 1u);
     __syncthreads();
-    const uint32_t h = s_hist[threadIdx.x];
+    // exclusive scan of the 256 bins by the first 8 warps
+    const uint32_t h = threadIdx.x < 256 ? s_hist[threadIdx.x] : 0u;
     const int incl = warp_incl_sum(static_cast<int>(h), lane);
-    if (lane == 31) s_wsum[warp] = static_cast<uint32_t>(incl);
+    if (threadIdx.x < 256 && lane == 31) s_wsum[warp] = static_cast<uint32_t>(incl);
     __syncthreads();
     uint32_t start = static_cast<uint32_t>(incl) - h;
 #pragma unroll
-    for (int w = 0; w < kWarpsPerBlock; ++w) start += w < warp ? s_wsum[w] : 0u;
+    for (int w = 0; w < 8; ++w) start += w < warp ? s_wsum[w] : 0u;
     __syncthreads();
-    s_hist[threadIdx.x] = start;                 // bin starts
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = start;     // bin starts
     __syncthreads();
     s_order[s_hist[key] + pos] = static_cast<uint16_t>(threadIdx.x);
     // The CTA's words, offsets[b0] .. offsets[b0 + cnt) (at most stage_cap of
@@ -776,13 +787,13 @@ __global__ void __launch_bounds__(kThreads, (decode_ctas_per_sm<FOUR, S>())) k_e
     const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
     const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
     const uint32_t* gwords = a.words.p[stream];
-    for (uint32_t i = threadIdx.x; i < nst; i += 4 * kThreads) {
+    for (uint32_t i = threadIdx.x; i < nst; i += 4 * NT) {
         uint32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = i + j * kThreads < nst ? __ldg(gwords + base + i + j * kThreads) : 0u;
+        for (int j = 0; j < 4; ++j) v[j] = i + j * NT < nst ? __ldg(gwords + base + i + j * NT) : 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (i + j * kThreads < nst) s_words[i + j * kThreads] = v[j];
+            if (i + j * NT < nst) s_words[i + j * NT] = v[j];
     }
     __syncthreads();
     const int task = s_order[threadIdx.x];
@@ -1509,15 +1520,16 @@ int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* cons
     a.s = s_levels;
     a.status = d_status;
     a.marks = nullptr;
-    const dim3 grid(static_cast<unsigned>(div_up(nb, kThreads)), static_cast<unsigned>(W));
     const bool four = s_levels <= 7;
+    const int nt = four ? decode_threads<true, 1>() : decode_threads<false, 1>();
+    const dim3 grid(static_cast<unsigned>(div_up(nb, nt)), static_cast<unsigned>(W));
     const int rc = four ? decode_stage_words<true, 1>(&a.stage_cap) : decode_stage_words<false, 1>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     if (four)
-        k_elias_decode<true, 1><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<true, 1><<<grid, nt, dyn, s>>>(a);
     else
-        k_elias_decode<false, 1><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<false, 1><<<grid, nt, dyn, s>>>(a);
     return launch_status();
 }
 
@@ -1548,16 +1560,17 @@ int qsgd_elias_decode_quarters(const uint32_t* words, const uint32_t* offsets, c
     a.marks = marks;
     const bool four = s_levels <= 7;
     const int S = four ? kPartsFour : kPartsEight;
-    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads / S)), 1u);
+    const int nt = four ? decode_threads<true, kPartsFour>() : decode_threads<false, kPartsEight>();
+    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, nt / S)), 1u);
     const int rc = four ? decode_stage_words<true, kPartsFour>(&a.stage_cap)
                         : decode_stage_words<false, kPartsEight>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (four)
-        k_elias_decode<true, kPartsFour><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<true, kPartsFour><<<grid, nt, dyn, s>>>(a);
     else
-        k_elias_decode<false, kPartsEight><<<grid, kThreads, dyn, s>>>(a);
+        k_elias_decode<false, kPartsEight><<<grid, nt, dyn, s>>>(a);
     return launch_status();
 }
 
