@@ -689,6 +689,50 @@ struct CodeWriter {
 // S > 1: each thread decodes 1/S of a bucket (S = 2 or 4), from the
 // bucket's quarter marks (qsgd_elias_decode_quarters); a CTA then covers
 // 256 / S buckets.
+// The CTA's NT tasks in order of stream length: a counting sort on `key`
+// (the task's word count, capped at 255), so that the threads of a warp walk
+// streams of about the same length instead of idling on the warp's longest
+// one.  Returns the task (a thread index of the CTA) this thread takes.
+template <int NT>
+__device__ __forceinline__ int task_by_length(uint32_t key) {
+    static_assert(NT % 256 == 0 && NT <= 1024, "256 bins, scanned by the first 8 warps");
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_wsum[8];
+    __shared__ uint16_t s_order[NT];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0u;
+    __syncthreads();
+    const uint32_t pos = atomicAdd(s_hist + key, 1u);
+    __syncthreads();
+    const uint32_t h = threadIdx.x < 256 ? s_hist[threadIdx.x] : 0u;
+    const int incl = warp_incl_sum(static_cast<int>(h), lane);
+    if (threadIdx.x < 256 && lane == 31) s_wsum[warp] = static_cast<uint32_t>(incl);
+    __syncthreads();
+    uint32_t start = static_cast<uint32_t>(incl) - h;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) start += w < warp ? s_wsum[w] : 0u;
+    __syncthreads();
+    if (threadIdx.x < 256) s_hist[threadIdx.x] = start;     // bin starts
+    __syncthreads();
+    s_order[s_hist[key] + pos] = static_cast<uint16_t>(threadIdx.x);
+    __syncthreads();
+    return s_order[threadIdx.x];
+}
+
+// Copies the nst stream words at g to shared memory with coalesced loads
+// (four in flight per thread).  The caller synchronises before reading them.
+template <int NT>
+__device__ __forceinline__ void stage_words(const uint32_t* g, uint32_t nst, uint32_t* s_words) {
+    for (uint32_t i = threadIdx.x; i < nst; i += 4 * NT) {
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = i + j * NT < nst ? __ldg(g + i + j * NT) : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (i + j * NT < nst) s_words[i + j * NT] = v[j];
+    }
+}
+
 // Threads per decoding CTA and the resident CTAs per SM its shared staging
 // is sized for.  Each CTA copies the codeword tables (19 KB for 4-bit codes,
 // 35 KB for 8-bit codes) to shared memory, so fewer, larger CTAs leave more
@@ -738,16 +782,6 @@ k_elias_decode(DecodeArgs a) {
         }
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x) single[i] = window_entry<8>(static_cast<uint32_t>(i));
-    // The CTA's NT tasks are handed to its threads in order of stream length
-    // (a counting sort on the word count, 256 bins), so that the threads of
-    // a warp walk streams of about the same length instead of idling on the
-    // warp's longest one.
-    __shared__ uint32_t s_hist[256];
-    __shared__ uint32_t s_wsum[8];
-    __shared__ uint16_t s_order[NT];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x < 256) s_hist[threadIdx.x] = 0u;
-    __syncthreads();
     const int stream = blockIdx.y;
     const uint32_t* offsets = a.offsets.p[stream];
     constexpr int kBucketsPerCta = NT / S;
@@ -763,40 +797,19 @@ k_elias_decode(DecodeArgs a) {
         }
         key = nw < 255u ? nw : 255u;
     }
-    const uint32_t pos = atomicAdd(s_hist + key, 1u);
-    __syncthreads();
-    // exclusive scan of the 256 bins by the first 8 warps
-    const uint32_t h = threadIdx.x < 256 ? s_hist[threadIdx.x] : 0u;
-    const int incl = warp_incl_sum(static_cast<int>(h), lane);
-    if (threadIdx.x < 256 && lane == 31) s_wsum[warp] = static_cast<uint32_t>(incl);
-    __syncthreads();
-    uint32_t start = static_cast<uint32_t>(incl) - h;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) start += w < warp ? s_wsum[w] : 0u;
-    __syncthreads();
-    if (threadIdx.x < 256) s_hist[threadIdx.x] = start;     // bin starts
-    __syncthreads();
-    s_order[s_hist[key] + pos] = static_cast<uint16_t>(threadIdx.x);
+    const int task = task_by_length<NT>(key);
     // The CTA's words, offsets[b0] .. offsets[b0 + cnt) (at most stage_cap of
-    // them), are copied to shared memory with coalesced loads, so that the
-    // walks below read from there.  Every word of that range lies inside the
-    // range of one of the CTA's buckets, whatever the offsets: the copy reads
-    // nothing a bucket would not.
+    // them), are copied to shared memory, so that the walks below read from
+    // there.  Every word of that range lies inside the range of one of the
+    // CTA's buckets, whatever the offsets: the copy reads nothing a bucket
+    // would not.
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kBucketsPerCta;
     const int64_t cnt = a.nbuckets - b0 < kBucketsPerCta ? a.nbuckets - b0 : kBucketsPerCta;
     const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
     const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
     const uint32_t* gwords = a.words.p[stream];
-    for (uint32_t i = threadIdx.x; i < nst; i += 4 * NT) {
-        uint32_t v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = i + j * NT < nst ? __ldg(gwords + base + i + j * NT) : 0u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (i + j * NT < nst) s_words[i + j * NT] = v[j];
-    }
+    stage_words<NT>(gwords + base, nst, s_words);
     __syncthreads();
-    const int task = s_order[threadIdx.x];
     const int64_t b = b0 + task / S;
     if (b >= a.nbuckets) return;
     const int kq = task % S;                    // the task's part of the bucket
@@ -933,19 +946,18 @@ k_elias_decode(DecodeArgs a) {
     if (bad && a.status) *a.status = GC_ERR_CORRUPT;
 }
 
-// Stream words one decoding CTA stages: the shared memory left, after the
-// kernel's static tables and the per-CTA reservation, when
-// decode_ctas_per_sm CTAs share an SM.  Computed once per device, which also
-// raises the kernel's dynamic shared-memory limit there.
 constexpr int kMaxDevices = 64;
 
-template <bool FOUR, int S>
-int decode_stage_words(uint32_t* cap) {
-    static std::atomic<uint32_t> cached[kMaxDevices];   // words + 1; 0 = not yet known
+// Stream words a CTA of `kernel` stages: the shared memory left, after its
+// static tables and the per-CTA reservation, when `ctas` CTAs share an SM.
+// Computed once per device (cache[device] = words + 1), which also raises the
+// kernel's dynamic shared-memory limit there.
+template <typename Kernel>
+int stage_cap_for(Kernel kernel, int ctas, std::atomic<uint32_t>* cache, uint32_t* cap) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return GC_ERR_CUDA;
     if (dev >= 0 && dev < kMaxDevices) {
-        const uint32_t c = cached[dev].load(std::memory_order_relaxed);
+        const uint32_t c = cache[dev].load(std::memory_order_relaxed);
         if (c) {
             *cap = c - 1;
             return GC_OK;
@@ -955,17 +967,22 @@ int decode_stage_words(uint32_t* cap) {
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, k_elias_decode<FOUR, S>) != cudaSuccess)
+        cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
         return GC_ERR_CUDA;
-    int64_t bytes = static_cast<int64_t>(per_sm) / decode_ctas_per_sm<FOUR, S>() - reserved -
-                    static_cast<int64_t>(fa.sharedSizeBytes);
+    int64_t bytes = static_cast<int64_t>(per_sm) / ctas - reserved - static_cast<int64_t>(fa.sharedSizeBytes);
     bytes = bytes > 0 ? bytes & ~static_cast<int64_t>(15) : 0;
-    if (cudaFuncSetAttribute(k_elias_decode<FOUR, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(bytes)) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+        cudaSuccess)
         return GC_ERR_CUDA;
     *cap = static_cast<uint32_t>(bytes / sizeof(uint32_t));
-    if (dev >= 0 && dev < kMaxDevices) cached[dev].store(*cap + 1, std::memory_order_relaxed);
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(*cap + 1, std::memory_order_relaxed);
     return GC_OK;
+}
+
+template <bool FOUR, int S>
+int decode_stage_words(uint32_t* cap) {
+    static std::atomic<uint32_t> cached[kMaxDevices];
+    return stage_cap_for(k_elias_decode<FOUR, S>, decode_ctas_per_sm<FOUR, S>(), cached, cap);
 }
 
 // ================================================================ sparse regimes
@@ -1281,12 +1298,14 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
     }
 }
 
-// Decode: one thread per bucket.  The CTA first zeroes the code bytes of its
-// buckets (coalesced), then each thread walks its bucket's words with a
-// 64-bit window and sets the codes of the non-zero coordinates.  A stream
-// this encoder did not write -- a distance past the bucket's end, a read past
-// its words, a level above s or an impossible codeword -- sets the status to
-// GC_ERR_CORRUPT.
+// Decode: a thread per bucket, in the dense decoder's way.  The CTA zeroes
+// the code bytes of its buckets (coalesced), hands its buckets to its threads
+// in order of stream length, and copies its stream words to shared memory;
+// each thread then walks its bucket with a 64-bit window (the next word
+// waiting in a register) and assembles the 32-bit code words that hold
+// non-zero coordinates, each stored once.  A stream this encoder did not
+// write -- a distance past the bucket's end, a read past its words, a level
+// above s or an impossible codeword -- sets the status to GC_ERR_CORRUPT.
 // Elias-omega codewords that end inside a 12-bit window (values up to 63),
 // looked up as (value << 4) | length, 0 when the codeword is longer.
 constexpr int kOmegaWin = 12;
@@ -1307,8 +1326,11 @@ __device__ __forceinline__ uint32_t omega_window_entry(uint32_t x) {
     return (N << 4) | static_cast<uint32_t>(pos);
 }
 
+constexpr int kSparseDecodeCtasPerSm = 4;
+
 template <bool FOUR>
-__global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_decode_sparse(DecodeArgs a) {
+    extern __shared__ uint32_t s_words[];   // a.stage_cap words
     __shared__ uint16_t otab[1 << kOmegaWin];
     for (int i = threadIdx.x; i < (1 << kOmegaWin); i += kThreads)
         otab[i] = static_cast<uint16_t>(omega_window_entry(static_cast<uint32_t>(i)));
@@ -1316,9 +1338,9 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) 
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kThreads;
     const int64_t cnt = a.nbuckets - b0 < kThreads ? a.nbuckets - b0 : kThreads;
     uint8_t* codes = a.codes.p[stream];
+    const int64_t total = FOUR ? (a.n + 1) / 2 : a.n;      // code bytes
     {
-        const int64_t bpb = FOUR ? a.d / 2 : a.d;                 // bytes per whole bucket (>= 64)
-        const int64_t total = FOUR ? (a.n + 1) / 2 : a.n;
+        const int64_t bpb = FOUR ? a.d / 2 : a.d;           // bytes per whole bucket (>= 64)
         const int64_t start = b0 * bpb;
         int64_t end = (b0 + cnt) * bpb;
         if (end > total) end = total;
@@ -1327,51 +1349,56 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) 
         for (int64_t i = threadIdx.x; i < nvec; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
         for (int64_t i = start + nvec * 16 + threadIdx.x; i < end; i += kThreads) codes[i] = 0;
     }
-    __syncthreads();
-    const int64_t b = b0 + threadIdx.x;
-    if (b >= a.nbuckets) return;
     const uint32_t* offsets = a.offsets.p[stream];
+    const int64_t bb = b0 + threadIdx.x;
+    uint32_t key = 255u;
+    if (bb < a.nbuckets) {
+        const uint32_t nw = offsets[bb + 1] - offsets[bb];
+        key = nw < 255u ? nw : 255u;
+    }
+    // (its barriers also order the zero fill before the code words below)
+    const int task = task_by_length<kThreads>(key);
+    const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
+    const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
+    const uint32_t* gwords = a.words.p[stream];
+    stage_words<kThreads>(gwords + base, nst, s_words);
+    __syncthreads();
+    const int64_t b = b0 + task;
+    if (b >= a.nbuckets) return;
     const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
+    const bool staged = w_lo - base <= nst && w_hi - base <= nst;
+    const uint32_t* src = staged ? s_words + (w_lo - base) : gwords + w_lo;
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
-    const uint32_t* src = a.words.p[stream] + w_lo;
+    auto word = [&](int64_t i) { return i < avail ? src[i] : 0u; };
     const int64_t lo = b * a.d;
     const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
     bool bad = avail == 0;
-    int64_t next = 0;
-    uint64_t win = 0;
-    int have = 0;
-    // the window may hold zero words read ahead past the bucket; only taking
-    // bits beyond its last word makes the stream corrupt
-    const int64_t limit = avail > 0 ? 32 * (avail - 1) : 0;
-    int64_t used = 0;
+    a.norms.p[stream][b] = __uint_as_float(word(0));
+    // window: `have` valid bits from the top of win, the next word in `pre`
+    uint64_t win = (static_cast<uint64_t>(word(1)) << 32) | word(2);
+    int have = 64;
+    uint32_t pre = word(3);
+    int64_t next = 4;
     auto refill = [&]() {
-        while (have <= 32) {
-            const uint32_t w = next < avail ? __ldg(src + next) : 0u;
-            ++next;
-            win |= static_cast<uint64_t>(w) << (32 - have);
+        if (have <= 32) {
+            win |= static_cast<uint64_t>(pre) << (32 - have);
             have += 32;
+            pre = word(next);
+            ++next;
         }
+    };
+    auto consume = [&](int l) {
+        win <<= l;
+        have -= l;
     };
     auto take = [&](int k) -> uint32_t {       // k in 1..31
         refill();
         const uint32_t v = static_cast<uint32_t>(win >> (64 - k));
-        win <<= k;
-        have -= k;
-        used += k;
-        bad |= used > limit;
+        consume(k);
         return v;
     };
-    auto get_omega = [&]() -> uint32_t {
-        refill();
-        const uint32_t e = otab[static_cast<uint32_t>(win >> (64 - kOmegaWin))];
-        if (e) {
-            const int l = static_cast<int>(e & 15u);
-            win <<= l;
-            have -= l;
-            used += l;
-            bad |= used > limit;
-            return e >> 4;
-        }
+    // a codeword longer than the table's window, bit by bit
+    auto omega_slow = [&]() -> uint32_t {
         uint32_t N = 1;
         while (take(1)) {
             if (N > 16) {                      // no distance or level of a valid stream is this long
@@ -1382,37 +1409,93 @@ __global__ void __launch_bounds__(kThreads) k_elias_decode_sparse(DecodeArgs a) 
         }
         return N;
     };
-    a.norms.p[stream][b] = __uint_as_float(avail ? __ldg(src) : 0u);
-    next = 1;
+    // bits after the norm word consumed so far; beyond its last word the
+    // stream is corrupt (the window may hold zero words read past it)
+    const int64_t limit = avail > 0 ? 32 * (avail - 1) : 0;
+    auto used = [&]() { return 32 * (next - 2) - have; };
+    // the code word (8 codes of 4 bits or 4 of 8) being assembled
+    uint32_t* out = reinterpret_cast<uint32_t*>(codes + (FOUR ? lo / 2 : lo));
+    const int64_t out_bytes = total - (FOUR ? lo / 2 : lo);
+    uint32_t cw = 0xFFFFFFFFu, cv = 0u;
+    auto flush = [&]() {
+        if (cw == 0xFFFFFFFFu) return;
+        if (4 * static_cast<int64_t>(cw) + 4 <= out_bytes) {
+            out[cw] = cv;
+        } else {                               // the last word of a ragged buffer
+            uint8_t* ob = reinterpret_cast<uint8_t*>(out + cw);
+            for (int j = 0; j < 4; ++j)
+                if (4 * static_cast<int64_t>(cw) + j < out_bytes) ob[j] = static_cast<uint8_t>(cv >> (8 * j));
+        }
+    };
     const uint32_t smax = static_cast<uint32_t>(a.s);
     int64_t p = -1;
     for (int guard = 0; guard <= len && !bad; ++guard) {
-        const uint32_t g = get_omega();
-        if (bad) break;
+        // After a refill the window holds more than 32 bits: a distance from
+        // the table (at most 12), the sign and a level from the table (at
+        // most 12) need no refill in between.
+        refill();
+        uint32_t g;
+        const uint32_t e1 = otab[static_cast<uint32_t>(win >> (64 - kOmegaWin))];
+        if (e1) {
+            g = e1 >> 4;
+            consume(static_cast<int>(e1 & 15u));
+        } else {
+            g = omega_slow();
+            if (bad) break;
+            refill();
+        }
         p += g;
         if (p >= len) {
             bad |= p > len;
             break;
         }
-        const uint32_t sign = take(1);
-        uint32_t level = a.s >= 2 ? get_omega() : 1u;
-        if (bad) break;
-        if (level > smax) {
+        const uint32_t sign = static_cast<uint32_t>(win >> 63);
+        consume(1);
+        uint32_t level = 1u;
+        if (a.s >= 2) {
+            const uint32_t e2 = otab[static_cast<uint32_t>(win >> (64 - kOmegaWin))];
+            if (e2) {
+                level = e2 >> 4;
+                consume(static_cast<int>(e2 & 15u));
+            } else {
+                level = omega_slow();
+                if (bad) break;
+            }
+        }
+        if (level > smax) {             // written as s; the walk stops after it
             bad = true;
             level = smax;
         }
-        const int64_t i = lo + p;
-        if (FOUR) {
-            const uint8_t code = static_cast<uint8_t>((sign << 3) | level);
-            codes[i >> 1] = static_cast<uint8_t>(codes[i >> 1] | ((i & 1) ? code : (code << 4)));
-        } else {
-            codes[i] = static_cast<uint8_t>((sign << 7) | level);
+        if (used() > limit) {           // read past the bucket's words
+            bad = true;
+            break;
         }
+        const uint32_t pp = static_cast<uint32_t>(p);
+        const uint32_t wi = FOUR ? pp >> 3 : pp >> 2;
+        if (wi != cw) {
+            flush();
+            cw = wi;
+            cv = 0u;
+        }
+        // element e of a word: byte e / 2, high nibble for even e (4-bit
+        // codes); byte e (8-bit codes)
+        if (FOUR)
+            cv |= ((sign << 3) | level) << (8 * ((pp & 7u) >> 1) + 4 * (1u - (pp & 1u)));
+        else
+            cv |= ((sign << 7) | level) << (8 * (pp & 3u));
     }
+    flush();
+    bad |= used() > limit;
     if (bad && a.status) *a.status = GC_ERR_CORRUPT;
 }
 
 }  // namespace
+template <bool FOUR>
+int sparse_stage_words(uint32_t* cap) {
+    static std::atomic<uint32_t> cached[kMaxDevices];
+    return stage_cap_for(k_elias_decode_sparse<FOUR>, kSparseDecodeCtasPerSm, cached, cap);
+}
+
 }  // namespace gc
 
 using namespace gc;
@@ -1632,14 +1715,17 @@ int qsgd_elias_decode_sparse(const uint32_t* words, const uint32_t* offsets, int
     a.nbuckets = div_up(n, bucket);
     a.s = s_levels;
     a.status = d_status;
-    a.stage_cap = 0;
     a.marks = nullptr;
     const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads)), 1u);
+    const bool four = s_levels <= 7;
+    const int rc = four ? sparse_stage_words<true>(&a.stage_cap) : sparse_stage_words<false>(&a.stage_cap);
+    if (rc != GC_OK) return rc;
+    const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (s_levels <= 7)
-        k_elias_decode_sparse<true><<<grid, kThreads, 0, s>>>(a);
+    if (four)
+        k_elias_decode_sparse<true><<<grid, kThreads, dyn, s>>>(a);
     else
-        k_elias_decode_sparse<false><<<grid, kThreads, 0, s>>>(a);
+        k_elias_decode_sparse<false><<<grid, kThreads, dyn, s>>>(a);
     return launch_status();
 }
 
