@@ -46,7 +46,7 @@ __all__ = [
     "gc_2bit_step", "gc_2bit_quantize_local", "gc_2bit_quantize_steps", "qsgd_quantize_maxnorm",
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
     "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step", "qsgd_elias_decode_batched",
-    "qsgd_elias_encode_marked", "qsgd_elias_decode_quarters",
+    "qsgd_elias_encode_marked", "qsgd_elias_decode_quarters", "qsgd_elias_encode_status",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -122,6 +122,8 @@ def load():
             "gc_testing_saps_round_one_pass": (i32, [i64, f64, u64, vp, i32, vp, f32, f32, vp, vp, vp, i64, vp,
                                                      vp, sz, vp, vp]),
             "saps_mask_compact_noalloc": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, vp]),
+            "gc_testing_qsgd_elias_encode_withhold": (i32, [vp, vp, i64, i32, i32, vp, u64, vp, vp, sz, i64, u64,
+                                                              vp]),
             "gc_testing_saps_mask_compact_withhold": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz,
                                                             vp, i64, u64, vp]),
         }
@@ -429,6 +431,12 @@ def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket
             None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words))
     keep = (words, offsets, codes, norms) + (() if status is None else (status,))
     return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
+
+
+def qsgd_elias_encode_status(workspace: torch.Tensor) -> int:
+    """The device status the last qsgd_elias_encode(_marked) left in its
+    workspace (its first 4 bytes): GC_OK or GC_ERR_TIMEOUT.  Synchronises."""
+    return int(workspace[:4].view(torch.int32).item())
 
 
 def qsgd_elias_encode_marked(codes: torch.Tensor, norms: torch.Tensor, n: int, bucket: int, s_levels: int,

@@ -8,14 +8,14 @@
 // word is padded with zero bits; offsets[b] is bucket b's first word and
 // offsets[nbuckets] the stream's length, so that buckets decode in parallel.
 //
-// Encode = two launches.  k_elias_count: one warp per bucket sums the coded
-// lengths (a 256-entry table turns one code byte into its codeword bits and
-// length), writes each bucket's word count, and the last CTA to finish turns
-// the per-CTA totals into an exclusive prefix (a ticket counter, no waiting).
-// k_elias_encode: every CTA scans its 64 buckets' counts from that prefix,
-// and each warp assembles one bucket at a time in shared memory (one warp
-// scan of bit lengths per 32 code words, then shared-memory atomicOr of at
-// most three words per lane) and stores it with coalesced 32-bit writes.
+// Encode = one launch reading the codes once.  Each CTA takes a chunk of 64
+// buckets (a ticket, so chunks go out in the order CTAs start); each warp
+// assembles its buckets in shared memory (a 256-entry table turns a code
+// byte into its codeword bits and length; one warp scan of bit lengths per
+// 32 code words, then shared-memory atomicOr of at most three words per
+// lane), publishes each bucket's word count, takes the bucket's first word
+// from a decoupled look-back over the buckets before it, and stores the
+// bucket with coalesced 32-bit writes.
 // Decode: one thread per bucket walks its stream with a 64-bit window; an
 // 11-bit (4-bit codes) or 12-bit (8-bit codes) lookahead table, built by the
 // compiler, decodes up to 8 or 4 whole codewords per step, and an 8-bit one
@@ -23,11 +23,13 @@
 #include <atomic>
 
 #include "gc_common.cuh"
+#include "../../include/gc_gb300_testing.h"
 
 namespace gc {
 namespace {
 
 constexpr int kChunk = 64;                          // buckets per CTA
+constexpr int kEncodeStageWords = 9216;             // the dense encoder's staging per CTA, at most
 constexpr size_t kTicketBytes = 16;
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -210,162 +212,27 @@ __device__ __forceinline__ Geometry geometry(int d) {
     return g;
 }
 
-// Coded bits of 16 code bytes.
-// For 4-bit codes the length follows from three comparisons of the level
-// (omega(level + 1) + sign is 1, 4, 7 or 8 bits for level 0, 1-2, 3-6, 7):
-// L = 1 + 3 [level >= 1] + 3 [level >= 3] + [level = 7], counted for the
-// eight codes of a word at once with bit tricks on the 3-bit level fields.
-template <bool FOUR>
-__device__ __forceinline__ uint32_t piece_bits(const uint4& v, const uint32_t* lut) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t bits = 0;
-    if (FOUR) {
-        uint32_t ge1 = 0, ge3 = 0, eq7 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t lv = w[i] & 0x77777777u;
-            const uint32_t b1 = lv >> 1, b2 = lv >> 2;
-            ge1 += __popc((lv | b1 | b2) & 0x11111111u);
-            ge3 += __popc((b2 | (b1 & lv)) & 0x11111111u);
-            eq7 += __popc(b2 & b1 & lv & 0x11111111u);
-        }
-        bits = 32u + 3u * (ge1 + ge3) + eq7;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) bits += lut[(w[i] >> (8 * j)) & 255u] & 31u;
-    }
-    return bits;
-}
+// ---------------------------------------------------------------- encode
 
-// Coded bits of a ragged bucket (the last one, when n is not a multiple of
-// d), by one warp, byte by byte at the edge.
-template <bool FOUR>
-__device__ uint32_t ragged_bits(const uint8_t* codes, int64_t n, int d, int64_t b, const uint32_t* lut,
-                                int lane) {
-    const BucketBytes bb = bucket_bytes<FOUR>(codes, n, d, b);
-    const int nw_in = (bb.valid + 3) >> 2;
-    int bits = 0;
-    for (int k = lane; k < nw_in; k += 32) {
-        uint64_t acc;
-        bits += word_bits<FOUR>(bb, k, lut, acc);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
-    return static_cast<uint32_t>(bits);
-}
-
-// ---------------------------------------------------------------- count
-
-struct CountArgs {
-    const uint8_t* codes;
-    int64_t n;
-    int d;
-    int64_t nbuckets;
-    Ws ws;
+// The encoder's workspace: a 16-byte header (the device status, then the
+// CTA ticket) and one look-back state word per chunk of buckets (its word
+// count, then its inclusive prefix).
+struct EncodeWs {
+    int* status;
+    uint32_t* ticket;
+    uint64_t* state;    // [nchunks] (at most nbuckets)
 };
 
-// Register bound for 8 CTAs per SM (measured fastest with the encoder below).
-template <bool FOUR>
-__global__ void __launch_bounds__(kThreads, 8) k_elias_count(CountArgs a) {
-    __shared__ uint32_t lut[256];
-    __shared__ uint32_t bits_s[kChunk];
-    __shared__ uint32_t wsum[kWarpsPerBlock];
-    __shared__ bool is_last;
-    build_lut<FOUR>(lut);
-    if (threadIdx.x < kChunk) bits_s[threadIdx.x] = 0u;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const Geometry g = geometry<FOUR>(a.d);
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
-    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
-    const bool ragged = (a.n % a.d) != 0 && b0 + nbc == a.nbuckets;
-    const int nfull = nbc - (ragged ? 1 : 0);
-    const uint4* src = reinterpret_cast<const uint4*>(a.codes + b0 * g.Bb);
-    const int npieces = nfull * g.P;
-    // four pieces per thread in flight, then their lengths
-    constexpr int kBatch = 4;
-    for (int q0 = warp * 32; q0 < npieces; q0 += kBatch * kThreads) {
-        uint4 v[kBatch];
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int q = q0 + i * kThreads + lane;
-            v[i] = q < npieces ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int q = q0 + i * kThreads + lane;
-            uint32_t bits = q < npieces ? piece_bits<FOUR>(v[i], lut) : 0u;
-            for (int o = g.G >> 1; o; o >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, o);
-            if ((lane & (g.G - 1)) == 0 && q < npieces) {
-                if (g.P <= 32)
-                    bits_s[q / g.P] = bits;
-                else
-                    atomicAdd(bits_s + q / g.P, bits);
-            }
-        }
-    }
-    if (ragged && warp == kWarpsPerBlock - 1) {
-        const uint32_t bits = ragged_bits<FOUR>(a.codes, a.n, a.d, b0 + nfull, lut, lane);
-        if (lane == 0) bits_s[nfull] = bits;
-    }
-    __syncthreads();
-    if (warp < kChunk / 32) {
-        const int t = threadIdx.x;
-        uint32_t nw = 0;
-        if (t < nbc) {
-            nw = (32u + bits_s[t] + 31u) >> 5;
-            a.ws.counts[b0 + t] = nw;
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) nw += __shfl_xor_sync(0xffffffffu, nw, o);
-        if (lane == 0) wsum[warp] = nw;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t t = 0;
-        for (int w = 0; w < kChunk / 32; ++w) t += wsum[w];
-        a.ws.chunk[blockIdx.x] = t;
-        __threadfence();
-        is_last = atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!is_last) return;
-    // The last CTA: exclusive prefix of the per-CTA totals, in place, and
-    // the grand total after them.  Every other CTA fenced its total before
-    // taking its ticket; the totals are read from L2.  Thread t scans the
-    // contiguous run [t*per, (t+1)*per) with all its loads in flight, then
-    // one block scan of the run totals gives each run its base.
-    __threadfence();
-    const int nchunks = static_cast<int>(gridDim.x);
-    const int per = (nchunks + kThreads - 1) / kThreads;
-    const int lo = threadIdx.x * per;
-    const int hi = lo + per < nchunks ? lo + per : nchunks;
-    uint32_t run = 0;
-    for (int i = lo; i < hi; ++i) run += __ldcg(a.ws.chunk + i);
-    const int incl = warp_incl_sum(static_cast<int>(run), lane);
-    if (lane == 31) wsum[warp] = static_cast<uint32_t>(incl);
-    __syncthreads();
-    uint32_t before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerBlock; ++w) {
-        before += w < warp ? wsum[w] : 0u;
-        total += wsum[w];
-    }
-    uint32_t acc = before + static_cast<uint32_t>(incl) - run;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t v = __ldcg(a.ws.chunk + i);
-        a.ws.chunk[i] = acc;
-        acc += v;
-    }
-    if (threadIdx.x == 0) {
-        a.ws.chunk[nchunks] = total;
-        *a.ws.ticket = 0u;
-    }
+inline size_t encode_ws_bytes(int64_t nbuckets) {
+    return kTicketBytes + static_cast<size_t>(div_up(nbuckets * 8, 16) * 16);
 }
 
-// ---------------------------------------------------------------- encode
+EncodeWs encode_ws(void* ws) {
+    char* p = static_cast<char*>(ws);
+    return EncodeWs{reinterpret_cast<int*>(p), reinterpret_cast<uint32_t*>(p + 4),
+                    reinterpret_cast<uint64_t*>(p + kTicketBytes)};
+}
+
 
 struct EncodeArgs {
     const uint8_t* codes;
@@ -373,13 +240,17 @@ struct EncodeArgs {
     int64_t n;
     int d;
     int64_t nbuckets;
-    Ws ws;
     uint32_t* words;
     uint32_t* offsets;
-    int stage_stride;   // staging words per bucket slot
-    int slots;          // bucket slots per warp (32 / G)
+    int stage_stride;   // staging words per bucket
+    int slots;          // buckets per warp and pass (32 / G)
     uint16_t* marks;    // quarter marks [3 * nbuckets], or null
+    EncodeWs ws;
+    uint64_t wait_ns;   // bound on each look-back wait
+    int64_t withhold;   // test hook: this chunk never publishes (-1: none)
+    int chunk;          // buckets per CTA (<= kChunk), all staged at once
 };
+
 
 // The stream bits of 16 code bytes (table entries e[]) OR-ed into the
 // staging words from bit position `start`: the entries are joined two at a
@@ -406,38 +277,32 @@ __device__ __forceinline__ void emit_piece(uint32_t* stage, uint32_t start, cons
     if (nacc > 0) atomicOr(stage + wi, lo << (32 - nacc));
 }
 
-// Register bound for 5 CTAs per SM (48 registers, no spills): 3-8% faster
-// than the 4 that 54-58 registers allow.
+// Register bound for 5 CTAs per SM (48 registers, no spills).  Every bucket
+// of the CTA's chunk is staged at once (chunk x stage_stride words), so the
+// chunk's word count is known when its encoding ends: it is published then,
+// and the look-back over the chunks before it rarely waits.
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
     extern __shared__ uint32_t smem[];
+    __shared__ uint32_t s_chunk, s_end;
+    __shared__ uint32_t s_nw[kChunk];             // words of each bucket, then its first word
     uint32_t* lut = smem;
-    uint32_t* offs = smem + 256;                       // [kChunk]
-    uint32_t* stages = smem + 256 + kChunk;            // [kWarpsPerBlock * slots][stage_stride]
+    uint32_t* stages = smem + 256;                // [chunk][stage_stride]
     build_lut<FOUR>(lut);
-    const int nstage = kWarpsPerBlock * a.slots * a.stage_stride;
+    const int nstage = a.chunk * a.stage_stride;
     for (int i = threadIdx.x; i < nstage; i += kThreads) stages[i] = 0u;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
-    if (warp == 0) {
-        const int64_t ba = b0 + 2 * lane, bb = ba + 1;
-        const uint32_t c0 = ba < a.nbuckets ? a.ws.counts[ba] : 0u;
-        const uint32_t c1 = bb < a.nbuckets ? a.ws.counts[bb] : 0u;
-        const int incl = warp_incl_sum(static_cast<int>(c0 + c1), lane);
-        const uint32_t o0 = a.ws.chunk[blockIdx.x] + static_cast<uint32_t>(incl) - c0 - c1;
-        offs[2 * lane] = o0;
-        offs[2 * lane + 1] = o0 + c0;
-        if (ba < a.nbuckets) a.offsets[ba] = o0;
-        if (bb < a.nbuckets) a.offsets[bb] = o0 + c0;
-        if (blockIdx.x == gridDim.x - 1 && lane == 0) a.offsets[a.nbuckets] = a.ws.chunk[gridDim.x];
-    }
+    // Chunks are taken in the order CTAs start (a ticket), so every chunk a
+    // look-back waits for belongs to a CTA already running: the waits end.
+    if (threadIdx.x == 0) s_chunk = atomicAdd(a.ws.ticket, 1u);
     __syncthreads();
+    const int64_t chunk = s_chunk;
+    const int64_t b0 = chunk * a.chunk;
     const Geometry g = geometry<FOUR>(a.d);
-    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
+    const int nbc = static_cast<int>(a.nbuckets - b0 < a.chunk ? a.nbuckets - b0 : a.chunk);
     const bool ragged = (a.n % a.d) != 0 && b0 + nbc == a.nbuckets;
     const int nfull = nbc - (ragged ? 1 : 0);
     const int grp = lane / g.G, gl = lane % g.G;
-    uint32_t* stage = stages + (warp * a.slots + grp) * a.stage_stride;
     const uint4* src = reinterpret_cast<const uint4*>(a.codes + b0 * g.Bb);
     // Items = (bucket pass j, round r); the next item's 16 bytes and norm are
     // loaded while the current one is coded.
@@ -460,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
         const int r = it % R;
         const int lb = first + (it / R) * step + grp;
         const bool active = lb < nfull;
+        uint32_t* stage = stages + lb * a.stage_stride;
         const uint4 v = vn;
         const float nrm = nn;
         if (it + 1 < items) load_item(it + 1, vn, nn);
@@ -491,27 +357,15 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
             if (c > 0 && c % q == 0) a.marks[3 * (b0 + lb) + c / q - 1] = static_cast<uint16_t>(pos + incl - len);
         }
         pos += __shfl_sync(0xffffffffu, incl, grp * g.G + g.G - 1);
-        if (r == R - 1) {
-            __syncwarp();
-            if (active) {
-                const int nw = static_cast<int>((pos + 31) >> 5);
-                uint32_t* dst = a.words + offs[lb];
-                for (int k = gl; k < nw; k += g.G) {
-                    dst[k] = stage[k];
-                    stage[k] = 0u;
-                }
-            }
-            __syncwarp();
-        }
+        if (r == R - 1 && active && gl == 0) s_nw[lb] = (pos + 31) >> 5;
     }
     if (ragged && warp == kWarpsPerBlock - 1) {
-        // the ragged last bucket, by one warp in slot 0 of this warp
+        // the ragged last bucket, by one warp
         const int lb = nfull;
         const int64_t b = b0 + lb;
         const BucketBytes bb = bucket_bytes<FOUR>(a.codes, a.n, a.d, b);
         const int nw_in = (bb.valid + 3) >> 2;
-        uint32_t* st0 = stages + warp * a.slots * a.stage_stride;
-        __syncwarp();
+        uint32_t* st0 = stages + lb * a.stage_stride;
         if (lane == 0) st0[0] = __float_as_uint(__ldg(a.norms + b));
         uint32_t pos = 32;
         const int q = a.d / 4;
@@ -530,10 +384,47 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
         }
         // quarters that start past the short bucket's end: the end
         if (a.marks && lane < 3 && (lane + 1) * q >= blen) a.marks[3 * b + lane] = static_cast<uint16_t>(pos);
-        __syncwarp();
-        const int nw = static_cast<int>((pos + 31) >> 5);
-        uint32_t* dst = a.words + offs[lb];
-        for (int k = lane; k < nw; k += 32) dst[k] = st0[k];
+        if (lane == 0) s_nw[lb] = (pos + 31) >> 5;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // the chunk's words, published at once; the buckets' first words
+        // within it; then the chunk's first word from the look-back
+        const uint32_t c0 = 2 * lane < nbc ? s_nw[2 * lane] : 0u;
+        const uint32_t c1 = 2 * lane + 1 < nbc ? s_nw[2 * lane + 1] : 0u;
+        const uint32_t incl = static_cast<uint32_t>(warp_incl_sum(static_cast<int>(c0 + c1), lane));
+        const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+        const bool publish = chunk != a.withhold;
+        if (lane == 0 && publish) st_state(a.ws.state + chunk, (chunk == 0 ? kFlagPrefix : kFlagAgg) | total);
+        bool timed_out = false;
+        const uint64_t base =
+            chunk == 0 ? 0 : lookback_exclusive(a.ws.state, chunk, lane, a.wait_ns, 0u, timed_out);
+        if (lane == 0) {
+            if (chunk != 0 && publish) st_state(a.ws.state + chunk, kFlagPrefix | (base + total));
+            if (timed_out) atomicExch(a.ws.status, GC_ERR_TIMEOUT);
+            if (b0 + nbc == a.nbuckets) a.offsets[a.nbuckets] = static_cast<uint32_t>(base) + total;
+            s_end = static_cast<uint32_t>(base) + total;
+        }
+        const uint32_t o0 = static_cast<uint32_t>(base) + incl - c0 - c1;
+        if (2 * lane < nbc) {
+            s_nw[2 * lane] = o0;
+            a.offsets[b0 + 2 * lane] = o0;
+        }
+        if (2 * lane + 1 < nbc) {
+            s_nw[2 * lane + 1] = o0 + c0;
+            a.offsets[b0 + 2 * lane + 1] = o0 + c0;
+        }
+    }
+    __syncthreads();
+    // each warp writes out buckets warp, warp + 8, ...: the stream words
+    // from the bucket's first word to the next bucket's, coalesced
+    const uint32_t chunk_end = s_end;
+    for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
+        const uint32_t off = s_nw[lb];
+        const uint32_t nw = (lb + 1 < nbc ? s_nw[lb + 1] : chunk_end) - off;
+        const uint32_t* st = stages + lb * a.stage_stride;
+        uint32_t* dst = a.words + off;
+        for (uint32_t k = lane; k < nw; k += 32) dst[k] = st[k];
     }
 }
 
@@ -1513,7 +1404,11 @@ uint64_t qsgd_elias_max_words(int64_t n, int bucket, int s_levels) {
 size_t qsgd_elias_workspace_bytes(int64_t n, int bucket) {
     if (n < 0 || !valid_bucket(bucket)) return 0;
     const int64_t nb = div_up(n, bucket), nchunks = div_up(nb, kChunk);
-    return kTicketBytes + chunk_bytes(nchunks) + static_cast<size_t>(div_up(nb * 4, 16) * 16);
+    // the dense encoder's header and look-back states, or the sparse
+    // encoder's ticket, chunk totals and bucket counts
+    const size_t sparse = kTicketBytes + chunk_bytes(nchunks) + static_cast<size_t>(div_up(nb * 4, 16) * 16);
+    const size_t dense = encode_ws_bytes(nb);
+    return sparse > dense ? sparse : dense;
 }
 
 }  // extern "C"
@@ -1522,7 +1417,7 @@ namespace {
 
 int encode_dense(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels, uint32_t* words,
                  uint64_t capacity_words, uint32_t* offsets, uint16_t* marks, void* workspace, size_t ws_bytes,
-                 gc_stream_t stream) {
+                 int64_t withhold, uint64_t wait_ns, gc_stream_t stream) {
     if (n < 0 || !valid_bucket(bucket) || s_levels < 1 || s_levels > 127) return GC_ERR_INVALID;
     if (!offsets || (n > 0 && (!codes || !norms || !words || !workspace))) return GC_ERR_INVALID;
     const uint64_t need = qsgd_elias_max_words(n, bucket, s_levels);
@@ -1533,29 +1428,34 @@ int encode_dense(const uint8_t* codes, const float* norms, int64_t n, int bucket
         !aligned16(offsets) || (workspace && !aligned16(workspace)))
         return GC_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (n == 0) return cudaMemsetAsync(offsets, 0, sizeof(uint32_t), s) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    if (n == 0) {
+        if (workspace && cudaMemsetAsync(workspace, 0, kTicketBytes, s) != cudaSuccess) return GC_ERR_CUDA;
+        return cudaMemsetAsync(offsets, 0, sizeof(uint32_t), s) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    }
     const bool four = s_levels <= 7;
-    const int64_t nb = div_up(n, bucket), nchunks = div_up(nb, kChunk);
-    const Ws ws = ws_layout(workspace, nchunks);
-    if (cudaMemsetAsync(ws.ticket, 0, kTicketBytes, s) != cudaSuccess) return GC_ERR_CUDA;
-    CountArgs ca{codes, n, bucket, nb, ws};
-    const unsigned grid = static_cast<unsigned>(nchunks);
-    if (four)
-        k_elias_count<true><<<grid, kThreads, 0, s>>>(ca);
-    else
-        k_elias_count<false><<<grid, kThreads, 0, s>>>(ca);
-    if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
+    const int64_t nb = div_up(n, bucket);
     const int P = (four ? bucket / 2 : bucket) / 16;
-    EncodeArgs ea{codes, norms, n, bucket, nb, ws, words, offsets,
-                  static_cast<int>(bucket_max_words(bucket, four)) + 2, P < 32 ? 32 / P : 1, marks};
-    const size_t smem = sizeof(uint32_t) *
-                        (256 + kChunk + static_cast<size_t>(kWarpsPerBlock) * ea.slots * ea.stage_stride);
+    const int stride = static_cast<int>(bucket_max_words(bucket, four)) + 2;
+    // buckets per CTA: 64, halved while their staging would pass 36 KB (so
+    // that five CTAs share an SM)
+    int chunk = kChunk;
+    while (chunk > 8 && chunk * stride > kEncodeStageWords) chunk /= 2;
+    const int64_t nchunks = div_up(nb, chunk);
+    // status, ticket and the look-back states start at zero
+    if (cudaMemsetAsync(workspace, 0, kTicketBytes + static_cast<size_t>(nchunks) * 8, s) != cudaSuccess)
+        return GC_ERR_CUDA;
+    EncodeArgs ea{codes, norms, n, bucket, nb, words, offsets, stride, P < 32 ? 32 / P : 1, marks,
+                  encode_ws(workspace), wait_ns, withhold < 0 ? -1 : withhold / chunk, chunk};
+    const size_t smem = sizeof(uint32_t) * (256 + static_cast<size_t>(chunk) * stride);
+    const unsigned grid = static_cast<unsigned>(nchunks);
     if (four)
         k_elias_encode<true><<<grid, kThreads, smem, s>>>(ea);
     else
         k_elias_encode<false><<<grid, kThreads, smem, s>>>(ea);
     return launch_status();
 }
+
+constexpr uint64_t kEncodeWaitNs = 1000000000ull;   // 1 s: only a fault elsewhere makes a wait that long
 
 }  // namespace
 
@@ -1565,7 +1465,7 @@ int qsgd_elias_encode(const uint8_t* codes, const float* norms, int64_t n, int b
                       uint32_t* words, uint64_t capacity_words, uint32_t* offsets, void* workspace,
                       size_t ws_bytes, gc_stream_t stream) {
     return encode_dense(codes, norms, n, bucket, s_levels, words, capacity_words, offsets, nullptr, workspace,
-                        ws_bytes, stream);
+                        ws_bytes, -1, kEncodeWaitNs, stream);
 }
 
 int qsgd_elias_encode_marked(const uint8_t* codes, const float* norms, int64_t n, int bucket, int s_levels,
@@ -1574,7 +1474,16 @@ int qsgd_elias_encode_marked(const uint8_t* codes, const float* norms, int64_t n
     if (n > 0 && !marks) return GC_ERR_INVALID;
     if (marks && !aligned16(marks)) return GC_ERR_ALIGN;
     return encode_dense(codes, norms, n, bucket, s_levels, words, capacity_words, offsets, marks, workspace,
-                        ws_bytes, stream);
+                        ws_bytes, -1, kEncodeWaitNs, stream);
+}
+
+int gc_testing_qsgd_elias_encode_withhold(const uint8_t* codes, const float* norms, int64_t n, int bucket,
+                                          int s_levels, uint32_t* words, uint64_t capacity_words, uint32_t* offsets,
+                                          void* workspace, size_t ws_bytes, int64_t withhold_bucket, uint64_t wait_ns,
+                                          gc_stream_t stream) {
+    if (wait_ns < 1 || wait_ns > kEncodeWaitNs || withhold_bucket < 0) return GC_ERR_INVALID;
+    return encode_dense(codes, norms, n, bucket, s_levels, words, capacity_words, offsets, nullptr, workspace,
+                        ws_bytes, withhold_bucket, wait_ns, stream);
 }
 
 int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* const* offsets, int W,

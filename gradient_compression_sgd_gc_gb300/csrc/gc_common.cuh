@@ -103,6 +103,73 @@ __host__ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
     return z ^ (z >> 31);
 }
 
+// ---------------------------------------------------------------- look-back
+
+// Decoupled look-back (Merrill and Garland, "Single-pass Parallel Prefix
+// Scan with Decoupled Look-back", 2016) over 64-bit state words, one per
+// tile: the flag in the top two bits (1: the tile's aggregate, 2: its
+// inclusive prefix), the value below.  A state word carries its own value and
+// no other data is published through it, so relaxed single-copy-atomic
+// 64-bit accesses at GPU scope are enough (no acquire/release fences).
+constexpr uint64_t kFlagAgg = 1ull << 62;
+constexpr uint64_t kFlagPrefix = 2ull << 62;
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+
+__device__ __forceinline__ uint64_t ld_state(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_state(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Exclusive prefix of tile `tile` (> 0), by one warp: walks back over the
+// predecessors' states 32 at a time (one coalesced 256-byte read) until it
+// meets an inclusive prefix, summing the aggregates on the way.  A pending
+// predecessor is polled again (after `backoff_ns` of sleep, 0: at once);
+// every wait is bounded: after wait_ns the predecessors still pending count
+// as zero and timed_out is set.  Every lane returns the prefix.
+__device__ __forceinline__ uint64_t lookback_exclusive(const uint64_t* state, int64_t tile, int lane,
+                                                       uint64_t wait_ns, unsigned backoff_ns, bool& timed_out) {
+    uint64_t excl = 0;
+    int64_t end = tile - 1;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        const int64_t j = end - lane;
+        uint64_t st = j >= 0 ? ld_state(state + j) : kFlagPrefix;
+        while (true) {
+            const bool pending = (st >> 62) == 0;
+            if (!__any_sync(0xffffffffu, pending)) break;
+            // lane 0's clock decides, so the whole warp leaves together
+            const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > wait_ns, 0);
+            if (expired) {
+                timed_out = true;
+                if (pending) st = kFlagAgg;   // unknown predecessor counts as 0
+                break;
+            }
+            if (backoff_ns) __nanosleep(backoff_ns);
+            if (pending) st = ld_state(state + j);
+        }
+        const unsigned prefix_lanes = __ballot_sync(0xffffffffu, (st >> 62) == 2);
+        const int last = prefix_lanes ? __ffs(prefix_lanes) - 1 : 31;
+        uint64_t v = lane <= last ? (st & kValueMask) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        excl += v;
+        if (prefix_lanes) break;
+        end -= 32;
+    }
+    return excl;
+}
+
 // bf16 bit pattern -> fp32 (exact).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -23,29 +23,6 @@ constexpr int kWarpSpan = 32 * kItems;             // 512 elements per warp
 constexpr int kTileElems = kWarpsPerBlock * kWarpSpan;   // 4096 elements per CTA tile
 constexpr size_t kWsHeader = 64;                   // tile counter + padding
 
-constexpr uint64_t kFlagAgg = 1ull << 62;
-constexpr uint64_t kFlagPrefix = 2ull << 62;
-constexpr uint64_t kValueMask = (1ull << 62) - 1;
-
-// The look-back state word carries its own value (flag + count), and no
-// other data is published through it, so relaxed single-copy-atomic 64-bit
-// accesses at GPU scope are enough (no acquire/release fences).
-__device__ __forceinline__ uint64_t ld_state(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_state(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 struct MaskArgs {
     int64_t n;
     uint64_t seed_t;
@@ -77,34 +54,8 @@ struct MaskArgs {
 __device__ uint64_t walk_back(const MaskArgs& a, int64_t tile, uint64_t agg, int lane) {
     const bool publish = tile != a.withhold_tile;
     if (tile == 0) return 0;
-    uint64_t excl = 0;
-    int64_t end = tile - 1;
-    const uint64_t t0 = global_ns();
     bool timed_out = false;
-    while (true) {
-        const int64_t j = end - lane;
-        uint64_t st = j >= 0 ? ld_state(a.state + j) : kFlagPrefix;
-        while (true) {
-            const bool pending = (st >> 62) == 0;
-            if (!__any_sync(0xffffffffu, pending)) break;
-            // lane 0's clock decides, so the whole warp leaves together
-            const bool expired = __shfl_sync(0xffffffffu, global_ns() - t0 > a.wait_ns, 0);
-            if (expired) {
-                timed_out = true;
-                if (pending) st = kFlagAgg;   // unknown predecessor counts as 0
-                break;
-            }
-            if (pending) st = ld_state(a.state + j);
-        }
-        const unsigned prefix_lanes = __ballot_sync(0xffffffffu, (st >> 62) == 2);
-        const int last = prefix_lanes ? __ffs(prefix_lanes) - 1 : 31;
-        uint64_t v = lane <= last ? (st & kValueMask) : 0;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        excl += v;
-        if (prefix_lanes) break;
-        end -= 32;
-    }
+    const uint64_t excl = lookback_exclusive(a.state, tile, lane, a.wait_ns, 0u, timed_out);
     if (lane == 0) {
         if (publish) st_state(a.state + tile, kFlagPrefix | (excl + agg));
         if (timed_out) atomicExch(a.d_status, GC_ERR_TIMEOUT);

@@ -365,9 +365,15 @@ GC_API int qsgd_step(const float *const *grads, int W, int64_t n, int bucket, in
  *                  least qsgd_elias_max_words(n, bucket, s_levels)
  *   offsets        device uint32 [ceil(n/bucket) + 1], written
  *   workspace      device, qsgd_elias_workspace_bytes(n, bucket) bytes
- *                  (contents need not be preserved between calls)
- * Two kernel launches and one memset on `stream`; the total length is
- * offsets[nbuckets] on the device.
+ *                  (contents need not be preserved between calls); after
+ *                  the call its first 4 bytes hold the device status: GC_OK,
+ *                  or GC_ERR_TIMEOUT when a wait of the look-back below ran
+ *                  out (only a fault elsewhere can delay a CTA that long;
+ *                  the stream is then not valid)
+ * One memset and one kernel launch on `stream`; the kernel reads the codes
+ * once: each bucket's first word comes from a decoupled look-back (Merrill
+ * and Garland 2016) over the word counts of the buckets before it.  The
+ * total length is offsets[nbuckets] on the device.
  * Errors: GC_ERR_INVALID (bad bucket or s_levels, n < 0, NULL, workspace too
  * small, a bound above 2^32 - 1 words), GC_ERR_CAPACITY (capacity_words below
  * the bound), GC_ERR_ALIGN, GC_ERR_CUDA.

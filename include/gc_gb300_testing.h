@@ -46,6 +46,24 @@ GC_API int gc_testing_saps_round_one_pass(int64_t n, double p, uint64_t seed_t,
                                           size_t workspace_bytes, int *d_status,
                                           gc_stream_t stream);
 
+/*
+ * gc_testing_qsgd_elias_encode_withhold -- qsgd_elias_encode in which bucket
+ * `withhold_bucket` never publishes its look-back state (word count or
+ * prefix), and every look-back wait is bounded by `wait_ns` nanoseconds
+ * (1 .. 10^9).  The buckets after it wait out their bound, count it as
+ * empty, record GC_ERR_TIMEOUT in the workspace's status word and finish;
+ * the kernel returns and the CUDA context stays usable.  Arguments otherwise
+ * as qsgd_elias_encode ("QSGD ...", Knowl 2; the bounded look-back).
+ * Errors: as qsgd_elias_encode, and GC_ERR_INVALID for wait_ns out of range
+ * or a negative bucket.
+ */
+GC_API int gc_testing_qsgd_elias_encode_withhold(const uint8_t *codes, const float *norms,
+                                                 int64_t n, int bucket, int s_levels,
+                                                 uint32_t *words, uint64_t capacity_words,
+                                                 uint32_t *offsets, void *workspace,
+                                                 size_t ws_bytes, int64_t withhold_bucket,
+                                                 uint64_t wait_ns, gc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

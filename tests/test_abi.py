@@ -147,6 +147,11 @@ def test_elias_sizes_and_validation():
     assert _call(m, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, MISALIGNED, FAKE, ws, None) == gc.GC_ERR_ALIGN
     assert _call(m, FAKE, FAKE, 10_000, 500, 7, FAKE, cap, FAKE, FAKE, FAKE, ws, None) == gc.GC_ERR_INVALID
     assert _call(m, FAKE, FAKE, 10_000, 512, 7, FAKE, cap - 1, FAKE, FAKE, FAKE, ws, None) == gc.GC_ERR_CAPACITY
+    t = "gc_testing_qsgd_elias_encode_withhold"
+    assert _call(t, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, FAKE, ws, 3, 0, None) == gc.GC_ERR_INVALID
+    assert _call(t, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, FAKE, ws, 3, 2_000_000_000, None) == gc.GC_ERR_INVALID
+    assert _call(t, FAKE, FAKE, 10_000, 512, 7, FAKE, cap, FAKE, FAKE, ws, -1, 1000, None) == gc.GC_ERR_INVALID
+    assert _call(t, FAKE, FAKE, 10_000, 512, 7, FAKE, cap - 1, FAKE, FAKE, ws, 3, 1000, None) == gc.GC_ERR_CAPACITY
     q = "qsgd_elias_decode_quarters"
     assert _call(q, FAKE, FAKE, None, 10_000, 512, 7, FAKE, FAKE, None, None) == gc.GC_ERR_INVALID
     assert _call(q, FAKE, FAKE, MISALIGNED, 10_000, 512, 7, FAKE, FAKE, None, None) == gc.GC_ERR_ALIGN
