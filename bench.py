@@ -687,7 +687,7 @@ def rows(args, dev, peak):
         bits = {"bits_per_coord": round(32 * total / n, 4),
                 "bits_per_coord_with_offsets": round(32 * (total + nb + 1) / n, 4),
                 "issue": issue_roofline(f"elias_encode_s{s}", tm.ms("e"))}
-        out[f"{qcfg.name}.elias_encode"] = _row(qcfg.name, "qsgd_elias_encode (count + encode)",
+        out[f"{qcfg.name}.elias_encode"] = _row(qcfg.name, "qsgd_elias_encode (one pass, look-back)",
                                                 cb + 4 * nb + 4 * total + 4 * (nb + 1), tm.ms("e"), peak, n,
                                                 bits)
         out[f"{qcfg.name}.elias_decode"] = _row(qcfg.name, "qsgd_elias_decode",
@@ -706,7 +706,7 @@ def rows(args, dev, peak):
         torch.cuda.synchronize(dev)
         total0 = int(offs[0][nb].item())
         out[f"{qcfg.name}.elias_encode_marked"] = _row(
-            qcfg.name, "qsgd_elias_encode_marked (count + encode + quarter marks)",
+            qcfg.name, "qsgd_elias_encode_marked (one pass + quarter marks)",
             cb + 4 * nb + 4 * total0 + 4 * (nb + 1) + 6 * nb, tm.ms("me"), peak, n,
             {"marks_bits_per_coord": round(48 * nb / n, 4)})
         out[f"{qcfg.name}.elias_decode_quarters"] = _row(
@@ -1140,11 +1140,11 @@ def run_case(name: str, n: int):
         offs = torch.empty(nb + 1, dtype=torch.int32, device=dev)
         ews = torch.empty(gc.qsgd_elias_workspace_bytes(n, 512), dtype=torch.uint8, device=dev)
         gc.qsgd_elias_encode(c, nm, n, 512, s, words, offs, ews)
-        # the encoders read the codes twice (count, then encode); each call
-        # starts from an L2 filled with other (clean) data -- a read of a
-        # buffer larger than L2, no write-back to come -- so that a capture
-        # without cache control sees the first read come from DRAM and the
-        # second from wherever it does in a real call
+        # each encoder call starts from an L2 filled with other (clean) data
+        # -- a read of a buffer larger than L2, no write-back to come -- so
+        # that a capture without cache control sees the codes come from DRAM
+        # (the sparse encoder reads them twice, count then encode: the second
+        # read from wherever it comes in a real call)
         flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
         flush_l2 = lambda buf: buf.sum()
         if name.startswith("elias_sparse"):
