@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kChunk = 64;                          // buckets per CTA
 constexpr int kEncodeStageWords = 9216;             // the dense encoder's staging per CTA, at most
+constexpr int kSparseStageWords = 9600;             // the sparse encoder's
 constexpr size_t kTicketBytes = 16;
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -47,24 +48,6 @@ inline int64_t bucket_max_words(int64_t len, bool four) {
     return 1 + div_up(len * max_code_bits(four), 32);
 }
 
-struct Ws {
-    uint32_t* ticket;
-    uint32_t* chunk;    // [nchunks + 1]: per-CTA word totals, then their exclusive prefix
-    uint32_t* counts;   // [nbuckets]: words of each bucket
-};
-
-inline size_t chunk_bytes(int64_t nchunks) {
-    return static_cast<size_t>(div_up((nchunks + 1) * 4, 16) * 16);
-}
-
-Ws ws_layout(void* ws, int64_t nchunks) {
-    char* p = static_cast<char*>(ws);
-    Ws w;
-    w.ticket = reinterpret_cast<uint32_t*>(p);
-    w.chunk = reinterpret_cast<uint32_t*>(p + kTicketBytes);
-    w.counts = reinterpret_cast<uint32_t*>(p + kTicketBytes + chunk_bytes(nchunks));
-    return w;
-}
 
 // ---------------------------------------------------------------- codewords
 
@@ -233,6 +216,54 @@ EncodeWs encode_ws(void* ws) {
                     reinterpret_cast<uint64_t*>(p + kTicketBytes)};
 }
 
+// Once every bucket of the CTA's chunk is staged (s_nw[lb] = its words), by
+// warp 0: publishes the chunk's word count, takes the chunk's first word from
+// the look-back over the chunks before it (Merrill and Garland's decoupled
+// look-back, bounded: a wait that runs out records GC_ERR_TIMEOUT in the
+// workspace), then its inclusive prefix; writes each bucket's first word to
+// offsets and to s_nw, the stream's length when this is the last chunk, and
+// the chunk's end to *s_end.  At most 64 buckets per chunk.
+__device__ __forceinline__ void chunk_offsets(const EncodeWs& ws, int64_t chunk, int64_t b0, int nbc,
+                                              int64_t nbuckets, uint32_t* offsets, uint32_t* s_nw,
+                                              uint32_t* s_end, uint64_t wait_ns, int64_t withhold, int lane) {
+    const uint32_t c0 = 2 * lane < nbc ? s_nw[2 * lane] : 0u;
+    const uint32_t c1 = 2 * lane + 1 < nbc ? s_nw[2 * lane + 1] : 0u;
+    const uint32_t incl = static_cast<uint32_t>(warp_incl_sum(static_cast<int>(c0 + c1), lane));
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    const bool publish = chunk != withhold;
+    if (lane == 0 && publish) st_state(ws.state + chunk, (chunk == 0 ? kFlagPrefix : kFlagAgg) | total);
+    bool timed_out = false;
+    const uint64_t base = chunk == 0 ? 0 : lookback_exclusive(ws.state, chunk, lane, wait_ns, 0u, timed_out);
+    if (lane == 0) {
+        if (chunk != 0 && publish) st_state(ws.state + chunk, kFlagPrefix | (base + total));
+        if (timed_out) atomicExch(ws.status, GC_ERR_TIMEOUT);
+        if (b0 + nbc == nbuckets) offsets[nbuckets] = static_cast<uint32_t>(base) + total;
+        *s_end = static_cast<uint32_t>(base) + total;
+    }
+    const uint32_t o0 = static_cast<uint32_t>(base) + incl - c0 - c1;
+    if (2 * lane < nbc) {
+        s_nw[2 * lane] = o0;
+        offsets[b0 + 2 * lane] = o0;
+    }
+    if (2 * lane + 1 < nbc) {
+        s_nw[2 * lane + 1] = o0 + c0;
+        offsets[b0 + 2 * lane + 1] = o0 + c0;
+    }
+}
+
+// Writes the chunk's staged buckets to the stream: warp w takes buckets w,
+// w + 8, ..., each from its first word (s_nw) to the next bucket's, coalesced.
+__device__ __forceinline__ void write_chunk(const uint32_t* stages, int stride, const uint32_t* s_nw,
+                                            uint32_t chunk_end, int nbc, uint32_t* words, int warp, int lane) {
+    for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
+        const uint32_t off = s_nw[lb];
+        const uint32_t nw = (lb + 1 < nbc ? s_nw[lb + 1] : chunk_end) - off;
+        const uint32_t* st = stages + lb * stride;
+        uint32_t* dst = words + off;
+        for (uint32_t k = lane; k < nw; k += 32) dst[k] = st[k];
+    }
+}
+
 
 struct EncodeArgs {
     const uint8_t* codes;
@@ -387,45 +418,10 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
         if (lane == 0) s_nw[lb] = (pos + 31) >> 5;
     }
     __syncthreads();
-    if (warp == 0) {
-        // the chunk's words, published at once; the buckets' first words
-        // within it; then the chunk's first word from the look-back
-        const uint32_t c0 = 2 * lane < nbc ? s_nw[2 * lane] : 0u;
-        const uint32_t c1 = 2 * lane + 1 < nbc ? s_nw[2 * lane + 1] : 0u;
-        const uint32_t incl = static_cast<uint32_t>(warp_incl_sum(static_cast<int>(c0 + c1), lane));
-        const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
-        const bool publish = chunk != a.withhold;
-        if (lane == 0 && publish) st_state(a.ws.state + chunk, (chunk == 0 ? kFlagPrefix : kFlagAgg) | total);
-        bool timed_out = false;
-        const uint64_t base =
-            chunk == 0 ? 0 : lookback_exclusive(a.ws.state, chunk, lane, a.wait_ns, 0u, timed_out);
-        if (lane == 0) {
-            if (chunk != 0 && publish) st_state(a.ws.state + chunk, kFlagPrefix | (base + total));
-            if (timed_out) atomicExch(a.ws.status, GC_ERR_TIMEOUT);
-            if (b0 + nbc == a.nbuckets) a.offsets[a.nbuckets] = static_cast<uint32_t>(base) + total;
-            s_end = static_cast<uint32_t>(base) + total;
-        }
-        const uint32_t o0 = static_cast<uint32_t>(base) + incl - c0 - c1;
-        if (2 * lane < nbc) {
-            s_nw[2 * lane] = o0;
-            a.offsets[b0 + 2 * lane] = o0;
-        }
-        if (2 * lane + 1 < nbc) {
-            s_nw[2 * lane + 1] = o0 + c0;
-            a.offsets[b0 + 2 * lane + 1] = o0 + c0;
-        }
-    }
+    if (warp == 0)
+        chunk_offsets(a.ws, chunk, b0, nbc, a.nbuckets, a.offsets, s_nw, &s_end, a.wait_ns, a.withhold, lane);
     __syncthreads();
-    // each warp writes out buckets warp, warp + 8, ...: the stream words
-    // from the bucket's first word to the next bucket's, coalesced
-    const uint32_t chunk_end = s_end;
-    for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
-        const uint32_t off = s_nw[lb];
-        const uint32_t nw = (lb + 1 < nbc ? s_nw[lb + 1] : chunk_end) - off;
-        const uint32_t* st = stages + lb * a.stage_stride;
-        uint32_t* dst = a.words + off;
-        for (uint32_t k = lane; k < nw; k += 32) dst[k] = st[k];
-    }
+    write_chunk(stages, a.stage_stride, s_nw, s_end, nbc, a.words, warp, lane);
 }
 
 // ---------------------------------------------------------------- decode
@@ -886,11 +882,11 @@ int decode_stage_words(uint32_t* cap) {
 // Same stream conventions as the dense code above (most significant bit
 // first, buckets on word boundaries, an offsets table).
 //
-// Encode = count + encode launches as for the dense code: one warp per
-// bucket, lane l owning coordinates [l d/32, (l+1) d/32); a lane's distances
-// need the last non-zero coordinate before its range, which a warp max-scan
-// supplies.  Decode: one thread per bucket, after its CTA has zeroed the
-// code bytes of its buckets.
+// Encode = one launch, as the dense code (chunks by ticket, a chunk-level
+// look-back): one warp per bucket, lane l owning coordinates
+// [l d/32, (l+1) d/32); a lane's distances need the last non-zero coordinate
+// before its range, which a warp max-scan supplies.  Decode: one thread per
+// bucket, after its CTA has zeroed the code bytes of its buckets.
 
 // Length of Elias-omega(N), N >= 1.
 __device__ __forceinline__ int omega_len(uint32_t N) {
@@ -1043,99 +1039,35 @@ struct SparseArgs {
     int d;
     int64_t nbuckets;
     bool levels;          // s >= 2
-    Ws ws;
     uint32_t* words;
     uint32_t* offsets;
-    int stage_words;      // staging words per warp
+    int stage_words;      // staging words per bucket
+    int chunk;            // buckets per CTA (<= kChunk), all staged at once
+    EncodeWs ws;
+    uint64_t wait_ns;     // bound on each look-back wait
 };
 
-// Count: words of each bucket and the exclusive prefix of the per-CTA totals
-// (the last CTA to finish turns the totals into it, as k_elias_count does).
-template <bool FOUR>
-__global__ void __launch_bounds__(kThreads) k_elias_sparse_count(SparseArgs a) {
-    __shared__ uint32_t wsum[kWarpsPerBlock];
-    __shared__ uint32_t lut[kOmegaLut];
-    __shared__ bool is_last;
-    build_omega_lut(lut);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
-    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
-    uint32_t mine = 0;
-    for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
-        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b0 + lb, a.levels, lane, lut);
-        const uint32_t nw = (sb.total + 31u) >> 5;
-        if (lane == 0) a.ws.counts[b0 + lb] = nw;
-        mine += nw;
-    }
-    if (lane == 0) wsum[warp] = mine;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t t = 0;
-        for (int w = 0; w < kWarpsPerBlock; ++w) t += wsum[w];
-        a.ws.chunk[blockIdx.x] = t;
-        __threadfence();
-        is_last = atomicAdd(a.ws.ticket, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    const int nchunks = static_cast<int>(gridDim.x);
-    const int per = (nchunks + kThreads - 1) / kThreads;
-    const int lo = threadIdx.x * per;
-    const int hi = lo + per < nchunks ? lo + per : nchunks;
-    uint32_t run = 0;
-    for (int i = lo; i < hi; ++i) run += __ldcg(a.ws.chunk + i);
-    const int incl = warp_incl_sum(static_cast<int>(run), lane);
-    __syncthreads();
-    if (lane == 31) wsum[warp] = static_cast<uint32_t>(incl);
-    __syncthreads();
-    uint32_t before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarpsPerBlock; ++w) {
-        before += w < warp ? wsum[w] : 0u;
-        total += wsum[w];
-    }
-    uint32_t acc = before + static_cast<uint32_t>(incl) - run;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t v = __ldcg(a.ws.chunk + i);
-        a.ws.chunk[i] = acc;
-        acc += v;
-    }
-    if (threadIdx.x == 0) {
-        a.ws.chunk[nchunks] = total;
-        *a.ws.ticket = 0u;
-    }
-}
-
-// Encode: each warp assembles one bucket at a time in its shared staging
-// words (shared-memory atomicOr of each entry's bits) and copies it out.
+// Encode, one launch: each CTA takes a chunk of buckets by ticket, each warp
+// assembles buckets warp, warp + 8, ... of it in the chunk's shared staging
+// (shared-memory atomicOr of each entry's bits), and the chunk goes out
+// after a look-back over the chunks before it, as in the dense encoder.
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) {
     extern __shared__ uint32_t smem[];
-    uint32_t* lut = smem;                        // [kOmegaLut]
-    uint32_t* offs = smem + kOmegaLut;           // [kChunk]
-    uint32_t* stages = smem + kOmegaLut + kChunk;   // [kWarpsPerBlock][stage_words]
+    __shared__ uint32_t s_chunk, s_end;
+    __shared__ uint32_t s_nw[kChunk];             // words of each bucket, then its first word
+    uint32_t* lut = smem;                         // [kOmegaLut]
+    uint32_t* stages = smem + kOmegaLut;          // [chunk][stage_words]
     build_omega_lut(lut);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kChunk;
-    for (int i = threadIdx.x; i < kWarpsPerBlock * a.stage_words; i += kThreads) stages[i] = 0u;
-    if (warp == 0) {
-        const int64_t ba = b0 + 2 * lane, bb = ba + 1;
-        const uint32_t c0 = ba < a.nbuckets ? a.ws.counts[ba] : 0u;
-        const uint32_t c1 = bb < a.nbuckets ? a.ws.counts[bb] : 0u;
-        const int incl = warp_incl_sum(static_cast<int>(c0 + c1), lane);
-        const uint32_t o0 = a.ws.chunk[blockIdx.x] + static_cast<uint32_t>(incl) - c0 - c1;
-        offs[2 * lane] = o0;
-        offs[2 * lane + 1] = o0 + c0;
-        if (ba < a.nbuckets) a.offsets[ba] = o0;
-        if (bb < a.nbuckets) a.offsets[bb] = o0 + c0;
-        if (blockIdx.x == gridDim.x - 1 && lane == 0) a.offsets[a.nbuckets] = a.ws.chunk[gridDim.x];
-    }
+    for (int i = threadIdx.x; i < a.chunk * a.stage_words; i += kThreads) stages[i] = 0u;
+    if (threadIdx.x == 0) s_chunk = atomicAdd(a.ws.ticket, 1u);
     __syncthreads();
-    uint32_t* stage = stages + warp * a.stage_words;
-    const int nbc = static_cast<int>(a.nbuckets - b0 < kChunk ? a.nbuckets - b0 : kChunk);
+    const int64_t chunk = s_chunk;
+    const int64_t b0 = chunk * a.chunk;
+    const int nbc = static_cast<int>(a.nbuckets - b0 < a.chunk ? a.nbuckets - b0 : a.chunk);
     for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
+        uint32_t* stage = stages + lb * a.stage_words;
         const int64_t b = b0 + lb;
         const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b, a.levels, lane, lut);
         if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
@@ -1177,16 +1109,14 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
             uint32_t tpat;
             const int tlen = omega_lut(lut, static_cast<uint32_t>(sb.len - sb.last_all), &tpat);
             emit(stage, sb.total - static_cast<uint32_t>(tlen), tpat, tlen);
+            s_nw[lb] = (sb.total + 31u) >> 5;
         }
-        __syncwarp();
-        const int nw = static_cast<int>((sb.total + 31u) >> 5);
-        uint32_t* dst = a.words + offs[lb];
-        for (int k = lane; k < nw; k += 32) {
-            dst[k] = stage[k];
-            stage[k] = 0u;
-        }
-        __syncwarp();
     }
+    __syncthreads();
+    if (warp == 0)
+        chunk_offsets(a.ws, chunk, b0, nbc, a.nbuckets, a.offsets, s_nw, &s_end, a.wait_ns, -1, lane);
+    __syncthreads();
+    write_chunk(stages, a.stage_words, s_nw, s_end, nbc, a.words, warp, lane);
 }
 
 // Decode: a thread per bucket, in the dense decoder's way.  The CTA zeroes
@@ -1403,12 +1333,7 @@ uint64_t qsgd_elias_max_words(int64_t n, int bucket, int s_levels) {
 
 size_t qsgd_elias_workspace_bytes(int64_t n, int bucket) {
     if (n < 0 || !valid_bucket(bucket)) return 0;
-    const int64_t nb = div_up(n, bucket), nchunks = div_up(nb, kChunk);
-    // the dense encoder's header and look-back states, or the sparse
-    // encoder's ticket, chunk totals and bucket counts
-    const size_t sparse = kTicketBytes + chunk_bytes(nchunks) + static_cast<size_t>(div_up(nb * 4, 16) * 16);
-    const size_t dense = encode_ws_bytes(nb);
-    return sparse > dense ? sparse : dense;
+    return encode_ws_bytes(div_up(n, bucket));
 }
 
 }  // extern "C"
@@ -1586,20 +1511,22 @@ int qsgd_elias_encode_sparse(const uint8_t* codes, const float* norms, int64_t n
         !aligned16(offsets) || (workspace && !aligned16(workspace)))
         return GC_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (n == 0) return cudaMemsetAsync(offsets, 0, sizeof(uint32_t), s) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    if (n == 0) {
+        if (workspace && cudaMemsetAsync(workspace, 0, kTicketBytes, s) != cudaSuccess) return GC_ERR_CUDA;
+        return cudaMemsetAsync(offsets, 0, sizeof(uint32_t), s) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    }
     const bool four = s_levels <= 7;
-    const int64_t nb = div_up(n, bucket), nchunks = div_up(nb, kChunk);
-    const Ws ws = ws_layout(workspace, nchunks);
-    if (cudaMemsetAsync(ws.ticket, 0, kTicketBytes, s) != cudaSuccess) return GC_ERR_CUDA;
-    SparseArgs a{codes, norms, n, bucket, nb, s_levels >= 2, ws, words, offsets,
-                 static_cast<int>(sparse_bucket_max_words(bucket)) + 2};
+    const int64_t nb = div_up(n, bucket);
+    const int stride = static_cast<int>(sparse_bucket_max_words(bucket)) + 2;
+    // buckets per CTA: as many as 37.5 KB of staging holds, at most 64
+    const int chunk = static_cast<int>(kSparseStageWords / stride < kChunk ? kSparseStageWords / stride : kChunk);
+    const int64_t nchunks = div_up(nb, chunk);
+    if (cudaMemsetAsync(workspace, 0, kTicketBytes + static_cast<size_t>(nchunks) * 8, s) != cudaSuccess)
+        return GC_ERR_CUDA;
+    SparseArgs a{codes, norms, n, bucket, nb, s_levels >= 2, words, offsets, stride, chunk, encode_ws(workspace),
+                 kEncodeWaitNs};
+    const size_t smem = sizeof(uint32_t) * (kOmegaLut + static_cast<size_t>(chunk) * stride);
     const unsigned grid = static_cast<unsigned>(nchunks);
-    if (four)
-        k_elias_sparse_count<true><<<grid, kThreads, 0, s>>>(a);
-    else
-        k_elias_sparse_count<false><<<grid, kThreads, 0, s>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
-    const size_t smem = sizeof(uint32_t) * (kOmegaLut + kChunk + static_cast<size_t>(kWarpsPerBlock) * a.stage_words);
     if (four)
         k_elias_sparse_encode<true><<<grid, kThreads, smem, s>>>(a);
     else

@@ -483,9 +483,12 @@ GC_API int qsgd_elias_decode_quarters(const uint32_t *words, const uint32_t *off
  * Worth it where most levels are 0 (s = 1, small s on peaked gradients).
  *
  *   codes, norms, n, bucket, s_levels, offsets, workspace, ws_bytes
- *                  as qsgd_elias_encode (same workspace size)
+ *                  as qsgd_elias_encode (same workspace size, same status
+ *                  word in its first 4 bytes after the call)
  *   words          device uint32 [capacity_words], at least
  *                  qsgd_elias_sparse_max_words(n, bucket)
+ * One memset and one kernel launch on `stream` (the codes are read once, as
+ * in qsgd_elias_encode).
  * Errors: GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CAPACITY, GC_ERR_CUDA.
  */
 GC_API int qsgd_elias_encode_sparse(const uint8_t *codes, const float *norms, int64_t n,
