@@ -729,7 +729,7 @@ def rows(args, dev, peak):
         torch.cuda.synchronize(dev)
         stotal = int(soffs[nb].item())
         out[f"{qcfg.name}.elias_sparse_encode"] = _row(
-            qcfg.name, "qsgd_elias_encode_sparse (count + encode)", cb + 4 * nb + 4 * stotal + 4 * (nb + 1),
+            qcfg.name, "qsgd_elias_encode_sparse (one pass, look-back)", cb + 4 * nb + 4 * stotal + 4 * (nb + 1),
             tm.ms("se"), peak, n, {"bits_per_coord": round(32 * stotal / n, 4)})
         out[f"{qcfg.name}.elias_sparse_decode"] = _row(
             qcfg.name, "qsgd_elias_decode_sparse", 4 * stotal + 4 * (nb + 1) + cb + 4 * nb, tm.ms("sd"), peak, n)
@@ -1143,8 +1143,6 @@ def run_case(name: str, n: int):
         # each encoder call starts from an L2 filled with other (clean) data
         # -- a read of a buffer larger than L2, no write-back to come -- so
         # that a capture without cache control sees the codes come from DRAM
-        # (the sparse encoder reads them twice, count then encode: the second
-        # read from wherever it comes in a real call)
         flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)
         flush_l2 = lambda buf: buf.sum()
         if name.startswith("elias_sparse"):
