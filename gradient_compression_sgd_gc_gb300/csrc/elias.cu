@@ -888,16 +888,6 @@ int decode_stage_words(uint32_t* cap) {
 // before its range, which a warp max-scan supplies.  Decode: one thread per
 // bucket, after its CTA has zeroed the code bytes of its buckets.
 
-// Length of Elias-omega(N), N >= 1.
-__device__ __forceinline__ int omega_len(uint32_t N) {
-    int len = 1;
-    while (N > 1) {
-        const int L = 32 - __clz(N);
-        len += L;
-        N = static_cast<uint32_t>(L - 1);
-    }
-    return len;
-}
 
 // Elias-omega codewords of 1..255 as (pattern << 5) | length (at most 14
 // bits), built per CTA in shared memory; longer values take omega().
@@ -911,9 +901,6 @@ __device__ __forceinline__ void build_omega_lut(uint32_t* lut) {
     }
 }
 
-__device__ __forceinline__ int omega_len_lut(const uint32_t* lut, uint32_t N) {
-    return N < kOmegaLut ? static_cast<int>(lut[N] & 31u) : omega_len(N);
-}
 
 __device__ __forceinline__ int omega_lut(const uint32_t* lut, uint32_t N, uint32_t* pat) {
     if (N < kOmegaLut) {
@@ -943,31 +930,22 @@ __device__ __forceinline__ void code_at(const uint8_t* codes, int64_t i, uint32_
     }
 }
 
-// The warp's view of one bucket: each lane's coded bits (its first distance
-// included), the last non-zero coordinate before each lane's range, and the
-// bucket's total bits.
-struct SparseBucket {
-    int64_t lo;          // first coordinate of the bucket
-    int len, c0, c1;     // bucket length; this lane's range [c0, c1)
-    int before;          // last non-zero coordinate before c0, or -1
-    int last_all;        // last non-zero coordinate of the bucket, or -1
-    uint32_t lane_bits;  // this lane's bits
-    uint32_t lane_pos;   // this lane's first bit within the bucket
-    uint32_t total;      // the bucket's bits, norm and closing distance included
-};
-
-// Calls f(c, sign, level) for each coordinate c in [c0, c1) of the bucket
-// starting at coordinate lo whose level is not 0, in order.  A whole bucket's
-// lane range is read a word (or, for 2-byte lane ranges, a half-word) at a
-// time and only non-zero codes are visited; the ragged last bucket reads
-// byte by byte so that nothing past the codes is touched.
-template <bool FOUR, typename F>
-__device__ __forceinline__ void for_nonzero(const uint8_t* codes, int64_t lo, int c0, int c1, bool whole, F f) {
+// Walks the codes of coordinates [c0, c1) of the bucket starting at
+// coordinate lo.  A whole bucket's range is read a word (or, for 2-byte
+// ranges, a half-word) at a time: word(k, w, nz) gets the word's first
+// coordinate k (relative to c0), the word with element e in field e (low
+// field first) and the mask of its non-zero fields (bit 0 of each 4-bit
+// field, bit 7 of each byte); the ragged last bucket is read byte by byte,
+// so that nothing past the codes is touched, and code(c) is called for each
+// of its non-zero coordinates.
+template <bool FOUR, typename Fw, typename Fc>
+__device__ __forceinline__ void for_nonzero_words(const uint8_t* codes, int64_t lo, int c0, int c1, bool whole,
+                                                  Fw word, Fc code) {
     if (!whole) {
         for (int c = c0; c < c1; ++c) {
             uint32_t sg, lv;
             code_at<FOUR>(codes, lo + c, sg, lv);
-            if (lv) f(c, sg, lv);
+            if (lv) code(c);
         }
         return;
     }
@@ -987,49 +965,40 @@ __device__ __forceinline__ void for_nonzero(const uint8_t* codes, int64_t lo, in
         } else {
             nz = ((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) & 0x80808080u;
         }
-        while (nz) {
-            const int bit = __ffs(nz) - 1;
-            nz &= nz - 1;
-            const int e = FOUR ? (bit >> 2) : (bit >> 3);
-            const uint32_t code = FOUR ? (w >> (4 * e)) & 15u : (w >> (8 * e)) & 255u;
-            f(c0 + k + e, FOUR ? code >> 3 : code >> 7, FOUR ? code & 7u : code & 127u);
-        }
+        word(k, w, nz);
     }
 }
 
+// Calls f(c, sign, level) for each coordinate c in [c0, c1) of the bucket
+// starting at coordinate lo whose level is not 0, in order.
+template <bool FOUR, typename F>
+__device__ __forceinline__ void for_nonzero(const uint8_t* codes, int64_t lo, int c0, int c1, bool whole, F f) {
+    for_nonzero_words<FOUR>(
+        codes, lo, c0, c1, whole,
+        [&](int k, uint32_t w, uint32_t nz) {
+            while (nz) {
+                const int bit = __ffs(nz) - 1;
+                nz &= nz - 1;
+                const int e = FOUR ? (bit >> 2) : (bit >> 3);
+                const uint32_t cd = FOUR ? (w >> (4 * e)) & 15u : (w >> (8 * e)) & 255u;
+                f(c0 + k + e, FOUR ? cd >> 3 : cd >> 7, FOUR ? cd & 7u : cd & 127u);
+            }
+        },
+        [&](int c) {
+            uint32_t sg, lv;
+            code_at<FOUR>(codes, lo + c, sg, lv);
+            f(c, sg, lv);
+        });
+}
+
+// Non-zero codes among coordinates [c0, c1) of the bucket at lo: one
+// population count per code word of a whole bucket.
 template <bool FOUR>
-__device__ SparseBucket sparse_bucket(const uint8_t* codes, int64_t n, int d, int64_t b, bool levels, int lane,
-                                      const uint32_t* lut) {
-    SparseBucket r;
-    r.lo = b * d;
-    r.len = static_cast<int>(n - r.lo < d ? n - r.lo : static_cast<int64_t>(d));
-    const int cpl = d / 32;
-    r.c0 = min(r.len, lane * cpl);
-    r.c1 = min(r.len, r.c0 + cpl);
-    int first = -1, prev = -1;
-    uint32_t bits = 0;
-    for_nonzero<FOUR>(codes, r.lo, r.c0, r.c1, r.len == d, [&](int c, uint32_t, uint32_t lv) {
-        if (prev >= 0) bits += omega_len_lut(lut, static_cast<uint32_t>(c - prev));
-        else first = c;
-        bits += 1 + (levels ? omega_len_lut(lut, lv) : 0);
-        prev = c;
-    });
-    int incl = prev;      // inclusive max-scan of the lanes' last non-zero coordinates
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl = max(incl, t);
-    }
-    const int excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    r.before = lane ? excl : -1;
-    r.last_all = __shfl_sync(0xffffffffu, incl, 31);
-    if (first >= 0) bits += omega_len_lut(lut, static_cast<uint32_t>(first - r.before));
-    r.lane_bits = bits;
-    const int in = warp_incl_sum(static_cast<int>(bits), lane);
-    r.lane_pos = 32u + static_cast<uint32_t>(in) - bits;
-    const uint32_t all = static_cast<uint32_t>(__shfl_sync(0xffffffffu, in, 31));
-    r.total = 32u + all + static_cast<uint32_t>(omega_len_lut(lut, static_cast<uint32_t>(r.len - r.last_all)));
-    return r;
+__device__ __forceinline__ int count_nonzero(const uint8_t* codes, int64_t lo, int c0, int c1, bool whole) {
+    int cnt = 0;
+    for_nonzero_words<FOUR>(codes, lo, c0, c1, whole, [&](int, uint32_t, uint32_t nz) { cnt += __popc(nz); },
+                            [&](int) { ++cnt; });
+    return cnt;
 }
 
 struct SparseArgs {
@@ -1047,10 +1016,16 @@ struct SparseArgs {
     uint64_t wait_ns;     // bound on each look-back wait
 };
 
-// Encode, one launch: each CTA takes a chunk of buckets by ticket, each warp
-// assembles buckets warp, warp + 8, ... of it in the chunk's shared staging
-// (shared-memory atomicOr of each entry's bits), and the chunk goes out
-// after a look-back over the chunks before it, as in the dense encoder.
+// Encode, one launch: each CTA takes a chunk of buckets by ticket and the
+// chunk goes out after a look-back over the chunks before it, as in the dense
+// encoder.  A warp codes one bucket at a time, spreading its non-zero
+// coordinates over the lanes: each lane counts those in its range of d/32
+// coordinates (a population count per code word), a warp scan ranks them,
+// and each lane writes its (coordinate, code) entries to the warp's list in
+// shared memory in order; then rounds of 32 entries, one per lane, take
+// their distance from the entry before, their codeword bits from the table,
+// their bit position from a warp scan of the lengths, and are OR-ed into the
+// bucket's staging words.
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) {
     extern __shared__ uint32_t smem[];
@@ -1058,6 +1033,7 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
     __shared__ uint32_t s_nw[kChunk];             // words of each bucket, then its first word
     uint32_t* lut = smem;                         // [kOmegaLut]
     uint32_t* stages = smem + kOmegaLut;          // [chunk][stage_words]
+    uint32_t* lists = stages + a.chunk * a.stage_words;   // [kWarpsPerBlock][d]: (coordinate << 16) | code
     build_omega_lut(lut);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < a.chunk * a.stage_words; i += kThreads) stages[i] = 0u;
@@ -1066,51 +1042,52 @@ __global__ void __launch_bounds__(kThreads) k_elias_sparse_encode(SparseArgs a) 
     const int64_t chunk = s_chunk;
     const int64_t b0 = chunk * a.chunk;
     const int nbc = static_cast<int>(a.nbuckets - b0 < a.chunk ? a.nbuckets - b0 : a.chunk);
+    uint32_t* list = lists + warp * a.d;
+    const int cpl = a.d / 32;
     for (int lb = warp; lb < nbc; lb += kWarpsPerBlock) {
         uint32_t* stage = stages + lb * a.stage_words;
         const int64_t b = b0 + lb;
-        const SparseBucket sb = sparse_bucket<FOUR>(a.codes, a.n, a.d, b, a.levels, lane, lut);
-        if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
-        // This lane's bits fill [lane_pos, lane_pos + lane_bits): words are
-        // assembled in a register; a completed word is stored plainly unless
-        // it is the lane's first word and the previous lane's bits end in it,
-        // and the last, partial word is OR-ed (the next lane may share it).
-        uint32_t wi = sb.lane_pos >> 5;
-        int fill = static_cast<int>(sb.lane_pos & 31u);
-        const bool shared_first = fill != 0;
-        const uint32_t first_wi = wi;
-        uint32_t cur = 0u;
-        int prev = sb.before;
-        const bool levels = a.levels;
-        for_nonzero<FOUR>(a.codes, sb.lo, sb.c0, sb.c1, sb.len == a.d, [&](int c, uint32_t sg, uint32_t lv) {
-            uint32_t gpat, lpat = 0;
-            const int glen = omega_lut(lut, static_cast<uint32_t>(c - prev), &gpat);
-            const int llen = levels ? omega_lut(lut, lv, &lpat) : 0;
-            uint64_t piece = ((((static_cast<uint64_t>(gpat) << 1) | sg) << llen) | lpat);
-            int len = glen + 1 + llen;                       // <= 34
-            while (len > 0) {
-                const int t = min(len, 32 - fill);
-                const uint32_t top = static_cast<uint32_t>(piece >> (len - t)) & (0xFFFFFFFFu >> (32 - t));
-                cur |= top << (32 - fill - t);
-                fill += t;
-                len -= t;
-                if (fill == 32) {
-                    if (shared_first && wi == first_wi) atomicOr(stage + wi, cur);
-                    else stage[wi] = cur;
-                    ++wi;
-                    cur = 0u;
-                    fill = 0;
-                }
-            }
-            prev = c;
+        const int64_t lo = b * a.d;
+        const int len = static_cast<int>(a.n - lo < a.d ? a.n - lo : static_cast<int64_t>(a.d));
+        const bool whole = len == a.d;
+        const int c0 = min(len, lane * cpl), c1 = min(len, c0 + cpl);
+        // rank the non-zero coordinates, then list them in order
+        const int cnt = count_nonzero<FOUR>(a.codes, lo, c0, c1, whole);
+        const int incl = warp_incl_sum(cnt, lane);
+        const int K = __shfl_sync(0xffffffffu, incl, 31);
+        int r = incl - cnt;
+        for_nonzero<FOUR>(a.codes, lo, c0, c1, whole, [&](int c, uint32_t sg, uint32_t lv) {
+            list[r++] = (static_cast<uint32_t>(c) << 16) | (sg << 8) | lv;
         });
-        if (fill > 0) atomicOr(stage + wi, cur);
-        if (lane == 0) {
-            uint32_t tpat;
-            const int tlen = omega_lut(lut, static_cast<uint32_t>(sb.len - sb.last_all), &tpat);
-            emit(stage, sb.total - static_cast<uint32_t>(tlen), tpat, tlen);
-            s_nw[lb] = (sb.total + 31u) >> 5;
+        __syncwarp();
+        if (lane == 0) stage[0] = __float_as_uint(__ldg(a.norms + b));
+        uint32_t pos = 32;
+        for (int r0 = 0; r0 < K; r0 += 32) {
+            const int k = r0 + lane;
+            uint64_t piece = 0;
+            int plen = 0;
+            if (k < K) {
+                const uint32_t ent = list[k];
+                const int c = static_cast<int>(ent >> 16);
+                const int prev = k ? static_cast<int>(list[k - 1] >> 16) : -1;
+                uint32_t gpat, lpat = 0;
+                const int glen = omega_lut(lut, static_cast<uint32_t>(c - prev), &gpat);
+                const int llen = a.levels ? omega_lut(lut, ent & 255u, &lpat) : 0;
+                piece = (((static_cast<uint64_t>(gpat) << 1) | ((ent >> 8) & 1u)) << llen) | lpat;
+                plen = glen + 1 + llen;                      // <= 34
+            }
+            const int pin = warp_incl_sum(plen, lane);
+            emit(stage, pos + static_cast<uint32_t>(pin - plen), piece, plen);
+            pos += static_cast<uint32_t>(__shfl_sync(0xffffffffu, pin, 31));
         }
+        if (lane == 0) {
+            const int last = K ? static_cast<int>(list[K - 1] >> 16) : -1;
+            uint32_t tpat;
+            const int tlen = omega_lut(lut, static_cast<uint32_t>(len - last), &tpat);
+            emit(stage, pos, tpat, tlen);
+            s_nw[lb] = (pos + static_cast<uint32_t>(tlen) + 31u) >> 5;
+        }
+        __syncwarp();
     }
     __syncthreads();
     if (warp == 0)
@@ -1311,6 +1288,15 @@ __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_deco
 }
 
 }  // namespace
+// Raises the sparse encoder's dynamic shared-memory limit to `bytes` when
+// it is above the default 48 KB (large buckets).
+template <bool FOUR>
+int sparse_encode_smem(size_t bytes) {
+    if (bytes <= 48 * 1024) return GC_OK;
+    return cudaFuncSetAttribute(k_elias_sparse_encode<FOUR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes)) == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
 template <bool FOUR>
 int sparse_stage_words(uint32_t* cap) {
     static std::atomic<uint32_t> cached[kMaxDevices];
@@ -1525,7 +1511,11 @@ int qsgd_elias_encode_sparse(const uint8_t* codes, const float* norms, int64_t n
         return GC_ERR_CUDA;
     SparseArgs a{codes, norms, n, bucket, nb, s_levels >= 2, words, offsets, stride, chunk, encode_ws(workspace),
                  kEncodeWaitNs};
-    const size_t smem = sizeof(uint32_t) * (kOmegaLut + static_cast<size_t>(chunk) * stride);
+    // the table, the chunk's staging, and each warp's list of non-zero coordinates
+    const size_t smem = sizeof(uint32_t) * (kOmegaLut + static_cast<size_t>(chunk) * stride +
+                                            static_cast<size_t>(kWarpsPerBlock) * bucket);
+    const int rc = four ? sparse_encode_smem<true>(smem) : sparse_encode_smem<false>(smem);
+    if (rc != GC_OK) return rc;
     const unsigned grid = static_cast<unsigned>(nchunks);
     if (four)
         k_elias_sparse_encode<true><<<grid, kThreads, smem, s>>>(a);
