@@ -654,10 +654,15 @@ k_2bit_steps(const StepsArgs a) {
         uint4 ga[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) ra[q] = ld_f4(a.res + tbase + step_group<BF16>(lane, q));
+        // the gradients of the next two steps are in flight while a step is
+        // coded (one step ahead measured 8% slower at 2^20 elements, where
+        // 13 warps per SM carry all the loads)
+        uint4 gb[4];
         step_load_grad<BF16>(a.grads.p[0], tbase, lane, ga);
+        if (a.S > 1) step_load_grad<BF16>(a.grads.p[1], tbase, lane, gb);
         for (int st = 0; st < a.S; ++st) {
-            uint4 gb[4];
-            if (st + 1 < a.S) step_load_grad<BF16>(a.grads.p[st + 1], tbase, lane, gb);
+            uint4 gn[4];
+            if (st + 2 < a.S) step_load_grad<BF16>(a.grads.p[st + 2], tbase, lane, gn);
             uint32_t c[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -687,9 +692,10 @@ k_2bit_steps(const StepsArgs a) {
                 for (int q = 0; q < 4; ++q)
                     cb[code_byte(tbase + step_group<BF16>(lane, q))] = static_cast<uint8_t>(c[q]);
             }
-            if (st + 1 < a.S) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) ga[q] = gb[q];
+            for (int q = 0; q < 4; ++q) {
+                ga[q] = gb[q];
+                gb[q] = gn[q];
             }
         }
 #pragma unroll
