@@ -8,18 +8,19 @@
 // word is padded with zero bits; offsets[b] is bucket b's first word and
 // offsets[nbuckets] the stream's length, so that buckets decode in parallel.
 //
-// Encode = one launch reading the codes once.  Each CTA takes a chunk of 64
-// buckets (a ticket, so chunks go out in the order CTAs start); each warp
-// assembles its buckets in shared memory (a 256-entry table turns a code
-// byte into its codeword bits and length; one warp scan of bit lengths per
-// 32 code words, then shared-memory atomicOr of at most three words per
-// lane), publishes each bucket's word count, takes the bucket's first word
-// from a decoupled look-back over the buckets before it, and stores the
-// bucket with coalesced 32-bit writes.
-// Decode: one thread per bucket walks its stream with a 64-bit window; an
-// 11-bit (4-bit codes) or 12-bit (8-bit codes) lookahead table, built by the
-// compiler, decodes up to 8 or 4 whole codewords per step, and an 8-bit one
-// the rest; each CTA first copies its buckets' words to shared memory.
+// Encode = one launch reading the codes once.  Each CTA takes a chunk of up
+// to 64 buckets (a ticket, so chunks go out in the order CTAs start) and
+// stages all of it in shared memory: its warps assemble the buckets (a
+// 256-entry table turns a code byte into its codeword bits and length; one
+// warp scan of bit lengths per 32 code words, then shared-memory atomicOr of
+// at most three words per lane); the chunk's word count is published, its
+// first word taken from a decoupled look-back over the chunks before it, and
+// the chunk stored with coalesced 32-bit writes.
+// Decode: one thread per bucket (or per quarter or half bucket, from the
+// quarter marks) walks its stream with a 64-bit window; an 11-bit (4-bit
+// codes) or 12-bit (8-bit codes) lookahead table, built by the compiler,
+// decodes up to 8 or 4 whole codewords per step, and an 8-bit one the rest;
+// each CTA first copies its buckets' words to shared memory.
 #include <atomic>
 
 #include "gc_common.cuh"
@@ -28,9 +29,9 @@
 namespace gc {
 namespace {
 
-constexpr int kChunk = 64;                          // buckets per CTA
+constexpr int kChunk = 64;                          // buckets per encoding CTA, at most
 constexpr int kEncodeStageWords = 9216;             // the dense encoder's staging per CTA, at most
-constexpr int kSparseStageWords = 9600;             // the sparse encoder's
+constexpr int kSparseStageWords = 9600;             // the sparse encoder's staging per CTA, at most
 constexpr size_t kTicketBytes = 16;
 
 inline int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -47,7 +48,6 @@ inline int max_code_bits(bool four) { return four ? 8 : 15; }
 inline int64_t bucket_max_words(int64_t len, bool four) {
     return 1 + div_up(len * max_code_bits(four), 32);
 }
-
 
 // ---------------------------------------------------------------- codewords
 
