@@ -782,14 +782,27 @@ def rows(args, dev, peak):
                 tm.around("e" + k, pe)
             else:
                 tm.around("f" + k, pf)
+        # the same compaction with this process's L2 fetch granularity at 32
+        # bytes (gc_l2_fetch_granularity; the gather's random 4-byte reads then
+        # fetch less per value), after the same streaming step as above
         torch.cuda.synchronize(dev)
+        prev = gc.gc_l2_fetch_granularity(32)
+        for i in range(22):
+            pe()
+            tm.around("g" if i >= 2 else "w", pm)
+        torch.cuda.synchronize(dev)
+        gc.gc_l2_fetch_granularity(prev)
         K = int(cnt.item())
         assert int(st.item()) == 0
         rm = tm.ms("m")
         mkey = "saps_mask" if scfg.p >= 0.01 else "saps_mask_p001"
+        g_ms = _median(tm.ms("g"))
         out[f"{scfg.name}.mask_compact"] = _row(scfg.name, "saps_mask_compact", 4 * K + W * 8 * K, rm, peak, n,
                                                 {"masked": K, "issue": issue_roofline(mkey, rm),
-                                                 "dram": dram_roofline(mkey, rm, peak)})
+                                                 "dram": dram_roofline(mkey, rm, peak),
+                                                 "l2_fetch_32B_ms": round(g_ms, 5),
+                                                 "l2_fetch_32B_frac": round((4 * K + W * 8 * K) / (g_ms * 1e-3)
+                                                                            / 1e9 / peak, 4)})
         out[f"{scfg.name}.peer_average"] = _row(scfg.name, "saps_peer_average", (W // 2) * 20 * K,
                                                 tm.ms("a"), peak, None,
                                                 {"dram": dram_roofline("saps_avg", tm.ms("a"), peak)

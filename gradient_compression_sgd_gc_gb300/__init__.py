@@ -19,7 +19,7 @@ Entry points (same names as the C ABI):
   qsgd_elias_workspace_bytes,
   saps_round_seed, saps_matching, saps_matching_bandwidth, saps_workspace_bytes, saps_mask_compact,
   saps_mask_compact_noalloc, saps_peer_average, saps_pair_average_remote, easgd_step_from_sum, saps_average_easgd_step, easgd_step,
-  saps_round, gc_status_string, gc_version
+  saps_round, gc_status_string, gc_version, gc_l2_fetch_granularity
 Front ends over them (per-key state, parameter rules): ``compression.py``.
 """
 from __future__ import annotations
@@ -47,6 +47,7 @@ __all__ = [
     "GC_ERR_CORRUPT", "qsgd_elias_encode", "qsgd_elias_decode", "qsgd_elias_max_words",
     "qsgd_elias_workspace_bytes", "saps_round", "qsgd_step", "qsgd_elias_decode_batched",
     "qsgd_elias_encode_marked", "qsgd_elias_decode_quarters", "qsgd_elias_encode_status",
+    "gc_l2_fetch_granularity",
 ]
 
 GC_OK, GC_ERR_INVALID, GC_ERR_ALIGN, GC_ERR_CUDA, GC_ERR_CAPACITY, GC_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
@@ -85,6 +86,7 @@ def load():
         sig = {
             "gc_status_string": (ctypes.c_char_p, [i32]),
             "gc_version": (i32, []),
+            "gc_l2_fetch_granularity": (i32, [sz, vp]),
             "gc_2bit_quantize": (i32, [vp, i32, vp, vp, i64, f32, vp]),
             "gc_2bit_quantize_batched": (i32, [vp, i32, vp, vp, vp, i32, f32, vp]),
             "gc_2bit_step": (i32, [vp, i32, vp, vp, i32, i64, f32, i32, f32, f32, vp, vp, vp, vp]),
@@ -431,6 +433,16 @@ def qsgd_elias_decode(words: torch.Tensor, offsets: torch.Tensor, n: int, bucket
             None if status is None else _dev(status, "status", torch.int32, 1), _stream(stream, words))
     keep = (words, offsets, codes, norms) + (() if status is None else (status,))
     return _invoke(lib.qsgd_elias_decode, args, "qsgd_elias_decode", prepare, keep)
+
+
+def gc_l2_fetch_granularity(nbytes: int) -> int:
+    """Sets the current context's L2 fetch-granularity hint (0..128 bytes);
+    returns the value it replaces."""
+    prev = ctypes.c_size_t(0)
+    rc = load().gc_l2_fetch_granularity(int(nbytes), ctypes.byref(prev))
+    if rc != GC_OK:
+        raise GcError(rc, "gc_l2_fetch_granularity")
+    return int(prev.value)
 
 
 def qsgd_elias_encode_status(workspace: torch.Tensor) -> int:

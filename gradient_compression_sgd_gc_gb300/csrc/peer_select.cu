@@ -238,3 +238,15 @@ extern "C" int saps_matching_bandwidth(int W, const double* bandwidth, double b_
     }
     return GC_OK;
 }
+
+// The CUDA runtime's L2 fetch-granularity hint of the current context (a
+// per-process limit); see the header.  Random 4-byte gathers move less DRAM
+// traffic per value at 32 or 64 bytes than at 128.
+extern "C" int gc_l2_fetch_granularity(size_t bytes, size_t* previous) {
+    if (bytes > 128) return GC_ERR_INVALID;
+    size_t old = 0;
+    if (cudaDeviceGetLimit(&old, cudaLimitMaxL2FetchGranularity) != cudaSuccess) return GC_ERR_CUDA;
+    if (cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, bytes) != cudaSuccess) return GC_ERR_CUDA;
+    if (previous) *previous = old;
+    return GC_OK;
+}

@@ -160,6 +160,11 @@ def test_elias_sizes_and_validation():
     assert _call(q, None, None, None, 0, 512, 7, None, None, None, None) == gc.GC_OK
 
 
+def test_l2_fetch_granularity_validation():
+    assert _call("gc_l2_fetch_granularity", 129, None) == gc.GC_ERR_INVALID
+    assert _call("gc_l2_fetch_granularity", 1 << 40, None) == gc.GC_ERR_INVALID
+
+
 def test_saps_validation():
     f = "saps_mask_compact"
     ws = gc.saps_workspace_bytes(1000)

@@ -79,6 +79,35 @@ def test_mask_compact_sixteen_workers_and_repeat_calls():
             np.testing.assert_array_equal(vals[w].astype(np.float64), rvals[w])
 
 
+def test_compaction_under_each_l2_fetch_granularity():
+    """The L2 fetch-granularity hint changes what the gather moves, never what
+    it returns: the compaction equals the oracle at 32, 64 and 128 bytes, and
+    the previous setting comes back."""
+    n, W = 300_007, 4
+    models = [wl.normal(n, 0.05, 4100 + w, device=DEV) for w in range(W)]
+    hm = [host_f32(m).astype(np.float64) for m in models]
+    comp = Compactor(n, W, 20_000)
+    seed_t = oracle.round_seed(5, 7)
+    rK, ridx, rvals = oracle.saps_mask_compact(n, 0.01, seed_t, hm)
+    torch.cuda.synchronize()
+    first = gc.gc_l2_fetch_granularity(32)
+    try:
+        for g in (32, 64, 128):
+            torch.cuda.synchronize()
+            gc.gc_l2_fetch_granularity(g)
+            comp.run(0.01, seed_t, models)
+            K, idx, vals, status = comp.result()
+            assert status == 0 and K == rK
+            np.testing.assert_array_equal(idx, ridx)
+            for w in range(W):
+                np.testing.assert_array_equal(vals[w].astype(np.float64), rvals[w])
+    finally:
+        torch.cuda.synchronize()
+        assert gc.gc_l2_fetch_granularity(first) == 128
+    with pytest.raises(gc.GcError, match="GC_ERR_INVALID"):
+        gc.gc_l2_fetch_granularity(256)
+
+
 @pytest.mark.parametrize("p,cap", [(0.1, 100), (0.5, 100), (0.5, 3000), (0.25, 1500)])
 def test_capacity_overflow_reports_and_truncates(p, cap):
     """The capacity cut lands inside a staged tile (p = 0.1), inside a dense
