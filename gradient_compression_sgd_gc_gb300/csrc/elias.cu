@@ -335,31 +335,32 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
     const int nfull = nbc - (ragged ? 1 : 0);
     const int grp = lane / g.G, gl = lane % g.G;
     const uint4* src = reinterpret_cast<const uint4*>(a.codes + b0 * g.Bb);
-    // Items = (bucket pass j, round r); the next item's 16 bytes and norm are
-    // loaded while the current one is coded.
+    // Items = (bucket pass j, round r), r < R (1, 2 or 4), counted without
+    // division; the next item's 16 bytes and norm are loaded while the
+    // current one is coded.
     const int R = g.P / g.G;
     const int first = warp * a.slots, step = kWarpsPerBlock * a.slots;
     const int passes = nfull > first ? (nfull - first + step - 1) / step : 0;
     const int items = passes * R;
-    auto load_item = [&](int it, uint4& v, float& nrm) {
-        const int lb = first + (it / R) * step + grp;
+    auto load_item = [&](int lb, int r, uint4& v, float& nrm) {
         if (lb < nfull) {
-            v = __ldg(src + lb * g.P + (it % R) * g.G + gl);
+            v = __ldg(src + lb * g.P + r * g.G + gl);
             nrm = __ldg(a.norms + b0 + lb);
         }
     };
     uint4 vn = make_uint4(0u, 0u, 0u, 0u);
     float nn = 0.0f;
-    if (items) load_item(0, vn, nn);
+    if (items) load_item(first + grp, 0, vn, nn);
     uint32_t pos = 32;
+    int r = 0, lb = first + grp;                  // the current item
     for (int it = 0; it < items; ++it) {
-        const int r = it % R;
-        const int lb = first + (it / R) * step + grp;
         const bool active = lb < nfull;
         uint32_t* stage = stages + lb * a.stage_stride;
         const uint4 v = vn;
         const float nrm = nn;
-        if (it + 1 < items) load_item(it + 1, vn, nn);
+        const bool last_round = r + 1 == R;
+        const int nlb = last_round ? lb + step : lb, nr = last_round ? 0 : r + 1;
+        if (it + 1 < items) load_item(nlb, nr, vn, nn);
         if (r == 0) {
             pos = 32;
             if (active && gl == 0) stage[0] = __float_as_uint(nrm);
@@ -383,12 +384,16 @@ __global__ void __launch_bounds__(kThreads, 5) k_elias_encode(EncodeArgs a) {
         if (active) emit_piece(stage, pos + incl - len, e);
         if (a.marks && active) {
             // a piece that starts a quarter of the bucket records its start bit
+            // (a quarter, d / 4, is a power of two)
             const int c = (r * g.G + gl) * (FOUR ? 32 : 16);
-            const int q = a.d / 4;
-            if (c > 0 && c % q == 0) a.marks[3 * (b0 + lb) + c / q - 1] = static_cast<uint16_t>(pos + incl - len);
+            const int qs = __ffs(a.d) - 3;
+            if (c > 0 && (c & ((1 << qs) - 1)) == 0)
+                a.marks[3 * (b0 + lb) + (c >> qs) - 1] = static_cast<uint16_t>(pos + incl - len);
         }
         pos += __shfl_sync(0xffffffffu, incl, grp * g.G + g.G - 1);
-        if (r == R - 1 && active && gl == 0) s_nw[lb] = (pos + 31) >> 5;
+        if (last_round && active && gl == 0) s_nw[lb] = (pos + 31) >> 5;
+        lb = nlb;
+        r = nr;
     }
     if (ragged && warp == kWarpsPerBlock - 1) {
         // the ragged last bucket, by one warp
