@@ -237,3 +237,20 @@ def test_full_size_marks_and_quarter_decode(cfg):
     assert st == 0
     np.testing.assert_array_equal(dc, rc)
     np.testing.assert_array_equal(dn.view(np.uint32), rn.view(np.uint32))
+
+
+def test_empty_input():
+    """n = 0: the marked encoder writes only offsets[0] = 0 and a clean
+    status word; the quarter decoder touches nothing."""
+    offsets = torch.full((4,), 7, dtype=torch.int32, device=DEV)
+    words = torch.zeros(4, dtype=torch.int32, device=DEV)
+    marks = torch.full((8,), 5, dtype=torch.int16, device=DEV)
+    codes = torch.full((16,), 9, dtype=torch.uint8, device=DEV)
+    norms = torch.zeros(4, device=DEV)
+    ws = torch.full((64,), 0xA5, dtype=torch.uint8, device=DEV)
+    gc.qsgd_elias_encode_marked(codes, norms, 0, 512, 7, words, offsets, marks, ws)
+    gc.qsgd_elias_decode_quarters(words, offsets, marks, 0, 512, 7, codes, norms)
+    torch.cuda.synchronize()
+    assert host_u32(offsets).tolist() == [0, 7, 7, 7]
+    assert marks.cpu().tolist() == [5] * 8 and codes.cpu().tolist() == [9] * 16
+    assert gc.qsgd_elias_encode_status(ws) == gc.GC_OK

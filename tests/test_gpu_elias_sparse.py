@@ -146,3 +146,19 @@ def test_sparse_encode_capacity_refused():
     ws = torch.empty(gc.qsgd_elias_workspace_bytes(n, d), dtype=torch.uint8, device=DEV)
     with pytest.raises(RuntimeError, match="GC_ERR_CAPACITY"):
         gc.qsgd_elias_encode_sparse(codes, norms, n, d, s, words, offs, ws)
+
+
+def test_sparse_empty_input():
+    """n = 0: the sparse encoder writes only offsets[0] = 0; the decoder
+    touches nothing."""
+    offsets = torch.full((4,), 7, dtype=torch.int32, device=DEV)
+    words = torch.zeros(4, dtype=torch.int32, device=DEV)
+    codes = torch.full((16,), 9, dtype=torch.uint8, device=DEV)
+    norms = torch.zeros(4, device=DEV)
+    ws = torch.full((64,), 0xA5, dtype=torch.uint8, device=DEV)
+    gc.qsgd_elias_encode_sparse(codes, norms, 0, 512, 7, words, offsets, ws)
+    gc.qsgd_elias_decode_sparse(words, offsets, 0, 512, 7, codes, norms)
+    torch.cuda.synchronize()
+    assert host_u32(offsets).tolist() == [0, 7, 7, 7]
+    assert codes.cpu().tolist() == [9] * 16
+    assert gc.qsgd_elias_encode_status(ws) == gc.GC_OK
