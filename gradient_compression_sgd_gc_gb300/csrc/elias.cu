@@ -446,6 +446,7 @@ struct DecodeArgs {
     int* status;
     uint32_t stage_cap;   // stream words a CTA stages in shared memory
     const uint16_t* marks;   // quarter marks of stream 0 (segmented decode), else null
+    int bpc;              // buckets per CTA (at most its threads / parts; balanced_bpc)
 };
 
 // Lookahead bits of the multi-codeword table: 11 for 4-bit codes, 12 for
@@ -579,8 +580,8 @@ struct CodeWriter {
 // One thread per bucket: its stream is walked with a 64-bit window (whi:wlo,
 // `have` valid bits from the top, the next word waiting in `pre`).
 // S > 1: each thread decodes 1/S of a bucket (S = 2 or 4), from the
-// bucket's quarter marks (qsgd_elias_decode_quarters); a CTA then covers
-// 256 / S buckets.
+// bucket's quarter marks (qsgd_elias_decode_quarters).  A CTA covers
+// DecodeArgs::bpc buckets, at most its threads / S.
 // The CTA's NT tasks in order of stream length: a counting sort on `key`
 // (the task's word count, capped at 255), so that the threads of a warp walk
 // streams of about the same length instead of idling on the warp's longest
@@ -629,10 +630,10 @@ __device__ __forceinline__ void stage_words(const uint32_t* g, uint32_t nst, uin
 // is sized for.  Each CTA copies the codeword tables (19 KB for 4-bit codes,
 // 35 KB for 8-bit codes) to shared memory, so fewer, larger CTAs leave more
 // of it for staging stream words.  4-bit codes: 256 threads, 4 CTAs per SM a
-// bucket per thread (one stream of 61 M coordinates needs 3.4 of them per SM
-// of the 152), 6 with a part of a bucket per thread; 512- or 1024-thread
-// CTAs measured no faster.  8-bit codes: one 1024-thread CTA per SM a bucket
-// per thread (all its words staged: 87 -> 76 us for 61 M coordinates),
+// bucket per thread (one stream of 61 M coordinates fills them in one wave
+// at 197 buckets a CTA, balanced_bpc), 6 with a part of a bucket per thread;
+// 512- or 1024-thread CTAs measured no faster.  8-bit codes: one 1024-thread
+// CTA per SM a bucket per thread (all its words staged),
 // three 512-thread CTAs a part per thread (72 -> 70 us, 85 -> 76 us with L2
 // flushed).
 template <bool FOUR, int S>
@@ -676,10 +677,10 @@ k_elias_decode(DecodeArgs a) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) single[i] = window_entry<8>(static_cast<uint32_t>(i));
     const int stream = blockIdx.y;
     const uint32_t* offsets = a.offsets.p[stream];
-    constexpr int kBucketsPerCta = NT / S;
-    const int64_t bb = static_cast<int64_t>(blockIdx.x) * kBucketsPerCta + threadIdx.x / S;
+    const int bpc = a.bpc;                  // <= NT / S
+    const int64_t bb = static_cast<int64_t>(blockIdx.x) * bpc + threadIdx.x / S;
     uint32_t key = 255u;
-    if (bb < a.nbuckets) {
+    if (static_cast<int>(threadIdx.x) / S < bpc && bb < a.nbuckets) {
         uint32_t nw = offsets[bb + 1] - offsets[bb];
         if (S > 1) {
             const int k = threadIdx.x % S;
@@ -695,13 +696,14 @@ k_elias_decode(DecodeArgs a) {
     // there.  Every word of that range lies inside the range of one of the
     // CTA's buckets, whatever the offsets: the copy reads nothing a bucket
     // would not.
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kBucketsPerCta;
-    const int64_t cnt = a.nbuckets - b0 < kBucketsPerCta ? a.nbuckets - b0 : kBucketsPerCta;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * bpc;
+    const int64_t cnt = a.nbuckets - b0 < bpc ? a.nbuckets - b0 : bpc;
     const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
     const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
     const uint32_t* gwords = a.words.p[stream];
     stage_words<NT>(gwords + base, nst, s_words);
     __syncthreads();
+    if (task / S >= bpc) return;                // a thread past the CTA's buckets
     const int64_t b = b0 + task / S;
     if (b >= a.nbuckets) return;
     const int kq = task % S;                    // the task's part of the bucket
@@ -875,6 +877,33 @@ template <bool FOUR, int S>
 int decode_stage_words(uint32_t* cap) {
     static std::atomic<uint32_t> cached[kMaxDevices];
     return stage_cap_for(k_elias_decode<FOUR, S>, decode_ctas_per_sm<FOUR, S>(), cached, cap);
+}
+
+// Buckets per CTA for a decode of W streams of nb buckets each, with CTAs of
+// at most maxb buckets of which `ctas` fit on an SM.  A decoding thread walks
+// a whole bucket (or part), so an SM's time is its bucket count: a grid of
+// maxb-bucket CTAs leaves a few SMs one CTA more than the rest (466 CTAs of
+// 256 on 152 SMs x 4: ten SMs with 1024 buckets, the others 768), or SMs
+// idle (117 one-per-SM CTAs of 1024).  Instead: the fewest waves of
+// SMs x ctas CTAs that hold the buckets, and the buckets spread evenly over
+// those CTAs.
+int balanced_bpc(int64_t nb, int W, int ctas, int maxb, int* bpc) {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
+        return GC_ERR_CUDA;
+    const int64_t slots = static_cast<int64_t>(nsm) * ctas;
+    int64_t waves = div_up(static_cast<int64_t>(W) * nb, slots * maxb);
+    if (waves < 1) waves = 1;
+    for (;; ++waves) {
+        const int64_t per_stream = slots * waves / W;
+        if (per_stream < 1) continue;
+        const int64_t b = div_up(nb, per_stream);
+        if (b <= maxb) {
+            *bpc = static_cast<int>(b);
+            return GC_OK;
+        }
+    }
 }
 
 // ================================================================ sparse regimes
@@ -1138,8 +1167,9 @@ __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_deco
     for (int i = threadIdx.x; i < (1 << kOmegaWin); i += kThreads)
         otab[i] = static_cast<uint16_t>(omega_window_entry(static_cast<uint32_t>(i)));
     const int stream = blockIdx.y;
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kThreads;
-    const int64_t cnt = a.nbuckets - b0 < kThreads ? a.nbuckets - b0 : kThreads;
+    const int bpc = a.bpc;                  // <= kThreads
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * bpc;
+    const int64_t cnt = a.nbuckets - b0 < bpc ? a.nbuckets - b0 : bpc;
     uint8_t* codes = a.codes.p[stream];
     const int64_t total = FOUR ? (a.n + 1) / 2 : a.n;      // code bytes
     {
@@ -1155,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_deco
     const uint32_t* offsets = a.offsets.p[stream];
     const int64_t bb = b0 + threadIdx.x;
     uint32_t key = 255u;
-    if (bb < a.nbuckets) {
+    if (static_cast<int>(threadIdx.x) < bpc && bb < a.nbuckets) {
         const uint32_t nw = offsets[bb + 1] - offsets[bb];
         key = nw < 255u ? nw : 255u;
     }
@@ -1166,6 +1196,7 @@ __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_deco
     const uint32_t* gwords = a.words.p[stream];
     stage_words<kThreads>(gwords + base, nst, s_words);
     __syncthreads();
+    if (task >= bpc) return;                    // a thread past the CTA's buckets
     const int64_t b = b0 + task;
     if (b >= a.nbuckets) return;
     const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
@@ -1430,8 +1461,10 @@ int qsgd_elias_decode_batched(const uint32_t* const* words, const uint32_t* cons
     a.marks = nullptr;
     const bool four = s_levels <= 7;
     const int nt = four ? decode_threads<true, 1>() : decode_threads<false, 1>();
-    const dim3 grid(static_cast<unsigned>(div_up(nb, nt)), static_cast<unsigned>(W));
-    const int rc = four ? decode_stage_words<true, 1>(&a.stage_cap) : decode_stage_words<false, 1>(&a.stage_cap);
+    int rc = balanced_bpc(nb, W, four ? decode_ctas_per_sm<true, 1>() : decode_ctas_per_sm<false, 1>(), nt, &a.bpc);
+    if (rc != GC_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(div_up(nb, a.bpc)), static_cast<unsigned>(W));
+    rc = four ? decode_stage_words<true, 1>(&a.stage_cap) : decode_stage_words<false, 1>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     if (four)
@@ -1469,7 +1502,11 @@ int qsgd_elias_decode_quarters(const uint32_t* words, const uint32_t* offsets, c
     const bool four = s_levels <= 7;
     const int S = four ? kPartsFour : kPartsEight;
     const int nt = four ? decode_threads<true, kPartsFour>() : decode_threads<false, kPartsEight>();
-    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, nt / S)), 1u);
+    // Full CTAs: with a part of a bucket per thread the grid is two or more
+    // waves already, and the extra CTAs of an even spread cost more in
+    // per-CTA set-up (table copy, length sort) than the spread saves.
+    a.bpc = nt / S;
+    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, a.bpc)), 1u);
     const int rc = four ? decode_stage_words<true, kPartsFour>(&a.stage_cap)
                         : decode_stage_words<false, kPartsEight>(&a.stage_cap);
     if (rc != GC_OK) return rc;
@@ -1547,9 +1584,11 @@ int qsgd_elias_decode_sparse(const uint32_t* words, const uint32_t* offsets, int
     a.s = s_levels;
     a.status = d_status;
     a.marks = nullptr;
-    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, kThreads)), 1u);
+    int rc = balanced_bpc(a.nbuckets, 1, kSparseDecodeCtasPerSm, kThreads, &a.bpc);
+    if (rc != GC_OK) return rc;
+    const dim3 grid(static_cast<unsigned>(div_up(a.nbuckets, a.bpc)), 1u);
     const bool four = s_levels <= 7;
-    const int rc = four ? sparse_stage_words<true>(&a.stage_cap) : sparse_stage_words<false>(&a.stage_cap);
+    rc = four ? sparse_stage_words<true>(&a.stage_cap) : sparse_stage_words<false>(&a.stage_cap);
     if (rc != GC_OK) return rc;
     const size_t dyn = static_cast<size_t>(a.stage_cap) * sizeof(uint32_t);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

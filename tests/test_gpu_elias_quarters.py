@@ -239,6 +239,44 @@ def test_full_size_marks_and_quarter_decode(cfg):
     np.testing.assert_array_equal(dn.view(np.uint32), rn.view(np.uint32))
 
 
+@pytest.mark.parametrize("s,nb", [(7, 90_000), (127, 66_000)])
+def test_buckets_past_the_staged_words(s, nb):
+    """Every coordinate at level s (the longest codeword: 129 words a bucket
+    of 512 for 4-bit codes, 241 for 8-bit codes), with enough buckets that a
+    decoding CTA's buckets hold about twice the words its shared memory
+    stages: its last buckets are read from global memory, by the whole-bucket
+    and by the quarter decoder.  Both give back the input codes (all levels
+    non-zero, so the input is the canonical form), and the marked encoder
+    writes the oracle's stream and marks."""
+    n, d = 512 * nb, 512
+    if s <= 7:
+        codes = np.full(n // 2, ((0x8 | s) << 4) | s, np.uint8)     # signs - and + alternating
+    else:
+        codes = np.empty(n, np.uint8)
+        codes[0::2], codes[1::2] = 0x80 | s, s
+    norms = np.random.default_rng(3).uniform(0.5, 2.0, nb).astype(np.float32)
+    ref_w, ref_off = oracle.qsgd_elias_encode(codes, norms, n, d, s)
+    assert int(ref_off[1]) == (129 if s <= 7 else 241)
+    ref_m = oracle.qsgd_elias_quarter_marks(codes, n, d, s)
+    words, offsets, marks = _encode_marked(codes, norms, n, d, s)
+    np.testing.assert_array_equal(host_u32(words[:ref_w.size]), ref_w)
+    np.testing.assert_array_equal(_host_u16(marks), ref_m)
+    del ref_w, ref_m
+    cb = gc.qsgd_code_bytes(n, s)
+    dc = torch.empty(cb, dtype=torch.uint8, device=DEV)
+    dn = torch.empty(nb, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gc.qsgd_elias_decode(words, offsets, n, d, s, dc, dn, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(dc.cpu().numpy(), codes)
+    np.testing.assert_array_equal(host_f32(dn).view(np.uint32), norms.view(np.uint32))
+    qc, qn, qst = _decode_quarters(words, offsets, marks, n, d, s)
+    assert qst == 0
+    np.testing.assert_array_equal(qc, codes)
+    np.testing.assert_array_equal(qn.view(np.uint32), norms.view(np.uint32))
+
+
 def test_empty_input():
     """n = 0: the marked encoder writes only offsets[0] = 0 and a clean
     status word; the quarter decoder touches nothing."""
