@@ -612,17 +612,74 @@ __device__ __forceinline__ int task_by_length(uint32_t key) {
     return s_order[threadIdx.x];
 }
 
-// Copies the nst stream words at g to shared memory with coalesced loads
-// (four in flight per thread).  The caller synchronises before reading them.
-template <int NT>
-__device__ __forceinline__ void stage_words(const uint32_t* g, uint32_t nst, uint32_t* s_words) {
-    for (uint32_t i = threadIdx.x; i < nst; i += 4 * NT) {
-        uint32_t v[4];
+// A decoding CTA's copy of the nst words at g (16-byte aligned buffer,
+// g = words + base) to shared memory in 16-byte pieces: the words before the
+// first 16-byte boundary (`lead`, at most 3), the vectors, and the words after
+// the last one (`tail`, at most 3).  stage_issue loads the first R x NT
+// vectors and the edge words into registers at the start of the CTA, so that
+// those loads are in flight during its other set-up; stage_store writes them
+// and copies any further vectors.  Word i goes to s[i], where s = the shared
+// array + (base & 3), so that the vectors land on 16-byte boundaries: the
+// array holds nst + 3 words.  Every load lies inside g[0, nst).
+struct StageSplit {
+    uint32_t lead, nv, tail;
+};
+
+__device__ __forceinline__ StageSplit stage_split(uint32_t base, uint32_t nst) {
+    StageSplit p;
+    const uint32_t a0 = (4u - (base & 3u)) & 3u;
+    p.lead = a0 < nst ? a0 : nst;
+    p.nv = (nst - p.lead) >> 2;
+    p.tail = nst - p.lead - 4u * p.nv;
+    return p;
+}
+
+// Thread t < lead holds word t, thread 4 + t < 4 + tail the t-th word after the vectors.
+__device__ __forceinline__ bool edge_word(const StageSplit& p, uint32_t& i) {
+    const uint32_t t = threadIdx.x;
+    if (t < p.lead) {
+        i = t;
+        return true;
+    }
+    if (t >= 4u && t - 4u < p.tail) {
+        i = p.lead + 4u * p.nv + (t - 4u);
+        return true;
+    }
+    return false;
+}
+
+template <int NT, int R>
+__device__ __forceinline__ void stage_issue(const uint32_t* g, const StageSplit& p, uint4 (&v)[R], uint32_t& edge) {
+    const uint4* gv = reinterpret_cast<const uint4*>(g + p.lead);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = i + j * NT < nst ? __ldg(g + i + j * NT) : 0u;
+    for (int j = 0; j < R; ++j) {
+        const uint32_t i = threadIdx.x + j * NT;
+        if (i < p.nv) v[j] = __ldg(gv + i);
+    }
+    uint32_t i;
+    edge = edge_word(p, i) ? __ldg(g + i) : 0u;
+}
+
+template <int NT, int R>
+__device__ __forceinline__ void stage_store(const uint32_t* g, const StageSplit& p, const uint4 (&v)[R],
+                                            uint32_t edge, uint32_t* s) {
+    uint4* sv = reinterpret_cast<uint4*>(s + p.lead);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const uint32_t i = threadIdx.x + j * NT;
+        if (i < p.nv) sv[i] = v[j];
+    }
+    uint32_t i;
+    if (edge_word(p, i)) s[i] = edge;
+    const uint4* gv = reinterpret_cast<const uint4*>(g + p.lead);
+    for (uint32_t k = threadIdx.x + R * NT; k < p.nv; k += 4 * NT) {
+        uint4 w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (i + j * NT < nst) s_words[i + j * NT] = v[j];
+            if (k + j * NT < p.nv) w[j] = __ldg(gv + k + j * NT);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (k + j * NT < p.nv) sv[k + j * NT] = w[j];
     }
 }
 
@@ -651,33 +708,64 @@ __global__ void __launch_bounds__((decode_threads<FOUR, S>()), (decode_ctas_per_
 k_elias_decode(DecodeArgs a) {
     constexpr int NT = decode_threads<FOUR, S>();
     static_assert(NT % 256 == 0 && NT <= 1024, "the length sort has 256 bins");
-    extern __shared__ uint32_t s_words[];   // a.stage_cap words
+    extern __shared__ __align__(16) uint32_t s_words[];   // a.stage_cap words
     static_assert(S == 1 || S == 2 || S == 4, "a bucket splits at its quarter marks");
     constexpr int QS = 4 / S;               // quarters per task
     constexpr int KMAX = FOUR ? 8 : 4;
     constexpr int W = win_bits<FOUR>();
+    // vectors of the staging held in registers through the set-up
+    constexpr int RS = S == 1 ? 4 : 2;
     __shared__ __align__(16) uint64_t multi[1 << W];
     __shared__ uint32_t single[256];
     const uint32_t smax = static_cast<uint32_t>(a.s);
+    const int stream = blockIdx.y;
+    const uint32_t* offsets = a.offsets.p[stream];
+    const int bpc = a.bpc;                  // <= NT / S
+    // The CTA's words, offsets[b0] .. offsets[b0 + cnt) (at most stage_cap - 3
+    // of them), are copied to shared memory, so that the walks below read from
+    // there; their loads are issued first.  Every word of that range lies
+    // inside the range of one of the CTA's buckets, whatever the offsets: the
+    // copy reads nothing a bucket would not.
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * bpc;
+    const int64_t cnt = a.nbuckets - b0 < bpc ? a.nbuckets - b0 : bpc;
+    const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
+    const uint32_t cap = a.stage_cap > 3u ? a.stage_cap - 3u : 0u;
+    const uint32_t nst = wend > base ? (wend - base < cap ? wend - base : cap) : 0u;
+    const uint32_t* gwords = a.words.p[stream];
+    const StageSplit sp = stage_split(base, nst);
+    uint4 sv[RS];
+    uint32_t sedge;
+    stage_issue<NT, RS>(gwords + base, sp, sv, sedge);
+    uint32_t* staged_words = s_words + (base & 3u);
     {
-        const uint4* src = reinterpret_cast<const uint4*>(FOUR ? kMulti4.e : kMulti8.e);
-        uint4* dst = reinterpret_cast<uint4*>(multi);
         // A window holding a level above s gets count 0, which sends it to
         // the one-codeword path (where that level is flagged): the main loop
         // then tests only the count.  Entries are (packed << 32) | meta, meta
         // = (max level << 8) | (count << 4) | bits; the shared copy drops the
-        // max level, so that the count is meta >> 4.
-        for (int i = threadIdx.x; i < (1 << W) / 2; i += blockDim.x) {
-            uint4 v = __ldg(src + i);
-            v.x = ((v.x >> 8) & 127u) > smax ? (v.x & 15u) : (v.x & 255u);
-            v.z = ((v.z >> 8) & 127u) > smax ? (v.z & 15u) : (v.z & 255u);
-            dst[i] = v;
+        // max level, so that the count is meta >> 4.  All of a thread's
+        // loads are issued before its stores.
+        constexpr int kTv = (1 << W) / 2;    // 16-byte pieces of the table
+        constexpr int kTi = (kTv + NT - 1) / NT;
+        const uint4* src = reinterpret_cast<const uint4*>(FOUR ? kMulti4.e : kMulti8.e);
+        uint4* dst = reinterpret_cast<uint4*>(multi);
+        uint4 tv[kTi];
+#pragma unroll
+        for (int j = 0; j < kTi; ++j) {
+            const int i = static_cast<int>(threadIdx.x) + j * NT;
+            if (i < kTv) tv[j] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int j = 0; j < kTi; ++j) {
+            const int i = static_cast<int>(threadIdx.x) + j * NT;
+            if (i < kTv) {
+                uint4 v = tv[j];
+                v.x = ((v.x >> 8) & 127u) > smax ? (v.x & 15u) : (v.x & 255u);
+                v.z = ((v.z >> 8) & 127u) > smax ? (v.z & 15u) : (v.z & 255u);
+                dst[i] = v;
+            }
         }
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x) single[i] = window_entry<8>(static_cast<uint32_t>(i));
-    const int stream = blockIdx.y;
-    const uint32_t* offsets = a.offsets.p[stream];
-    const int bpc = a.bpc;                  // <= NT / S
     const int64_t bb = static_cast<int64_t>(blockIdx.x) * bpc + threadIdx.x / S;
     uint32_t key = 255u;
     if (static_cast<int>(threadIdx.x) / S < bpc && bb < a.nbuckets) {
@@ -691,17 +779,7 @@ k_elias_decode(DecodeArgs a) {
         key = nw < 255u ? nw : 255u;
     }
     const int task = task_by_length<NT>(key);
-    // The CTA's words, offsets[b0] .. offsets[b0 + cnt) (at most stage_cap of
-    // them), are copied to shared memory, so that the walks below read from
-    // there.  Every word of that range lies inside the range of one of the
-    // CTA's buckets, whatever the offsets: the copy reads nothing a bucket
-    // would not.
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * bpc;
-    const int64_t cnt = a.nbuckets - b0 < bpc ? a.nbuckets - b0 : bpc;
-    const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
-    const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
-    const uint32_t* gwords = a.words.p[stream];
-    stage_words<NT>(gwords + base, nst, s_words);
+    stage_store<NT, RS>(gwords + base, sp, sv, sedge, staged_words);
     __syncthreads();
     if (task / S >= bpc) return;                // a thread past the CTA's buckets
     const int64_t b = b0 + task / S;
@@ -718,7 +796,7 @@ k_elias_decode(DecodeArgs a) {
     // a bucket wholly inside the staged words reads shared memory (through a
     // generic pointer), any other bucket global memory
     const bool staged = w_lo - base <= nst && w_hi - base <= nst;
-    const uint32_t* src = staged ? s_words + (w_lo - base) : gwords + w_lo;
+    const uint32_t* src = staged ? staged_words + (w_lo - base) : gwords + w_lo;
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
     bool bad = avail == 0;
     auto word = [&](int64_t i) { return i < avail ? src[i] : 0u; };
@@ -1162,14 +1240,25 @@ constexpr int kSparseDecodeCtasPerSm = 4;
 
 template <bool FOUR>
 __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_decode_sparse(DecodeArgs a) {
-    extern __shared__ uint32_t s_words[];   // a.stage_cap words
+    extern __shared__ __align__(16) uint32_t s_words[];   // a.stage_cap words
     __shared__ uint16_t otab[1 << kOmegaWin];
-    for (int i = threadIdx.x; i < (1 << kOmegaWin); i += kThreads)
-        otab[i] = static_cast<uint16_t>(omega_window_entry(static_cast<uint32_t>(i)));
     const int stream = blockIdx.y;
     const int bpc = a.bpc;                  // <= kThreads
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * bpc;
     const int64_t cnt = a.nbuckets - b0 < bpc ? a.nbuckets - b0 : bpc;
+    // the CTA's words (at most stage_cap - 3) to shared memory: loads first
+    const uint32_t* offsets = a.offsets.p[stream];
+    const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
+    const uint32_t cap = a.stage_cap > 3u ? a.stage_cap - 3u : 0u;
+    const uint32_t nst = wend > base ? (wend - base < cap ? wend - base : cap) : 0u;
+    const uint32_t* gwords = a.words.p[stream];
+    const StageSplit sp = stage_split(base, nst);
+    uint4 sv[2];
+    uint32_t sedge;
+    stage_issue<kThreads, 2>(gwords + base, sp, sv, sedge);
+    uint32_t* staged_words = s_words + (base & 3u);
+    for (int i = threadIdx.x; i < (1 << kOmegaWin); i += kThreads)
+        otab[i] = static_cast<uint16_t>(omega_window_entry(static_cast<uint32_t>(i)));
     uint8_t* codes = a.codes.p[stream];
     const int64_t total = FOUR ? (a.n + 1) / 2 : a.n;      // code bytes
     {
@@ -1182,7 +1271,6 @@ __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_deco
         for (int64_t i = threadIdx.x; i < nvec; i += kThreads) v[i] = make_uint4(0u, 0u, 0u, 0u);
         for (int64_t i = start + nvec * 16 + threadIdx.x; i < end; i += kThreads) codes[i] = 0;
     }
-    const uint32_t* offsets = a.offsets.p[stream];
     const int64_t bb = b0 + threadIdx.x;
     uint32_t key = 255u;
     if (static_cast<int>(threadIdx.x) < bpc && bb < a.nbuckets) {
@@ -1191,17 +1279,14 @@ __global__ void __launch_bounds__(kThreads, kSparseDecodeCtasPerSm) k_elias_deco
     }
     // (its barriers also order the zero fill before the code words below)
     const int task = task_by_length<kThreads>(key);
-    const uint32_t base = offsets[b0], wend = offsets[b0 + cnt];
-    const uint32_t nst = wend > base ? (wend - base < a.stage_cap ? wend - base : a.stage_cap) : 0u;
-    const uint32_t* gwords = a.words.p[stream];
-    stage_words<kThreads>(gwords + base, nst, s_words);
+    stage_store<kThreads, 2>(gwords + base, sp, sv, sedge, staged_words);
     __syncthreads();
     if (task >= bpc) return;                    // a thread past the CTA's buckets
     const int64_t b = b0 + task;
     if (b >= a.nbuckets) return;
     const uint32_t w_lo = offsets[b], w_hi = offsets[b + 1];
     const bool staged = w_lo - base <= nst && w_hi - base <= nst;
-    const uint32_t* src = staged ? s_words + (w_lo - base) : gwords + w_lo;
+    const uint32_t* src = staged ? staged_words + (w_lo - base) : gwords + w_lo;
     const int64_t avail = w_hi > w_lo ? static_cast<int64_t>(w_hi - w_lo) : 0;
     auto word = [&](int64_t i) { return i < avail ? src[i] : 0u; };
     const int64_t lo = b * a.d;
