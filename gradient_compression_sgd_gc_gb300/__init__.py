@@ -128,6 +128,7 @@ def load():
                                                               vp]),
             "gc_testing_saps_mask_compact_withhold": (i32, [i64, f64, u64, vp, i32, vp, vp, i64, vp, vp, sz,
                                                             vp, i64, u64, vp]),
+            "gc_testing_decode_buckets_per_cta": (i32, [i64, i32, i64, i32, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -957,31 +957,19 @@ int decode_stage_words(uint32_t* cap) {
     return stage_cap_for(k_elias_decode<FOUR, S>, decode_ctas_per_sm<FOUR, S>(), cached, cap);
 }
 
-// Buckets per CTA for a decode of W streams of nb buckets each, with CTAs of
-// at most maxb buckets of which `ctas` fit on an SM.  A decoding thread walks
-// a whole bucket (or part), so an SM's time is its bucket count: a grid of
-// maxb-bucket CTAs leaves a few SMs one CTA more than the rest (466 CTAs of
-// 256 on 152 SMs x 4: ten SMs with 1024 buckets, the others 768), or SMs
-// idle (117 one-per-SM CTAs of 1024).  Instead: the fewest waves of
-// SMs x ctas CTAs that hold the buckets, and the buckets spread evenly over
-// those CTAs.
+// Buckets per CTA (even_buckets_per_cta) for the current device's SMs, with
+// `ctas` CTAs of at most maxb buckets resident per SM.  At 61.1 M coordinates
+// (119,338 buckets): 197 buckets in each of 606 CTAs of 256 threads (4-bit
+// codes, four per SM) where full CTAs left ten SMs 1024 buckets against 768
+// elsewhere, and 786 in each of 152 CTAs of 1024 (8-bit codes) where full
+// CTAs left 35 SMs idle.
 int balanced_bpc(int64_t nb, int W, int ctas, int maxb, int* bpc) {
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm < 1)
         return GC_ERR_CUDA;
-    const int64_t slots = static_cast<int64_t>(nsm) * ctas;
-    int64_t waves = div_up(static_cast<int64_t>(W) * nb, slots * maxb);
-    if (waves < 1) waves = 1;
-    for (;; ++waves) {
-        const int64_t per_stream = slots * waves / W;
-        if (per_stream < 1) continue;
-        const int64_t b = div_up(nb, per_stream);
-        if (b <= maxb) {
-            *bpc = static_cast<int>(b);
-            return GC_OK;
-        }
-    }
+    *bpc = static_cast<int>(even_buckets_per_cta(nb, W, static_cast<int64_t>(nsm) * ctas, maxb));
+    return GC_OK;
 }
 
 // ================================================================ sparse regimes

@@ -30,6 +30,24 @@ inline unsigned blocks_for_tiles(int64_t tiles) {
     return static_cast<unsigned>((tiles + kWarpsPerBlock - 1) / kWarpsPerBlock);
 }
 
+// Buckets per CTA for a decode that gives each thread one bucket (or part of
+// one), so that an SM's time is its bucket count: W streams of nb buckets, at
+// most maxb buckets a CTA, `slots` CTAs resident at once (SMs x CTAs per SM).
+// A grid of maxb-bucket CTAs leaves a few SMs one CTA more than the rest, or
+// SMs idle; instead, the fewest waves of `slots` CTAs that hold the buckets,
+// and the buckets spread evenly over those CTAs.  The grid is then
+// ceil(nb / result) CTAs per stream.  nb, W, slots, maxb >= 1.
+inline int64_t even_buckets_per_cta(int64_t nb, int64_t W, int64_t slots, int64_t maxb) {
+    int64_t waves = (W * nb + slots * maxb - 1) / (slots * maxb);
+    if (waves < 1) waves = 1;
+    for (;; ++waves) {
+        const int64_t per_stream = slots * waves / W;
+        if (per_stream < 1) continue;
+        const int64_t b = (nb + per_stream - 1) / per_stream;
+        if (b <= maxb) return b;
+    }
+}
+
 inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

@@ -27,6 +27,7 @@
 #include <vector>
 
 #include "gc_common.cuh"
+#include "../../include/gc_gb300_testing.h"
 
 namespace gc {
 namespace {
@@ -236,6 +237,15 @@ extern "C" int saps_matching_bandwidth(int W, const double* bandwidth, double b_
             last_round[mate[i] * W + i] = t;
         }
     }
+    return GC_OK;
+}
+
+// The Elias decoders' CTA sizing rule, on given sizes (no device needed).
+extern "C" int gc_testing_decode_buckets_per_cta(int64_t nb, int W, int64_t slots, int maxb, int64_t* bpc) {
+    if (nb < 1 || nb > (int64_t{1} << 40) || W < 1 || W > GC_MAX_WORKERS || slots < 1 ||
+        slots > (int64_t{1} << 20) || maxb < 1 || maxb > 1024 || !bpc)
+        return GC_ERR_INVALID;
+    *bpc = gc::even_buckets_per_cta(nb, W, slots, maxb);
     return GC_OK;
 }
 

@@ -1,7 +1,8 @@
 /*
  * gc_gb300_testing.h -- test hooks of libgc_gb300.so.  Not part of the
  * production ABI; they exist so that the failure paths of the library can be
- * exercised without faulting, trapping or hanging a GPU.
+ * exercised without faulting, trapping or hanging a GPU, and its host-side
+ * launch rules checked without one.
  */
 #ifndef GC_GB300_TESTING_H
 #define GC_GB300_TESTING_H
@@ -45,6 +46,21 @@ GC_API int gc_testing_saps_round_one_pass(int64_t n, double p, uint64_t seed_t,
                                           uint64_t *d_count, void *workspace,
                                           size_t workspace_bytes, int *d_status,
                                           gc_stream_t stream);
+
+/*
+ * gc_testing_decode_buckets_per_cta -- the Elias decoders' host rule for the
+ * buckets each decoding CTA takes ("QSGD ...", Knowl 2; a thread walks one
+ * bucket's stream, so an SM's time is its bucket count), on given sizes and
+ * without a device: W streams of nb buckets, CTAs of at most maxb buckets,
+ * `slots` CTAs resident at once (SMs x CTAs per SM).  The rule takes the
+ * fewest waves of `slots` CTAs that hold the buckets and spreads the buckets
+ * evenly over them; the decoders then launch ceil(nb / *bpc) CTAs per stream.
+ *   nb       1 .. 2^40       W      1 .. GC_MAX_WORKERS
+ *   slots    1 .. 2^20       maxb   1 .. 1024
+ *   bpc      host int64, out: 1 .. maxb
+ * Errors: GC_ERR_INVALID for an argument out of range or a NULL bpc.
+ */
+GC_API int gc_testing_decode_buckets_per_cta(int64_t nb, int W, int64_t slots, int maxb, int64_t *bpc);
 
 /*
  * gc_testing_qsgd_elias_encode_withhold -- qsgd_elias_encode in which bucket
