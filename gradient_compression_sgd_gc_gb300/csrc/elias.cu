@@ -444,7 +444,7 @@ struct DecodeArgs {
     int64_t nbuckets;
     int s;
     int* status;
-    uint32_t stage_cap;   // stream words a CTA stages in shared memory
+    uint32_t stage_cap;   // shared words for the staged stream words (at most stage_cap - 3 of them)
     const uint16_t* marks;   // quarter marks of stream 0 (segmented decode), else null
     int bpc;              // buckets per CTA (at most its threads / parts; balanced_bpc)
 };
