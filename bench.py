@@ -534,20 +534,37 @@ def rows(args, dev, peak):
     pq = gc.gc_2bit_quantize(g, r, c, cfg.threshold, stream=stream, prepare=True)
     pd = gc.gc_2bit_dequant_sum_update([c], n, cfg.threshold, gc.GC_UPD_NONE, out=o, stream=stream,
                                        prepare=True)
+    # the launch floor of this timing: the same call on 16 elements (one warp,
+    # no work to speak of), timed the same way -- event pair, host submission
+    # and kernel launch; the config's single launches sit a few us above it
+    g16, r16 = g[:16].clone(), torch.zeros(16, device=dev)
+    c16 = torch.empty(gc.code_words(16), dtype=torch.int32, device=dev)
+    pf = gc.gc_2bit_quantize(g16, r16, c16, cfg.threshold, stream=stream, prepare=True)
     for i in range(reps + 3):
         flush_l2(flush)
         tm.around("q" if i >= 3 else "w", pq)
         flush_l2(flush)
         tm.around("d" if i >= 3 else "w", pd)
+        flush_l2(flush)
+        tm.around("f" if i >= 3 else "w", pf)
     for i in range(reps + 3):
         tm.around("qh" if i >= 3 else "w", pq)
     torch.cuda.synchronize(dev)
+    floor_ms = _median(tm.ms("f"))
+
+    def above_floor(bytes_, key):
+        t = _median(tm.ms(key)) - floor_ms
+        return {"launch_floor_ms": round(floor_ms, 5),
+                "frac_above_floor": round(bytes_ / (t * 1e-3) / 1e9 / peak, 3) if t > 0 else None}
+
+    out["twobit_w1.launch_floor"] = _row("twobit_w1", "gc_2bit_quantize f32 on 16 elements (L2 flushed): the "
+                                         "floor of a single timed launch", 12.25 * 16, tm.ms("f"), peak, 16)
     out["twobit_w1.quantize"] = _row("twobit_w1", "gc_2bit_quantize f32 (L2 flushed)", 12.25 * n,
-                                     tm.ms("q"), peak, n)
+                                     tm.ms("q"), peak, n, above_floor(12.25 * n, "q"))
     out["twobit_w1.quantize_l2"] = _row("twobit_w1", "gc_2bit_quantize f32 (L2-resident)", 12.25 * n,
-                                        tm.ms("qh"), peak, n)
+                                        tm.ms("qh"), peak, n, above_floor(12.25 * n, "qh"))
     out["twobit_w1.dequant"] = _row("twobit_w1", "gc_2bit_dequant_sum_update NONE W=1", 4.25 * n,
-                                    tm.ms("d"), peak, n)
+                                    tm.ms("d"), peak, n, above_floor(4.25 * n, "d"))
     # the configuration's ten steps (fresh gradient each step, residual
     # carried, codes dequantised) captured once as a CUDA graph: 20 launches
     # replayed without host launch overhead, against the same calls eagerly
@@ -602,7 +619,7 @@ def rows(args, dev, peak):
     out["twobit_w1.ten_fused_steps_graph"] = _row("twobit_w1", "10 x gc_2bit_step (W=1, NONE: quantise + "
                                                   "dequant in one launch) as one CUDA graph (L2 flushed)",
                                                   ten_bytes, tm.ms("f"), peak, cfg.steps * n)
-    del g, r, c, o, gs, cs, os_, graphs, r_ms
+    del g, r, c, o, gs, cs, os_, graphs, r_ms, g16, r16, c16
 
     # config 2 as one fused launch per step vs the two-launch path of the headline
     cfg2 = wl.TWOBIT_DQ_SGD
