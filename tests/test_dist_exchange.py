@@ -7,8 +7,9 @@ What is checked is the exchange: that what each rank gathers, sends and
 reduces puts in front of the arithmetic exactly the data a single process
 holding all W workers has, so the per-rank results equal the single-process
 oracle run over the W workers -- bit for bit for 2-bit and QSGD (the same
-arithmetic on the same codes), and to rounding for SAPS + EASGD (the
-all-reduce sums the models in its own order).
+arithmetic on the same codes; any world size, odd ones included), and to
+rounding for SAPS + EASGD (the all-reduce sums the models in its own order;
+even world sizes, as a perfect matching needs).
 """
 import os
 import socket
@@ -146,7 +147,7 @@ def _run(world, case):
         return dict(out)
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_two_bit_exchange_equals_single_process(world):
     import oracle
     got = _run(world, "2bit")
@@ -163,7 +164,7 @@ def test_two_bit_exchange_equals_single_process(world):
         np.testing.assert_array_equal(got[r][1], res[r])
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_qsgd_exchange_equals_single_process(world):
     import oracle
     got = _run(world, "qsgd")
@@ -202,3 +203,11 @@ def test_saps_exchange_equals_single_process(world, case):
     for r in range(world):
         np.testing.assert_allclose(got[r][0], models[r], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(got[r][1], center, rtol=1e-12, atol=1e-15)
+
+
+def test_peer_of_reads_the_matching():
+    from gradient_compression_sgd_gc_gb300 import dist as gdist
+    pairs = [3, 0, 2, 1]
+    assert [gdist.peer_of(pairs, r) for r in range(4)] == [3, 2, 1, 0]
+    with pytest.raises(ValueError):
+        gdist.peer_of(pairs, 4)
