@@ -27,7 +27,9 @@
  *   Execution   Each call validates its arguments on the host, enqueues its
  *               kernels on `stream` (a cudaStream_t; NULL is the legacy
  *               default stream) and returns.  Results are valid once the
- *               stream reaches that point.
+ *               stream reaches that point.  `stream` belongs to the current
+ *               device: launch shapes (SM count, shared-memory sizes) are
+ *               taken from it.
  *   Status      The return value is GC_OK or a negative GC_ERR_* code from
  *               host validation, or GC_ERR_CUDA when a launch failed.  Errors
  *               found on the device (compaction capacity, look-back timeout,
